@@ -1,0 +1,399 @@
+"""Benchmark of the local W4A16 MoE forward on one GB300.
+
+Workload (default): 384 experts, hidden 7168, intermediate 256, gated SwiGLU,
+top-k 8, INT4 group-32 weights with BF16 scales, BF16 activations, seeded
+synthetic inputs, renormalize=False.  One step = route preparation + gate/up
+GEMM + SwiGLU + down GEMM + FP32 top-k combine over one batch of T tokens
+(default T = 2048), replayed from a CUDA graph.  The L2 is flushed (a 512 MB
+write) before every timed step, outside the timed events.  The token sweep
+1, 8, 32, 256, 1024 is measured the same way and reported under "sweep".
+
+Prints ONE JSON line.  ``--impl reference`` times the CPU oracle instead (a
+bounded sample of the same workload on the host cores).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from workloads import gen  # noqa: E402
+
+HEADLINE_TOKENS = 2048
+SWEEP_TOKENS = (1, 8, 32, 256, 1024)
+# Pages' number for this exact workload and metric (CuTe W4A16, one H200, T=2048,
+# LMDeploy PR page, Benchmark table): context from another machine.
+PAGE_LATENCY_US = {2048: 1280.327, 1024: 844.461, 256: 604.272, 32: 269.418, 8: 91.890, 1: 22.690}
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            pk = json.load(f)
+        return float(pk["hbm_gbs"]), float(pk["bf16_tflops"]), "measured"
+    return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
+
+
+# ---------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.tmp = None
+
+    def start(self):
+        try:
+            self.tmp = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.dev}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.tmp, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.tmp.flush()
+        self.tmp.seek(0)
+        rows = [r.strip().split(",") for r in self.tmp.read().splitlines() if r.strip()]
+        self.tmp.close()
+        os.unlink(self.tmp.name)
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                mx = float(r[2])
+                for n, v in zip(names, r[5:9]):
+                    if v.strip().lower() == "active":
+                        reasons.add(n)
+            except (ValueError, IndexError):
+                continue
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+
+def l2_flush_buffer(device):
+    return torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=device)
+
+
+def capture(moe, w, x, ids, tw, out, stream):
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            moe(x, w, tw, ids, out=out, stream=stream)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        moe(x, w, tw, ids, out=out, stream=stream)
+    torch.cuda.synchronize()
+    return g
+
+
+def time_graph(g, flush, stream, steps, warmup):
+    for _ in range(warmup):
+        flush.zero_()
+        g.replay()
+    torch.cuda.synchronize()
+    times = []
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    with torch.cuda.stream(stream):
+        for a, b in ev:
+            flush.zero_()
+            a.record(stream)
+            g.replay()
+            b.record(stream)
+    torch.cuda.synchronize()
+    for a, b in ev:
+        times.append(a.elapsed_time(b) * 1000.0)  # us
+    return times
+
+
+def time_stages(moe, w, x, ids, tw, out, flush, stream, steps):
+    """Per-kernel device time of the GEMMs and combine (eager launches, events
+    recorded by the library between kernels, L2 flushed before each step)."""
+    from weight_only_int4_histogram_gb300 import _lib
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    for e in evs:           # torch creates the CUDA event on first record
+        e.record(stream)
+    torch.cuda.synchronize()
+    _lib.w4a16_moe_set_stage_events(moe.plan, [e.cuda_event for e in evs])
+    acc = [[], [], []]
+    try:
+        for _ in range(steps):
+            with torch.cuda.stream(stream):
+                flush.zero_()
+                moe(x, w, tw, ids, out=out, stream=stream)
+            torch.cuda.synchronize()
+            for i in range(3):
+                acc[i].append(evs[i].elapsed_time(evs[i + 1]) * 1000.0)
+    finally:
+        _lib.w4a16_moe_set_stage_events(moe.plan, [])
+    return [statistics.mean(a) for a in acc]
+
+
+def stage_bytes(cfg, ids):
+    """Algorithmic bytes per launch of each kernel: the touched experts'
+    packed weights + scales, the activations it must read, the output."""
+    T = ids.shape[0]
+    loc = ids.long() - cfg.expert_offset
+    valid = (ids >= 0) & (loc >= 0) & (loc < cfg.num_experts)
+    touched = int(torch.unique(loc[valid]).numel())
+    H, I, N1 = cfg.hidden, cfg.inter, cfg.n1
+    g = cfg.scale_kind == gen.SCALE_GROUP32
+    b1 = touched * (H * N1 // 2 + (H * N1 // 32 * 2 if g else N1 * 2)) + T * H * 2
+    b2 = touched * (I * H // 2 + (I * H // 32 * 2 if g else H * 2))
+    b3 = T * H * 2 + T * cfg.top_k * 8
+    return b1, b2, b3
+
+
+def run_gpu(args):
+    from weight_only_int4_histogram_gb300 import W4A16MoE, build
+    build.build()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    cfg = gen.CONFIGS[args.config]
+    hbm, bf16, peak_kind = load_peaks()
+
+    w = gen.make_weights(cfg, dev)
+    moe = W4A16MoE.from_config(cfg, max_tokens=max(max(cfg.tokens), args.tokens), device=dev)
+    flush = l2_flush_buffer(dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    def measure(T, steps, warmup, sample_clocks=False):
+        x = gen.make_activations(cfg, T, dev)
+        ids, tw = gen.make_routes(cfg, T, dev)
+        out = torch.empty(T, cfg.hidden, dtype=cfg.torch_act_dtype(), device=dev)
+        g = capture(moe, w, x, ids, tw, out, stream)
+        clk = ClockSampler(local_rank)
+        if sample_clocks:
+            clk.start()
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+        times = time_graph(g, flush, stream, steps, warmup)
+        torch.cuda.synchronize()
+        if dist is not None:
+            dist.barrier()
+        clocks = clk.stop() if sample_clocks else None
+        moe.check_device_error()
+        med = statistics.median(times)
+        nbytes = gen.algorithmic_bytes(cfg, ids)
+        flops = gen.algorithmic_flops(cfg, ids)
+        t_roof = max(nbytes / (hbm * 1e9), flops / (bf16 * 1e12)) * 1e6
+        res = dict(tokens=T, us=round(med, 3), us_min=round(min(times), 3),
+                   gbs=round(nbytes / med / 1e3, 1), alg_bytes=nbytes, alg_flops=flops,
+                   roofline_us=round(t_roof, 3), roofline_frac=round(t_roof / med, 4),
+                   bound="hbm" if nbytes / (hbm * 1e9) >= flops / (bf16 * 1e12) else "tensor")
+        return res, (x, ids, tw, out, g), times, clocks
+
+    head, (x, ids, tw, out, g), times, clocks = measure(args.tokens, args.steps, args.warmup, True)
+    # the dominant kernel's live timing and roofline
+    st = time_stages(moe, w, x, ids, tw, out, flush, stream, max(args.steps, 5))
+    b = stage_bytes(cfg, ids)
+    k = max(range(3), key=lambda i: st[i])
+    names = ["gate_up_gemm", "down_gemm", "combine"]
+    achieved = b[k] / (st[k] * 1e-6) / 1e9
+    roof = {"kernel": names[k], "bound": "hbm", "achieved": round(achieved, 1), "peak": hbm,
+            "peak_kind": f"{peak_kind} hbm_gbs", "unit": "GB/s",
+            "frac": round(achieved / hbm, 4), "traffic": None,
+            "alg_bytes_per_launch": b[k], "launch_us": round(st[k], 3),
+            "stage_us": {n: round(v, 3) for n, v in zip(names, st)}}
+
+    sweep = []
+    if not args.no_sweep:
+        for T in SWEEP_TOKENS:
+            if T == args.tokens:
+                continue
+            r, *_ = measure(T, max(10, args.steps // 2), args.warmup)
+            sweep.append(r)
+        sweep.append(head)
+        sweep.sort(key=lambda r: r["tokens"])
+
+    # end to end through the C ABI with pinned host buffers (copies in the timed region)
+    xh = x.cpu().pin_memory()
+    idh = ids.cpu().pin_memory()
+    twh = tw.cpu().pin_memory()
+    oh = torch.empty(args.tokens, cfg.hidden, dtype=cfg.torch_act_dtype(), pin_memory=True)
+    for _ in range(args.warmup):
+        moe.forward_host(xh, w, twh, idh, out_host=oh, stream=stream)
+    e2e = []
+    for _ in range(args.steps):
+        flush.zero_()
+        torch.cuda.synchronize()
+        a = torch.cuda.Event(enable_timing=True)
+        bb = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        moe.forward_host(xh, w, twh, idh, out_host=oh, stream=stream)
+        bb.record(stream)
+        torch.cuda.synchronize()
+        e2e.append(a.elapsed_time(bb) * 1000.0)
+    e2e_med = statistics.median(e2e)
+    h2d = xh.numel() * 2 + idh.numel() * 4 + twh.numel() * 4
+    d2h = oh.numel() * 2
+
+    med = head["us"]
+    if dist is not None:
+        tmax = torch.tensor([med, e2e_med], device=dev)
+        dist.all_reduce(tmax, op=dist.ReduceOp.MAX)
+        med, e2e_med = float(tmax[0]), float(tmax[1])
+    line = {
+        "metric": "W4A16 MoE forward latency (us), Kimi TP8 shard shape",
+        "value": round(med, 3),
+        "unit": "us",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(med / 1000.0, 6),
+        "higher_is_better": False,
+        "scaling": "weak",
+        "vs_baseline": round(med / PAGE_LATENCY_US[args.tokens], 4) if args.tokens in PAGE_LATENCY_US and cfg is gen.KIMI else None,
+        "dtype": "bf16" if cfg.act_dtype == gen.DT_BF16 else "f16",
+        "data": "synthetic (seeded; weights N(0,0.02) quantised to INT4 g32, x N(0,1), softmax top-k routes)",
+        "config": {"workload": cfg.name, "tokens": args.tokens, "experts": cfg.num_experts,
+                   "hidden": cfg.hidden, "inter": cfg.inter, "top_k": cfg.top_k,
+                   "timing": "CUDA-graph replay, median of steps, CUDA events on the launch stream",
+                   "l2": "flushed before every timed step (512 MB write)",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "roofline": roof,
+        "headline": head,
+        "sweep": sweep,
+        "e2e": {"value": round(e2e_med, 3), "unit": "us", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": 4 * args.steps,
+        "clocks": clocks,
+    }
+    if not args.no_cpu_baseline and rank == 0 and world == 1:
+        line["cpu_baseline"] = cpu_baseline(cfg, args.tokens, args.cpu_sample_tokens,
+                                            (w.to("cpu"), x.cpu(), ids.cpu(), tw.cpu()))
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle (reported baseline / reference arm)
+# ---------------------------------------------------------------------------
+
+def cpu_baseline(cfg, tokens, sample_tokens, inputs=None):
+    import oracle
+    oracle.build()
+    if inputs is None:
+        inputs = make_inputs_for_cpu(cfg, tokens)
+    w, x, ids, tw = inputs
+    rows = list(range(min(sample_tokens, tokens)))
+    t0 = time.perf_counter()
+    oracle.moe_forward(cfg, x, w, tw, ids, rows=rows)
+    dt = time.perf_counter() - t0
+    per_step_us = dt * 1e6 * tokens / len(rows)
+    return {"value": round(per_step_us, 1), "unit": "us", "cores": oracle.num_threads(),
+            "kind": "oracle",
+            "sample": f"first {len(rows)} of {tokens} tokens of the same workload, "
+                      f"{dt:.2f} s of CPU work, scaled by {tokens}/{len(rows)}"}
+
+
+def make_inputs_for_cpu(cfg, tokens):
+    # Generated on the GPU when there is one (seconds instead of a minute), then
+    # copied to host memory; input generation is never timed.
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    w = gen.make_weights(cfg, dev).to("cpu")
+    x = gen.make_activations(cfg, tokens, dev).cpu()
+    ids, tw = gen.make_routes(cfg, tokens, dev)
+    return w, x, ids.cpu(), tw.cpu()
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    cfg = gen.CONFIGS[args.config]
+    import oracle
+    oracle.build()
+    w, x, ids, tw = make_inputs_for_cpu(cfg, args.tokens)
+    rows = list(range(min(args.ref_sample_tokens, args.tokens)))
+    for _ in range(args.warmup):
+        oracle.moe_forward(cfg, x, w, tw, ids, rows=rows[:1])
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle.moe_forward(cfg, x, w, tw, ids, rows=rows)
+        times.append((time.perf_counter() - t0) * 1e6 * args.tokens / len(rows))
+    v = statistics.median(times)
+    line = {
+        "impl": "reference",
+        "metric": "W4A16 MoE forward latency (us), Kimi TP8 shard shape",
+        "value": round(v, 1), "unit": "us", "n_gpus": int(os.environ.get("WORLD_SIZE", "1")),
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(v / 1000.0, 3),
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded)",
+        "config": {"workload": cfg.name, "tokens": args.tokens},
+        "cpu_baseline": {"value": round(v, 1), "unit": "us", "cores": oracle.num_threads(),
+                         "kind": "oracle",
+                         "sample": f"each step: first {len(rows)} of {args.tokens} tokens, "
+                                   f"scaled by {args.tokens}/{len(rows)}"},
+        "e2e": {"value": round(v, 1), "unit": "us", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", default=gen.KIMI.name, choices=list(gen.CONFIGS))
+    ap.add_argument("--tokens", type=int, default=HEADLINE_TOKENS)
+    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-sample-tokens", type=int, default=512)
+    ap.add_argument("--ref-sample-tokens", type=int, default=16)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

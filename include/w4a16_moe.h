@@ -1,0 +1,238 @@
+/*
+ * w4a16_moe.h -- C ABI of the GB300 (sm_103a) local W4A16 MoE forward.
+ *
+ * The operation.  For T tokens with activations x[T, H], top-k expert ids and
+ * FP32 routing weights, every valid route (t, j) to local expert e computes
+ *
+ *     h   = W13[e] . x[t]            gate/up GEMM, INT4 weights x 16-bit scales
+ *     a   = silu(h_gate) * h_up      (SwiGLU)   or   a = max(h, 0)^2 (ReLU^2)
+ *     y   = W2[e] . a                down GEMM
+ *
+ * and out[t] = cast( sum_{j = 0..k-1, route valid} w'[t, j] * y_{t,j} ), the
+ * sum taken in FP32 in fixed top-k order with one final cast.  Sources:
+ *   - "feat(pytorch): add CuTeDSL W4A16 MoE backend" (LMDeploy PR 4947),
+ *     sections Modification and Benchmark: route preparation, gate/up GEMM,
+ *     SiLU, down GEMM, weighted reduction; INT4 group size 32 with BF16
+ *     scales; invalid routes and masked expert counts; split-K for small
+ *     batches and route-count-based tile selection.
+ *   - "perf: reduce split W4A16 routing and output overhead" (FlashInfer PR
+ *     5186), section Description: expert outputs are stored, then combined in
+ *     FP32 in fixed top-k order before one output cast, without atomics.
+ *   - "[None][feat] Add W4A16 per-channel weight-only support for Cutlass
+ *     fused MoE" (TensorRT-LLM PR 18313), sections Checkpoint format
+ *     (per-output-channel scale = absmax/7, two INT4 per byte along the
+ *     output dim, even index in the low nibble) and Validation (non-gated
+ *     Relu2 arm).
+ *
+ * Conventions shared by all entry points
+ *   - INT4 codes are two's complement nibbles in [-8, 7]; in every packed byte
+ *     the even logical index sits in the low nibble.
+ *   - Gated W13 holds the I gate rows first, then the I up rows.
+ *   - Scales are always BF16.  Activations / output are BF16 or FP16.
+ *   - Route validity: id != -1 and 0 <= id - expert_offset < num_experts.
+ *     Other ids (routes that live on other ranks) are masked: they add
+ *     nothing.  A token whose routes are all invalid gets an exact +0 row.
+ *   - Sizes in the descriptor are LOGICAL (unpacked) sizes.  Packed sizes are
+ *     derived from them; nothing is inferred from a pointer's element type.
+ *   - Device pointers must be 16-byte aligned; arrays are dense row-major.
+ *   - Calls are asynchronous on the given stream (a cudaStream_t passed as
+ *     void*, NULL = legacy default stream).  prepare_routes and forward never
+ *     allocate, synchronise or copy device->host, so both can be captured in a
+ *     CUDA graph.
+ *   - Errors are reported before any launch as a status code; the message of
+ *     the most recent failing call on this host thread is returned by
+ *     w4a16_moe_last_error().  Device-side work has no error conditions apart
+ *     from a bounded-wait timeout inside the GEMM pipeline, which sets a flag
+ *     in the workspace that w4a16_moe_check_device_error() reads.
+ */
+#ifndef W4A16_MOE_H
+#define W4A16_MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  W4A16_OK = 0,
+  W4A16_ERR_INVALID_ARG = 1,       /* null / misaligned pointer, bad size */
+  W4A16_ERR_UNSUPPORTED = 2,       /* shape or option the kernels do not cover */
+  W4A16_ERR_WORKSPACE_TOO_SMALL = 3,
+  W4A16_ERR_CUDA = 4,              /* a CUDA runtime call or launch failed */
+  W4A16_ERR_DEVICE_TIMEOUT = 5     /* a bounded wait inside a kernel gave up */
+} w4a16_status;
+
+typedef enum { W4A16_ACT_SWIGLU = 0, W4A16_ACT_RELU2 = 1 } w4a16_act;
+typedef enum { W4A16_SCALE_GROUP32_K = 0, W4A16_SCALE_PER_CHANNEL = 1 } w4a16_scale;
+typedef enum { W4A16_DT_BF16 = 0, W4A16_DT_FP16 = 1 } w4a16_dtype;
+
+/*
+ * Problem descriptor (logical sizes).
+ *   num_experts   E, experts held by this GPU (1..1024)
+ *   expert_offset global id of local expert 0 (>= 0); stands in for expert
+ *                 parallelism: ids outside [offset, offset + E) are masked
+ *   hidden        H, multiple of 64
+ *   inter         I, multiple of 64
+ *   top_k         k, 1..16
+ *   max_tokens    largest T any later call may pass (1..65536)
+ *   act           w4a16_act: SWIGLU (W13 has N1 = 2I rows) or RELU2 (N1 = I)
+ *   scale_kind    w4a16_scale
+ *   act_dtype     w4a16_dtype of x and out (and of the intermediate)
+ *
+ * Weight layouts (uint8 packed codes, uint16 BF16 scale bits):
+ *   GROUP32_K:    W13 [E, N1, H/2]  S13 [E, N1, H/32]
+ *                 W2  [E, H,  I/2]  S2  [E, H,  I/32]
+ *                 byte b of a row holds K index 2b (low) and 2b+1 (high)
+ *   PER_CHANNEL:  W13 [E, N1/2, H]  S13 [E, N1]
+ *                 W2  [E, H/2,  I]  S2  [E, H]
+ *                 byte [p, c] holds row 2p (low) and row 2p+1 (high)
+ */
+typedef struct {
+  int32_t num_experts;
+  int32_t expert_offset;
+  int32_t hidden;
+  int32_t inter;
+  int32_t top_k;
+  int32_t max_tokens;
+  int32_t act;
+  int32_t scale_kind;
+  int32_t act_dtype;
+} w4a16_moe_desc;
+
+typedef struct w4a16_moe_plan_s* w4a16_moe_plan_t;
+
+/*
+ * w4a16_moe_plan -- validate a descriptor and build a host-side plan.
+ *   desc             problem descriptor (read only, copied)
+ *   out              receives the plan handle (owned by the caller; free with
+ *                    w4a16_moe_plan_destroy)
+ *   workspace_bytes  receives the device workspace size that every later call
+ *                    with num_tokens <= max_tokens needs
+ * Host only: no device work, no allocation on the device.  Queries the current
+ * device's SM count.  Returns INVALID_ARG / UNSUPPORTED for a bad descriptor.
+ */
+w4a16_status w4a16_moe_plan(const w4a16_moe_desc* desc, w4a16_moe_plan_t* out,
+                            size_t* workspace_bytes);
+
+/* Frees the plan's host memory.  NULL is accepted. */
+w4a16_status w4a16_moe_plan_destroy(w4a16_moe_plan_t plan);
+
+/*
+ * w4a16_moe_prepare_routes -- route layout ("histogram") for one batch.
+ * Passage: the LMDeploy page, Benchmark ("route preparation") and
+ * Modification ("invalid routes and masked expert counts"); the FlashInfer
+ * page, Description (top-k known at compile time in routing).
+ *   num_tokens  T, 0 <= T <= max_tokens (T = 0: no-op)
+ *   topk_ids    device int32 [T, k]
+ *   workspace   device buffer of workspace_bytes (caller-owned); receives the
+ *               per-expert counts, padded segment offsets, the stable
+ *               slot -> route permutation, its inverse and the tile list
+ *   stream      cudaStream_t as void*
+ * Device result (read back with w4a16_moe_route_info offsets):
+ *   counts[e]   valid routes of local expert e
+ *   offs[e]     first slot of expert e; segments padded to the route-tile
+ *               height bm; offs[E] = total slots
+ *   perm[slot]  flat route t*k + j, -1 in padding slots; within an expert
+ *               routes keep ascending flat order (stable)
+ *   inv[r]      slot of route r, -1 when invalid or masked
+ *   tiles[i]    int32 x4 (expert, first slot, valid rows, 0), i < num_tiles
+ */
+w4a16_status w4a16_moe_prepare_routes(w4a16_moe_plan_t plan, int32_t num_tokens,
+                                      const int32_t* topk_ids, void* workspace, void* stream);
+
+/*
+ * w4a16_moe_forward -- gate/up GEMM + activation + down GEMM + FP32 top-k
+ * combine, consuming the route layout that prepare_routes left in the same
+ * workspace for the same topk_ids and num_tokens.
+ * Passage: the LMDeploy page, Modification and Benchmark; the FlashInfer
+ * page, Description (non-fused finalisation, FP32 fixed-order combine, one
+ * cast, no atomics); the TensorRT-LLM page, Checkpoint format.
+ *   x             device [T, H] act_dtype
+ *   w13, s13      device packed gate/up (or fc1) weights and BF16 scales
+ *   w2, s2        device packed down weights and BF16 scales
+ *   topk_weights  device float32 [T, k]
+ *   topk_ids      device int32 [T, k] (the ids given to prepare_routes)
+ *   renormalize   nonzero: w'[t, j] = w[t, j] / sum_j w[t, j] (FP32, j
+ *                 ascending, over all k entries; zero sum -> zero weights)
+ *   out           device [T, H] act_dtype (written, never read)
+ *   workspace     the buffer prepare_routes filled
+ * All buffers are caller-owned.  Deterministic: identical inputs give
+ * bit-identical outputs.
+ */
+w4a16_status w4a16_moe_forward(w4a16_moe_plan_t plan, int32_t num_tokens, const void* x,
+                               const uint8_t* w13, const uint16_t* s13, const uint8_t* w2,
+                               const uint16_t* s2, const float* topk_weights,
+                               const int32_t* topk_ids, int32_t renormalize, void* out,
+                               void* workspace, void* stream);
+
+/*
+ * w4a16_moe_forward_host -- end-to-end call with HOST activations, ids,
+ * routing weights and output (expert weights stay resident on the device).
+ * Copies x / ids / weights host->device into staging space inside the
+ * workspace, runs prepare_routes + forward, and copies out back, all on
+ * `stream`, then synchronises the stream.  Host buffers should be pinned for
+ * asynchronous copies.  Same argument meaning as above otherwise.
+ */
+w4a16_status w4a16_moe_forward_host(w4a16_moe_plan_t plan, int32_t num_tokens, const void* x_host,
+                                    const uint8_t* w13, const uint16_t* s13, const uint8_t* w2,
+                                    const uint16_t* s2, const float* topk_weights_host,
+                                    const int32_t* topk_ids_host, int32_t renormalize,
+                                    void* out_host, void* workspace, void* stream);
+
+/* Route-layout description for a batch of num_tokens (host only). */
+typedef struct {
+  int32_t tile_rows;       /* bm: route-tile height, also the MMA N */
+  int32_t max_slots;       /* capacity of perm */
+  int32_t max_tiles;       /* capacity of the tile list */
+  int32_t gemm1_splits;    /* split-K factor of the gate/up GEMM */
+  int32_t gemm2_splits;    /* split-K factor of the down GEMM */
+  int32_t gemm1_ctas;      /* persistent grid sizes */
+  int32_t gemm2_ctas;
+  int32_t pipeline_stages;
+  size_t off_counts, off_offs, off_perm, off_inv, off_tiles, off_num_tiles;  /* bytes */
+  size_t off_inter;        /* intermediate activations [max_slots, I] (act dtype) */
+  size_t off_expert_out;   /* FP32 expert outputs [gemm2_splits, max_slots, H] */
+} w4a16_route_info;
+
+w4a16_status w4a16_moe_route_info(w4a16_moe_plan_t plan, int32_t num_tokens,
+                                  w4a16_route_info* info);
+
+/*
+ * Test / tuning overrides for later calls with this plan: force the route-tile
+ * height (16..128, multiple of 16) and split-K factors (1..64; a factor larger
+ * than the number of K blocks leaves empty partitions, which write zeros).
+ * 0 restores the automatic choice.  workspace_bytes receives the workspace
+ * size later calls need with these overrides in effect (it can exceed the
+ * size plan reported).
+ */
+w4a16_status w4a16_moe_set_overrides(w4a16_moe_plan_t plan, int32_t tile_rows,
+                                     int32_t gemm1_splits, int32_t gemm2_splits,
+                                     size_t* workspace_bytes);
+
+/*
+ * Reads (synchronously, on `stream`) and clears the device error flag in the
+ * workspace.  Returns W4A16_ERR_DEVICE_TIMEOUT if a kernel gave up waiting.
+ */
+w4a16_status w4a16_moe_check_device_error(w4a16_moe_plan_t plan, void* workspace, void* stream);
+
+/*
+ * Diagnostic timing hook.  With n == 4 and non-NULL `events` (cudaEvent_t
+ * handles passed as void*), later forward calls on this plan record
+ * events[0] before the gate/up GEMM, events[1] after it, events[2] after the
+ * down GEMM and events[3] after the combine, on the forward's stream.  The
+ * recordings separate the kernels, so the programmatic-launch overlap between
+ * them is lost while they are on.  n == 0 turns the hook off.  The plan does
+ * not own the events.
+ */
+w4a16_status w4a16_moe_set_stage_events(w4a16_moe_plan_t plan, void* const* events, int32_t n);
+
+/* Message for the last non-OK status on this host thread ("" if none). */
+const char* w4a16_moe_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* W4A16_MOE_H */

@@ -1,0 +1,113 @@
+"""C-ABI checks that need no GPU: the library builds, loads and exports every
+entry point include/w4a16_moe.h declares; descriptor validation and argument
+checks return the documented status codes before any launch."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from weight_only_int4_histogram_gb300 import _lib, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "w4a16_moe.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return _lib.load()
+
+
+def header_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(w4a16_moe_\w+)\s*\(", src)))
+
+
+def test_header_declares_the_binding_list():
+    assert header_functions() == sorted(_lib.EXPORTED)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in header_functions():
+        assert hasattr(lib, name), name
+        assert getattr(lib, name) is not None
+
+
+def good_desc(**kw):
+    d = dict(num_experts=8, expert_offset=0, hidden=256, inter=384, top_k=2, max_tokens=64,
+             act=0, scale_kind=0, act_dtype=0)
+    d.update(kw)
+    return _lib.Desc(**d)
+
+
+def test_plan_ok_and_workspace_positive(lib):
+    plan, ws = _lib.w4a16_moe_plan(good_desc())
+    assert ws > 0
+    info = _lib.w4a16_moe_route_info(plan, 16)
+    assert info.tile_rows % 16 == 0 and 16 <= info.tile_rows <= 128
+    assert info.pipeline_stages >= 2
+    _lib.w4a16_moe_plan_destroy(plan)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(num_experts=0), 2), (dict(num_experts=2000), 2), (dict(expert_offset=-1), 1),
+    (dict(hidden=100), 2), (dict(inter=96), 2), (dict(top_k=0), 2), (dict(top_k=17), 2),
+    (dict(max_tokens=0), 2), (dict(act=5), 1), (dict(scale_kind=3), 1), (dict(act_dtype=2), 1),
+])
+def test_plan_rejects_bad_descriptors(lib, kw, status):
+    with pytest.raises(_lib.W4A16Error) as ei:
+        _lib.w4a16_moe_plan(good_desc(**kw))
+    assert ei.value.status == status
+    assert lib.w4a16_moe_last_error().decode() != ""
+
+
+def test_calls_reject_bad_arguments_without_launching(lib):
+    plan, ws = _lib.w4a16_moe_plan(good_desc())
+    fake = 0x10000  # never dereferenced: validation fails first
+    # T outside [0, max_tokens]
+    with pytest.raises(_lib.W4A16Error) as ei:
+        _lib.w4a16_moe_prepare_routes(plan, 65, fake, fake, 0)
+    assert ei.value.status == 1
+    # null ids
+    with pytest.raises(_lib.W4A16Error):
+        _lib.w4a16_moe_prepare_routes(plan, 4, 0, fake, 0)
+    # misaligned workspace
+    with pytest.raises(_lib.W4A16Error) as ei:
+        _lib.w4a16_moe_prepare_routes(plan, 4, fake, fake + 8, 0)
+    assert "aligned" in str(ei.value)
+    # misaligned x in forward
+    with pytest.raises(_lib.W4A16Error) as ei:
+        _lib.w4a16_moe_forward(plan, 4, fake + 2, fake, fake, fake, fake, fake, fake, 0, fake, fake, 0)
+    assert "x" in str(ei.value)
+    # T = 0 is a no-op that succeeds even with null pointers
+    _lib.w4a16_moe_prepare_routes(plan, 0, 0, 0, 0)
+    _lib.w4a16_moe_forward(plan, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0)
+    _lib.w4a16_moe_plan_destroy(plan)
+
+
+def test_overrides_validate_and_resize_workspace(lib):
+    plan, ws = _lib.w4a16_moe_plan(good_desc())
+    with pytest.raises(_lib.W4A16Error):
+        _lib.w4a16_moe_set_overrides(plan, 24, 0, 0)
+    with pytest.raises(_lib.W4A16Error):
+        _lib.w4a16_moe_set_overrides(plan, 0, 65, 0)
+    ws2 = _lib.w4a16_moe_set_overrides(plan, 128, 4, 2)
+    info = _lib.w4a16_moe_route_info(plan, 16)
+    assert info.tile_rows == 128 and info.gemm1_splits == 4 and info.gemm2_splits == 2
+    assert ws2 >= ws
+    _lib.w4a16_moe_set_overrides(plan, 0, 0, 0)
+    _lib.w4a16_moe_plan_destroy(plan)
+
+
+def test_planner_tile_height_follows_route_counts(lib):
+    """Route-count-based tile selection: taller route tiles as routes per
+    expert grow (LMDeploy page, Modification)."""
+    plan, _ = _lib.w4a16_moe_plan(good_desc(num_experts=384, hidden=7168, inter=256, top_k=8,
+                                            max_tokens=2048))
+    bns = [_lib.w4a16_moe_route_info(plan, t).tile_rows for t in (1, 8, 32, 256, 1024, 2048)]
+    assert bns == sorted(bns) and bns[0] == 16 and bns[-1] >= 64
+    s1 = [_lib.w4a16_moe_route_info(plan, t).gemm1_splits for t in (1, 2048)]
+    assert s1[0] > 1 and s1[1] == 1  # split-K only for small batches
+    _lib.w4a16_moe_plan_destroy(plan)

@@ -1,0 +1,246 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle.
+
+Sizes span several route tiles, weight tiles and K blocks with ragged tails;
+full-size workloads are checked on sampled tokens in the launch configuration
+the benchmark times.
+"""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from workloads import gen
+from moe_testlib import compare, make_moe, case_on_gpu, oracle_rows, small_cfg
+
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _build():
+    from weight_only_int4_histogram_gb300 import build
+    build.build()
+
+
+# ---------------------------------------------------------------------------
+# route preparation: bit-exact
+# ---------------------------------------------------------------------------
+
+def check_routes(moe, cfg, ids):
+    T = ids.shape[0]
+    moe.prepare_routes(ids)
+    torch.cuda.synchronize()
+    got = moe.read_route_layout(T)
+    want = oracle.prepare_routes(cfg, ids.cpu(), got["tile_rows"])
+    np.testing.assert_array_equal(got["counts"].numpy(), want["counts"])
+    np.testing.assert_array_equal(got["offs"].numpy(), want["offs"])
+    np.testing.assert_array_equal(got["perm"].numpy(), want["perm"])
+    np.testing.assert_array_equal(got["inv"].numpy(), want["inv"])
+    assert got["num_tiles"] == want["num_tiles"]
+    np.testing.assert_array_equal(got["tiles"].numpy(), want["tiles"])
+
+
+@pytest.mark.parametrize("name", list(gen.CONFIGS))
+def test_route_prep_bit_exact_on_workloads(name):
+    cfg = gen.CONFIGS[name]
+    moe = make_moe(cfg, max(cfg.tokens))
+    for T in cfg.tokens:
+        ids, _ = gen.make_routes(cfg, T, "cuda")
+        check_routes(moe, cfg, ids)
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_route_prep_bit_exact_fuzz(seed):
+    rng = np.random.default_rng(100 + seed)
+    E = int(rng.choice([1, 3, 8, 33, 384, 1024]))
+    k = int(rng.choice([1, 2, 3, 4, 6, 8]))
+    T = int(rng.integers(1, 700))
+    off = int(rng.integers(0, 5))
+    cfg = gen.MoEConfig("fuzz", E, 256, 256, k, expert_offset=off)
+    moe = make_moe(cfg, 700)
+    if seed % 4 == 1:
+        moe.set_overrides(tile_rows=int(rng.choice([16, 32, 64, 128])))
+    frac_invalid = [0.0, 0.3, 1.0, 0.05][seed % 4]
+    ids = rng.integers(off, off + E, size=(T, k))
+    ids = np.where(rng.random((T, k)) < frac_invalid, -1, ids)
+    ids = np.where(rng.random((T, k)) < 0.05, off + E + 7, ids)  # masked (other rank)
+    if seed == 5:
+        ids[:] = off  # every route on one expert
+    check_routes(moe, cfg, torch.from_numpy(ids.astype(np.int32)).cuda())
+
+
+# ---------------------------------------------------------------------------
+# MoE output parity
+# ---------------------------------------------------------------------------
+
+def run_and_compare(cfg, T, overrides=None, renormalize=False, ids=None, what=""):
+    w, x, ids_, tw = case_on_gpu(cfg, T)
+    if ids is not None:
+        ids_ = ids.cuda()
+    moe = make_moe(cfg, max(T, 1))
+    if overrides:
+        moe.set_overrides(**overrides)
+    out = moe(x, w, tw, ids_, renormalize=renormalize)
+    torch.cuda.synchronize()
+    moe.check_device_error()
+    ref = oracle_rows(cfg, w, x, ids_, tw, renormalize=renormalize)
+    return compare(out, ref, what or f"{cfg.name} T={T} {overrides}"), (moe, w, x, ids_, tw, out)
+
+
+def test_tiny_workload_parity():
+    cfg = gen.TINY
+    run_and_compare(cfg, 16)
+
+
+SHAPES = [
+    dict(act=gen.ACT_SWIGLU, scale=gen.SCALE_GROUP32, dt=gen.DT_BF16),
+    dict(act=gen.ACT_RELU2, scale=gen.SCALE_GROUP32, dt=gen.DT_BF16),
+    dict(act=gen.ACT_SWIGLU, scale=gen.SCALE_PER_CHANNEL, dt=gen.DT_BF16),
+    dict(act=gen.ACT_SWIGLU, scale=gen.SCALE_PER_CHANNEL, dt=gen.DT_FP16),
+    dict(act=gen.ACT_RELU2, scale=gen.SCALE_PER_CHANNEL, dt=gen.DT_BF16),
+    dict(act=gen.ACT_SWIGLU, scale=gen.SCALE_GROUP32, dt=gen.DT_FP16),
+]
+
+
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: f"a{s['act']}s{s['scale']}d{s['dt']}")
+@pytest.mark.parametrize("T", [1, 7, 61])
+def test_small_shapes_parity(shape, T):
+    # H = 704: 2 full K blocks + a ragged one; I = 320: ragged weight tiles
+    cfg = small_cfg(E=5, H=704, I=320, k=3, **shape)
+    run_and_compare(cfg, T)
+
+
+@pytest.mark.parametrize("tile_rows", [16, 32, 48, 128])
+def test_route_tile_heights(tile_rows):
+    """Route-tile boundary cases: full tiles plus partial tails at several
+    heights, top-k 2 and 3."""
+    for k in (2, 3):
+        cfg = small_cfg(E=4, H=512, I=256, k=k)
+        run_and_compare(cfg, 45, overrides=dict(tile_rows=tile_rows))
+
+
+@pytest.mark.parametrize("s1,s2", [(1, 1), (2, 1), (3, 2), (5, 4)])
+def test_split_k_with_nan_poisoned_workspace(s1, s2):
+    """Split-K factors above the number of K blocks leave empty partitions;
+    they must write zero partials (workspace poisoned with NaN bytes first)."""
+    cfg = small_cfg(E=4, H=768, I=256, k=2)   # 3 K blocks in GEMM1, 1 in GEMM2
+    w, x, ids, tw = case_on_gpu(cfg, 9)
+    moe = make_moe(cfg, 9)
+    moe.set_overrides(gemm1_splits=s1, gemm2_splits=s2)
+    moe.workspace.fill_(0xFF)
+    out = moe(x, w, tw, ids)
+    torch.cuda.synchronize()
+    moe.check_device_error()
+    compare(out, oracle_rows(cfg, w, x, ids, tw), f"splits {s1},{s2}")
+
+
+def test_all_routes_invalid_gives_exact_zero():
+    cfg = small_cfg()
+    w, x, ids, tw = case_on_gpu(cfg, 13)
+    ids = torch.full_like(ids, -1)
+    moe = make_moe(cfg, 13)
+    moe.workspace.fill_(0xFF)
+    out = moe(x, w, tw, ids)
+    torch.cuda.synchronize()
+    assert torch.all(out.view(torch.int16) == 0)
+
+
+def test_masked_ids_and_expert_offset():
+    cfg = small_cfg(E=6, expert_offset=10)
+    w, x, _, tw = case_on_gpu(cfg, 20)
+    g = torch.Generator().manual_seed(5)
+    ids = torch.randint(8, 18, (20, 2), generator=g, dtype=torch.int32)  # 8, 9, 16, 17: other ranks
+    ids[3, 1] = -1
+    moe = make_moe(cfg, 20)
+    out = moe(x, w, tw, ids.cuda())
+    torch.cuda.synchronize()
+    compare(out, oracle_rows(cfg, w, x, ids, tw), "masked")
+
+
+def test_renormalize():
+    cfg = small_cfg(k=4)
+    run_and_compare(cfg, 17, renormalize=True)
+
+
+def test_deterministic_bitwise_and_pdl_off(monkeypatch):
+    cfg = small_cfg(E=8, H=1024, I=256, k=4)
+    w, x, ids, tw = case_on_gpu(cfg, 50)
+    moe = make_moe(cfg, 50)
+    outs = [moe(x, w, tw, ids).clone() for _ in range(3)]
+    monkeypatch.setenv("W4A16_MOE_PDL", "0")
+    moe2 = make_moe(cfg, 50)
+    outs.append(moe2(x, w, tw, ids).clone())
+    moe.set_overrides(gemm1_splits=2)
+    split_out = moe(x, w, tw, ids).clone()
+    torch.cuda.synchronize()
+    for o in outs[1:]:
+        assert torch.equal(o.view(torch.int16), outs[0].view(torch.int16))
+    compare(split_out, oracle_rows(cfg, w, x, ids, tw), "split")
+
+
+def test_cuda_graph_replay_with_new_inputs():
+    cfg = small_cfg(E=8, H=1024, I=256, k=2)
+    w, x, ids, tw = case_on_gpu(cfg, 33)
+    moe = make_moe(cfg, 33)
+    out = torch.empty(33, cfg.hidden, dtype=torch.bfloat16, device="cuda")
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        moe(x, w, tw, ids, out=out, stream=s)  # warm up on the capture stream
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        moe(x, w, tw, ids, out=out, stream=s)
+    for trial in range(3):
+        x2 = gen.make_activations(cfg, 33, "cuda", seed=100 + trial)
+        ids2, tw2 = gen.make_routes(cfg, 33, "cuda", seed=200 + trial)
+        x.copy_(x2)
+        ids.copy_(ids2)
+        tw.copy_(tw2)
+        g.replay()
+        torch.cuda.synchronize()
+        eager = moe(x2, w, tw2, ids2).clone()
+        torch.cuda.synchronize()
+        assert torch.equal(out.view(torch.int16), eager.view(torch.int16))
+        compare(out, oracle_rows(cfg, w, x2, ids2, tw2), f"graph replay {trial}")
+
+
+def test_forward_host_matches_device_path():
+    cfg = small_cfg()
+    w, x, ids, tw = case_on_gpu(cfg, 19)
+    moe = make_moe(cfg, 19)
+    dev = moe(x, w, tw, ids).clone()
+    torch.cuda.synchronize()
+    host = moe.forward_host(x.cpu().pin_memory(), w, tw.cpu().pin_memory(), ids.cpu().pin_memory())
+    assert torch.equal(host.view(torch.int16), dev.cpu().view(torch.int16))
+
+
+# ---------------------------------------------------------------------------
+# full-size workloads, sampled tokens, benchmark launch configuration
+# ---------------------------------------------------------------------------
+
+FULL = [("kimi_tp8_e384_h7168_i256_k8", (1, 32, 2048)),
+        ("deepseek_local_e32of256_h7168_i2048_k8", (4, 2048)),
+        ("per_channel_e60_h2048_i1408_k4", (8, 1024)),
+        ("per_channel_fp16_e60_h2048_i1408_k4", (1024,)),
+        ("relu2_skew_e64_h2688_i1856_k6", (32, 4096))]
+
+
+@pytest.mark.parametrize("name,tokens", FULL, ids=[f[0] for f in FULL])
+def test_full_size_sampled_rows(name, tokens):
+    cfg = gen.CONFIGS[name]
+    w = gen.make_weights(cfg, "cuda")
+    w_cpu = w.to("cpu")
+    moe = make_moe(cfg, max(cfg.tokens))
+    for T in tokens:
+        _, x, ids, tw = case_on_gpu(cfg, T, weights_gpu=w)
+        out = moe(x, w, tw, ids)
+        torch.cuda.synchronize()
+        moe.check_device_error()
+        rng = np.random.default_rng(T)
+        rows = sorted(set([0, T - 1] + rng.integers(0, T, size=min(T, 6)).tolist()))
+        ref = oracle_rows(cfg, w, x, ids, tw, rows=rows, w_cpu=w_cpu)
+        compare(out[rows], ref, f"{name} T={T}")

@@ -1,0 +1,548 @@
+// Host side of the C ABI in include/w4a16_moe.h: descriptor validation, the
+// per-batch planner (route-tile height, split-K factors, persistent grid
+// sizes, workspace layout), TMA descriptor encoding and the launch sequence
+//   route_prep -> gate/up GEMM -> down GEMM -> combine
+// chained with programmatic dependent launch.  No allocation, host sync or
+// device->host copy happens in prepare_routes / forward.
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <string>
+
+#include "common.cuh"
+#include "w4a16_moe.h"
+
+using namespace w4a16;
+
+struct w4a16_moe_plan_s {
+  w4a16_moe_desc d;
+  int num_sms;
+  int ov_bn, ov_s1, ov_s2;
+  size_t ws_bytes;
+  bool pdl;
+  cudaEvent_t ev[4];
+  bool has_ev;
+};
+
+namespace {
+
+thread_local std::string g_err;
+
+w4a16_status fail(w4a16_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_err = buf;
+  return s;
+}
+
+w4a16_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(W4A16_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+int cdiv(int a, int b) { return (a + b - 1) / b; }
+
+struct Layout {
+  int T, R, bn, tiles_cap;
+  int64_t slots_cap;
+  int n1;
+  int nt1, kb1, s1, kbps1;
+  int nt2, kb2, s2, kbps2;
+  int stages, stage_bytes, smem;
+  int grid1, grid2;
+  size_t off_err, off_counts, off_offs, off_ntiles, off_tiles, off_perm, off_inv, off_ctr;
+  size_t off_part, off_inter, off_y;
+  size_t off_sx, off_sids, off_sw, off_sout;
+  size_t total;
+};
+
+int choose_bn(const w4a16_moe_plan_s& P, int T) {
+  if (P.ov_bn) return P.ov_bn;
+  // Route-count-based tile height: expected routes per expert plus ~3.5
+  // standard deviations, so that one route tile usually covers an expert.
+  const double lam = static_cast<double>(T) * P.d.top_k / P.d.num_experts;
+  const double want = lam + 3.5 * std::sqrt(lam) + 1.0;
+  int bn = static_cast<int>(std::ceil(want / 16.0)) * 16;
+  return std::min(kMaxBN, std::max(16, bn));
+}
+
+// Split-K factor minimising (waves of units) x (K blocks per unit + overhead)
+// for the expected number of route tiles.
+int choose_splits(double tiles_est, int n_tiles, int kb, int num_sms, double overhead) {
+  int best = 1;
+  double best_cost = 1e300;
+  for (int s = 1; s <= std::min(kb, 64); ++s) {
+    const int kbps = cdiv(kb, s);
+    const int s_eff = cdiv(kb, kbps);
+    if (s_eff != s) continue;
+    const double units = tiles_est * n_tiles * s;
+    const double waves = std::ceil(units / num_sms);
+    const double cost = waves * (kbps + overhead);
+    if (cost < best_cost - 1e-9) {
+      best_cost = cost;
+      best = s;
+    }
+  }
+  return best;
+}
+
+Layout make_layout(const w4a16_moe_plan_s& P, int T) {
+  const w4a16_moe_desc& d = P.d;
+  Layout L = {};
+  L.T = T;
+  L.R = T * d.top_k;
+  L.bn = choose_bn(P, T);
+  const int E = d.num_experts;
+  const int touched_max = std::min(E, std::max(L.R, 1));
+  L.tiles_cap = (L.R + touched_max * (L.bn - 1)) / L.bn + 1;
+  L.slots_cap = static_cast<int64_t>(L.R) + static_cast<int64_t>(touched_max) * (L.bn - 1) + L.bn;
+  const bool gated = d.act == W4A16_ACT_SWIGLU;
+  L.n1 = gated ? 2 * d.inter : d.inter;
+  L.nt1 = gated ? d.inter / 64 : cdiv(d.inter, kTileRows);
+  L.kb1 = cdiv(d.hidden, kBlockK);
+  L.nt2 = cdiv(d.hidden, kTileRows);
+  L.kb2 = cdiv(d.inter, kBlockK);
+  // expected route tiles (uniform routing): touched experts x tiles per expert
+  const double touched = std::max(1.0, E * (1.0 - std::exp(-static_cast<double>(L.R) / E)));
+  const double per = L.R / touched;
+  const double tiles_est = touched * std::max(1.0, std::ceil(per / L.bn));
+  L.s1 = P.ov_s1 ? P.ov_s1 : choose_splits(tiles_est, L.nt1, L.kb1, P.num_sms, 1.5);
+  L.s2 = P.ov_s2 ? P.ov_s2 : choose_splits(tiles_est, L.nt2, L.kb2, P.num_sms, 1.0);
+  L.kbps1 = cdiv(L.kb1, L.s1);
+  L.kbps2 = cdiv(L.kb2, L.s2);
+  L.stage_bytes = kStageA + L.bn * 512 + kStageS;
+  const int smem_budget = 232448 - 2048;
+  L.stages = std::min(kMaxStages, smem_budget / L.stage_bytes);
+  L.smem = 2048 + L.stages * L.stage_bytes;
+  L.grid1 = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(P.num_sms, static_cast<int64_t>(L.tiles_cap) * L.nt1 * L.s1)));
+  L.grid2 = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(P.num_sms, static_cast<int64_t>(L.tiles_cap) * L.nt2 * L.s2)));
+
+  const int act_bytes = 2;
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o = align_up(o + std::max<size_t>(bytes, 1), 256);
+    return at;
+  };
+  L.off_err = take(16);
+  L.off_counts = take(sizeof(int32_t) * E);
+  L.off_offs = take(sizeof(int32_t) * (E + 1));
+  L.off_ntiles = take(sizeof(int32_t));
+  L.off_tiles = take(sizeof(int32_t) * 4 * L.tiles_cap);
+  L.off_perm = take(sizeof(int32_t) * L.slots_cap);
+  L.off_inv = take(sizeof(int32_t) * std::max(L.R, 1));
+  L.off_ctr = take(sizeof(int32_t) * L.tiles_cap * L.nt1);
+  L.off_part = take(L.s1 > 1 ? sizeof(float) * L.s1 * L.slots_cap * L.n1 : 0);
+  L.off_inter = take(static_cast<size_t>(act_bytes) * L.slots_cap * d.inter);
+  L.off_y = take(sizeof(float) * L.s2 * L.slots_cap * d.hidden);
+  L.off_sx = take(static_cast<size_t>(act_bytes) * T * d.hidden);
+  L.off_sids = take(sizeof(int32_t) * std::max(L.R, 1));
+  L.off_sw = take(sizeof(float) * std::max(L.R, 1));
+  L.off_sout = take(static_cast<size_t>(act_bytes) * T * d.hidden);
+  L.total = o;
+  return L;
+}
+
+size_t max_workspace(const w4a16_moe_plan_s& P) {
+  size_t m = 0;
+  for (int T = 1; T <= P.d.max_tokens; ++T) m = std::max(m, make_layout(P, T).total);
+  return m;
+}
+
+int route_prep_smem(int E) { return (kRoutePrepWarps * E + E + 2 * (E + 1) + 64) * 4; }
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
+// Packed INT4 weights as a 3D uint8 tensor [E][rows][inner bytes], 128-byte
+// swizzled boxes of 128 bytes x box_rows.
+bool encode_weights(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint64_t E,
+                    uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {inner, rows, E};
+  cuuint64_t strides[2] = {inner, inner * rows};
+  cuuint32_t box[3] = {128, box_rows, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// A row-major 16-bit matrix [rows][cols], boxes of 64 columns x box_rows, 128B swizzle.
+bool encode_rows16(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint32_t box_rows,
+                   int dtype) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  return fn(m, dtype == W4A16_DT_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+            2, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+w4a16_status validate_desc(const w4a16_moe_desc* d) {
+  if (!d) return fail(W4A16_ERR_INVALID_ARG, "desc is NULL");
+  if (d->num_experts < 1 || d->num_experts > 1024)
+    return fail(W4A16_ERR_UNSUPPORTED, "num_experts must be in [1, 1024], got %d", d->num_experts);
+  if (d->expert_offset < 0) return fail(W4A16_ERR_INVALID_ARG, "expert_offset must be >= 0");
+  if (d->hidden <= 0 || d->hidden % 64 != 0)
+    return fail(W4A16_ERR_UNSUPPORTED, "hidden must be a positive multiple of 64, got %d", d->hidden);
+  if (d->inter <= 0 || d->inter % 64 != 0)
+    return fail(W4A16_ERR_UNSUPPORTED, "inter must be a positive multiple of 64, got %d", d->inter);
+  if (d->top_k < 1 || d->top_k > 16)
+    return fail(W4A16_ERR_UNSUPPORTED, "top_k must be in [1, 16], got %d", d->top_k);
+  if (d->max_tokens < 1 || d->max_tokens > 65536)
+    return fail(W4A16_ERR_UNSUPPORTED, "max_tokens must be in [1, 65536], got %d", d->max_tokens);
+  if (d->act != W4A16_ACT_SWIGLU && d->act != W4A16_ACT_RELU2)
+    return fail(W4A16_ERR_INVALID_ARG, "unknown activation %d", d->act);
+  if (d->scale_kind != W4A16_SCALE_GROUP32_K && d->scale_kind != W4A16_SCALE_PER_CHANNEL)
+    return fail(W4A16_ERR_INVALID_ARG, "unknown scale kind %d", d->scale_kind);
+  if (d->act_dtype != W4A16_DT_BF16 && d->act_dtype != W4A16_DT_FP16)
+    return fail(W4A16_ERR_INVALID_ARG, "unknown activation dtype %d", d->act_dtype);
+  if (static_cast<int64_t>(d->max_tokens) * d->top_k > (1 << 24))
+    return fail(W4A16_ERR_UNSUPPORTED, "max_tokens * top_k too large");
+  return W4A16_OK;
+}
+
+w4a16_status check_ptr(const void* p, size_t align, const char* name) {
+  if (!p) return fail(W4A16_ERR_INVALID_ARG, "%s is NULL", name);
+  if (!aligned(p, align)) return fail(W4A16_ERR_INVALID_ARG, "%s must be %zu-byte aligned", name, align);
+  return W4A16_OK;
+}
+
+bool env_flag(const char* name, bool dflt) {
+  const char* v = getenv(name);
+  if (!v || !*v) return dflt;
+  return !(v[0] == '0' && v[1] == 0);
+}
+
+w4a16_status launch_prepare(const w4a16_moe_plan_s& P, const Layout& L, const int32_t* ids,
+                            uint8_t* ws, cudaStream_t s) {
+  RoutePrepParams rp = {};
+  rp.ids = ids;
+  rp.T = L.T;
+  rp.k = P.d.top_k;
+  rp.E = P.d.num_experts;
+  rp.expert_offset = P.d.expert_offset;
+  rp.bm = L.bn;
+  rp.counts = reinterpret_cast<int32_t*>(ws + L.off_counts);
+  rp.offs = reinterpret_cast<int32_t*>(ws + L.off_offs);
+  rp.perm = reinterpret_cast<int32_t*>(ws + L.off_perm);
+  rp.inv = reinterpret_cast<int32_t*>(ws + L.off_inv);
+  rp.tiles = reinterpret_cast<int4*>(ws + L.off_tiles);
+  rp.num_tiles = reinterpret_cast<int32_t*>(ws + L.off_ntiles);
+  rp.counters = reinterpret_cast<int32_t*>(ws + L.off_ctr);
+  rp.ctr_len = L.tiles_cap * L.nt1;
+  rp.err = reinterpret_cast<int32_t*>(ws + L.off_err);
+  cudaError_t e = launch_route_prep(rp, route_prep_smem(P.d.num_experts), s, P.pdl);
+  if (e != cudaSuccess) return cuda_fail(e, "route_prep launch");
+  return W4A16_OK;
+}
+
+w4a16_status launch_forward(const w4a16_moe_plan_s& P, const Layout& L, const void* x,
+                            const uint8_t* w13, const uint16_t* s13, const uint8_t* w2,
+                            const uint16_t* s2, const float* tw, int32_t renorm, void* out,
+                            uint8_t* ws, cudaStream_t s) {
+  const w4a16_moe_desc& d = P.d;
+  const bool group = d.scale_kind == W4A16_SCALE_GROUP32_K;
+  CUtensorMap tmA1, tmA2, tmB2;
+  bool ok;
+  if (group) {
+    ok = encode_weights(&tmA1, w13, d.hidden / 2, L.n1, d.num_experts, 64) &&
+         encode_weights(&tmA2, w2, d.inter / 2, d.hidden, d.num_experts, 64);
+  } else {
+    ok = encode_weights(&tmA1, w13, d.hidden, L.n1 / 2, d.num_experts, 32) &&
+         encode_weights(&tmA2, w2, d.inter, d.hidden / 2, d.num_experts, 32);
+  }
+  ok = ok && encode_rows16(&tmB2, ws + L.off_inter, d.inter, L.slots_cap, L.bn, d.act_dtype);
+  if (!ok) return fail(W4A16_ERR_CUDA, "cuTensorMapEncodeTiled failed (driver entry point or arguments)");
+
+  GemmParams g = {};
+  g.act = d.act;
+  g.E = d.num_experts;
+  g.inter = d.inter;
+  g.bn = L.bn;
+  g.stages = L.stages;
+  g.stage_bytes = L.stage_bytes;
+  g.top_k = d.top_k;
+  g.tiles = reinterpret_cast<const int4*>(ws + L.off_tiles);
+  g.num_tiles = reinterpret_cast<const int32_t*>(ws + L.off_ntiles);
+  g.perm = reinterpret_cast<const int32_t*>(ws + L.off_perm);
+  g.slots_cap = L.slots_cap;
+  g.err = reinterpret_cast<int32_t*>(ws + L.off_err);
+
+  GemmParams g1 = g;
+  g1.n_rows = L.n1;
+  g1.K = d.hidden;
+  g1.out_cols = d.inter;
+  g1.n_tiles = L.nt1;
+  g1.kb_total = L.kb1;
+  g1.splits = L.s1;
+  g1.kb_per_split = L.kbps1;
+  g1.x = x;
+  g1.scales = s13;
+  g1.out = ws + L.off_inter;
+  g1.part = reinterpret_cast<float*>(ws + L.off_part);
+  g1.counters = reinterpret_cast<int32_t*>(ws + L.off_ctr);
+  cudaError_t e;
+  if (P.has_ev && (e = cudaEventRecord(P.ev[0], s)) != cudaSuccess) return cuda_fail(e, "event record");
+  e = launch_gemm(GEMM_UP, d.scale_kind, d.act_dtype, g1, tmA1, tmA1, L.grid1, L.smem, s, P.pdl);
+  if (e != cudaSuccess) return cuda_fail(e, "gate/up GEMM launch");
+  if (P.has_ev && (e = cudaEventRecord(P.ev[1], s)) != cudaSuccess) return cuda_fail(e, "event record");
+
+  GemmParams g2 = g;
+  g2.n_rows = d.hidden;
+  g2.K = d.inter;
+  g2.out_cols = d.hidden;
+  g2.n_tiles = L.nt2;
+  g2.kb_total = L.kb2;
+  g2.splits = L.s2;
+  g2.kb_per_split = L.kbps2;
+  g2.x = nullptr;
+  g2.scales = s2;
+  g2.out = ws + L.off_y;
+  g2.part = nullptr;
+  g2.counters = nullptr;
+  e = launch_gemm(GEMM_DOWN, d.scale_kind, d.act_dtype, g2, tmA2, tmB2, L.grid2, L.smem, s, P.pdl);
+  if (e != cudaSuccess) return cuda_fail(e, "down GEMM launch");
+  if (P.has_ev && (e = cudaEventRecord(P.ev[2], s)) != cudaSuccess) return cuda_fail(e, "event record");
+
+  CombineParams c = {};
+  c.y = reinterpret_cast<const float*>(ws + L.off_y);
+  c.slots_cap = L.slots_cap;
+  c.splits = L.s2;
+  c.inv = reinterpret_cast<const int32_t*>(ws + L.off_inv);
+  c.topk_weights = tw;
+  c.T = L.T;
+  c.H = d.hidden;
+  c.k = d.top_k;
+  c.renormalize = renorm ? 1 : 0;
+  c.out = out;
+  e = launch_combine(d.act_dtype, c, s, P.pdl);
+  if (e != cudaSuccess) return cuda_fail(e, "combine launch");
+  if (P.has_ev && (e = cudaEventRecord(P.ev[3], s)) != cudaSuccess) return cuda_fail(e, "event record");
+  return W4A16_OK;
+}
+
+}  // namespace
+
+namespace w4a16 {
+template <int DT>
+cudaError_t launch_gemm_dt(int which, int scale_kind, const GemmParams& p, const CUtensorMap& tmA,
+                           const CUtensorMap& tmB, int grid, int smem_bytes, cudaStream_t s, bool pdl);
+extern template cudaError_t launch_gemm_dt<DT_BF16>(int, int, const GemmParams&, const CUtensorMap&,
+                                                     const CUtensorMap&, int, int, cudaStream_t, bool);
+extern template cudaError_t launch_gemm_dt<DT_FP16>(int, int, const GemmParams&, const CUtensorMap&,
+                                                     const CUtensorMap&, int, int, cudaStream_t, bool);
+
+cudaError_t launch_gemm(int which, int scale_kind, int dtype, const GemmParams& p,
+                        const CUtensorMap& tmA, const CUtensorMap& tmB, int grid, int smem_bytes,
+                        cudaStream_t s, bool pdl) {
+  if (dtype == DT_BF16) return launch_gemm_dt<DT_BF16>(which, scale_kind, p, tmA, tmB, grid, smem_bytes, s, pdl);
+  return launch_gemm_dt<DT_FP16>(which, scale_kind, p, tmA, tmB, grid, smem_bytes, s, pdl);
+}
+}  // namespace w4a16
+
+extern "C" {
+
+w4a16_status w4a16_moe_plan(const w4a16_moe_desc* desc, w4a16_moe_plan_t* out, size_t* workspace_bytes) {
+  if (!out || !workspace_bytes) return fail(W4A16_ERR_INVALID_ARG, "out / workspace_bytes is NULL");
+  *out = nullptr;
+  w4a16_status st = validate_desc(desc);
+  if (st != W4A16_OK) return st;
+  auto* P = new w4a16_moe_plan_s();
+  P->d = *desc;
+  P->num_sms = 152;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess &&
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && sms > 0) {
+    P->num_sms = sms;
+  } else {
+    cudaGetLastError();  // no device here: plan with the GB300 SM count
+  }
+  P->pdl = env_flag("W4A16_MOE_PDL", true);
+  P->ws_bytes = max_workspace(*P);
+  *out = P;
+  *workspace_bytes = P->ws_bytes;
+  return W4A16_OK;
+}
+
+w4a16_status w4a16_moe_plan_destroy(w4a16_moe_plan_t plan) {
+  delete plan;
+  return W4A16_OK;
+}
+
+w4a16_status w4a16_moe_set_overrides(w4a16_moe_plan_t plan, int32_t tile_rows, int32_t s1, int32_t s2,
+                                     size_t* workspace_bytes) {
+  if (!plan) return fail(W4A16_ERR_INVALID_ARG, "plan is NULL");
+  if (tile_rows != 0 && (tile_rows < 16 || tile_rows > kMaxBN || tile_rows % 16 != 0))
+    return fail(W4A16_ERR_INVALID_ARG, "tile_rows must be 0 or a multiple of 16 in [16, %d]", kMaxBN);
+  if (s1 < 0 || s1 > 64 || s2 < 0 || s2 > 64)
+    return fail(W4A16_ERR_INVALID_ARG, "split factors must be in [0, 64]");
+  plan->ov_bn = tile_rows;
+  plan->ov_s1 = s1;
+  plan->ov_s2 = s2;
+  plan->ws_bytes = max_workspace(*plan);
+  if (workspace_bytes) *workspace_bytes = plan->ws_bytes;
+  return W4A16_OK;
+}
+
+w4a16_status w4a16_moe_route_info(w4a16_moe_plan_t plan, int32_t num_tokens, w4a16_route_info* info) {
+  if (!plan || !info) return fail(W4A16_ERR_INVALID_ARG, "plan / info is NULL");
+  if (num_tokens < 0 || num_tokens > plan->d.max_tokens)
+    return fail(W4A16_ERR_INVALID_ARG, "num_tokens %d outside [0, %d]", num_tokens, plan->d.max_tokens);
+  const Layout L = make_layout(*plan, num_tokens);
+  info->tile_rows = L.bn;
+  info->max_slots = static_cast<int32_t>(L.slots_cap);
+  info->max_tiles = L.tiles_cap;
+  info->gemm1_splits = L.s1;
+  info->gemm2_splits = L.s2;
+  info->gemm1_ctas = L.grid1;
+  info->gemm2_ctas = L.grid2;
+  info->pipeline_stages = L.stages;
+  info->off_counts = L.off_counts;
+  info->off_offs = L.off_offs;
+  info->off_perm = L.off_perm;
+  info->off_inv = L.off_inv;
+  info->off_tiles = L.off_tiles;
+  info->off_num_tiles = L.off_ntiles;
+  info->off_inter = L.off_inter;
+  info->off_expert_out = L.off_y;
+  return W4A16_OK;
+}
+
+w4a16_status w4a16_moe_prepare_routes(w4a16_moe_plan_t plan, int32_t num_tokens, const int32_t* topk_ids,
+                                      void* workspace, void* stream) {
+  if (!plan) return fail(W4A16_ERR_INVALID_ARG, "plan is NULL");
+  if (num_tokens < 0 || num_tokens > plan->d.max_tokens)
+    return fail(W4A16_ERR_INVALID_ARG, "num_tokens %d outside [0, %d]", num_tokens, plan->d.max_tokens);
+  if (num_tokens == 0) return W4A16_OK;
+  w4a16_status st;
+  if ((st = check_ptr(topk_ids, 4, "topk_ids")) != W4A16_OK) return st;
+  if ((st = check_ptr(workspace, 256, "workspace")) != W4A16_OK) return st;
+  const Layout L = make_layout(*plan, num_tokens);
+  return launch_prepare(*plan, L, topk_ids, static_cast<uint8_t*>(workspace),
+                        static_cast<cudaStream_t>(stream));
+}
+
+w4a16_status w4a16_moe_forward(w4a16_moe_plan_t plan, int32_t num_tokens, const void* x, const uint8_t* w13,
+                               const uint16_t* s13, const uint8_t* w2, const uint16_t* s2,
+                               const float* topk_weights, const int32_t* topk_ids, int32_t renormalize,
+                               void* out, void* workspace, void* stream) {
+  if (!plan) return fail(W4A16_ERR_INVALID_ARG, "plan is NULL");
+  if (num_tokens < 0 || num_tokens > plan->d.max_tokens)
+    return fail(W4A16_ERR_INVALID_ARG, "num_tokens %d outside [0, %d]", num_tokens, plan->d.max_tokens);
+  if (num_tokens == 0) return W4A16_OK;
+  w4a16_status st;
+  if ((st = check_ptr(x, 16, "x")) != W4A16_OK) return st;
+  if ((st = check_ptr(w13, 16, "w13")) != W4A16_OK) return st;
+  if ((st = check_ptr(s13, 4, "s13")) != W4A16_OK) return st;
+  if ((st = check_ptr(w2, 16, "w2")) != W4A16_OK) return st;
+  if ((st = check_ptr(s2, 4, "s2")) != W4A16_OK) return st;
+  if ((st = check_ptr(topk_weights, 4, "topk_weights")) != W4A16_OK) return st;
+  if ((st = check_ptr(topk_ids, 4, "topk_ids")) != W4A16_OK) return st;
+  if ((st = check_ptr(out, 16, "out")) != W4A16_OK) return st;
+  if ((st = check_ptr(workspace, 256, "workspace")) != W4A16_OK) return st;
+  const Layout L = make_layout(*plan, num_tokens);
+  return launch_forward(*plan, L, x, w13, s13, w2, s2, topk_weights, renormalize, out,
+                        static_cast<uint8_t*>(workspace), static_cast<cudaStream_t>(stream));
+}
+
+w4a16_status w4a16_moe_forward_host(w4a16_moe_plan_t plan, int32_t num_tokens, const void* x_host,
+                                    const uint8_t* w13, const uint16_t* s13, const uint8_t* w2,
+                                    const uint16_t* s2, const float* topk_weights_host,
+                                    const int32_t* topk_ids_host, int32_t renormalize, void* out_host,
+                                    void* workspace, void* stream) {
+  if (!plan) return fail(W4A16_ERR_INVALID_ARG, "plan is NULL");
+  if (num_tokens < 0 || num_tokens > plan->d.max_tokens)
+    return fail(W4A16_ERR_INVALID_ARG, "num_tokens %d outside [0, %d]", num_tokens, plan->d.max_tokens);
+  if (num_tokens == 0) return W4A16_OK;
+  if (!x_host || !topk_weights_host || !topk_ids_host || !out_host)
+    return fail(W4A16_ERR_INVALID_ARG, "host buffer is NULL");
+  w4a16_status st;
+  if ((st = check_ptr(workspace, 256, "workspace")) != W4A16_OK) return st;
+  const Layout L = make_layout(*plan, num_tokens);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t xb = static_cast<size_t>(num_tokens) * plan->d.hidden * 2;
+  const size_t rb = static_cast<size_t>(L.R) * 4;
+  cudaError_t e;
+  if ((e = cudaMemcpyAsync(ws + L.off_sx, x_host, xb, cudaMemcpyHostToDevice, s)) != cudaSuccess)
+    return cuda_fail(e, "copy x");
+  if ((e = cudaMemcpyAsync(ws + L.off_sids, topk_ids_host, rb, cudaMemcpyHostToDevice, s)) != cudaSuccess)
+    return cuda_fail(e, "copy topk_ids");
+  if ((e = cudaMemcpyAsync(ws + L.off_sw, topk_weights_host, rb, cudaMemcpyHostToDevice, s)) != cudaSuccess)
+    return cuda_fail(e, "copy topk_weights");
+  st = w4a16_moe_prepare_routes(plan, num_tokens, reinterpret_cast<const int32_t*>(ws + L.off_sids), workspace,
+                                stream);
+  if (st != W4A16_OK) return st;
+  st = w4a16_moe_forward(plan, num_tokens, ws + L.off_sx, w13, s13, w2, s2,
+                         reinterpret_cast<const float*>(ws + L.off_sw),
+                         reinterpret_cast<const int32_t*>(ws + L.off_sids), renormalize, ws + L.off_sout,
+                         workspace, stream);
+  if (st != W4A16_OK) return st;
+  if ((e = cudaMemcpyAsync(out_host, ws + L.off_sout, xb, cudaMemcpyDeviceToHost, s)) != cudaSuccess)
+    return cuda_fail(e, "copy out");
+  if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return cuda_fail(e, "stream sync");
+  return W4A16_OK;
+}
+
+w4a16_status w4a16_moe_check_device_error(w4a16_moe_plan_t plan, void* workspace, void* stream) {
+  if (!plan || !workspace) return fail(W4A16_ERR_INVALID_ARG, "plan / workspace is NULL");
+  const Layout L = make_layout(*plan, 1);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int32_t flag = 0;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  cudaError_t e = cudaMemcpyAsync(&flag, ws + L.off_err, sizeof(flag), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "read device error flag");
+  if (flag != 0) {
+    e = cudaMemsetAsync(ws + L.off_err, 0, sizeof(int32_t), s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    return fail(W4A16_ERR_DEVICE_TIMEOUT, "a bounded wait inside a kernel timed out (flag %d)", flag);
+  }
+  return W4A16_OK;
+}
+
+w4a16_status w4a16_moe_set_stage_events(w4a16_moe_plan_t plan, void* const* events, int32_t n) {
+  if (!plan) return fail(W4A16_ERR_INVALID_ARG, "plan is NULL");
+  if (n == 0) {
+    plan->has_ev = false;
+    return W4A16_OK;
+  }
+  if (n != 4 || !events) return fail(W4A16_ERR_INVALID_ARG, "need exactly 4 events");
+  for (int i = 0; i < 4; ++i) {
+    if (!events[i]) return fail(W4A16_ERR_INVALID_ARG, "event %d is NULL", i);
+    plan->ev[i] = static_cast<cudaEvent_t>(events[i]);
+  }
+  plan->has_ev = true;
+  return W4A16_OK;
+}
+
+const char* w4a16_moe_last_error(void) { return g_err.c_str(); }
+
+}  // extern "C"

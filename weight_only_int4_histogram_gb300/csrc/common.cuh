@@ -1,0 +1,374 @@
+// Shared definitions of the sm_103a W4A16 MoE kernels: launch parameter
+// structs (host <-> device) and thin inline-PTX wrappers for mbarriers, TMA,
+// tcgen05 (TMEM allocation, MMA, loads/stores) and programmatic dependent
+// launch.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+namespace w4a16 {
+
+// ---------------------------------------------------------------------------
+// Tiling constants
+// ---------------------------------------------------------------------------
+constexpr int kTileRows = 128;       // weight rows per MMA tile (MMA M)
+constexpr int kBlockK = 256;         // K elements per pipeline stage
+constexpr int kGroup = 32;           // group size of the group-wise scales
+constexpr int kMaxStages = 8;
+constexpr int kGemmThreads = 512;    // 16 warps: see the role map in gemm.cuh
+constexpr int kTmemCols = 512;
+constexpr int kAbufCols = kBlockK / 2;  // one stage of BF16/FP16 A in TMEM columns
+constexpr int kMaxBN = 128;
+constexpr int kStageA = kTileRows * kBlockK / 2;   // 16 KB packed INT4 per stage
+constexpr int kStageS = kTileRows * 16;             // 8 BF16 scales per row per stage
+
+enum { ACT_SWIGLU = 0, ACT_RELU2 = 1 };
+enum { SCALE_GROUP = 0, SCALE_CHANNEL = 1 };
+enum { DT_BF16 = 0, DT_FP16 = 1 };
+enum { GEMM_UP = 0, GEMM_DOWN = 1 };
+
+// ---------------------------------------------------------------------------
+// Launch parameters
+// ---------------------------------------------------------------------------
+struct RoutePrepParams {
+  const int32_t* ids;      // [T, k]
+  int32_t T, k, E, expert_offset, bm;
+  int32_t* counts;         // [E]
+  int32_t* offs;           // [E + 1]
+  int32_t* perm;           // [slots_cap]
+  int32_t* inv;            // [T * k]
+  int4* tiles;             // [tiles_cap]
+  int32_t* num_tiles;      // [1]
+  int32_t* counters;       // [ctr_len] split-K arrival counters, zeroed here
+  int32_t ctr_len;
+  int32_t* err;            // device error flag, cleared here
+};
+
+struct GemmParams {
+  int32_t act;             // ACT_* (gate/up GEMM epilogue)
+  int32_t E;               // local experts
+  int32_t n_rows;          // weight rows per expert: N1 (gate/up) or H (down)
+  int32_t K;               // reduction length: H (gate/up) or I (down)
+  int32_t inter;           // I
+  int32_t out_cols;        // row length of the output buffer (I or H)
+  int32_t bn;              // route-tile height = MMA N
+  int32_t n_tiles;         // 128-row weight tiles per expert
+  int32_t kb_total;        // K blocks of kBlockK
+  int32_t splits;          // split-K factor
+  int32_t kb_per_split;
+  int32_t stages;
+  int32_t top_k;
+  int32_t stage_bytes;
+  const int4* tiles;       // route tiles (expert, first slot, valid rows, 0)
+  const int32_t* num_tiles;
+  const int32_t* perm;     // slot -> flat route (gate/up gather)
+  const void* x;           // gate/up: activations [T, H]
+  const uint16_t* scales;  // BF16 scale bits of this GEMM's weights
+  int64_t slots_cap;
+  void* out;               // gate/up: intermediate [slots_cap, I] act dtype
+                           // down: FP32 partial outputs [splits, slots_cap, H]
+  float* part;             // gate/up split-K partials [splits, slots_cap, N1]
+  int32_t* counters;       // gate/up split-K arrival counters [tiles_cap * n_tiles]
+  int32_t* err;
+};
+
+struct CombineParams {
+  const float* y;          // [splits, slots_cap, H]
+  int64_t slots_cap;
+  int32_t splits;
+  const int32_t* inv;      // [T * k]
+  const float* topk_weights;
+  int32_t T, H, k, renormalize;
+  void* out;               // [T, H] act dtype
+};
+
+// Host-side launchers (one translation unit each).
+cudaError_t launch_route_prep(const RoutePrepParams& p, int smem_bytes, cudaStream_t s, bool pdl);
+cudaError_t launch_gemm(int which, int scale_kind, int dtype, const GemmParams& p,
+                        const CUtensorMap& tmA, const CUtensorMap& tmB, int grid, int smem_bytes,
+                        cudaStream_t s, bool pdl);
+cudaError_t launch_combine(int dtype, const CombineParams& p, cudaStream_t s, bool pdl);
+int gemm_smem_bytes(int bn, int stages);
+int gemm_stage_bytes(int bn);
+
+constexpr int kRoutePrepThreads = 1024;
+constexpr int kRoutePrepWarps = kRoutePrepThreads / 32;
+
+#if defined(__CUDACC__)
+
+// Error codes written to the device error flag.
+constexpr int kErrTimeout = 1;
+constexpr unsigned long long kWaitTimeoutNs = 2000000000ull;  // 2 s
+
+// ---------------------------------------------------------------------------
+// Generic helpers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ uint32_t lane_id() { return threadIdx.x & 31; }
+
+// Programmatic dependent launch.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------
+// mbarrier
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+               : "memory");
+}
+
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile(
+      "{\n\t.reg .b64 st;\n\t"
+      "mbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile(
+      "{\n\t.reg .b64 st;\n\t"
+      "mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(smem_u32(bar)),
+      "r"(bytes)
+      : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait: returns false when the CTA-wide abort flag is raised or the
+// wait has lasted kWaitTimeoutNs, after raising the abort flag and the global
+// error flag.  Every spin in the GEMM pipeline goes through here.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                          int32_t* err) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t n = 1;; ++n) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((n & 63) == 0) {
+      if (*abort_flag) return false;
+      if (global_timer_ns() - t0 > kWaitTimeoutNs) {
+        *abort_flag = 1;
+        atomicExch(err, kErrTimeout);
+        return false;
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// TMA (tensor) loads, completion signalled on an mbarrier as transaction bytes
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar,
+                                            int c0, int c1, int c2, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::"
+      "cache_hint [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2),
+      "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar,
+                                            int c0, int c1, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::"
+      "cache_hint [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "l"(policy)
+      : "memory");
+}
+
+// Four rows (r0..r3) of a 2D tensor, each `box[0]` elements wide starting at
+// column c0; the tensor map's box is one row high.
+__device__ __forceinline__ void tma_gather4(void* dst, const CUtensorMap* map, uint64_t* bar,
+                                            int c0, int r0, int r1, int r2, int r3,
+                                            uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%3, %4, %5, %6, %7}], [%2], %8;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(r0), "r"(r1),
+      "r"(r2), "r"(r3), "l"(policy)
+      : "memory");
+}
+
+// Ampere-style asynchronous copies (used for the small group-scale tiles whose
+// global row stride is not a multiple of 16 bytes in general).
+template <int BYTES>
+__device__ __forceinline__ void cp_async(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], %2;" ::"r"(smem_u32(dst)), "l"(src),
+               "n"(BYTES)
+               : "memory");
+}
+
+// Arrive on `bar` once this thread's earlier cp.async copies have landed; the
+// pending count is raised first, so the barrier's expected count is unchanged.
+__device__ __forceinline__ void cp_async_mbar_arrive(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// tcgen05: tensor memory, MMA, loads and stores
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                   smem_u32(dst_smem)),
+               "r"(ncols)
+               : "memory");
+}
+
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// D[tmem] (+)= A[tmem] x B[smem]^T, kind::f16 (BF16/FP16 in, FP32 accumulate).
+__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                       uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrive on `bar` once every tcgen05.mma issued so far by this thread is done.
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          smem_u32(bar))
+      : "memory");
+}
+
+// Instruction descriptor of kind::f16: FP32 accumulator, A and B of the same
+// 16-bit type (bf16 when `bf16`), both K-major, shape M x N.
+__host__ __device__ constexpr uint32_t make_idesc_f16(bool bf16, int m, int n) {
+  return (1u << 4)                                   // D format: F32
+         | ((bf16 ? 1u : 0u) << 7)                   // A format
+         | ((bf16 ? 1u : 0u) << 10)                  // B format
+         | (static_cast<uint32_t>(n >> 3) << 17)     // N / 8
+         | (static_cast<uint32_t>(m >> 4) << 24);    // M / 16
+}
+
+// Shared-memory matrix descriptor: K-major operand stored with the 128-byte
+// swizzle (rows of 128 bytes, 8-row atoms of 1024 bytes).
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFF);          // start address
+  d |= static_cast<uint64_t>(1) << 16;                        // leading byte offset (unused)
+  d |= static_cast<uint64_t>(1024 >> 4) << 32;                // stride byte offset: 8 rows
+  d |= static_cast<uint64_t>(1) << 46;                        // descriptor version
+  d |= static_cast<uint64_t>(2) << 61;                        // swizzle: 128B
+  return d;
+}
+
+// 32 lanes x 32 bit, repeated over N consecutive columns.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+      "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
+      "r"(v[15])
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&v)[8]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(
+          taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tmem_wait_ld() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Named barrier over a subset of warps.
+__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+__device__ __forceinline__ uint32_t lop3_and_xor(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("lop3.b32 %0, %1, %2, %3, 0x6A;" : "=r"(d) : "r"(a), "r"(b), "r"(c));  // (a & b) ^ c
+  return d;
+}
+
+#endif  // __CUDACC__
+
+}  // namespace w4a16

@@ -1,0 +1,660 @@
+// Expert-grouped W4A16 GEMM for sm_103a (both MoE GEMMs).
+//
+// Computes, per route tile (expert e, bn consecutive slots) and per 128-row
+// weight tile, the swapped product  D[row, route] = sum_k Wq[e][row, k] * B[route, k]
+// with the INT4 weights dequantised on chip.  This is the "gate/up GEMM" and
+// "down GEMM" of "feat(pytorch): add CuTeDSL W4A16 MoE backend" (LMDeploy),
+// sections Modification (register-side INT4 dequantisation, FP32
+// accumulation, TMA buffering, small-batch split-K, route-count-based tile
+// selection) and Benchmark; the dequantisation is done by two warp-specialised
+// warpgroups as in "perf: reduce split W4A16 routing and output overhead"
+// (FlashInfer), section Description.  Blackwell design (not the pages'):
+//
+//   weights (A, M = 128 rows)  TMA (128B swizzle) -> SMEM packed INT4
+//                              -> dequant warps -> BF16/FP16 A operand in TMEM
+//   activations (B, N = bn)    gate/up: cp.async row gather by slot -> token
+//                              down:    TMA tile of the intermediate
+//                              -> SMEM (128B-swizzled, K-major)
+//   tcgen05.mma.kind::f16 (A from TMEM, B from SMEM), FP32 accumulators in TMEM,
+//   double-buffered, drained by four epilogue warps.
+//
+// Warp roles (512 threads):
+//   warp 0       TMA producer: packed weights, group scales (cp.async), and for
+//                the down GEMM the intermediate tile
+//   warp 1       TMEM allocation + single-thread MMA issuer
+//   warps 2, 3   gate/up GEMM: activation-row gather (cp.async, 16 B per lane)
+//   warps 4..11  two dequant warpgroups; warpgroup g handles pipeline stages
+//                with (stage counter & 1) == g and owns TMEM A buffer g
+//   warps 12..15 epilogue (TMEM -> registers -> activation / scaling -> HBM)
+//
+// Work is a persistent loop over units (route tile, weight tile, K split);
+// every role walks the same unit sequence.  All waits are bounded (see
+// mbar_wait): a stuck pipeline raises an error flag and the CTA winds down,
+// draining its copies and MMAs before freeing TMEM.
+#pragma once
+#include "common.cuh"
+
+namespace w4a16 {
+
+// 16-bit type helpers -------------------------------------------------------
+template <int DT> struct F16;
+template <> struct F16<DT_BF16> {
+  // bits of 128 + (nibble ^ 8) in BF16 once ORed/XORed with the nibble, and of 136.0
+  static constexpr uint32_t kMagic = 0x43084308u;
+  __device__ static __forceinline__ uint32_t sub(uint32_t a, uint32_t b) {
+    __nv_bfloat162 r = __hsub2(*reinterpret_cast<__nv_bfloat162*>(&a),
+                               *reinterpret_cast<__nv_bfloat162*>(&b));
+    return *reinterpret_cast<uint32_t*>(&r);
+  }
+  __device__ static __forceinline__ uint32_t mul(uint32_t a, uint32_t b) {
+    __nv_bfloat162 r = __hmul2(*reinterpret_cast<__nv_bfloat162*>(&a),
+                               *reinterpret_cast<__nv_bfloat162*>(&b));
+    return *reinterpret_cast<uint32_t*>(&r);
+  }
+  // BF16 scale bits -> this type's bits (identity for BF16)
+  __device__ static __forceinline__ uint16_t from_bf16(uint16_t s) { return s; }
+  __device__ static __forceinline__ uint16_t from_float(float f) {
+    __nv_bfloat16 h = __float2bfloat16_rn(f);
+    return *reinterpret_cast<uint16_t*>(&h);
+  }
+};
+template <> struct F16<DT_FP16> {
+  // FP16: 1024 + (nibble ^ 8) and 1032.0
+  static constexpr uint32_t kMagic = 0x64086408u;
+  __device__ static __forceinline__ uint32_t sub(uint32_t a, uint32_t b) {
+    __half2 r = __hsub2(*reinterpret_cast<__half2*>(&a), *reinterpret_cast<__half2*>(&b));
+    return *reinterpret_cast<uint32_t*>(&r);
+  }
+  __device__ static __forceinline__ uint32_t mul(uint32_t a, uint32_t b) {
+    __half2 r = __hmul2(*reinterpret_cast<__half2*>(&a), *reinterpret_cast<__half2*>(&b));
+    return *reinterpret_cast<uint32_t*>(&r);
+  }
+  __device__ static __forceinline__ uint16_t from_bf16(uint16_t s) {
+    const float f = __uint_as_float(static_cast<uint32_t>(s) << 16);
+    __half h = __float2half_rn(f);
+    return *reinterpret_cast<uint16_t*>(&h);
+  }
+  __device__ static __forceinline__ uint16_t from_float(float f) {
+    __half h = __float2half_rn(f);
+    return *reinterpret_cast<uint16_t*>(&h);
+  }
+};
+
+__device__ __forceinline__ float bf16_bits_to_float(uint16_t b) {
+  return __uint_as_float(static_cast<uint32_t>(b) << 16);
+}
+
+// Unit decoding shared by every role.
+struct Unit {
+  int tile, nt, split, kb0, kb1;
+};
+
+__device__ __forceinline__ Unit decode_unit(const GemmParams& p, int u) {
+  Unit w;
+  w.split = u % p.splits;
+  const int r = u / p.splits;
+  w.nt = r % p.n_tiles;
+  w.tile = r / p.n_tiles;
+  w.kb0 = w.split * p.kb_per_split;
+  w.kb1 = min(w.kb0 + p.kb_per_split, p.kb_total);
+  return w;
+}
+
+// Row (within the expert) of the weight rows held in tile rows 0..63 / 64..127.
+template <int WHICH>
+__device__ __forceinline__ void tile_row_bases(const GemmParams& p, int nt, int& r0, int& r1) {
+  if (WHICH == GEMM_UP && p.act == ACT_SWIGLU) {
+    r0 = 64 * nt;            // gate rows
+    r1 = p.inter + 64 * nt;  // matching up rows
+  } else {
+    r0 = 128 * nt;
+    r1 = 128 * nt + 64;
+  }
+}
+
+// Tile row (0..127, the row index inside the SMEM weight tile) fed to TMEM lane
+// `l`.  For SwiGLU the gate row and the up row of one intermediate index sit in
+// lanes l and l ^ 16 of the same warp, so the epilogue pairs them with a shuffle.
+template <int WHICH>
+__device__ __forceinline__ int tile_row_of_lane(const GemmParams& p, int l) {
+  if (WHICH == GEMM_UP && p.act == ACT_SWIGLU) {
+    const int q = l >> 5, t = l & 31;
+    const int i_local = 16 * q + (t & 15);
+    return (t >> 4) ? 64 + i_local : i_local;
+  }
+  return l;
+}
+
+// Dequantise one stage (kBlockK = 256 K values) of this thread's weight row
+// into TMEM columns [a_col, a_col + 128) of its lane.
+//   group scales: packed along K, 128 rows x 128 B (one 16 B chunk = one group
+//   of 32), scales 8 per row per stage; the A operand is q * s rounded once.
+//   per-channel: packed along rows, 4 boxes (K half, row block) of 32 row pairs
+//   x 128 B; the A operand is the exact code q (the scale is applied to the FP32
+//   accumulator in the epilogue).
+template <int SCALE, int DT>
+__device__ __forceinline__ void dequant_stage(const uint8_t* sA, const uint8_t* sS, int tr,
+                                              uint32_t a_taddr) {
+  using T = F16<DT>;
+  const uint32_t kMask = 0x000F000Fu;
+  if (SCALE == SCALE_GROUP) {
+    const uint4 sc = *reinterpret_cast<const uint4*>(sS + tr * 16);
+    const uint32_t sw[4] = {sc.x, sc.y, sc.z, sc.w};
+    const uint8_t* row = sA + tr * 128;
+#pragma unroll
+    for (int g = 0; g < 8; ++g) {
+      const uint4 w = *reinterpret_cast<const uint4*>(row + ((g ^ (tr & 7)) << 4));
+      const uint16_t s16 = T::from_bf16(static_cast<uint16_t>(sw[g >> 1] >> ((g & 1) * 16)));
+      const uint32_t s2 = static_cast<uint32_t>(s16) * 0x00010001u;
+      const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+      uint32_t out[16];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t x = ws[i];
+        const uint32_t sh = x >> 4;
+        // (k, k+1) = low and high nibble of byte m, moved to the two halves
+        const uint32_t p0 = __byte_perm(x, sh, 0x0400);
+        const uint32_t p1 = __byte_perm(x, sh, 0x0501);
+        const uint32_t p2 = __byte_perm(x, sh, 0x0602);
+        const uint32_t p3 = __byte_perm(x, sh, 0x0703);
+        out[4 * i + 0] = T::mul(T::sub(lop3_and_xor(p0, kMask, T::kMagic), T::kMagic), s2);
+        out[4 * i + 1] = T::mul(T::sub(lop3_and_xor(p1, kMask, T::kMagic), T::kMagic), s2);
+        out[4 * i + 2] = T::mul(T::sub(lop3_and_xor(p2, kMask, T::kMagic), T::kMagic), s2);
+        out[4 * i + 3] = T::mul(T::sub(lop3_and_xor(p3, kMask, T::kMagic), T::kMagic), s2);
+      }
+      tmem_st16(a_taddr + 16 * g, out);
+    }
+  } else {
+    const int b = tr >> 6;
+    const int lr = tr & 63;
+    const int pr = lr >> 1;
+    const int shift = (lr & 1) * 4;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const uint8_t* row = sA + (h * 2 + b) * 4096 + pr * 128;
+#pragma unroll 2
+      for (int c = 0; c < 8; ++c) {
+        const uint4 w = *reinterpret_cast<const uint4*>(row + ((c ^ (pr & 7)) << 4));
+        const uint32_t ws[4] = {w.x >> shift, w.y >> shift, w.z >> shift, w.w >> shift};
+        uint32_t out[8];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const uint32_t p0 = __byte_perm(ws[i], 0, 0x0100);
+          const uint32_t p1 = __byte_perm(ws[i], 0, 0x0302);
+          out[2 * i + 0] = T::sub(lop3_and_xor(p0, kMask, T::kMagic), T::kMagic);
+          out[2 * i + 1] = T::sub(lop3_and_xor(p1, kMask, T::kMagic), T::kMagic);
+        }
+        tmem_st8(a_taddr + h * 64 + c * 8, out);
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ float silu_f(float g) { return g / (1.0f + expf(-g)); }
+
+template <int WHICH, int SCALE, int DT>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    w4a16_gemm_kernel(const __grid_constant__ GemmParams p, const __grid_constant__ CUtensorMap tmA,
+                      const __grid_constant__ CUtensorMap tmB) {
+  using T = F16<DT>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const int stages = p.stages;
+  const int bn = p.bn;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + stages * p.stage_bytes);
+  uint64_t* empty = full + kMaxStages;
+  uint64_t* afull = empty + kMaxStages;
+  uint64_t* aempty = afull + 2;
+  uint64_t* accfull = aempty + 2;
+  uint64_t* accempty = accfull + 2;
+  uint64_t* drain = accempty + 2;
+  uint64_t* epibar = drain + 1;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(epibar + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+  volatile int* fixup_flag = reinterpret_cast<volatile int*>(tmem_holder + 2);
+  int32_t* tok_s = reinterpret_cast<int32_t*>(tmem_holder + 4);  // [kMaxBN]
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const bool gather_b = (WHICH == GEMM_UP);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < stages; ++s) {
+      mbar_init(&full[s], gather_b ? 3 : 1);   // producer (+ two gather warps)
+      mbar_init(&empty[s], 5);                 // 4 dequant warps + MMA commit
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&afull[b], 4);
+      mbar_init(&aempty[b], 1);
+      mbar_init(&accfull[b], 1);
+      mbar_init(&accempty[b], 4);
+    }
+    mbar_init(drain, 1);
+    mbar_init(epibar, 4);
+    *abort_flag = 0;
+    *fixup_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    if (!gather_b) tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_holder, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+
+  // Everything below reads what the previous kernels wrote.
+  pdl_wait();
+  pdl_launch_dependents();
+
+  const int n_units = (*p.num_tiles) * p.n_tiles * p.splits;
+  const int N1 = p.n_rows;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------------ producer
+    const uint64_t pol_w = l2_policy_evict_first();
+    const uint64_t pol_b = l2_policy_evict_last();
+    const int groups_row = p.K / kGroup;
+    const int sbytes_row = groups_row * 2;
+    uint32_t it = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+      const Unit w = decode_unit(p, u);
+      if (w.kb1 <= w.kb0) continue;
+      const int4 ti = p.tiles[w.tile];
+      const int e = ti.x, m0 = ti.y;
+      int r0, r1;
+      tile_row_bases<WHICH>(p, w.nt, r0, r1);
+      for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
+        const int st = it % stages;
+        if (!mbar_wait(&empty[st], ((it / stages) & 1) ^ 1, abort_flag, p.err)) {
+          ok = false;
+          break;
+        }
+        uint8_t* sA = smem + st * p.stage_bytes;
+        uint8_t* sB = sA + kStageA;
+        uint8_t* sS = sB + bn * 512;
+        if (SCALE == SCALE_GROUP) {
+          // 8 scales (16 B) per tile row; lane handles rows lane + 32 i.
+          const int g0 = kb * 8;
+          const int ng = min(8, groups_row - g0);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int tr = lane + 32 * i;
+            const int grow = tr < 64 ? r0 + tr : r1 + (tr - 64);
+            uint8_t* dst = sS + tr * 16;
+            if (grow < N1 && ng > 0) {
+              const uint8_t* src = reinterpret_cast<const uint8_t*>(p.scales) +
+                                   (static_cast<int64_t>(e) * N1 + grow) * sbytes_row + g0 * 2;
+              const int nbytes = ng * 2;
+              const uint32_t a = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(src));
+              if ((a & 15) == 0 && nbytes == 16) {
+                cp_async<16>(dst, src);
+              } else if ((a & 7) == 0 && (nbytes & 7) == 0) {
+                for (int o = 0; o < nbytes; o += 8) cp_async<8>(dst + o, src + o);
+              } else {
+                for (int o = 0; o < nbytes; o += 4) cp_async<4>(dst + o, src + o);
+              }
+              for (int o = nbytes; o < 16; o += 4) *reinterpret_cast<uint32_t*>(dst + o) = 0u;
+            } else {
+              *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
+            }
+          }
+          cp_async_mbar_arrive(&full[st]);
+        }
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&full[st], kStageA + (gather_b ? 0 : bn * 512));
+          if (SCALE == SCALE_GROUP) {
+            tma_load_3d(sA, &tmA, &full[st], kb * 128, r0, e, pol_w);
+            tma_load_3d(sA + 8192, &tmA, &full[st], kb * 128, r1, e, pol_w);
+          } else {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              tma_load_3d(sA + (h * 2 + 0) * 4096, &tmA, &full[st], kb * 256 + h * 128, r0 / 2, e,
+                          pol_w);
+              tma_load_3d(sA + (h * 2 + 1) * 4096, &tmA, &full[st], kb * 256 + h * 128, r1 / 2, e,
+                          pol_w);
+            }
+          }
+          if (!gather_b) {
+#pragma unroll
+            for (int a = 0; a < 4; ++a)
+              tma_load_2d(sB + a * bn * 128, &tmB, &full[st], kb * 256 + a * 64, m0, pol_b);
+          }
+        }
+        __syncwarp();
+      }
+    }
+    // Wind-down after an abort: wait (bounded) for the copies still in flight.
+    if (!ok && lane == 0) {
+      volatile int no_abort = 0;
+      for (uint32_t j = (it > (uint32_t)stages ? it - stages : 0); j < it; ++j)
+        mbar_wait(&full[j % stages], (j / stages) & 1, &no_abort, p.err);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = make_idesc_f16(DT == DT_BF16, kTileRows, bn);
+      uint32_t it = 0, jc = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+        const Unit w = decode_unit(p, u);
+        if (w.kb1 <= w.kb0) continue;
+        const int b = jc & 1;
+        if (!mbar_wait(&accempty[b], ((jc >> 1) & 1) ^ 1, abort_flag, p.err)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem + 2 * kAbufCols + b * bn;
+        for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
+          const int st = it % stages;
+          const int g = it & 1;
+          if (!mbar_wait(&full[st], (it / stages) & 1, abort_flag, p.err) ||
+              !mbar_wait(&afull[g], (it >> 1) & 1, abort_flag, p.err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sB = smem_u32(smem + st * p.stage_bytes + kStageA);
+#pragma unroll
+          for (int kk = 0; kk < kBlockK / 16; ++kk) {
+            const uint64_t bdesc = smem_desc_sw128(sB + (kk >> 2) * bn * 128 + (kk & 3) * 32);
+            mma_ts(d_tmem, tmem + g * kAbufCols + kk * 8, bdesc, idesc,
+                   (kb > w.kb0 || kk > 0) ? 1u : 0u);
+          }
+          mma_commit(&aempty[g]);
+          mma_commit(&empty[st]);
+        }
+        if (!ok) break;
+        mma_commit(&accfull[b]);
+        ++jc;
+      }
+      // Drain: every MMA issued by this thread has finished before TMEM is freed.
+      mma_commit(drain);
+      volatile int no_abort = 0;
+      mbar_wait(drain, 0, &no_abort, p.err);
+    }
+  } else if (warp == 2 || warp == 3) {
+    // ------------------------------------------------------------------ activation gather
+    if (gather_b) {
+      const int gw = warp - 2;
+      const int rows_per = bn / 2;
+      const uint16_t* x = reinterpret_cast<const uint16_t*>(p.x);
+      const int atom = lane >> 3, ch = lane & 7;
+      uint32_t it = 0;
+      int pending = -1;
+      bool ok = true;
+      for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+        const Unit w = decode_unit(p, u);
+        if (w.kb1 <= w.kb0) continue;
+        const int m0 = p.tiles[w.tile].y;
+        __syncwarp();
+        for (int r = lane; r < rows_per; r += 32) {
+          const int route = p.perm[m0 + gw * rows_per + r];
+          tok_s[gw * (kMaxBN / 2) + r] = route >= 0 ? route / p.top_k : 0;
+        }
+        __syncwarp();
+        for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
+          const int st = it % stages;
+          if (!mbar_wait(&empty[st], ((it / stages) & 1) ^ 1, abort_flag, p.err)) {
+            ok = false;
+            break;
+          }
+          uint8_t* sB = smem + st * p.stage_bytes + kStageA;
+          const int col = kb * kBlockK + lane * 8;
+          const bool valid = col < p.K;
+          for (int rr = 0; rr < rows_per; ++rr) {
+            const int r = gw * rows_per + rr;
+            uint8_t* dst = sB + atom * bn * 128 + r * 128 + ((ch ^ (r & 7)) << 4);
+            if (valid) {
+              const int tok = tok_s[gw * (kMaxBN / 2) + rr];
+              cp_async<16>(dst, x + static_cast<int64_t>(tok) * p.K + col);
+            } else {
+              *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
+            }
+          }
+          asm volatile("cp.async.commit_group;" ::: "memory");
+          if (pending >= 0) {
+            asm volatile("cp.async.wait_group 1;" ::: "memory");
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&full[pending]);
+          }
+          pending = st;
+        }
+      }
+      asm volatile("cp.async.wait_group 0;" ::: "memory");
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      __syncwarp();
+      if (pending >= 0 && lane == 0) mbar_arrive(&full[pending]);
+    }
+  } else if (warp < 12) {
+    // ------------------------------------------------------------------ dequant warpgroups
+    const int wg = (warp - 4) >> 2;
+    const int q = warp & 3;
+    const int tr = tile_row_of_lane<WHICH>(p, q * 32 + lane);
+    const uint32_t t_lane = tmem + (static_cast<uint32_t>(q * 32) << 16);
+    uint32_t it = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+      const Unit w = decode_unit(p, u);
+      if (w.kb1 <= w.kb0) continue;
+      for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
+        if ((it & 1) != static_cast<uint32_t>(wg)) continue;
+        const int st = it % stages;
+        if (!mbar_wait(&full[st], (it / stages) & 1, abort_flag, p.err) ||
+            !mbar_wait(&aempty[wg], ((it >> 1) & 1) ^ 1, abort_flag, p.err)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint8_t* sA = smem + st * p.stage_bytes;
+        const uint8_t* sS = sA + kStageA + bn * 512;
+        dequant_stage<SCALE, DT>(sA, sS, tr, t_lane + wg * kAbufCols);
+        tmem_wait_st();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[st]);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&afull[wg]);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------------ epilogue
+    const int q = warp & 3;
+    const int tr = tile_row_of_lane<WHICH>(p, q * 32 + lane);
+    const uint32_t t_lane = tmem + (static_cast<uint32_t>(q * 32) << 16);
+    const int epi_tid = threadIdx.x - 12 * 32;
+    const bool swiglu = (WHICH == GEMM_UP && p.act == ACT_SWIGLU);
+    uint32_t jc = 0, eph = 0;
+    bool ok = true;
+    // Bounded barrier over the four epilogue warps.
+    auto epi_sync = [&]() -> bool {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(epibar);
+      const bool r = mbar_wait(epibar, eph & 1, abort_flag, p.err);
+      ++eph;
+      return r;
+    };
+    for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+      const Unit w = decode_unit(p, u);
+      const bool has_k = w.kb1 > w.kb0;
+      const int4 ti = p.tiles[w.tile];
+      const int e = ti.x, m0 = ti.y, rows = ti.z;
+      int r0, r1;
+      tile_row_bases<WHICH>(p, w.nt, r0, r1);
+      const int grow = tr < 64 ? r0 + tr : r1 + (tr - 64);   // weight row in the expert
+      const bool row_ok = swiglu ? (64 * w.nt + (tr & 63)) < p.inter : grow < N1;
+      float scale = 1.0f;
+      if (SCALE == SCALE_CHANNEL && row_ok)
+        scale = bf16_bits_to_float(p.scales[static_cast<int64_t>(e) * N1 + grow]);
+      const int b = jc & 1;
+      if (has_k) {
+        if (!mbar_wait(&accfull[b], (jc >> 1) & 1, abort_flag, p.err)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+      }
+      const uint32_t acc_col = 2 * kAbufCols + b * bn;
+      // intermediate column of this lane (SwiGLU: gate/up pair index)
+      const int icol = swiglu ? 64 * w.nt + 16 * q + (lane & 15) : grow;
+      for (int c0 = 0; c0 < bn; c0 += 16) {
+        float v[16];
+        if (has_k) {
+          tmem_ld16(t_lane + acc_col + c0, v);
+          tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) v[j] = 0.0f;
+        }
+#pragma unroll
+        for (int j = 0; j < 16; ++j) v[j] *= scale;
+        if (WHICH == GEMM_DOWN) {
+          float* y = reinterpret_cast<float*>(p.out) +
+                     (static_cast<int64_t>(w.split) * p.slots_cap + m0) * p.out_cols + grow;
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int r = c0 + j;
+            if (r < rows && row_ok) y[static_cast<int64_t>(r) * p.out_cols] = v[j];
+          }
+        } else if (p.splits > 1) {
+          float* part = p.part + (static_cast<int64_t>(w.split) * p.slots_cap + m0) * N1 + grow;
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int r = c0 + j;
+            if (r < rows && row_ok) part[static_cast<int64_t>(r) * N1] = v[j];
+          }
+        } else {
+          uint16_t* inter = reinterpret_cast<uint16_t*>(p.out) + static_cast<int64_t>(m0) * p.inter;
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int r = c0 + j;
+            if (swiglu) {
+              const float other = __shfl_xor_sync(0xFFFFFFFFu, v[j], 16);
+              if ((j & 1) == (lane >> 4) && r < rows && row_ok) {
+                const float g = (lane < 16) ? v[j] : other;
+                const float up = (lane < 16) ? other : v[j];
+                inter[static_cast<int64_t>(r) * p.inter + icol] = T::from_float(silu_f(g) * up);
+              }
+            } else if (r < rows && row_ok) {
+              const float h = v[j] > 0.0f ? v[j] : 0.0f;
+              inter[static_cast<int64_t>(r) * p.inter + icol] = T::from_float(h * h);
+            }
+          }
+        }
+      }
+      if (has_k) {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&accempty[b]);
+        ++jc;
+      }
+      if (WHICH == GEMM_UP && p.splits > 1) {
+        // Split-K fix-up: the last split to finish sums all partials in split
+        // order (deterministic) and applies the activation.
+        __threadfence();
+        if (!epi_sync()) {
+          ok = false;
+          break;
+        }
+        if (epi_tid == 0) {
+          const int prev = atomicAdd(&p.counters[w.tile * p.n_tiles + w.nt], 1);
+          *fixup_flag = (prev == p.splits - 1) ? 1 : 0;
+        }
+        if (!epi_sync()) {
+          ok = false;
+          break;
+        }
+        if (*fixup_flag) {
+          __threadfence();
+          uint16_t* inter = reinterpret_cast<uint16_t*>(p.out) + static_cast<int64_t>(m0) * p.inter;
+          for (int c0 = 0; c0 < bn; c0 += 16) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const int r = c0 + j;
+              float h = 0.0f;
+              if (r < rows && row_ok) {
+                const float* src = p.part + static_cast<int64_t>(m0 + r) * N1 + grow;
+                for (int s = 0; s < p.splits; ++s) h += __ldcg(src + static_cast<int64_t>(s) * p.slots_cap * N1);
+              }
+              if (swiglu) {
+                const float other = __shfl_xor_sync(0xFFFFFFFFu, h, 16);
+                if ((j & 1) == (lane >> 4) && r < rows && row_ok) {
+                  const float g = (lane < 16) ? h : other;
+                  const float up = (lane < 16) ? other : h;
+                  inter[static_cast<int64_t>(r) * p.inter + icol] = T::from_float(silu_f(g) * up);
+                }
+              } else if (r < rows && row_ok) {
+                const float a = h > 0.0f ? h : 0.0f;
+                inter[static_cast<int64_t>(r) * p.inter + icol] = T::from_float(a * a);
+              }
+            }
+          }
+          if (epi_tid == 0) p.counters[w.tile * p.n_tiles + w.nt] = 0;
+        }
+      }
+    }
+  }
+
+  // ------------------------------------------------------------------ teardown
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+}  // namespace w4a16
+
+namespace w4a16 {
+
+template <int WHICH, int SCALE, int DT>
+cudaError_t launch_gemm_one(const GemmParams& p, const CUtensorMap& tmA, const CUtensorMap& tmB,
+                            int grid, int smem_bytes, cudaStream_t s, bool pdl) {
+  auto kern = w4a16_gemm_kernel<WHICH, SCALE, DT>;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  static int configured_for[64] = {0};
+  if (dev < 64 && configured_for[dev] < smem_bytes) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+    if (e != cudaSuccess) return e;
+    configured_for[dev] = smem_bytes;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kGemmThreads);
+  cfg.dynamicSmemBytes = smem_bytes;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, p, tmA, tmB);
+}
+
+template <int DT>
+cudaError_t launch_gemm_dt(int which, int scale_kind, const GemmParams& p, const CUtensorMap& tmA,
+                           const CUtensorMap& tmB, int grid, int smem_bytes, cudaStream_t s,
+                           bool pdl) {
+  if (which == GEMM_UP) {
+    return scale_kind == SCALE_GROUP
+               ? launch_gemm_one<GEMM_UP, SCALE_GROUP, DT>(p, tmA, tmB, grid, smem_bytes, s, pdl)
+               : launch_gemm_one<GEMM_UP, SCALE_CHANNEL, DT>(p, tmA, tmB, grid, smem_bytes, s, pdl);
+  }
+  return scale_kind == SCALE_GROUP
+             ? launch_gemm_one<GEMM_DOWN, SCALE_GROUP, DT>(p, tmA, tmB, grid, smem_bytes, s, pdl)
+             : launch_gemm_one<GEMM_DOWN, SCALE_CHANNEL, DT>(p, tmA, tmB, grid, smem_bytes, s, pdl);
+}
+
+}  // namespace w4a16

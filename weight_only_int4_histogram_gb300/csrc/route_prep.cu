@@ -1,0 +1,187 @@
+// Route-layout preparation ("histogram") for the local W4A16 MoE forward.
+//
+// Follows "feat(pytorch): add CuTeDSL W4A16 MoE backend" (LMDeploy),
+// sections Benchmark (route preparation is part of the timed forward) and
+// Modification (invalid routes and masked expert counts), and "perf: reduce
+// split W4A16 routing and output overhead" (FlashInfer), section Description
+// (routing-side bookkeeping on the route tiles).
+//
+// One CTA of 32 warps.  The flat routes r = t*k + j are cut into 32 contiguous
+// chunks, one per warp, so "earlier warp" means "smaller flat index":
+//   pass 1  per-warp histograms hist[w][e] (warp-synchronous, no atomics):
+//           lanes holding the same expert find each other with match_any and
+//           their lowest lane adds the group size;
+//   pass 2  column prefix over warps (routes of expert e in earlier chunks),
+//           then a warp-shuffle exclusive scan over experts of the padded
+//           segment sizes and of the tile counts;
+//   pass 3  every valid route takes slot offs[e] + earlier-chunk count +
+//           earlier-round count + rank among equal lanes of its round, which
+//           is its rank in ascending flat order: a stable permutation.
+// Padding slots get perm = -1 and the tile list (expert, first slot, valid
+// rows) is written per expert.  Integer work only: results are bit-exact and
+// independent of scheduling.
+#include "common.cuh"
+
+namespace w4a16 {
+
+__global__ void __launch_bounds__(kRoutePrepThreads, 1) route_prep_kernel(const RoutePrepParams p) {
+  extern __shared__ int32_t sm[];
+  const int E = p.E;
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  int32_t* hist = sm;                        // [32][E]
+  int32_t* cnt = hist + kRoutePrepWarps * E;  // [E]
+  int32_t* poff = cnt + E;                   // [E + 1]
+  int32_t* toff = poff + E + 1;              // [E + 1]
+  int32_t* wsum = toff + E + 1;              // [2][32]
+
+  // The ids come from upstream work and the previous forward may still read
+  // this workspace: wait for the preceding grid before touching anything.
+  pdl_wait();
+  pdl_launch_dependents();
+
+  for (int i = tid; i < kRoutePrepWarps * E; i += kRoutePrepThreads) hist[i] = 0;
+  for (int i = tid; i < p.ctr_len; i += kRoutePrepThreads) p.counters[i] = 0;
+  __syncthreads();
+
+  const int R = p.T * p.k;
+  const int chunk = ((R + kRoutePrepWarps - 1) / kRoutePrepWarps + 31) / 32 * 32;
+  const int r_begin = warp * chunk;
+  const int r_end = min(R, r_begin + chunk);
+  const unsigned full = 0xFFFFFFFFu;
+  const unsigned lt_mask = (1u << lane) - 1u;
+
+  auto local_of = [&](int r) -> int {
+    if (r >= r_end) return -1;
+    const int id = p.ids[r];
+    if (id == -1) return -1;
+    const long long l = static_cast<long long>(id) - p.expert_offset;
+    return (l >= 0 && l < E) ? static_cast<int>(l) : -1;
+  };
+
+  // pass 1: per-warp histograms
+  for (int base = r_begin; base < r_end; base += 32) {
+    const int e = local_of(base + lane);
+    const unsigned m = __match_any_sync(full, e);
+    if (e >= 0 && (m & lt_mask) == 0) hist[warp * E + e] += __popc(m);
+  }
+  __syncthreads();
+
+  // pass 2a: exclusive prefix over warps, per expert; total counts
+  for (int e = tid; e < E; e += kRoutePrepThreads) {
+    int run = 0;
+    for (int w = 0; w < kRoutePrepWarps; ++w) {
+      const int t = hist[w * E + e];
+      hist[w * E + e] = run;
+      run += t;
+    }
+    cnt[e] = run;
+  }
+  __syncthreads();
+
+  // pass 2b: exclusive scan over experts (E <= 1024 = one value per thread)
+  int v_pad = 0, v_til = 0;
+  if (tid < E) {
+    const int nt = (cnt[tid] + p.bm - 1) / p.bm;
+    v_til = nt;
+    v_pad = nt * p.bm;
+  }
+  const int own_pad = v_pad, own_til = v_til;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int a = __shfl_up_sync(full, v_pad, o);
+    const int b = __shfl_up_sync(full, v_til, o);
+    if (lane >= o) {
+      v_pad += a;
+      v_til += b;
+    }
+  }
+  if (lane == 31) {
+    wsum[warp] = v_pad;
+    wsum[32 + warp] = v_til;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    int a = wsum[lane], b = wsum[32 + lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int a2 = __shfl_up_sync(full, a, o);
+      const int b2 = __shfl_up_sync(full, b, o);
+      if (lane >= o) {
+        a += a2;
+        b += b2;
+      }
+    }
+    wsum[lane] = a;       // inclusive over warps
+    wsum[32 + lane] = b;
+  }
+  __syncthreads();
+  if (tid < E) {
+    const int pre_pad = (warp > 0 ? wsum[warp - 1] : 0) + v_pad - own_pad;
+    const int pre_til = (warp > 0 ? wsum[32 + warp - 1] : 0) + v_til - own_til;
+    poff[tid] = pre_pad;
+    toff[tid] = pre_til;
+    if (tid == E - 1) {
+      poff[E] = pre_pad + own_pad;
+      toff[E] = pre_til + own_til;
+    }
+  }
+  __syncthreads();
+
+  // pass 3: stable placement
+  for (int base = r_begin; base < r_end; base += 32) {
+    const int r = base + lane;
+    const int e = local_of(r);
+    const unsigned m = __match_any_sync(full, e);
+    if (e >= 0) {
+      const int slot = poff[e] + hist[warp * E + e] + __popc(m & lt_mask);
+      p.perm[slot] = r;
+      p.inv[r] = slot;
+    } else if (r < r_end) {
+      p.inv[r] = -1;
+    }
+    __syncwarp();
+    if (e >= 0 && (m & lt_mask) == 0) hist[warp * E + e] += __popc(m);
+    __syncwarp();
+  }
+
+  // padding slots, tile list, counts and offsets
+  for (int e = tid; e < E; e += kRoutePrepThreads) {
+    const int c = cnt[e];
+    for (int s = poff[e] + c; s < poff[e + 1]; ++s) p.perm[s] = -1;
+    const int nt = toff[e + 1] - toff[e];
+    for (int i = 0; i < nt; ++i) {
+      p.tiles[toff[e] + i] = make_int4(e, poff[e] + i * p.bm, min(p.bm, c - i * p.bm), 0);
+    }
+    p.counts[e] = c;
+    p.offs[e] = poff[e];
+  }
+  if (tid == 0) {
+    p.offs[E] = poff[E];
+    *p.num_tiles = toff[E];
+  }
+}
+
+cudaError_t launch_route_prep(const RoutePrepParams& p, int smem_bytes, cudaStream_t s, bool pdl) {
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(route_prep_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(1);
+  cfg.blockDim = dim3(kRoutePrepThreads);
+  cfg.dynamicSmemBytes = smem_bytes;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, route_prep_kernel, p);
+}
+
+}  // namespace w4a16
