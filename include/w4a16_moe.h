@@ -213,7 +213,8 @@ w4a16_status w4a16_moe_set_overrides(w4a16_moe_plan_t plan, int32_t tile_rows,
 
 /*
  * Reads (synchronously, on `stream`) and clears the device error flag in the
- * workspace.  Returns W4A16_ERR_DEVICE_TIMEOUT if a kernel gave up waiting.
+ * workspace.  Returns W4A16_ERR_DEVICE_TIMEOUT if a kernel gave up waiting
+ * since the last prepare_routes on this workspace (prepare_routes clears it).
  */
 w4a16_status w4a16_moe_check_device_error(w4a16_moe_plan_t plan, void* workspace, void* stream);
 

@@ -43,6 +43,7 @@ __global__ void __launch_bounds__(kRoutePrepThreads, 1) route_prep_kernel(const 
 
   for (int i = tid; i < kRoutePrepWarps * E; i += kRoutePrepThreads) hist[i] = 0;
   for (int i = tid; i < p.ctr_len; i += kRoutePrepThreads) p.counters[i] = 0;
+  if (tid == 0) *p.err = 0;  // the flag reports timeouts since this call
   __syncthreads();
 
   const int R = p.T * p.k;
@@ -60,11 +61,20 @@ __global__ void __launch_bounds__(kRoutePrepThreads, 1) route_prep_kernel(const 
     return (l >= 0 && l < E) ? static_cast<int>(l) : -1;
   };
 
-  // pass 1: per-warp histograms
-  for (int base = r_begin; base < r_end; base += 32) {
-    const int e = local_of(base + lane);
-    const unsigned m = __match_any_sync(full, e);
-    if (e >= 0 && (m & lt_mask) == 0) hist[warp * E + e] += __popc(m);
+  // pass 1: per-warp histograms (ids fetched kBatch rounds at a time so the
+  // global loads overlap instead of forming a latency chain)
+  constexpr int kBatch = 8;
+  for (int base = r_begin; base < r_end; base += 32 * kBatch) {
+    int eb[kBatch];
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i) eb[i] = local_of(base + 32 * i + lane);
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i) {
+      const int e = eb[i];
+      const unsigned m = __match_any_sync(full, e);
+      if (e >= 0 && (m & lt_mask) == 0) hist[warp * E + e] += __popc(m);
+      __syncwarp();
+    }
   }
   __syncthreads();
 
@@ -130,20 +140,26 @@ __global__ void __launch_bounds__(kRoutePrepThreads, 1) route_prep_kernel(const 
   __syncthreads();
 
   // pass 3: stable placement
-  for (int base = r_begin; base < r_end; base += 32) {
-    const int r = base + lane;
-    const int e = local_of(r);
-    const unsigned m = __match_any_sync(full, e);
-    if (e >= 0) {
-      const int slot = poff[e] + hist[warp * E + e] + __popc(m & lt_mask);
-      p.perm[slot] = r;
-      p.inv[r] = slot;
-    } else if (r < r_end) {
-      p.inv[r] = -1;
+  for (int base = r_begin; base < r_end; base += 32 * kBatch) {
+    int eb[kBatch];
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i) eb[i] = local_of(base + 32 * i + lane);
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i) {
+      const int r = base + 32 * i + lane;
+      const int e = eb[i];
+      const unsigned m = __match_any_sync(full, e);
+      if (e >= 0) {
+        const int slot = poff[e] + hist[warp * E + e] + __popc(m & lt_mask);
+        p.perm[slot] = r;
+        p.inv[r] = slot;
+      } else if (r < r_end) {
+        p.inv[r] = -1;
+      }
+      __syncwarp();
+      if (e >= 0 && (m & lt_mask) == 0) hist[warp * E + e] += __popc(m);
+      __syncwarp();
     }
-    __syncwarp();
-    if (e >= 0 && (m & lt_mask) == 0) hist[warp * E + e] += __popc(m);
-    __syncwarp();
   }
 
   // padding slots, tile list, counts and offsets
