@@ -240,6 +240,11 @@ def test_full_size_sampled_rows(name, tokens):
         out = moe(x, w, tw, ids)
         torch.cuda.synchronize()
         moe.check_device_error()
+        # repeat runs are bit-identical (also catches stale operand reads)
+        for _ in range(2):
+            again = moe(x, w, tw, ids)
+            torch.cuda.synchronize()
+            assert torch.equal(again.view(torch.int16), out.view(torch.int16)), f"{name} T={T} not deterministic"
         rng = np.random.default_rng(T)
         rows = sorted(set([0, T - 1] + rng.integers(0, T, size=min(T, 6)).tolist()))
         ref = oracle_rows(cfg, w, x, ids, tw, rows=rows, w_cpu=w_cpu)

@@ -74,24 +74,25 @@ int choose_bn(const w4a16_moe_plan_s& P, int T) {
   return std::min(kMaxBN, std::max(16, bn));
 }
 
-// Split-K factor minimising (waves of units) x (K blocks per unit + overhead)
-// for the expected number of route tiles.
+// Split-K factor for the expected number of route tiles: the cost model is
+// (waves of units) x (K blocks per unit + per-unit overhead); among factors
+// within 5% of the cheapest, the smallest wins (splits add partial traffic).
 int choose_splits(double tiles_est, int n_tiles, int kb, int num_sms, double overhead) {
-  int best = 1;
+  double cost[65] = {0};
   double best_cost = 1e300;
-  for (int s = 1; s <= std::min(kb, 64); ++s) {
+  const int smax = std::min(kb, 64);
+  for (int s = 1; s <= smax; ++s) {
     const int kbps = cdiv(kb, s);
-    const int s_eff = cdiv(kb, kbps);
-    if (s_eff != s) continue;
+    cost[s] = 1e300;
+    if (cdiv(kb, kbps) != s) continue;
     const double units = tiles_est * n_tiles * s;
     const double waves = std::ceil(units / num_sms);
-    const double cost = waves * (kbps + overhead);
-    if (cost < best_cost - 1e-9) {
-      best_cost = cost;
-      best = s;
-    }
+    cost[s] = waves * (kbps + overhead);
+    best_cost = std::min(best_cost, cost[s]);
   }
-  return best;
+  for (int s = 1; s <= smax; ++s)
+    if (cost[s] <= best_cost * 1.05) return s;
+  return 1;
 }
 
 Layout make_layout(const w4a16_moe_plan_s& P, int T) {
@@ -118,10 +119,12 @@ Layout make_layout(const w4a16_moe_plan_s& P, int T) {
   L.s2 = P.ov_s2 ? P.ov_s2 : choose_splits(tiles_est, L.nt2, L.kb2, P.num_sms, 1.0);
   L.kbps1 = cdiv(L.kb1, L.s1);
   L.kbps2 = cdiv(L.kb2, L.s2);
-  L.stage_bytes = kStageA + L.bn * 512 + kStageS;
-  const int smem_budget = 232448 - 2048;
+  L.stage_bytes = kStageA + L.bn * kStageBRow + kStageS;
+  // dynamic shared memory: 1 KB alignment slack + stages + 2 KB control block
+  // (mbarriers, TMEM address, flags, token list)
+  const int smem_budget = 232448 - 3072;
   L.stages = std::min(kMaxStages, smem_budget / L.stage_bytes);
-  L.smem = 2048 + L.stages * L.stage_bytes;
+  L.smem = 3072 + L.stages * L.stage_bytes;
   L.grid1 = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(P.num_sms, static_cast<int64_t>(L.tiles_cap) * L.nt1 * L.s1)));
   L.grid2 = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(P.num_sms, static_cast<int64_t>(L.tiles_cap) * L.nt2 * L.s2)));
 
@@ -177,16 +180,17 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // Packed INT4 weights as a 3D uint8 tensor [E][rows][inner bytes], 128-byte
 // swizzled boxes of 128 bytes x box_rows.
 bool encode_weights(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint64_t E,
-                    uint32_t box_rows) {
+                    uint32_t box_inner, uint32_t box_rows) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[3] = {inner, rows, E};
   cuuint64_t strides[2] = {inner, inner * rows};
-  cuuint32_t box[3] = {128, box_rows, 1};
+  cuuint32_t box[3] = {box_inner, box_rows, 1};
   cuuint32_t es[3] = {1, 1, 1};
+  const CUtensorMapSwizzle sw = box_inner == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B;
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+            CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // A row-major 16-bit matrix [rows][cols], boxes of 64 columns x box_rows, 128B swizzle.
@@ -272,11 +276,13 @@ w4a16_status launch_forward(const w4a16_moe_plan_s& P, const Layout& L, const vo
   CUtensorMap tmA1, tmA2, tmB2;
   bool ok;
   if (group) {
-    ok = encode_weights(&tmA1, w13, d.hidden / 2, L.n1, d.num_experts, 64) &&
-         encode_weights(&tmA2, w2, d.inter / 2, d.hidden, d.num_experts, 64);
+    // rows of packed bytes along K; boxes of 64 bytes (128 K values) x 64 rows
+    ok = encode_weights(&tmA1, w13, d.hidden / 2, L.n1, d.num_experts, kBlockK / 2, 64) &&
+         encode_weights(&tmA2, w2, d.inter / 2, d.hidden, d.num_experts, kBlockK / 2, 64);
   } else {
-    ok = encode_weights(&tmA1, w13, d.hidden, L.n1 / 2, d.num_experts, 32) &&
-         encode_weights(&tmA2, w2, d.inter, d.hidden / 2, d.num_experts, 32);
+    // row pairs of K bytes; boxes of 128 bytes (128 K values) x 32 row pairs
+    ok = encode_weights(&tmA1, w13, d.hidden, L.n1 / 2, d.num_experts, kBlockK, 32) &&
+         encode_weights(&tmA2, w2, d.inter, d.hidden / 2, d.num_experts, kBlockK, 32);
   }
   ok = ok && encode_rows16(&tmB2, ws + L.off_inter, d.inter, L.slots_cap, L.bn, d.act_dtype);
   if (!ok) return fail(W4A16_ERR_CUDA, "cuTensorMapEncodeTiled failed (driver entry point or arguments)");

@@ -16,15 +16,19 @@ namespace w4a16 {
 // Tiling constants
 // ---------------------------------------------------------------------------
 constexpr int kTileRows = 128;       // weight rows per MMA tile (MMA M)
-constexpr int kBlockK = 256;         // K elements per pipeline stage
+constexpr int kBlockK = 128;         // K elements per pipeline stage
 constexpr int kGroup = 32;           // group size of the group-wise scales
-constexpr int kMaxStages = 8;
+constexpr int kGroupsPerStage = kBlockK / kGroup;
+constexpr int kMaxStages = 12;
 constexpr int kGemmThreads = 512;    // 16 warps: see the role map in gemm.cuh
 constexpr int kTmemCols = 512;
 constexpr int kAbufCols = kBlockK / 2;  // one stage of BF16/FP16 A in TMEM columns
+constexpr int kNumAbuf = 4;             // A buffers: two per dequant warpgroup
+constexpr int kAccCol0 = kNumAbuf * kAbufCols;  // first accumulator column
 constexpr int kMaxBN = 128;
-constexpr int kStageA = kTileRows * kBlockK / 2;   // 16 KB packed INT4 per stage
-constexpr int kStageS = kTileRows * 16;             // 8 BF16 scales per row per stage
+constexpr int kStageA = kTileRows * kBlockK / 2;   // 8 KB packed INT4 per stage
+constexpr int kStageS = kTileRows * kGroupsPerStage * 2;  // BF16 scales per stage
+constexpr int kStageBRow = kBlockK * 2;            // bytes of one activation row per stage
 
 enum { ACT_SWIGLU = 0, ACT_RELU2 = 1 };
 enum { SCALE_GROUP = 0, SCALE_CHANNEL = 1 };
@@ -167,9 +171,8 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // Bounded wait: returns false when the CTA-wide abort flag is raised or the
 // wait has lasted kWaitTimeoutNs, after raising the abort flag and the global
 // error flag.  Every spin in the GEMM pipeline goes through here.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                          int32_t* err) {
-  if (mbar_try_wait(bar, parity)) return true;
+static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                            int32_t* err) {
   const uint64_t t0 = global_timer_ns();
   for (uint32_t n = 1;; ++n) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -182,6 +185,15 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
       }
     }
   }
+}
+
+// Fast path inline (one try_wait), the bounded spin out of line: the wait is
+// used at many sites and inlining the spin loop everywhere bloats the code
+// that all warp roles share in the instruction cache.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                          int32_t* err) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return mbar_wait_slow(bar, parity, abort_flag, err);
 }
 
 // ---------------------------------------------------------------------------
@@ -242,6 +254,24 @@ __device__ __forceinline__ void cp_async(void* dst, const void* src) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], %2;" ::"r"(smem_u32(dst)), "l"(src),
                "n"(BYTES)
                : "memory");
+}
+
+// 16-byte copy that bypasses L1; copies src_bytes (0 or 16) and zero-fills the rest.
+__device__ __forceinline__ void cp_async_cg16(void* dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src),
+               "r"(src_bytes)
+               : "memory");
+}
+
+// Arrive on `bar` once this thread's earlier cp.async copies have landed; the
+// barrier's expected count includes this arrival (no pending-count increment).
+__device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 // Arrive on `bar` once this thread's earlier cp.async copies have landed; the
@@ -317,23 +347,22 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
   return d;
 }
 
-// 32 lanes x 32 bit, repeated over N consecutive columns.
+// 32 lanes x 32 bit, repeated over N consecutive columns.  No "memory" clobber:
+// the stores only read registers; tcgen05.wait::st (which has one) orders them.
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
       "%11, %12, %13, %14, %15, %16};" ::"r"(taddr),
       "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
       "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
-      "r"(v[15])
-      : "memory");
+      "r"(v[15]));
 }
 
 __device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&v)[8]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(
           taddr),
-      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
-      : "memory");
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]));
 }
 
 __device__ __forceinline__ void tmem_wait_st() {

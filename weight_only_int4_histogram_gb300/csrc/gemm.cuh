@@ -10,8 +10,10 @@
 // warpgroups as in "perf: reduce split W4A16 routing and output overhead"
 // (FlashInfer), section Description.  Blackwell design (not the pages'):
 //
-//   weights (A, M = 128 rows)  TMA (128B swizzle) -> SMEM packed INT4
+//   weights (A, M = 128 rows)  TMA (64B / 128B swizzle) -> SMEM packed INT4
 //                              -> dequant warps -> BF16/FP16 A operand in TMEM
+//                                 (four A buffers: each warpgroup alternates two,
+//                                 so dequantisation overlaps the MMAs)
 //   activations (B, N = bn)    gate/up: cp.async row gather by slot -> token
 //                              down:    TMA tile of the intermediate
 //                              -> SMEM (128B-swizzled, K-major)
@@ -24,7 +26,8 @@
 //   warp 1       TMEM allocation + single-thread MMA issuer
 //   warps 2, 3   gate/up GEMM: activation-row gather (cp.async, 16 B per lane)
 //   warps 4..11  two dequant warpgroups; warpgroup g handles pipeline stages
-//                with (stage counter & 1) == g and owns TMEM A buffer g
+//                with (stage counter & 1) == g, writing TMEM A buffer
+//                (stage counter & 3)
 //   warps 12..15 epilogue (TMEM -> registers -> activation / scaling -> HBM)
 //
 // Work is a persistent loop over units (route tile, weight tile, K split);
@@ -100,6 +103,13 @@ __device__ __forceinline__ Unit decode_unit(const GemmParams& p, int u) {
   return w;
 }
 
+// Route-tile record of unit u.  Every unit index below the grid-size bound maps
+// to a tile index below the tile-list capacity, so this may be issued before the
+// tile count is known (speculatively, to overlap its latency).
+__device__ __forceinline__ int4 load_tile(const GemmParams& p, int u) {
+  return p.tiles[u / (p.splits * p.n_tiles)];
+}
+
 // Row (within the expert) of the weight rows held in tile rows 0..63 / 64..127.
 template <int WHICH>
 __device__ __forceinline__ void tile_row_bases(const GemmParams& p, int nt, int& r0, int& r1) {
@@ -125,26 +135,30 @@ __device__ __forceinline__ int tile_row_of_lane(const GemmParams& p, int l) {
   return l;
 }
 
-// Dequantise one stage (kBlockK = 256 K values) of this thread's weight row
-// into TMEM columns [a_col, a_col + 128) of its lane.
-//   group scales: packed along K, 128 rows x 128 B (one 16 B chunk = one group
-//   of 32), scales 8 per row per stage; the A operand is q * s rounded once.
-//   per-channel: packed along rows, 4 boxes (K half, row block) of 32 row pairs
-//   x 128 B; the A operand is the exact code q (the scale is applied to the FP32
-//   accumulator in the epilogue).
+// Dequantise one stage (kBlockK = 128 K values) of this thread's weight row
+// into TMEM columns [a_col, a_col + 64) of its lane.
+//   group scales: packed along K, 128 rows x 64 B with the 64-byte swizzle (one
+//   16 B chunk = one group of 32), 4 scales per row per stage; the A operand is
+//   q * s rounded once to the 16-bit type.
+//   per-channel: packed along rows, 2 boxes (row block) of 32 row pairs x 128 B
+//   with the 128-byte swizzle; the A operand is the exact code q (the scale is
+//   applied to the FP32 accumulator in the epilogue).
 template <int SCALE, int DT>
 __device__ __forceinline__ void dequant_stage(const uint8_t* sA, const uint8_t* sS, int tr,
                                               uint32_t a_taddr) {
   using T = F16<DT>;
   const uint32_t kMask = 0x000F000Fu;
   if (SCALE == SCALE_GROUP) {
-    const uint4 sc = *reinterpret_cast<const uint4*>(sS + tr * 16);
-    const uint32_t sw[4] = {sc.x, sc.y, sc.z, sc.w};
-    const uint8_t* row = sA + tr * 128;
-#pragma unroll
-    for (int g = 0; g < 8; ++g) {
-      const uint4 w = *reinterpret_cast<const uint4*>(row + ((g ^ (tr & 7)) << 4));
-      const uint16_t s16 = T::from_bf16(static_cast<uint16_t>(sw[g >> 1] >> ((g & 1) * 16)));
+    const uint2 sc = *reinterpret_cast<const uint2*>(sS + tr * 8);
+    const uint8_t* row = sA + tr * 64;
+    const int sw = (tr >> 1) & 3;
+    // Compact loop (not unrolled): the body stays small in the instruction
+    // cache, which the other warp roles of the CTA share.
+#pragma unroll 1
+    for (int g = 0; g < kGroupsPerStage; ++g) {
+      const uint4 w = *reinterpret_cast<const uint4*>(row + ((g ^ sw) << 4));
+      const uint32_t sword = (g < 2) ? sc.x : sc.y;
+      const uint16_t s16 = T::from_bf16(static_cast<uint16_t>(sword >> ((g & 1) * 16)));
       const uint32_t s2 = static_cast<uint32_t>(s16) * 0x00010001u;
       const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
       uint32_t out[16];
@@ -169,23 +183,20 @@ __device__ __forceinline__ void dequant_stage(const uint8_t* sA, const uint8_t* 
     const int lr = tr & 63;
     const int pr = lr >> 1;
     const int shift = (lr & 1) * 4;
+    const uint8_t* row = sA + b * 4096 + pr * 128;
+#pragma unroll 1
+    for (int c = 0; c < 8; ++c) {
+      const uint4 w = *reinterpret_cast<const uint4*>(row + ((c ^ (pr & 7)) << 4));
+      const uint32_t ws[4] = {w.x >> shift, w.y >> shift, w.z >> shift, w.w >> shift};
+      uint32_t out[8];
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const uint8_t* row = sA + (h * 2 + b) * 4096 + pr * 128;
-#pragma unroll 2
-      for (int c = 0; c < 8; ++c) {
-        const uint4 w = *reinterpret_cast<const uint4*>(row + ((c ^ (pr & 7)) << 4));
-        const uint32_t ws[4] = {w.x >> shift, w.y >> shift, w.z >> shift, w.w >> shift};
-        uint32_t out[8];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const uint32_t p0 = __byte_perm(ws[i], 0, 0x0100);
-          const uint32_t p1 = __byte_perm(ws[i], 0, 0x0302);
-          out[2 * i + 0] = T::sub(lop3_and_xor(p0, kMask, T::kMagic), T::kMagic);
-          out[2 * i + 1] = T::sub(lop3_and_xor(p1, kMask, T::kMagic), T::kMagic);
-        }
-        tmem_st8(a_taddr + h * 64 + c * 8, out);
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t p0 = __byte_perm(ws[i], 0, 0x0100);
+        const uint32_t p1 = __byte_perm(ws[i], 0, 0x0302);
+        out[2 * i + 0] = T::sub(lop3_and_xor(p0, kMask, T::kMagic), T::kMagic);
+        out[2 * i + 1] = T::sub(lop3_and_xor(p1, kMask, T::kMagic), T::kMagic);
       }
+      tmem_st8(a_taddr + c * 8, out);
     }
   }
 }
@@ -198,17 +209,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                       const __grid_constant__ CUtensorMap tmB) {
   using T = F16<DT>;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~static_cast<uintptr_t>(1023));
+  // 1024-byte aligned base, derived by pointer arithmetic on the shared array so
+  // the compiler keeps the shared address space (LDS/STS, not generic loads).
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const int stages = p.stages;
   const int bn = p.bn;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + stages * p.stage_bytes);
   uint64_t* empty = full + kMaxStages;
   uint64_t* afull = empty + kMaxStages;
-  uint64_t* aempty = afull + 2;
-  uint64_t* accfull = aempty + 2;
+  uint64_t* aempty = afull + kNumAbuf;
+  uint64_t* accfull = aempty + kNumAbuf;
   uint64_t* accempty = accfull + 2;
-  uint64_t* drain = accempty + 2;
+  uint64_t* gbar = accempty + 2;             // [kMaxStages] gather-copy completion
+  uint64_t* drain = gbar + kMaxStages;
   uint64_t* epibar = drain + 1;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(epibar + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
@@ -221,15 +234,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < stages; ++s) {
-      mbar_init(&full[s], gather_b ? 3 : 1);   // producer (+ two gather warps)
+      mbar_init(&full[s], 1);                  // producer (TMA bytes + scale copies)
       mbar_init(&empty[s], 5);                 // 4 dequant warps + MMA commit
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < kNumAbuf; ++b) {
       mbar_init(&afull[b], 4);
       mbar_init(&aempty[b], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
       mbar_init(&accfull[b], 1);
       mbar_init(&accempty[b], 4);
     }
+    for (int s = 0; s < kMaxStages; ++s) mbar_init(&gbar[s], 64);  // gather lanes
     mbar_init(drain, 1);
     mbar_init(epibar, 4);
     *abort_flag = 0;
@@ -253,6 +269,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   pdl_wait();
   pdl_launch_dependents();
 
+  // The first unit's tile record is fetched together with the tile count.
+  const int4 first_ti = load_tile(p, blockIdx.x);
   const int n_units = (*p.num_tiles) * p.n_tiles * p.splits;
   const int N1 = p.n_rows;
 
@@ -264,13 +282,30 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int sbytes_row = groups_row * 2;
     uint32_t it = 0;
     bool ok = true;
+    int4 ti_next = first_ti;
     for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
       const Unit w = decode_unit(p, u);
+      const int4 ti = ti_next;
+      if (u + (int)gridDim.x < n_units) ti_next = load_tile(p, u + gridDim.x);  // prefetch
       if (w.kb1 <= w.kb0) continue;
-      const int4 ti = p.tiles[w.tile];
       const int e = ti.x, m0 = ti.y;
       int r0, r1;
       tile_row_bases<WHICH>(p, w.nt, r0, r1);
+      // scale rows of this unit for this lane's tile rows (lane + 32 i); null
+      // when the row lies beyond the expert's rows
+      const uint8_t* srow[4];
+      bool srow_al8 = true;
+      if (SCALE == SCALE_GROUP) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int tr = lane + 32 * i;
+          const int grow = tr < 64 ? r0 + tr : r1 + (tr - 64);
+          srow[i] = grow < N1 ? reinterpret_cast<const uint8_t*>(p.scales) +
+                                    (static_cast<int64_t>(e) * N1 + grow) * sbytes_row
+                              : nullptr;
+          srow_al8 = srow_al8 && ((reinterpret_cast<uintptr_t>(srow[i]) & 7) == 0);
+        }
+      }
       for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
         const int st = it % stages;
         if (!mbar_wait(&empty[st], ((it / stages) & 1) ^ 1, abort_flag, p.err)) {
@@ -279,54 +314,46 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
         uint8_t* sA = smem + st * p.stage_bytes;
         uint8_t* sB = sA + kStageA;
-        uint8_t* sS = sB + bn * 512;
+        uint8_t* sS = sB + bn * kStageBRow;
         if (SCALE == SCALE_GROUP) {
-          // 8 scales (16 B) per tile row; lane handles rows lane + 32 i.
-          const int g0 = kb * 8;
-          const int ng = min(8, groups_row - g0);
+          // kGroupsPerStage scales (8 B) per tile row; lane handles rows lane + 32 i.
+          const int g0 = kb * kGroupsPerStage;
+          const int ng = min(kGroupsPerStage, groups_row - g0);
+          if (srow_al8 && ng == kGroupsPerStage) {
+            // common case: one 8-byte copy per row
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int tr = lane + 32 * i;
-            const int grow = tr < 64 ? r0 + tr : r1 + (tr - 64);
-            uint8_t* dst = sS + tr * 16;
-            if (grow < N1 && ng > 0) {
-              const uint8_t* src = reinterpret_cast<const uint8_t*>(p.scales) +
-                                   (static_cast<int64_t>(e) * N1 + grow) * sbytes_row + g0 * 2;
-              const int nbytes = ng * 2;
-              const uint32_t a = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(src));
-              if ((a & 15) == 0 && nbytes == 16) {
-                cp_async<16>(dst, src);
-              } else if ((a & 7) == 0 && (nbytes & 7) == 0) {
-                for (int o = 0; o < nbytes; o += 8) cp_async<8>(dst + o, src + o);
-              } else {
-                for (int o = 0; o < nbytes; o += 4) cp_async<4>(dst + o, src + o);
-              }
-              for (int o = nbytes; o < 16; o += 4) *reinterpret_cast<uint32_t*>(dst + o) = 0u;
-            } else {
-              *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
+            for (int i = 0; i < 4; ++i) {
+              uint8_t* dst = sS + (lane + 32 * i) * 8;
+              if (srow[i]) cp_async<8>(dst, srow[i] + g0 * 2);
+              else *reinterpret_cast<uint2*>(dst) = make_uint2(0, 0);
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              uint8_t* dst = sS + (lane + 32 * i) * 8;
+              const int nbytes = srow[i] ? max(ng, 0) * 2 : 0;
+              for (int o = 0; o < nbytes; o += 4) cp_async<4>(dst + o, srow[i] + g0 * 2 + o);
+              for (int o = nbytes; o < 8; o += 4) *reinterpret_cast<uint32_t*>(dst + o) = 0u;
             }
           }
           cp_async_mbar_arrive(&full[st]);
         }
         __syncwarp();
         if (lane == 0) {
-          mbar_arrive_expect_tx(&full[st], kStageA + (gather_b ? 0 : bn * 512));
+          mbar_arrive_expect_tx(&full[st], kStageA + (gather_b ? 0 : bn * kStageBRow));
           if (SCALE == SCALE_GROUP) {
-            tma_load_3d(sA, &tmA, &full[st], kb * 128, r0, e, pol_w);
-            tma_load_3d(sA + 8192, &tmA, &full[st], kb * 128, r1, e, pol_w);
+            // two 64-row boxes of 64 packed bytes (128 K values), 64-byte swizzle
+            tma_load_3d(sA, &tmA, &full[st], kb * (kBlockK / 2), r0, e, pol_w);
+            tma_load_3d(sA + 4096, &tmA, &full[st], kb * (kBlockK / 2), r1, e, pol_w);
           } else {
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              tma_load_3d(sA + (h * 2 + 0) * 4096, &tmA, &full[st], kb * 256 + h * 128, r0 / 2, e,
-                          pol_w);
-              tma_load_3d(sA + (h * 2 + 1) * 4096, &tmA, &full[st], kb * 256 + h * 128, r1 / 2, e,
-                          pol_w);
-            }
+            // two boxes of 32 row pairs x 128 K bytes, 128-byte swizzle
+            tma_load_3d(sA, &tmA, &full[st], kb * kBlockK, r0 / 2, e, pol_w);
+            tma_load_3d(sA + 4096, &tmA, &full[st], kb * kBlockK, r1 / 2, e, pol_w);
           }
           if (!gather_b) {
 #pragma unroll
-            for (int a = 0; a < 4; ++a)
-              tma_load_2d(sB + a * bn * 128, &tmB, &full[st], kb * 256 + a * 64, m0, pol_b);
+            for (int a = 0; a < kBlockK / 64; ++a)
+              tma_load_2d(sB + a * bn * 128, &tmB, &full[st], kb * kBlockK + a * 64, m0, pol_b);
           }
         }
         __syncwarp();
@@ -342,6 +369,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // ------------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       const uint32_t idesc = make_idesc_f16(DT == DT_BF16, kTileRows, bn);
+      const uint64_t bdesc_base = smem_desc_sw128(smem_u32(smem + kStageA));
+      const uint64_t atom_step = static_cast<uint64_t>(bn) * 128 / 16;
       uint32_t it = 0, jc = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
@@ -353,24 +382,32 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           break;
         }
         tc_fence_after();
-        const uint32_t d_tmem = tmem + 2 * kAbufCols + b * bn;
+        const uint32_t d_tmem = tmem + kAccCol0 + b * bn;
         for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
           const int st = it % stages;
-          const int g = it & 1;
-          if (!mbar_wait(&full[st], (it / stages) & 1, abort_flag, p.err) ||
-              !mbar_wait(&afull[g], (it >> 1) & 1, abort_flag, p.err)) {
+          const int ab = it % kNumAbuf;
+          // B: TMA bytes (down GEMM, on `full`) or gathered rows (gate/up, on
+          // `gbar`, written through the generic proxy: fence before the MMA).
+          if (!mbar_wait(gather_b ? &gbar[st] : &full[st], (it / stages) & 1, abort_flag, p.err) ||
+              !mbar_wait(&afull[ab], (it / kNumAbuf) & 1, abort_flag, p.err)) {
             ok = false;
             break;
           }
+          if (gather_b) fence_proxy_async_smem();
           tc_fence_after();
-          const uint32_t sB = smem_u32(smem + st * p.stage_bytes + kStageA);
+          // B descriptors of this stage: the start-address field (bits 0-13,
+          // address >> 4) advances by 2 per 32-byte K step inside a 128-byte
+          // swizzle atom and by bn * 8 per atom; adding to the 64-bit value
+          // never carries out of the field (shared addresses are < 256 KB).
+          const uint64_t d0 = bdesc_base + static_cast<uint64_t>(st) * (p.stage_bytes >> 4);
+          const uint32_t a0 = tmem + ab * kAbufCols;
+          const uint32_t acc0 = kb > w.kb0 ? 1u : 0u;
 #pragma unroll
           for (int kk = 0; kk < kBlockK / 16; ++kk) {
-            const uint64_t bdesc = smem_desc_sw128(sB + (kk >> 2) * bn * 128 + (kk & 3) * 32);
-            mma_ts(d_tmem, tmem + g * kAbufCols + kk * 8, bdesc, idesc,
-                   (kb > w.kb0 || kk > 0) ? 1u : 0u);
+            mma_ts(d_tmem, a0 + kk * 8, d0 + (kk >> 2) * atom_step + (kk & 3) * 2, idesc,
+                   kk > 0 ? 1u : acc0);
           }
-          mma_commit(&aempty[g]);
+          mma_commit(&aempty[ab]);
           mma_commit(&empty[st]);
         }
         if (!ok) break;
@@ -384,24 +421,55 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
   } else if (warp == 2 || warp == 3) {
     // ------------------------------------------------------------------ activation gather
+    // Each warp copies half of the route tile's rows (16 B per lane, two rows
+    // per instruction) straight from x by token, with cp.async (out-of-range K
+    // columns are zero-filled by the copy itself).  Completion is signalled on
+    // gbar[stage] without blocking the warp; the MMA thread, the only reader of
+    // these rows, waits on gbar and issues the generic->async proxy fence.
     if (gather_b) {
       const int gw = warp - 2;
       const int rows_per = bn / 2;
       const uint16_t* x = reinterpret_cast<const uint16_t*>(p.x);
-      const int atom = lane >> 3, ch = lane & 7;
+      const int c = lane & 15, atom = c >> 3, ch = c & 7, rsub = lane >> 4;
       uint32_t it = 0;
-      int pending = -1;
       bool ok = true;
+      // perm entries of this warp's rows (lane, lane + 32), one unit ahead
+      auto load_perm = [&](int m0, int r) -> int {
+        return r < rows_per ? p.perm[m0 + gw * rows_per + r] : -1;
+      };
+      int4 ti_next = first_ti;
+      int pa_next = -1, pb_next = -1;
+      if (blockIdx.x < n_units) {
+        pa_next = load_perm(ti_next.y, lane);
+        pb_next = load_perm(ti_next.y, lane + 32);
+      }
       for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
         const Unit w = decode_unit(p, u);
-        if (w.kb1 <= w.kb0) continue;
-        const int m0 = p.tiles[w.tile].y;
-        __syncwarp();
-        for (int r = lane; r < rows_per; r += 32) {
-          const int route = p.perm[m0 + gw * rows_per + r];
-          tok_s[gw * (kMaxBN / 2) + r] = route >= 0 ? route / p.top_k : 0;
+        const int pa = pa_next, pb = pb_next;
+        if (u + (int)gridDim.x < n_units) {
+          ti_next = load_tile(p, u + gridDim.x);
+          pa_next = load_perm(ti_next.y, lane);
+          pb_next = load_perm(ti_next.y, lane + 32);
         }
+        if (w.kb1 <= w.kb0) continue;
         __syncwarp();
+        if (lane < rows_per) tok_s[gw * (kMaxBN / 2) + lane] = pa >= 0 ? pa / p.top_k : 0;
+        if (lane + 32 < rows_per) tok_s[gw * (kMaxBN / 2) + lane + 32] = pb >= 0 ? pb / p.top_k : 0;
+        __syncwarp();
+        // This lane's rows are r_j = gw * rows_per + 2 j + rsub; their source rows
+        // (first kRowsReg in registers, the rest re-read from tok_s) and their
+        // swizzled destination offsets inside a stage.
+        constexpr int kRowsReg = 8;
+        const uint16_t* src_j[kRowsReg];
+        uint32_t dst_j[kRowsReg];
+#pragma unroll
+        for (int j = 0; j < kRowsReg; ++j) {
+          const int rr = 2 * j + rsub;
+          const int r = gw * rows_per + rr;
+          const int tok = rr < rows_per ? tok_s[gw * (kMaxBN / 2) + rr] : 0;
+          src_j[j] = x + static_cast<int64_t>(tok) * p.K;
+          dst_j[j] = atom * bn * 128 + r * 128 + ((ch ^ (r & 7)) << 4);
+        }
         for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
           const int st = it % stages;
           if (!mbar_wait(&empty[st], ((it / stages) & 1) ^ 1, abort_flag, p.err)) {
@@ -409,32 +477,22 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             break;
           }
           uint8_t* sB = smem + st * p.stage_bytes + kStageA;
-          const int col = kb * kBlockK + lane * 8;
-          const bool valid = col < p.K;
-          for (int rr = 0; rr < rows_per; ++rr) {
-            const int r = gw * rows_per + rr;
-            uint8_t* dst = sB + atom * bn * 128 + r * 128 + ((ch ^ (r & 7)) << 4);
-            if (valid) {
-              const int tok = tok_s[gw * (kMaxBN / 2) + rr];
-              cp_async<16>(dst, x + static_cast<int64_t>(tok) * p.K + col);
-            } else {
-              *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
-            }
+          const int col = kb * kBlockK + c * 8;
+          const uint32_t nbytes = col < p.K ? 16u : 0u;
+          const int colc = col < p.K ? col : 0;
+#pragma unroll
+          for (int j = 0; j < kRowsReg; ++j)
+            if (2 * j < rows_per) cp_async_cg16(sB + dst_j[j], src_j[j] + colc, nbytes);
+          for (int rr = 2 * kRowsReg; rr < rows_per; rr += 2) {
+            const int r = gw * rows_per + rr + rsub;
+            const int tok = tok_s[gw * (kMaxBN / 2) + rr + rsub];
+            cp_async_cg16(sB + atom * bn * 128 + r * 128 + ((ch ^ (r & 7)) << 4),
+                          x + static_cast<int64_t>(tok) * p.K + colc, nbytes);
           }
-          asm volatile("cp.async.commit_group;" ::: "memory");
-          if (pending >= 0) {
-            asm volatile("cp.async.wait_group 1;" ::: "memory");
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&full[pending]);
-          }
-          pending = st;
+          cp_async_mbar_arrive_noinc(&gbar[st]);
         }
       }
-      asm volatile("cp.async.wait_group 0;" ::: "memory");
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      __syncwarp();
-      if (pending >= 0 && lane == 0) mbar_arrive(&full[pending]);
+      asm volatile("cp.async.wait_all;" ::: "memory");
     }
   } else if (warp < 12) {
     // ------------------------------------------------------------------ dequant warpgroups
@@ -450,21 +508,22 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
         if ((it & 1) != static_cast<uint32_t>(wg)) continue;
         const int st = it % stages;
+        const int ab = it % kNumAbuf;
         if (!mbar_wait(&full[st], (it / stages) & 1, abort_flag, p.err) ||
-            !mbar_wait(&aempty[wg], ((it >> 1) & 1) ^ 1, abort_flag, p.err)) {
+            !mbar_wait(&aempty[ab], ((it / kNumAbuf) & 1) ^ 1, abort_flag, p.err)) {
           ok = false;
           break;
         }
         tc_fence_after();
         const uint8_t* sA = smem + st * p.stage_bytes;
-        const uint8_t* sS = sA + kStageA + bn * 512;
-        dequant_stage<SCALE, DT>(sA, sS, tr, t_lane + wg * kAbufCols);
+        const uint8_t* sS = sA + kStageA + bn * kStageBRow;
+        dequant_stage<SCALE, DT>(sA, sS, tr, t_lane + ab * kAbufCols);
         tmem_wait_st();
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[st]);
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&afull[wg]);
+        if (lane == 0) mbar_arrive(&afull[ab]);
       }
     }
   } else {
@@ -484,10 +543,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       ++eph;
       return r;
     };
+    int4 ti_next = first_ti;
     for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
       const Unit w = decode_unit(p, u);
       const bool has_k = w.kb1 > w.kb0;
-      const int4 ti = p.tiles[w.tile];
+      const int4 ti = ti_next;
+      if (u + (int)gridDim.x < n_units) ti_next = load_tile(p, u + gridDim.x);  // prefetch
       const int e = ti.x, m0 = ti.y, rows = ti.z;
       int r0, r1;
       tile_row_bases<WHICH>(p, w.nt, r0, r1);
@@ -504,7 +565,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
         tc_fence_after();
       }
-      const uint32_t acc_col = 2 * kAbufCols + b * bn;
+      const uint32_t acc_col = kAccCol0 + b * bn;
       // intermediate column of this lane (SwiGLU: gate/up pair index)
       const int icol = swiglu ? 64 * w.nt + 16 * q + (lane & 15) : grow;
       for (int c0 = 0; c0 < bn; c0 += 16) {
