@@ -229,6 +229,35 @@ w4a16_status w4a16_moe_check_device_error(w4a16_moe_plan_t plan, void* workspace
  */
 w4a16_status w4a16_moe_set_stage_events(w4a16_moe_plan_t plan, void* const* events, int32_t n);
 
+/*
+ * w4a16_moe_forward_static_workspace -- prepare_routes + forward without any
+ * caller-provided workspace and without allocating anything.
+ * No counterpart on the pages: this is a library convenience for callers that
+ * cannot allocate device memory themselves -- for instance code that runs
+ * inside a CUDA graph capture (where cudaMalloc is not allowed), applications
+ * whose memory is reserved up front by a pool that libraries may not bypass,
+ * or plug-in hosts that give a library no allocator.
+ *   The scratch lives in one file-scope device array of
+ *   W4A16_STATIC_WORKSPACE_BYTES (32 MiB), which every GPU that loads this
+ *   library holds until the process exits.  Batches whose layout needs more
+ *   return W4A16_ERR_WORKSPACE_TOO_SMALL before any launch (the regular entry
+ *   points report the need as workspace_bytes / w4a16_route_info).
+ *   The first call on a device (with that device current) looks up the
+ *   array's device address; make that first call before any stream capture.
+ *   Every call shares the one array and leaves its contents behind (route
+ *   preparation clears what must start at zero), so calls that overlap on the
+ *   GPU -- on different streams without ordering -- race and must be avoided.
+ *   No cudaMalloc, cudaFree or allocating library routine is called.
+ * Arguments as for w4a16_moe_forward (device pointers, same layouts).
+ */
+#define W4A16_STATIC_WORKSPACE_BYTES (32u * 1024u * 1024u)
+w4a16_status w4a16_moe_forward_static_workspace(w4a16_moe_plan_t plan, int32_t num_tokens,
+                                                const void* x, const uint8_t* w13,
+                                                const uint16_t* s13, const uint8_t* w2,
+                                                const uint16_t* s2, const float* topk_weights,
+                                                const int32_t* topk_ids, int32_t renormalize,
+                                                void* out, void* stream);
+
 /* Message for the last non-OK status on this host thread ("" if none). */
 const char* w4a16_moe_last_error(void);
 

@@ -28,6 +28,7 @@ EXPORTED = (
     "w4a16_moe_set_overrides",
     "w4a16_moe_check_device_error",
     "w4a16_moe_set_stage_events",
+    "w4a16_moe_forward_static_workspace",
     "w4a16_moe_last_error",
 )
 
@@ -91,6 +92,8 @@ def load(path: str = LIB_PATH):
     L.w4a16_moe_check_device_error.restype = st
     L.w4a16_moe_set_stage_events.argtypes = [P, ctypes.POINTER(P), i32]
     L.w4a16_moe_set_stage_events.restype = st
+    L.w4a16_moe_forward_static_workspace.argtypes = [P, i32, P, P, P, P, P, P, P, i32, P, P]
+    L.w4a16_moe_forward_static_workspace.restype = st
     L.w4a16_moe_last_error.argtypes = []
     L.w4a16_moe_last_error.restype = ctypes.c_char_p
     _lib = L
@@ -151,3 +154,13 @@ def w4a16_moe_set_stage_events(plan, event_handles):
     n = len(event_handles)
     arr = (ctypes.c_void_p * max(n, 1))(*event_handles)
     check(load().w4a16_moe_set_stage_events(plan, arr if n else None, n))
+
+
+STATIC_WORKSPACE_BYTES = 32 * 1024 * 1024
+
+
+def w4a16_moe_forward_static_workspace(plan, num_tokens, x, w13, s13, w2, s2, topk_weights, topk_ids,
+                                       renormalize, out, stream):
+    """prepare_routes + forward on the library's fixed device workspace (no allocation)."""
+    check(load().w4a16_moe_forward_static_workspace(plan, num_tokens, x, w13, s13, w2, s2, topk_weights,
+                                                    topk_ids, int(renormalize), out, stream))

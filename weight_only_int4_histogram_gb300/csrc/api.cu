@@ -12,6 +12,7 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <mutex>
 #include <string>
 
 #include "common.cuh"
@@ -550,5 +551,63 @@ w4a16_status w4a16_moe_set_stage_events(w4a16_moe_plan_t plan, void* const* even
 }
 
 const char* w4a16_moe_last_error(void) { return g_err.c_str(); }
+
+}  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Fixed-size workspace for callers that cannot allocate (see the header).
+// ---------------------------------------------------------------------------
+namespace {
+
+static __device__ __align__(256) uint8_t g_static_workspace[W4A16_STATIC_WORKSPACE_BYTES];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_static_ws_mutex;
+void* g_static_ws_ptr[kMaxDevices] = {nullptr};
+
+// Device address of g_static_workspace on the current device (looked up once per
+// device; the name is only a host-side stand-in for the device storage).
+w4a16_status static_workspace_ptr(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(W4A16_ERR_UNSUPPORTED, "device index %d too large", dev);
+  std::lock_guard<std::mutex> lock(g_static_ws_mutex);
+  if (!g_static_ws_ptr[dev]) {
+    void* ptr = nullptr;
+    e = cudaGetSymbolAddress(&ptr, g_static_workspace);
+    if (e != cudaSuccess || !ptr) return cuda_fail(e, "cudaGetSymbolAddress(static workspace)");
+    g_static_ws_ptr[dev] = ptr;
+  }
+  *out = g_static_ws_ptr[dev];
+  return W4A16_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+w4a16_status w4a16_moe_forward_static_workspace(w4a16_moe_plan_t plan, int32_t num_tokens, const void* x,
+                                                const uint8_t* w13, const uint16_t* s13, const uint8_t* w2,
+                                                const uint16_t* s2, const float* topk_weights,
+                                                const int32_t* topk_ids, int32_t renormalize, void* out,
+                                                void* stream) {
+  if (!plan) return fail(W4A16_ERR_INVALID_ARG, "plan is NULL");
+  if (num_tokens < 0 || num_tokens > plan->d.max_tokens)
+    return fail(W4A16_ERR_INVALID_ARG, "num_tokens %d outside [0, %d]", num_tokens, plan->d.max_tokens);
+  if (num_tokens == 0) return W4A16_OK;
+  const size_t need = make_layout(*plan, num_tokens).total;
+  if (need > W4A16_STATIC_WORKSPACE_BYTES)
+    return fail(W4A16_ERR_WORKSPACE_TOO_SMALL,
+                "batch of %d tokens needs %zu bytes of workspace; the static workspace holds %u",
+                num_tokens, need, W4A16_STATIC_WORKSPACE_BYTES);
+  void* ws = nullptr;
+  w4a16_status st = static_workspace_ptr(&ws);
+  if (st != W4A16_OK) return st;
+  st = w4a16_moe_prepare_routes(plan, num_tokens, topk_ids, ws, stream);
+  if (st != W4A16_OK) return st;
+  return w4a16_moe_forward(plan, num_tokens, x, w13, s13, w2, s2, topk_weights, topk_ids, renormalize, out,
+                           ws, stream);
+}
 
 }  // extern "C"
