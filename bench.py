@@ -31,6 +31,8 @@ from workloads import gen  # noqa: E402
 
 HEADLINE_TOKENS = 2048
 SWEEP_TOKENS = (1, 8, 32, 256, 1024)
+GEMM_PATHS = {"auto": 0, "tc": 1, "cc": 2}
+PATH_NAMES = {1: "tensor_cores", 2: "cuda_cores"}
 # Pages' number for this exact workload and metric (CuTe W4A16, one H200, T=2048,
 # LMDeploy PR page, Benchmark table): context from another machine.
 PAGE_LATENCY_US = {2048: 1280.327, 1024: 844.461, 256: 604.272, 32: 269.418, 8: 91.890, 1: 22.690}
@@ -220,7 +222,9 @@ def run_gpu(args):
     hbm, bf16, peak_kind = load_peaks()
 
     w = gen.make_weights(cfg, dev)
-    moe = W4A16MoE.from_config(cfg, max_tokens=max(max(cfg.tokens), args.tokens), device=dev)
+    moe = W4A16MoE.from_config(cfg, max_tokens=max(max(cfg.tokens), args.tokens, max(args.sweep_tokens)),
+                               device=dev)
+    moe.set_gemm_path(GEMM_PATHS[args.gemm_path])
     flush = l2_flush_buffer(dev)
     stream = torch.cuda.Stream(device=dev)
 
@@ -248,7 +252,8 @@ def run_gpu(args):
         res = dict(tokens=T, us=round(med, 3), us_min=round(min(times), 3),
                    gbs=round(nbytes / med / 1e3, 1), alg_bytes=nbytes, alg_flops=flops,
                    roofline_us=round(t_roof, 3), roofline_frac=round(t_roof / med, 4),
-                   bound="hbm" if nbytes / (hbm * 1e9) >= flops / (bf16 * 1e12) else "tensor")
+                   bound="hbm" if nbytes / (hbm * 1e9) >= flops / (bf16 * 1e12) else "tensor",
+                   gemm_path=PATH_NAMES[moe.route_info(T).gemm_path])
         return res, (x, ids, tw, out, g), times, clocks
 
     head, (x, ids, tw, out, g), times, clocks = measure(args.tokens, args.steps, args.warmup, True)
@@ -267,7 +272,7 @@ def run_gpu(args):
 
     sweep = []
     if not args.no_sweep:
-        for T in SWEEP_TOKENS:
+        for T in args.sweep_tokens:
             if T == args.tokens:
                 continue
             r, *_ = measure(T, max(10, args.steps // 2), args.warmup)
@@ -411,10 +416,15 @@ def main():
     ap.add_argument("--config", default=gen.KIMI.name, choices=list(gen.CONFIGS))
     ap.add_argument("--tokens", type=int, default=HEADLINE_TOKENS)
     ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--sweep", default=",".join(str(t) for t in SWEEP_TOKENS),
+                    help="comma-separated token counts of the sweep")
+    ap.add_argument("--gemm-path", default="auto", choices=list(GEMM_PATHS),
+                    help="where the expert GEMMs run (auto: planner's choice per batch)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample-tokens", type=int, default=512)
     ap.add_argument("--ref-sample-tokens", type=int, default=16)
     args = ap.parse_args()
+    args.sweep_tokens = tuple(int(t) for t in args.sweep.split(",") if t.strip())
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":

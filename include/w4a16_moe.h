@@ -67,6 +67,12 @@ typedef enum {
 typedef enum { W4A16_ACT_SWIGLU = 0, W4A16_ACT_RELU2 = 1 } w4a16_act;
 typedef enum { W4A16_SCALE_GROUP32_K = 0, W4A16_SCALE_PER_CHANNEL = 1 } w4a16_scale;
 typedef enum { W4A16_DT_BF16 = 0, W4A16_DT_FP16 = 1 } w4a16_dtype;
+/* Where the two expert GEMMs run (see w4a16_moe_set_gemm_path). */
+typedef enum {
+  W4A16_PATH_AUTO = 0,          /* planner's choice per batch size */
+  W4A16_PATH_TENSOR_CORES = 1,  /* tcgen05 MMA on dequantised tiles */
+  W4A16_PATH_CUDA_CORES = 2     /* FP16 FMA GEMV, route tiles of <= 16 routes */
+} w4a16_gemm_path;
 
 /*
  * Problem descriptor (logical sizes).
@@ -191,6 +197,7 @@ typedef struct {
   int32_t gemm1_ctas;      /* persistent grid sizes */
   int32_t gemm2_ctas;
   int32_t pipeline_stages;
+  int32_t gemm_path;       /* W4A16_PATH_TENSOR_CORES or W4A16_PATH_CUDA_CORES */
   size_t off_counts, off_offs, off_perm, off_inv, off_tiles, off_num_tiles;  /* bytes */
   size_t off_inter;        /* intermediate activations [max_slots, I] (act dtype) */
   size_t off_expert_out;   /* FP32 expert outputs [gemm2_splits, max_slots, H] */
@@ -210,6 +217,23 @@ w4a16_status w4a16_moe_route_info(w4a16_moe_plan_t plan, int32_t num_tokens,
 w4a16_status w4a16_moe_set_overrides(w4a16_moe_plan_t plan, int32_t tile_rows,
                                      int32_t gemm1_splits, int32_t gemm2_splits,
                                      size_t* workspace_bytes);
+
+/*
+ * Chooses where the expert GEMMs run for later calls with this plan.
+ * W4A16_PATH_AUTO (the default) takes the CUDA-core GEMV while the expected
+ * routes per local expert, num_tokens * top_k / num_experts, are at most 3,
+ * and the tensor cores above that.  Both paths compute the same function
+ * (the expert MLPs of "feat(pytorch): add CuTeDSL W4A16 MoE backend"
+ * (LMDeploy), section Modification); they round differently (the tensor-core
+ * path rounds each dequantised weight to the activation type, the CUDA-core
+ * path sums exact code x activation products in FP16 over one 32-element
+ * group), so outputs of the two agree within the parity tolerance, not bit
+ * for bit.  The CUDA-core path uses route tiles of 16 routes (tile_rows
+ * overrides apply to the tensor-core path only).  workspace_bytes (if not
+ * NULL) receives the workspace size later calls need.  Unknown path:
+ * W4A16_ERR_INVALID_ARG.
+ */
+w4a16_status w4a16_moe_set_gemm_path(w4a16_moe_plan_t plan, int32_t path, size_t* workspace_bytes);
 
 /*
  * Reads (synchronously, on `stream`) and clears the device error flag in the

@@ -14,6 +14,9 @@ import oracle
 from workloads import gen
 from moe_testlib import compare, make_moe, case_on_gpu, oracle_rows, small_cfg
 
+# GEMM paths: tensor cores (tcgen05) and the CUDA-core GEMV for few routes per expert
+PATHS = {"tc": 1, "cc": 2}
+
 pytestmark = pytest.mark.gpu
 
 if not torch.cuda.is_available():
@@ -77,18 +80,21 @@ def test_route_prep_bit_exact_fuzz(seed):
 # MoE output parity
 # ---------------------------------------------------------------------------
 
-def run_and_compare(cfg, T, overrides=None, renormalize=False, ids=None, what=""):
+def run_and_compare(cfg, T, overrides=None, renormalize=False, ids=None, what="", path=None):
     w, x, ids_, tw = case_on_gpu(cfg, T)
     if ids is not None:
         ids_ = ids.cuda()
     moe = make_moe(cfg, max(T, 1))
+    if path is not None:
+        moe.set_gemm_path(PATHS[path])
+        assert moe.route_info(T).gemm_path == PATHS[path]
     if overrides:
         moe.set_overrides(**overrides)
     out = moe(x, w, tw, ids_, renormalize=renormalize)
     torch.cuda.synchronize()
     moe.check_device_error()
     ref = oracle_rows(cfg, w, x, ids_, tw, renormalize=renormalize)
-    return compare(out, ref, what or f"{cfg.name} T={T} {overrides}"), (moe, w, x, ids_, tw, out)
+    return compare(out, ref, what or f"{cfg.name} T={T} {overrides} {path}"), (moe, w, x, ids_, tw, out)
 
 
 def test_tiny_workload_parity():
@@ -106,12 +112,63 @@ SHAPES = [
 ]
 
 
+@pytest.mark.parametrize("path", list(PATHS))
 @pytest.mark.parametrize("shape", SHAPES, ids=lambda s: f"a{s['act']}s{s['scale']}d{s['dt']}")
 @pytest.mark.parametrize("T", [1, 7, 61])
-def test_small_shapes_parity(shape, T):
+def test_small_shapes_parity(shape, T, path):
     # H = 704: 2 full K blocks + a ragged one; I = 320: ragged weight tiles
     cfg = small_cfg(E=5, H=704, I=320, k=3, **shape)
-    run_and_compare(cfg, T)
+    run_and_compare(cfg, T, path=path)
+
+
+def bucket_ids(E, counts, k, seed=0):
+    """ids [T, k] giving expert e exactly counts[e] routes (remaining slots
+    -1), tokens shuffled."""
+    rng = np.random.default_rng(seed)
+    flat = np.concatenate([np.full(c, e) for e, c in enumerate(counts)])
+    T = -(-len(flat) // k)
+    flat = np.concatenate([flat, np.full(T * k - len(flat), -1)])
+    rng.shuffle(flat)
+    return torch.from_numpy(flat.reshape(T, k).astype(np.int32)), T
+
+
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: f"a{s['act']}s{s['scale']}d{s['dt']}")
+def test_cuda_core_route_count_buckets(shape):
+    """Experts with 1, 2, 3, 4, 5, 8, 9, 16, 17 and 40 routes: every route-count
+    specialisation of the CUDA-core GEMV, full and partial 16-route tiles, and
+    experts spanning several tiles."""
+    counts = [1, 2, 3, 4, 5, 8, 9, 16, 17, 40, 0]
+    cfg = small_cfg(E=len(counts), H=640, I=192, k=4, **shape)
+    ids, T = bucket_ids(cfg.num_experts, counts, cfg.top_k)
+    run_and_compare(cfg, T, ids=ids, path="cc")
+
+
+@pytest.mark.parametrize("path", list(PATHS))
+@pytest.mark.parametrize("shape", [SHAPES[0], SHAPES[2], SHAPES[3]], ids=lambda s: f"s{s['scale']}d{s['dt']}")
+@pytest.mark.parametrize("mag", ["tiny", "huge", "mixed"])
+def test_activation_magnitudes(shape, mag, path):
+    """Activations far from unit scale (the CUDA-core path rescales them by
+    powers of two before its FP16 sums): per-token factors 2^-20 .. 2^12 for
+    BF16, 2^-6 .. 2^3 for FP16 (whose intermediate would leave its range)."""
+    cfg = small_cfg(E=4, H=512, I=256, k=2, **shape)
+    T = 24
+    lo, hi = (-20, 12) if shape["dt"] == gen.DT_BF16 else (-6, 3)
+    if mag == "tiny":
+        f = torch.full((T, 1), 2.0 ** lo)
+    elif mag == "huge":
+        f = torch.full((T, 1), 2.0 ** hi)
+    else:
+        f = 2.0 ** torch.linspace(lo, hi, T).round().reshape(T, 1)
+    w, x, ids, tw = case_on_gpu(cfg, T)
+    x = (x.float() * f.cuda()).to(x.dtype)
+    moe = make_moe(cfg, T)
+    moe.set_gemm_path(PATHS[path])
+    out = moe(x, w, tw, ids)
+    torch.cuda.synchronize()
+    ref = oracle_rows(cfg, w, x, ids, tw)
+    # each token's output scales with its factor: compare token by token
+    for t in range(T):
+        compare(out[t:t + 1], ref[t:t + 1], f"{mag} token {t} {path}")
 
 
 @pytest.mark.parametrize("tile_rows", [16, 32, 48, 128])
@@ -123,56 +180,71 @@ def test_route_tile_heights(tile_rows):
         run_and_compare(cfg, 45, overrides=dict(tile_rows=tile_rows))
 
 
+@pytest.mark.parametrize("path", list(PATHS))
 @pytest.mark.parametrize("s1,s2", [(1, 1), (2, 1), (3, 2), (5, 4)])
-def test_split_k_with_nan_poisoned_workspace(s1, s2):
+def test_split_k_with_nan_poisoned_workspace(s1, s2, path):
     """Split-K factors above the number of K blocks leave empty partitions;
     they must write zero partials (workspace poisoned with NaN bytes first)."""
-    cfg = small_cfg(E=4, H=768, I=256, k=2)   # 3 K blocks in GEMM1, 1 in GEMM2
+    for act in (gen.ACT_SWIGLU, gen.ACT_RELU2):
+        cfg = small_cfg(E=4, H=768, I=256, k=2, act=act)   # 3 K blocks in GEMM1, 1 in GEMM2
+        split_case(cfg, s1, s2, path)
+
+
+def split_case(cfg, s1, s2, path):
     w, x, ids, tw = case_on_gpu(cfg, 9)
     moe = make_moe(cfg, 9)
+    moe.set_gemm_path(PATHS[path])
     moe.set_overrides(gemm1_splits=s1, gemm2_splits=s2)
     moe.workspace.fill_(0xFF)
     out = moe(x, w, tw, ids)
     torch.cuda.synchronize()
     moe.check_device_error()
-    compare(out, oracle_rows(cfg, w, x, ids, tw), f"splits {s1},{s2}")
+    compare(out, oracle_rows(cfg, w, x, ids, tw), f"splits {s1},{s2} {path} act {cfg.act}")
 
 
-def test_all_routes_invalid_gives_exact_zero():
+@pytest.mark.parametrize("path", list(PATHS))
+def test_all_routes_invalid_gives_exact_zero(path):
     cfg = small_cfg()
     w, x, ids, tw = case_on_gpu(cfg, 13)
     ids = torch.full_like(ids, -1)
     moe = make_moe(cfg, 13)
+    moe.set_gemm_path(PATHS[path])
     moe.workspace.fill_(0xFF)
     out = moe(x, w, tw, ids)
     torch.cuda.synchronize()
     assert torch.all(out.view(torch.int16) == 0)
 
 
-def test_masked_ids_and_expert_offset():
+@pytest.mark.parametrize("path", list(PATHS))
+def test_masked_ids_and_expert_offset(path):
     cfg = small_cfg(E=6, expert_offset=10)
     w, x, _, tw = case_on_gpu(cfg, 20)
     g = torch.Generator().manual_seed(5)
     ids = torch.randint(8, 18, (20, 2), generator=g, dtype=torch.int32)  # 8, 9, 16, 17: other ranks
     ids[3, 1] = -1
     moe = make_moe(cfg, 20)
+    moe.set_gemm_path(PATHS[path])
     out = moe(x, w, tw, ids.cuda())
     torch.cuda.synchronize()
     compare(out, oracle_rows(cfg, w, x, ids, tw), "masked")
 
 
-def test_renormalize():
+@pytest.mark.parametrize("path", list(PATHS))
+def test_renormalize(path):
     cfg = small_cfg(k=4)
-    run_and_compare(cfg, 17, renormalize=True)
+    run_and_compare(cfg, 17, renormalize=True, path=path)
 
 
-def test_deterministic_bitwise_and_pdl_off(monkeypatch):
+@pytest.mark.parametrize("path", list(PATHS))
+def test_deterministic_bitwise_and_pdl_off(monkeypatch, path):
     cfg = small_cfg(E=8, H=1024, I=256, k=4)
     w, x, ids, tw = case_on_gpu(cfg, 50)
     moe = make_moe(cfg, 50)
+    moe.set_gemm_path(PATHS[path])
     outs = [moe(x, w, tw, ids).clone() for _ in range(3)]
     monkeypatch.setenv("W4A16_MOE_PDL", "0")
     moe2 = make_moe(cfg, 50)
+    moe2.set_gemm_path(PATHS[path])
     outs.append(moe2(x, w, tw, ids).clone())
     moe.set_overrides(gemm1_splits=2)
     split_out = moe(x, w, tw, ids).clone()
@@ -182,10 +254,12 @@ def test_deterministic_bitwise_and_pdl_off(monkeypatch):
     compare(split_out, oracle_rows(cfg, w, x, ids, tw), "split")
 
 
-def test_cuda_graph_replay_with_new_inputs():
+@pytest.mark.parametrize("path", list(PATHS))
+def test_cuda_graph_replay_with_new_inputs(path):
     cfg = small_cfg(E=8, H=1024, I=256, k=2)
     w, x, ids, tw = case_on_gpu(cfg, 33)
     moe = make_moe(cfg, 33)
+    moe.set_gemm_path(PATHS[path])
     out = torch.empty(33, cfg.hidden, dtype=torch.bfloat16, device="cuda")
     s = torch.cuda.Stream()
     with torch.cuda.stream(s):

@@ -14,7 +14,8 @@ from . import _lib
 from ._lib import (Desc, RouteInfo, W4A16Error, w4a16_moe_check_device_error,  # noqa: F401
                    w4a16_moe_forward, w4a16_moe_forward_host, w4a16_moe_plan,
                    w4a16_moe_plan_destroy, w4a16_moe_prepare_routes, w4a16_moe_route_info,
-                   w4a16_moe_set_overrides)
+                   w4a16_moe_set_gemm_path, w4a16_moe_set_overrides)
+from ._lib import PATH_AUTO, PATH_CUDA_CORES, PATH_TENSOR_CORES  # noqa: F401
 
 ACT_SWIGLU, ACT_RELU2 = 0, 1
 SCALE_GROUP32_K, SCALE_PER_CHANNEL = 0, 1
@@ -70,6 +71,13 @@ class W4A16MoE:
 
     def set_overrides(self, tile_rows=0, gemm1_splits=0, gemm2_splits=0):
         need = w4a16_moe_set_overrides(self.plan, tile_rows, gemm1_splits, gemm2_splits)
+        if need > self.workspace.numel():
+            self.workspace = torch.empty(need, dtype=torch.uint8, device=self.device)
+        self.workspace_bytes = need
+
+    def set_gemm_path(self, path=PATH_AUTO):
+        """PATH_AUTO, PATH_TENSOR_CORES or PATH_CUDA_CORES for later calls."""
+        need = w4a16_moe_set_gemm_path(self.plan, path)
         if need > self.workspace.numel():
             self.workspace = torch.empty(need, dtype=torch.uint8, device=self.device)
         self.workspace_bytes = need

@@ -14,6 +14,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libw4a16_moe.so")
 
 W4A16_OK = 0
+PATH_AUTO, PATH_TENSOR_CORES, PATH_CUDA_CORES = 0, 1, 2
 STATUS_NAMES = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "WORKSPACE_TOO_SMALL",
                 4: "CUDA", 5: "DEVICE_TIMEOUT"}
 
@@ -26,6 +27,7 @@ EXPORTED = (
     "w4a16_moe_forward_host",
     "w4a16_moe_route_info",
     "w4a16_moe_set_overrides",
+    "w4a16_moe_set_gemm_path",
     "w4a16_moe_check_device_error",
     "w4a16_moe_set_stage_events",
     "w4a16_moe_forward_static_workspace",
@@ -51,6 +53,7 @@ class RouteInfo(ctypes.Structure):
         ("max_tiles", ctypes.c_int32), ("gemm1_splits", ctypes.c_int32),
         ("gemm2_splits", ctypes.c_int32), ("gemm1_ctas", ctypes.c_int32),
         ("gemm2_ctas", ctypes.c_int32), ("pipeline_stages", ctypes.c_int32),
+        ("gemm_path", ctypes.c_int32),
         ("off_counts", ctypes.c_size_t), ("off_offs", ctypes.c_size_t),
         ("off_perm", ctypes.c_size_t), ("off_inv", ctypes.c_size_t),
         ("off_tiles", ctypes.c_size_t), ("off_num_tiles", ctypes.c_size_t),
@@ -88,6 +91,8 @@ def load(path: str = LIB_PATH):
     L.w4a16_moe_route_info.restype = st
     L.w4a16_moe_set_overrides.argtypes = [P, i32, i32, i32, ctypes.POINTER(ctypes.c_size_t)]
     L.w4a16_moe_set_overrides.restype = st
+    L.w4a16_moe_set_gemm_path.argtypes = [P, i32, ctypes.POINTER(ctypes.c_size_t)]
+    L.w4a16_moe_set_gemm_path.restype = st
     L.w4a16_moe_check_device_error.argtypes = [P, P, P]
     L.w4a16_moe_check_device_error.restype = st
     L.w4a16_moe_set_stage_events.argtypes = [P, ctypes.POINTER(P), i32]
@@ -142,6 +147,12 @@ def w4a16_moe_route_info(plan, num_tokens: int) -> RouteInfo:
 def w4a16_moe_set_overrides(plan, tile_rows: int = 0, gemm1_splits: int = 0, gemm2_splits: int = 0) -> int:
     ws = ctypes.c_size_t()
     check(load().w4a16_moe_set_overrides(plan, tile_rows, gemm1_splits, gemm2_splits, ctypes.byref(ws)))
+    return int(ws.value)
+
+
+def w4a16_moe_set_gemm_path(plan, path: int) -> int:
+    ws = ctypes.c_size_t()
+    check(load().w4a16_moe_set_gemm_path(plan, path, ctypes.byref(ws)))
     return int(ws.value)
 
 

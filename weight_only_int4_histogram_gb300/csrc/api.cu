@@ -1,8 +1,11 @@
 // Host side of the C ABI in include/w4a16_moe.h: descriptor validation, the
-// per-batch planner (route-tile height, split-K factors, persistent grid
-// sizes, workspace layout), TMA descriptor encoding and the launch sequence
+// per-batch planner (GEMM path, route-tile height, split-K factors,
+// persistent grid sizes, workspace layout), TMA descriptor encoding and the
+// launch sequence
 //   route_prep -> gate/up GEMM -> down GEMM -> combine
-// chained with programmatic dependent launch.  No allocation, host sync or
+// chained with programmatic dependent launch.  Both GEMMs run either on the
+// tensor cores (gemm.cuh) or, when experts see only a few routes each, on the
+// CUDA cores (gemv.cuh).  No allocation, host sync or
 // device->host copy happens in prepare_routes / forward.
 #include <cudaTypedefs.h>
 
@@ -24,6 +27,7 @@ struct w4a16_moe_plan_s {
   w4a16_moe_desc d;
   int num_sms;
   int ov_bn, ov_s1, ov_s2;
+  int path;  // W4A16_PATH_*
   size_t ws_bytes;
   bool pdl;
   cudaEvent_t ev[4];
@@ -52,6 +56,7 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 int cdiv(int a, int b) { return (a + b - 1) / b; }
 
 struct Layout {
+  bool gemv;  // CUDA-core path for both GEMMs
   int T, R, bn, tiles_cap;
   int64_t slots_cap;
   int n1;
@@ -64,6 +69,18 @@ struct Layout {
   size_t off_sx, off_sids, off_sw, off_sout;
   size_t total;
 };
+
+// Expected routes per local expert up to which the CUDA-core GEMV runs both
+// GEMMs: its FP16 FMA work grows with the routes per tile while the
+// tensor-core MMA cost per weight tile is flat.
+constexpr double kGemvMaxRoutesPerExpert = 3.0;
+
+bool use_gemv(const w4a16_moe_plan_s& P, int T) {
+  if (P.path == W4A16_PATH_TENSOR_CORES) return false;
+  if (P.path == W4A16_PATH_CUDA_CORES) return true;
+  const double lam = static_cast<double>(T) * P.d.top_k / P.d.num_experts;
+  return lam <= kGemvMaxRoutesPerExpert;
+}
 
 int choose_bn(const w4a16_moe_plan_s& P, int T) {
   if (P.ov_bn) return P.ov_bn;
@@ -101,7 +118,8 @@ Layout make_layout(const w4a16_moe_plan_s& P, int T) {
   Layout L = {};
   L.T = T;
   L.R = T * d.top_k;
-  L.bn = choose_bn(P, T);
+  L.gemv = use_gemv(P, T);
+  L.bn = L.gemv ? kGemvMaxR : choose_bn(P, T);
   const int E = d.num_experts;
   const int touched_max = std::min(E, std::max(L.R, 1));
   L.tiles_cap = (L.R + touched_max * (L.bn - 1)) / L.bn + 1;
@@ -120,12 +138,18 @@ Layout make_layout(const w4a16_moe_plan_s& P, int T) {
   L.s2 = P.ov_s2 ? P.ov_s2 : choose_splits(tiles_est, L.nt2, L.kb2, P.num_sms, 1.0);
   L.kbps1 = cdiv(L.kb1, L.s1);
   L.kbps2 = cdiv(L.kb2, L.s2);
-  L.stage_bytes = kStageA + L.bn * kStageBRow + kStageS;
-  // dynamic shared memory: 1 KB alignment slack + stages + 2 KB control block
-  // (mbarriers, TMEM address, flags, token list)
-  const int smem_budget = 232448 - 3072;
-  L.stages = std::min(kMaxStages, smem_budget / L.stage_bytes);
-  L.smem = 3072 + L.stages * L.stage_bytes;
+  if (L.gemv) {
+    L.stage_bytes = kGemvStageBytes;
+    L.stages = kGemvStages;
+    L.smem = gemv_smem_bytes();
+  } else {
+    L.stage_bytes = kStageA + L.bn * kStageBRow + kStageS;
+    // dynamic shared memory: 1 KB alignment slack + stages + 2 KB control block
+    // (mbarriers, TMEM address, flags, token list)
+    const int smem_budget = 232448 - 3072;
+    L.stages = std::min(kMaxStages, smem_budget / L.stage_bytes);
+    L.smem = 3072 + L.stages * L.stage_bytes;
+  }
   L.grid1 = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(P.num_sms, static_cast<int64_t>(L.tiles_cap) * L.nt1 * L.s1)));
   L.grid2 = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(P.num_sms, static_cast<int64_t>(L.tiles_cap) * L.nt2 * L.s2)));
 
@@ -317,7 +341,8 @@ w4a16_status launch_forward(const w4a16_moe_plan_s& P, const Layout& L, const vo
   g1.counters = reinterpret_cast<int32_t*>(ws + L.off_ctr);
   cudaError_t e;
   if (P.has_ev && (e = cudaEventRecord(P.ev[0], s)) != cudaSuccess) return cuda_fail(e, "event record");
-  e = launch_gemm(GEMM_UP, d.scale_kind, d.act_dtype, g1, tmA1, tmA1, L.grid1, L.smem, s, P.pdl);
+  e = L.gemv ? launch_gemv(GEMM_UP, d.scale_kind, d.act_dtype, g1, tmA1, L.grid1, s, P.pdl)
+             : launch_gemm(GEMM_UP, d.scale_kind, d.act_dtype, g1, tmA1, tmA1, L.grid1, L.smem, s, P.pdl);
   if (e != cudaSuccess) return cuda_fail(e, "gate/up GEMM launch");
   if (P.has_ev && (e = cudaEventRecord(P.ev[1], s)) != cudaSuccess) return cuda_fail(e, "event record");
 
@@ -329,12 +354,13 @@ w4a16_status launch_forward(const w4a16_moe_plan_s& P, const Layout& L, const vo
   g2.kb_total = L.kb2;
   g2.splits = L.s2;
   g2.kb_per_split = L.kbps2;
-  g2.x = nullptr;
+  g2.x = ws + L.off_inter;
   g2.scales = s2;
   g2.out = ws + L.off_y;
   g2.part = nullptr;
   g2.counters = nullptr;
-  e = launch_gemm(GEMM_DOWN, d.scale_kind, d.act_dtype, g2, tmA2, tmB2, L.grid2, L.smem, s, P.pdl);
+  e = L.gemv ? launch_gemv(GEMM_DOWN, d.scale_kind, d.act_dtype, g2, tmA2, L.grid2, s, P.pdl)
+             : launch_gemm(GEMM_DOWN, d.scale_kind, d.act_dtype, g2, tmA2, tmB2, L.grid2, L.smem, s, P.pdl);
   if (e != cudaSuccess) return cuda_fail(e, "down GEMM launch");
   if (P.has_ev && (e = cudaEventRecord(P.ev[2], s)) != cudaSuccess) return cuda_fail(e, "event record");
 
@@ -371,6 +397,20 @@ cudaError_t launch_gemm(int which, int scale_kind, int dtype, const GemmParams& 
                         cudaStream_t s, bool pdl) {
   if (dtype == DT_BF16) return launch_gemm_dt<DT_BF16>(which, scale_kind, p, tmA, tmB, grid, smem_bytes, s, pdl);
   return launch_gemm_dt<DT_FP16>(which, scale_kind, p, tmA, tmB, grid, smem_bytes, s, pdl);
+}
+
+template <int DT>
+cudaError_t launch_gemv_dt(int which, int scale_kind, const GemmParams& p, const CUtensorMap& tmA, int grid,
+                           cudaStream_t s, bool pdl);
+extern template cudaError_t launch_gemv_dt<DT_BF16>(int, int, const GemmParams&, const CUtensorMap&, int,
+                                                     cudaStream_t, bool);
+extern template cudaError_t launch_gemv_dt<DT_FP16>(int, int, const GemmParams&, const CUtensorMap&, int,
+                                                     cudaStream_t, bool);
+
+cudaError_t launch_gemv(int which, int scale_kind, int dtype, const GemmParams& p, const CUtensorMap& tmA,
+                        int grid, cudaStream_t s, bool pdl) {
+  if (dtype == DT_BF16) return launch_gemv_dt<DT_BF16>(which, scale_kind, p, tmA, grid, s, pdl);
+  return launch_gemv_dt<DT_FP16>(which, scale_kind, p, tmA, grid, s, pdl);
 }
 }  // namespace w4a16
 
@@ -418,6 +458,16 @@ w4a16_status w4a16_moe_set_overrides(w4a16_moe_plan_t plan, int32_t tile_rows, i
   return W4A16_OK;
 }
 
+w4a16_status w4a16_moe_set_gemm_path(w4a16_moe_plan_t plan, int32_t path, size_t* workspace_bytes) {
+  if (!plan) return fail(W4A16_ERR_INVALID_ARG, "plan is NULL");
+  if (path != W4A16_PATH_AUTO && path != W4A16_PATH_TENSOR_CORES && path != W4A16_PATH_CUDA_CORES)
+    return fail(W4A16_ERR_INVALID_ARG, "unknown GEMM path %d", path);
+  plan->path = path;
+  plan->ws_bytes = max_workspace(*plan);
+  if (workspace_bytes) *workspace_bytes = plan->ws_bytes;
+  return W4A16_OK;
+}
+
 w4a16_status w4a16_moe_route_info(w4a16_moe_plan_t plan, int32_t num_tokens, w4a16_route_info* info) {
   if (!plan || !info) return fail(W4A16_ERR_INVALID_ARG, "plan / info is NULL");
   if (num_tokens < 0 || num_tokens > plan->d.max_tokens)
@@ -431,6 +481,7 @@ w4a16_status w4a16_moe_route_info(w4a16_moe_plan_t plan, int32_t num_tokens, w4a
   info->gemm1_ctas = L.grid1;
   info->gemm2_ctas = L.grid2;
   info->pipeline_stages = L.stages;
+  info->gemm_path = L.gemv ? W4A16_PATH_CUDA_CORES : W4A16_PATH_TENSOR_CORES;
   info->off_counts = L.off_counts;
   info->off_offs = L.off_offs;
   info->off_perm = L.off_perm;

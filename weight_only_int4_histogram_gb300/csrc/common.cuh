@@ -30,6 +30,16 @@ constexpr int kStageA = kTileRows * kBlockK / 2;   // 8 KB packed INT4 per stage
 constexpr int kStageS = kTileRows * kGroupsPerStage * 2;  // BF16 scales per stage
 constexpr int kStageBRow = kBlockK * 2;            // bytes of one activation row per stage
 
+// CUDA-core GEMV path (gemv.cuh): route tiles of at most kGemvMaxR routes.
+constexpr int kGemvThreads = 320;    // 10 warps: see the role map in gemv.cuh
+constexpr int kGemvMaxR = 16;
+constexpr int kGemvStages = 12;
+constexpr int kGemvStageBytes = 18432;  // weights, scales, raw + staged activations
+constexpr int kGemvCtrlBytes = 512;     // mbarriers and flags after the stages
+__host__ __device__ constexpr int gemv_smem_bytes() {
+  return 1024 + kGemvStages * kGemvStageBytes + kGemvCtrlBytes;  // 1 KB alignment slack
+}
+
 enum { ACT_SWIGLU = 0, ACT_RELU2 = 1 };
 enum { SCALE_GROUP = 0, SCALE_CHANNEL = 1 };
 enum { DT_BF16 = 0, DT_FP16 = 1 };
@@ -70,7 +80,8 @@ struct GemmParams {
   const int4* tiles;       // route tiles (expert, first slot, valid rows, 0)
   const int32_t* num_tiles;
   const int32_t* perm;     // slot -> flat route (gate/up gather)
-  const void* x;           // gate/up: activations [T, H]
+  const void* x;           // gate/up: activations [T, H]; down: the intermediate
+                           // [slots_cap, I] (read by the CUDA-core path only)
   const uint16_t* scales;  // BF16 scale bits of this GEMM's weights
   int64_t slots_cap;
   void* out;               // gate/up: intermediate [slots_cap, I] act dtype
@@ -95,6 +106,8 @@ cudaError_t launch_route_prep(const RoutePrepParams& p, int smem_bytes, cudaStre
 cudaError_t launch_gemm(int which, int scale_kind, int dtype, const GemmParams& p,
                         const CUtensorMap& tmA, const CUtensorMap& tmB, int grid, int smem_bytes,
                         cudaStream_t s, bool pdl);
+cudaError_t launch_gemv(int which, int scale_kind, int dtype, const GemmParams& p,
+                        const CUtensorMap& tmA, int grid, cudaStream_t s, bool pdl);
 cudaError_t launch_combine(int dtype, const CombineParams& p, cudaStream_t s, bool pdl);
 int gemm_smem_bytes(int bn, int stages);
 int gemm_stage_bytes(int bn);
