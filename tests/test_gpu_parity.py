@@ -149,10 +149,11 @@ def test_cuda_core_route_count_buckets(shape):
 def test_activation_magnitudes(shape, mag, path):
     """Activations far from unit scale (the CUDA-core path rescales them by
     powers of two before its FP16 sums): per-token factors 2^-20 .. 2^12 for
-    BF16, 2^-6 .. 2^3 for FP16 (whose intermediate would leave its range)."""
+    BF16, 2^-2 .. 2^3 for FP16 (outputs grow like the factor squared and would
+    otherwise leave FP16's normal range in the final cast)."""
     cfg = small_cfg(E=4, H=512, I=256, k=2, **shape)
     T = 24
-    lo, hi = (-20, 12) if shape["dt"] == gen.DT_BF16 else (-6, 3)
+    lo, hi = (-20, 12) if shape["dt"] == gen.DT_BF16 else (-2, 3)
     if mag == "tiny":
         f = torch.full((T, 1), 2.0 ** lo)
     elif mag == "huge":
