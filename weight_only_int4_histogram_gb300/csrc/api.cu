@@ -127,9 +127,10 @@ Layout make_layout(const w4a16_moe_plan_s& P, int T) {
   const bool gated = d.act == W4A16_ACT_SWIGLU;
   L.n1 = gated ? 2 * d.inter : d.inter;
   L.nt1 = gated ? d.inter / 64 : cdiv(d.inter, kTileRows);
-  L.kb1 = cdiv(d.hidden, kBlockK);
+  const int block_k = L.gemv ? kGemvBlockK : kBlockK;  // K values per pipeline stage
+  L.kb1 = cdiv(d.hidden, block_k);
   L.nt2 = cdiv(d.hidden, kTileRows);
-  L.kb2 = cdiv(d.inter, kBlockK);
+  L.kb2 = cdiv(d.inter, block_k);
   // expected route tiles (uniform routing): touched experts x tiles per expert
   const double touched = std::max(1.0, E * (1.0 - std::exp(-static_cast<double>(L.R) / E)));
   const double per = L.R / touched;
@@ -218,6 +219,20 @@ bool encode_weights(CUtensorMap* m, const void* base, uint64_t inner, uint64_t r
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// BF16 group scales as a 3D tensor [E][rows][groups], unswizzled boxes of 8
+// groups (16 bytes) x 64 rows; needs 16-byte aligned rows (groups % 8 == 0).
+bool encode_scales(CUtensorMap* m, const void* base, uint64_t groups, uint64_t rows, uint64_t E) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {groups, rows, E};
+  cuuint64_t strides[2] = {groups * 2, groups * rows * 2};
+  cuuint32_t box[3] = {kGemvBlockK / kGroup, 64, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // A row-major 16-bit matrix [rows][cols], boxes of 64 columns x box_rows, 128B swizzle.
 bool encode_rows16(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint32_t box_rows,
                    int dtype) {
@@ -301,15 +316,26 @@ w4a16_status launch_forward(const w4a16_moe_plan_s& P, const Layout& L, const vo
   CUtensorMap tmA1, tmA2, tmB2;
   bool ok;
   if (group) {
-    // rows of packed bytes along K; boxes of 64 bytes (128 K values) x 64 rows
-    ok = encode_weights(&tmA1, w13, d.hidden / 2, L.n1, d.num_experts, kBlockK / 2, 64) &&
-         encode_weights(&tmA2, w2, d.inter / 2, d.hidden, d.num_experts, kBlockK / 2, 64);
+    // rows of packed bytes along K; boxes of 64 rows x one stage of K: 64 bytes
+    // (128 K values, 64-byte swizzle) for the tensor-core path, 128 bytes (256 K
+    // values, 128-byte swizzle) for the CUDA-core path
+    const uint32_t box = L.gemv ? kGemvBlockK / 2 : kBlockK / 2;
+    ok = encode_weights(&tmA1, w13, d.hidden / 2, L.n1, d.num_experts, box, 64) &&
+         encode_weights(&tmA2, w2, d.inter / 2, d.hidden, d.num_experts, box, 64);
   } else {
     // row pairs of K bytes; boxes of 128 bytes (128 K values) x 32 row pairs
     ok = encode_weights(&tmA1, w13, d.hidden, L.n1 / 2, d.num_experts, kBlockK, 32) &&
          encode_weights(&tmA2, w2, d.inter, d.hidden / 2, d.num_experts, kBlockK, 32);
   }
   ok = ok && encode_rows16(&tmB2, ws + L.off_inter, d.inter, L.slots_cap, L.bn, d.act_dtype);
+  // CUDA-core path: group scales by TMA where their rows are 16-byte multiples
+  CUtensorMap tmS1, tmS2;
+  memset(&tmS1, 0, sizeof(tmS1));
+  memset(&tmS2, 0, sizeof(tmS2));
+  const bool stma1 = L.gemv && group && (d.hidden / kGroup) % 8 == 0 && aligned(s13, 16);
+  const bool stma2 = L.gemv && group && (d.inter / kGroup) % 8 == 0 && aligned(s2, 16);
+  if (stma1) ok = ok && encode_scales(&tmS1, s13, d.hidden / kGroup, L.n1, d.num_experts);
+  if (stma2) ok = ok && encode_scales(&tmS2, s2, d.inter / kGroup, d.hidden, d.num_experts);
   if (!ok) return fail(W4A16_ERR_CUDA, "cuTensorMapEncodeTiled failed (driver entry point or arguments)");
 
   GemmParams g = {};
@@ -325,6 +351,7 @@ w4a16_status launch_forward(const w4a16_moe_plan_s& P, const Layout& L, const vo
   g.perm = reinterpret_cast<const int32_t*>(ws + L.off_perm);
   g.slots_cap = L.slots_cap;
   g.err = reinterpret_cast<int32_t*>(ws + L.off_err);
+  g.tiles_cap = L.tiles_cap;
 
   GemmParams g1 = g;
   g1.n_rows = L.n1;
@@ -339,9 +366,10 @@ w4a16_status launch_forward(const w4a16_moe_plan_s& P, const Layout& L, const vo
   g1.out = ws + L.off_inter;
   g1.part = reinterpret_cast<float*>(ws + L.off_part);
   g1.counters = reinterpret_cast<int32_t*>(ws + L.off_ctr);
+  g1.scale_tma = stma1 ? 1 : 0;
   cudaError_t e;
   if (P.has_ev && (e = cudaEventRecord(P.ev[0], s)) != cudaSuccess) return cuda_fail(e, "event record");
-  e = L.gemv ? launch_gemv(GEMM_UP, d.scale_kind, d.act_dtype, g1, tmA1, L.grid1, s, P.pdl)
+  e = L.gemv ? launch_gemv(GEMM_UP, d.scale_kind, d.act_dtype, g1, tmA1, tmS1, L.grid1, s, P.pdl)
              : launch_gemm(GEMM_UP, d.scale_kind, d.act_dtype, g1, tmA1, tmA1, L.grid1, L.smem, s, P.pdl);
   if (e != cudaSuccess) return cuda_fail(e, "gate/up GEMM launch");
   if (P.has_ev && (e = cudaEventRecord(P.ev[1], s)) != cudaSuccess) return cuda_fail(e, "event record");
@@ -359,7 +387,8 @@ w4a16_status launch_forward(const w4a16_moe_plan_s& P, const Layout& L, const vo
   g2.out = ws + L.off_y;
   g2.part = nullptr;
   g2.counters = nullptr;
-  e = L.gemv ? launch_gemv(GEMM_DOWN, d.scale_kind, d.act_dtype, g2, tmA2, L.grid2, s, P.pdl)
+  g2.scale_tma = stma2 ? 1 : 0;
+  e = L.gemv ? launch_gemv(GEMM_DOWN, d.scale_kind, d.act_dtype, g2, tmA2, tmS2, L.grid2, s, P.pdl)
              : launch_gemm(GEMM_DOWN, d.scale_kind, d.act_dtype, g2, tmA2, tmB2, L.grid2, L.smem, s, P.pdl);
   if (e != cudaSuccess) return cuda_fail(e, "down GEMM launch");
   if (P.has_ev && (e = cudaEventRecord(P.ev[2], s)) != cudaSuccess) return cuda_fail(e, "event record");
@@ -400,17 +429,17 @@ cudaError_t launch_gemm(int which, int scale_kind, int dtype, const GemmParams& 
 }
 
 template <int DT>
-cudaError_t launch_gemv_dt(int which, int scale_kind, const GemmParams& p, const CUtensorMap& tmA, int grid,
-                           cudaStream_t s, bool pdl);
-extern template cudaError_t launch_gemv_dt<DT_BF16>(int, int, const GemmParams&, const CUtensorMap&, int,
-                                                     cudaStream_t, bool);
-extern template cudaError_t launch_gemv_dt<DT_FP16>(int, int, const GemmParams&, const CUtensorMap&, int,
-                                                     cudaStream_t, bool);
+cudaError_t launch_gemv_dt(int which, int scale_kind, const GemmParams& p, const CUtensorMap& tmA,
+                           const CUtensorMap& tmS, int grid, cudaStream_t s, bool pdl);
+extern template cudaError_t launch_gemv_dt<DT_BF16>(int, int, const GemmParams&, const CUtensorMap&,
+                                                     const CUtensorMap&, int, cudaStream_t, bool);
+extern template cudaError_t launch_gemv_dt<DT_FP16>(int, int, const GemmParams&, const CUtensorMap&,
+                                                     const CUtensorMap&, int, cudaStream_t, bool);
 
 cudaError_t launch_gemv(int which, int scale_kind, int dtype, const GemmParams& p, const CUtensorMap& tmA,
-                        int grid, cudaStream_t s, bool pdl) {
-  if (dtype == DT_BF16) return launch_gemv_dt<DT_BF16>(which, scale_kind, p, tmA, grid, s, pdl);
-  return launch_gemv_dt<DT_FP16>(which, scale_kind, p, tmA, grid, s, pdl);
+                        const CUtensorMap& tmS, int grid, cudaStream_t s, bool pdl) {
+  if (dtype == DT_BF16) return launch_gemv_dt<DT_BF16>(which, scale_kind, p, tmA, tmS, grid, s, pdl);
+  return launch_gemv_dt<DT_FP16>(which, scale_kind, p, tmA, tmS, grid, s, pdl);
 }
 }  // namespace w4a16
 

@@ -30,12 +30,14 @@ constexpr int kStageA = kTileRows * kBlockK / 2;   // 8 KB packed INT4 per stage
 constexpr int kStageS = kTileRows * kGroupsPerStage * 2;  // BF16 scales per stage
 constexpr int kStageBRow = kBlockK * 2;            // bytes of one activation row per stage
 
-// CUDA-core GEMV path (gemv.cuh): route tiles of at most kGemvMaxR routes.
-constexpr int kGemvThreads = 320;    // 10 warps: see the role map in gemv.cuh
-constexpr int kGemvMaxR = 16;
-constexpr int kGemvStages = 12;
-constexpr int kGemvStageBytes = 18432;  // weights, scales, raw + staged activations
-constexpr int kGemvCtrlBytes = 512;     // mbarriers and flags after the stages
+// CUDA-core GEMV path (gemv.cuh): route tiles of at most kGemvMaxR routes,
+// pipeline stages of kGemvBlockK K values.
+constexpr int kGemvThreads = 576;    // 18 warps: see the role map in gemv.cuh
+constexpr int kGemvMaxR = 8;
+constexpr int kGemvBlockK = 256;
+constexpr int kGemvStages = 9;
+constexpr int kGemvStageBytes = 23552;  // weights, scales, activation rows
+constexpr int kGemvCtrlBytes = 12800;   // mbarriers, flags, K-half exchange, tile table
 __host__ __device__ constexpr int gemv_smem_bytes() {
   return 1024 + kGemvStages * kGemvStageBytes + kGemvCtrlBytes;  // 1 KB alignment slack
 }
@@ -89,6 +91,8 @@ struct GemmParams {
   float* part;             // gate/up split-K partials [splits, slots_cap, N1]
   int32_t* counters;       // gate/up split-K arrival counters [tiles_cap * n_tiles]
   int32_t* err;
+  int32_t tiles_cap;       // capacity of `tiles`
+  int32_t scale_tma;       // CUDA-core path: group scales loaded by TMA (16-byte rows)
 };
 
 struct CombineParams {
@@ -107,7 +111,8 @@ cudaError_t launch_gemm(int which, int scale_kind, int dtype, const GemmParams& 
                         const CUtensorMap& tmA, const CUtensorMap& tmB, int grid, int smem_bytes,
                         cudaStream_t s, bool pdl);
 cudaError_t launch_gemv(int which, int scale_kind, int dtype, const GemmParams& p,
-                        const CUtensorMap& tmA, int grid, cudaStream_t s, bool pdl);
+                        const CUtensorMap& tmA, const CUtensorMap& tmS, int grid, cudaStream_t s,
+                        bool pdl);
 cudaError_t launch_combine(int dtype, const CombineParams& p, cudaStream_t s, bool pdl);
 int gemm_smem_bytes(int bn, int stages);
 int gemm_stage_bytes(int bn);

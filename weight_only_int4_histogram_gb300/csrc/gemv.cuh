@@ -1,60 +1,66 @@
-// Expert-grouped W4A16 GEMV for sm_103a CUDA cores (both MoE GEMMs, few
-// routes per expert).
+// Expert-grouped W4A16 GEMV for sm_103a (both MoE GEMMs, few routes per
+// expert), on warp-level MMAs fed by register-side dequantisation.
 //
-// Same operation, work units and outputs as the tensor-core kernel in gemm.cuh
+// Same operation, work units and outputs as the tcgen05 kernel in gemm.cuh
 // (route tile x 128-row weight tile x K split; the "gate/up GEMM" and "down
 // GEMM" of "feat(pytorch): add CuTeDSL W4A16 MoE backend" (LMDeploy), sections
 // Modification and Benchmark), for batches where an expert sees only a handful
 // of routes.  There each weight is used by 1-4 routes: the contraction is a
 // matrix-vector product whose cost is streaming the packed INT4 weights, and a
-// tensor-core tile (N >= 16 columns, a fixed issue cost per MMA) would waste
-// most of its work.  The route tiles here are at most 16 routes high; each unit
-// is run with a compile-time route count R in {1, 2, 3, 4, 8, 16} (the smallest
-// that covers the tile).
+// 128-row tcgen05 tile with TMEM staging has a fixed cost per MMA that such
+// thin tiles cannot amortise.  Here the route tile (<= kGemvMaxR = 8 routes)
+// is the N = 8 side of mma.sync m16n8k16 and the dequantised weights go to the
+// MMA straight from registers.
 //
-// Arithmetic (per weight row, per 32-element group):
-//   * two nibbles of one 32-bit word go to the two FP16 halves with one lop3
-//     ((w & mask) ^ magic = FP16 1024 + (nibble ^ 8), or 1024 + 16 (nibble ^ 8)
-//     for a nibble in the high half of its byte) and one HSUB2 gives the exact
-//     codes q (or 16 q);
-//   * the activations are staged in shared memory as FP16, multiplied by a
-//     power of two 2^s per (route pair, K block) that puts their largest
-//     magnitude in [64, 128) (group scales) or [4, 8) (per-channel scales), and
-//     pre-divided by 16 where the weight code is 16 q; so every product q * x
-//     is exact and every FP16 partial sum stays below 2^15;
-//   * HFMA2 accumulates the 32 products of a group in FP16 (two interleaved
-//     chains per route), the group sum is widened to FP32, multiplied by the
-//     group scale and accumulated in FP32; 2^-s is applied per K block.
+// Arithmetic (per weight row, per 32-element group), in the activation type
+// (BF16 or FP16) with FP32 accumulation:
+//   * a nibble goes to each 16-bit half of a register with one lop3
+//     ((w & 0x000F000F) ^ magic = 2^m + 8 + q in the activation type, m = 7
+//     for BF16 and 10 for FP16, nibble = q & 15) and one HSUB2 of 2^m + 8
+//     leaves the exact code q; shifting the word by 4, 8 and 12 bits gives the
+//     other three nibble pairs;
+//   * the MMA multiplies the exact codes by the activations as given and sums
+//     in FP32, one group (two MMAs) at a time; the group result is multiplied
+//     by the group scale and accumulated in FP32.
 //   Per-channel scales multiply the FP32 total in the epilogue.
 //
-// Warp roles (320 threads):
-//   warp 0     TMA producer of the packed weight tile and the group scales
-//              (cp.async), as in the tensor-core kernel
-//   warp 1     activation staging: cp.async of the tile's rows (gate/up: token
-//              rows of x by slot; down: intermediate rows), then conversion to
-//              scaled, permuted FP16 kGemvLag stages later
-//   warps 2-9  compute: thread (warp 2 + c, lane l) owns one weight row of the
-//              128-row tile and the K half (l >> 4) of every 128-K stage; the
-//              halves meet with one shuffle per unit.  For SwiGLU the gate row
-//              and the up row of one intermediate index sit in lanes l and
-//              l ^ 8 of one warp.
+// A pipeline stage is 128 weight rows x kGemvBlockK (256) K values: 128 bytes
+// of every packed row per visit, read by TMA in 128-byte-swizzled boxes.
+//
+// Warp roles (576 threads):
+//   warp 0      TMA producer of the packed weight tile and the group scales
+//               (TMA when their rows are 16-byte multiples, else cp.async)
+//   warp 1      activation rows: cp.async of the tile's rows (gate/up: token
+//               rows of x by slot; down: intermediate rows), completion
+//               signalled on the stage's mbarrier without blocking the warp
+//   warps 2-17  compute: warp 2 + c takes row block c % 8 (16 rows) and K half
+//               c / 8 of every stage; the halves meet once per unit through
+//               shared memory.  For SwiGLU a row block holds 8 gate rows and
+//               their 8 up rows, so the activation is applied in registers.
 #pragma once
 #include "gemm.cuh"
 
 namespace w4a16 {
 
 // Stage layout (bytes from the 1024-aligned stage base).
-constexpr int kGvOffS = kStageA;                                // group scales
-constexpr int kGvOffRaw = kGvOffS + kStageS;                    // raw activation rows
-constexpr int kGvHalfBytes = 144;                               // 64 FP16 + 16 B pad
-constexpr int kGvRouteBytes = 2 * kGvHalfBytes;
-constexpr int kGvOffX = kGvOffRaw + kGemvMaxR * kStageBRow;     // staged FP16 rows
-constexpr int kGvOffInv = kGvOffX + kGemvMaxR * kGvRouteBytes;  // 2^-s per route
-static_assert(kGvOffInv + kGemvMaxR * 4 <= kGemvStageBytes, "GEMV stage overflow");
+constexpr int kGvWeightBytes = kTileRows * kGemvBlockK / 2;          // packed weights
+constexpr int kGvScaleRowBytes = kGemvBlockK / kGroup * 2;            // 8 BF16 scales per row
+constexpr int kGvOffS = kGvWeightBytes;
+constexpr int kGvOffX = kGvOffS + kTileRows * kGvScaleRowBytes;       // activation rows
+constexpr int kGvRouteBytes = kGemvBlockK * 2 + 64;                   // + pad: 64 mod 128
+static_assert(kGvOffX + kGemvMaxR * kGvRouteBytes <= kGemvStageBytes, "GEMV stage overflow");
 static_assert(kGemvStageBytes % 1024 == 0, "GEMV stages must keep 1024-byte alignment");
-constexpr int kGemvLag = 6;  // stages between an activation copy and its conversion
-static_assert(kGemvLag + 2 <= kGemvStages, "conversion lag needs a deeper ring");
-static_assert(kGemvCtrlBytes >= 3 * kGemvStages * 8 + 8 + 8 + 4 * kGemvStages, "control block");
+constexpr int kGemvComputeWarps = 16;
+static_assert(kGemvThreads == 32 * (2 + kGemvComputeWarps), "warp roles");
+// Control block: mbarriers and flags; the K-half exchange (two buffers of 8
+// warps x 32 lanes x 4 floats) from kGvCtrlRedOff; the tile records of the
+// CTA's first kGemvTileTab units from kGvCtrlTabOff.
+constexpr int kGvCtrlRedOff = 512;
+constexpr int kGvCtrlTabOff = kGvCtrlRedOff + 2 * 8 * 32 * 16;
+constexpr int kGemvTileTab = 256;
+static_assert(3 * kGemvStages * 8 + 8 + 8 <= kGvCtrlRedOff, "control block");
+static_assert(kGvCtrlTabOff + kGemvTileTab * 16 <= kGemvCtrlBytes, "tile table");
+static_assert(kGemvTileTab <= kGemvThreads, "one record per thread");
 
 __device__ __forceinline__ void ring_next(int& st, uint32_t& ph) {
   if (++st == kGemvStages) {
@@ -63,151 +69,178 @@ __device__ __forceinline__ void ring_next(int& st, uint32_t& ph) {
   }
 }
 
-__device__ __forceinline__ uint32_t hsub2_bits(uint32_t a, uint32_t b) {
-  __half2 r = __hsub2(*reinterpret_cast<__half2*>(&a), *reinterpret_cast<__half2*>(&b));
-  return *reinterpret_cast<uint32_t*>(&r);
+// Tile record of this CTA's i-th unit u: from the shared table (filled at
+// kernel start) or, past its end, from global memory.
+__device__ __forceinline__ int4 tile_of(const GemmParams& p, const int4* tab, int i, int u) {
+  return i < kGemvTileTab ? tab[i] : load_tile(p, u);
 }
 
-__device__ __forceinline__ uint32_t f2_to_h2_bits(float lo, float hi) {
-  __half2 h = __floats2half2_rn(lo, hi);
-  return *reinterpret_cast<uint32_t*>(&h);
+// Iterates this CTA's units u = blockIdx.x + i * gridDim.x, keeping the
+// (split, weight tile, route tile) digits of u up to date with carries instead
+// of divisions.
+struct UnitIter {
+  int u, split, nt, tile, ds, dnt, dtile;
+  __device__ __forceinline__ void init(const GemmParams& p) {
+    u = blockIdx.x;
+    split = u % p.splits;
+    const int r = u / p.splits;
+    nt = r % p.n_tiles;
+    tile = r / p.n_tiles;
+    const int G = gridDim.x;
+    ds = G % p.splits;
+    const int gr = G / p.splits;
+    dnt = gr % p.n_tiles;
+    dtile = gr / p.n_tiles;
+  }
+  __device__ __forceinline__ void next(const GemmParams& p) {
+    u += gridDim.x;
+    split += ds;
+    int c = 0;
+    if (split >= p.splits) {
+      split -= p.splits;
+      c = 1;
+    }
+    nt += dnt + c;
+    c = 0;
+    if (nt >= p.n_tiles) {
+      nt -= p.n_tiles;
+      c = 1;
+    }
+    tile += dtile + c;
+  }
+  __device__ __forceinline__ Unit unit(const GemmParams& p) const {
+    Unit w;
+    w.split = split;
+    w.nt = nt;
+    w.tile = tile;
+    w.kb0 = split * p.kb_per_split;
+    w.kb1 = min(w.kb0 + p.kb_per_split, p.kb_total);
+    return w;
+  }
+};
+
+// D (16 x 8, FP32) += A (16 x 16) * B (16 x 8), A and B in the activation
+// type; fragments as the PTX ISA gives them for m16n8k16: lane (g = lane / 4,
+// t = lane % 4) holds A rows g and g + 8 at K 2t, 2t + 1 (a0, a1) and 2t + 8,
+// 2t + 9 (a2, a3), B column g at the same K (b0, b1), D rows g, g + 8 at
+// columns 2t, 2t + 1.
+template <int DT>
+__device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                          uint32_t b0, uint32_t b1) {
+  if (DT == DT_BF16) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+  } else {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+  }
 }
 
-__device__ __forceinline__ __half2 h2_of(uint32_t b) { return *reinterpret_cast<__half2*>(&b); }
+// Exact code pair of the low nibbles of the two 16-bit halves of v.
+template <int DT>
+__device__ __forceinline__ uint32_t code_pair(uint32_t v) {
+  return F16<DT>::sub(lop3_and_xor(v, 0x000F000Fu, F16<DT>::kMagic), F16<DT>::kMagic);
+}
 
-// One unit (route tile x weight tile x K split) for a compile-time route count
-// R >= rows.  Routes rows..R-1 read stale staging data; their sums are never
-// stored.
+// One unit (route tile x weight tile x K split) on one compute warp: 16 weight
+// rows (MMA rows g: rowA, g + 8: rowB) x one K half of every stage x the
+// tile's <= 8 routes (MMA columns; columns past the route count read stale
+// data and are never stored).
 //
-// Codes of one 32-element group, as FP16 pairs matching the staged activations:
-//   group scales (K-packed, byte b = K 2b | K 2b+1 << 4): word v holds K
-//     8v..8v+7 and gives q[4v..4v+3] = (k0, k4), 16 (k1, k5), (k2, k6), 16 (k3, k7)
+// K order inside an MMA: any bijection works as long as A and B agree, so each
+// lane feeds whole packed words in the order the nibble extraction yields and
+// pairs its activations the same way with byte permutes:
+//   group scales (K-packed, byte b = K 2b | K 2b+1 << 4): lane t takes word t
+//     of group c's 16-byte chunk (K 32c + 8t .. + 7); its code pairs
+//     (k0, k4), (k1, k5), (k2, k6), (k3, k7) feed two MMAs whose sum over the
+//     four lanes is exactly group c, so the group scale multiplies that result;
 //   per-channel (row-pair packed, one byte per K, even row in the low nibble):
-//     word j holds K 4j..4j+3 and gives q[2j] = (k0, k2), q[2j + 1] = (k1, k3),
-//     times 16 for odd rows
-template <int WHICH, int SCALE, int DT, int R>
+//     lane t takes 16-byte chunks t and t + 4 of the K half; word i of a chunk
+//     (4 K) gives (k0, k2) and (k1, k3) for one MMA.
+template <int WHICH, int SCALE, int DT>
 __device__ __forceinline__ bool gemv_unit(const GemmParams& p, uint8_t* smem, uint64_t* full,
                                           uint64_t* bfull, uint64_t* empty, uint64_t* epibar,
                                           volatile int* abort_flag, volatile int* fixup_flag,
-                                          const Unit& w, int e, int m0, int rows, int row,
-                                          int cw, int lane, int& st, uint32_t& ph, uint32_t& eph) {
+                                          float* red, const Unit& w, int e, int m0, int rows,
+                                          int rowA, int rowB, int rb, int kh, int lane, int& st,
+                                          uint32_t& ph, uint32_t& eph) {
   using T = F16<DT>;
-  const int khalf = lane >> 4;
+  const int g = lane >> 2, t = lane & 3;
   const bool gated = (WHICH == GEMM_UP && p.act == ACT_SWIGLU);
   const int N1 = p.n_rows;
-  float tot[R];
-#pragma unroll
-  for (int r = 0; r < R; ++r) tot[r] = 0.0f;
-
-  // per-channel: the row's nibble (parity) selects mask and magic
-  const uint32_t pc_mask = (row & 1) ? 0x00F000F0u : 0x000F000Fu;
-  const uint32_t pc_magic = (row & 1) ? 0x64806480u : 0x64086408u;
+  // tot[0..1]: rowA x routes 2t, 2t + 1; tot[2..3]: rowB x the same routes
+  float tot[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+  // per-channel: the rows' nibble (rowA and rowB have the same parity)
+  const int pc_shift = (rowA & 1) * 4;
 
   for (int kb = w.kb0; kb < w.kb1; ++kb) {
     if (!mbar_wait(&full[st], ph, abort_flag, p.err) || !mbar_wait(&bfull[st], ph, abort_flag, p.err))
       return false;
     const uint8_t* sA = smem + st * kGemvStageBytes;
-    const uint8_t* sX = sA + kGvOffX + khalf * kGvHalfBytes;
-    const float* sInv = reinterpret_cast<const float*>(sA + kGvOffInv);
-    float acc[R];
-#pragma unroll
-    for (int r = 0; r < R; ++r) acc[r] = 0.0f;
-    // this thread's 64 K of packed codes
-    uint32_t wd[16];
-    uint2 sc = make_uint2(0, 0);
+    const uint8_t* sXr = sA + kGvOffX + g * kGvRouteBytes;  // this lane's B column (route g)
     if (SCALE == SCALE_GROUP) {
-      // 64 bytes per row, 64-byte swizzle: 16-byte chunk c sits at c ^ ((row >> 1) & 3)
-      const uint8_t* rowp = sA + row * 64;
-      const int sw = (row >> 1) & 3;
+      // boxes of 64 rows x 128 bytes, 128-byte swizzle: chunk c of row r at c ^ (r & 7)
+      const uint8_t* pA = sA + (rowA >> 6) * 8192 + (rowA & 63) * 128 + 4 * t;
+      const uint8_t* pB = sA + (rowB >> 6) * 8192 + (rowB & 63) * 128 + 4 * t;
+      const uint2 sa = *reinterpret_cast<const uint2*>(sA + kGvOffS + rowA * kGvScaleRowBytes + kh * 8);
+      const uint2 sb = *reinterpret_cast<const uint2*>(sA + kGvOffS + rowB * kGvScaleRowBytes + kh * 8);
 #pragma unroll
-      for (int g = 0; g < 2; ++g) {
-        const uint4 v = *reinterpret_cast<const uint4*>(rowp + (((2 * khalf + g) ^ sw) << 4));
-        wd[4 * g + 0] = v.x;
-        wd[4 * g + 1] = v.y;
-        wd[4 * g + 2] = v.z;
-        wd[4 * g + 3] = v.w;
+      for (int m = 0; m < 4; ++m) {
+        const int c = 4 * kh + m;  // group of the stage
+        const uint32_t wa = *reinterpret_cast<const uint32_t*>(pA + ((c ^ (rowA & 7)) << 4));
+        const uint32_t wb = *reinterpret_cast<const uint32_t*>(pB + ((c ^ (rowB & 7)) << 4));
+        // activations K 32c + 8t .. + 7 of route g: (x0 x1) (x2 x3) (x4 x5) (x6 x7)
+        const uint4 xv = *reinterpret_cast<const uint4*>(sXr + (4 * c + t) * 16);
+        float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        mma_16816<DT>(d, code_pair<DT>(wa), code_pair<DT>(wb), code_pair<DT>(wa >> 4), code_pair<DT>(wb >> 4),
+                      __byte_perm(xv.x, xv.z, 0x5410), __byte_perm(xv.x, xv.z, 0x7632));
+        mma_16816<DT>(d, code_pair<DT>(wa >> 8), code_pair<DT>(wb >> 8), code_pair<DT>(wa >> 12),
+                      code_pair<DT>(wb >> 12), __byte_perm(xv.y, xv.w, 0x5410), __byte_perm(xv.y, xv.w, 0x7632));
+        // BF16 group scales of rowA / rowB -> FP32 exactly
+        const uint32_t swa = (m < 2) ? sa.x : sa.y, swb = (m < 2) ? sb.x : sb.y;
+        const float fa = __uint_as_float((m & 1) ? (swa & 0xFFFF0000u) : (swa << 16));
+        const float fb = __uint_as_float((m & 1) ? (swb & 0xFFFF0000u) : (swb << 16));
+        tot[0] = fmaf(fa, d[0], tot[0]);
+        tot[1] = fmaf(fa, d[1], tot[1]);
+        tot[2] = fmaf(fb, d[2], tot[2]);
+        tot[3] = fmaf(fb, d[3], tot[3]);
       }
-      sc = *reinterpret_cast<const uint2*>(sA + kGvOffS + row * 8);
     } else {
-      // two boxes of 32 row pairs x 128 K bytes, 128-byte swizzle
-      const int pr = (row & 63) >> 1;
-      const uint8_t* rowp = sA + (row >> 6) * 4096 + pr * 128;
+      // boxes (row block, K half) of 32 row pairs x 128 K bytes, 128-byte swizzle
+      const int prA = (rowA & 63) >> 1, prB = (rowB & 63) >> 1;
+      const uint8_t* pA = sA + ((rowA >> 6) * 2 + kh) * 4096 + prA * 128;
+      const uint8_t* pB = sA + ((rowB >> 6) * 2 + kh) * 4096 + prB * 128;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const uint4 v = *reinterpret_cast<const uint4*>(rowp + (((4 * khalf + c) ^ (pr & 7)) << 4));
-        wd[4 * c + 0] = v.x;
-        wd[4 * c + 1] = v.y;
-        wd[4 * c + 2] = v.z;
-        wd[4 * c + 3] = v.w;
+      for (int m = 0; m < 2; ++m) {
+        const int jj = 4 * m + t;  // 16-K chunk of the K half
+        const uint4 ca = *reinterpret_cast<const uint4*>(pA + ((jj ^ (prA & 7)) << 4));
+        const uint4 cb = *reinterpret_cast<const uint4*>(pB + ((jj ^ (prB & 7)) << 4));
+        // activations of the chunk: K 128 kh + 16 jj .. + 15 of route g
+        const uint8_t* xp = sXr + (8 * kh + jj) * 32;
+        const uint4 x0 = *reinterpret_cast<const uint4*>(xp);
+        const uint4 x1 = *reinterpret_cast<const uint4*>(xp + 16);
+        const uint32_t wa[4] = {ca.x, ca.y, ca.z, ca.w}, wb[4] = {cb.x, cb.y, cb.z, cb.w};
+        const uint32_t xb[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const uint32_t a = wa[i] >> pc_shift, b = wb[i] >> pc_shift;
+          // word i = K 4i .. 4i + 3: code pairs (k0, k2), (k1, k3); activations likewise
+          mma_16816<DT>(tot, code_pair<DT>(a), code_pair<DT>(b), code_pair<DT>(a >> 8), code_pair<DT>(b >> 8),
+                        __byte_perm(xb[2 * i], xb[2 * i + 1], 0x5410),
+                        __byte_perm(xb[2 * i], xb[2 * i + 1], 0x7632));
+        }
       }
     }
-#pragma unroll
-    for (int g = 0; g < 2; ++g) {
-      uint32_t q[16];
-      if (SCALE == SCALE_GROUP) {
-        const uint32_t kLoMask = 0x000F000Fu, kLoMagic = 0x64086408u;  // 1024 + (n ^ 8); 1032
-        const uint32_t kHiMask = 0x00F000F0u, kHiMagic = 0x64806480u;  // 1024 + 16 (n ^ 8); 1152
-#pragma unroll
-        for (int v = 0; v < 4; ++v) {
-          const uint32_t wv = wd[4 * g + v];
-          const uint32_t w8 = wv >> 8;
-          q[4 * v + 0] = hsub2_bits(lop3_and_xor(wv, kLoMask, kLoMagic), kLoMagic);
-          q[4 * v + 1] = hsub2_bits(lop3_and_xor(wv, kHiMask, kHiMagic), kHiMagic);
-          q[4 * v + 2] = hsub2_bits(lop3_and_xor(w8, kLoMask, kLoMagic), kLoMagic);
-          q[4 * v + 3] = hsub2_bits(lop3_and_xor(w8, kHiMask, kHiMagic), kHiMagic);
-        }
-      } else {
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const uint32_t wv = wd[8 * g + j];
-          q[2 * j + 0] = hsub2_bits(lop3_and_xor(wv, pc_mask, pc_magic), pc_magic);
-          q[2 * j + 1] = hsub2_bits(lop3_and_xor(wv >> 8, pc_mask, pc_magic), pc_magic);
-        }
-      }
-      // group scale, BF16 -> FP32 exactly (per-channel: applied in the epilogue)
-      float sg = 1.0f;
-      if (SCALE == SCALE_GROUP) {
-        const int grp = 2 * khalf + g;
-        const uint32_t sword = (grp < 2) ? sc.x : sc.y;
-        sg = __uint_as_float((grp & 1) ? (sword & 0xFFFF0000u) : (sword << 16));
-      }
-#pragma unroll
-      for (int r = 0; r < R; ++r) {
-        const uint8_t* xr = sX + r * kGvRouteBytes + g * 64;
-        __half2 h0 = __float2half2_rn(0.0f), h1 = h0;
-#pragma unroll
-        for (int v = 0; v < 4; ++v) {
-          const uint4 xv = *reinterpret_cast<const uint4*>(xr + v * 16);
-          h0 = __hfma2(h2_of(q[4 * v + 0]), h2_of(xv.x), h0);
-          h1 = __hfma2(h2_of(q[4 * v + 1]), h2_of(xv.y), h1);
-          h0 = __hfma2(h2_of(q[4 * v + 2]), h2_of(xv.z), h0);
-          h1 = __hfma2(h2_of(q[4 * v + 3]), h2_of(xv.w), h1);
-        }
-        const float2 f = __half22float2(__hadd2(h0, h1));
-        acc[r] = fmaf(sg, f.x + f.y, acc[r]);
-      }
-    }
-#pragma unroll
-    for (int r = 0; r < R; ++r) tot[r] = fmaf(sInv[r], acc[r], tot[r]);
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[st]);
     ring_next(st, ph);
   }
 
   // ---------------------------------------------------------------- epilogue
-  // the two K halves of a row: lanes l and l ^ 16
-#pragma unroll
-  for (int r = 0; r < R; ++r) tot[r] += __shfl_xor_sync(0xFFFFFFFFu, tot[r], 16);
-  int r0, r1;
-  tile_row_bases<WHICH>(p, w.nt, r0, r1);
-  const int grow = row < 64 ? r0 + row : r1 + (row - 64);  // weight row in the expert
-  const bool row_ok = gated ? (64 * w.nt + (row & 63)) < p.inter : grow < N1;
-  float scale = 1.0f;
-  if (SCALE == SCALE_CHANNEL) {
-    if (row_ok) scale = bf16_bits_to_float(p.scales[static_cast<int64_t>(e) * N1 + grow]);
-    if (row & 1) scale *= 0.0625f;  // odd rows were accumulated as 16 q
-  }
-  const bool writer = khalf == 0;
   auto epi_sync = [&]() -> bool {
     __syncwarp();
     if (lane == 0) mbar_arrive(epibar);
@@ -215,79 +248,116 @@ __device__ __forceinline__ bool gemv_unit(const GemmParams& p, uint8_t* smem, ui
     ++eph;
     return ok;
   };
+  // K halves meet: the second half's warps leave their sums in one of two
+  // buffers (alternating per unit: a buffer is rewritten only after every warp
+  // passed the next barrier, i.e. after the first half read it).
+  float4* rbuf = reinterpret_cast<float4*>(red) + ((eph & 1) * 8 + rb) * 32 + lane;
+  if (kh == 1) *rbuf = make_float4(tot[0], tot[1], tot[2], tot[3]);
+  if (!epi_sync()) return false;
+  const bool fin = kh == 0;  // the first half finishes the unit
+  if (fin) {
+    const float4 o = *rbuf;
+    tot[0] += o.x;
+    tot[1] += o.y;
+    tot[2] += o.z;
+    tot[3] += o.w;
+  }
+  int r0, r1;
+  tile_row_bases<WHICH>(p, w.nt, r0, r1);
+  const int growA = rowA < 64 ? r0 + rowA : r1 + (rowA - 64);  // weight rows in the expert
+  const int growB = rowB < 64 ? r0 + rowB : r1 + (rowB - 64);
+  const bool okA = gated ? (64 * w.nt + (rowA & 63)) < p.inter : growA < N1;
+  const bool okB = gated ? okA : growB < N1;
+  float scA = 1.0f, scB = 1.0f;
+  if (SCALE == SCALE_CHANNEL) {
+    if (okA) scA = bf16_bits_to_float(p.scales[static_cast<int64_t>(e) * N1 + growA]);
+    if (okB) scB = bf16_bits_to_float(p.scales[static_cast<int64_t>(e) * N1 + growB]);
+  }
+  const float vA0 = tot[0] * scA, vA1 = tot[1] * scA, vB0 = tot[2] * scB, vB1 = tot[3] * scB;
+  const int rt0 = 2 * t, rt1 = 2 * t + 1;  // this lane's routes
 
   if (WHICH == GEMM_DOWN) {
-    float* y = reinterpret_cast<float*>(p.out) +
-               (static_cast<int64_t>(w.split) * p.slots_cap + m0) * p.out_cols + grow;
-#pragma unroll
-    for (int r = 0; r < R; ++r)
-      if (writer && r < rows && row_ok) y[static_cast<int64_t>(r) * p.out_cols] = tot[r] * scale;
+    if (fin) {
+      float* y = reinterpret_cast<float*>(p.out) + (static_cast<int64_t>(w.split) * p.slots_cap + m0) * p.out_cols;
+      const int64_t oc = p.out_cols;
+      if (rt0 < rows && okA) y[rt0 * oc + growA] = vA0;
+      if (rt1 < rows && okA) y[rt1 * oc + growA] = vA1;
+      if (rt0 < rows && okB) y[rt0 * oc + growB] = vB0;
+      if (rt1 < rows && okB) y[rt1 * oc + growB] = vB1;
+    }
     return true;
   }
 
   uint16_t* inter = reinterpret_cast<uint16_t*>(p.out) + static_cast<int64_t>(m0) * p.inter;
   if (p.splits > 1) {
-    float* part = p.part + (static_cast<int64_t>(w.split) * p.slots_cap + m0) * N1 + grow;
-#pragma unroll
-    for (int r = 0; r < R; ++r)
-      if (writer && r < rows && row_ok) part[static_cast<int64_t>(r) * N1] = tot[r] * scale;
+    if (fin) {
+      float* part = p.part + (static_cast<int64_t>(w.split) * p.slots_cap + m0) * N1;
+      if (rt0 < rows && okA) part[static_cast<int64_t>(rt0) * N1 + growA] = vA0;
+      if (rt1 < rows && okA) part[static_cast<int64_t>(rt1) * N1 + growA] = vA1;
+      if (rt0 < rows && okB) part[static_cast<int64_t>(rt0) * N1 + growB] = vB0;
+      if (rt1 < rows && okB) part[static_cast<int64_t>(rt1) * N1 + growB] = vB1;
+    }
     // The last split to finish sums the partials in split order
     // (deterministic) and applies the activation.
     __threadfence();
     if (!epi_sync()) return false;
-    if (cw == 0 && lane == 0) {
+    if (rb == 0 && kh == 0 && lane == 0) {
       const int prev = atomicAdd(&p.counters[w.tile * p.n_tiles + w.nt], 1);
       *fixup_flag = (prev == p.splits - 1) ? 1 : 0;
     }
     if (!epi_sync()) return false;
-    if (*fixup_flag) {
+    const bool last = *fixup_flag != 0;
+    if (last && fin) {
       __threadfence();
       const int64_t sstride = p.slots_cap * static_cast<int64_t>(N1);
-      if (gated) {
-        const int i = 64 * w.nt + 8 * cw + lane;
-        if (lane < 8 && i < p.inter) {
-          for (int r = 0; r < rows; ++r) {
-            const float* src = p.part + static_cast<int64_t>(m0 + r) * N1;
-            float g = 0.0f, up = 0.0f;
+      // lanes t take routes t and t + 4 of their rows
+      for (int r = t; r < rows; r += 4) {
+        const float* src = p.part + static_cast<int64_t>(m0 + r) * N1;
+        if (gated) {
+          const int i = 64 * w.nt + (rowA & 63);
+          if (okA) {
+            float gs = 0.0f, us = 0.0f;
             for (int s = 0; s < p.splits; ++s) {
-              g += __ldcg(src + s * sstride + i);
-              up += __ldcg(src + s * sstride + p.inter + i);
+              gs += __ldcg(src + s * sstride + i);
+              us += __ldcg(src + s * sstride + p.inter + i);
             }
-            inter[static_cast<int64_t>(r) * p.inter + i] = T::from_float(silu_f(g) * up);
+            inter[static_cast<int64_t>(r) * p.inter + i] = T::from_float(silu_f(gs) * us);
+          }
+        } else {
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int gr = h ? growB : growA;
+            if (h ? okB : okA) {
+              float hs = 0.0f;
+              for (int s = 0; s < p.splits; ++s) hs += __ldcg(src + s * sstride + gr);
+              const float a = hs > 0.0f ? hs : 0.0f;
+              inter[static_cast<int64_t>(r) * p.inter + gr] = T::from_float(a * a);
+            }
           }
         }
-      } else if (writer && row_ok) {
-        for (int r = 0; r < rows; ++r) {
-          const float* src = p.part + static_cast<int64_t>(m0 + r) * N1 + grow;
-          float h = 0.0f;
-          for (int s = 0; s < p.splits; ++s) h += __ldcg(src + s * sstride);
-          const float a = h > 0.0f ? h : 0.0f;
-          inter[static_cast<int64_t>(r) * p.inter + grow] = T::from_float(a * a);
-        }
       }
-      if (cw == 0 && lane == 0) p.counters[w.tile * p.n_tiles + w.nt] = 0;
     }
+    if (last && rb == 0 && kh == 0 && lane == 0) p.counters[w.tile * p.n_tiles + w.nt] = 0;
     return true;
   }
 
-  if (gated) {
-    // lanes 0..7: gate rows; lanes 8..15: the matching up rows
-#pragma unroll
-    for (int r = 0; r < R; ++r) {
-      const float v = tot[r] * scale;
-      const float up = __shfl_xor_sync(0xFFFFFFFFu, v, 8);
-      const int i = 64 * w.nt + 8 * cw + (lane & 7);
-      if (lane < 8 && r < rows && i < p.inter)
-        inter[static_cast<int64_t>(r) * p.inter + i] = T::from_float(silu_f(v) * up);
-    }
-  } else {
-#pragma unroll
-    for (int r = 0; r < R; ++r) {
-      if (writer && r < rows && row_ok) {
-        const float h = tot[r] * scale;
-        const float a = h > 0.0f ? h : 0.0f;
-        inter[static_cast<int64_t>(r) * p.inter + grow] = T::from_float(a * a);
+  if (fin) {
+    if (gated) {
+      // rowA = gate row, rowB = its up row (same intermediate index)
+      const int i = 64 * w.nt + (rowA & 63);
+      if (okA) {
+        if (rt0 < rows) inter[static_cast<int64_t>(rt0) * p.inter + i] = T::from_float(silu_f(vA0) * vB0);
+        if (rt1 < rows) inter[static_cast<int64_t>(rt1) * p.inter + i] = T::from_float(silu_f(vA1) * vB1);
       }
+    } else {
+      auto relu2 = [](float h) {
+        const float a = h > 0.0f ? h : 0.0f;
+        return a * a;
+      };
+      if (rt0 < rows && okA) inter[static_cast<int64_t>(rt0) * p.inter + growA] = T::from_float(relu2(vA0));
+      if (rt1 < rows && okA) inter[static_cast<int64_t>(rt1) * p.inter + growA] = T::from_float(relu2(vA1));
+      if (rt0 < rows && okB) inter[static_cast<int64_t>(rt0) * p.inter + growB] = T::from_float(relu2(vB0));
+      if (rt1 < rows && okB) inter[static_cast<int64_t>(rt1) * p.inter + growB] = T::from_float(relu2(vB1));
     }
   }
   return true;
@@ -295,7 +365,8 @@ __device__ __forceinline__ bool gemv_unit(const GemmParams& p, uint8_t* smem, ui
 
 template <int WHICH, int SCALE, int DT>
 __global__ void __launch_bounds__(kGemvThreads, 1)
-    w4a16_gemv_kernel(const __grid_constant__ GemmParams p, const __grid_constant__ CUtensorMap tmA) {
+    w4a16_gemv_kernel(const __grid_constant__ GemmParams p, const __grid_constant__ CUtensorMap tmA,
+                      const __grid_constant__ CUtensorMap tmS) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* ctrl = smem + kGemvStages * kGemvStageBytes;
@@ -305,61 +376,76 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
   uint64_t* epibar = empty + kGemvStages;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(epibar + 1);
   volatile int* fixup_flag = abort_flag + 1;
-  int* stage_rows = reinterpret_cast<int*>(epibar + 2);  // [kGemvStages], staging warp only
+  float* red = reinterpret_cast<float*>(ctrl + kGvCtrlRedOff);
+  int4* tile_tab = reinterpret_cast<int4*>(ctrl + kGvCtrlTabOff);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kGemvStages; ++s) {
-      mbar_init(&full[s], 1);    // producer (TMA bytes + scale copies)
-      mbar_init(&bfull[s], 1);   // staging warp
-      mbar_init(&empty[s], 8);   // compute warps
+      mbar_init(&full[s], 1);                  // producer (TMA bytes + scale copies)
+      mbar_init(&bfull[s], 32);                // the 32 lanes' activation copies
+      mbar_init(&empty[s], kGemvComputeWarps);
     }
-    mbar_init(epibar, 8);
+    mbar_init(epibar, kGemvComputeWarps);
     *abort_flag = 0;
     *fixup_flag = 0;
     fence_barrier_init();
   }
-  if (warp == 0 && lane == 0) tma_prefetch_desc(&tmA);
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    if (p.scale_tma) tma_prefetch_desc(&tmS);
+  }
   __syncthreads();
 
   // Everything below reads what the previous kernels wrote.
   pdl_wait();
   pdl_launch_dependents();
 
-  const int4 first_ti = load_tile(p, blockIdx.x);
+  // Tile records of this CTA's units blockIdx.x + i * gridDim.x, i < kGemvTileTab,
+  // one per thread, loaded together with the tile count (indices clamped to
+  // the list's capacity; records past the count are never used).
+  if (threadIdx.x < kGemvTileTab) {
+    const int64_t u = blockIdx.x + static_cast<int64_t>(threadIdx.x) * gridDim.x;
+    const int64_t t = min(u / (p.splits * p.n_tiles), static_cast<int64_t>(p.tiles_cap - 1));
+    tile_tab[threadIdx.x] = p.tiles[t];
+  }
   const int n_units = (*p.num_tiles) * p.n_tiles * p.splits;
   const int N1 = p.n_rows;
+  __syncthreads();
 
   if (warp == 0) {
     // ------------------------------------------------------------------ producer
     const uint64_t pol_w = l2_policy_evict_first();
+    const uint64_t pol_s = l2_policy_evict_last();  // each scale sector serves two stages
     const int groups_row = p.K / kGroup;
     const int sbytes_row = groups_row * 2;
     int st = 0;
     uint32_t ph = 0, issued = 0;
     bool ok = true;
-    int4 ti_next = first_ti;
-    for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-      const Unit w = decode_unit(p, u);
-      const int4 ti = ti_next;
-      if (u + (int)gridDim.x < n_units) ti_next = load_tile(p, u + gridDim.x);
+    UnitIter it;
+    it.init(p);
+    for (int i = 0; it.u < n_units && ok; it.next(p), ++i) {
+      const Unit w = it.unit(p);
+      const int4 ti = tile_of(p, tile_tab, i, it.u);
       if (w.kb1 <= w.kb0) continue;
       const int e = ti.x;
       int r0, r1;
       tile_row_bases<WHICH>(p, w.nt, r0, r1);
+      // scale rows of this unit for this lane's tile rows (lane + 32 i); null
+      // when the row lies beyond the expert's rows
       const uint8_t* srow[4];
-      bool srow_al8 = true;
-      if (SCALE == SCALE_GROUP) {
+      bool srow_al16 = true;
+      if (SCALE == SCALE_GROUP && !p.scale_tma) {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int tr = lane + 32 * i;
+        for (int j = 0; j < 4; ++j) {
+          const int tr = lane + 32 * j;
           const int grow = tr < 64 ? r0 + tr : r1 + (tr - 64);
-          srow[i] = grow < N1 ? reinterpret_cast<const uint8_t*>(p.scales) +
+          srow[j] = grow < N1 ? reinterpret_cast<const uint8_t*>(p.scales) +
                                     (static_cast<int64_t>(e) * N1 + grow) * sbytes_row
                               : nullptr;
-          srow_al8 = srow_al8 && ((reinterpret_cast<uintptr_t>(srow[i]) & 7) == 0);
+          srow_al16 = srow_al16 && ((reinterpret_cast<uintptr_t>(srow[j]) & 15) == 0);
         }
       }
       for (int kb = w.kb0; kb < w.kb1; ++kb) {
@@ -369,38 +455,49 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
         }
         uint8_t* sA = smem + st * kGemvStageBytes;
         uint8_t* sS = sA + kGvOffS;
-        if (SCALE == SCALE_GROUP) {
-          const int g0 = kb * kGroupsPerStage;
-          const int ng = min(kGroupsPerStage, groups_row - g0);
-          if (srow_al8 && ng == kGroupsPerStage) {
+        if (SCALE == SCALE_GROUP && !p.scale_tma) {
+          // the stage's 8 group scales (16 bytes) of each tile row
+          const int g0 = kb * (kGemvBlockK / kGroup);
+          const int ng = min(kGemvBlockK / kGroup, groups_row - g0);
+          if (srow_al16 && ng == kGemvBlockK / kGroup) {
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              uint8_t* dst = sS + (lane + 32 * i) * 8;
-              if (srow[i]) cp_async<8>(dst, srow[i] + g0 * 2);
-              else *reinterpret_cast<uint2*>(dst) = make_uint2(0, 0);
+            for (int j = 0; j < 4; ++j) {
+              uint8_t* dst = sS + (lane + 32 * j) * kGvScaleRowBytes;
+              if (srow[j]) cp_async_cg16(dst, srow[j] + g0 * 2, 16u);
+              else *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
             }
           } else {
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              uint8_t* dst = sS + (lane + 32 * i) * 8;
-              const int nbytes = srow[i] ? max(ng, 0) * 2 : 0;
-              for (int o = 0; o < nbytes; o += 4) cp_async<4>(dst + o, srow[i] + g0 * 2 + o);
-              for (int o = nbytes; o < 8; o += 4) *reinterpret_cast<uint32_t*>(dst + o) = 0u;
+            for (int j = 0; j < 4; ++j) {
+              uint8_t* dst = sS + (lane + 32 * j) * kGvScaleRowBytes;
+              const int nbytes = srow[j] ? max(ng, 0) * 2 : 0;
+              for (int o = 0; o < nbytes; o += 4) cp_async<4>(dst + o, srow[j] + g0 * 2 + o);
+              for (int o = nbytes; o < kGvScaleRowBytes; o += 4) *reinterpret_cast<uint32_t*>(dst + o) = 0u;
             }
           }
           cp_async_mbar_arrive(&full[st]);
         }
         __syncwarp();
         if (lane == 0) {
-          mbar_arrive_expect_tx(&full[st], kStageA);
+          const bool stma = SCALE == SCALE_GROUP && p.scale_tma;
+          mbar_arrive_expect_tx(&full[st], kGvWeightBytes + (stma ? kTileRows * kGvScaleRowBytes : 0));
           if (SCALE == SCALE_GROUP) {
-            // two 64-row boxes of 64 packed bytes (128 K values), 64-byte swizzle
-            tma_load_3d(sA, &tmA, &full[st], kb * (kBlockK / 2), r0, e, pol_w);
-            tma_load_3d(sA + 4096, &tmA, &full[st], kb * (kBlockK / 2), r1, e, pol_w);
+            // two 64-row boxes of 128 packed bytes (256 K values)
+            tma_load_3d(sA, &tmA, &full[st], kb * (kGemvBlockK / 2), r0, e, pol_w);
+            tma_load_3d(sA + 8192, &tmA, &full[st], kb * (kGemvBlockK / 2), r1, e, pol_w);
+            if (stma) {
+              // two 64-row boxes of the stage's 8 BF16 scales
+              tma_load_3d(sS, &tmS, &full[st], kb * (kGemvBlockK / kGroup), r0, e, pol_s);
+              tma_load_3d(sS + 64 * kGvScaleRowBytes, &tmS, &full[st], kb * (kGemvBlockK / kGroup), r1, e, pol_s);
+            }
           } else {
-            // two boxes of 32 row pairs x 128 K bytes, 128-byte swizzle
-            tma_load_3d(sA, &tmA, &full[st], kb * kBlockK, r0 / 2, e, pol_w);
-            tma_load_3d(sA + 4096, &tmA, &full[st], kb * kBlockK, r1 / 2, e, pol_w);
+            // (row block, K half) boxes of 32 row pairs x 128 K bytes
+#pragma unroll
+            for (int b = 0; b < 2; ++b)
+#pragma unroll
+              for (int h = 0; h < 2; ++h)
+                tma_load_3d(sA + (b * 2 + h) * 4096, &tmA, &full[st], kb * kGemvBlockK + h * 128,
+                            (b ? r1 : r0) / 2, e, pol_w);
           }
         }
         __syncwarp();
@@ -416,156 +513,87 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
         mbar_wait(&full[j % kGemvStages], (j / kGemvStages) & 1, &no_abort, p.err);
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------------ activation staging
-    // Lanes 0-15 stage route 2i, lanes 16-31 route 2i + 1, 8 K values (16 B)
-    // per lane.  Copies land by cp.async; kGemvLag stages later each lane
-    // converts what it copied itself (so only its own copies need waiting
-    // for), and lane 0 publishes bfull.
+    // ------------------------------------------------------------------ activation rows
+    // One route row per pass, 8 K values (16 B) per lane, straight from x (by
+    // token) or the intermediate (by slot) with cp.async; out-of-range K is
+    // zero-filled by the copy.  Each lane's cp.async.mbarrier.arrive marks the
+    // stage's bfull once its copies have landed; the warp never blocks on them.
     const uint16_t* xsrc = reinterpret_cast<const uint16_t*>(p.x);
-    const int hr = lane >> 4, l16 = lane & 15;
-    int st = 0, cst = 0;
-    uint32_t ph = 0, pending = 0;
+    int st = 0;
+    uint32_t ph = 0;
     bool ok = true;
-    auto convert = [&]() {
-      const int rows = stage_rows[cst];
-      const uint8_t* raw = smem + cst * kGemvStageBytes + kGvOffRaw;
-      uint8_t* xh = smem + cst * kGemvStageBytes + kGvOffX;
-      float* inv = reinterpret_cast<float*>(smem + cst * kGemvStageBytes + kGvOffInv);
-      for (int rp = 0; rp < rows; rp += 2) {
-        const int r = rp + hr;
-        float v[8];
-        if (r < rows) {
-          const uint4 b = *reinterpret_cast<const uint4*>(raw + r * kStageBRow + l16 * 16);
-          const uint32_t bw[4] = {b.x, b.y, b.z, b.w};
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            float2 f;
-            if (DT == DT_BF16) f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&bw[i]));
-            else f = __half22float2(*reinterpret_cast<const __half2*>(&bw[i]));
-            v[2 * i] = f.x;
-            v[2 * i + 1] = f.y;
-          }
-        } else {
-#pragma unroll
-          for (int i = 0; i < 8; ++i) v[i] = 0.0f;
-        }
-        float m = 0.0f;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(v[i]));
-        // largest magnitude of the route pair (the bit patterns of non-negative
-        // floats order like the values)
-        const uint32_t mb = __reduce_max_sync(0xFFFFFFFFu, __float_as_uint(m));
-        const int ex = static_cast<int>((mb >> 23) & 0xFFu);
-        // 2^s puts the maximum in [2^6, 2^7) (group) or [2^2, 2^3) (per-channel)
-        int s = (ex == 0 || ex == 255) ? 0 : ((SCALE == SCALE_GROUP ? 133 : 129) - ex);
-        s = max(-100, min(100, s));
-        const float sc = __uint_as_float(static_cast<uint32_t>(s + 127) << 23);
-        uint4 o;
-        if (SCALE == SCALE_GROUP) {
-          // (x0, x4), (x1, x5) / 16, (x2, x6), (x3, x7) / 16
-          const float sc16 = sc * 0.0625f;
-          o.x = f2_to_h2_bits(v[0] * sc, v[4] * sc);
-          o.y = f2_to_h2_bits(v[1] * sc16, v[5] * sc16);
-          o.z = f2_to_h2_bits(v[2] * sc, v[6] * sc);
-          o.w = f2_to_h2_bits(v[3] * sc16, v[7] * sc16);
-        } else {
-          // (x0, x2), (x1, x3), (x4, x6), (x5, x7)
-          o.x = f2_to_h2_bits(v[0] * sc, v[2] * sc);
-          o.y = f2_to_h2_bits(v[1] * sc, v[3] * sc);
-          o.z = f2_to_h2_bits(v[4] * sc, v[6] * sc);
-          o.w = f2_to_h2_bits(v[5] * sc, v[7] * sc);
-        }
-        if (r < rows) {
-          *reinterpret_cast<uint4*>(xh + r * kGvRouteBytes + (l16 >> 3) * kGvHalfBytes + (l16 & 7) * 16) = o;
-          if (l16 == 0) inv[r] = __uint_as_float(static_cast<uint32_t>(127 - s) << 23);
-        }
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bfull[cst]);
-      if (++cst == kGemvStages) cst = 0;
-      --pending;
-    };
-    int4 ti_next = first_ti;
-    for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-      const Unit w = decode_unit(p, u);
-      const int4 ti = ti_next;
-      if (u + (int)gridDim.x < n_units) ti_next = load_tile(p, u + gridDim.x);
-      if (w.kb1 <= w.kb0) continue;
-      const int m0 = ti.y, rows = min(ti.z, kGemvMaxR);
-      // source row of route `lane` (lanes below rows)
+    // source row of route `lane` of a tile (lanes below its route count)
+    auto src_of = [&](const int4& t) -> int {
       int src = 0;
-      if (lane < rows) {
+      if (lane < min(t.z, kGemvMaxR)) {
         if (WHICH == GEMM_UP) {
-          const int route = p.perm[m0 + lane];
+          const int route = p.perm[t.y + lane];
           src = route >= 0 ? route / p.top_k : 0;
         } else {
-          src = m0 + lane;
+          src = t.y + lane;
         }
       }
+      return src;
+    };
+    int src_next = static_cast<int>(blockIdx.x) < n_units ? src_of(tile_tab[0]) : 0;
+    UnitIter it;
+    it.init(p);
+    for (int i = 0; it.u < n_units && ok; it.next(p), ++i) {
+      const int u = it.u;
+      const Unit w = it.unit(p);
+      const int4 ti = tile_of(p, tile_tab, i, u);
+      const int src = src_next;
+      const int rows = min(ti.z, kGemvMaxR);
       for (int kb = w.kb0; kb < w.kb1; ++kb) {
         if (!mbar_wait(&empty[st], ph ^ 1u, abort_flag, p.err)) {
           ok = false;
           break;
         }
-        if (lane == 0) stage_rows[st] = rows;
-        uint8_t* raw = smem + st * kGemvStageBytes + kGvOffRaw;
-        const int col = kb * kBlockK + l16 * 8;
+        uint8_t* xs = smem + st * kGemvStageBytes + kGvOffX;
+        const int col = kb * kGemvBlockK + lane * 8;
         const bool valid = col < p.K;
-        for (int rp = 0; rp < rows; rp += 2) {
-          const int r = rp + hr;
-          const int srow = __shfl_sync(0xFFFFFFFFu, src, r & 31);
-          if (r < rows)
-            cp_async_cg16(raw + r * kStageBRow + l16 * 16,
-                          xsrc + static_cast<int64_t>(srow) * p.K + (valid ? col : 0), valid ? 16u : 0u);
+        for (int r = 0; r < rows; ++r) {
+          const int srow = __shfl_sync(0xFFFFFFFFu, src, r);
+          cp_async_cg16(xs + r * kGvRouteBytes + lane * 16,
+                        xsrc + static_cast<int64_t>(srow) * p.K + (valid ? col : 0), valid ? 16u : 0u);
         }
-        asm volatile("cp.async.commit_group;" ::: "memory");
-        __syncwarp();
-        ++pending;
+        cp_async_mbar_arrive_noinc(&bfull[st]);
         ring_next(st, ph);
-        if (pending > static_cast<uint32_t>(kGemvLag)) {
-          asm volatile("cp.async.wait_group %0;" ::"n"(kGemvLag) : "memory");
-          __syncwarp();
-          convert();
-        }
       }
+      // the next unit's source rows, loaded while this unit streams
+      const int u_next = u + static_cast<int>(gridDim.x);
+      if (u_next < n_units) src_next = src_of(tile_of(p, tile_tab, i + 1, u_next));
     }
+    // Every copy lands before the CTA exits (bounded by the compute warps'
+    // waits on bfull; the final barrier below follows them).
     asm volatile("cp.async.wait_all;" ::: "memory");
-    __syncwarp();
-    while (ok && pending > 0) convert();
   } else {
     // ------------------------------------------------------------------ compute + epilogue
-    const int cw = warp - 2;
-    const int l16 = lane & 15;
+    // warp 2 + c: row block rb = c % 8 (16 MMA rows), K half kh = c / 8
+    const int cw = warp - 2, rb = cw & 7, kh = cw >> 3, g = lane >> 2;
     const bool gated = (WHICH == GEMM_UP && p.act == ACT_SWIGLU);
-    const int row = gated ? ((l16 >> 3) * 64 + 8 * cw + (l16 & 7)) : (16 * cw + l16);
+    // SwiGLU: MMA row g = gate row, g + 8 = its up row; otherwise 16 consecutive rows
+    const int rowA = gated ? 8 * rb + g : 16 * rb + g;
+    const int rowB = gated ? 64 + 8 * rb + g : 16 * rb + 8 + g;
     int st = 0;
     uint32_t ph = 0, eph = 0;
-    int4 ti_next = first_ti;
-    for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
-      const Unit w = decode_unit(p, u);
-      const int4 ti = ti_next;
-      if (u + (int)gridDim.x < n_units) ti_next = load_tile(p, u + gridDim.x);
-      const int e = ti.x, m0 = ti.y, rows = min(ti.z, kGemvMaxR);
-      bool ok;
-#define W4A16_GEMV_UNIT(RR)                                                                     \
-  gemv_unit<WHICH, SCALE, DT, RR>(p, smem, full, bfull, empty, epibar, abort_flag, fixup_flag, \
-                                  w, e, m0, rows, row, cw, lane, st, ph, eph)
-      if (rows <= 1) ok = W4A16_GEMV_UNIT(1);
-      else if (rows <= 2) ok = W4A16_GEMV_UNIT(2);
-      else if (rows <= 3) ok = W4A16_GEMV_UNIT(3);
-      else if (rows <= 4) ok = W4A16_GEMV_UNIT(4);
-      else if (rows <= 8) ok = W4A16_GEMV_UNIT(8);
-      else ok = W4A16_GEMV_UNIT(16);
-#undef W4A16_GEMV_UNIT
-      if (!ok) break;
+    UnitIter it;
+    it.init(p);
+    for (int i = 0; it.u < n_units; it.next(p), ++i) {
+      const Unit w = it.unit(p);
+      const int4 ti = tile_of(p, tile_tab, i, it.u);
+      const int rows = min(ti.z, kGemvMaxR);
+      if (!gemv_unit<WHICH, SCALE, DT>(p, smem, full, bfull, empty, epibar, abort_flag, fixup_flag, red, w,
+                                       ti.x, ti.y, rows, rowA, rowB, rb, kh, lane, st, ph, eph))
+        break;
     }
   }
   __syncthreads();
 }
 
 template <int WHICH, int SCALE, int DT>
-cudaError_t launch_gemv_one(const GemmParams& p, const CUtensorMap& tmA, int grid, cudaStream_t s,
-                            bool pdl) {
+cudaError_t launch_gemv_one(const GemmParams& p, const CUtensorMap& tmA, const CUtensorMap& tmS, int grid,
+                            cudaStream_t s, bool pdl) {
   auto kern = w4a16_gemv_kernel<WHICH, SCALE, DT>;
   const int smem_bytes = gemv_smem_bytes();
   int dev = 0;
@@ -587,18 +615,18 @@ cudaError_t launch_gemv_one(const GemmParams& p, const CUtensorMap& tmA, int gri
   attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, p, tmA);
+  return cudaLaunchKernelEx(&cfg, kern, p, tmA, tmS);
 }
 
 template <int DT>
 cudaError_t launch_gemv_dt(int which, int scale_kind, const GemmParams& p, const CUtensorMap& tmA,
-                           int grid, cudaStream_t s, bool pdl) {
+                           const CUtensorMap& tmS, int grid, cudaStream_t s, bool pdl) {
   if (which == GEMM_UP) {
-    return scale_kind == SCALE_GROUP ? launch_gemv_one<GEMM_UP, SCALE_GROUP, DT>(p, tmA, grid, s, pdl)
-                                     : launch_gemv_one<GEMM_UP, SCALE_CHANNEL, DT>(p, tmA, grid, s, pdl);
+    return scale_kind == SCALE_GROUP ? launch_gemv_one<GEMM_UP, SCALE_GROUP, DT>(p, tmA, tmS, grid, s, pdl)
+                                     : launch_gemv_one<GEMM_UP, SCALE_CHANNEL, DT>(p, tmA, tmS, grid, s, pdl);
   }
-  return scale_kind == SCALE_GROUP ? launch_gemv_one<GEMM_DOWN, SCALE_GROUP, DT>(p, tmA, grid, s, pdl)
-                                   : launch_gemv_one<GEMM_DOWN, SCALE_CHANNEL, DT>(p, tmA, grid, s, pdl);
+  return scale_kind == SCALE_GROUP ? launch_gemv_one<GEMM_DOWN, SCALE_GROUP, DT>(p, tmA, tmS, grid, s, pdl)
+                                   : launch_gemv_one<GEMM_DOWN, SCALE_CHANNEL, DT>(p, tmA, tmS, grid, s, pdl);
 }
 
 }  // namespace w4a16

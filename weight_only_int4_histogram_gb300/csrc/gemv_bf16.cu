@@ -2,6 +2,6 @@
 #include "gemv.cuh"
 
 namespace w4a16 {
-template cudaError_t launch_gemv_dt<DT_BF16>(int, int, const GemmParams&, const CUtensorMap&, int,
-                                               cudaStream_t, bool);
+template cudaError_t launch_gemv_dt<DT_BF16>(int, int, const GemmParams&, const CUtensorMap&,
+                                               const CUtensorMap&, int, cudaStream_t, bool);
 }
