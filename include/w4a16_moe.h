@@ -71,7 +71,7 @@ typedef enum { W4A16_DT_BF16 = 0, W4A16_DT_FP16 = 1 } w4a16_dtype;
 typedef enum {
   W4A16_PATH_AUTO = 0,          /* planner's choice per batch size */
   W4A16_PATH_TENSOR_CORES = 1,  /* tcgen05 MMA on dequantised tiles */
-  W4A16_PATH_CUDA_CORES = 2     /* FP16 FMA GEMV, route tiles of <= 16 routes */
+  W4A16_PATH_CUDA_CORES = 2     /* warp-MMA GEMV, route tiles of <= 8 routes */
 } w4a16_gemm_path;
 
 /*
@@ -225,11 +225,12 @@ w4a16_status w4a16_moe_set_overrides(w4a16_moe_plan_t plan, int32_t tile_rows,
  * and the tensor cores above that.  Both paths compute the same function
  * (the expert MLPs of "feat(pytorch): add CuTeDSL W4A16 MoE backend"
  * (LMDeploy), section Modification); they round differently (the tensor-core
- * path rounds each dequantised weight to the activation type, the CUDA-core
- * path sums exact code x activation products in FP16 over one 32-element
- * group), so outputs of the two agree within the parity tolerance, not bit
- * for bit.  The CUDA-core path uses route tiles of 16 routes (tile_rows
- * overrides apply to the tensor-core path only).  workspace_bytes (if not
+ * path rounds each dequantised weight q * s to the activation type, the
+ * CUDA-core path multiplies the exact codes q by the activations, sums a
+ * 32-element group in FP32 and applies s to that sum), so outputs of the two
+ * agree within the parity tolerance, not bit for bit.  The CUDA-core path
+ * uses route tiles of 8 routes (tile_rows overrides apply to the tensor-core
+ * path only).  workspace_bytes (if not
  * NULL) receives the workspace size later calls need.  Unknown path:
  * W4A16_ERR_INVALID_ARG.
  */

@@ -107,30 +107,31 @@ def test_planner_tile_height_follows_route_counts(lib):
     plan, _ = _lib.w4a16_moe_plan(good_desc(num_experts=384, hidden=7168, inter=256, top_k=8,
                                             max_tokens=2048))
     bns = [_lib.w4a16_moe_route_info(plan, t).tile_rows for t in (1, 8, 32, 256, 1024, 2048)]
-    assert bns == sorted(bns) and bns[0] == 16 and bns[-1] >= 64
+    # CUDA-core GEMV tiles (8 routes) for the smallest batches, then tensor-core tiles
+    assert bns == sorted(bns) and bns[0] == 8 and bns[-1] >= 64
     s1 = [_lib.w4a16_moe_route_info(plan, t).gemm1_splits for t in (1, 2048)]
     assert s1[0] > 1 and s1[1] == 1  # split-K only for small batches
     _lib.w4a16_moe_plan_destroy(plan)
 
 
 def test_gemm_path_choice_and_validation(lib):
-    """Few routes per expert -> CUDA-core GEMV with 16-route tiles; many ->
+    """Few routes per expert -> CUDA-core GEMV with 8-route tiles; many ->
     tensor cores; forced paths hold at every batch size."""
     plan, _ = _lib.w4a16_moe_plan(good_desc(num_experts=384, hidden=7168, inter=256, top_k=8,
                                             max_tokens=2048))
     paths = {t: _lib.w4a16_moe_route_info(plan, t).gemm_path for t in (1, 32, 144, 145, 2048)}
     assert paths == {1: _lib.PATH_CUDA_CORES, 32: _lib.PATH_CUDA_CORES, 144: _lib.PATH_CUDA_CORES,
                      145: _lib.PATH_TENSOR_CORES, 2048: _lib.PATH_TENSOR_CORES}
-    assert _lib.w4a16_moe_route_info(plan, 32).tile_rows == 16
+    assert _lib.w4a16_moe_route_info(plan, 32).tile_rows == 8
     with pytest.raises(_lib.W4A16Error) as ei:
         _lib.w4a16_moe_set_gemm_path(plan, 3)
     assert ei.value.status == 1
     ws_cc = _lib.w4a16_moe_set_gemm_path(plan, _lib.PATH_CUDA_CORES)
     info = _lib.w4a16_moe_route_info(plan, 2048)
-    assert info.gemm_path == _lib.PATH_CUDA_CORES and info.tile_rows == 16
+    assert info.gemm_path == _lib.PATH_CUDA_CORES and info.tile_rows == 8
     # tile_rows overrides apply to the tensor-core path only
     _lib.w4a16_moe_set_overrides(plan, 64, 0, 0)
-    assert _lib.w4a16_moe_route_info(plan, 2048).tile_rows == 16
+    assert _lib.w4a16_moe_route_info(plan, 2048).tile_rows == 8
     _lib.w4a16_moe_set_gemm_path(plan, _lib.PATH_TENSOR_CORES)
     assert _lib.w4a16_moe_route_info(plan, 1).gemm_path == _lib.PATH_TENSOR_CORES
     assert _lib.w4a16_moe_route_info(plan, 1).tile_rows == 64
