@@ -81,6 +81,15 @@ def load_peaks():
 # ---------------------------------------------------------------------------
 
 class ClockSampler:
+    """SM clock and clock-event reasons sampled during the timed region.
+
+    Polls NVML (read-only queries through ctypes) from a background thread
+    every millisecond, so that even a timed region of a few milliseconds gets
+    samples; falls back to `nvidia-smi -lms 200` when NVML cannot be loaded.
+    Nothing here changes a GPU setting."""
+
+    REASON_BITS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+                   0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -89,8 +98,65 @@ class ClockSampler:
         self.dev = device_index
         self.proc = None
         self.tmp = None
+        self.thread = None
+        self.samples = []
+        self.reasons = set()
+        self.max_mhz = None
+        self.nvml = None
+        self.handle = None
+
+    def _open_nvml(self):
+        import ctypes
+        for name in ("libnvidia-ml.so.1", "libnvidia-ml.so"):
+            try:
+                lib = ctypes.CDLL(name)
+                break
+            except OSError:
+                lib = None
+        if lib is None or lib.nvmlInit_v2() != 0:
+            return False
+        handle = ctypes.c_void_p()
+        bus = None
+        try:
+            props = torch.cuda.get_device_properties(self.dev)
+            bus = "%08x:%02x:%02x.0" % (props.pci_domain_id, props.pci_bus_id, props.pci_device_id)
+        except Exception:
+            pass
+        ok = bus is not None and lib.nvmlDeviceGetHandleByPciBusId_v2(bus.encode(), ctypes.byref(handle)) == 0
+        if not ok and lib.nvmlDeviceGetHandleByIndex_v2(self.dev, ctypes.byref(handle)) != 0:
+            return False
+        mx = ctypes.c_uint()
+        if lib.nvmlDeviceGetMaxClockInfo(handle, 1, ctypes.byref(mx)) == 0:  # NVML_CLOCK_SM
+            self.max_mhz = float(mx.value)
+        self.reasons_fn = (getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None)
+                           or getattr(lib, "nvmlDeviceGetCurrentClocksThrottleReasons", None))
+        self.nvml, self.handle = lib, handle
+        return True
+
+    def _poll(self):
+        import ctypes
+        mhz = ctypes.c_uint()
+        rs = ctypes.c_ulonglong()
+        while not self._stop:
+            if self.nvml.nvmlDeviceGetClockInfo(self.handle, 1, ctypes.byref(mhz)) == 0:
+                self.samples.append(float(mhz.value))
+            if self.reasons_fn is not None and self.reasons_fn(self.handle, ctypes.byref(rs)) == 0:
+                for bit, name in self.REASON_BITS.items():
+                    if rs.value & bit:
+                        self.reasons.add(name)
+            time.sleep(0.001)
 
     def start(self):
+        import threading
+        try:
+            if self._open_nvml():
+                self._stop = False
+                self.thread = threading.Thread(target=self._poll, daemon=True)
+                self.thread.start()
+                time.sleep(0.01)  # first samples before the timed region
+                return
+        except Exception:
+            self.nvml = None
         try:
             self.tmp = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
             self.proc = subprocess.Popen(
@@ -101,6 +167,14 @@ class ClockSampler:
             self.proc = None
 
     def stop(self):
+        if self.thread is not None:
+            self._stop = True
+            self.thread.join(timeout=5)
+            # samples taken while the GPU ran the timed steps (the last few
+            # milliseconds of idle are dropped with the tail)
+            sm = self.samples
+            return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": self.max_mhz,
+                    "reasons": sorted(self.reasons), "samples": len(sm), "source": "nvml"}
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         self.proc.terminate()
@@ -125,7 +199,7 @@ class ClockSampler:
             except (ValueError, IndexError):
                 continue
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "reasons": sorted(reasons), "samples": len(sm), "source": "nvidia-smi"}
 
 
 # ---------------------------------------------------------------------------

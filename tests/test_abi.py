@@ -46,7 +46,10 @@ def test_plan_ok_and_workspace_positive(lib):
     plan, ws = _lib.w4a16_moe_plan(good_desc())
     assert ws > 0
     info = _lib.w4a16_moe_route_info(plan, 16)
-    assert info.tile_rows % 16 == 0 and 16 <= info.tile_rows <= 128
+    if info.gemm_path == _lib.PATH_TENSOR_CORES:
+        assert info.tile_rows % 16 == 0 and 16 <= info.tile_rows <= 128
+    else:
+        assert info.tile_rows == 8
     assert info.pipeline_stages >= 2
     _lib.w4a16_moe_plan_destroy(plan)
 
@@ -93,6 +96,7 @@ def test_overrides_validate_and_resize_workspace(lib):
         _lib.w4a16_moe_set_overrides(plan, 24, 0, 0)
     with pytest.raises(_lib.W4A16Error):
         _lib.w4a16_moe_set_overrides(plan, 0, 65, 0)
+    _lib.w4a16_moe_set_gemm_path(plan, _lib.PATH_TENSOR_CORES)  # tile_rows applies to this path
     ws2 = _lib.w4a16_moe_set_overrides(plan, 128, 4, 2)
     info = _lib.w4a16_moe_route_info(plan, 16)
     assert info.tile_rows == 128 and info.gemm1_splits == 4 and info.gemm2_splits == 2
@@ -119,9 +123,10 @@ def test_gemm_path_choice_and_validation(lib):
     tensor cores; forced paths hold at every batch size."""
     plan, _ = _lib.w4a16_moe_plan(good_desc(num_experts=384, hidden=7168, inter=256, top_k=8,
                                             max_tokens=2048))
-    paths = {t: _lib.w4a16_moe_route_info(plan, t).gemm_path for t in (1, 32, 144, 145, 2048)}
-    assert paths == {1: _lib.PATH_CUDA_CORES, 32: _lib.PATH_CUDA_CORES, 144: _lib.PATH_CUDA_CORES,
-                     145: _lib.PATH_TENSOR_CORES, 2048: _lib.PATH_TENSOR_CORES}
+    # 384 experts, top-8: 12 routes per expert at 576 tokens
+    paths = {t: _lib.w4a16_moe_route_info(plan, t).gemm_path for t in (1, 32, 576, 577, 2048)}
+    assert paths == {1: _lib.PATH_CUDA_CORES, 32: _lib.PATH_CUDA_CORES, 576: _lib.PATH_CUDA_CORES,
+                     577: _lib.PATH_TENSOR_CORES, 2048: _lib.PATH_TENSOR_CORES}
     assert _lib.w4a16_moe_route_info(plan, 32).tile_rows == 8
     with pytest.raises(_lib.W4A16Error) as ei:
         _lib.w4a16_moe_set_gemm_path(plan, 3)

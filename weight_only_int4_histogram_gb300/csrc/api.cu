@@ -70,10 +70,12 @@ struct Layout {
   size_t total;
 };
 
-// Expected routes per local expert up to which the CUDA-core GEMV runs both
-// GEMMs: its FP16 FMA work grows with the routes per tile while the
-// tensor-core MMA cost per weight tile is flat.
-constexpr double kGemvMaxRoutesPerExpert = 3.0;
+// Expected routes per local expert up to which the warp-MMA GEMV runs both
+// GEMMs.  Its route tiles hold 8 routes, so above this an expert's weights are
+// streamed once per tile and the tcgen05 path (route tiles up to 128) wins;
+// measured crossovers on GB300 lay between 12 and 17 routes per expert for
+// the uniform-routing workloads.
+constexpr double kGemvMaxRoutesPerExpert = 12.0;
 
 bool use_gemv(const w4a16_moe_plan_s& P, int T) {
   if (P.path == W4A16_PATH_TENSOR_CORES) return false;

@@ -15,10 +15,9 @@
 // Arithmetic (per weight row, per 32-element group), in the activation type
 // (BF16 or FP16) with FP32 accumulation:
 //   * a nibble goes to each 16-bit half of a register with one lop3
-//     ((w & 0x000F000F) ^ magic = 2^m + 8 + q in the activation type, m = 7
-//     for BF16 and 10 for FP16, nibble = q & 15) and one HSUB2 of 2^m + 8
-//     leaves the exact code q; shifting the word by 4, 8 and 12 bits gives the
-//     other three nibble pairs;
+//     ((w & 0x000F000F) ^ magic = B + q exactly, B = 136 for BF16 and 1032
+//     for FP16, nibble = q & 15) and one HSUB2 of B leaves the exact code q;
+//     shifting the word by 4, 8 and 12 bits gives the other three nibble pairs;
 //   * the MMA multiplies the exact codes by the activations as given and sums
 //     in FP32, one group (two MMAs) at a time; the group result is multiplied
 //     by the group scale and accumulated in FP32.
@@ -140,10 +139,23 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a
   }
 }
 
-// Exact code pair of the low nibbles of the two 16-bit halves of v.
+// Exact code pair q of the low nibbles of the two 16-bit halves of v:
+// (v & 0x000F000F) ^ magic = B + q exactly (B = 136 for BF16, 1032 for FP16;
+// nibble = q & 15), minus B.
 template <int DT>
 __device__ __forceinline__ uint32_t code_pair(uint32_t v) {
   return F16<DT>::sub(lop3_and_xor(v, 0x000F000Fu, F16<DT>::kMagic), F16<DT>::kMagic);
+}
+
+// Four 8 x 8 b16 matrices from shared memory; lane l gives the address of row
+// l % 8 of matrix l / 8 and receives bytes 4 (l % 4) .. + 3 of row l / 4 of
+// each matrix.
+__device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                            uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr)
+               : "memory");
 }
 
 // One unit (route tile x weight tile x K split) on one compute warp: 16 weight
@@ -155,12 +167,13 @@ __device__ __forceinline__ uint32_t code_pair(uint32_t v) {
 // lane feeds whole packed words in the order the nibble extraction yields and
 // pairs its activations the same way with byte permutes:
 //   group scales (K-packed, byte b = K 2b | K 2b+1 << 4): lane t takes word t
-//     of group c's 16-byte chunk (K 32c + 8t .. + 7); its code pairs
-//     (k0, k4), (k1, k5), (k2, k6), (k3, k7) feed two MMAs whose sum over the
-//     four lanes is exactly group c, so the group scale multiplies that result;
+//     of group c's 16-byte chunk (K 32c + 8t .. + 7; one ldmatrix.x4 fetches
+//     it for rowA and rowB and two groups); its code pairs (k0, k4), (k1, k5),
+//     (k2, k6), (k3, k7) feed MMAs whose sum over the four lanes is exactly
+//     group c, so the group scale multiplies that result;
 //   per-channel (row-pair packed, one byte per K, even row in the low nibble):
 //     lane t takes 16-byte chunks t and t + 4 of the K half; word i of a chunk
-//     (4 K) gives (k0, k2) and (k1, k3) for one MMA.
+//     (4 K) gives (k0, k2) and (k1, k3) for one MMA pair.
 template <int WHICH, int SCALE, int DT>
 __device__ __forceinline__ bool gemv_unit(const GemmParams& p, uint8_t* smem, uint64_t* full,
                                           uint64_t* bfull, uint64_t* empty, uint64_t* epibar,
@@ -176,6 +189,12 @@ __device__ __forceinline__ bool gemv_unit(const GemmParams& p, uint8_t* smem, ui
   float tot[4] = {0.0f, 0.0f, 0.0f, 0.0f};
   // per-channel: the rows' nibble (rowA and rowB have the same parity)
   const int pc_shift = (rowA & 1) * 4;
+  // ldmatrix row of this lane: matrix l / 8 = (rowA or rowB of row l % 8, chunk
+  // offset 0 or 1); byte offset of the row in the stage, its swizzle phase
+  const int ld_i = lane & 7, ld_j = lane >> 3;
+  const int ld_row = (ld_j & 1) ? rowB - g + ld_i : rowA - g + ld_i;
+  const uint32_t ld_row_off = (ld_row >> 6) * 8192 + (ld_row & 63) * 128;
+  const int ld_row7 = ld_row & 7, ld_chunk = ld_j >> 1;
 
   for (int kb = w.kb0; kb < w.kb1; ++kb) {
     if (!mbar_wait(&full[st], ph, abort_flag, p.err) || !mbar_wait(&bfull[st], ph, abort_flag, p.err))
@@ -183,31 +202,40 @@ __device__ __forceinline__ bool gemv_unit(const GemmParams& p, uint8_t* smem, ui
     const uint8_t* sA = smem + st * kGemvStageBytes;
     const uint8_t* sXr = sA + kGvOffX + g * kGvRouteBytes;  // this lane's B column (route g)
     if (SCALE == SCALE_GROUP) {
-      // boxes of 64 rows x 128 bytes, 128-byte swizzle: chunk c of row r at c ^ (r & 7)
-      const uint8_t* pA = sA + (rowA >> 6) * 8192 + (rowA & 63) * 128 + 4 * t;
-      const uint8_t* pB = sA + (rowB >> 6) * 8192 + (rowB & 63) * 128 + 4 * t;
       const uint2 sa = *reinterpret_cast<const uint2*>(sA + kGvOffS + rowA * kGvScaleRowBytes + kh * 8);
       const uint2 sb = *reinterpret_cast<const uint2*>(sA + kGvOffS + rowB * kGvScaleRowBytes + kh * 8);
+      const uint32_t sbase = smem_u32(sA);
 #pragma unroll
-      for (int m = 0; m < 4; ++m) {
-        const int c = 4 * kh + m;  // group of the stage
-        const uint32_t wa = *reinterpret_cast<const uint32_t*>(pA + ((c ^ (rowA & 7)) << 4));
-        const uint32_t wb = *reinterpret_cast<const uint32_t*>(pB + ((c ^ (rowB & 7)) << 4));
-        // activations K 32c + 8t .. + 7 of route g: (x0 x1) (x2 x3) (x4 x5) (x6 x7)
-        const uint4 xv = *reinterpret_cast<const uint4*>(sXr + (4 * c + t) * 16);
-        float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-        mma_16816<DT>(d, code_pair<DT>(wa), code_pair<DT>(wb), code_pair<DT>(wa >> 4), code_pair<DT>(wb >> 4),
-                      __byte_perm(xv.x, xv.z, 0x5410), __byte_perm(xv.x, xv.z, 0x7632));
-        mma_16816<DT>(d, code_pair<DT>(wa >> 8), code_pair<DT>(wb >> 8), code_pair<DT>(wa >> 12),
-                      code_pair<DT>(wb >> 12), __byte_perm(xv.y, xv.w, 0x5410), __byte_perm(xv.y, xv.w, 0x7632));
-        // BF16 group scales of rowA / rowB -> FP32 exactly
-        const uint32_t swa = (m < 2) ? sa.x : sa.y, swb = (m < 2) ? sb.x : sb.y;
-        const float fa = __uint_as_float((m & 1) ? (swa & 0xFFFF0000u) : (swa << 16));
-        const float fb = __uint_as_float((m & 1) ? (swb & 0xFFFF0000u) : (swb << 16));
-        tot[0] = fmaf(fa, d[0], tot[0]);
-        tot[1] = fmaf(fa, d[1], tot[1]);
-        tot[2] = fmaf(fb, d[2], tot[2]);
-        tot[3] = fmaf(fb, d[3], tot[3]);
+      for (int pq = 0; pq < 2; ++pq) {
+        // words t of rowA / rowB in groups 4 kh + 2 pq and + 1 (128-byte swizzle:
+        // chunk c of row r at c ^ (r & 7))
+        uint32_t w4[4];
+        ldmatrix_x4(sbase + ld_row_off + ((((4 * kh + 2 * pq) + ld_chunk) ^ ld_row7) << 4), w4[0], w4[1], w4[2],
+                    w4[3]);
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          const int m = 2 * pq + q;
+          const int c = 4 * kh + m;  // group of the stage
+          const uint32_t wa = w4[2 * q], wb = w4[2 * q + 1];
+          // activations K 32c + 8t .. + 7 of route g: (x0 x1) (x2 x3) (x4 x5) (x6 x7),
+          // paired as the codes: (x0 x4) (x1 x5) | (x2 x6) (x3 x7)
+          const uint4 xv = *reinterpret_cast<const uint4*>(sXr + (4 * c + t) * 16);
+          const uint32_t b0 = __byte_perm(xv.x, xv.z, 0x5410), b1 = __byte_perm(xv.x, xv.z, 0x7632);
+          const uint32_t b2 = __byte_perm(xv.y, xv.w, 0x5410), b3 = __byte_perm(xv.y, xv.w, 0x7632);
+          float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+          mma_16816<DT>(d, code_pair<DT>(wa), code_pair<DT>(wb), code_pair<DT>(wa >> 4), code_pair<DT>(wb >> 4),
+                        b0, b1);
+          mma_16816<DT>(d, code_pair<DT>(wa >> 8), code_pair<DT>(wb >> 8), code_pair<DT>(wa >> 12),
+                        code_pair<DT>(wb >> 12), b2, b3);
+          // BF16 group scales of rowA / rowB -> FP32 exactly
+          const uint32_t swa = (m < 2) ? sa.x : sa.y, swb = (m < 2) ? sb.x : sb.y;
+          const float fa = __uint_as_float((m & 1) ? (swa & 0xFFFF0000u) : (swa << 16));
+          const float fb = __uint_as_float((m & 1) ? (swb & 0xFFFF0000u) : (swb << 16));
+          tot[0] = fmaf(fa, d[0], tot[0]);
+          tot[1] = fmaf(fa, d[1], tot[1]);
+          tot[2] = fmaf(fb, d[2], tot[2]);
+          tot[3] = fmaf(fb, d[3], tot[3]);
+        }
       }
     } else {
       // boxes (row block, K half) of 32 row pairs x 128 K bytes, 128-byte swizzle
@@ -219,7 +247,7 @@ __device__ __forceinline__ bool gemv_unit(const GemmParams& p, uint8_t* smem, ui
         const int jj = 4 * m + t;  // 16-K chunk of the K half
         const uint4 ca = *reinterpret_cast<const uint4*>(pA + ((jj ^ (prA & 7)) << 4));
         const uint4 cb = *reinterpret_cast<const uint4*>(pB + ((jj ^ (prB & 7)) << 4));
-        // activations of the chunk: K 128 kh + 16 jj .. + 15 of route g
+        // activations of the chunk (K 128 kh + 16 jj .. + 15 of route g)
         const uint8_t* xp = sXr + (8 * kh + jj) * 32;
         const uint4 x0 = *reinterpret_cast<const uint4*>(xp);
         const uint4 x1 = *reinterpret_cast<const uint4*>(xp + 16);
