@@ -161,7 +161,9 @@ __device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t& r0, uint32_
 // One unit (route tile x weight tile x K split) on one compute warp: 16 weight
 // rows (MMA rows g: rowA, g + 8: rowB) x one K half of every stage x the
 // tile's <= 8 routes (MMA columns; columns past the route count read stale
-// data and are never stored).
+// data and are never stored).  ALT (single-stage units, no split): the warp
+// takes both K halves, the two warp groups take alternate units, and no
+// cross-warp reduction is needed.
 //
 // K order inside an MMA: any bijection works as long as A and B agree, so each
 // lane feeds whole packed words in the order the nibble extraction yields and
@@ -174,7 +176,7 @@ __device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t& r0, uint32_
 //   per-channel (row-pair packed, one byte per K, even row in the low nibble):
 //     lane t takes 16-byte chunks t and t + 4 of the K half; word i of a chunk
 //     (4 K) gives (k0, k2) and (k1, k3) for one MMA pair.
-template <int WHICH, int SCALE, int DT>
+template <int WHICH, int SCALE, int DT, bool ALT>
 __device__ __forceinline__ bool gemv_unit(const GemmParams& p, uint8_t* smem, uint64_t* full,
                                           uint64_t* bfull, uint64_t* empty, uint64_t* epibar,
                                           volatile int* abort_flag, volatile int* fixup_flag,
@@ -201,65 +203,70 @@ __device__ __forceinline__ bool gemv_unit(const GemmParams& p, uint8_t* smem, ui
       return false;
     const uint8_t* sA = smem + st * kGemvStageBytes;
     const uint8_t* sXr = sA + kGvOffX + g * kGvRouteBytes;  // this lane's B column (route g)
-    if (SCALE == SCALE_GROUP) {
-      const uint2 sa = *reinterpret_cast<const uint2*>(sA + kGvOffS + rowA * kGvScaleRowBytes + kh * 8);
-      const uint2 sb = *reinterpret_cast<const uint2*>(sA + kGvOffS + rowB * kGvScaleRowBytes + kh * 8);
-      const uint32_t sbase = smem_u32(sA);
+    // K halves of the stage handled by this warp: its own, or both (ALT)
 #pragma unroll
-      for (int pq = 0; pq < 2; ++pq) {
-        // words t of rowA / rowB in groups 4 kh + 2 pq and + 1 (128-byte swizzle:
-        // chunk c of row r at c ^ (r & 7))
-        uint32_t w4[4];
-        ldmatrix_x4(sbase + ld_row_off + ((((4 * kh + 2 * pq) + ld_chunk) ^ ld_row7) << 4), w4[0], w4[1], w4[2],
-                    w4[3]);
-#pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          const int m = 2 * pq + q;
-          const int c = 4 * kh + m;  // group of the stage
-          const uint32_t wa = w4[2 * q], wb = w4[2 * q + 1];
-          // activations K 32c + 8t .. + 7 of route g: (x0 x1) (x2 x3) (x4 x5) (x6 x7),
-          // paired as the codes: (x0 x4) (x1 x5) | (x2 x6) (x3 x7)
-          const uint4 xv = *reinterpret_cast<const uint4*>(sXr + (4 * c + t) * 16);
-          const uint32_t b0 = __byte_perm(xv.x, xv.z, 0x5410), b1 = __byte_perm(xv.x, xv.z, 0x7632);
-          const uint32_t b2 = __byte_perm(xv.y, xv.w, 0x5410), b3 = __byte_perm(xv.y, xv.w, 0x7632);
-          float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-          mma_16816<DT>(d, code_pair<DT>(wa), code_pair<DT>(wb), code_pair<DT>(wa >> 4), code_pair<DT>(wb >> 4),
-                        b0, b1);
-          mma_16816<DT>(d, code_pair<DT>(wa >> 8), code_pair<DT>(wb >> 8), code_pair<DT>(wa >> 12),
-                        code_pair<DT>(wb >> 12), b2, b3);
-          // BF16 group scales of rowA / rowB -> FP32 exactly
-          const uint32_t swa = (m < 2) ? sa.x : sa.y, swb = (m < 2) ? sb.x : sb.y;
-          const float fa = __uint_as_float((m & 1) ? (swa & 0xFFFF0000u) : (swa << 16));
-          const float fb = __uint_as_float((m & 1) ? (swb & 0xFFFF0000u) : (swb << 16));
-          tot[0] = fmaf(fa, d[0], tot[0]);
-          tot[1] = fmaf(fa, d[1], tot[1]);
-          tot[2] = fmaf(fb, d[2], tot[2]);
-          tot[3] = fmaf(fb, d[3], tot[3]);
+    for (int kk = 0; kk < (ALT ? 2 : 1); ++kk) {
+      const int khh = ALT ? kk : kh;
+      if (SCALE == SCALE_GROUP) {
+        const uint2 sa = *reinterpret_cast<const uint2*>(sA + kGvOffS + rowA * kGvScaleRowBytes + khh * 8);
+        const uint2 sb = *reinterpret_cast<const uint2*>(sA + kGvOffS + rowB * kGvScaleRowBytes + khh * 8);
+        const uint32_t sbase = smem_u32(sA);
+  #pragma unroll
+        for (int pq = 0; pq < 2; ++pq) {
+          // words t of rowA / rowB in groups 4 khh + 2 pq and + 1 (128-byte swizzle:
+          // chunk c of row r at c ^ (r & 7))
+          uint32_t w4[4];
+          ldmatrix_x4(sbase + ld_row_off + ((((4 * khh + 2 * pq) + ld_chunk) ^ ld_row7) << 4), w4[0], w4[1], w4[2],
+                      w4[3]);
+  #pragma unroll
+          for (int q = 0; q < 2; ++q) {
+            const int m = 2 * pq + q;
+            const int c = 4 * khh + m;  // group of the stage
+            const uint32_t wa = w4[2 * q], wb = w4[2 * q + 1];
+            // activations K 32c + 8t .. + 7 of route g: (x0 x1) (x2 x3) (x4 x5) (x6 x7),
+            // paired as the codes: (x0 x4) (x1 x5) | (x2 x6) (x3 x7)
+            const uint4 xv = *reinterpret_cast<const uint4*>(sXr + (4 * c + t) * 16);
+            const uint32_t b0 = __byte_perm(xv.x, xv.z, 0x5410), b1 = __byte_perm(xv.x, xv.z, 0x7632);
+            const uint32_t b2 = __byte_perm(xv.y, xv.w, 0x5410), b3 = __byte_perm(xv.y, xv.w, 0x7632);
+            float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+            mma_16816<DT>(d, code_pair<DT>(wa), code_pair<DT>(wb), code_pair<DT>(wa >> 4), code_pair<DT>(wb >> 4),
+                          b0, b1);
+            mma_16816<DT>(d, code_pair<DT>(wa >> 8), code_pair<DT>(wb >> 8), code_pair<DT>(wa >> 12),
+                          code_pair<DT>(wb >> 12), b2, b3);
+            // BF16 group scales of rowA / rowB -> FP32 exactly
+            const uint32_t swa = (m < 2) ? sa.x : sa.y, swb = (m < 2) ? sb.x : sb.y;
+            const float fa = __uint_as_float((m & 1) ? (swa & 0xFFFF0000u) : (swa << 16));
+            const float fb = __uint_as_float((m & 1) ? (swb & 0xFFFF0000u) : (swb << 16));
+            tot[0] = fmaf(fa, d[0], tot[0]);
+            tot[1] = fmaf(fa, d[1], tot[1]);
+            tot[2] = fmaf(fb, d[2], tot[2]);
+            tot[3] = fmaf(fb, d[3], tot[3]);
+          }
         }
-      }
-    } else {
-      // boxes (row block, K half) of 32 row pairs x 128 K bytes, 128-byte swizzle
-      const int prA = (rowA & 63) >> 1, prB = (rowB & 63) >> 1;
-      const uint8_t* pA = sA + ((rowA >> 6) * 2 + kh) * 4096 + prA * 128;
-      const uint8_t* pB = sA + ((rowB >> 6) * 2 + kh) * 4096 + prB * 128;
-#pragma unroll
-      for (int m = 0; m < 2; ++m) {
-        const int jj = 4 * m + t;  // 16-K chunk of the K half
-        const uint4 ca = *reinterpret_cast<const uint4*>(pA + ((jj ^ (prA & 7)) << 4));
-        const uint4 cb = *reinterpret_cast<const uint4*>(pB + ((jj ^ (prB & 7)) << 4));
-        // activations of the chunk (K 128 kh + 16 jj .. + 15 of route g)
-        const uint8_t* xp = sXr + (8 * kh + jj) * 32;
-        const uint4 x0 = *reinterpret_cast<const uint4*>(xp);
-        const uint4 x1 = *reinterpret_cast<const uint4*>(xp + 16);
-        const uint32_t wa[4] = {ca.x, ca.y, ca.z, ca.w}, wb[4] = {cb.x, cb.y, cb.z, cb.w};
-        const uint32_t xb[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const uint32_t a = wa[i] >> pc_shift, b = wb[i] >> pc_shift;
-          // word i = K 4i .. 4i + 3: code pairs (k0, k2), (k1, k3); activations likewise
-          mma_16816<DT>(tot, code_pair<DT>(a), code_pair<DT>(b), code_pair<DT>(a >> 8), code_pair<DT>(b >> 8),
-                        __byte_perm(xb[2 * i], xb[2 * i + 1], 0x5410),
-                        __byte_perm(xb[2 * i], xb[2 * i + 1], 0x7632));
+      } else {
+        // boxes (row block, K half) of 32 row pairs x 128 K bytes, 128-byte swizzle
+        const int prA = (rowA & 63) >> 1, prB = (rowB & 63) >> 1;
+        const uint8_t* pA = sA + ((rowA >> 6) * 2 + khh) * 4096 + prA * 128;
+        const uint8_t* pB = sA + ((rowB >> 6) * 2 + khh) * 4096 + prB * 128;
+  #pragma unroll
+        for (int m = 0; m < 2; ++m) {
+          const int jj = 4 * m + t;  // 16-K chunk of the K half
+          const uint4 ca = *reinterpret_cast<const uint4*>(pA + ((jj ^ (prA & 7)) << 4));
+          const uint4 cb = *reinterpret_cast<const uint4*>(pB + ((jj ^ (prB & 7)) << 4));
+          // activations of the chunk (K 128 khh + 16 jj .. + 15 of route g)
+          const uint8_t* xp = sXr + (8 * khh + jj) * 32;
+          const uint4 x0 = *reinterpret_cast<const uint4*>(xp);
+          const uint4 x1 = *reinterpret_cast<const uint4*>(xp + 16);
+          const uint32_t wa[4] = {ca.x, ca.y, ca.z, ca.w}, wb[4] = {cb.x, cb.y, cb.z, cb.w};
+          const uint32_t xb[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+  #pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const uint32_t a = wa[i] >> pc_shift, b = wb[i] >> pc_shift;
+            // word i = K 4i .. 4i + 3: code pairs (k0, k2), (k1, k3); activations likewise
+            mma_16816<DT>(tot, code_pair<DT>(a), code_pair<DT>(b), code_pair<DT>(a >> 8), code_pair<DT>(b >> 8),
+                          __byte_perm(xb[2 * i], xb[2 * i + 1], 0x5410),
+                          __byte_perm(xb[2 * i], xb[2 * i + 1], 0x7632));
+          }
         }
       }
     }
@@ -279,16 +286,19 @@ __device__ __forceinline__ bool gemv_unit(const GemmParams& p, uint8_t* smem, ui
   // K halves meet: the second half's warps leave their sums in one of two
   // buffers (alternating per unit: a buffer is rewritten only after every warp
   // passed the next barrier, i.e. after the first half read it).
-  float4* rbuf = reinterpret_cast<float4*>(red) + ((eph & 1) * 8 + rb) * 32 + lane;
-  if (kh == 1) *rbuf = make_float4(tot[0], tot[1], tot[2], tot[3]);
-  if (!epi_sync()) return false;
-  const bool fin = kh == 0;  // the first half finishes the unit
-  if (fin) {
-    const float4 o = *rbuf;
-    tot[0] += o.x;
-    tot[1] += o.y;
-    tot[2] += o.z;
-    tot[3] += o.w;
+  bool fin = true;  // this warp finishes the unit
+  if (!ALT) {
+    float4* rbuf = reinterpret_cast<float4*>(red) + ((eph & 1) * 8 + rb) * 32 + lane;
+    if (kh == 1) *rbuf = make_float4(tot[0], tot[1], tot[2], tot[3]);
+    if (!epi_sync()) return false;
+    fin = kh == 0;  // the first half finishes the unit
+    if (fin) {
+      const float4 o = *rbuf;
+      tot[0] += o.x;
+      tot[1] += o.y;
+      tot[2] += o.z;
+      tot[3] += o.w;
+    }
   }
   int r0, r1;
   tile_row_bases<WHICH>(p, w.nt, r0, r1);
@@ -414,7 +424,9 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
     for (int s = 0; s < kGemvStages; ++s) {
       mbar_init(&full[s], 1);                  // producer (TMA bytes + scale copies)
       mbar_init(&bfull[s], 32);                // the 32 lanes' activation copies
-      mbar_init(&empty[s], kGemvComputeWarps);
+      // every compute warp, or one warp group of 8 when the groups take
+      // alternate single-stage units
+      mbar_init(&empty[s], (p.splits == 1 && p.kb_total == 1) ? kGemvComputeWarps / 2 : kGemvComputeWarps);
     }
     mbar_init(epibar, kGemvComputeWarps);
     *abort_flag = 0;
@@ -603,17 +615,26 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
     // SwiGLU: MMA row g = gate row, g + 8 = its up row; otherwise 16 consecutive rows
     const int rowA = gated ? 8 * rb + g : 16 * rb + g;
     const int rowB = gated ? 64 + 8 * rb + g : 16 * rb + 8 + g;
+    // single-stage units without split: the groups (kh) take alternate units
+    const bool alt = p.splits == 1 && p.kb_total == 1;
     int st = 0;
     uint32_t ph = 0, eph = 0;
     UnitIter it;
     it.init(p);
     for (int i = 0; it.u < n_units; it.next(p), ++i) {
+      if (alt && (i & 1) != kh) {  // the other group's unit: skip its one stage
+        ring_next(st, ph);
+        continue;
+      }
       const Unit w = it.unit(p);
       const int4 ti = tile_of(p, tile_tab, i, it.u);
       const int rows = min(ti.z, kGemvMaxR);
-      if (!gemv_unit<WHICH, SCALE, DT>(p, smem, full, bfull, empty, epibar, abort_flag, fixup_flag, red, w,
-                                       ti.x, ti.y, rows, rowA, rowB, rb, kh, lane, st, ph, eph))
-        break;
+      const bool ok =
+          alt ? gemv_unit<WHICH, SCALE, DT, true>(p, smem, full, bfull, empty, epibar, abort_flag, fixup_flag, red,
+                                                  w, ti.x, ti.y, rows, rowA, rowB, rb, kh, lane, st, ph, eph)
+              : gemv_unit<WHICH, SCALE, DT, false>(p, smem, full, bfull, empty, epibar, abort_flag, fixup_flag, red,
+                                                   w, ti.x, ti.y, rows, rowA, rowB, rb, kh, lane, st, ph, eph);
+      if (!ok) break;
     }
   }
   __syncthreads();
