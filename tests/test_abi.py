@@ -49,7 +49,7 @@ def test_plan_ok_and_workspace_positive(lib):
     if info.gemm_path == _lib.PATH_TENSOR_CORES:
         assert info.tile_rows % 16 == 0 and 16 <= info.tile_rows <= 128
     else:
-        assert info.tile_rows == 8
+        assert info.tile_rows in (8, 16, 32)
     assert info.pipeline_stages >= 2
     _lib.w4a16_moe_plan_destroy(plan)
 
@@ -119,7 +119,7 @@ def test_planner_tile_height_follows_route_counts(lib):
 
 
 def test_gemm_path_choice_and_validation(lib):
-    """Few routes per expert -> CUDA-core GEMV with 8-route tiles; many ->
+    """Few routes per expert -> CUDA-core GEMV with 8- to 32-route tiles; many ->
     tensor cores; forced paths hold at every batch size."""
     plan, _ = _lib.w4a16_moe_plan(good_desc(num_experts=384, hidden=7168, inter=256, top_k=8,
                                             max_tokens=2048))
@@ -133,10 +133,10 @@ def test_gemm_path_choice_and_validation(lib):
     assert ei.value.status == 1
     ws_cc = _lib.w4a16_moe_set_gemm_path(plan, _lib.PATH_CUDA_CORES)
     info = _lib.w4a16_moe_route_info(plan, 2048)
-    assert info.gemm_path == _lib.PATH_CUDA_CORES and info.tile_rows == 8
+    assert info.gemm_path == _lib.PATH_CUDA_CORES and info.tile_rows == 32
     # tile_rows overrides apply to the tensor-core path only
     _lib.w4a16_moe_set_overrides(plan, 64, 0, 0)
-    assert _lib.w4a16_moe_route_info(plan, 2048).tile_rows == 8
+    assert _lib.w4a16_moe_route_info(plan, 2048).tile_rows == 32
     _lib.w4a16_moe_set_gemm_path(plan, _lib.PATH_TENSOR_CORES)
     assert _lib.w4a16_moe_route_info(plan, 1).gemm_path == _lib.PATH_TENSOR_CORES
     assert _lib.w4a16_moe_route_info(plan, 1).tile_rows == 64

@@ -84,6 +84,14 @@ bool use_gemv(const w4a16_moe_plan_s& P, int T) {
   return lam <= kGemvMaxRoutesPerExpert;
 }
 
+// CUDA-core path: route tiles of 8, 16 or 32 routes (one, two or four MMA N
+// blocks), from the expected routes per expert plus ~3.5 standard deviations.
+int choose_bn_gemv(const w4a16_moe_plan_s& P, int T) {
+  const double lam = static_cast<double>(T) * P.d.top_k / P.d.num_experts;
+  const double want = lam + 3.5 * std::sqrt(lam) + 1.0;
+  return want <= 8.0 ? 8 : (want <= 16.0 ? 16 : kGemvMaxR);
+}
+
 int choose_bn(const w4a16_moe_plan_s& P, int T) {
   if (P.ov_bn) return P.ov_bn;
   // Route-count-based tile height: expected routes per expert plus ~3.5
@@ -121,7 +129,7 @@ Layout make_layout(const w4a16_moe_plan_s& P, int T) {
   L.T = T;
   L.R = T * d.top_k;
   L.gemv = use_gemv(P, T);
-  L.bn = L.gemv ? kGemvMaxR : choose_bn(P, T);
+  L.bn = L.gemv ? choose_bn_gemv(P, T) : choose_bn(P, T);
   const int E = d.num_experts;
   const int touched_max = std::min(E, std::max(L.R, 1));
   L.tiles_cap = (L.R + touched_max * (L.bn - 1)) / L.bn + 1;
@@ -142,9 +150,11 @@ Layout make_layout(const w4a16_moe_plan_s& P, int T) {
   L.kbps1 = cdiv(L.kb1, L.s1);
   L.kbps2 = cdiv(L.kb2, L.s2);
   if (L.gemv) {
-    L.stage_bytes = kGemvStageBytes;
-    L.stages = kGemvStages;
-    L.smem = gemv_smem_bytes();
+    // K-half exchange buffers unless both GEMMs have single-stage units only
+    const bool ksplit = !(L.kb1 == 1 && L.s1 == 1 && L.kb2 == 1 && L.s2 == 1);
+    L.stage_bytes = gemv_stage_bytes(L.bn);
+    L.stages = gemv_stages(L.bn, ksplit);
+    L.smem = gemv_smem_bytes(L.bn, ksplit);
   } else {
     L.stage_bytes = kStageA + L.bn * kStageBRow + kStageS;
     // dynamic shared memory: 1 KB alignment slack + stages + 2 KB control block
@@ -371,7 +381,7 @@ w4a16_status launch_forward(const w4a16_moe_plan_s& P, const Layout& L, const vo
   g1.scale_tma = stma1 ? 1 : 0;
   cudaError_t e;
   if (P.has_ev && (e = cudaEventRecord(P.ev[0], s)) != cudaSuccess) return cuda_fail(e, "event record");
-  e = L.gemv ? launch_gemv(GEMM_UP, d.scale_kind, d.act_dtype, g1, tmA1, tmS1, L.grid1, s, P.pdl)
+  e = L.gemv ? launch_gemv(GEMM_UP, d.scale_kind, d.act_dtype, g1, tmA1, tmS1, L.grid1, L.smem, s, P.pdl)
              : launch_gemm(GEMM_UP, d.scale_kind, d.act_dtype, g1, tmA1, tmA1, L.grid1, L.smem, s, P.pdl);
   if (e != cudaSuccess) return cuda_fail(e, "gate/up GEMM launch");
   if (P.has_ev && (e = cudaEventRecord(P.ev[1], s)) != cudaSuccess) return cuda_fail(e, "event record");
@@ -390,7 +400,7 @@ w4a16_status launch_forward(const w4a16_moe_plan_s& P, const Layout& L, const vo
   g2.part = nullptr;
   g2.counters = nullptr;
   g2.scale_tma = stma2 ? 1 : 0;
-  e = L.gemv ? launch_gemv(GEMM_DOWN, d.scale_kind, d.act_dtype, g2, tmA2, tmS2, L.grid2, s, P.pdl)
+  e = L.gemv ? launch_gemv(GEMM_DOWN, d.scale_kind, d.act_dtype, g2, tmA2, tmS2, L.grid2, L.smem, s, P.pdl)
              : launch_gemm(GEMM_DOWN, d.scale_kind, d.act_dtype, g2, tmA2, tmB2, L.grid2, L.smem, s, P.pdl);
   if (e != cudaSuccess) return cuda_fail(e, "down GEMM launch");
   if (P.has_ev && (e = cudaEventRecord(P.ev[2], s)) != cudaSuccess) return cuda_fail(e, "event record");
@@ -432,16 +442,16 @@ cudaError_t launch_gemm(int which, int scale_kind, int dtype, const GemmParams& 
 
 template <int DT>
 cudaError_t launch_gemv_dt(int which, int scale_kind, const GemmParams& p, const CUtensorMap& tmA,
-                           const CUtensorMap& tmS, int grid, cudaStream_t s, bool pdl);
+                           const CUtensorMap& tmS, int grid, int smem_bytes, cudaStream_t s, bool pdl);
 extern template cudaError_t launch_gemv_dt<DT_BF16>(int, int, const GemmParams&, const CUtensorMap&,
-                                                     const CUtensorMap&, int, cudaStream_t, bool);
+                                                     const CUtensorMap&, int, int, cudaStream_t, bool);
 extern template cudaError_t launch_gemv_dt<DT_FP16>(int, int, const GemmParams&, const CUtensorMap&,
-                                                     const CUtensorMap&, int, cudaStream_t, bool);
+                                                     const CUtensorMap&, int, int, cudaStream_t, bool);
 
 cudaError_t launch_gemv(int which, int scale_kind, int dtype, const GemmParams& p, const CUtensorMap& tmA,
-                        const CUtensorMap& tmS, int grid, cudaStream_t s, bool pdl) {
-  if (dtype == DT_BF16) return launch_gemv_dt<DT_BF16>(which, scale_kind, p, tmA, tmS, grid, s, pdl);
-  return launch_gemv_dt<DT_FP16>(which, scale_kind, p, tmA, tmS, grid, s, pdl);
+                        const CUtensorMap& tmS, int grid, int smem_bytes, cudaStream_t s, bool pdl) {
+  if (dtype == DT_BF16) return launch_gemv_dt<DT_BF16>(which, scale_kind, p, tmA, tmS, grid, smem_bytes, s, pdl);
+  return launch_gemv_dt<DT_FP16>(which, scale_kind, p, tmA, tmS, grid, smem_bytes, s, pdl);
 }
 }  // namespace w4a16
 

@@ -31,15 +31,30 @@ constexpr int kStageS = kTileRows * kGroupsPerStage * 2;  // BF16 scales per sta
 constexpr int kStageBRow = kBlockK * 2;            // bytes of one activation row per stage
 
 // CUDA-core GEMV path (gemv.cuh): route tiles of at most kGemvMaxR routes,
-// pipeline stages of kGemvBlockK K values.
+// pipeline stages of kGemvBlockK K values; the stage size (and so the number
+// of stages) follows the route-tile height, and units of several stages need
+// a K-half exchange buffer (ksplit).
 constexpr int kGemvThreads = 576;    // 18 warps: see the role map in gemv.cuh
-constexpr int kGemvMaxR = 8;
+constexpr int kGemvMaxR = 32;
 constexpr int kGemvBlockK = 256;
-constexpr int kGemvStages = 9;
-constexpr int kGemvStageBytes = 23552;  // weights, scales, activation rows
-constexpr int kGemvCtrlBytes = 12800;   // mbarriers, flags, K-half exchange, tile table
-__host__ __device__ constexpr int gemv_smem_bytes() {
-  return 1024 + kGemvStages * kGemvStageBytes + kGemvCtrlBytes;  // 1 KB alignment slack
+constexpr int kGemvMaxStages = 12;
+constexpr int kGemvCtrlBytes = 4608;   // mbarriers, flags, tile table
+constexpr int kGemvSmemLimit = 232448;
+// weights (16 KB) + BF16 scales (2 KB) + rows of bn routes (512 B + 64 B pad each)
+__host__ __device__ constexpr int gemv_stage_bytes(int bn) {
+  return (kTileRows * kGemvBlockK / 2 + kTileRows * 16 + bn * 576 + 1023) / 1024 * 1024;
+}
+// control block + two exchange buffers of 8 warps x bn / 8 blocks x 32 lanes x 16 B
+__host__ __device__ constexpr int gemv_ctrl_bytes(int bn, bool ksplit) {
+  return kGemvCtrlBytes + (ksplit ? 2 * 8 * (bn / 8) * 32 * 16 : 0);
+}
+__host__ __device__ constexpr int gemv_stages(int bn, bool ksplit) {
+  return (kGemvSmemLimit - 1024 - gemv_ctrl_bytes(bn, ksplit)) / gemv_stage_bytes(bn) < kGemvMaxStages
+             ? (kGemvSmemLimit - 1024 - gemv_ctrl_bytes(bn, ksplit)) / gemv_stage_bytes(bn)
+             : kGemvMaxStages;
+}
+__host__ __device__ constexpr int gemv_smem_bytes(int bn, bool ksplit) {
+  return 1024 + gemv_stages(bn, ksplit) * gemv_stage_bytes(bn) + gemv_ctrl_bytes(bn, ksplit);  // 1 KB slack
 }
 
 enum { ACT_SWIGLU = 0, ACT_RELU2 = 1 };
@@ -111,8 +126,8 @@ cudaError_t launch_gemm(int which, int scale_kind, int dtype, const GemmParams& 
                         const CUtensorMap& tmA, const CUtensorMap& tmB, int grid, int smem_bytes,
                         cudaStream_t s, bool pdl);
 cudaError_t launch_gemv(int which, int scale_kind, int dtype, const GemmParams& p,
-                        const CUtensorMap& tmA, const CUtensorMap& tmS, int grid, cudaStream_t s,
-                        bool pdl);
+                        const CUtensorMap& tmA, const CUtensorMap& tmS, int grid, int smem_bytes,
+                        cudaStream_t s, bool pdl);
 cudaError_t launch_combine(int dtype, const CombineParams& p, cudaStream_t s, bool pdl);
 int gemm_smem_bytes(int bn, int stages);
 int gemm_stage_bytes(int bn);

@@ -1,16 +1,17 @@
-// Expert-grouped W4A16 GEMV for sm_103a (both MoE GEMMs, few routes per
+// Expert-grouped W4A16 GEMV for sm_103a (both MoE GEMMs, up to ~12 routes per
 // expert), on warp-level MMAs fed by register-side dequantisation.
 //
 // Same operation, work units and outputs as the tcgen05 kernel in gemm.cuh
 // (route tile x 128-row weight tile x K split; the "gate/up GEMM" and "down
 // GEMM" of "feat(pytorch): add CuTeDSL W4A16 MoE backend" (LMDeploy), sections
-// Modification and Benchmark), for batches where an expert sees only a handful
-// of routes.  There each weight is used by 1-4 routes: the contraction is a
-// matrix-vector product whose cost is streaming the packed INT4 weights, and a
+// Modification and Benchmark), for batches where an expert sees only a few
+// routes.  There each weight is used by a handful of routes: the contraction
+// is a thin product whose cost is streaming the packed INT4 weights, and a
 // 128-row tcgen05 tile with TMEM staging has a fixed cost per MMA that such
-// thin tiles cannot amortise.  Here the route tile (<= kGemvMaxR = 8 routes)
-// is the N = 8 side of mma.sync m16n8k16 and the dequantised weights go to the
-// MMA straight from registers.
+// thin tiles cannot amortise.  Here a route tile (<= kGemvMaxR = 32 routes) is
+// the N side of mma.sync m16n8k16 -- up to four N = 8 blocks sharing each
+// dequantised A fragment -- and the dequantised weights go to the MMAs
+// straight from registers.
 //
 // Arithmetic (per weight row, per 32-element group), in the activation type
 // (BF16 or FP16) with FP32 accumulation:
@@ -19,12 +20,20 @@
 //     for FP16, nibble = q & 15) and one HSUB2 of B leaves the exact code q;
 //     shifting the word by 4, 8 and 12 bits gives the other three nibble pairs;
 //   * the MMA multiplies the exact codes by the activations as given and sums
-//     in FP32, one group (two MMAs) at a time; the group result is multiplied
-//     by the group scale and accumulated in FP32.
+//     in FP32, one group (two MMAs per N block) at a time; the group result is
+//     multiplied by the group scale and accumulated in FP32.
 //   Per-channel scales multiply the FP32 total in the epilogue.
 //
 // A pipeline stage is 128 weight rows x kGemvBlockK (256) K values: 128 bytes
 // of every packed row per visit, read by TMA in 128-byte-swizzled boxes.
+//
+// Compute mapping: 16 warps = 8 row blocks (16 rows each) x 2 groups.
+//   * units of several stages: group h takes K half h of every stage; the
+//     halves meet once per unit through a double-buffered shared exchange;
+//   * single-stage units without split (e.g. the down GEMM at I = 256): group
+//     h takes the units of ordinal parity h over the full K, no exchange.
+// In the second case each group has a ring of stages of its own (see
+// gemv_unit for why every consumer of a ring sees every phase of it).
 //
 // Warp roles (576 threads):
 //   warp 0      TMA producer of the packed weight tile and the group scales
@@ -32,37 +41,40 @@
 //   warp 1      activation rows: cp.async of the tile's rows (gate/up: token
 //               rows of x by slot; down: intermediate rows), completion
 //               signalled on the stage's mbarrier without blocking the warp
-//   warps 2-17  compute: warp 2 + c takes row block c % 8 (16 rows) and K half
-//               c / 8 of every stage; the halves meet once per unit through
-//               shared memory.  For SwiGLU a row block holds 8 gate rows and
-//               their 8 up rows, so the activation is applied in registers.
+//   warps 2-17  compute: warp 2 + c is in group c / 8 and takes row block
+//               c % 8 (16 rows: MMA rows g and g + 8).  For SwiGLU a row block
+//               holds 8 gate rows and their 8 up rows, so the activation is
+//               applied in registers.
 #pragma once
 #include "gemm.cuh"
 
 namespace w4a16 {
 
-// Stage layout (bytes from the 1024-aligned stage base).
+// Stage layout (bytes from the 1024-aligned stage base); the activation rows
+// take the rest of the stage (gemv_stage_bytes).
 constexpr int kGvWeightBytes = kTileRows * kGemvBlockK / 2;          // packed weights
 constexpr int kGvScaleRowBytes = kGemvBlockK / kGroup * 2;            // 8 BF16 scales per row
 constexpr int kGvOffS = kGvWeightBytes;
 constexpr int kGvOffX = kGvOffS + kTileRows * kGvScaleRowBytes;       // activation rows
 constexpr int kGvRouteBytes = kGemvBlockK * 2 + 64;                   // + pad: 64 mod 128
-static_assert(kGvOffX + kGemvMaxR * kGvRouteBytes <= kGemvStageBytes, "GEMV stage overflow");
-static_assert(kGemvStageBytes % 1024 == 0, "GEMV stages must keep 1024-byte alignment");
+static_assert(kGvRouteBytes == 576, "stage size formula");
+constexpr int kGemvMaxNB = kGemvMaxR / 8;
 constexpr int kGemvComputeWarps = 16;
 static_assert(kGemvThreads == 32 * (2 + kGemvComputeWarps), "warp roles");
-// Control block: mbarriers and flags; the K-half exchange (two buffers of 8
-// warps x 32 lanes x 4 floats) from kGvCtrlRedOff; the tile records of the
-// CTA's first kGemvTileTab units from kGvCtrlTabOff.
-constexpr int kGvCtrlRedOff = 512;
-constexpr int kGvCtrlTabOff = kGvCtrlRedOff + 2 * 8 * 32 * 16;
+// Control block: mbarriers and flags, then the tile records of the CTA's first
+// kGemvTileTab units from kGvCtrlTabOff, then (units of several stages) the
+// K-half exchange from kGvCtrlRedOff: two buffers of 8 warps x NB blocks x 32
+// lanes x 4 floats (gemv_ctrl_bytes).
+constexpr int kGvCtrlTabOff = 512;
+constexpr int kGvCtrlRedOff = kGemvCtrlBytes;
 constexpr int kGemvTileTab = 256;
-static_assert(3 * kGemvStages * 8 + 8 + 8 <= kGvCtrlRedOff, "control block");
+static_assert(3 * kGemvMaxStages * 8 + 8 + 8 <= kGvCtrlTabOff, "control block");
 static_assert(kGvCtrlTabOff + kGemvTileTab * 16 <= kGemvCtrlBytes, "tile table");
 static_assert(kGemvTileTab <= kGemvThreads, "one record per thread");
+static_assert(gemv_smem_bytes(kGemvMaxR, true) <= kGemvSmemLimit && gemv_stages(kGemvMaxR, true) >= 4, "smem");
 
-__device__ __forceinline__ void ring_next(int& st, uint32_t& ph) {
-  if (++st == kGemvStages) {
+__device__ __forceinline__ void ring_next(int& st, uint32_t& ph, int stages) {
+  if (++st == stages) {
     st = 0;
     ph ^= 1u;
   }
@@ -124,17 +136,17 @@ struct UnitIter {
 // 2t + 9 (a2, a3), B column g at the same K (b0, b1), D rows g, g + 8 at
 // columns 2t, 2t + 1.
 template <int DT>
-__device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                          uint32_t b0, uint32_t b1) {
+__device__ __forceinline__ void mma_16816(float& d0, float& d1, float& d2, float& d3, uint32_t a0, uint32_t a1,
+                                          uint32_t a2, uint32_t a3, uint32_t b0, uint32_t b1) {
   if (DT == DT_BF16) {
     asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
         "{%0, %1, %2, %3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "+f"(d0), "+f"(d1), "+f"(d2), "+f"(d3)
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
   } else {
     asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
         "{%0, %1, %2, %3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "+f"(d0), "+f"(d1), "+f"(d2), "+f"(d3)
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
   }
 }
@@ -158,12 +170,10 @@ __device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t& r0, uint32_
                : "memory");
 }
 
-// One unit (route tile x weight tile x K split) on one compute warp: 16 weight
-// rows (MMA rows g: rowA, g + 8: rowB) x one K half of every stage x the
-// tile's <= 8 routes (MMA columns; columns past the route count read stale
-// data and are never stored).  ALT (single-stage units, no split): the warp
-// takes both K halves, the two warp groups take alternate units, and no
-// cross-warp reduction is needed.
+// One stage of one compute warp: 16 weight rows (MMA rows g: rowA, g + 8:
+// rowB) x the full stage K (FULLK) or its half kh x NB blocks of 8 routes (MMA columns; columns past
+// the route count read stale data and are never stored).  tot[4 n + 0..1]:
+// rowA x routes 8 n + 2t, + 1; tot[4 n + 2..3]: rowB x the same routes.
 //
 // K order inside an MMA: any bijection works as long as A and B agree, so each
 // lane feeds whole packed words in the order the nibble extraction yields and
@@ -174,132 +184,109 @@ __device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t& r0, uint32_
 //     (k2, k6), (k3, k7) feed MMAs whose sum over the four lanes is exactly
 //     group c, so the group scale multiplies that result;
 //   per-channel (row-pair packed, one byte per K, even row in the low nibble):
-//     lane t takes 16-byte chunks t and t + 4 of the K half; word i of a chunk
-//     (4 K) gives (k0, k2) and (k1, k3) for one MMA pair.
-template <int WHICH, int SCALE, int DT, bool ALT>
-__device__ __forceinline__ bool gemv_unit(const GemmParams& p, uint8_t* smem, uint64_t* full,
-                                          uint64_t* bfull, uint64_t* empty, uint64_t* epibar,
-                                          volatile int* abort_flag, volatile int* fixup_flag,
-                                          float* red, const Unit& w, int e, int m0, int rows,
-                                          int rowA, int rowB, int rb, int kh, int lane, int& st,
-                                          uint32_t& ph, uint32_t& eph) {
-  using T = F16<DT>;
+//     lane t takes 16-byte chunks t and t + 4 of each K half; word i of a chunk
+//     (4 K) gives (k0, k2) and (k1, k3) for one MMA.
+template <int SCALE, int DT, int NB, bool FULLK>
+__device__ __forceinline__ void gemv_stage(const uint8_t* sA, int rowA, int rowB, int kh, int lane,
+                                           uint32_t ld_row_off, int ld_row7, int ld_chunk, float (&tot)[4 * NB]) {
   const int g = lane >> 2, t = lane & 3;
-  const bool gated = (WHICH == GEMM_UP && p.act == ACT_SWIGLU);
-  const int N1 = p.n_rows;
-  // tot[0..1]: rowA x routes 2t, 2t + 1; tot[2..3]: rowB x the same routes
-  float tot[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-  // per-channel: the rows' nibble (rowA and rowB have the same parity)
-  const int pc_shift = (rowA & 1) * 4;
-  // ldmatrix row of this lane: matrix l / 8 = (rowA or rowB of row l % 8, chunk
-  // offset 0 or 1); byte offset of the row in the stage, its swizzle phase
-  const int ld_i = lane & 7, ld_j = lane >> 3;
-  const int ld_row = (ld_j & 1) ? rowB - g + ld_i : rowA - g + ld_i;
-  const uint32_t ld_row_off = (ld_row >> 6) * 8192 + (ld_row & 63) * 128;
-  const int ld_row7 = ld_row & 7, ld_chunk = ld_j >> 1;
-
-  for (int kb = w.kb0; kb < w.kb1; ++kb) {
-    if (!mbar_wait(&full[st], ph, abort_flag, p.err) || !mbar_wait(&bfull[st], ph, abort_flag, p.err))
-      return false;
-    const uint8_t* sA = smem + st * kGemvStageBytes;
-    const uint8_t* sXr = sA + kGvOffX + g * kGvRouteBytes;  // this lane's B column (route g)
-    // K halves of the stage handled by this warp: its own, or both (ALT)
+  const uint8_t* sX = sA + kGvOffX + g * kGvRouteBytes;  // this lane's B column in block 0 (route g)
+  if (SCALE == SCALE_GROUP) {
+    // BF16 scales of the groups this warp handles, two per word: word pp holds
+    // the groups of ldmatrix step pp
+    uint32_t saw[4], sbw[4];
+    if (FULLK) {
+      const uint4 sa = *reinterpret_cast<const uint4*>(sA + kGvOffS + rowA * kGvScaleRowBytes);
+      const uint4 sb = *reinterpret_cast<const uint4*>(sA + kGvOffS + rowB * kGvScaleRowBytes);
+      saw[0] = sa.x; saw[1] = sa.y; saw[2] = sa.z; saw[3] = sa.w;
+      sbw[0] = sb.x; sbw[1] = sb.y; sbw[2] = sb.z; sbw[3] = sb.w;
+    } else {
+      const uint2 sa = *reinterpret_cast<const uint2*>(sA + kGvOffS + rowA * kGvScaleRowBytes + kh * 8);
+      const uint2 sb = *reinterpret_cast<const uint2*>(sA + kGvOffS + rowB * kGvScaleRowBytes + kh * 8);
+      saw[0] = sa.x; saw[1] = sa.y; saw[2] = 0u; saw[3] = 0u;
+      sbw[0] = sb.x; sbw[1] = sb.y; sbw[2] = 0u; sbw[3] = 0u;
+    }
+    const uint32_t sbase = smem_u32(sA);
 #pragma unroll
-    for (int kk = 0; kk < (ALT ? 2 : 1); ++kk) {
-      const int khh = ALT ? kk : kh;
-      if (SCALE == SCALE_GROUP) {
-        const uint2 sa = *reinterpret_cast<const uint2*>(sA + kGvOffS + rowA * kGvScaleRowBytes + khh * 8);
-        const uint2 sb = *reinterpret_cast<const uint2*>(sA + kGvOffS + rowB * kGvScaleRowBytes + khh * 8);
-        const uint32_t sbase = smem_u32(sA);
-  #pragma unroll
-        for (int pq = 0; pq < 2; ++pq) {
-          // words t of rowA / rowB in groups 4 khh + 2 pq and + 1 (128-byte swizzle:
-          // chunk c of row r at c ^ (r & 7))
-          uint32_t w4[4];
-          ldmatrix_x4(sbase + ld_row_off + ((((4 * khh + 2 * pq) + ld_chunk) ^ ld_row7) << 4), w4[0], w4[1], w4[2],
-                      w4[3]);
-  #pragma unroll
-          for (int q = 0; q < 2; ++q) {
-            const int m = 2 * pq + q;
-            const int c = 4 * khh + m;  // group of the stage
-            const uint32_t wa = w4[2 * q], wb = w4[2 * q + 1];
-            // activations K 32c + 8t .. + 7 of route g: (x0 x1) (x2 x3) (x4 x5) (x6 x7),
-            // paired as the codes: (x0 x4) (x1 x5) | (x2 x6) (x3 x7)
-            const uint4 xv = *reinterpret_cast<const uint4*>(sXr + (4 * c + t) * 16);
-            const uint32_t b0 = __byte_perm(xv.x, xv.z, 0x5410), b1 = __byte_perm(xv.x, xv.z, 0x7632);
-            const uint32_t b2 = __byte_perm(xv.y, xv.w, 0x5410), b3 = __byte_perm(xv.y, xv.w, 0x7632);
-            float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-            mma_16816<DT>(d, code_pair<DT>(wa), code_pair<DT>(wb), code_pair<DT>(wa >> 4), code_pair<DT>(wb >> 4),
-                          b0, b1);
-            mma_16816<DT>(d, code_pair<DT>(wa >> 8), code_pair<DT>(wb >> 8), code_pair<DT>(wa >> 12),
-                          code_pair<DT>(wb >> 12), b2, b3);
-            // BF16 group scales of rowA / rowB -> FP32 exactly
-            const uint32_t swa = (m < 2) ? sa.x : sa.y, swb = (m < 2) ? sb.x : sb.y;
-            const float fa = __uint_as_float((m & 1) ? (swa & 0xFFFF0000u) : (swa << 16));
-            const float fb = __uint_as_float((m & 1) ? (swb & 0xFFFF0000u) : (swb << 16));
-            tot[0] = fmaf(fa, d[0], tot[0]);
-            tot[1] = fmaf(fa, d[1], tot[1]);
-            tot[2] = fmaf(fb, d[2], tot[2]);
-            tot[3] = fmaf(fb, d[3], tot[3]);
-          }
+    for (int pp = 0; pp < (FULLK ? 4 : 2); ++pp) {
+      const int pq = FULLK ? pp : 2 * kh + pp;
+      // words t of rowA / rowB in groups 2 pq and 2 pq + 1 (128-byte swizzle:
+      // chunk c of row r at c ^ (r & 7))
+      uint32_t w4[4];
+      ldmatrix_x4(sbase + ld_row_off + (((2 * pq + ld_chunk) ^ ld_row7) << 4), w4[0], w4[1], w4[2], w4[3]);
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        const int c = 2 * pq + q;  // group of the stage
+        const uint32_t wa = w4[2 * q], wb = w4[2 * q + 1];
+        const uint32_t a0 = code_pair<DT>(wa), a1 = code_pair<DT>(wb);
+        const uint32_t a2 = code_pair<DT>(wa >> 4), a3 = code_pair<DT>(wb >> 4);
+        const uint32_t a4 = code_pair<DT>(wa >> 8), a5 = code_pair<DT>(wb >> 8);
+        const uint32_t a6 = code_pair<DT>(wa >> 12), a7 = code_pair<DT>(wb >> 12);
+        // BF16 group scales of rowA / rowB -> FP32 exactly
+        const float fa = __uint_as_float(q ? (saw[pp] & 0xFFFF0000u) : (saw[pp] << 16));
+        const float fb = __uint_as_float(q ? (sbw[pp] & 0xFFFF0000u) : (sbw[pp] << 16));
+#pragma unroll
+        for (int n = 0; n < NB; ++n) {
+          // activations K 32c + 8t .. + 7 of route 8n + g: (x0 x1) (x2 x3) (x4 x5)
+          // (x6 x7), paired as the codes: (x0 x4) (x1 x5) | (x2 x6) (x3 x7)
+          const uint4 xv = *reinterpret_cast<const uint4*>(sX + n * 8 * kGvRouteBytes + (4 * c + t) * 16);
+          float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+          mma_16816<DT>(d[0], d[1], d[2], d[3], a0, a1, a2, a3, __byte_perm(xv.x, xv.z, 0x5410),
+                        __byte_perm(xv.x, xv.z, 0x7632));
+          mma_16816<DT>(d[0], d[1], d[2], d[3], a4, a5, a6, a7, __byte_perm(xv.y, xv.w, 0x5410),
+                        __byte_perm(xv.y, xv.w, 0x7632));
+          tot[4 * n + 0] = fmaf(fa, d[0], tot[4 * n + 0]);
+          tot[4 * n + 1] = fmaf(fa, d[1], tot[4 * n + 1]);
+          tot[4 * n + 2] = fmaf(fb, d[2], tot[4 * n + 2]);
+          tot[4 * n + 3] = fmaf(fb, d[3], tot[4 * n + 3]);
         }
-      } else {
-        // boxes (row block, K half) of 32 row pairs x 128 K bytes, 128-byte swizzle
-        const int prA = (rowA & 63) >> 1, prB = (rowB & 63) >> 1;
-        const uint8_t* pA = sA + ((rowA >> 6) * 2 + khh) * 4096 + prA * 128;
-        const uint8_t* pB = sA + ((rowB >> 6) * 2 + khh) * 4096 + prB * 128;
-  #pragma unroll
-        for (int m = 0; m < 2; ++m) {
-          const int jj = 4 * m + t;  // 16-K chunk of the K half
-          const uint4 ca = *reinterpret_cast<const uint4*>(pA + ((jj ^ (prA & 7)) << 4));
-          const uint4 cb = *reinterpret_cast<const uint4*>(pB + ((jj ^ (prB & 7)) << 4));
-          // activations of the chunk (K 128 khh + 16 jj .. + 15 of route g)
-          const uint8_t* xp = sXr + (8 * khh + jj) * 32;
-          const uint4 x0 = *reinterpret_cast<const uint4*>(xp);
-          const uint4 x1 = *reinterpret_cast<const uint4*>(xp + 16);
-          const uint32_t wa[4] = {ca.x, ca.y, ca.z, ca.w}, wb[4] = {cb.x, cb.y, cb.z, cb.w};
-          const uint32_t xb[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-  #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const uint32_t a = wa[i] >> pc_shift, b = wb[i] >> pc_shift;
-            // word i = K 4i .. 4i + 3: code pairs (k0, k2), (k1, k3); activations likewise
-            mma_16816<DT>(tot, code_pair<DT>(a), code_pair<DT>(b), code_pair<DT>(a >> 8), code_pair<DT>(b >> 8),
-                          __byte_perm(xb[2 * i], xb[2 * i + 1], 0x5410),
-                          __byte_perm(xb[2 * i], xb[2 * i + 1], 0x7632));
+      }
+    }
+  } else {
+    // boxes (row block, K half) of 32 row pairs x 128 K bytes, 128-byte swizzle
+    const int pc_shift = (rowA & 1) * 4;  // the rows' nibble (rowA, rowB: same parity)
+    const int prA = (rowA & 63) >> 1, prB = (rowB & 63) >> 1;
+#pragma unroll
+    for (int hh = 0; hh < (FULLK ? 2 : 1); ++hh) {
+      const int h = FULLK ? hh : kh;
+      const uint8_t* pA = sA + ((rowA >> 6) * 2 + h) * 4096 + prA * 128;
+      const uint8_t* pB = sA + ((rowB >> 6) * 2 + h) * 4096 + prB * 128;
+#pragma unroll
+      for (int m = 0; m < 2; ++m) {
+        const int jj = 4 * m + t;  // 16-K chunk of the K half
+        const uint4 ca = *reinterpret_cast<const uint4*>(pA + ((jj ^ (prA & 7)) << 4));
+        const uint4 cb = *reinterpret_cast<const uint4*>(pB + ((jj ^ (prB & 7)) << 4));
+        const uint32_t wa[4] = {ca.x, ca.y, ca.z, ca.w}, wb[4] = {cb.x, cb.y, cb.z, cb.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          // word i = K 4i .. 4i + 3: code pairs (k0, k2), (k1, k3); activations likewise
+          const uint32_t a = wa[i] >> pc_shift, b = wb[i] >> pc_shift;
+          const uint32_t a0 = code_pair<DT>(a), a1 = code_pair<DT>(b);
+          const uint32_t a2 = code_pair<DT>(a >> 8), a3 = code_pair<DT>(b >> 8);
+#pragma unroll
+          for (int n = 0; n < NB; ++n) {
+            // activations K 128 h + 16 jj + 4 i .. + 3 of route 8n + g
+            const uint2 xv = *reinterpret_cast<const uint2*>(sX + n * 8 * kGvRouteBytes + (8 * h + jj) * 32 + i * 8);
+            mma_16816<DT>(tot[4 * n + 0], tot[4 * n + 1], tot[4 * n + 2], tot[4 * n + 3], a0, a1, a2, a3,
+                          __byte_perm(xv.x, xv.y, 0x5410), __byte_perm(xv.x, xv.y, 0x7632));
           }
         }
       }
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[st]);
-    ring_next(st, ph);
   }
+}
 
-  // ---------------------------------------------------------------- epilogue
-  auto epi_sync = [&]() -> bool {
-    __syncwarp();
-    if (lane == 0) mbar_arrive(epibar);
-    const bool ok = mbar_wait(epibar, eph & 1, abort_flag, p.err);
-    ++eph;
-    return ok;
-  };
-  // K halves meet: the second half's warps leave their sums in one of two
-  // buffers (alternating per unit: a buffer is rewritten only after every warp
-  // passed the next barrier, i.e. after the first half read it).
-  bool fin = true;  // this warp finishes the unit
-  if (!ALT) {
-    float4* rbuf = reinterpret_cast<float4*>(red) + ((eph & 1) * 8 + rb) * 32 + lane;
-    if (kh == 1) *rbuf = make_float4(tot[0], tot[1], tot[2], tot[3]);
-    if (!epi_sync()) return false;
-    fin = kh == 0;  // the first half finishes the unit
-    if (fin) {
-      const float4 o = *rbuf;
-      tot[0] += o.x;
-      tot[1] += o.y;
-      tot[2] += o.z;
-      tot[3] += o.w;
-    }
-  }
+// Epilogue of one unit on one compute warp; only `fin` warps hold final sums
+// and store, every warp takes part in the split-K barriers.
+template <int WHICH, int SCALE, int DT, int NB>
+__device__ __forceinline__ bool gemv_epilogue(const GemmParams& p, uint64_t* epibar, volatile int* abort_flag,
+                                              volatile int* fixup_flag, const Unit& w, int e, int m0, int rows,
+                                              int rowA, int rowB, int rb, int lane, bool fin, uint32_t& eph,
+                                              const float (&tot)[4 * NB]) {
+  using T = F16<DT>;
+  const int t = lane & 3;
+  const bool gated = (WHICH == GEMM_UP && p.act == ACT_SWIGLU);
+  const int N1 = p.n_rows;
   int r0, r1;
   tile_row_bases<WHICH>(p, w.nt, r0, r1);
   const int growA = rowA < 64 ? r0 + rowA : r1 + (rowA - 64);  // weight rows in the expert
@@ -311,44 +298,56 @@ __device__ __forceinline__ bool gemv_unit(const GemmParams& p, uint8_t* smem, ui
     if (okA) scA = bf16_bits_to_float(p.scales[static_cast<int64_t>(e) * N1 + growA]);
     if (okB) scB = bf16_bits_to_float(p.scales[static_cast<int64_t>(e) * N1 + growB]);
   }
-  const float vA0 = tot[0] * scA, vA1 = tot[1] * scA, vB0 = tot[2] * scB, vB1 = tot[3] * scB;
-  const int rt0 = 2 * t, rt1 = 2 * t + 1;  // this lane's routes
+  // Bounded barrier over the 16 compute warps.
+  auto grp_sync = [&]() -> bool {
+    __syncwarp();
+    if (lane == 0) mbar_arrive(epibar);
+    const bool ok = mbar_wait(epibar, eph & 1, abort_flag, p.err);
+    ++eph;
+    return ok;
+  };
 
   if (WHICH == GEMM_DOWN) {
-    if (fin) {
-      float* y = reinterpret_cast<float*>(p.out) + (static_cast<int64_t>(w.split) * p.slots_cap + m0) * p.out_cols;
-      const int64_t oc = p.out_cols;
-      if (rt0 < rows && okA) y[rt0 * oc + growA] = vA0;
-      if (rt1 < rows && okA) y[rt1 * oc + growA] = vA1;
-      if (rt0 < rows && okB) y[rt0 * oc + growB] = vB0;
-      if (rt1 < rows && okB) y[rt1 * oc + growB] = vB1;
+    if (!fin) return true;
+    float* y = reinterpret_cast<float*>(p.out) + (static_cast<int64_t>(w.split) * p.slots_cap + m0) * p.out_cols;
+    const int64_t oc = p.out_cols;
+#pragma unroll
+    for (int n = 0; n < NB; ++n) {
+      const int rt0 = 8 * n + 2 * t, rt1 = rt0 + 1;
+      if (rt0 < rows && okA) y[rt0 * oc + growA] = tot[4 * n + 0] * scA;
+      if (rt1 < rows && okA) y[rt1 * oc + growA] = tot[4 * n + 1] * scA;
+      if (rt0 < rows && okB) y[rt0 * oc + growB] = tot[4 * n + 2] * scB;
+      if (rt1 < rows && okB) y[rt1 * oc + growB] = tot[4 * n + 3] * scB;
     }
     return true;
   }
 
   uint16_t* inter = reinterpret_cast<uint16_t*>(p.out) + static_cast<int64_t>(m0) * p.inter;
   if (p.splits > 1) {
-    if (fin) {
-      float* part = p.part + (static_cast<int64_t>(w.split) * p.slots_cap + m0) * N1;
-      if (rt0 < rows && okA) part[static_cast<int64_t>(rt0) * N1 + growA] = vA0;
-      if (rt1 < rows && okA) part[static_cast<int64_t>(rt1) * N1 + growA] = vA1;
-      if (rt0 < rows && okB) part[static_cast<int64_t>(rt0) * N1 + growB] = vB0;
-      if (rt1 < rows && okB) part[static_cast<int64_t>(rt1) * N1 + growB] = vB1;
+    float* part = p.part + (static_cast<int64_t>(w.split) * p.slots_cap + m0) * N1;
+#pragma unroll
+    for (int n = 0; n < NB; ++n) {
+      const int rt0 = 8 * n + 2 * t, rt1 = rt0 + 1;
+      if (!fin) break;
+      if (rt0 < rows && okA) part[static_cast<int64_t>(rt0) * N1 + growA] = tot[4 * n + 0] * scA;
+      if (rt1 < rows && okA) part[static_cast<int64_t>(rt1) * N1 + growA] = tot[4 * n + 1] * scA;
+      if (rt0 < rows && okB) part[static_cast<int64_t>(rt0) * N1 + growB] = tot[4 * n + 2] * scB;
+      if (rt1 < rows && okB) part[static_cast<int64_t>(rt1) * N1 + growB] = tot[4 * n + 3] * scB;
     }
     // The last split to finish sums the partials in split order
     // (deterministic) and applies the activation.
     __threadfence();
-    if (!epi_sync()) return false;
-    if (rb == 0 && kh == 0 && lane == 0) {
+    if (!grp_sync()) return false;
+    if (fin && rb == 0 && lane == 0) {
       const int prev = atomicAdd(&p.counters[w.tile * p.n_tiles + w.nt], 1);
       *fixup_flag = (prev == p.splits - 1) ? 1 : 0;
     }
-    if (!epi_sync()) return false;
+    if (!grp_sync()) return false;
     const bool last = *fixup_flag != 0;
     if (last && fin) {
       __threadfence();
       const int64_t sstride = p.slots_cap * static_cast<int64_t>(N1);
-      // lanes t take routes t and t + 4 of their rows
+      // lanes t take routes t, t + 4, ... of their rows
       for (int r = t; r < rows; r += 4) {
         const float* src = p.part + static_cast<int64_t>(m0 + r) * N1;
         if (gated) {
@@ -374,12 +373,18 @@ __device__ __forceinline__ bool gemv_unit(const GemmParams& p, uint8_t* smem, ui
           }
         }
       }
+      if (rb == 0 && lane == 0) p.counters[w.tile * p.n_tiles + w.nt] = 0;
     }
-    if (last && rb == 0 && kh == 0 && lane == 0) p.counters[w.tile * p.n_tiles + w.nt] = 0;
+    // the flag is rewritten only after this group's next two barriers
     return true;
   }
 
-  if (fin) {
+  if (!fin) return true;
+#pragma unroll
+  for (int n = 0; n < NB; ++n) {
+    const int rt0 = 8 * n + 2 * t, rt1 = rt0 + 1;
+    const float vA0 = tot[4 * n + 0] * scA, vA1 = tot[4 * n + 1] * scA;
+    const float vB0 = tot[4 * n + 2] * scB, vB1 = tot[4 * n + 3] * scB;
     if (gated) {
       // rowA = gate row, rowB = its up row (same intermediate index)
       const int i = 64 * w.nt + (rowA & 63);
@@ -401,32 +406,98 @@ __device__ __forceinline__ bool gemv_unit(const GemmParams& p, uint8_t* smem, ui
   return true;
 }
 
+// One unit on one compute warp of group `grp`.  Units of several stages
+// (!alt): the warp computes K half `grp` of every stage and the halves meet in
+// the exchange buffer.  Single-stage units (alt): group `grp` takes the units
+// of ordinal parity `grp` over the full K, on a ring of its own.
+//
+// Every consumer of a ring waits on every phase of its slots: a ring is shared
+// by all 16 compute warps (!alt), or belongs to one group (alt), whose 8 warps
+// are then its only consumers.  Parity waits therefore never see a slot more
+// than one phase away, and the producer refills a slot only after all of its
+// consumers left it.
+template <int WHICH, int SCALE, int DT, int NB>
+__device__ __forceinline__ bool gemv_unit(const GemmParams& p, uint8_t* smem, uint64_t* full, uint64_t* bfull,
+                                          uint64_t* empty, uint64_t* epibar, volatile int* abort_flag,
+                                          volatile int* fixup_flag, float* red, const Unit& w, const int4& ti,
+                                          bool alt, int grp, int rowA, int rowB, int rb, int lane,
+                                          uint32_t ld_row_off, int ld_row7, int ld_chunk, int ring0, int ring_len,
+                                          int& st, uint32_t& ph, uint32_t& eph) {
+  float tot[4 * NB];
+#pragma unroll
+  for (int j = 0; j < 4 * NB; ++j) tot[j] = 0.0f;
+  for (int kb = w.kb0; kb < w.kb1; ++kb) {
+    const int slot = ring0 + st;
+    if (!mbar_wait(&full[slot], ph, abort_flag, p.err) || !mbar_wait(&bfull[slot], ph, abort_flag, p.err))
+      return false;
+    const uint8_t* sA = smem + slot * p.stage_bytes;
+    if (alt) gemv_stage<SCALE, DT, NB, true>(sA, rowA, rowB, grp, lane, ld_row_off, ld_row7, ld_chunk, tot);
+    else gemv_stage<SCALE, DT, NB, false>(sA, rowA, rowB, grp, lane, ld_row_off, ld_row7, ld_chunk, tot);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[slot]);
+    ring_next(st, ph, ring_len);
+  }
+  bool fin = true;
+  if (!alt) {
+    // K halves meet: group 1 leaves its sums in one of two buffers (alternating
+    // per unit: a buffer is rewritten only after every warp passed the next
+    // barrier, i.e. after group 0 read it); group 0 adds them and finishes.
+    float4* rbuf = reinterpret_cast<float4*>(red) + ((eph & 1) * 8 + rb) * NB * 32 + lane;
+    if (grp == 1) {
+#pragma unroll
+      for (int n = 0; n < NB; ++n)
+        rbuf[n * 32] = make_float4(tot[4 * n + 0], tot[4 * n + 1], tot[4 * n + 2], tot[4 * n + 3]);
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(epibar);
+    if (!mbar_wait(epibar, eph & 1, abort_flag, p.err)) return false;
+    ++eph;
+    fin = grp == 0;
+    if (fin) {
+#pragma unroll
+      for (int n = 0; n < NB; ++n) {
+        const float4 o = rbuf[n * 32];
+        tot[4 * n + 0] += o.x;
+        tot[4 * n + 1] += o.y;
+        tot[4 * n + 2] += o.z;
+        tot[4 * n + 3] += o.w;
+      }
+    }
+  }
+  return gemv_epilogue<WHICH, SCALE, DT, NB>(p, epibar, abort_flag, fixup_flag, w, ti.x, ti.y,
+                                             min(ti.z, kGemvMaxR), rowA, rowB, rb, lane, fin, eph, tot);
+}
+
 template <int WHICH, int SCALE, int DT>
 __global__ void __launch_bounds__(kGemvThreads, 1)
     w4a16_gemv_kernel(const __grid_constant__ GemmParams p, const __grid_constant__ CUtensorMap tmA,
                       const __grid_constant__ CUtensorMap tmS) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  uint8_t* ctrl = smem + kGemvStages * kGemvStageBytes;
+  const int stages = p.stages;
+  uint8_t* ctrl = smem + stages * p.stage_bytes;
   uint64_t* full = reinterpret_cast<uint64_t*>(ctrl);
-  uint64_t* bfull = full + kGemvStages;
-  uint64_t* empty = bfull + kGemvStages;
-  uint64_t* epibar = empty + kGemvStages;
+  uint64_t* bfull = full + kGemvMaxStages;
+  uint64_t* empty = bfull + kGemvMaxStages;
+  uint64_t* epibar = empty + kGemvMaxStages;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(epibar + 1);
   volatile int* fixup_flag = abort_flag + 1;
-  float* red = reinterpret_cast<float*>(ctrl + kGvCtrlRedOff);
   int4* tile_tab = reinterpret_cast<int4*>(ctrl + kGvCtrlTabOff);
+  float* red = reinterpret_cast<float*>(ctrl + kGvCtrlRedOff);
+  // single-stage units without split: the compute groups take alternate units,
+  // each on a ring of its own (slots [0, ring_len) and [ring_len, 2 ring_len))
+  const bool alt = p.splits == 1 && p.kb_total == 1;
+  const int ring_len = alt ? stages / 2 : stages;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const int G = static_cast<int>(gridDim.x);
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kGemvStages; ++s) {
-      mbar_init(&full[s], 1);                  // producer (TMA bytes + scale copies)
-      mbar_init(&bfull[s], 32);                // the 32 lanes' activation copies
-      // every compute warp, or one warp group of 8 when the groups take
-      // alternate single-stage units
-      mbar_init(&empty[s], (p.splits == 1 && p.kb_total == 1) ? kGemvComputeWarps / 2 : kGemvComputeWarps);
+    for (int s = 0; s < stages; ++s) {
+      mbar_init(&full[s], 1);                    // producer (TMA bytes + scale copies)
+      mbar_init(&bfull[s], 32);                  // the 32 lanes' activation copies
+      mbar_init(&empty[s], alt ? kGemvComputeWarps / 2 : kGemvComputeWarps);  // the ring's consumers
     }
     mbar_init(epibar, kGemvComputeWarps);
     *abort_flag = 0;
@@ -461,8 +532,9 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
     const uint64_t pol_s = l2_policy_evict_last();  // each scale sector serves two stages
     const int groups_row = p.K / kGroup;
     const int sbytes_row = groups_row * 2;
-    int st = 0;
-    uint32_t ph = 0, issued = 0;
+    const bool stma = SCALE == SCALE_GROUP && p.scale_tma;
+    int st_r0 = 0, st_r1 = 0;
+    uint32_t ph_r0 = 0, ph_r1 = 0, issued_r0 = 0, issued_r1 = 0;
     bool ok = true;
     UnitIter it;
     it.init(p);
@@ -473,62 +545,50 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
       const int e = ti.x;
       int r0, r1;
       tile_row_bases<WHICH>(p, w.nt, r0, r1);
-      // scale rows of this unit for this lane's tile rows (lane + 32 i); null
-      // when the row lies beyond the expert's rows
-      const uint8_t* srow[4];
-      bool srow_al16 = true;
-      if (SCALE == SCALE_GROUP && !p.scale_tma) {
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int tr = lane + 32 * j;
-          const int grow = tr < 64 ? r0 + tr : r1 + (tr - 64);
-          srow[j] = grow < N1 ? reinterpret_cast<const uint8_t*>(p.scales) +
-                                    (static_cast<int64_t>(e) * N1 + grow) * sbytes_row
-                              : nullptr;
-          srow_al16 = srow_al16 && ((reinterpret_cast<uintptr_t>(srow[j]) & 15) == 0);
-        }
-      }
+      const int ring = alt ? (i & 1) : 0;
+      int st = ring ? st_r1 : st_r0;
+      uint32_t ph = ring ? ph_r1 : ph_r0;
       for (int kb = w.kb0; kb < w.kb1; ++kb) {
-        if (!mbar_wait(&empty[st], ph ^ 1u, abort_flag, p.err)) {
+        const int slot = ring * ring_len + st;
+        if (!mbar_wait(&empty[slot], ph ^ 1u, abort_flag, p.err)) {
           ok = false;
           break;
         }
-        uint8_t* sA = smem + st * kGemvStageBytes;
+        uint8_t* sA = smem + slot * p.stage_bytes;
         uint8_t* sS = sA + kGvOffS;
-        if (SCALE == SCALE_GROUP && !p.scale_tma) {
-          // the stage's 8 group scales (16 bytes) of each tile row
+        if (SCALE == SCALE_GROUP && !stma) {
+          // the stage's 8 group scales (16 bytes) of each tile row (lane + 32 j);
+          // rows beyond the expert's rows read as zero
           const int g0 = kb * (kGemvBlockK / kGroup);
           const int ng = min(kGemvBlockK / kGroup, groups_row - g0);
-          if (srow_al16 && ng == kGemvBlockK / kGroup) {
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              uint8_t* dst = sS + (lane + 32 * j) * kGvScaleRowBytes;
-              if (srow[j]) cp_async_cg16(dst, srow[j] + g0 * 2, 16u);
-              else *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
-            }
-          } else {
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              uint8_t* dst = sS + (lane + 32 * j) * kGvScaleRowBytes;
-              const int nbytes = srow[j] ? max(ng, 0) * 2 : 0;
-              for (int o = 0; o < nbytes; o += 4) cp_async<4>(dst + o, srow[j] + g0 * 2 + o);
+          for (int j = 0; j < 4; ++j) {
+            const int tr = lane + 32 * j;
+            const int grow = tr < 64 ? r0 + tr : r1 + (tr - 64);
+            uint8_t* dst = sS + tr * kGvScaleRowBytes;
+            const uint8_t* src = reinterpret_cast<const uint8_t*>(p.scales) +
+                                 (static_cast<int64_t>(e) * N1 + grow) * sbytes_row + g0 * 2;
+            const int nbytes = grow < N1 ? max(ng, 0) * 2 : 0;
+            if (nbytes == kGvScaleRowBytes && (reinterpret_cast<uintptr_t>(src) & 15) == 0) {
+              cp_async_cg16(dst, src, 16u);
+            } else {
+              for (int o = 0; o < nbytes; o += 4) cp_async<4>(dst + o, src + o);
               for (int o = nbytes; o < kGvScaleRowBytes; o += 4) *reinterpret_cast<uint32_t*>(dst + o) = 0u;
             }
           }
-          cp_async_mbar_arrive(&full[st]);
+          cp_async_mbar_arrive(&full[slot]);
         }
         __syncwarp();
         if (lane == 0) {
-          const bool stma = SCALE == SCALE_GROUP && p.scale_tma;
-          mbar_arrive_expect_tx(&full[st], kGvWeightBytes + (stma ? kTileRows * kGvScaleRowBytes : 0));
+          mbar_arrive_expect_tx(&full[slot], kGvWeightBytes + (stma ? kTileRows * kGvScaleRowBytes : 0));
           if (SCALE == SCALE_GROUP) {
             // two 64-row boxes of 128 packed bytes (256 K values)
-            tma_load_3d(sA, &tmA, &full[st], kb * (kGemvBlockK / 2), r0, e, pol_w);
-            tma_load_3d(sA + 8192, &tmA, &full[st], kb * (kGemvBlockK / 2), r1, e, pol_w);
+            tma_load_3d(sA, &tmA, &full[slot], kb * (kGemvBlockK / 2), r0, e, pol_w);
+            tma_load_3d(sA + 8192, &tmA, &full[slot], kb * (kGemvBlockK / 2), r1, e, pol_w);
             if (stma) {
               // two 64-row boxes of the stage's 8 BF16 scales
-              tma_load_3d(sS, &tmS, &full[st], kb * (kGemvBlockK / kGroup), r0, e, pol_s);
-              tma_load_3d(sS + 64 * kGvScaleRowBytes, &tmS, &full[st], kb * (kGemvBlockK / kGroup), r1, e, pol_s);
+              tma_load_3d(sS, &tmS, &full[slot], kb * (kGemvBlockK / kGroup), r0, e, pol_s);
+              tma_load_3d(sS + 64 * kGvScaleRowBytes, &tmS, &full[slot], kb * (kGemvBlockK / kGroup), r1, e, pol_s);
             }
           } else {
             // (row block, K half) boxes of 32 row pairs x 128 K bytes
@@ -536,21 +596,33 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
             for (int b = 0; b < 2; ++b)
 #pragma unroll
               for (int h = 0; h < 2; ++h)
-                tma_load_3d(sA + (b * 2 + h) * 4096, &tmA, &full[st], kb * kGemvBlockK + h * 128,
+                tma_load_3d(sA + (b * 2 + h) * 4096, &tmA, &full[slot], kb * kGemvBlockK + h * 128,
                             (b ? r1 : r0) / 2, e, pol_w);
           }
         }
         __syncwarp();
-        ++issued;
-        ring_next(st, ph);
+        if (ring) ++issued_r1;
+        else ++issued_r0;
+        ring_next(st, ph, ring_len);
+      }
+      if (ring) {
+        st_r1 = st;
+        ph_r1 = ph;
+      } else {
+        st_r0 = st;
+        ph_r0 = ph;
       }
     }
     // Wind-down after an abort: wait (bounded) for the copies still in flight.
     if (!ok && lane == 0) {
       volatile int no_abort = 0;
-      const uint32_t from = issued > static_cast<uint32_t>(kGemvStages) ? issued - kGemvStages : 0;
-      for (uint32_t j = from; j < issued; ++j)
-        mbar_wait(&full[j % kGemvStages], (j / kGemvStages) & 1, &no_abort, p.err);
+      auto drain = [&](int r, uint32_t n) {
+        const uint32_t from = n > static_cast<uint32_t>(ring_len) ? n - ring_len : 0;
+        for (uint32_t j = from; j < n; ++j)
+          mbar_wait(&full[r * ring_len + j % ring_len], (j / ring_len) & 1, &no_abort, p.err);
+      };
+      drain(0, issued_r0);
+      if (alt) drain(1, issued_r1);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------------ activation rows
@@ -559,8 +631,8 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
     // zero-filled by the copy.  Each lane's cp.async.mbarrier.arrive marks the
     // stage's bfull once its copies have landed; the warp never blocks on them.
     const uint16_t* xsrc = reinterpret_cast<const uint16_t*>(p.x);
-    int st = 0;
-    uint32_t ph = 0;
+    int st_r0 = 0, st_r1 = 0;
+    uint32_t ph_r0 = 0, ph_r1 = 0;
     bool ok = true;
     // source row of route `lane` of a tile (lanes below its route count)
     auto src_of = [&](const int4& t) -> int {
@@ -584,12 +656,16 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
       const int4 ti = tile_of(p, tile_tab, i, u);
       const int src = src_next;
       const int rows = min(ti.z, kGemvMaxR);
+      const int ring = alt ? (i & 1) : 0;
+      int st = ring ? st_r1 : st_r0;
+      uint32_t ph = ring ? ph_r1 : ph_r0;
       for (int kb = w.kb0; kb < w.kb1; ++kb) {
-        if (!mbar_wait(&empty[st], ph ^ 1u, abort_flag, p.err)) {
+        const int slot = ring * ring_len + st;
+        if (!mbar_wait(&empty[slot], ph ^ 1u, abort_flag, p.err)) {
           ok = false;
           break;
         }
-        uint8_t* xs = smem + st * kGemvStageBytes + kGvOffX;
+        uint8_t* xs = smem + slot * p.stage_bytes + kGvOffX;
         const int col = kb * kGemvBlockK + lane * 8;
         const bool valid = col < p.K;
         for (int r = 0; r < rows; ++r) {
@@ -597,11 +673,18 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
           cp_async_cg16(xs + r * kGvRouteBytes + lane * 16,
                         xsrc + static_cast<int64_t>(srow) * p.K + (valid ? col : 0), valid ? 16u : 0u);
         }
-        cp_async_mbar_arrive_noinc(&bfull[st]);
-        ring_next(st, ph);
+        cp_async_mbar_arrive_noinc(&bfull[slot]);
+        ring_next(st, ph, ring_len);
+      }
+      if (ring) {
+        st_r1 = st;
+        ph_r1 = ph;
+      } else {
+        st_r0 = st;
+        ph_r0 = ph;
       }
       // the next unit's source rows, loaded while this unit streams
-      const int u_next = u + static_cast<int>(gridDim.x);
+      const int u_next = u + G;
       if (u_next < n_units) src_next = src_of(tile_of(p, tile_tab, i + 1, u_next));
     }
     // Every copy lands before the CTA exits (bounded by the compute warps'
@@ -609,31 +692,38 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
     asm volatile("cp.async.wait_all;" ::: "memory");
   } else {
     // ------------------------------------------------------------------ compute + epilogue
-    // warp 2 + c: row block rb = c % 8 (16 MMA rows), K half kh = c / 8
-    const int cw = warp - 2, rb = cw & 7, kh = cw >> 3, g = lane >> 2;
+    // warp 2 + c: group c / 8 (K half, or units of that ordinal parity when
+    // alt), row block rb = c % 8
+    const int cw = warp - 2, grp = cw >> 3, rb = cw & 7, g = lane >> 2;
     const bool gated = (WHICH == GEMM_UP && p.act == ACT_SWIGLU);
     // SwiGLU: MMA row g = gate row, g + 8 = its up row; otherwise 16 consecutive rows
     const int rowA = gated ? 8 * rb + g : 16 * rb + g;
     const int rowB = gated ? 64 + 8 * rb + g : 16 * rb + 8 + g;
-    // single-stage units without split: the groups (kh) take alternate units
-    const bool alt = p.splits == 1 && p.kb_total == 1;
+    // ldmatrix row of this lane: matrix l / 8 = (rowA or rowB of row l % 8, group
+    // offset 0 or 1); byte offset of the row in the stage, its swizzle phase
+    const int ld_i = lane & 7, ld_j = lane >> 3;
+    const int ld_row = (ld_j & 1) ? rowB - g + ld_i : rowA - g + ld_i;
+    const uint32_t ld_row_off = (ld_row >> 6) * 8192 + (ld_row & 63) * 128;
+    const int ld_row7 = ld_row & 7, ld_chunk = ld_j >> 1;
     int st = 0;
     uint32_t ph = 0, eph = 0;
     UnitIter it;
     it.init(p);
+    const int ring0 = alt ? grp * ring_len : 0;
     for (int i = 0; it.u < n_units; it.next(p), ++i) {
-      if (alt && (i & 1) != kh) {  // the other group's unit: skip its one stage
-        ring_next(st, ph);
-        continue;
-      }
+      if (alt && (i & 1) != grp) continue;  // the other group's unit, on the other ring
       const Unit w = it.unit(p);
       const int4 ti = tile_of(p, tile_tab, i, it.u);
-      const int rows = min(ti.z, kGemvMaxR);
-      const bool ok =
-          alt ? gemv_unit<WHICH, SCALE, DT, true>(p, smem, full, bfull, empty, epibar, abort_flag, fixup_flag, red,
-                                                  w, ti.x, ti.y, rows, rowA, rowB, rb, kh, lane, st, ph, eph)
-              : gemv_unit<WHICH, SCALE, DT, false>(p, smem, full, bfull, empty, epibar, abort_flag, fixup_flag, red,
-                                                   w, ti.x, ti.y, rows, rowA, rowB, rb, kh, lane, st, ph, eph);
+      const int nb = (min(ti.z, kGemvMaxR) + 7) >> 3;
+      bool ok;
+#define W4A16_GEMV_UNIT(NBV)                                                                                    \
+  gemv_unit<WHICH, SCALE, DT, NBV>(p, smem, full, bfull, empty, epibar, abort_flag, fixup_flag, red, w, ti, alt, \
+                                   grp, rowA, rowB, rb, lane, ld_row_off, ld_row7, ld_chunk, ring0, ring_len, st, \
+                                   ph, eph)
+      if (nb <= 1) ok = W4A16_GEMV_UNIT(1);
+      else if (nb == 2) ok = W4A16_GEMV_UNIT(2);
+      else ok = W4A16_GEMV_UNIT(4);
+#undef W4A16_GEMV_UNIT
       if (!ok) break;
     }
   }
@@ -642,17 +732,16 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
 
 template <int WHICH, int SCALE, int DT>
 cudaError_t launch_gemv_one(const GemmParams& p, const CUtensorMap& tmA, const CUtensorMap& tmS, int grid,
-                            cudaStream_t s, bool pdl) {
+                            int smem_bytes, cudaStream_t s, bool pdl) {
   auto kern = w4a16_gemv_kernel<WHICH, SCALE, DT>;
-  const int smem_bytes = gemv_smem_bytes();
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  static bool configured_for[64] = {false};
-  if (dev < 64 && !configured_for[dev]) {
+  static int configured_for[64] = {0};
+  if (dev < 64 && configured_for[dev] < smem_bytes) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
     if (e != cudaSuccess) return e;
-    configured_for[dev] = true;
+    configured_for[dev] = smem_bytes;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
@@ -669,13 +758,15 @@ cudaError_t launch_gemv_one(const GemmParams& p, const CUtensorMap& tmA, const C
 
 template <int DT>
 cudaError_t launch_gemv_dt(int which, int scale_kind, const GemmParams& p, const CUtensorMap& tmA,
-                           const CUtensorMap& tmS, int grid, cudaStream_t s, bool pdl) {
+                           const CUtensorMap& tmS, int grid, int smem_bytes, cudaStream_t s, bool pdl) {
   if (which == GEMM_UP) {
-    return scale_kind == SCALE_GROUP ? launch_gemv_one<GEMM_UP, SCALE_GROUP, DT>(p, tmA, tmS, grid, s, pdl)
-                                     : launch_gemv_one<GEMM_UP, SCALE_CHANNEL, DT>(p, tmA, tmS, grid, s, pdl);
+    return scale_kind == SCALE_GROUP
+               ? launch_gemv_one<GEMM_UP, SCALE_GROUP, DT>(p, tmA, tmS, grid, smem_bytes, s, pdl)
+               : launch_gemv_one<GEMM_UP, SCALE_CHANNEL, DT>(p, tmA, tmS, grid, smem_bytes, s, pdl);
   }
-  return scale_kind == SCALE_GROUP ? launch_gemv_one<GEMM_DOWN, SCALE_GROUP, DT>(p, tmA, tmS, grid, s, pdl)
-                                   : launch_gemv_one<GEMM_DOWN, SCALE_CHANNEL, DT>(p, tmA, tmS, grid, s, pdl);
+  return scale_kind == SCALE_GROUP
+             ? launch_gemv_one<GEMM_DOWN, SCALE_GROUP, DT>(p, tmA, tmS, grid, smem_bytes, s, pdl)
+             : launch_gemv_one<GEMM_DOWN, SCALE_CHANNEL, DT>(p, tmA, tmS, grid, smem_bytes, s, pdl);
 }
 
 }  // namespace w4a16

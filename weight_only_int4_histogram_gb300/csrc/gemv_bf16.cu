@@ -3,5 +3,5 @@
 
 namespace w4a16 {
 template cudaError_t launch_gemv_dt<DT_BF16>(int, int, const GemmParams&, const CUtensorMap&,
-                                               const CUtensorMap&, int, cudaStream_t, bool);
+                                               const CUtensorMap&, int, int, cudaStream_t, bool);
 }
