@@ -221,8 +221,8 @@ w4a16_status w4a16_moe_set_overrides(w4a16_moe_plan_t plan, int32_t tile_rows,
 /*
  * Chooses where the expert GEMMs run for later calls with this plan.
  * W4A16_PATH_AUTO (the default) takes the CUDA-core GEMV while the expected
- * routes per local expert, num_tokens * top_k / num_experts, are at most 12,
- * and the tensor cores above that.  Both paths compute the same function
+ * routes per local expert, num_tokens * top_k / num_experts, are at most 24
+ * (group scales) or 16 (per-channel scales), and the tensor cores above that.  Both paths compute the same function
  * (the expert MLPs of "feat(pytorch): add CuTeDSL W4A16 MoE backend"
  * (LMDeploy), section Modification); they round differently (the tensor-core
  * path rounds each dequantised weight q * s to the activation type, the

@@ -71,25 +71,27 @@ struct Layout {
 };
 
 // Expected routes per local expert up to which the warp-MMA GEMV runs both
-// GEMMs.  Its route tiles hold 8 routes, so above this an expert's weights are
-// streamed once per tile and the tcgen05 path (route tiles up to 128) wins;
-// measured crossovers on GB300 lay between 12 and 17 routes per expert for
-// the uniform-routing workloads.
-constexpr double kGemvMaxRoutesPerExpert = 12.0;
+// GEMMs; above it the tcgen05 path (route tiles up to 128 routes, MMA work
+// independent of the tile's fill) wins.  Measured crossovers on GB300: about
+// 27 routes per expert for the group-scale Kimi shape, 17-24 for the
+// per-channel workloads.
+constexpr double kGemvMaxRoutesGroup = 24.0;
+constexpr double kGemvMaxRoutesChannel = 16.0;
 
 bool use_gemv(const w4a16_moe_plan_s& P, int T) {
   if (P.path == W4A16_PATH_TENSOR_CORES) return false;
   if (P.path == W4A16_PATH_CUDA_CORES) return true;
   const double lam = static_cast<double>(T) * P.d.top_k / P.d.num_experts;
-  return lam <= kGemvMaxRoutesPerExpert;
+  return lam <= (P.d.scale_kind == W4A16_SCALE_GROUP32_K ? kGemvMaxRoutesGroup : kGemvMaxRoutesChannel);
 }
 
 // CUDA-core path: route tiles of 8, 16 or 32 routes (one, two or four MMA N
-// blocks), from the expected routes per expert plus ~3.5 standard deviations.
+// blocks).  Taller tiles stream an expert's weights fewer times but take
+// larger stages (a shallower ring); measured on GB300 they pay off from about
+// 4 (16 routes) and 10 (32 routes) expected routes per expert.
 int choose_bn_gemv(const w4a16_moe_plan_s& P, int T) {
   const double lam = static_cast<double>(T) * P.d.top_k / P.d.num_experts;
-  const double want = lam + 3.5 * std::sqrt(lam) + 1.0;
-  return want <= 8.0 ? 8 : (want <= 16.0 ? 16 : kGemvMaxR);
+  return lam <= 4.0 ? 8 : (lam <= 10.0 ? 16 : kGemvMaxR);
 }
 
 int choose_bn(const w4a16_moe_plan_s& P, int T) {

@@ -257,19 +257,28 @@ __device__ __forceinline__ void gemv_stage(const uint8_t* sA, int rowA, int rowB
         const uint4 ca = *reinterpret_cast<const uint4*>(pA + ((jj ^ (prA & 7)) << 4));
         const uint4 cb = *reinterpret_cast<const uint4*>(pB + ((jj ^ (prB & 7)) << 4));
         const uint32_t wa[4] = {ca.x, ca.y, ca.z, ca.w}, wb[4] = {cb.x, cb.y, cb.z, cb.w};
+        // code pairs of word i = K 4i .. 4i + 3: (k0, k2), (k1, k3)
+        uint32_t a0[4], a1[4], a2[4], a3[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          // word i = K 4i .. 4i + 3: code pairs (k0, k2), (k1, k3); activations likewise
           const uint32_t a = wa[i] >> pc_shift, b = wb[i] >> pc_shift;
-          const uint32_t a0 = code_pair<DT>(a), a1 = code_pair<DT>(b);
-          const uint32_t a2 = code_pair<DT>(a >> 8), a3 = code_pair<DT>(b >> 8);
+          a0[i] = code_pair<DT>(a);
+          a1[i] = code_pair<DT>(b);
+          a2[i] = code_pair<DT>(a >> 8);
+          a3[i] = code_pair<DT>(b >> 8);
+        }
 #pragma unroll
-          for (int n = 0; n < NB; ++n) {
-            // activations K 128 h + 16 jj + 4 i .. + 3 of route 8n + g
-            const uint2 xv = *reinterpret_cast<const uint2*>(sX + n * 8 * kGvRouteBytes + (8 * h + jj) * 32 + i * 8);
-            mma_16816<DT>(tot[4 * n + 0], tot[4 * n + 1], tot[4 * n + 2], tot[4 * n + 3], a0, a1, a2, a3,
-                          __byte_perm(xv.x, xv.y, 0x5410), __byte_perm(xv.x, xv.y, 0x7632));
-          }
+        for (int n = 0; n < NB; ++n) {
+          // activations K 128 h + 16 jj .. + 15 of route 8n + g, paired likewise
+          const uint8_t* xp = sX + n * 8 * kGvRouteBytes + (8 * h + jj) * 32;
+          const uint4 x0 = *reinterpret_cast<const uint4*>(xp);
+          const uint4 x1 = *reinterpret_cast<const uint4*>(xp + 16);
+          const uint32_t xb[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            mma_16816<DT>(tot[4 * n + 0], tot[4 * n + 1], tot[4 * n + 2], tot[4 * n + 3], a0[i], a1[i], a2[i],
+                          a3[i], __byte_perm(xb[2 * i], xb[2 * i + 1], 0x5410),
+                          __byte_perm(xb[2 * i], xb[2 * i + 1], 0x7632));
         }
       }
     }
