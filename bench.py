@@ -41,30 +41,35 @@ FALLBACK_BF16_TFLOPS = 1900.0
 
 
 def kernel_source_hash():
+    """Hash of the GEMM kernel sources; a committed traffic capture counts only
+    while it matches."""
     import hashlib
     h = hashlib.sha256()
     for f in ("weight_only_int4_histogram_gb300/csrc/gemm.cuh",
+              "weight_only_int4_histogram_gb300/csrc/gemv.cuh",
               "weight_only_int4_histogram_gb300/csrc/common.cuh"):
         with open(os.path.join(ROOT, f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
 
-def measured_traffic(workload, tokens, kernel):
-    """DRAM bytes per launch from the committed ncu summary, or None when the
-    capture does not match this workload or the kernel has changed since."""
+def measured_traffic(workload, tokens, kernel, path_name):
+    """DRAM bytes per launch from the committed ncu summaries, or None when no
+    capture matches this workload, kernel and GEMM path, or the kernel
+    sources have changed since."""
     path = os.path.join(ROOT, "profiles", "roofline_traffic.json")
     try:
         with open(path) as f:
             tr = json.load(f)
     except (OSError, ValueError):
         return None
-    if tr.get("workload") != workload or tr.get("tokens") != tokens:
-        return None
     if tr.get("kernel_source_hash") != kernel_source_hash():
         return None
-    v = tr.get(f"{kernel}_dram_bytes")
-    return int(v) if v is not None else None
+    for c in tr.get("captures", []):
+        if (c.get("workload"), c.get("tokens"), c.get("kernel"), c.get("gemm_path")) == \
+                (workload, tokens, kernel, path_name):
+            return int(c["dram_bytes"])
+    return None
 
 
 def load_peaks():
@@ -340,7 +345,7 @@ def run_gpu(args):
     roof = {"kernel": names[k], "bound": "hbm", "achieved": round(achieved, 1), "peak": hbm,
             "peak_kind": f"{peak_kind} hbm_gbs", "unit": "GB/s",
             "frac": round(achieved / hbm, 4),
-            "traffic": measured_traffic(cfg.name, args.tokens, names[k]),
+            "traffic": measured_traffic(cfg.name, args.tokens, names[k], head["gemm_path"]),
             "alg_bytes_per_launch": b[k], "launch_us": round(st[k], 3),
             "stage_us": {n: round(v, 3) for n, v in zip(names, st)}}
 
