@@ -65,7 +65,7 @@ struct Layout {
   int stages, stage_bytes, smem;
   int grid1, grid2;
   size_t off_err, off_counts, off_offs, off_ntiles, off_tiles, off_perm, off_inv, off_ctr;
-  size_t off_part, off_inter, off_y;
+  size_t off_part, off_inter, off_y, off_xs;
   size_t off_sx, off_sids, off_sw, off_sout;
   size_t total;
 };
@@ -186,6 +186,7 @@ Layout make_layout(const w4a16_moe_plan_s& P, int T) {
   L.off_part = take(L.s1 > 1 ? sizeof(float) * L.s1 * L.slots_cap * L.n1 : 0);
   L.off_inter = take(static_cast<size_t>(act_bytes) * L.slots_cap * d.inter);
   L.off_y = take(sizeof(float) * L.s2 * L.slots_cap * d.hidden);
+  L.off_xs = take(L.gemv ? 0 : static_cast<size_t>(act_bytes) * L.slots_cap * d.hidden);
   L.off_sx = take(static_cast<size_t>(act_bytes) * T * d.hidden);
   L.off_sids = take(sizeof(int32_t) * std::max(L.R, 1));
   L.off_sw = take(sizeof(float) * std::max(L.R, 1));
@@ -342,6 +343,10 @@ w4a16_status launch_forward(const w4a16_moe_plan_s& P, const Layout& L, const vo
          encode_weights(&tmA2, w2, d.inter, d.hidden / 2, d.num_experts, kBlockK, 32);
   }
   ok = ok && encode_rows16(&tmB2, ws + L.off_inter, d.inter, L.slots_cap, L.bn, d.act_dtype);
+  // tensor-core path: activation rows copied into slot order, read as tiles
+  CUtensorMap tmX;
+  memset(&tmX, 0, sizeof(tmX));
+  if (!L.gemv) ok = ok && encode_rows16(&tmX, ws + L.off_xs, d.hidden, L.slots_cap, L.bn, d.act_dtype);
   // CUDA-core path: group scales by TMA where their rows are 16-byte multiples
   CUtensorMap tmS1, tmS2;
   memset(&tmS1, 0, sizeof(tmS1));
@@ -382,9 +387,22 @@ w4a16_status launch_forward(const w4a16_moe_plan_s& P, const Layout& L, const vo
   g1.counters = reinterpret_cast<int32_t*>(ws + L.off_ctr);
   g1.scale_tma = stma1 ? 1 : 0;
   cudaError_t e;
+  if (!L.gemv) {
+    PermuteParams pp = {};
+    pp.x = x;
+    pp.inv = reinterpret_cast<const int32_t*>(ws + L.off_inv);
+    pp.xs = ws + L.off_xs;
+    pp.R = L.R;
+    pp.k = d.top_k;
+    pp.H = d.hidden;
+    const int warps_per_block = kPermuteThreads / 32;
+    const int grid = std::max(1, std::min((L.R + warps_per_block - 1) / warps_per_block, 8 * P.num_sms));
+    e = launch_permute(pp, grid, s, P.pdl);
+    if (e != cudaSuccess) return cuda_fail(e, "activation permute launch");
+  }
   if (P.has_ev && (e = cudaEventRecord(P.ev[0], s)) != cudaSuccess) return cuda_fail(e, "event record");
   e = L.gemv ? launch_gemv(GEMM_UP, d.scale_kind, d.act_dtype, g1, tmA1, tmS1, L.grid1, L.smem, s, P.pdl)
-             : launch_gemm(GEMM_UP, d.scale_kind, d.act_dtype, g1, tmA1, tmA1, L.grid1, L.smem, s, P.pdl);
+             : launch_gemm(GEMM_UP, d.scale_kind, d.act_dtype, g1, tmA1, tmX, L.grid1, L.smem, s, P.pdl);
   if (e != cudaSuccess) return cuda_fail(e, "gate/up GEMM launch");
   if (P.has_ev && (e = cudaEventRecord(P.ev[1], s)) != cudaSuccess) return cuda_fail(e, "event record");
 

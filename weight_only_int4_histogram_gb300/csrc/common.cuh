@@ -79,6 +79,14 @@ struct RoutePrepParams {
   int32_t* err;            // device error flag, cleared here
 };
 
+// Slot-ordered copy of the activation rows for the tensor-core gate/up GEMM.
+struct PermuteParams {
+  const void* x;           // [T, H] activations (16-bit)
+  const int32_t* inv;      // [R] slot of flat route r = t * k + j, -1 if dropped
+  void* xs;                // [slots_cap, H]: row inv[r] receives x[r / k]
+  int32_t R, k, H;
+};
+
 struct GemmParams {
   int32_t act;             // ACT_* (gate/up GEMM epilogue)
   int32_t E;               // local experts
@@ -97,8 +105,8 @@ struct GemmParams {
   const int4* tiles;       // route tiles (expert, first slot, valid rows, 0)
   const int32_t* num_tiles;
   const int32_t* perm;     // slot -> flat route (gate/up gather)
-  const void* x;           // gate/up: activations [T, H]; down: the intermediate
-                           // [slots_cap, I] (read by the CUDA-core path only)
+  const void* x;           // CUDA-core path only: activations [T, H] (gate/up)
+                           // or the intermediate [slots_cap, I] (down)
   const uint16_t* scales;  // BF16 scale bits of this GEMM's weights
   int64_t slots_cap;
   void* out;               // gate/up: intermediate [slots_cap, I] act dtype
@@ -122,6 +130,8 @@ struct CombineParams {
 
 // Host-side launchers (one translation unit each).
 cudaError_t launch_route_prep(const RoutePrepParams& p, int smem_bytes, cudaStream_t s, bool pdl);
+cudaError_t launch_permute(const PermuteParams& p, int grid, cudaStream_t s, bool pdl);
+constexpr int kPermuteThreads = 256;
 cudaError_t launch_gemm(int which, int scale_kind, int dtype, const GemmParams& p,
                         const CUtensorMap& tmA, const CUtensorMap& tmB, int grid, int smem_bytes,
                         cudaStream_t s, bool pdl);

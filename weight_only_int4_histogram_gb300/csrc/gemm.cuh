@@ -14,17 +14,18 @@
 //                              -> dequant warps -> BF16/FP16 A operand in TMEM
 //                                 (four A buffers: each warpgroup alternates two,
 //                                 so dequantisation overlaps the MMAs)
-//   activations (B, N = bn)    gate/up: cp.async row gather by slot -> token
-//                              down:    TMA tile of the intermediate
-//                              -> SMEM (128B-swizzled, K-major)
+//   activations (B, N = bn)    TMA tile of a slot-ordered matrix: the token
+//                              rows of x copied by route (gate/up) or the
+//                              intermediate (down) -> SMEM (128B-swizzled,
+//                              K-major)
 //   tcgen05.mma.kind::f16 (A from TMEM, B from SMEM), FP32 accumulators in TMEM,
 //   double-buffered, drained by four epilogue warps.
 //
 // Warp roles (512 threads):
-//   warp 0       TMA producer: packed weights, group scales (cp.async), and for
-//                the down GEMM the intermediate tile
+//   warp 0       TMA producer: packed weights, group scales (cp.async) and the
+//                activation tile
 //   warp 1       TMEM allocation + single-thread MMA issuer
-//   warps 2, 3   gate/up GEMM: activation-row gather (cp.async, 16 B per lane)
+//   warps 2, 3   idle
 //   warps 4..11  two dequant warpgroups; warpgroup g handles pipeline stages
 //                with (stage counter & 1) == g, writing TMEM A buffer
 //                (stage counter & 3)
@@ -220,17 +221,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   uint64_t* aempty = afull + kNumAbuf;
   uint64_t* accfull = aempty + kNumAbuf;
   uint64_t* accempty = accfull + 2;
-  uint64_t* gbar = accempty + 2;             // [kMaxStages] gather-copy completion
-  uint64_t* drain = gbar + kMaxStages;
+  uint64_t* drain = accempty + 2;
   uint64_t* epibar = drain + 1;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(epibar + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   volatile int* fixup_flag = reinterpret_cast<volatile int*>(tmem_holder + 2);
-  int32_t* tok_s = reinterpret_cast<int32_t*>(tmem_holder + 4);  // [kMaxBN]
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const bool gather_b = (WHICH == GEMM_UP);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < stages; ++s) {
@@ -245,7 +243,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       mbar_init(&accfull[b], 1);
       mbar_init(&accempty[b], 4);
     }
-    for (int s = 0; s < kMaxStages; ++s) mbar_init(&gbar[s], 64);  // gather lanes
     mbar_init(drain, 1);
     mbar_init(epibar, 4);
     *abort_flag = 0;
@@ -254,7 +251,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   }
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmA);
-    if (!gather_b) tma_prefetch_desc(&tmB);
+    tma_prefetch_desc(&tmB);
   }
   if (warp == 1) {
     tmem_alloc(tmem_holder, kTmemCols);
@@ -340,7 +337,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
         __syncwarp();
         if (lane == 0) {
-          mbar_arrive_expect_tx(&full[st], kStageA + (gather_b ? 0 : bn * kStageBRow));
+          mbar_arrive_expect_tx(&full[st], kStageA + bn * kStageBRow);
           if (SCALE == SCALE_GROUP) {
             // two 64-row boxes of 64 packed bytes (128 K values), 64-byte swizzle
             tma_load_3d(sA, &tmA, &full[st], kb * (kBlockK / 2), r0, e, pol_w);
@@ -350,11 +347,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             tma_load_3d(sA, &tmA, &full[st], kb * kBlockK, r0 / 2, e, pol_w);
             tma_load_3d(sA + 4096, &tmA, &full[st], kb * kBlockK, r1 / 2, e, pol_w);
           }
-          if (!gather_b) {
 #pragma unroll
-            for (int a = 0; a < kBlockK / 64; ++a)
-              tma_load_2d(sB + a * bn * 128, &tmB, &full[st], kb * kBlockK + a * 64, m0, pol_b);
-          }
+          for (int a = 0; a < kBlockK / 64; ++a)
+            tma_load_2d(sB + a * bn * 128, &tmB, &full[st], kb * kBlockK + a * 64, m0, pol_b);
         }
         __syncwarp();
       }
@@ -386,14 +381,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
           const int st = it % stages;
           const int ab = it % kNumAbuf;
-          // B: TMA bytes (down GEMM, on `full`) or gathered rows (gate/up, on
-          // `gbar`, written through the generic proxy: fence before the MMA).
-          if (!mbar_wait(gather_b ? &gbar[st] : &full[st], (it / stages) & 1, abort_flag, p.err) ||
+          // A (dequantised, in TMEM) and B (TMA bytes, on `full`)
+          if (!mbar_wait(&full[st], (it / stages) & 1, abort_flag, p.err) ||
               !mbar_wait(&afull[ab], (it / kNumAbuf) & 1, abort_flag, p.err)) {
             ok = false;
             break;
           }
-          if (gather_b) fence_proxy_async_smem();
           tc_fence_after();
           // B descriptors of this stage: the start-address field (bits 0-13,
           // address >> 4) advances by 2 per 32-byte K step inside a 128-byte
@@ -419,81 +412,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       volatile int no_abort = 0;
       mbar_wait(drain, 0, &no_abort, p.err);
     }
-  } else if (warp == 2 || warp == 3) {
-    // ------------------------------------------------------------------ activation gather
-    // Each warp copies half of the route tile's rows (16 B per lane, two rows
-    // per instruction) straight from x by token, with cp.async (out-of-range K
-    // columns are zero-filled by the copy itself).  Completion is signalled on
-    // gbar[stage] without blocking the warp; the MMA thread, the only reader of
-    // these rows, waits on gbar and issues the generic->async proxy fence.
-    if (gather_b) {
-      const int gw = warp - 2;
-      const int rows_per = bn / 2;
-      const uint16_t* x = reinterpret_cast<const uint16_t*>(p.x);
-      const int c = lane & 15, atom = c >> 3, ch = c & 7, rsub = lane >> 4;
-      uint32_t it = 0;
-      bool ok = true;
-      // perm entries of this warp's rows (lane, lane + 32), one unit ahead
-      auto load_perm = [&](int m0, int r) -> int {
-        return r < rows_per ? p.perm[m0 + gw * rows_per + r] : -1;
-      };
-      int4 ti_next = first_ti;
-      int pa_next = -1, pb_next = -1;
-      if (blockIdx.x < n_units) {
-        pa_next = load_perm(ti_next.y, lane);
-        pb_next = load_perm(ti_next.y, lane + 32);
-      }
-      for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-        const Unit w = decode_unit(p, u);
-        const int pa = pa_next, pb = pb_next;
-        if (u + (int)gridDim.x < n_units) {
-          ti_next = load_tile(p, u + gridDim.x);
-          pa_next = load_perm(ti_next.y, lane);
-          pb_next = load_perm(ti_next.y, lane + 32);
-        }
-        if (w.kb1 <= w.kb0) continue;
-        __syncwarp();
-        if (lane < rows_per) tok_s[gw * (kMaxBN / 2) + lane] = pa >= 0 ? pa / p.top_k : 0;
-        if (lane + 32 < rows_per) tok_s[gw * (kMaxBN / 2) + lane + 32] = pb >= 0 ? pb / p.top_k : 0;
-        __syncwarp();
-        // This lane's rows are r_j = gw * rows_per + 2 j + rsub; their source rows
-        // (first kRowsReg in registers, the rest re-read from tok_s) and their
-        // swizzled destination offsets inside a stage.
-        constexpr int kRowsReg = 8;
-        const uint16_t* src_j[kRowsReg];
-        uint32_t dst_j[kRowsReg];
-#pragma unroll
-        for (int j = 0; j < kRowsReg; ++j) {
-          const int rr = 2 * j + rsub;
-          const int r = gw * rows_per + rr;
-          const int tok = rr < rows_per ? tok_s[gw * (kMaxBN / 2) + rr] : 0;
-          src_j[j] = x + static_cast<int64_t>(tok) * p.K;
-          dst_j[j] = atom * bn * 128 + r * 128 + ((ch ^ (r & 7)) << 4);
-        }
-        for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
-          const int st = it % stages;
-          if (!mbar_wait(&empty[st], ((it / stages) & 1) ^ 1, abort_flag, p.err)) {
-            ok = false;
-            break;
-          }
-          uint8_t* sB = smem + st * p.stage_bytes + kStageA;
-          const int col = kb * kBlockK + c * 8;
-          const uint32_t nbytes = col < p.K ? 16u : 0u;
-          const int colc = col < p.K ? col : 0;
-#pragma unroll
-          for (int j = 0; j < kRowsReg; ++j)
-            if (2 * j < rows_per) cp_async_cg16(sB + dst_j[j], src_j[j] + colc, nbytes);
-          for (int rr = 2 * kRowsReg; rr < rows_per; rr += 2) {
-            const int r = gw * rows_per + rr + rsub;
-            const int tok = tok_s[gw * (kMaxBN / 2) + rr + rsub];
-            cp_async_cg16(sB + atom * bn * 128 + r * 128 + ((ch ^ (r & 7)) << 4),
-                          x + static_cast<int64_t>(tok) * p.K + colc, nbytes);
-          }
-          cp_async_mbar_arrive_noinc(&gbar[st]);
-        }
-      }
-      asm volatile("cp.async.wait_all;" ::: "memory");
-    }
+  } else if (warp < 4) {
+    // warps 2 and 3 have no role
   } else if (warp < 12) {
     // ------------------------------------------------------------------ dequant warpgroups
     const int wg = (warp - 4) >> 2;
@@ -568,7 +488,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const uint32_t acc_col = kAccCol0 + b * bn;
       // intermediate column of this lane (SwiGLU: gate/up pair index)
       const int icol = swiglu ? 64 * w.nt + 16 * q + (lane & 15) : grow;
-      for (int c0 = 0; c0 < bn; c0 += 16) {
+      for (int c0 = 0; c0 < rows; c0 += 16) {
         float v[16];
         if (has_k) {
           tmem_ld16(t_lane + acc_col + c0, v);
@@ -638,7 +558,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         if (*fixup_flag) {
           __threadfence();
           uint16_t* inter = reinterpret_cast<uint16_t*>(p.out) + static_cast<int64_t>(m0) * p.inter;
-          for (int c0 = 0; c0 < bn; c0 += 16) {
+          for (int c0 = 0; c0 < rows; c0 += 16) {
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
               const int r = c0 + j;

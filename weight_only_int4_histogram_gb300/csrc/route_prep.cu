@@ -9,8 +9,8 @@
 // One CTA of 32 warps.  The flat routes r = t*k + j are cut into 32 contiguous
 // chunks, one per warp, so "earlier warp" means "smaller flat index":
 //   pass 1  per-warp histograms hist[w][e] (warp-synchronous, no atomics):
-//           lanes holding the same expert find each other with match_any and
-//           their lowest lane adds the group size;
+//           lanes holding the same expert find each other with one ballot per
+//           bit of the expert index and their lowest lane adds the group size;
 //   pass 2  column prefix over warps (routes of expert e in earlier chunks),
 //           then a warp-shuffle exclusive scan over experts of the padded
 //           segment sizes and of the tile counts;
@@ -18,11 +18,23 @@
 //           earlier-round count + rank among equal lanes of its round, which
 //           is its rank in ascending flat order: a stable permutation.
 // Padding slots get perm = -1 and the tile list (expert, first slot, valid
-// rows) is written per expert.  Integer work only: results are bit-exact and
+// rows) is written per expert, one warp per expert (coalesced stores).  Integer work only: results are bit-exact and
 // independent of scheduling.
 #include "common.cuh"
 
 namespace w4a16 {
+
+// Mask of the lanes whose key equals this lane's, for keys below 2^nbits: one
+// ballot per key bit (cheaper than match.any when most keys differ).
+__device__ __forceinline__ unsigned lanes_with_key(int key, int nbits) {
+  unsigned m = 0xFFFFFFFFu;
+  for (int b = 0; b < nbits; ++b) {
+    const bool bit = (key >> b) & 1;
+    const unsigned bal = __ballot_sync(0xFFFFFFFFu, bit);
+    m &= bit ? bal : ~bal;
+  }
+  return m;
+}
 
 __global__ void __launch_bounds__(kRoutePrepThreads, 1) route_prep_kernel(const RoutePrepParams p) {
   extern __shared__ int32_t sm[];
@@ -52,6 +64,7 @@ __global__ void __launch_bounds__(kRoutePrepThreads, 1) route_prep_kernel(const 
   const int r_end = min(R, r_begin + chunk);
   const unsigned full = 0xFFFFFFFFu;
   const unsigned lt_mask = (1u << lane) - 1u;
+  const int key_bits = 32 - __clz(E);  // keys e + 1 lie in [0, E]
 
   auto local_of = [&](int r) -> int {
     if (r >= r_end) return -1;
@@ -71,7 +84,7 @@ __global__ void __launch_bounds__(kRoutePrepThreads, 1) route_prep_kernel(const 
 #pragma unroll
     for (int i = 0; i < kBatch; ++i) {
       const int e = eb[i];
-      const unsigned m = __match_any_sync(full, e);
+      const unsigned m = lanes_with_key(e + 1, key_bits);
       if (e >= 0 && (m & lt_mask) == 0) hist[warp * E + e] += __popc(m);
       __syncwarp();
     }
@@ -148,7 +161,7 @@ __global__ void __launch_bounds__(kRoutePrepThreads, 1) route_prep_kernel(const 
     for (int i = 0; i < kBatch; ++i) {
       const int r = base + 32 * i + lane;
       const int e = eb[i];
-      const unsigned m = __match_any_sync(full, e);
+      const unsigned m = lanes_with_key(e + 1, key_bits);
       if (e >= 0) {
         const int slot = poff[e] + hist[warp * E + e] + __popc(m & lt_mask);
         p.perm[slot] = r;
@@ -162,21 +175,56 @@ __global__ void __launch_bounds__(kRoutePrepThreads, 1) route_prep_kernel(const 
     }
   }
 
-  // padding slots, tile list, counts and offsets
-  for (int e = tid; e < E; e += kRoutePrepThreads) {
+  // padding slots, tile list, counts and offsets (one warp per expert)
+  for (int e = warp; e < E; e += kRoutePrepWarps) {
     const int c = cnt[e];
-    for (int s = poff[e] + c; s < poff[e + 1]; ++s) p.perm[s] = -1;
+    const int s0 = poff[e];
+    for (int s = s0 + c + lane; s < poff[e + 1]; s += 32) p.perm[s] = -1;
     const int nt = toff[e + 1] - toff[e];
-    for (int i = 0; i < nt; ++i) {
-      p.tiles[toff[e] + i] = make_int4(e, poff[e] + i * p.bm, min(p.bm, c - i * p.bm), 0);
+    for (int i = lane; i < nt; i += 32) p.tiles[toff[e] + i] = make_int4(e, s0 + i * p.bm, min(p.bm, c - i * p.bm), 0);
+    if (lane == 0) {
+      p.counts[e] = c;
+      p.offs[e] = s0;
     }
-    p.counts[e] = c;
-    p.offs[e] = poff[e];
   }
   if (tid == 0) {
     p.offs[E] = poff[E];
     *p.num_tiles = toff[E];
   }
+}
+
+// Activation rows in slot order for the tensor-core gate/up GEMM: every valid
+// flat route r copies token row x[r / k] to row inv[r] of xs, one warp per
+// route (16-byte vectors, H a multiple of 64), so that the GEMM reads its
+// activation operand as plain TMA tiles of consecutive slots.  Padding slots
+// are not written: their MMA columns are never read.
+__global__ void __launch_bounds__(kPermuteThreads) permute_rows_kernel(const PermuteParams p) {
+  pdl_wait();
+  pdl_launch_dependents();
+  const int lane = threadIdx.x & 31;
+  const int warps = gridDim.x * (kPermuteThreads / 32);
+  const int vecs = p.H / 8;  // 16-byte vectors per row
+  for (int r = blockIdx.x * (kPermuteThreads / 32) + (threadIdx.x >> 5); r < p.R; r += warps) {
+    const int slot = p.inv[r];
+    if (slot < 0) continue;
+    const uint4* src = reinterpret_cast<const uint4*>(p.x) + static_cast<int64_t>(r / p.k) * vecs;
+    uint4* dst = reinterpret_cast<uint4*>(p.xs) + static_cast<int64_t>(slot) * vecs;
+    for (int v = lane; v < vecs; v += 32) dst[v] = __ldg(src + v);
+  }
+}
+
+cudaError_t launch_permute(const PermuteParams& p, int grid, cudaStream_t s, bool pdl) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kPermuteThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, permute_rows_kernel, p);
 }
 
 cudaError_t launch_route_prep(const RoutePrepParams& p, int smem_bytes, cudaStream_t s, bool pdl) {
