@@ -239,6 +239,14 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   return mbar_wait_slow(bar, parity, abort_flag, err);
 }
 
+// Next use of a ring of `stages` slots: slot index and the parity of its phase.
+__device__ __forceinline__ void ring_next(int& st, uint32_t& ph, int stages) {
+  if (++st == stages) {
+    st = 0;
+    ph ^= 1u;
+  }
+}
+
 // ---------------------------------------------------------------------------
 // TMA (tensor) loads, completion signalled on an mbarrier as transaction bytes
 // ---------------------------------------------------------------------------

@@ -277,7 +277,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const uint64_t pol_b = l2_policy_evict_last();
     const int groups_row = p.K / kGroup;
     const int sbytes_row = groups_row * 2;
-    uint32_t it = 0;
+    uint32_t it = 0, ph = 0;
+    int st = 0;
     bool ok = true;
     int4 ti_next = first_ti;
     for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
@@ -303,9 +304,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           srow_al8 = srow_al8 && ((reinterpret_cast<uintptr_t>(srow[i]) & 7) == 0);
         }
       }
-      for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
-        const int st = it % stages;
-        if (!mbar_wait(&empty[st], ((it / stages) & 1) ^ 1, abort_flag, p.err)) {
+      for (int kb = w.kb0; kb < w.kb1; ++kb, ++it, ring_next(st, ph, stages)) {
+        if (!mbar_wait(&empty[st], ph ^ 1, abort_flag, p.err)) {
           ok = false;
           break;
         }
@@ -366,7 +366,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const uint32_t idesc = make_idesc_f16(DT == DT_BF16, kTileRows, bn);
       const uint64_t bdesc_base = smem_desc_sw128(smem_u32(smem + kStageA));
       const uint64_t atom_step = static_cast<uint64_t>(bn) * 128 / 16;
-      uint32_t it = 0, jc = 0;
+      uint32_t it = 0, jc = 0, ph = 0;
+      int st = 0;
+      uint64_t d_st = bdesc_base;  // B descriptor of stage st
+      const uint64_t d_stage = static_cast<uint64_t>(p.stage_bytes >> 4);
       bool ok = true;
       for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
         const Unit w = decode_unit(p, u);
@@ -379,11 +382,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         tc_fence_after();
         const uint32_t d_tmem = tmem + kAccCol0 + b * bn;
         for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
-          const int st = it % stages;
           const int ab = it % kNumAbuf;
-          // A (dequantised, in TMEM) and B (TMA bytes, on `full`)
-          if (!mbar_wait(&full[st], (it / stages) & 1, abort_flag, p.err) ||
-              !mbar_wait(&afull[ab], (it / kNumAbuf) & 1, abort_flag, p.err)) {
+          // A: the dequant warps arrive on afull[ab] only after they observed
+          // full[st] complete, and full[st] also carries this stage's B bytes
+          // (one expect_tx covers weights and activations), so afull alone
+          // orders both operands before the MMAs.
+          if (!mbar_wait(&afull[ab], (it / kNumAbuf) & 1, abort_flag, p.err)) {
             ok = false;
             break;
           }
@@ -392,7 +396,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           // address >> 4) advances by 2 per 32-byte K step inside a 128-byte
           // swizzle atom and by bn * 8 per atom; adding to the 64-bit value
           // never carries out of the field (shared addresses are < 256 KB).
-          const uint64_t d0 = bdesc_base + static_cast<uint64_t>(st) * (p.stage_bytes >> 4);
+          const uint64_t d0 = d_st;
           const uint32_t a0 = tmem + ab * kAbufCols;
           const uint32_t acc0 = kb > w.kb0 ? 1u : 0u;
 #pragma unroll
@@ -402,6 +406,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           }
           mma_commit(&aempty[ab]);
           mma_commit(&empty[st]);
+          ring_next(st, ph, stages);
+          d_st = st == 0 ? bdesc_base : d_st + d_stage;
         }
         if (!ok) break;
         mma_commit(&accfull[b]);
@@ -420,16 +426,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int q = warp & 3;
     const int tr = tile_row_of_lane<WHICH>(p, q * 32 + lane);
     const uint32_t t_lane = tmem + (static_cast<uint32_t>(q * 32) << 16);
-    uint32_t it = 0;
+    uint32_t it = 0, ph = 0;
+    int st = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
       const Unit w = decode_unit(p, u);
       if (w.kb1 <= w.kb0) continue;
-      for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
+      for (int kb = w.kb0; kb < w.kb1; ++kb, ++it, ring_next(st, ph, stages)) {
         if ((it & 1) != static_cast<uint32_t>(wg)) continue;
-        const int st = it % stages;
         const int ab = it % kNumAbuf;
-        if (!mbar_wait(&full[st], (it / stages) & 1, abort_flag, p.err) ||
+        if (!mbar_wait(&full[st], ph, abort_flag, p.err) ||
             !mbar_wait(&aempty[ab], ((it / kNumAbuf) & 1) ^ 1, abort_flag, p.err)) {
           ok = false;
           break;

@@ -73,13 +73,6 @@ static_assert(kGvCtrlTabOff + kGemvTileTab * 16 <= kGemvCtrlBytes, "tile table")
 static_assert(kGemvTileTab <= kGemvThreads, "one record per thread");
 static_assert(gemv_smem_bytes(kGemvMaxR, true) <= kGemvSmemLimit && gemv_stages(kGemvMaxR, true) >= 4, "smem");
 
-__device__ __forceinline__ void ring_next(int& st, uint32_t& ph, int stages) {
-  if (++st == stages) {
-    st = 0;
-    ph ^= 1u;
-  }
-}
-
 // Tile record of this CTA's i-th unit u: from the shared table (filled at
 // kernel start) or, past its end, from global memory.
 __device__ __forceinline__ int4 tile_of(const GemmParams& p, const int4* tab, int i, int u) {
