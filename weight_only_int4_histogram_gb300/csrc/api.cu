@@ -161,9 +161,9 @@ Layout make_layout(const w4a16_moe_plan_s& P, int T) {
     L.stage_bytes = kStageA + L.bn * kStageBRow + kStageS;
     // dynamic shared memory: 1 KB alignment slack + stages + 2 KB control block
     // (mbarriers, TMEM address, flags, token list)
-    const int smem_budget = 232448 - 3072;
+    const int smem_budget = 232448 - 3072 - kEpiStageBytes;
     L.stages = std::min(kMaxStages, smem_budget / L.stage_bytes);
-    L.smem = 3072 + L.stages * L.stage_bytes;
+    L.smem = 3072 + kEpiStageBytes + L.stages * L.stage_bytes;
   }
   L.grid1 = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(P.num_sms, static_cast<int64_t>(L.tiles_cap) * L.nt1 * L.s1)));
   L.grid2 = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(P.num_sms, static_cast<int64_t>(L.tiles_cap) * L.nt2 * L.s2)));
@@ -231,6 +231,20 @@ bool encode_weights(CUtensorMap* m, const void* base, uint64_t inner, uint64_t r
   const CUtensorMapSwizzle sw = box_inner == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B;
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// FP32 row-major matrix [rows][cols], unswizzled boxes of 32 columns x 16 rows
+// (the down GEMM's output stores).
+bool encode_out32(CUtensorMap* m, void* base, uint64_t cols, uint64_t rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 4};
+  cuuint32_t box[2] = {32, 16};
+  cuuint32_t es[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -347,6 +361,10 @@ w4a16_status launch_forward(const w4a16_moe_plan_s& P, const Layout& L, const vo
   CUtensorMap tmX;
   memset(&tmX, 0, sizeof(tmX));
   if (!L.gemv) ok = ok && encode_rows16(&tmX, ws + L.off_xs, d.hidden, L.slots_cap, L.bn, d.act_dtype);
+  // tensor-core path: FP32 expert outputs y [splits * slots_cap, H], TMA-stored
+  CUtensorMap tmY;
+  memset(&tmY, 0, sizeof(tmY));
+  if (!L.gemv) ok = ok && encode_out32(&tmY, ws + L.off_y, d.hidden, static_cast<uint64_t>(L.s2) * L.slots_cap);
   // CUDA-core path: group scales by TMA where their rows are 16-byte multiples
   CUtensorMap tmS1, tmS2;
   memset(&tmS1, 0, sizeof(tmS1));
@@ -402,7 +420,7 @@ w4a16_status launch_forward(const w4a16_moe_plan_s& P, const Layout& L, const vo
   }
   if (P.has_ev && (e = cudaEventRecord(P.ev[0], s)) != cudaSuccess) return cuda_fail(e, "event record");
   e = L.gemv ? launch_gemv(GEMM_UP, d.scale_kind, d.act_dtype, g1, tmA1, tmS1, L.grid1, L.smem, s, P.pdl)
-             : launch_gemm(GEMM_UP, d.scale_kind, d.act_dtype, g1, tmA1, tmX, L.grid1, L.smem, s, P.pdl);
+             : launch_gemm(GEMM_UP, d.scale_kind, d.act_dtype, g1, tmA1, tmX, tmY, L.grid1, L.smem, s, P.pdl);
   if (e != cudaSuccess) return cuda_fail(e, "gate/up GEMM launch");
   if (P.has_ev && (e = cudaEventRecord(P.ev[1], s)) != cudaSuccess) return cuda_fail(e, "event record");
 
@@ -421,7 +439,7 @@ w4a16_status launch_forward(const w4a16_moe_plan_s& P, const Layout& L, const vo
   g2.counters = nullptr;
   g2.scale_tma = stma2 ? 1 : 0;
   e = L.gemv ? launch_gemv(GEMM_DOWN, d.scale_kind, d.act_dtype, g2, tmA2, tmS2, L.grid2, L.smem, s, P.pdl)
-             : launch_gemm(GEMM_DOWN, d.scale_kind, d.act_dtype, g2, tmA2, tmB2, L.grid2, L.smem, s, P.pdl);
+             : launch_gemm(GEMM_DOWN, d.scale_kind, d.act_dtype, g2, tmA2, tmB2, tmY, L.grid2, L.smem, s, P.pdl);
   if (e != cudaSuccess) return cuda_fail(e, "down GEMM launch");
   if (P.has_ev && (e = cudaEventRecord(P.ev[2], s)) != cudaSuccess) return cuda_fail(e, "event record");
 
@@ -447,17 +465,21 @@ w4a16_status launch_forward(const w4a16_moe_plan_s& P, const Layout& L, const vo
 namespace w4a16 {
 template <int DT>
 cudaError_t launch_gemm_dt(int which, int scale_kind, const GemmParams& p, const CUtensorMap& tmA,
-                           const CUtensorMap& tmB, int grid, int smem_bytes, cudaStream_t s, bool pdl);
+                           const CUtensorMap& tmB, const CUtensorMap& tmC, int grid, int smem_bytes,
+                           cudaStream_t s, bool pdl);
 extern template cudaError_t launch_gemm_dt<DT_BF16>(int, int, const GemmParams&, const CUtensorMap&,
-                                                     const CUtensorMap&, int, int, cudaStream_t, bool);
+                                                     const CUtensorMap&, const CUtensorMap&, int, int,
+                                                     cudaStream_t, bool);
 extern template cudaError_t launch_gemm_dt<DT_FP16>(int, int, const GemmParams&, const CUtensorMap&,
-                                                     const CUtensorMap&, int, int, cudaStream_t, bool);
+                                                     const CUtensorMap&, const CUtensorMap&, int, int,
+                                                     cudaStream_t, bool);
 
 cudaError_t launch_gemm(int which, int scale_kind, int dtype, const GemmParams& p,
-                        const CUtensorMap& tmA, const CUtensorMap& tmB, int grid, int smem_bytes,
-                        cudaStream_t s, bool pdl) {
-  if (dtype == DT_BF16) return launch_gemm_dt<DT_BF16>(which, scale_kind, p, tmA, tmB, grid, smem_bytes, s, pdl);
-  return launch_gemm_dt<DT_FP16>(which, scale_kind, p, tmA, tmB, grid, smem_bytes, s, pdl);
+                        const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
+                        int grid, int smem_bytes, cudaStream_t s, bool pdl) {
+  if (dtype == DT_BF16)
+    return launch_gemm_dt<DT_BF16>(which, scale_kind, p, tmA, tmB, tmC, grid, smem_bytes, s, pdl);
+  return launch_gemm_dt<DT_FP16>(which, scale_kind, p, tmA, tmB, tmC, grid, smem_bytes, s, pdl);
 }
 
 template <int DT>

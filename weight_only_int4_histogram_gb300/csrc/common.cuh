@@ -29,6 +29,8 @@ constexpr int kMaxBN = 128;
 constexpr int kStageA = kTileRows * kBlockK / 2;   // 8 KB packed INT4 per stage
 constexpr int kStageS = kTileRows * kGroupsPerStage * 2;  // BF16 scales per stage
 constexpr int kStageBRow = kBlockK * 2;            // bytes of one activation row per stage
+// Down-GEMM output staging: 4 epilogue warps x 2 buffers x (16 routes x 32 rows FP32)
+constexpr int kEpiStageBytes = 4 * 2 * 16 * 32 * 4;
 
 // CUDA-core GEMV path (gemv.cuh): route tiles of at most kGemvMaxR routes,
 // pipeline stages of kGemvBlockK K values; the stage size (and so the number
@@ -133,8 +135,8 @@ cudaError_t launch_route_prep(const RoutePrepParams& p, int smem_bytes, cudaStre
 cudaError_t launch_permute(const PermuteParams& p, int grid, cudaStream_t s, bool pdl);
 constexpr int kPermuteThreads = 256;
 cudaError_t launch_gemm(int which, int scale_kind, int dtype, const GemmParams& p,
-                        const CUtensorMap& tmA, const CUtensorMap& tmB, int grid, int smem_bytes,
-                        cudaStream_t s, bool pdl);
+                        const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
+                        int grid, int smem_bytes, cudaStream_t s, bool pdl);
 cudaError_t launch_gemv(int which, int scale_kind, int dtype, const GemmParams& p,
                         const CUtensorMap& tmA, const CUtensorMap& tmS, int grid, int smem_bytes,
                         cudaStream_t s, bool pdl);
@@ -297,6 +299,23 @@ __device__ __forceinline__ void tma_gather4(void* dst, const CUtensorMap* map, u
       "r"(r2), "r"(r3), "l"(policy)
       : "memory");
 }
+
+// Store a box of a 2D tensor from shared memory; completion is tracked by the
+// issuing thread's bulk async-groups.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void* src, int c0, int c1) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(smem_u32(src)), "r"(c0), "r"(c1)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Wait until at most N of this thread's bulk groups still read shared memory.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+// Wait until all of this thread's bulk groups have completed (writes performed).
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 // Ampere-style asynchronous copies (used for the small group-scale tiles whose
 // global row stride is not a multiple of 16 bytes in general).

@@ -19,7 +19,8 @@
 //                              intermediate (down) -> SMEM (128B-swizzled,
 //                              K-major)
 //   tcgen05.mma.kind::f16 (A from TMEM, B from SMEM), FP32 accumulators in TMEM,
-//   double-buffered, drained by four epilogue warps.
+//   double-buffered, drained by four epilogue warps; the down GEMM's FP32
+//   outputs leave through SMEM staging buffers as TMA tensor stores.
 //
 // Warp roles (512 threads):
 //   warp 0       TMA producer: packed weights, group scales (cp.async) and the
@@ -207,7 +208,7 @@ __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + expf(-g));
 template <int WHICH, int SCALE, int DT>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     w4a16_gemm_kernel(const __grid_constant__ GemmParams p, const __grid_constant__ CUtensorMap tmA,
-                      const __grid_constant__ CUtensorMap tmB) {
+                      const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmC) {
   using T = F16<DT>;
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte aligned base, derived by pointer arithmetic on the shared array so
@@ -215,7 +216,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const int stages = p.stages;
   const int bn = p.bn;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + stages * p.stage_bytes);
+  float* epi_stage = reinterpret_cast<float*>(smem + stages * p.stage_bytes);  // [4][2][16 x 32]
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + stages * p.stage_bytes + kEpiStageBytes);
   uint64_t* empty = full + kMaxStages;
   uint64_t* afull = empty + kMaxStages;
   uint64_t* aempty = afull + kNumAbuf;
@@ -252,6 +254,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
+    if (WHICH == GEMM_DOWN) tma_prefetch_desc(&tmC);
   }
   if (warp == 1) {
     tmem_alloc(tmem_holder, kTmemCols);
@@ -460,6 +463,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int epi_tid = threadIdx.x - 12 * 32;
     const bool swiglu = (WHICH == GEMM_UP && p.act == ACT_SWIGLU);
     uint32_t jc = 0, eph = 0;
+    int sbuf = 0;  // down GEMM: staging buffer of this warp's next chunk
     bool ok = true;
     // Bounded barrier over the four epilogue warps.
     auto epi_sync = [&]() -> bool {
@@ -506,13 +510,22 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 #pragma unroll
         for (int j = 0; j < 16; ++j) v[j] *= scale;
         if (WHICH == GEMM_DOWN) {
-          float* y = reinterpret_cast<float*>(p.out) +
-                     (static_cast<int64_t>(w.split) * p.slots_cap + m0) * p.out_cols + grow;
+          // This warp's 32 output columns x 16 slots through a staging buffer
+          // (slot-major, conflict-free) and one TMA store.  Slots past the
+          // tile's valid rows are padding slots of y, never read.
+          float* stg = epi_stage + (q * 2 + sbuf) * (16 * 32);
+          if (lane == 0) bulk_wait_read<1>();  // the store that last read this buffer
+          __syncwarp();
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int r = c0 + j;
-            if (r < rows && row_ok) y[static_cast<int64_t>(r) * p.out_cols] = v[j];
+          for (int j = 0; j < 16; ++j) stg[j * 32 + lane] = v[j];
+          fence_proxy_async_smem();
+          __syncwarp();
+          const int col0 = grow - lane;
+          if (lane == 0 && col0 < p.out_cols) {
+            tma_store_2d(&tmC, stg, col0, static_cast<int>(w.split * p.slots_cap) + m0 + c0);
+            bulk_commit();
           }
+          sbuf ^= 1;
         } else if (p.splits > 1) {
           float* part = p.part + (static_cast<int64_t>(w.split) * p.slots_cap + m0) * N1 + grow;
 #pragma unroll
@@ -593,6 +606,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   }
 
   // ------------------------------------------------------------------ teardown
+  if (WHICH == GEMM_DOWN && warp >= 12 && lane == 0) bulk_wait_all();  // output stores done
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
@@ -606,7 +620,7 @@ namespace w4a16 {
 
 template <int WHICH, int SCALE, int DT>
 cudaError_t launch_gemm_one(const GemmParams& p, const CUtensorMap& tmA, const CUtensorMap& tmB,
-                            int grid, int smem_bytes, cudaStream_t s, bool pdl) {
+                            const CUtensorMap& tmC, int grid, int smem_bytes, cudaStream_t s, bool pdl) {
   auto kern = w4a16_gemm_kernel<WHICH, SCALE, DT>;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -627,21 +641,21 @@ cudaError_t launch_gemm_one(const GemmParams& p, const CUtensorMap& tmA, const C
   attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, p, tmA, tmB);
+  return cudaLaunchKernelEx(&cfg, kern, p, tmA, tmB, tmC);
 }
 
 template <int DT>
 cudaError_t launch_gemm_dt(int which, int scale_kind, const GemmParams& p, const CUtensorMap& tmA,
-                           const CUtensorMap& tmB, int grid, int smem_bytes, cudaStream_t s,
-                           bool pdl) {
+                           const CUtensorMap& tmB, const CUtensorMap& tmC, int grid, int smem_bytes,
+                           cudaStream_t s, bool pdl) {
   if (which == GEMM_UP) {
     return scale_kind == SCALE_GROUP
-               ? launch_gemm_one<GEMM_UP, SCALE_GROUP, DT>(p, tmA, tmB, grid, smem_bytes, s, pdl)
-               : launch_gemm_one<GEMM_UP, SCALE_CHANNEL, DT>(p, tmA, tmB, grid, smem_bytes, s, pdl);
+               ? launch_gemm_one<GEMM_UP, SCALE_GROUP, DT>(p, tmA, tmB, tmC, grid, smem_bytes, s, pdl)
+               : launch_gemm_one<GEMM_UP, SCALE_CHANNEL, DT>(p, tmA, tmB, tmC, grid, smem_bytes, s, pdl);
   }
   return scale_kind == SCALE_GROUP
-             ? launch_gemm_one<GEMM_DOWN, SCALE_GROUP, DT>(p, tmA, tmB, grid, smem_bytes, s, pdl)
-             : launch_gemm_one<GEMM_DOWN, SCALE_CHANNEL, DT>(p, tmA, tmB, grid, smem_bytes, s, pdl);
+             ? launch_gemm_one<GEMM_DOWN, SCALE_GROUP, DT>(p, tmA, tmB, tmC, grid, smem_bytes, s, pdl)
+             : launch_gemm_one<GEMM_DOWN, SCALE_CHANNEL, DT>(p, tmA, tmB, tmC, grid, smem_bytes, s, pdl);
 }
 
 }  // namespace w4a16
