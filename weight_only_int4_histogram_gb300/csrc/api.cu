@@ -345,16 +345,15 @@ w4a16_status launch_forward(const w4a16_moe_plan_s& P, const Layout& L, const vo
   CUtensorMap tmA1, tmA2, tmB2;
   bool ok;
   if (group) {
-    // rows of packed bytes along K; boxes of 64 rows x one stage of K: 64 bytes
-    // (128 K values, 64-byte swizzle) for the tensor-core path, 128 bytes (256 K
-    // values, 128-byte swizzle) for the CUDA-core path
+    // rows of packed bytes along K; boxes of 64 rows x one stage of K (128
+    // bytes = 256 K values, 128-byte swizzle) on both paths
     const uint32_t box = L.gemv ? kGemvBlockK / 2 : kBlockK / 2;
     ok = encode_weights(&tmA1, w13, d.hidden / 2, L.n1, d.num_experts, box, 64) &&
          encode_weights(&tmA2, w2, d.inter / 2, d.hidden, d.num_experts, box, 64);
   } else {
     // row pairs of K bytes; boxes of 128 bytes (128 K values) x 32 row pairs
-    ok = encode_weights(&tmA1, w13, d.hidden, L.n1 / 2, d.num_experts, kBlockK, 32) &&
-         encode_weights(&tmA2, w2, d.inter, d.hidden / 2, d.num_experts, kBlockK, 32);
+    ok = encode_weights(&tmA1, w13, d.hidden, L.n1 / 2, d.num_experts, 128, 32) &&
+         encode_weights(&tmA2, w2, d.inter, d.hidden / 2, d.num_experts, 128, 32);
   }
   ok = ok && encode_rows16(&tmB2, ws + L.off_inter, d.inter, L.slots_cap, L.bn, d.act_dtype);
   // tensor-core path: activation rows copied into slot order, read as tiles
@@ -365,12 +364,12 @@ w4a16_status launch_forward(const w4a16_moe_plan_s& P, const Layout& L, const vo
   CUtensorMap tmY;
   memset(&tmY, 0, sizeof(tmY));
   if (!L.gemv) ok = ok && encode_out32(&tmY, ws + L.off_y, d.hidden, static_cast<uint64_t>(L.s2) * L.slots_cap);
-  // CUDA-core path: group scales by TMA where their rows are 16-byte multiples
+  // group scales by TMA (boxes of 8 groups) where their rows are 16-byte multiples
   CUtensorMap tmS1, tmS2;
   memset(&tmS1, 0, sizeof(tmS1));
   memset(&tmS2, 0, sizeof(tmS2));
-  const bool stma1 = L.gemv && group && (d.hidden / kGroup) % 8 == 0 && aligned(s13, 16);
-  const bool stma2 = L.gemv && group && (d.inter / kGroup) % 8 == 0 && aligned(s2, 16);
+  const bool stma1 = group && (d.hidden / kGroup) % 8 == 0 && aligned(s13, 16);
+  const bool stma2 = group && (d.inter / kGroup) % 8 == 0 && aligned(s2, 16);
   if (stma1) ok = ok && encode_scales(&tmS1, s13, d.hidden / kGroup, L.n1, d.num_experts);
   if (stma2) ok = ok && encode_scales(&tmS2, s2, d.inter / kGroup, d.hidden, d.num_experts);
   if (!ok) return fail(W4A16_ERR_CUDA, "cuTensorMapEncodeTiled failed (driver entry point or arguments)");
@@ -420,7 +419,7 @@ w4a16_status launch_forward(const w4a16_moe_plan_s& P, const Layout& L, const vo
   }
   if (P.has_ev && (e = cudaEventRecord(P.ev[0], s)) != cudaSuccess) return cuda_fail(e, "event record");
   e = L.gemv ? launch_gemv(GEMM_UP, d.scale_kind, d.act_dtype, g1, tmA1, tmS1, L.grid1, L.smem, s, P.pdl)
-             : launch_gemm(GEMM_UP, d.scale_kind, d.act_dtype, g1, tmA1, tmX, tmY, L.grid1, L.smem, s, P.pdl);
+             : launch_gemm(GEMM_UP, d.scale_kind, d.act_dtype, g1, tmA1, tmX, tmY, tmS1, L.grid1, L.smem, s, P.pdl);
   if (e != cudaSuccess) return cuda_fail(e, "gate/up GEMM launch");
   if (P.has_ev && (e = cudaEventRecord(P.ev[1], s)) != cudaSuccess) return cuda_fail(e, "event record");
 
@@ -439,7 +438,7 @@ w4a16_status launch_forward(const w4a16_moe_plan_s& P, const Layout& L, const vo
   g2.counters = nullptr;
   g2.scale_tma = stma2 ? 1 : 0;
   e = L.gemv ? launch_gemv(GEMM_DOWN, d.scale_kind, d.act_dtype, g2, tmA2, tmS2, L.grid2, L.smem, s, P.pdl)
-             : launch_gemm(GEMM_DOWN, d.scale_kind, d.act_dtype, g2, tmA2, tmB2, tmY, L.grid2, L.smem, s, P.pdl);
+             : launch_gemm(GEMM_DOWN, d.scale_kind, d.act_dtype, g2, tmA2, tmB2, tmY, tmS2, L.grid2, L.smem, s, P.pdl);
   if (e != cudaSuccess) return cuda_fail(e, "down GEMM launch");
   if (P.has_ev && (e = cudaEventRecord(P.ev[2], s)) != cudaSuccess) return cuda_fail(e, "event record");
 
@@ -465,21 +464,21 @@ w4a16_status launch_forward(const w4a16_moe_plan_s& P, const Layout& L, const vo
 namespace w4a16 {
 template <int DT>
 cudaError_t launch_gemm_dt(int which, int scale_kind, const GemmParams& p, const CUtensorMap& tmA,
-                           const CUtensorMap& tmB, const CUtensorMap& tmC, int grid, int smem_bytes,
-                           cudaStream_t s, bool pdl);
+                           const CUtensorMap& tmB, const CUtensorMap& tmC, const CUtensorMap& tmS,
+                           int grid, int smem_bytes, cudaStream_t s, bool pdl);
 extern template cudaError_t launch_gemm_dt<DT_BF16>(int, int, const GemmParams&, const CUtensorMap&,
-                                                     const CUtensorMap&, const CUtensorMap&, int, int,
-                                                     cudaStream_t, bool);
+                                                     const CUtensorMap&, const CUtensorMap&,
+                                                     const CUtensorMap&, int, int, cudaStream_t, bool);
 extern template cudaError_t launch_gemm_dt<DT_FP16>(int, int, const GemmParams&, const CUtensorMap&,
-                                                     const CUtensorMap&, const CUtensorMap&, int, int,
-                                                     cudaStream_t, bool);
+                                                     const CUtensorMap&, const CUtensorMap&,
+                                                     const CUtensorMap&, int, int, cudaStream_t, bool);
 
 cudaError_t launch_gemm(int which, int scale_kind, int dtype, const GemmParams& p,
                         const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
-                        int grid, int smem_bytes, cudaStream_t s, bool pdl) {
+                        const CUtensorMap& tmS, int grid, int smem_bytes, cudaStream_t s, bool pdl) {
   if (dtype == DT_BF16)
-    return launch_gemm_dt<DT_BF16>(which, scale_kind, p, tmA, tmB, tmC, grid, smem_bytes, s, pdl);
-  return launch_gemm_dt<DT_FP16>(which, scale_kind, p, tmA, tmB, tmC, grid, smem_bytes, s, pdl);
+    return launch_gemm_dt<DT_BF16>(which, scale_kind, p, tmA, tmB, tmC, tmS, grid, smem_bytes, s, pdl);
+  return launch_gemm_dt<DT_FP16>(which, scale_kind, p, tmA, tmB, tmC, tmS, grid, smem_bytes, s, pdl);
 }
 
 template <int DT>

@@ -16,18 +16,19 @@ namespace w4a16 {
 // Tiling constants
 // ---------------------------------------------------------------------------
 constexpr int kTileRows = 128;       // weight rows per MMA tile (MMA M)
-constexpr int kBlockK = 128;         // K elements per pipeline stage
+constexpr int kBlockK = 256;         // K elements per pipeline stage (shared-memory ring)
+constexpr int kHalfK = kBlockK / 2;  // K elements per TMEM A buffer (one dequant warpgroup's half)
 constexpr int kGroup = 32;           // group size of the group-wise scales
 constexpr int kGroupsPerStage = kBlockK / kGroup;
 constexpr int kMaxStages = 12;
 constexpr int kGemmThreads = 512;    // 16 warps: see the role map in gemm.cuh
 constexpr int kTmemCols = 512;
-constexpr int kAbufCols = kBlockK / 2;  // one stage of BF16/FP16 A in TMEM columns
+constexpr int kAbufCols = kHalfK / 2;   // one half-stage of BF16/FP16 A in TMEM columns
 constexpr int kNumAbuf = 4;             // A buffers: two per dequant warpgroup
 constexpr int kAccCol0 = kNumAbuf * kAbufCols;  // first accumulator column
 constexpr int kMaxBN = 128;
-constexpr int kStageA = kTileRows * kBlockK / 2;   // 8 KB packed INT4 per stage
-constexpr int kStageS = kTileRows * kGroupsPerStage * 2;  // BF16 scales per stage
+constexpr int kStageA = kTileRows * kBlockK / 2;   // 16 KB packed INT4 per stage
+constexpr int kStageS = kTileRows * kGroupsPerStage * 2;  // 2 KB BF16 group scales per stage
 constexpr int kStageBRow = kBlockK * 2;            // bytes of one activation row per stage
 // Down-GEMM output staging: 4 epilogue warps x 2 buffers x (16 routes x 32 rows FP32)
 constexpr int kEpiStageBytes = 4 * 2 * 16 * 32 * 4;
@@ -117,7 +118,7 @@ struct GemmParams {
   int32_t* counters;       // gate/up split-K arrival counters [tiles_cap * n_tiles]
   int32_t* err;
   int32_t tiles_cap;       // capacity of `tiles`
-  int32_t scale_tma;       // CUDA-core path: group scales loaded by TMA (16-byte rows)
+  int32_t scale_tma;       // group scales loaded by TMA (their rows are 16-byte multiples)
 };
 
 struct CombineParams {
@@ -136,7 +137,7 @@ cudaError_t launch_permute(const PermuteParams& p, int grid, cudaStream_t s, boo
 constexpr int kPermuteThreads = 256;
 cudaError_t launch_gemm(int which, int scale_kind, int dtype, const GemmParams& p,
                         const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
-                        int grid, int smem_bytes, cudaStream_t s, bool pdl);
+                        const CUtensorMap& tmS, int grid, int smem_bytes, cudaStream_t s, bool pdl);
 cudaError_t launch_gemv(int which, int scale_kind, int dtype, const GemmParams& p,
                         const CUtensorMap& tmA, const CUtensorMap& tmS, int grid, int smem_bytes,
                         cudaStream_t s, bool pdl);

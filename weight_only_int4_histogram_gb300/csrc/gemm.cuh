@@ -10,10 +10,13 @@
 // warpgroups as in "perf: reduce split W4A16 routing and output overhead"
 // (FlashInfer), section Description.  Blackwell design (not the pages'):
 //
-//   weights (A, M = 128 rows)  TMA (64B / 128B swizzle) -> SMEM packed INT4
-//                              -> dequant warps -> BF16/FP16 A operand in TMEM
-//                                 (four A buffers: each warpgroup alternates two,
-//                                 so dequantisation overlaps the MMAs)
+//   weights (A, M = 128 rows)  TMA (128B swizzle) -> SMEM packed INT4, 256 K
+//                              values per stage -> dequant warps -> BF16/FP16
+//                              A operand in TMEM (four A buffers of 128 K
+//                              values: warpgroup g dequantises K-half g of
+//                              every stage into its two buffers, so
+//                              dequantisation overlaps the MMAs)
+//   group scales               TMA boxes of 8 groups (16-byte rows), else cp.async
 //   activations (B, N = bn)    TMA tile of a slot-ordered matrix: the token
 //                              rows of x copied by route (gate/up) or the
 //                              intermediate (down) -> SMEM (128B-swizzled,
@@ -23,13 +26,12 @@
 //   outputs leave through SMEM staging buffers as TMA tensor stores.
 //
 // Warp roles (512 threads):
-//   warp 0       TMA producer: packed weights, group scales (cp.async) and the
-//                activation tile
+//   warp 0       TMA producer: packed weights, group scales and the activation
+//                tile
 //   warp 1       TMEM allocation + single-thread MMA issuer
 //   warps 2, 3   idle
-//   warps 4..11  two dequant warpgroups; warpgroup g handles pipeline stages
-//                with (stage counter & 1) == g, writing TMEM A buffer
-//                (stage counter & 3)
+//   warps 4..11  two dequant warpgroups; warpgroup g dequantises K-half g of
+//                every stage into TMEM A buffer (2 * stage counter + g) & 3
 //   warps 12..15 epilogue (TMEM -> registers -> activation / scaling -> HBM)
 //
 // Work is a persistent loop over units (route tile, weight tile, K split);
@@ -137,28 +139,28 @@ __device__ __forceinline__ int tile_row_of_lane(const GemmParams& p, int l) {
   return l;
 }
 
-// Dequantise one stage (kBlockK = 128 K values) of this thread's weight row
-// into TMEM columns [a_col, a_col + 64) of its lane.
-//   group scales: packed along K, 128 rows x 64 B with the 64-byte swizzle (one
-//   16 B chunk = one group of 32), 4 scales per row per stage; the A operand is
-//   q * s rounded once to the 16-bit type.
-//   per-channel: packed along rows, 2 boxes (row block) of 32 row pairs x 128 B
-//   with the 128-byte swizzle; the A operand is the exact code q (the scale is
-//   applied to the FP32 accumulator in the epilogue).
+// Dequantise K-half h (kHalfK = 128 K values) of one stage of this thread's
+// weight row into TMEM columns [a_col, a_col + 64) of its lane.
+//   group scales: 2 boxes (row block) of 64 rows x 128 B (256 K values) with
+//   the 128-byte swizzle (one 16 B chunk = one group of 32); scales as 128 rows
+//   x 16 B (8 groups); the A operand is q * s rounded once to the 16-bit type.
+//   per-channel: packed along rows, 4 boxes (row block, K half) of 32 row pairs
+//   x 128 B with the 128-byte swizzle; the A operand is the exact code q (the
+//   scale is applied to the FP32 accumulator in the epilogue).
 template <int SCALE, int DT>
-__device__ __forceinline__ void dequant_stage(const uint8_t* sA, const uint8_t* sS, int tr,
+__device__ __forceinline__ void dequant_stage(const uint8_t* sA, const uint8_t* sS, int tr, int h,
                                               uint32_t a_taddr) {
   using T = F16<DT>;
   const uint32_t kMask = 0x000F000Fu;
   if (SCALE == SCALE_GROUP) {
-    const uint2 sc = *reinterpret_cast<const uint2*>(sS + tr * 8);
-    const uint8_t* row = sA + tr * 64;
-    const int sw = (tr >> 1) & 3;
+    const uint2 sc = *reinterpret_cast<const uint2*>(sS + tr * 16 + h * 8);
+    const uint8_t* row = sA + (tr >> 6) * 8192 + (tr & 63) * 128;
+    const int sw = tr & 7;
     // Compact loop (not unrolled): the body stays small in the instruction
     // cache, which the other warp roles of the CTA share.
 #pragma unroll 1
-    for (int g = 0; g < kGroupsPerStage; ++g) {
-      const uint4 w = *reinterpret_cast<const uint4*>(row + ((g ^ sw) << 4));
+    for (int g = 0; g < kHalfK / kGroup; ++g) {
+      const uint4 w = *reinterpret_cast<const uint4*>(row + (((4 * h + g) ^ sw) << 4));
       const uint32_t sword = (g < 2) ? sc.x : sc.y;
       const uint16_t s16 = T::from_bf16(static_cast<uint16_t>(sword >> ((g & 1) * 16)));
       const uint32_t s2 = static_cast<uint32_t>(s16) * 0x00010001u;
@@ -185,7 +187,7 @@ __device__ __forceinline__ void dequant_stage(const uint8_t* sA, const uint8_t* 
     const int lr = tr & 63;
     const int pr = lr >> 1;
     const int shift = (lr & 1) * 4;
-    const uint8_t* row = sA + b * 4096 + pr * 128;
+    const uint8_t* row = sA + (b * 2 + h) * 4096 + pr * 128;
 #pragma unroll 1
     for (int c = 0; c < 8; ++c) {
       const uint4 w = *reinterpret_cast<const uint4*>(row + ((c ^ (pr & 7)) << 4));
@@ -208,7 +210,8 @@ __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + expf(-g));
 template <int WHICH, int SCALE, int DT>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     w4a16_gemm_kernel(const __grid_constant__ GemmParams p, const __grid_constant__ CUtensorMap tmA,
-                      const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmC) {
+                      const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmC,
+                      const __grid_constant__ CUtensorMap tmS) {
   using T = F16<DT>;
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte aligned base, derived by pointer arithmetic on the shared array so
@@ -235,7 +238,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < stages; ++s) {
       mbar_init(&full[s], 1);                  // producer (TMA bytes + scale copies)
-      mbar_init(&empty[s], 5);                 // 4 dequant warps + MMA commit
+      mbar_init(&empty[s], 9);                 // 8 dequant warps + MMA commit
     }
     for (int b = 0; b < kNumAbuf; ++b) {
       mbar_init(&afull[b], 4);
@@ -255,6 +258,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
     if (WHICH == GEMM_DOWN) tma_prefetch_desc(&tmC);
+    if (SCALE == SCALE_GROUP && p.scale_tma) tma_prefetch_desc(&tmS);
   }
   if (warp == 1) {
     tmem_alloc(tmem_holder, kTmemCols);
@@ -292,11 +296,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const int e = ti.x, m0 = ti.y;
       int r0, r1;
       tile_row_bases<WHICH>(p, w.nt, r0, r1);
-      // scale rows of this unit for this lane's tile rows (lane + 32 i); null
-      // when the row lies beyond the expert's rows
+      // cp.async scale rows of this unit for this lane's tile rows (lane + 32 i);
+      // null when the row lies beyond the expert's rows
+      const bool scale_copy = SCALE == SCALE_GROUP && !p.scale_tma;
       const uint8_t* srow[4];
-      bool srow_al8 = true;
-      if (SCALE == SCALE_GROUP) {
+      bool srow_al16 = true;
+      if (scale_copy) {
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int tr = lane + 32 * i;
@@ -304,9 +309,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           srow[i] = grow < N1 ? reinterpret_cast<const uint8_t*>(p.scales) +
                                     (static_cast<int64_t>(e) * N1 + grow) * sbytes_row
                               : nullptr;
-          srow_al8 = srow_al8 && ((reinterpret_cast<uintptr_t>(srow[i]) & 7) == 0);
+          srow_al16 = srow_al16 && ((reinterpret_cast<uintptr_t>(srow[i]) & 15) == 0);
         }
       }
+      const uint32_t stage_tx = kStageA + bn * kStageBRow + (SCALE == SCALE_GROUP && p.scale_tma ? kStageS : 0);
       for (int kb = w.kb0; kb < w.kb1; ++kb, ++it, ring_next(st, ph, stages)) {
         if (!mbar_wait(&empty[st], ph ^ 1, abort_flag, p.err)) {
           ok = false;
@@ -315,40 +321,49 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         uint8_t* sA = smem + st * p.stage_bytes;
         uint8_t* sB = sA + kStageA;
         uint8_t* sS = sB + bn * kStageBRow;
-        if (SCALE == SCALE_GROUP) {
-          // kGroupsPerStage scales (8 B) per tile row; lane handles rows lane + 32 i.
+        if (scale_copy) {
+          // kGroupsPerStage scales (16 B) per tile row; lane handles rows lane + 32 i.
           const int g0 = kb * kGroupsPerStage;
           const int ng = min(kGroupsPerStage, groups_row - g0);
-          if (srow_al8 && ng == kGroupsPerStage) {
-            // common case: one 8-byte copy per row
+          if (srow_al16 && ng == kGroupsPerStage) {
+            // common case: one 16-byte copy per row
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-              uint8_t* dst = sS + (lane + 32 * i) * 8;
-              if (srow[i]) cp_async<8>(dst, srow[i] + g0 * 2);
-              else *reinterpret_cast<uint2*>(dst) = make_uint2(0, 0);
+              uint8_t* dst = sS + (lane + 32 * i) * 16;
+              if (srow[i]) cp_async<16>(dst, srow[i] + g0 * 2);
+              else *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
             }
           } else {
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-              uint8_t* dst = sS + (lane + 32 * i) * 8;
+              uint8_t* dst = sS + (lane + 32 * i) * 16;
               const int nbytes = srow[i] ? max(ng, 0) * 2 : 0;
               for (int o = 0; o < nbytes; o += 4) cp_async<4>(dst + o, srow[i] + g0 * 2 + o);
-              for (int o = nbytes; o < 8; o += 4) *reinterpret_cast<uint32_t*>(dst + o) = 0u;
+              for (int o = nbytes; o < 16; o += 4) *reinterpret_cast<uint32_t*>(dst + o) = 0u;
             }
           }
           cp_async_mbar_arrive(&full[st]);
         }
         __syncwarp();
         if (lane == 0) {
-          mbar_arrive_expect_tx(&full[st], kStageA + bn * kStageBRow);
+          mbar_arrive_expect_tx(&full[st], stage_tx);
           if (SCALE == SCALE_GROUP) {
-            // two 64-row boxes of 64 packed bytes (128 K values), 64-byte swizzle
+            // two 64-row boxes of 128 packed bytes (256 K values), 128-byte swizzle
             tma_load_3d(sA, &tmA, &full[st], kb * (kBlockK / 2), r0, e, pol_w);
-            tma_load_3d(sA + 4096, &tmA, &full[st], kb * (kBlockK / 2), r1, e, pol_w);
+            tma_load_3d(sA + 8192, &tmA, &full[st], kb * (kBlockK / 2), r1, e, pol_w);
+            if (p.scale_tma) {
+              // two 64-row boxes of 8 group scales (16 bytes)
+              tma_load_3d(sS, &tmS, &full[st], kb * kGroupsPerStage, r0, e, pol_w);
+              tma_load_3d(sS + 1024, &tmS, &full[st], kb * kGroupsPerStage, r1, e, pol_w);
+            }
           } else {
-            // two boxes of 32 row pairs x 128 K bytes, 128-byte swizzle
-            tma_load_3d(sA, &tmA, &full[st], kb * kBlockK, r0 / 2, e, pol_w);
-            tma_load_3d(sA + 4096, &tmA, &full[st], kb * kBlockK, r1 / 2, e, pol_w);
+            // four boxes (row block, K half) of 32 row pairs x 128 K bytes, 128-byte swizzle
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              tma_load_3d(sA + h * 4096, &tmA, &full[st], kb * kBlockK + h * kHalfK, r0 / 2, e, pol_w);
+              tma_load_3d(sA + (2 + h) * 4096, &tmA, &full[st], kb * kBlockK + h * kHalfK, r1 / 2, e,
+                          pol_w);
+            }
           }
 #pragma unroll
           for (int a = 0; a < kBlockK / 64; ++a)
@@ -385,29 +400,34 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         tc_fence_after();
         const uint32_t d_tmem = tmem + kAccCol0 + b * bn;
         for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
-          const int ab = it % kNumAbuf;
           // A: the dequant warps arrive on afull[ab] only after they observed
           // full[st] complete, and full[st] also carries this stage's B bytes
-          // (one expect_tx covers weights and activations), so afull alone
-          // orders both operands before the MMAs.
-          if (!mbar_wait(&afull[ab], (it / kNumAbuf) & 1, abort_flag, p.err)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          // B descriptors of this stage: the start-address field (bits 0-13,
-          // address >> 4) advances by 2 per 32-byte K step inside a 128-byte
-          // swizzle atom and by bn * 8 per atom; adding to the 64-bit value
-          // never carries out of the field (shared addresses are < 256 KB).
-          const uint64_t d0 = d_st;
-          const uint32_t a0 = tmem + ab * kAbufCols;
-          const uint32_t acc0 = kb > w.kb0 ? 1u : 0u;
+          // (one expect_tx covers weights, scales and activations), so afull
+          // alone orders both operands before the MMAs.
 #pragma unroll
-          for (int kk = 0; kk < kBlockK / 16; ++kk) {
-            mma_ts(d_tmem, a0 + kk * 8, d0 + (kk >> 2) * atom_step + (kk & 3) * 2, idesc,
-                   kk > 0 ? 1u : acc0);
+          for (int h = 0; h < 2; ++h) {
+            const uint32_t a_seq = 2 * it + h;
+            const int ab = a_seq % kNumAbuf;
+            if (!mbar_wait(&afull[ab], (a_seq / kNumAbuf) & 1, abort_flag, p.err)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            // B descriptors of this stage: the start-address field (bits 0-13,
+            // address >> 4) advances by 2 per 32-byte K step inside a 128-byte
+            // swizzle atom and by bn * 8 per 64-value atom; adding to the 64-bit
+            // value never carries out of the field (shared addresses < 256 KB).
+            const uint64_t d0 = d_st + static_cast<uint64_t>(2 * h) * atom_step;
+            const uint32_t a0 = tmem + ab * kAbufCols;
+            const uint32_t acc0 = (kb > w.kb0 || h > 0) ? 1u : 0u;
+#pragma unroll
+            for (int kk = 0; kk < kHalfK / 16; ++kk) {
+              mma_ts(d_tmem, a0 + kk * 8, d0 + (kk >> 2) * atom_step + (kk & 3) * 2, idesc,
+                     kk > 0 ? 1u : acc0);
+            }
+            mma_commit(&aempty[ab]);
           }
-          mma_commit(&aempty[ab]);
+          if (!ok) break;
           mma_commit(&empty[st]);
           ring_next(st, ph, stages);
           d_st = st == 0 ? bdesc_base : d_st + d_stage;
@@ -436,17 +456,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const Unit w = decode_unit(p, u);
       if (w.kb1 <= w.kb0) continue;
       for (int kb = w.kb0; kb < w.kb1; ++kb, ++it, ring_next(st, ph, stages)) {
-        if ((it & 1) != static_cast<uint32_t>(wg)) continue;
-        const int ab = it % kNumAbuf;
+        const uint32_t a_seq = 2 * it + wg;
+        const int ab = a_seq % kNumAbuf;
         if (!mbar_wait(&full[st], ph, abort_flag, p.err) ||
-            !mbar_wait(&aempty[ab], ((it / kNumAbuf) & 1) ^ 1, abort_flag, p.err)) {
+            !mbar_wait(&aempty[ab], ((a_seq / kNumAbuf) & 1) ^ 1, abort_flag, p.err)) {
           ok = false;
           break;
         }
         tc_fence_after();
         const uint8_t* sA = smem + st * p.stage_bytes;
         const uint8_t* sS = sA + kStageA + bn * kStageBRow;
-        dequant_stage<SCALE, DT>(sA, sS, tr, t_lane + ab * kAbufCols);
+        dequant_stage<SCALE, DT>(sA, sS, tr, wg, t_lane + ab * kAbufCols);
         tmem_wait_st();
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[st]);
@@ -620,7 +640,8 @@ namespace w4a16 {
 
 template <int WHICH, int SCALE, int DT>
 cudaError_t launch_gemm_one(const GemmParams& p, const CUtensorMap& tmA, const CUtensorMap& tmB,
-                            const CUtensorMap& tmC, int grid, int smem_bytes, cudaStream_t s, bool pdl) {
+                            const CUtensorMap& tmC, const CUtensorMap& tmS, int grid, int smem_bytes,
+                            cudaStream_t s, bool pdl) {
   auto kern = w4a16_gemm_kernel<WHICH, SCALE, DT>;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -641,21 +662,21 @@ cudaError_t launch_gemm_one(const GemmParams& p, const CUtensorMap& tmA, const C
   attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, p, tmA, tmB, tmC);
+  return cudaLaunchKernelEx(&cfg, kern, p, tmA, tmB, tmC, tmS);
 }
 
 template <int DT>
 cudaError_t launch_gemm_dt(int which, int scale_kind, const GemmParams& p, const CUtensorMap& tmA,
-                           const CUtensorMap& tmB, const CUtensorMap& tmC, int grid, int smem_bytes,
-                           cudaStream_t s, bool pdl) {
+                           const CUtensorMap& tmB, const CUtensorMap& tmC, const CUtensorMap& tmS,
+                           int grid, int smem_bytes, cudaStream_t s, bool pdl) {
   if (which == GEMM_UP) {
     return scale_kind == SCALE_GROUP
-               ? launch_gemm_one<GEMM_UP, SCALE_GROUP, DT>(p, tmA, tmB, tmC, grid, smem_bytes, s, pdl)
-               : launch_gemm_one<GEMM_UP, SCALE_CHANNEL, DT>(p, tmA, tmB, tmC, grid, smem_bytes, s, pdl);
+               ? launch_gemm_one<GEMM_UP, SCALE_GROUP, DT>(p, tmA, tmB, tmC, tmS, grid, smem_bytes, s, pdl)
+               : launch_gemm_one<GEMM_UP, SCALE_CHANNEL, DT>(p, tmA, tmB, tmC, tmS, grid, smem_bytes, s, pdl);
   }
   return scale_kind == SCALE_GROUP
-             ? launch_gemm_one<GEMM_DOWN, SCALE_GROUP, DT>(p, tmA, tmB, tmC, grid, smem_bytes, s, pdl)
-             : launch_gemm_one<GEMM_DOWN, SCALE_CHANNEL, DT>(p, tmA, tmB, tmC, grid, smem_bytes, s, pdl);
+             ? launch_gemm_one<GEMM_DOWN, SCALE_GROUP, DT>(p, tmA, tmB, tmC, tmS, grid, smem_bytes, s, pdl)
+             : launch_gemm_one<GEMM_DOWN, SCALE_CHANNEL, DT>(p, tmA, tmB, tmC, tmS, grid, smem_bytes, s, pdl);
 }
 
 }  // namespace w4a16
