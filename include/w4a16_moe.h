@@ -196,7 +196,7 @@ typedef struct {
   int32_t gemm2_splits;    /* split-K factor of the down GEMM */
   int32_t gemm1_ctas;      /* persistent grid sizes */
   int32_t gemm2_ctas;
-  int32_t pipeline_stages;
+  int32_t pipeline_stages; /* shared-memory stages of the gate/up GEMM ring */
   int32_t gemm_path;       /* W4A16_PATH_TENSOR_CORES or W4A16_PATH_CUDA_CORES */
   size_t off_counts, off_offs, off_perm, off_inv, off_tiles, off_num_tiles;  /* bytes */
   size_t off_inter;        /* intermediate activations [max_slots, I] (act dtype) */

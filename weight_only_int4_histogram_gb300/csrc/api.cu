@@ -62,7 +62,8 @@ struct Layout {
   int n1;
   int nt1, kb1, s1, kbps1;
   int nt2, kb2, s2, kbps2;
-  int stages, stage_bytes, smem;
+  int stages, stage_bytes, smem;   // gate/up GEMM (and the CUDA-core path's both GEMMs)
+  int stages2, smem2;              // tensor-core down GEMM (output staging buffers)
   int grid1, grid2;
   size_t off_err, off_counts, off_offs, off_ntiles, off_tiles, off_perm, off_inv, off_ctr;
   size_t off_part, off_inter, off_y, off_xs;
@@ -94,14 +95,19 @@ int choose_bn_gemv(const w4a16_moe_plan_s& P, int T) {
   return lam <= 4.0 ? 8 : (lam <= 10.0 ? 16 : kGemvMaxR);
 }
 
+constexpr int kAutoMaxBN = 64;
+
 int choose_bn(const w4a16_moe_plan_s& P, int T) {
   if (P.ov_bn) return P.ov_bn;
-  // Route-count-based tile height: expected routes per expert plus ~3.5
-  // standard deviations, so that one route tile usually covers an expert.
+  // Route-count-based tile height: expected routes per expert plus three
+  // standard deviations, so that one route tile usually covers an expert, at
+  // most kAutoMaxBN routes: a stage holds the tile's activation rows (512 bytes
+  // each), and taller tiles leave too few stages in shared memory to cover
+  // the weight-load latency (4 stages at 64 routes, 2 at 128).
   const double lam = static_cast<double>(T) * P.d.top_k / P.d.num_experts;
-  const double want = lam + 3.5 * std::sqrt(lam) + 1.0;
+  const double want = lam + 3.0 * std::sqrt(lam) + 1.0;
   int bn = static_cast<int>(std::ceil(want / 16.0)) * 16;
-  return std::min(kMaxBN, std::max(16, bn));
+  return std::min(kAutoMaxBN, std::max(16, bn));
 }
 
 // Split-K factor for the expected number of route tiles: the cost model is
@@ -157,13 +163,17 @@ Layout make_layout(const w4a16_moe_plan_s& P, int T) {
     L.stage_bytes = gemv_stage_bytes(L.bn);
     L.stages = gemv_stages(L.bn, ksplit);
     L.smem = gemv_smem_bytes(L.bn, ksplit);
+    L.stages2 = L.stages;
+    L.smem2 = L.smem;
   } else {
     L.stage_bytes = kStageA + L.bn * kStageBRow + kStageS;
     // dynamic shared memory: 1 KB alignment slack + stages + 2 KB control block
     // (mbarriers, TMEM address, flags, token list)
-    const int smem_budget = 232448 - 3072 - kEpiStageBytes;
+    const int smem_budget = 232448 - 3072;
     L.stages = std::min(kMaxStages, smem_budget / L.stage_bytes);
-    L.smem = 3072 + kEpiStageBytes + L.stages * L.stage_bytes;
+    L.smem = 3072 + L.stages * L.stage_bytes;
+    L.stages2 = std::min(kMaxStages, (smem_budget - kEpiStageBytes) / L.stage_bytes);
+    L.smem2 = 3072 + kEpiStageBytes + L.stages2 * L.stage_bytes;
   }
   L.grid1 = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(P.num_sms, static_cast<int64_t>(L.tiles_cap) * L.nt1 * L.s1)));
   L.grid2 = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(P.num_sms, static_cast<int64_t>(L.tiles_cap) * L.nt2 * L.s2)));
@@ -424,6 +434,7 @@ w4a16_status launch_forward(const w4a16_moe_plan_s& P, const Layout& L, const vo
   if (P.has_ev && (e = cudaEventRecord(P.ev[1], s)) != cudaSuccess) return cuda_fail(e, "event record");
 
   GemmParams g2 = g;
+  g2.stages = L.stages2;
   g2.n_rows = d.hidden;
   g2.K = d.inter;
   g2.out_cols = d.hidden;
@@ -437,8 +448,8 @@ w4a16_status launch_forward(const w4a16_moe_plan_s& P, const Layout& L, const vo
   g2.part = nullptr;
   g2.counters = nullptr;
   g2.scale_tma = stma2 ? 1 : 0;
-  e = L.gemv ? launch_gemv(GEMM_DOWN, d.scale_kind, d.act_dtype, g2, tmA2, tmS2, L.grid2, L.smem, s, P.pdl)
-             : launch_gemm(GEMM_DOWN, d.scale_kind, d.act_dtype, g2, tmA2, tmB2, tmY, tmS2, L.grid2, L.smem, s, P.pdl);
+  e = L.gemv ? launch_gemv(GEMM_DOWN, d.scale_kind, d.act_dtype, g2, tmA2, tmS2, L.grid2, L.smem2, s, P.pdl)
+             : launch_gemm(GEMM_DOWN, d.scale_kind, d.act_dtype, g2, tmA2, tmB2, tmY, tmS2, L.grid2, L.smem2, s, P.pdl);
   if (e != cudaSuccess) return cuda_fail(e, "down GEMM launch");
   if (P.has_ev && (e = cudaEventRecord(P.ev[2], s)) != cudaSuccess) return cuda_fail(e, "event record");
 

@@ -219,8 +219,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const int stages = p.stages;
   const int bn = p.bn;
-  float* epi_stage = reinterpret_cast<float*>(smem + stages * p.stage_bytes);  // [4][2][16 x 32]
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + stages * p.stage_bytes + kEpiStageBytes);
+  // down GEMM: output staging [4 warps][2][16 x 32] after the stages
+  float* epi_stage = reinterpret_cast<float*>(smem + stages * p.stage_bytes);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + stages * p.stage_bytes +
+                                               (WHICH == GEMM_DOWN ? kEpiStageBytes : 0));
   uint64_t* empty = full + kMaxStages;
   uint64_t* afull = empty + kMaxStages;
   uint64_t* aempty = afull + kNumAbuf;
