@@ -221,16 +221,18 @@ w4a16_status w4a16_moe_set_overrides(w4a16_moe_plan_t plan, int32_t tile_rows,
 /*
  * Chooses where the expert GEMMs run for later calls with this plan.
  * W4A16_PATH_AUTO (the default) takes the CUDA-core GEMV while the expected
- * routes per local expert, num_tokens * top_k / num_experts, are at most 24
- * (group scales) or 16 (per-channel scales), and the tensor cores above that.  Both paths compute the same function
+ * routes per local expert, num_tokens * top_k / num_experts, are at most 13
+ * (group scales) or 10 (per-channel scales), or at most 80 when hidden and
+ * inter are both at least 2048, and the tensor cores above that (measured
+ * crossovers on GB300).  Both paths compute the same function
  * (the expert MLPs of "feat(pytorch): add CuTeDSL W4A16 MoE backend"
  * (LMDeploy), section Modification); they round differently (the tensor-core
  * path rounds each dequantised weight q * s to the activation type, the
  * CUDA-core path multiplies the exact codes q by the activations, sums a
  * 32-element group in FP32 and applies s to that sum), so outputs of the two
  * agree within the parity tolerance, not bit for bit.  The CUDA-core path
- * uses route tiles of 8 routes (tile_rows overrides apply to the tensor-core
- * path only).  workspace_bytes (if not
+ * uses route tiles of 8, 16 or 32 routes (tile_rows overrides apply to the
+ * tensor-core path only).  workspace_bytes (if not
  * NULL) receives the workspace size later calls need.  Unknown path:
  * W4A16_ERR_INVALID_ARG.
  */

@@ -72,18 +72,26 @@ struct Layout {
 };
 
 // Expected routes per local expert up to which the warp-MMA GEMV runs both
-// GEMMs; above it the tcgen05 path (route tiles up to 128 routes, MMA work
-// independent of the tile's fill) wins.  Measured crossovers on GB300: about
-// 27 routes per expert for the group-scale Kimi shape, 17-24 for the
-// per-channel workloads.
-constexpr double kGemvMaxRoutesGroup = 24.0;
-constexpr double kGemvMaxRoutesChannel = 16.0;
+// GEMMs; above it the tcgen05 path wins (its MMA time per weight is the same
+// for any tile fill up to 64 routes).  Measured crossovers on GB300: about 13
+// routes per expert for the group-scale Kimi and ReLU^2 shapes, about 10 for
+// the per-channel shape.  When both GEMMs reduce over at least 2048 values
+// (every GEMV unit streams eight or more 256-value stages) the GEMV stays
+// ahead much longer: on the 32-expert H = 7168, I = 2048 shape it was faster
+// through 64 routes per expert and slower at 96.
+constexpr double kGemvMaxRoutesGroup = 13.0;
+constexpr double kGemvMaxRoutesChannel = 10.0;
+constexpr double kGemvMaxRoutesLongK = 80.0;
 
 bool use_gemv(const w4a16_moe_plan_s& P, int T) {
   if (P.path == W4A16_PATH_TENSOR_CORES) return false;
   if (P.path == W4A16_PATH_CUDA_CORES) return true;
   const double lam = static_cast<double>(T) * P.d.top_k / P.d.num_experts;
-  return lam <= (P.d.scale_kind == W4A16_SCALE_GROUP32_K ? kGemvMaxRoutesGroup : kGemvMaxRoutesChannel);
+  const bool long_k = P.d.hidden >= 2048 && P.d.inter >= 2048;
+  const double limit = long_k ? kGemvMaxRoutesLongK
+                              : (P.d.scale_kind == W4A16_SCALE_GROUP32_K ? kGemvMaxRoutesGroup
+                                                                        : kGemvMaxRoutesChannel);
+  return lam <= limit;
 }
 
 // CUDA-core path: route tiles of 8, 16 or 32 routes (one, two or four MMA N

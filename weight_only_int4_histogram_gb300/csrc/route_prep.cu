@@ -9,8 +9,10 @@
 // One CTA of 32 warps.  The flat routes r = t*k + j are cut into 32 contiguous
 // chunks, one per warp, so "earlier warp" means "smaller flat index":
 //   pass 1  per-warp histograms hist[w][e] (warp-synchronous, no atomics):
-//           lanes holding the same expert find each other with one ballot per
-//           bit of the expert index and their lowest lane adds the group size;
+//           lanes holding the same expert find each other (match_any for short
+//           chunks, one ballot per bit of the expert index for long ones, which
+//           measured faster at thousands of routes) and their lowest lane adds
+//           the group size;
 //   pass 2  column prefix over warps (routes of expert e in earlier chunks),
 //           then a warp-shuffle exclusive scan over experts of the padded
 //           segment sizes and of the tile counts;
@@ -18,7 +20,7 @@
 //           earlier-round count + rank among equal lanes of its round, which
 //           is its rank in ascending flat order: a stable permutation.
 // Padding slots get perm = -1 and the tile list (expert, first slot, valid
-// rows) is written per expert, one warp per expert (coalesced stores).  Integer work only: results are bit-exact and
+// rows) is written per expert.  Integer work only: results are bit-exact and
 // independent of scheduling.
 #include "common.cuh"
 
@@ -65,6 +67,10 @@ __global__ void __launch_bounds__(kRoutePrepThreads, 1) route_prep_kernel(const 
   const unsigned full = 0xFFFFFFFFu;
   const unsigned lt_mask = (1u << lane) - 1u;
   const int key_bits = 32 - __clz(E);  // keys e + 1 lie in [0, E]
+  const bool by_ballot = chunk > 64;    // uniform over the CTA
+  auto same_expert = [&](int e) -> unsigned {
+    return by_ballot ? lanes_with_key(e + 1, key_bits) : __match_any_sync(full, e);
+  };
 
   auto local_of = [&](int r) -> int {
     if (r >= r_end) return -1;
@@ -84,7 +90,7 @@ __global__ void __launch_bounds__(kRoutePrepThreads, 1) route_prep_kernel(const 
 #pragma unroll
     for (int i = 0; i < kBatch; ++i) {
       const int e = eb[i];
-      const unsigned m = lanes_with_key(e + 1, key_bits);
+      const unsigned m = same_expert(e);
       if (e >= 0 && (m & lt_mask) == 0) hist[warp * E + e] += __popc(m);
       __syncwarp();
     }
@@ -161,7 +167,7 @@ __global__ void __launch_bounds__(kRoutePrepThreads, 1) route_prep_kernel(const 
     for (int i = 0; i < kBatch; ++i) {
       const int r = base + 32 * i + lane;
       const int e = eb[i];
-      const unsigned m = lanes_with_key(e + 1, key_bits);
+      const unsigned m = same_expert(e);
       if (e >= 0) {
         const int slot = poff[e] + hist[warp * E + e] + __popc(m & lt_mask);
         p.perm[slot] = r;
@@ -175,17 +181,16 @@ __global__ void __launch_bounds__(kRoutePrepThreads, 1) route_prep_kernel(const 
     }
   }
 
-  // padding slots, tile list, counts and offsets (one warp per expert)
-  for (int e = warp; e < E; e += kRoutePrepWarps) {
+  // padding slots, tile list, counts and offsets
+  for (int e = tid; e < E; e += kRoutePrepThreads) {
     const int c = cnt[e];
-    const int s0 = poff[e];
-    for (int s = s0 + c + lane; s < poff[e + 1]; s += 32) p.perm[s] = -1;
+    for (int s = poff[e] + c; s < poff[e + 1]; ++s) p.perm[s] = -1;
     const int nt = toff[e + 1] - toff[e];
-    for (int i = lane; i < nt; i += 32) p.tiles[toff[e] + i] = make_int4(e, s0 + i * p.bm, min(p.bm, c - i * p.bm), 0);
-    if (lane == 0) {
-      p.counts[e] = c;
-      p.offs[e] = s0;
+    for (int i = 0; i < nt; ++i) {
+      p.tiles[toff[e] + i] = make_int4(e, poff[e] + i * p.bm, min(p.bm, c - i * p.bm), 0);
     }
+    p.counts[e] = c;
+    p.offs[e] = poff[e];
   }
   if (tid == 0) {
     p.offs[E] = poff[E];
