@@ -200,7 +200,8 @@ typedef struct {
   int32_t gemm_path;       /* W4A16_PATH_TENSOR_CORES or W4A16_PATH_CUDA_CORES */
   size_t off_counts, off_offs, off_perm, off_inv, off_tiles, off_num_tiles;  /* bytes */
   size_t off_inter;        /* intermediate activations [max_slots, I] (act dtype) */
-  size_t off_expert_out;   /* FP32 expert outputs [gemm2_splits, max_slots, H] */
+  size_t off_expert_out;   /* expert outputs [max_slots, H] in the activation dtype, or FP32
+                              split partials [gemm2_splits, max_slots, H] when gemm2_splits > 1 */
 } w4a16_route_info;
 
 w4a16_status w4a16_moe_route_info(w4a16_moe_plan_t plan, int32_t num_tokens,

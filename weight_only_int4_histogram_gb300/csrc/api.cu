@@ -203,7 +203,8 @@ Layout make_layout(const w4a16_moe_plan_s& P, int T) {
   L.off_ctr = take(sizeof(int32_t) * L.tiles_cap * L.nt1);
   L.off_part = take(L.s1 > 1 ? sizeof(float) * L.s1 * L.slots_cap * L.n1 : 0);
   L.off_inter = take(static_cast<size_t>(act_bytes) * L.slots_cap * d.inter);
-  L.off_y = take(sizeof(float) * L.s2 * L.slots_cap * d.hidden);
+  // expert outputs: the activation dtype without down split-K, FP32 partials with it
+  L.off_y = take((L.s2 == 1 ? static_cast<size_t>(act_bytes) : sizeof(float) * L.s2) * L.slots_cap * d.hidden);
   L.off_xs = take(L.gemv ? 0 : static_cast<size_t>(act_bytes) * L.slots_cap * d.hidden);
   L.off_sx = take(static_cast<size_t>(act_bytes) * T * d.hidden);
   L.off_sids = take(sizeof(int32_t) * std::max(L.R, 1));
@@ -252,18 +253,21 @@ bool encode_weights(CUtensorMap* m, const void* base, uint64_t inner, uint64_t r
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// FP32 row-major matrix [rows][cols], unswizzled boxes of 32 columns x 16 rows
-// (the down GEMM's output stores).
-bool encode_out32(CUtensorMap* m, void* base, uint64_t cols, uint64_t rows) {
+// Expert outputs y [rows][cols] (FP32, or the 16-bit activation dtype), unswizzled
+// boxes of 32 columns x 16 rows (the down GEMM's output stores).
+bool encode_out(CUtensorMap* m, void* base, uint64_t cols, uint64_t rows, bool fp32, int dtype) {
   auto fn = encode_fn();
   if (!fn) return false;
+  const uint64_t es_bytes = fp32 ? 4 : 2;
   cuuint64_t dims[2] = {cols, rows};
-  cuuint64_t strides[1] = {cols * 4};
+  cuuint64_t strides[1] = {cols * es_bytes};
   cuuint32_t box[2] = {32, 16};
   cuuint32_t es[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-            CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  const CUtensorMapDataType t = fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                     : (dtype == W4A16_DT_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                               : CU_TENSOR_MAP_DATA_TYPE_FLOAT16);
+  return fn(m, t, 2, base, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // BF16 group scales as a 3D tensor [E][rows][groups], unswizzled boxes of 8
@@ -378,10 +382,12 @@ w4a16_status launch_forward(const w4a16_moe_plan_s& P, const Layout& L, const vo
   CUtensorMap tmX;
   memset(&tmX, 0, sizeof(tmX));
   if (!L.gemv) ok = ok && encode_rows16(&tmX, ws + L.off_xs, d.hidden, L.slots_cap, L.bn, d.act_dtype);
-  // tensor-core path: FP32 expert outputs y [splits * slots_cap, H], TMA-stored
+  // tensor-core path: expert outputs y [splits * slots_cap, H], TMA-stored
+  const bool y16 = L.s2 == 1;
   CUtensorMap tmY;
   memset(&tmY, 0, sizeof(tmY));
-  if (!L.gemv) ok = ok && encode_out32(&tmY, ws + L.off_y, d.hidden, static_cast<uint64_t>(L.s2) * L.slots_cap);
+  if (!L.gemv)
+    ok = ok && encode_out(&tmY, ws + L.off_y, d.hidden, static_cast<uint64_t>(L.s2) * L.slots_cap, !y16, d.act_dtype);
   // group scales by TMA (boxes of 8 groups) where their rows are 16-byte multiples
   CUtensorMap tmS1, tmS2;
   memset(&tmS1, 0, sizeof(tmS1));
@@ -456,13 +462,15 @@ w4a16_status launch_forward(const w4a16_moe_plan_s& P, const Layout& L, const vo
   g2.part = nullptr;
   g2.counters = nullptr;
   g2.scale_tma = stma2 ? 1 : 0;
+  g2.out16 = y16 ? 1 : 0;
   e = L.gemv ? launch_gemv(GEMM_DOWN, d.scale_kind, d.act_dtype, g2, tmA2, tmS2, L.grid2, L.smem2, s, P.pdl)
              : launch_gemm(GEMM_DOWN, d.scale_kind, d.act_dtype, g2, tmA2, tmB2, tmY, tmS2, L.grid2, L.smem2, s, P.pdl);
   if (e != cudaSuccess) return cuda_fail(e, "down GEMM launch");
   if (P.has_ev && (e = cudaEventRecord(P.ev[2], s)) != cudaSuccess) return cuda_fail(e, "event record");
 
   CombineParams c = {};
-  c.y = reinterpret_cast<const float*>(ws + L.off_y);
+  c.y = ws + L.off_y;
+  c.y16 = y16 ? 1 : 0;
   c.slots_cap = L.slots_cap;
   c.splits = L.s2;
   c.inv = reinterpret_cast<const int32_t*>(ws + L.off_inv);

@@ -30,7 +30,7 @@ constexpr int kMaxBN = 128;
 constexpr int kStageA = kTileRows * kBlockK / 2;   // 16 KB packed INT4 per stage
 constexpr int kStageS = kTileRows * kGroupsPerStage * 2;  // 2 KB BF16 group scales per stage
 constexpr int kStageBRow = kBlockK * 2;            // bytes of one activation row per stage
-// Down-GEMM output staging: 4 epilogue warps x 2 buffers x (16 routes x 32 rows FP32)
+// Down-GEMM output staging: 4 epilogue warps x 2 buffers x (16 routes x 32 rows, up to FP32)
 constexpr int kEpiStageBytes = 4 * 2 * 16 * 32 * 4;
 
 // CUDA-core GEMV path (gemv.cuh): route tiles of at most kGemvMaxR routes,
@@ -119,10 +119,13 @@ struct GemmParams {
   int32_t* err;
   int32_t tiles_cap;       // capacity of `tiles`
   int32_t scale_tma;       // group scales loaded by TMA (their rows are 16-byte multiples)
+  int32_t out16;           // down GEMM: expert outputs in the activation dtype (no split-K),
+                           // else FP32 split partials
 };
 
 struct CombineParams {
-  const float* y;          // [splits, slots_cap, H]
+  const void* y;           // [splits, slots_cap, H]: activation dtype when y16, else FP32
+  int32_t y16;
   int64_t slots_cap;
   int32_t splits;
   const int32_t* inv;      // [T * k]

@@ -22,8 +22,9 @@
 //                              intermediate (down) -> SMEM (128B-swizzled,
 //                              K-major)
 //   tcgen05.mma.kind::f16 (A from TMEM, B from SMEM), FP32 accumulators in TMEM,
-//   double-buffered, drained by four epilogue warps; the down GEMM's FP32
-//   outputs leave through SMEM staging buffers as TMA tensor stores.
+//   double-buffered, drained by four epilogue warps; the down GEMM's outputs
+//   (activation dtype, or FP32 split partials) leave through SMEM staging
+//   buffers as TMA tensor stores.
 //
 // Warp roles (512 threads):
 //   warp 0       TMA producer: packed weights, group scales and the activation
@@ -533,13 +534,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         for (int j = 0; j < 16; ++j) v[j] *= scale;
         if (WHICH == GEMM_DOWN) {
           // This warp's 32 output columns x 16 slots through a staging buffer
-          // (slot-major, conflict-free) and one TMA store.  Slots past the
+          // (slot-major, conflict-free) and one TMA store, in the activation
+          // dtype (one rounding) or as FP32 split partials.  Slots past the
           // tile's valid rows are padding slots of y, never read.
           float* stg = epi_stage + (q * 2 + sbuf) * (16 * 32);
           if (lane == 0) bulk_wait_read<1>();  // the store that last read this buffer
           __syncwarp();
+          if (p.out16) {
+            uint16_t* stg16 = reinterpret_cast<uint16_t*>(stg);
 #pragma unroll
-          for (int j = 0; j < 16; ++j) stg[j * 32 + lane] = v[j];
+            for (int j = 0; j < 16; ++j) stg16[j * 32 + lane] = T::from_float(v[j]);
+          } else {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) stg[j * 32 + lane] = v[j];
+          }
           fence_proxy_async_smem();
           __syncwarp();
           const int col0 = grow - lane;

@@ -311,8 +311,22 @@ __device__ __forceinline__ bool gemv_epilogue(const GemmParams& p, uint64_t* epi
 
   if (WHICH == GEMM_DOWN) {
     if (!fin) return true;
-    float* y = reinterpret_cast<float*>(p.out) + (static_cast<int64_t>(w.split) * p.slots_cap + m0) * p.out_cols;
     const int64_t oc = p.out_cols;
+    const int64_t y0 = (static_cast<int64_t>(w.split) * p.slots_cap + m0) * oc;
+    if (p.out16) {
+      // expert outputs in the activation dtype (one rounding)
+      uint16_t* y = reinterpret_cast<uint16_t*>(p.out) + y0;
+#pragma unroll
+      for (int n = 0; n < NB; ++n) {
+        const int rt0 = 8 * n + 2 * t, rt1 = rt0 + 1;
+        if (rt0 < rows && okA) y[rt0 * oc + growA] = F16<DT>::from_float(tot[4 * n + 0] * scA);
+        if (rt1 < rows && okA) y[rt1 * oc + growA] = F16<DT>::from_float(tot[4 * n + 1] * scA);
+        if (rt0 < rows && okB) y[rt0 * oc + growB] = F16<DT>::from_float(tot[4 * n + 2] * scB);
+        if (rt1 < rows && okB) y[rt1 * oc + growB] = F16<DT>::from_float(tot[4 * n + 3] * scB);
+      }
+      return true;
+    }
+    float* y = reinterpret_cast<float*>(p.out) + y0;
 #pragma unroll
     for (int n = 0; n < NB; ++n) {
       const int rt0 = 8 * n + 2 * t, rt1 = rt0 + 1;
