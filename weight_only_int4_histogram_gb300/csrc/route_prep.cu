@@ -8,17 +8,17 @@
 //
 // One CTA of 32 warps.  The flat routes r = t*k + j are cut into 32 contiguous
 // chunks, one per warp, so "earlier warp" means "smaller flat index":
-//   pass 1  per-warp histograms hist[w][e] (warp-synchronous, no atomics):
-//           lanes holding the same expert find each other (match_any for short
-//           chunks, one ballot per bit of the expert index for long ones, which
-//           measured faster at thousands of routes) and their lowest lane adds
-//           the group size;
+//   pass 1  per-warp histograms hist[w][e]: counts only, so shared-memory
+//           integer atomics (exact, order-independent) suffice;
 //   pass 2  column prefix over warps (routes of expert e in earlier chunks),
 //           then a warp-shuffle exclusive scan over experts of the padded
 //           segment sizes and of the tile counts;
 //   pass 3  every valid route takes slot offs[e] + earlier-chunk count +
 //           earlier-round count + rank among equal lanes of its round, which
-//           is its rank in ascending flat order: a stable permutation.
+//           is its rank in ascending flat order: a stable permutation.  Lanes
+//           holding the same expert find each other with match_any for short
+//           chunks and with one ballot per bit of the expert index for long
+//           ones (measured faster at thousands of routes).
 // Padding slots get perm = -1 and the tile list (expert, first slot, valid
 // rows) is written per expert.  Integer work only: results are bit-exact and
 // independent of scheduling.
@@ -88,12 +88,8 @@ __global__ void __launch_bounds__(kRoutePrepThreads, 1) route_prep_kernel(const 
 #pragma unroll
     for (int i = 0; i < kBatch; ++i) eb[i] = local_of(base + 32 * i + lane);
 #pragma unroll
-    for (int i = 0; i < kBatch; ++i) {
-      const int e = eb[i];
-      const unsigned m = same_expert(e);
-      if (e >= 0 && (m & lt_mask) == 0) hist[warp * E + e] += __popc(m);
-      __syncwarp();
-    }
+    for (int i = 0; i < kBatch; ++i)
+      if (eb[i] >= 0) atomicAdd(&hist[warp * E + eb[i]], 1);
   }
   __syncthreads();
 
