@@ -240,16 +240,15 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // Packed INT4 weights as a 3D uint8 tensor [E][rows][inner bytes], 128-byte
 // swizzled boxes of 128 bytes x box_rows.
 bool encode_weights(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint64_t E,
-                    uint32_t box_inner, uint32_t box_rows) {
+                    uint32_t box_rows) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[3] = {inner, rows, E};
   cuuint64_t strides[2] = {inner, inner * rows};
-  cuuint32_t box[3] = {box_inner, box_rows, 1};
+  cuuint32_t box[3] = {128, box_rows, 1};
   cuuint32_t es[3] = {1, 1, 1};
-  const CUtensorMapSwizzle sw = box_inner == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B;
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -369,13 +368,13 @@ w4a16_status launch_forward(const w4a16_moe_plan_s& P, const Layout& L, const vo
   if (group) {
     // rows of packed bytes along K; boxes of 64 rows x one stage of K (128
     // bytes = 256 K values, 128-byte swizzle) on both paths
-    const uint32_t box = L.gemv ? kGemvBlockK / 2 : kBlockK / 2;
-    ok = encode_weights(&tmA1, w13, d.hidden / 2, L.n1, d.num_experts, box, 64) &&
-         encode_weights(&tmA2, w2, d.inter / 2, d.hidden, d.num_experts, box, 64);
+    static_assert(kGemvBlockK / 2 == 128 && kBlockK / 2 == 128, "weight boxes are 128 bytes wide");
+    ok = encode_weights(&tmA1, w13, d.hidden / 2, L.n1, d.num_experts, 64) &&
+         encode_weights(&tmA2, w2, d.inter / 2, d.hidden, d.num_experts, 64);
   } else {
     // row pairs of K bytes; boxes of 128 bytes (128 K values) x 32 row pairs
-    ok = encode_weights(&tmA1, w13, d.hidden, L.n1 / 2, d.num_experts, 128, 32) &&
-         encode_weights(&tmA2, w2, d.inter, d.hidden / 2, d.num_experts, 128, 32);
+    ok = encode_weights(&tmA1, w13, d.hidden, L.n1 / 2, d.num_experts, 32) &&
+         encode_weights(&tmA2, w2, d.inter, d.hidden / 2, d.num_experts, 32);
   }
   ok = ok && encode_rows16(&tmB2, ws + L.off_inter, d.inter, L.slots_cap, L.bn, d.act_dtype);
   // tensor-core path: activation rows copied into slot order, read as tiles

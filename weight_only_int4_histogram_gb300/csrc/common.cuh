@@ -107,7 +107,7 @@ struct GemmParams {
   int32_t stage_bytes;
   const int4* tiles;       // route tiles (expert, first slot, valid rows, 0)
   const int32_t* num_tiles;
-  const int32_t* perm;     // slot -> flat route (gate/up gather)
+  const int32_t* perm;     // slot -> flat route (CUDA-core path: activation rows by token)
   const void* x;           // CUDA-core path only: activations [T, H] (gate/up)
                            // or the intermediate [slots_cap, I] (down)
   const uint16_t* scales;  // BF16 scale bits of this GEMM's weights
@@ -170,7 +170,6 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
   return t;
 }
 
-__device__ __forceinline__ uint32_t lane_id() { return threadIdx.x & 31; }
 
 // Programmatic dependent launch.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
@@ -288,19 +287,6 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, u
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::"
       "cache_hint [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "l"(policy)
-      : "memory");
-}
-
-// Four rows (r0..r3) of a 2D tensor, each `box[0]` elements wide starting at
-// column c0; the tensor map's box is one row high.
-__device__ __forceinline__ void tma_gather4(void* dst, const CUtensorMap* map, uint64_t* bar,
-                                            int c0, int r0, int r1, int r2, int r3,
-                                            uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
-      ".L2::cache_hint [%0], [%1, {%3, %4, %5, %6, %7}], [%2], %8;" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(r0), "r"(r1),
-      "r"(r2), "r"(r3), "l"(policy)
       : "memory");
 }
 
@@ -459,11 +445,6 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
 
 __device__ __forceinline__ void tmem_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
-
-// Named barrier over a subset of warps.
-__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
 __device__ __forceinline__ uint32_t lop3_and_xor(uint32_t a, uint32_t b, uint32_t c) {

@@ -20,7 +20,7 @@
 //           chunks and with one ballot per bit of the expert index for long
 //           ones (measured faster at thousands of routes).
 // Padding slots get perm = -1 and the tile list (expert, first slot, valid
-// rows) is written per expert.  Integer work only: results are bit-exact and
+// rows) is written per expert, several threads per expert when E is small.  Integer work only: results are bit-exact and
 // independent of scheduling.
 #include "common.cuh"
 
@@ -177,16 +177,23 @@ __global__ void __launch_bounds__(kRoutePrepThreads, 1) route_prep_kernel(const 
     }
   }
 
-  // padding slots, tile list, counts and offsets
-  for (int e = tid; e < E; e += kRoutePrepThreads) {
+  // padding slots, tile list, counts and offsets: tpe threads per expert (the
+  // largest power of two with E * tpe <= the block), each taking every tpe-th
+  // padding slot and tile of its expert
+  int tpe = 1;
+  while (2 * tpe * E <= kRoutePrepThreads) tpe *= 2;
+  for (int i = tid; i < E * tpe; i += kRoutePrepThreads) {
+    const int e = i / tpe, sub = i % tpe;
     const int c = cnt[e];
-    for (int s = poff[e] + c; s < poff[e + 1]; ++s) p.perm[s] = -1;
+    for (int s = poff[e] + c + sub; s < poff[e + 1]; s += tpe) p.perm[s] = -1;
     const int nt = toff[e + 1] - toff[e];
-    for (int i = 0; i < nt; ++i) {
-      p.tiles[toff[e] + i] = make_int4(e, poff[e] + i * p.bm, min(p.bm, c - i * p.bm), 0);
+    for (int t = sub; t < nt; t += tpe) {
+      p.tiles[toff[e] + t] = make_int4(e, poff[e] + t * p.bm, min(p.bm, c - t * p.bm), 0);
     }
-    p.counts[e] = c;
-    p.offs[e] = poff[e];
+    if (sub == 0) {
+      p.counts[e] = c;
+      p.offs[e] = poff[e];
+    }
   }
   if (tid == 0) {
     p.offs[E] = poff[E];
