@@ -54,6 +54,8 @@ def lib():
             L.oracle_moe_forward.argtypes = [P, i32, P, P, P, P, P, P, P, i32, P, i32, P, P, i32]
             L.oracle_moe_forward.restype = ctypes.c_int
             L.oracle_num_threads.restype = ctypes.c_int
+            L.oracle_route_topk.argtypes = [P, i32, i32, i32, P, P]
+            L.oracle_route_topk.restype = ctypes.c_int
             _lib = L
     return _lib
 
@@ -150,6 +152,19 @@ def prepare_routes(cfg, ids, bm: int):
         raise RuntimeError(f"oracle_prepare_routes failed: {rc}")
     return dict(counts=counts, offs=offs, perm=perm[: offs[E]].copy(), inv=inv[:R].copy(),
                 tiles=tiles[: nt[0]].copy(), num_tiles=int(nt[0]))
+
+
+def route_topk(logits, top_k: int):
+    """Router softmax + top-k.  logits [T, G] FP32; returns (ids int32 [T, k],
+    weights float64 [T, k]) (the oracle's definition, see w4a16_oracle.cpp)."""
+    lg = np.ascontiguousarray(_np(logits, np.float32))
+    T, G = lg.shape
+    ids = np.zeros((T, top_k), np.int32)
+    w = np.zeros((T, top_k), np.float64)
+    rc = lib().oracle_route_topk(_ptr(lg), T, G, top_k, _ptr(ids), _ptr(w))
+    if rc != 0:
+        raise RuntimeError(f"oracle_route_topk failed: {rc}")
+    return ids, w
 
 
 def moe_forward(cfg, x, weights, topk_weights, ids, renormalize: bool = False,

@@ -222,6 +222,41 @@ int oracle_prepare_routes(const int32_t* desc_in, int32_t num_tokens, const int3
   return 0;
 }
 
+// Router scores -> routes, the step before the route layout: "feat(pytorch):
+// add CuTeDSL W4A16 MoE backend" (LMDeploy), section *Benchmark*, takes the
+// routes from a router score / top-k computation (outside its timed region)
+// and gives the routing weights as FP32 with renormalize=False.  Plainest
+// reading: probabilities p = softmax(logits[t, :]) over all num_global
+// experts; the k experts with the largest p, in descending order, ties to the
+// lower expert index; weights are those p.  softmax is strictly increasing in
+// the logit, so the order is taken on the logits themselves (exact); p is
+// computed in double.
+int oracle_route_topk(const float* logits, int32_t num_tokens, int32_t num_global, int32_t top_k,
+                      int32_t* ids, double* weights) {
+  if (num_tokens < 0 || num_global < 1 || top_k < 1 || top_k > num_global) return 1;
+  std::vector<int32_t> order(num_global);
+  for (int32_t t = 0; t < num_tokens; ++t) {
+    const float* l = logits + static_cast<int64_t>(t) * num_global;
+    double m = l[0];
+    for (int32_t e = 1; e < num_global; ++e) m = l[e] > m ? l[e] : m;
+    double sum = 0.0;
+    for (int32_t e = 0; e < num_global; ++e) sum += std::exp(static_cast<double>(l[e]) - m);
+    // selection: repeatedly take the largest remaining logit (lowest index on ties)
+    std::vector<char> taken(num_global, 0);
+    for (int32_t j = 0; j < top_k; ++j) {
+      int32_t best = -1;
+      for (int32_t e = 0; e < num_global; ++e) {
+        if (taken[e]) continue;
+        if (best < 0 || l[e] > l[best]) best = e;
+      }
+      taken[best] = 1;
+      ids[static_cast<int64_t>(t) * top_k + j] = best;
+      weights[static_cast<int64_t>(t) * top_k + j] = std::exp(static_cast<double>(l[best]) - m) / sum;
+    }
+  }
+  return 0;
+}
+
 // The MoE forward for a subset of tokens (rows == nullptr: all tokens).
 // x [T, H] (bf16 or fp16 bits), topk_weights/ids [T, k].
 // acc_out [nrows, H] FP32 combine result before the cast; out [nrows, H] bits.
