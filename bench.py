@@ -270,6 +270,32 @@ def time_stages(moe, w, x, ids, tw, out, flush, stream, steps):
     return [statistics.mean(a) for a in acc]
 
 
+def time_router(cfg, T, flush, stream, steps, hbm):
+    """The router step (softmax + top-k over the workload's logits), timed on
+    its own: the pages keep it outside the forward's timed region.  L2 flushed
+    before every launch; algorithmic bytes = logits read + ids/weights written."""
+    import weight_only_int4_histogram_gb300 as W
+    logits = gen.make_logits(cfg, T, "cuda")
+    for _ in range(3):
+        W.route_topk(logits, cfg.top_k, stream=stream)
+    times = []
+    for _ in range(steps):
+        with torch.cuda.stream(stream):
+            flush.zero_()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        W.route_topk(logits, cfg.top_k, stream=stream)
+        b.record(stream)
+        torch.cuda.synchronize()
+        times.append(a.elapsed_time(b) * 1000.0)
+    us = statistics.median(times)
+    nbytes = T * cfg.n_global * 4 + T * cfg.top_k * 8
+    gbs = nbytes / (us * 1e-6) / 1e9
+    return {"us": round(us, 3), "gbs": round(gbs, 1), "frac": round(gbs / hbm, 4), "alg_bytes": nbytes,
+            "what": "router softmax + top-k of the same tokens (outside the forward's timed region)"}
+
+
 def stage_bytes(cfg, ids):
     """Algorithmic bytes per launch of each kernel: the touched experts'
     packed weights + scales, the activations it must read, the output."""
@@ -348,6 +374,7 @@ def run_gpu(args):
             "traffic": measured_traffic(cfg.name, args.tokens, names[k], head["gemm_path"]),
             "alg_bytes_per_launch": b[k], "launch_us": round(st[k], 3),
             "stage_us": {n: round(v, 3) for n, v in zip(names, st)}}
+    router = time_router(cfg, args.tokens, flush, stream, max(args.steps, 5), hbm)
 
     sweep = []
     if not args.no_sweep:
@@ -409,7 +436,9 @@ def run_gpu(args):
         "sweep": sweep,
         "e2e": {"value": round(e2e_med, 3), "unit": "us", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
-        "gpu_launches": 4 * args.steps,
+        # route prep, (slot-order copy on the tensor-core path,) two GEMMs, combine
+        "gpu_launches": (5 if head["gemm_path"] == "tensor_cores" else 4) * args.steps,
+        "router": router,
         "clocks": clocks,
     }
     if not args.no_cpu_baseline and rank == 0 and world == 1:

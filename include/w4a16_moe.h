@@ -240,6 +240,31 @@ w4a16_status w4a16_moe_set_overrides(w4a16_moe_plan_t plan, int32_t tile_rows,
 w4a16_status w4a16_moe_set_gemm_path(w4a16_moe_plan_t plan, int32_t path, size_t* workspace_bytes);
 
 /*
+ * w4a16_moe_route_topk -- the router step before prepare_routes: softmax over
+ * each token's router logits, then its top_k experts.  "feat(pytorch): add
+ * CuTeDSL W4A16 MoE backend" (LMDeploy), section Benchmark, takes the routes
+ * (INT32 expert ids, FP32 routing weights, renormalize=False) from a router
+ * score / top-k computation.
+ *   logits        [num_tokens, num_global] FP32, row-major (device, 4-byte
+ *                 aligned); num_global = experts of the whole model, 1..1024
+ *   top_k         1..min(16, num_global)
+ *   topk_ids      [num_tokens, top_k] int32 out (device): global expert
+ *                 indices by descending probability, ties to the lower index;
+ *                 feed them (with the plan's expert_offset) to prepare_routes
+ *                 and forward, which mask the experts of other ranks
+ *   topk_weights  [num_tokens, top_k] FP32 out (device): the softmax
+ *                 probabilities of the selected experts (not renormalised;
+ *                 forward's `renormalize` does that)
+ * The selection compares the logits exactly (softmax is increasing in them);
+ * the probabilities are FP32.  Asynchronous on `stream`, no allocation, CUDA
+ * graph capturable; num_tokens == 0 is a no-op.  Errors: W4A16_ERR_INVALID_ARG
+ * (NULL or misaligned pointers, negative num_tokens), W4A16_ERR_UNSUPPORTED
+ * (num_global or top_k out of range), W4A16_ERR_CUDA (launch failure).
+ */
+w4a16_status w4a16_moe_route_topk(const float* logits, int32_t num_tokens, int32_t num_global, int32_t top_k,
+                                  int32_t* topk_ids, float* topk_weights, void* stream);
+
+/*
  * Reads (synchronously, on `stream`) and clears the device error flag in the
  * workspace.  Returns W4A16_ERR_DEVICE_TIMEOUT if a kernel gave up waiting
  * since the last prepare_routes on this workspace (prepare_routes clears it).

@@ -90,6 +90,24 @@ def test_calls_reject_bad_arguments_without_launching(lib):
     _lib.w4a16_moe_plan_destroy(plan)
 
 
+def test_route_topk_rejects_bad_arguments_without_launching(lib):
+    fake = 0x10000  # never dereferenced: validation fails first
+    for args, status in [((fake, -1, 8, 2, fake, fake), 1),       # negative num_tokens
+                         ((fake, 4, 0, 1, fake, fake), 2),        # num_global < 1
+                         ((fake, 4, 1025, 8, fake, fake), 2),     # num_global > 1024
+                         ((fake, 4, 8, 0, fake, fake), 2),        # top_k < 1
+                         ((fake, 4, 8, 9, fake, fake), 2),        # top_k > num_global
+                         ((fake, 4, 64, 17, fake, fake), 2),      # top_k > 16
+                         ((0, 4, 8, 2, fake, fake), 1),           # null logits
+                         ((fake + 2, 4, 8, 2, fake, fake), 1),    # misaligned logits
+                         ((fake, 4, 8, 2, fake, 0), 1)]:          # null weights
+        with pytest.raises(_lib.W4A16Error) as ei:
+            _lib.w4a16_moe_route_topk(*args, 0)
+        assert ei.value.status == status, args
+    # an empty batch succeeds even with null pointers
+    _lib.w4a16_moe_route_topk(0, 0, 8, 2, 0, 0, 0)
+
+
 def test_overrides_validate_and_resize_workspace(lib):
     plan, ws = _lib.w4a16_moe_plan(good_desc())
     with pytest.raises(_lib.W4A16Error):

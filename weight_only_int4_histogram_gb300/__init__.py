@@ -1,7 +1,8 @@
 """GB300 (sm_103a) local W4A16 MoE forward.
 
-The computation (route preparation, expert-grouped gate/up GEMM over packed
-INT4 weights, SwiGLU / ReLU^2, down GEMM, FP32 top-k combine) runs entirely in
+The computation (optionally the router's softmax + top-k, route preparation,
+expert-grouped gate/up GEMM over packed INT4 weights, SwiGLU / ReLU^2, down
+GEMM, FP32 top-k combine) runs entirely in
 the hand-written kernels of ``libw4a16_moe.so`` behind the C ABI declared in
 ``include/w4a16_moe.h``.  This package only marshals torch tensors (device
 memory and streams) into that ABI.
@@ -14,7 +15,7 @@ from . import _lib
 from ._lib import (Desc, RouteInfo, W4A16Error, w4a16_moe_check_device_error,  # noqa: F401
                    w4a16_moe_forward, w4a16_moe_forward_host, w4a16_moe_plan,
                    w4a16_moe_plan_destroy, w4a16_moe_prepare_routes, w4a16_moe_route_info,
-                   w4a16_moe_set_gemm_path, w4a16_moe_set_overrides)
+                   w4a16_moe_route_topk, w4a16_moe_set_gemm_path, w4a16_moe_set_overrides)
 from ._lib import PATH_AUTO, PATH_CUDA_CORES, PATH_TENSOR_CORES  # noqa: F401
 
 ACT_SWIGLU, ACT_RELU2 = 0, 1
@@ -33,6 +34,21 @@ def _ptr(t) -> int:
 def _stream(stream) -> int:
     s = stream if stream is not None else torch.cuda.current_stream()
     return s.cuda_stream
+
+
+def route_topk(logits: torch.Tensor, top_k: int, stream=None):
+    """Router softmax + top-k on the GPU (``w4a16_moe_route_topk``).
+
+    logits: [T, G] FP32 CUDA tensor.  Returns (topk_ids int32 [T, k],
+    topk_weights fp32 [T, k]): global expert indices by descending probability
+    (ties to the lower index) and their softmax probabilities."""
+    if logits.dtype != torch.float32 or not logits.is_cuda or logits.dim() != 2:
+        raise ValueError("logits must be a 2-D float32 CUDA tensor")
+    T, G = logits.shape
+    ids = torch.empty(T, top_k, dtype=torch.int32, device=logits.device)
+    w = torch.empty(T, top_k, dtype=torch.float32, device=logits.device)
+    w4a16_moe_route_topk(_ptr(logits), T, G, top_k, _ptr(ids), _ptr(w), _stream(stream))
+    return ids, w
 
 
 class W4A16MoE:

@@ -32,6 +32,7 @@ EXPORTED = (
     "w4a16_moe_set_stage_events",
     "w4a16_moe_forward_static_workspace",
     "w4a16_moe_last_error",
+    "w4a16_moe_route_topk",
 )
 
 
@@ -99,6 +100,8 @@ def load(path: str = LIB_PATH):
     L.w4a16_moe_set_stage_events.restype = st
     L.w4a16_moe_forward_static_workspace.argtypes = [P, i32, P, P, P, P, P, P, P, i32, P, P]
     L.w4a16_moe_forward_static_workspace.restype = st
+    L.w4a16_moe_route_topk.argtypes = [P, i32, i32, i32, P, P, P]
+    L.w4a16_moe_route_topk.restype = ctypes.c_int
     L.w4a16_moe_last_error.argtypes = []
     L.w4a16_moe_last_error.restype = ctypes.c_char_p
     _lib = L
@@ -158,6 +161,11 @@ def w4a16_moe_set_gemm_path(plan, path: int) -> int:
 
 def w4a16_moe_check_device_error(plan, workspace_ptr: int, stream: int):
     check(load().w4a16_moe_check_device_error(plan, workspace_ptr, stream))
+
+
+def w4a16_moe_route_topk(logits_ptr: int, num_tokens: int, num_global: int, top_k: int, ids_ptr: int,
+                         weights_ptr: int, stream: int):
+    check(load().w4a16_moe_route_topk(logits_ptr, num_tokens, num_global, top_k, ids_ptr, weights_ptr, stream))
 
 
 def w4a16_moe_set_stage_events(plan, event_handles):

@@ -19,6 +19,7 @@
 #include <string>
 
 #include "common.cuh"
+#include "router.cuh"
 #include "w4a16_moe.h"
 
 using namespace w4a16;
@@ -691,6 +692,34 @@ w4a16_status w4a16_moe_check_device_error(w4a16_moe_plan_t plan, void* workspace
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     return fail(W4A16_ERR_DEVICE_TIMEOUT, "a bounded wait inside a kernel timed out (flag %d)", flag);
   }
+  return W4A16_OK;
+}
+
+w4a16_status w4a16_moe_route_topk(const float* logits, int32_t num_tokens, int32_t num_global, int32_t top_k,
+                                  int32_t* topk_ids, float* topk_weights, void* stream) {
+  if (num_tokens < 0) return fail(W4A16_ERR_INVALID_ARG, "num_tokens must be >= 0, got %d", num_tokens);
+  if (num_global < 1 || num_global > 1024)
+    return fail(W4A16_ERR_UNSUPPORTED, "num_global must be in [1, 1024], got %d", num_global);
+  if (top_k < 1 || top_k > 16 || top_k > num_global)
+    return fail(W4A16_ERR_UNSUPPORTED, "top_k must be in [1, min(16, num_global)], got %d", top_k);
+  if (num_tokens == 0) return W4A16_OK;
+  w4a16_status st;
+  if ((st = check_ptr(logits, 4, "logits")) != W4A16_OK) return st;
+  if ((st = check_ptr(topk_ids, 4, "topk_ids")) != W4A16_OK) return st;
+  if ((st = check_ptr(topk_weights, 4, "topk_weights")) != W4A16_OK) return st;
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return cuda_fail(e, "device query");
+  w4a16::RouterParams rp;
+  rp.logits = logits;
+  rp.T = num_tokens;
+  rp.G = num_global;
+  rp.k = top_k;
+  rp.ids = topk_ids;
+  rp.weights = topk_weights;
+  e = w4a16::launch_router(rp, sms, static_cast<cudaStream_t>(stream), env_flag("W4A16_MOE_PDL", true));
+  if (e != cudaSuccess) return cuda_fail(e, "router launch");
   return W4A16_OK;
 }
 

@@ -232,14 +232,8 @@ def make_activations(cfg: MoEConfig, tokens: int, device="cpu", seed: Optional[i
     return x.to(cfg.torch_act_dtype())
 
 
-def make_routes(cfg: MoEConfig, tokens: int, device="cpu", seed: Optional[int] = None):
-    """Router logits -> softmax -> top-k over the global experts.
-
-    Returns (topk_ids int32 [T, k], topk_weights fp32 [T, k]).  Weights are the
-    softmax probabilities (renormalize=False in every workload).  Global ids
-    outside [expert_offset, expert_offset + E) stay as they are (the forward
-    treats them as masked); ``forced_invalid`` routes become -1.
-    """
+def make_logits(cfg: MoEConfig, tokens: int, device="cpu", seed: Optional[int] = None):
+    """Router logits [T, n_global] FP32 of the workload (the draws make_routes uses)."""
     seed = cfg.seed if seed is None else seed
     g = _gen(seed, 4 + 31 * tokens, device)
     ng = cfg.n_global
@@ -250,6 +244,18 @@ def make_routes(cfg: MoEConfig, tokens: int, device="cpu", seed: Optional[int] =
     if cfg.hot_experts:
         idx = torch.tensor(cfg.hot_experts, device=device)
         logits[:, idx] += cfg.hot_bias
+    return logits.float().contiguous()
+
+
+def make_routes(cfg: MoEConfig, tokens: int, device="cpu", seed: Optional[int] = None):
+    """Router logits -> softmax -> top-k over the global experts.
+
+    Returns (topk_ids int32 [T, k], topk_weights fp32 [T, k]).  Weights are the
+    softmax probabilities (renormalize=False in every workload).  Global ids
+    outside [expert_offset, expert_offset + E) stay as they are (the forward
+    treats them as masked); ``forced_invalid`` routes become -1.
+    """
+    logits = make_logits(cfg, tokens, device, seed)
     probs = torch.softmax(logits.float(), dim=-1)
     w, ids = torch.topk(probs, cfg.top_k, dim=-1)
     ids = ids.to(torch.int32)
