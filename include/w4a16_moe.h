@@ -16,8 +16,9 @@
  *     scales; invalid routes and masked expert counts; split-K for small
  *     batches and route-count-based tile selection.
  *   - "perf: reduce split W4A16 routing and output overhead" (FlashInfer PR
- *     5186), section Description: expert outputs are stored, then combined in
- *     FP32 in fixed top-k order before one output cast, without atomics.
+ *     5186), section Description: expert outputs are stored in the 16-bit
+ *     activation dtype, then combined in FP32 in fixed top-k order before one
+ *     output cast, without atomics.
  *   - "[None][feat] Add W4A16 per-channel weight-only support for Cutlass
  *     fused MoE" (TensorRT-LLM PR 18313), sections Checkpoint format
  *     (per-output-channel scale = absmax/7, two INT4 per byte along the
