@@ -56,6 +56,8 @@ def lib():
             L.oracle_num_threads.restype = ctypes.c_int
             L.oracle_route_topk.argtypes = [P, i32, i32, i32, P, P]
             L.oracle_route_topk.restype = ctypes.c_int
+            L.oracle_masked_routes.argtypes = [P, i32, i32, i32, P, P]
+            L.oracle_masked_routes.restype = ctypes.c_int
             _lib = L
     return _lib
 
@@ -165,6 +167,29 @@ def route_topk(logits, top_k: int):
     if rc != 0:
         raise RuntimeError(f"oracle_route_topk failed: {rc}")
     return ids, w
+
+
+def masked_routes(counts, max_rows: int, expert_offset: int = 0):
+    """Routes of the masked-count layout: (ids int32 [E * max_rows, 1],
+    weights float32 [E * max_rows, 1]); see w4a16_oracle.cpp."""
+    c = np.ascontiguousarray(_np(counts, np.int32))
+    E = c.shape[0]
+    ids = np.zeros((E * max_rows, 1), np.int32)
+    w = np.zeros((E * max_rows, 1), np.float32)
+    rc = lib().oracle_masked_routes(_ptr(c), E, max_rows, expert_offset, _ptr(ids), _ptr(w))
+    if rc != 0:
+        raise RuntimeError(f"oracle_masked_routes failed: {rc}")
+    return ids, w
+
+
+def masked_forward(cfg, x, weights, counts, max_rows: int, nthreads: int = 0):
+    """Expert MLPs on the masked-count layout.  x [E * max_rows, H] (16-bit
+    bits or tensor); cfg must have top_k == 1.  Returns (acc fp32 [E*max_rows, H],
+    out bits): the forward over masked_routes()."""
+    if cfg.top_k != 1:
+        raise ValueError("the masked-count layout routes every row once: top_k must be 1")
+    ids, w = masked_routes(counts, max_rows, cfg.expert_offset)
+    return moe_forward(cfg, x, weights, torch.from_numpy(w), torch.from_numpy(ids), nthreads=nthreads)
 
 
 def moe_forward(cfg, x, weights, topk_weights, ids, renormalize: bool = False,

@@ -257,6 +257,32 @@ int oracle_route_topk(const float* logits, int32_t num_tokens, int32_t num_globa
   return 0;
 }
 
+// Masked-count layout ("feat(pytorch): add CuTeDSL W4A16 MoE backend"
+// (LMDeploy), section Modification: invalid routes and masked expert counts,
+// the layout a low-latency expert-parallel dispatch hands over): the
+// activations of local expert e sit in rows [e * max_rows, e * max_rows +
+// counts[e]) of an [E * max_rows, H] buffer and the rest is ignored.  As routes:
+// row r = e * max_rows + i is one token with a single route, to global expert
+// expert_offset + e with weight 1.0, when i < counts[e] (counts clamped to
+// [0, max_rows]), else an invalid route (-1).  The forward over these routes
+// (top_k = 1) gives every valid row its expert's MLP output and zero rows
+// elsewhere.
+int oracle_masked_routes(const int32_t* counts, int32_t E, int32_t max_rows, int32_t expert_offset,
+                         int32_t* ids, float* weights) {
+  if (E < 1 || max_rows < 0) return 1;
+  for (int32_t e = 0; e < E; ++e) {
+    int32_t c = counts[e];
+    if (c < 0) c = 0;
+    if (c > max_rows) c = max_rows;
+    for (int32_t i = 0; i < max_rows; ++i) {
+      const int64_t r = static_cast<int64_t>(e) * max_rows + i;
+      ids[r] = i < c ? expert_offset + e : -1;
+      weights[r] = 1.0f;
+    }
+  }
+  return 0;
+}
+
 // The MoE forward for a subset of tokens (rows == nullptr: all tokens).
 // x [T, H] (bf16 or fp16 bits), topk_weights/ids [T, k].
 // acc_out [nrows, H] FP32 combine result before the cast; out [nrows, H] bits.

@@ -404,3 +404,42 @@ def test_tiny_workload_has_the_two_forced_invalid_routes(tiny_case):
     cfg, c = tiny_case
     assert int(c["ids"][0, 1]) == -1 and int(c["ids"][5, 0]) == -1
     assert int((c["ids"] == -1).sum()) == 2
+
+
+# ---------------------------------------------------------------------------
+# masked-count layout (expert-major rows + counts): routes and forward
+# ---------------------------------------------------------------------------
+
+def test_masked_routes_structure():
+    """Per expert: a prefix of clamp(counts[e], 0, max_rows) valid rows routed to
+    the expert's global id, the rest invalid; every weight 1."""
+    counts = np.array([0, 3, 7, 5, -2, 9], np.int32)
+    M, off = 5, 40
+    ids, w = oracle.masked_routes(counts, M, off)
+    assert ids.shape == (len(counts) * M, 1)
+    assert (w == 1.0).all()
+    for e, c in enumerate(counts):
+        rows = ids[e * M:(e + 1) * M, 0]
+        n = min(max(int(c), 0), M)
+        assert (rows[:n] == off + e).all() and (rows[n:] == -1).all()
+
+
+@pytest.mark.parametrize("case", CASES[:3])
+def test_masked_forward_equals_dense_expert_mlp(case):
+    """Every valid row equals its expert's MLP from an independently written
+    float64 evaluation; rows past an expert's count are exact zeros."""
+    cfg = small_cfg(**case, E=3, k=1)
+    w = gen.make_weights(cfg)
+    M = 4
+    counts = np.array([2, 0, 4], np.int32)
+    x = gen.make_activations(cfg, cfg.num_experts * M)
+    acc, _ = oracle.masked_forward(cfg, x, w, counts, M)
+    W = np_weights(cfg, w)
+    for e in range(cfg.num_experts):
+        for i in range(M):
+            r = e * M + i
+            if i < counts[e]:
+                want = np_expert_mlp(cfg, W, np_act_in(cfg, x[r]), e)
+                np.testing.assert_allclose(acc[r], want, rtol=2e-6, atol=1e-7 * np.abs(want).max())
+            else:
+                assert (acc[r] == 0.0).all()
