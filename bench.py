@@ -296,6 +296,48 @@ def time_router(cfg, T, flush, stream, steps, hbm):
             "what": "router softmax + top-k of the same tokens (outside the forward's timed region)"}
 
 
+def time_masked(cfg, ids, w, flush, stream, steps, hbm):
+    """The masked-count entry point on the rows a dispatch of the same routes
+    would deliver: counts[e] = routes to local expert e, rows padded to
+    max_rows = max count rounded up to 16.  Same kernels as the forward (each
+    row one route of weight 1); algorithmic bytes = touched experts' weights
+    and scales + the valid rows in and out."""
+    from weight_only_int4_histogram_gb300 import W4A16MoE
+    loc = ids.long() - cfg.expert_offset
+    valid = (ids >= 0) & (loc >= 0) & (loc < cfg.num_experts)
+    counts = torch.bincount(loc[valid], minlength=cfg.num_experts).to(torch.int32)
+    M = int((int(counts.max()) + 15) // 16 * 16)
+    E = cfg.num_experts
+    mcfg = cfg.with_(top_k=1)
+    moe = W4A16MoE.from_config(mcfg, max_tokens=E * M)
+    x = gen.make_activations(mcfg, E * M, "cuda").view(E, M, cfg.hidden)
+    cnt = counts.cuda()
+    y = torch.empty_like(x)
+    for _ in range(3):
+        moe.forward_masked(x, w, cnt, out=y, stream=stream)
+    times = []
+    for _ in range(steps):
+        with torch.cuda.stream(stream):
+            flush.zero_()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        moe.forward_masked(x, w, cnt, out=y, stream=stream)
+        b.record(stream)
+        torch.cuda.synchronize()
+        times.append(a.elapsed_time(b) * 1000.0)
+    moe.check_device_error()
+    us = statistics.median(times)
+    b1, b2, _ = stage_bytes(cfg, ids)
+    rows = int(counts.sum())
+    nbytes = b1 - ids.shape[0] * cfg.hidden * 2 + b2 + 2 * rows * cfg.hidden * 2
+    gbs = nbytes / (us * 1e-6) / 1e9
+    moe.close()
+    return {"us": round(us, 3), "gbs": round(gbs, 1), "frac": round(gbs / hbm, 4), "alg_bytes": nbytes,
+            "rows": rows, "max_rows": M,
+            "what": "masked-count layout entry (per-expert rows of the same routes; eager launches, L2 flushed)"}
+
+
 def stage_bytes(cfg, ids):
     """Algorithmic bytes per launch of each kernel: the touched experts'
     packed weights + scales, the activations it must read, the output."""
@@ -375,6 +417,7 @@ def run_gpu(args):
             "alg_bytes_per_launch": b[k], "launch_us": round(st[k], 3),
             "stage_us": {n: round(v, 3) for n, v in zip(names, st)}}
     router = time_router(cfg, args.tokens, flush, stream, max(args.steps, 5), hbm)
+    masked = time_masked(cfg, ids, w, flush, stream, max(args.steps, 5), hbm)
 
     sweep = []
     if not args.no_sweep:
@@ -439,6 +482,7 @@ def run_gpu(args):
         # route prep, (slot-order copy on the tensor-core path,) two GEMMs, combine
         "gpu_launches": (5 if head["gemm_path"] == "tensor_cores" else 4) * args.steps,
         "router": router,
+        "masked_layout": masked,
         "clocks": clocks,
     }
     if not args.no_cpu_baseline and rank == 0 and world == 1:

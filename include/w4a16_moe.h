@@ -241,6 +241,27 @@ w4a16_status w4a16_moe_set_overrides(w4a16_moe_plan_t plan, int32_t tile_rows,
 w4a16_status w4a16_moe_set_gemm_path(w4a16_moe_plan_t plan, int32_t path, size_t* workspace_bytes);
 
 /*
+ * w4a16_moe_forward_masked -- the expert MLPs on the masked-count layout that a
+ * low-latency expert-parallel dispatch hands over ("feat(pytorch): add CuTeDSL
+ * W4A16 MoE backend" (LMDeploy), section Modification: invalid routes and
+ * masked expert counts): x [num_experts, max_rows, H] act_dtype with counts[e]
+ * valid rows for local expert e (rows past the count are ignored); y, same
+ * shape, receives y[e][i] = W2[e] . act(W13[e] . x[e][i]) for i < counts[e]
+ * and +0 rows elsewhere; the combine over top-k happens after the return
+ * dispatch, outside this call.  Counts are clamped to [0, max_rows].  Every
+ * row is one token with a single route of weight 1, so the plan must have
+ * top_k == 1 and max_tokens >= num_experts * max_rows; prepare_routes and
+ * forward run on that plan's workspace (the expanded routes live in its
+ * staging area).  counts: device int32 [num_experts]; other arguments as for
+ * w4a16_moe_forward.  max_rows == 0 is a no-op.  Errors: W4A16_ERR_UNSUPPORTED
+ * (plan top_k != 1), W4A16_ERR_INVALID_ARG (negative max_rows, too many rows,
+ * NULL/misaligned pointers), and those of prepare_routes / forward.
+ */
+w4a16_status w4a16_moe_forward_masked(w4a16_moe_plan_t plan, int32_t max_rows, const int32_t* counts,
+                                      const void* x, const uint8_t* w13, const uint16_t* s13, const uint8_t* w2,
+                                      const uint16_t* s2, void* y, void* workspace, void* stream);
+
+/*
  * w4a16_moe_route_topk -- the router step before prepare_routes: softmax over
  * each token's router logits, then its top_k experts.  "feat(pytorch): add
  * CuTeDSL W4A16 MoE backend" (LMDeploy), section Benchmark, takes the routes

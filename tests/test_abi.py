@@ -108,6 +108,26 @@ def test_route_topk_rejects_bad_arguments_without_launching(lib):
     _lib.w4a16_moe_route_topk(0, 0, 8, 2, 0, 0, 0)
 
 
+def test_forward_masked_validates_plan_and_sizes(lib):
+    fake = 0x10000  # never dereferenced: validation fails first
+    plan8, _ = _lib.w4a16_moe_plan(good_desc())  # top_k 2
+    with pytest.raises(_lib.W4A16Error) as ei:
+        _lib.w4a16_moe_forward_masked(plan8, 4, fake, fake, fake, fake, fake, fake, fake, fake, 0)
+    assert ei.value.status == 2 and "top_k" in str(ei.value)
+    _lib.w4a16_moe_plan_destroy(plan8)
+    plan1, _ = _lib.w4a16_moe_plan(good_desc(top_k=1, max_tokens=64))
+    E = good_desc().num_experts
+    with pytest.raises(_lib.W4A16Error) as ei:  # more rows than max_tokens
+        _lib.w4a16_moe_forward_masked(plan1, 64 // E + 1, fake, fake, fake, fake, fake, fake, fake, fake, 0)
+    assert ei.value.status == 1
+    with pytest.raises(_lib.W4A16Error):  # negative max_rows
+        _lib.w4a16_moe_forward_masked(plan1, -1, fake, fake, fake, fake, fake, fake, fake, fake, 0)
+    with pytest.raises(_lib.W4A16Error):  # null counts
+        _lib.w4a16_moe_forward_masked(plan1, 2, 0, fake, fake, fake, fake, fake, fake, fake, 0)
+    _lib.w4a16_moe_forward_masked(plan1, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0)  # no rows: no-op
+    _lib.w4a16_moe_plan_destroy(plan1)
+
+
 def test_overrides_validate_and_resize_workspace(lib):
     plan, ws = _lib.w4a16_moe_plan(good_desc())
     with pytest.raises(_lib.W4A16Error):

@@ -15,7 +15,8 @@ from . import _lib
 from ._lib import (Desc, RouteInfo, W4A16Error, w4a16_moe_check_device_error,  # noqa: F401
                    w4a16_moe_forward, w4a16_moe_forward_host, w4a16_moe_plan,
                    w4a16_moe_plan_destroy, w4a16_moe_prepare_routes, w4a16_moe_route_info,
-                   w4a16_moe_route_topk, w4a16_moe_set_gemm_path, w4a16_moe_set_overrides)
+                   w4a16_moe_route_topk, w4a16_moe_set_gemm_path, w4a16_moe_set_overrides,
+                   w4a16_moe_forward_masked)
 from ._lib import PATH_AUTO, PATH_CUDA_CORES, PATH_TENSOR_CORES  # noqa: F401
 
 ACT_SWIGLU, ACT_RELU2 = 0, 1
@@ -112,6 +113,19 @@ class W4A16MoE:
         w4a16_moe_forward(self.plan, T, _ptr(x), _ptr(weights.w13), _ptr(weights.s13),
                           _ptr(weights.w2), _ptr(weights.s2), _ptr(topk_weights), _ptr(topk_ids),
                           renormalize, _ptr(out), _ptr(self.workspace), _stream(stream))
+        return out
+
+    def forward_masked(self, x, weights, counts, out=None, stream=None):
+        """Expert MLPs on the masked-count layout (``w4a16_moe_forward_masked``):
+        x [E, max_rows, H], counts int32 [E] on the device; needs a plan built
+        with top_k == 1 and max_tokens >= E * max_rows."""
+        if x.dim() != 3 or x.shape[0] != self.desc.num_experts:
+            raise ValueError("x must be [num_experts, max_rows, hidden]")
+        if out is None:
+            out = torch.empty_like(x)
+        w4a16_moe_forward_masked(self.plan, x.shape[1], _ptr(counts), _ptr(x), _ptr(weights.w13),
+                                 _ptr(weights.s13), _ptr(weights.w2), _ptr(weights.s2), _ptr(out),
+                                 _ptr(self.workspace), _stream(stream))
         return out
 
     def __call__(self, x, weights, topk_weights, topk_ids, renormalize=False, out=None, stream=None):

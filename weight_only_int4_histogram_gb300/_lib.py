@@ -33,6 +33,7 @@ EXPORTED = (
     "w4a16_moe_forward_static_workspace",
     "w4a16_moe_last_error",
     "w4a16_moe_route_topk",
+    "w4a16_moe_forward_masked",
 )
 
 
@@ -101,6 +102,8 @@ def load(path: str = LIB_PATH):
     L.w4a16_moe_forward_static_workspace.argtypes = [P, i32, P, P, P, P, P, P, P, i32, P, P]
     L.w4a16_moe_forward_static_workspace.restype = st
     L.w4a16_moe_route_topk.argtypes = [P, i32, i32, i32, P, P, P]
+    L.w4a16_moe_forward_masked.argtypes = [P, i32, P, P, P, P, P, P, P, P, P]
+    L.w4a16_moe_forward_masked.restype = ctypes.c_int
     L.w4a16_moe_route_topk.restype = ctypes.c_int
     L.w4a16_moe_last_error.argtypes = []
     L.w4a16_moe_last_error.restype = ctypes.c_char_p
@@ -161,6 +164,12 @@ def w4a16_moe_set_gemm_path(plan, path: int) -> int:
 
 def w4a16_moe_check_device_error(plan, workspace_ptr: int, stream: int):
     check(load().w4a16_moe_check_device_error(plan, workspace_ptr, stream))
+
+
+def w4a16_moe_forward_masked(plan, max_rows: int, counts_ptr: int, x_ptr: int, w13: int, s13: int, w2: int,
+                             s2: int, y_ptr: int, workspace_ptr: int, stream: int):
+    check(load().w4a16_moe_forward_masked(plan, max_rows, counts_ptr, x_ptr, w13, s13, w2, s2, y_ptr,
+                                          workspace_ptr, stream))
 
 
 def w4a16_moe_route_topk(logits_ptr: int, num_tokens: int, num_global: int, top_k: int, ids_ptr: int,

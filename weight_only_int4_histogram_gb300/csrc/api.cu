@@ -19,6 +19,7 @@
 #include <string>
 
 #include "common.cuh"
+#include "masked.cuh"
 #include "router.cuh"
 #include "w4a16_moe.h"
 
@@ -693,6 +694,35 @@ w4a16_status w4a16_moe_check_device_error(w4a16_moe_plan_t plan, void* workspace
     return fail(W4A16_ERR_DEVICE_TIMEOUT, "a bounded wait inside a kernel timed out (flag %d)", flag);
   }
   return W4A16_OK;
+}
+
+w4a16_status w4a16_moe_forward_masked(w4a16_moe_plan_t plan, int32_t max_rows, const int32_t* counts,
+                                      const void* x, const uint8_t* w13, const uint16_t* s13, const uint8_t* w2,
+                                      const uint16_t* s2, void* y, void* workspace, void* stream) {
+  if (!plan) return fail(W4A16_ERR_INVALID_ARG, "plan is NULL");
+  if (plan->d.top_k != 1)
+    return fail(W4A16_ERR_UNSUPPORTED, "the masked-count layout routes every row once: the plan needs top_k == 1, got %d",
+                plan->d.top_k);
+  if (max_rows < 0) return fail(W4A16_ERR_INVALID_ARG, "max_rows must be >= 0, got %d", max_rows);
+  const int64_t rows = static_cast<int64_t>(plan->d.num_experts) * max_rows;
+  if (rows > plan->d.max_tokens)
+    return fail(W4A16_ERR_INVALID_ARG, "num_experts * max_rows = %lld exceeds the plan's max_tokens %d",
+                static_cast<long long>(rows), plan->d.max_tokens);
+  if (rows == 0) return W4A16_OK;
+  w4a16_status st;
+  if ((st = check_ptr(counts, 4, "counts")) != W4A16_OK) return st;
+  if ((st = check_ptr(workspace, 256, "workspace")) != W4A16_OK) return st;
+  const int32_t T = static_cast<int32_t>(rows);
+  const Layout L = make_layout(*plan, T);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  int32_t* ids = reinterpret_cast<int32_t*>(ws + L.off_sids);
+  float* wts = reinterpret_cast<float*>(ws + L.off_sw);
+  cudaError_t e = launch_masked_routes(counts, plan->d.num_experts, max_rows, plan->d.expert_offset, ids, wts,
+                                       plan->num_sms, static_cast<cudaStream_t>(stream), plan->pdl);
+  if (e != cudaSuccess) return cuda_fail(e, "masked-route launch");
+  st = w4a16_moe_prepare_routes(plan, T, ids, workspace, stream);
+  if (st != W4A16_OK) return st;
+  return w4a16_moe_forward(plan, T, x, w13, s13, w2, s2, wts, ids, 0, y, workspace, stream);
 }
 
 w4a16_status w4a16_moe_route_topk(const float* logits, int32_t num_tokens, int32_t num_global, int32_t top_k,

@@ -22,7 +22,10 @@
 // Padding slots get perm = -1 and the tile list (expert, first slot, valid
 // rows) is written per expert, several threads per expert when E is small.  Integer work only: results are bit-exact and
 // independent of scheduling.
+#include <algorithm>
+
 #include "common.cuh"
+#include "masked.cuh"
 
 namespace w4a16 {
 
@@ -233,6 +236,43 @@ cudaError_t launch_permute(const PermuteParams& p, int grid, cudaStream_t s, boo
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, permute_rows_kernel, p);
+}
+
+// Masked-count layout ("feat(pytorch): add CuTeDSL W4A16 MoE backend"
+// (LMDeploy), section Modification: invalid routes and masked expert counts):
+// expert-major rows with a count per expert become single routes of weight 1
+// (rows past an expert's count: invalid), which route preparation and the
+// forward then treat like any other routes.
+__global__ void __launch_bounds__(256) masked_routes_kernel(const int32_t* counts, int32_t E, int32_t max_rows,
+                                                            int32_t expert_offset, int32_t* ids, float* weights) {
+  pdl_wait();
+  pdl_launch_dependents();
+  const int64_t n = static_cast<int64_t>(E) * max_rows;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t r = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; r < n; r += stride) {
+    const int32_t e = static_cast<int32_t>(r / max_rows);
+    const int32_t i = static_cast<int32_t>(r - static_cast<int64_t>(e) * max_rows);
+    const int32_t c = min(max(counts[e], 0), max_rows);
+    ids[r] = i < c ? expert_offset + e : -1;
+    weights[r] = 1.0f;
+  }
+}
+
+cudaError_t launch_masked_routes(const int32_t* counts, int32_t E, int32_t max_rows, int32_t expert_offset,
+                                 int32_t* ids, float* weights, int num_sms, cudaStream_t s, bool pdl) {
+  const int64_t n = static_cast<int64_t>(E) * max_rows;
+  const int64_t blocks = (n + 255) / 256;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(std::max<int64_t>(1, std::min<int64_t>(blocks, 8 * num_sms))));
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, masked_routes_kernel, counts, E, max_rows, expert_offset, ids, weights);
 }
 
 cudaError_t launch_route_prep(const RoutePrepParams& p, int smem_bytes, cudaStream_t s, bool pdl) {
