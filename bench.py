@@ -353,6 +353,16 @@ def stage_bytes(cfg, ids):
     return b1, b2, b3
 
 
+def max_over_ranks(values, dist, device):
+    """Element-wise maximum of per-rank times: the job takes as long as its
+    slowest rank (replicas run the same work on every GPU)."""
+    if dist is None:
+        return [float(v) for v in values]
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
 def run_gpu(args):
     from weight_only_int4_histogram_gb300 import W4A16MoE, build
     build.build()
@@ -451,11 +461,7 @@ def run_gpu(args):
     h2d = xh.numel() * 2 + idh.numel() * 4 + twh.numel() * 4
     d2h = oh.numel() * 2
 
-    med = head["us"]
-    if dist is not None:
-        tmax = torch.tensor([med, e2e_med], device=dev)
-        dist.all_reduce(tmax, op=dist.ReduceOp.MAX)
-        med, e2e_med = float(tmax[0]), float(tmax[1])
+    med, e2e_med = max_over_ranks([head["us"], e2e_med], dist, dev)
     line = {
         "metric": "W4A16 MoE forward latency (us), Kimi TP8 shard shape",
         "value": round(med, 3),
