@@ -247,6 +247,24 @@ def time_graph(g, flush, stream, steps, warmup):
     return times
 
 
+def time_warm(g, stream, samples=3, reps=10):
+    """The pages' protocol, for comparison with their figures: warm CUDA-graph
+    replays (no L2 flush), each sample the mean of `reps` back-to-back
+    replays, the median of `samples` samples."""
+    out = []
+    with torch.cuda.stream(stream):
+        for _ in range(samples):
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for _ in range(reps):
+                g.replay()
+            b.record(stream)
+            torch.cuda.synchronize()
+            out.append(a.elapsed_time(b) * 1000.0 / reps)
+    return statistics.median(out)
+
+
 def time_stages(moe, w, x, ids, tw, out, flush, stream, steps):
     """Per-kernel device time of the GEMMs and combine (eager launches, events
     recorded by the library between kernels, L2 flushed before each step)."""
@@ -414,6 +432,7 @@ def run_gpu(args):
         return res, (x, ids, tw, out, g), times, clocks
 
     head, (x, ids, tw, out, g), times, clocks = measure(args.tokens, args.steps, args.warmup, True)
+    warm = time_warm(g, stream)
     # the dominant kernel's live timing and roofline
     st = time_stages(moe, w, x, ids, tw, out, flush, stream, max(args.steps, 5))
     b = stage_bytes(cfg, ids)
@@ -461,7 +480,7 @@ def run_gpu(args):
     h2d = xh.numel() * 2 + idh.numel() * 4 + twh.numel() * 4
     d2h = oh.numel() * 2
 
-    med, e2e_med = max_over_ranks([head["us"], e2e_med], dist, dev)
+    med, e2e_med, warm = max_over_ranks([head["us"], e2e_med, warm], dist, dev)
     line = {
         "metric": "W4A16 MoE forward latency (us), Kimi TP8 shard shape",
         "value": round(med, 3),
@@ -487,6 +506,8 @@ def run_gpu(args):
                 "d2h_bytes_per_step": d2h},
         # route prep, (slot-order copy on the tensor-core path,) two GEMMs, combine
         "gpu_launches": (5 if head["gemm_path"] == "tensor_cores" else 4) * args.steps,
+        "warm_replay": {"us": round(warm, 3),
+                        "protocol": "the pages' timing: warm CUDA-graph replays, mean of 10, median of 3 samples"},
         "router": router,
         "masked_layout": masked,
         "clocks": clocks,
