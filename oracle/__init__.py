@@ -58,6 +58,8 @@ def lib():
             L.oracle_route_topk.restype = ctypes.c_int
             L.oracle_masked_routes.argtypes = [P, i32, i32, i32, P, P]
             L.oracle_masked_routes.restype = ctypes.c_int
+            L.oracle_relayout_interleaved.argtypes = [P, i32, i64, i64, i64, P]
+            L.oracle_relayout_interleaved.restype = ctypes.c_int
             _lib = L
     return _lib
 
@@ -154,6 +156,17 @@ def prepare_routes(cfg, ids, bm: int):
         raise RuntimeError(f"oracle_prepare_routes failed: {rc}")
     return dict(counts=counts, offs=offs, perm=perm[: offs[E]].copy(), inv=inv[:R].copy(),
                 tiles=tiles[: nt[0]].copy(), num_tiles=int(nt[0]))
+
+
+def relayout_interleaved(packed, scale_kind: int, E: int, N: int, K: int) -> np.ndarray:
+    """The interleaved packed-weight layout of ``w4a16_moe_relayout_weights``
+    (see w4a16_oracle.cpp): uint8 [E, N, K/2] from the checkpoint layout."""
+    p = _np(packed, np.uint8)
+    out = np.empty((E, N, K // 2), np.uint8)
+    rc = lib().oracle_relayout_interleaved(_ptr(p), int(scale_kind), E, N, K, _ptr(out))
+    if rc != 0:
+        raise RuntimeError(f"oracle_relayout_interleaved failed: {rc}")
+    return out
 
 
 def route_topk(logits, top_k: int):

@@ -390,6 +390,44 @@ int oracle_moe_forward(const int32_t* desc_in, int32_t num_tokens, const uint16_
   return 0;
 }
 
+// Interleaved relayout of packed weights: the layout w4a16_moe_relayout_weights
+// documents in include/w4a16_moe.h (the library's own, not the pages'; the
+// pages only say the packed INT4 weights are reordered once at setup:
+// "feat(pytorch): add CuTeDSL W4A16 MoE backend" (LMDeploy), Motivation, and
+// "[None][feat] Add W4A16 per-channel weight-only support for Cutlass fused
+// MoE" (TensorRT-LLM), Changes).  Written out code by code from that
+// definition: output rows are packed along K; the code of K index k of row n
+// goes to 32-bit word k / 8 of the row, at nibble position p where
+// {0, 2, 4, 6, 1, 3, 5, 7}[p] = k % 8 (nibble position p = byte p / 2 of the
+// little-endian word, high nibble when p is odd).  Input: the checkpoint
+// layout for scale_kind (0: [E, N, K/2] packed along K; 1: [E, N/2, K] packed
+// along rows).  Returns 0, or -1 when K is not a multiple of 8 or (row-pair
+// input) N is odd.
+int oracle_relayout_interleaved(const uint8_t* packed, int32_t scale_kind, int64_t E, int64_t N, int64_t K,
+                                uint8_t* out) {
+  if (K % 8 != 0 || (scale_kind != 0 && N % 2 != 0)) return -1;
+  std::memset(out, 0, static_cast<size_t>(E * N * (K / 2)));
+  for (int64_t e = 0; e < E; ++e) {
+    for (int64_t n = 0; n < N; ++n) {
+      for (int64_t k = 0; k < K; ++k) {
+        unsigned code;
+        if (scale_kind == 0) {
+          const uint8_t b = packed[(e * N + n) * (K / 2) + k / 2];
+          code = (k % 2 == 0) ? (b & 0xF) : (b >> 4);
+        } else {
+          const uint8_t b = packed[(e * (N / 2) + n / 2) * K + k];
+          code = (n % 2 == 0) ? (b & 0xF) : (b >> 4);
+        }
+        const int64_t j = k % 8;
+        const int64_t pos = (j % 2 == 0) ? j / 2 : 4 + j / 2;
+        uint8_t& dst = out[(e * N + n) * (K / 2) + (k / 8) * 4 + pos / 2];
+        dst = static_cast<uint8_t>(dst | ((pos % 2 == 0) ? code : (code << 4)));
+      }
+    }
+  }
+  return 0;
+}
+
 int oracle_num_threads(void) {
 #ifdef _OPENMP
   return omp_get_max_threads();

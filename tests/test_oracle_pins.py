@@ -124,6 +124,49 @@ def test_generator_packers_match_golden_bytes():
 
 
 # ---------------------------------------------------------------------------
+# Interleaved relayout of the packed weights (the layout the library's
+# w4a16_moe_relayout_weights documents)
+# ---------------------------------------------------------------------------
+
+def read_relayout_golden():
+    cases = []
+    with open(os.path.join(GOLDEN, "interleaved_relayout.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            head, src, dst = (part.split() for part in line.split("|"))
+            kind, n, k = (int(v) for v in head)
+            cases.append((kind, n, k, bytes(int(h, 16) for h in src), bytes(int(h, 16) for h in dst)))
+    return cases
+
+
+def test_relayout_hand_worked_words():
+    cases = read_relayout_golden()
+    assert len(cases) == 4
+    for kind, n, k, src, dst in cases:
+        out = oracle.relayout_interleaved(np.frombuffer(src, np.uint8), kind, 1, n, k)
+        assert out.tobytes() == dst, (kind, n, k, out.tobytes().hex(), dst.hex())
+
+
+def test_relayout_group_and_per_channel_inputs_agree():
+    """The same code matrix packed either way (the generator's two packers,
+    checked against hand-built bytes above) relays out to the same bytes, and
+    each 32-bit word of a row holds the multiset of that word's codes."""
+    rng = np.random.default_rng(3)
+    E, N, K = 3, 6, 48
+    q = torch.from_numpy(rng.integers(-8, 8, size=(E, N, K)).astype(np.int8))
+    along_k = torch.stack([gen.pack_int4_along_k(q[e]) for e in range(E)])
+    along_rows = torch.stack([gen.pack_int4_along_rows(q[e]) for e in range(E)])
+    a = oracle.relayout_interleaved(along_k, 0, E, N, K)
+    b = oracle.relayout_interleaved(along_rows, 1, E, N, K)
+    np.testing.assert_array_equal(a, b)
+    nib = np.stack([a & 0xF, a >> 4], axis=-1).reshape(E, N, K // 8, 8)
+    codes = np.sort(((nib.astype(np.int16) ^ 8) - 8), axis=-1)
+    np.testing.assert_array_equal(codes, np.sort(q.numpy().reshape(E, N, K // 8, 8), axis=-1))
+
+
+# ---------------------------------------------------------------------------
 # O2: quantiser round trip through the oracle's dequantiser
 # ---------------------------------------------------------------------------
 
