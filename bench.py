@@ -314,7 +314,7 @@ def time_router(cfg, T, flush, stream, steps, hbm):
             "what": "router softmax + top-k of the same tokens (outside the forward's timed region)"}
 
 
-def time_masked(cfg, ids, w, flush, stream, steps, hbm):
+def time_masked(cfg, ids, w, flush, stream, steps, hbm, layout=0):
     """The masked-count entry point on the rows a dispatch of the same routes
     would deliver: counts[e] = routes to local expert e, rows padded to
     max_rows = max count rounded up to 16.  Same kernels as the forward (each
@@ -328,6 +328,7 @@ def time_masked(cfg, ids, w, flush, stream, steps, hbm):
     E = cfg.num_experts
     mcfg = cfg.with_(top_k=1)
     moe = W4A16MoE.from_config(mcfg, max_tokens=E * M)
+    moe.set_weight_layout(layout)
     x = gen.make_activations(mcfg, E * M, "cuda").view(E, M, cfg.hidden)
     cnt = counts.cuda()
     y = torch.empty_like(x)
@@ -396,10 +397,13 @@ def run_gpu(args):
     cfg = gen.CONFIGS[args.config]
     hbm, bf16, peak_kind = load_peaks()
 
-    w = gen.make_weights(cfg, dev)
+    w_ckpt = gen.make_weights(cfg, dev)
     moe = W4A16MoE.from_config(cfg, max_tokens=max(max(cfg.tokens), args.tokens, max(args.sweep_tokens)),
                                device=dev)
     moe.set_gemm_path(GEMM_PATHS[args.gemm_path])
+    # setup, outside every timed region: the plan-time relayout of the packed weights
+    w = moe.relayout_weights(w_ckpt) if args.weights == "interleaved" else w_ckpt
+    torch.cuda.synchronize()
     flush = l2_flush_buffer(dev)
     stream = torch.cuda.Stream(device=dev)
 
@@ -446,7 +450,8 @@ def run_gpu(args):
             "alg_bytes_per_launch": b[k], "launch_us": round(st[k], 3),
             "stage_us": {n: round(v, 3) for n, v in zip(names, st)}}
     router = time_router(cfg, args.tokens, flush, stream, max(args.steps, 5), hbm)
-    masked = time_masked(cfg, ids, w, flush, stream, max(args.steps, 5), hbm)
+    masked = time_masked(cfg, ids, w, flush, stream, max(args.steps, 5), hbm,
+                         layout=1 if args.weights == "interleaved" else 0)
 
     sweep = []
     if not args.no_sweep:
@@ -496,6 +501,7 @@ def run_gpu(args):
         "data": "synthetic (seeded; weights N(0,0.02) quantised to INT4 g32, x N(0,1), softmax top-k routes)",
         "config": {"workload": cfg.name, "tokens": args.tokens, "experts": cfg.num_experts,
                    "hidden": cfg.hidden, "inter": cfg.inter, "top_k": cfg.top_k,
+                   "weights": args.weights,
                    "timing": "CUDA-graph replay, median of steps, CUDA events on the launch stream",
                    "l2": "flushed before every timed step (512 MB write)",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
@@ -504,8 +510,8 @@ def run_gpu(args):
         "sweep": sweep,
         "e2e": {"value": round(e2e_med, 3), "unit": "us", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
-        # route prep, (slot-order copy on the tensor-core path,) two GEMMs, combine
-        "gpu_launches": (5 if head["gemm_path"] == "tensor_cores" else 4) * args.steps,
+        # route prep, two GEMMs, combine
+        "gpu_launches": 4 * args.steps,
         "warm_replay": {"us": round(warm, 3),
                         "protocol": "the pages' timing: warm CUDA-graph replays, mean of 10, median of 3 samples"},
         "router": router,
@@ -514,7 +520,7 @@ def run_gpu(args):
     }
     if not args.no_cpu_baseline and rank == 0 and world == 1:
         line["cpu_baseline"] = cpu_baseline(cfg, args.tokens, args.cpu_sample_tokens,
-                                            (w.to("cpu"), x.cpu(), ids.cpu(), tw.cpu()))
+                                            (w_ckpt.to("cpu"), x.cpu(), ids.cpu(), tw.cpu()))
     if rank == 0:
         print(json.dumps(line), flush=True)
     if dist is not None:
@@ -599,6 +605,8 @@ def main():
                     help="comma-separated token counts of the sweep")
     ap.add_argument("--gemm-path", default="auto", choices=list(GEMM_PATHS),
                     help="where the expert GEMMs run (auto: planner's choice per batch)")
+    ap.add_argument("--weights", default="interleaved", choices=["interleaved", "checkpoint"],
+                    help="packed weight layout the forward reads (interleaved: relaid out once at setup)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample-tokens", type=int, default=512)
     ap.add_argument("--ref-sample-tokens", type=int, default=16)

@@ -68,6 +68,11 @@ typedef enum {
 typedef enum { W4A16_ACT_SWIGLU = 0, W4A16_ACT_RELU2 = 1 } w4a16_act;
 typedef enum { W4A16_SCALE_GROUP32_K = 0, W4A16_SCALE_PER_CHANNEL = 1 } w4a16_scale;
 typedef enum { W4A16_DT_BF16 = 0, W4A16_DT_FP16 = 1 } w4a16_dtype;
+/* Packed weight layouts a forward can take (see w4a16_moe_relayout_weights). */
+typedef enum {
+  W4A16_LAYOUT_CHECKPOINT = 0,   /* the layouts documented with w4a16_moe_desc */
+  W4A16_LAYOUT_INTERLEAVED = 1   /* the library's relaid-out layout */
+} w4a16_weight_layout;
 /* Where the two expert GEMMs run (see w4a16_moe_set_gemm_path). */
 typedef enum {
   W4A16_PATH_AUTO = 0,          /* planner's choice per batch size */
@@ -287,9 +292,51 @@ w4a16_status w4a16_moe_route_topk(const float* logits, int32_t num_tokens, int32
                                   int32_t* topk_ids, float* topk_weights, void* stream);
 
 /*
+ * w4a16_moe_relayout_weights -- plan-time relayout of one packed weight tensor
+ * into W4A16_LAYOUT_INTERLEAVED, the order the GEMM kernels dequantise with
+ * shifts and masks alone (no byte permutes).  Passages: "feat(pytorch): add
+ * CuTeDSL W4A16 MoE backend" (LMDeploy), section Motivation (weights stay
+ * packed INT4, no persistent BF16 expansion); "[None][feat] Add W4A16
+ * per-channel weight-only support for Cutlass fused MoE" (TensorRT-LLM),
+ * section Changes (setup-time preprocessing of the packed weights).  A
+ * one-time setup step, outside any timed forward; codes are copied bit for
+ * bit, the byte count does not change.
+ *   which   0: W13 (N = N1 rows, K = hidden), 1: W2 (N = hidden rows, K = inter)
+ *   in      device, the checkpoint layout of w4a16_moe_desc for the plan's
+ *           scale_kind
+ *   out     device, E x N x K/2 bytes: rows packed along K; in every 32-bit
+ *           word (K values 8w .. 8w+7 of a row) the nibble at bit position 4p
+ *           holds the code of K index 8w + {0,2,4,6,1,3,5,7}[p]
+ *           GROUP32_K: out may equal in (in place) or be disjoint;
+ *           PER_CHANNEL (row-pair input): out and in must be disjoint
+ * Scales are not touched.  Later forwards read such weights after
+ * w4a16_moe_set_weight_layout(plan, W4A16_LAYOUT_INTERLEAVED).  Asynchronous
+ * on `stream`.  Errors: W4A16_ERR_INVALID_ARG (NULL / misaligned / overlapping
+ * pointers, which not 0 or 1), W4A16_ERR_CUDA (launch failure).
+ */
+w4a16_status w4a16_moe_relayout_weights(w4a16_moe_plan_t plan, int32_t which, const uint8_t* in, uint8_t* out,
+                                        void* stream);
+
+/*
+ * Declares the layout of the packed weights that later forward calls on this
+ * plan receive (both W13 and W2): W4A16_LAYOUT_CHECKPOINT (the default) or
+ * W4A16_LAYOUT_INTERLEAVED (the output of w4a16_moe_relayout_weights).  Both
+ * layouts give bit-identical results.  Host only; unknown layout:
+ * W4A16_ERR_INVALID_ARG.
+ */
+w4a16_status w4a16_moe_set_weight_layout(w4a16_moe_plan_t plan, int32_t layout);
+
+/*
  * Reads (synchronously, on `stream`) and clears the device error flag in the
  * workspace.  Returns W4A16_ERR_DEVICE_TIMEOUT if a kernel gave up waiting
  * since the last prepare_routes on this workspace (prepare_routes clears it).
+ * workspace == NULL reads the fixed workspace of
+ * w4a16_moe_forward_static_workspace on the current device.
+ * Every bounded wait in the GEMM pipelines gives up after 2 s by default; the
+ * environment variable W4A16_MOE_WAIT_TIMEOUT_NS, read when a plan is created,
+ * sets a different limit in nanoseconds for that plan's forwards (a test hook:
+ * a limit shorter than a normal wait makes the kernels give up, wind down
+ * their copies and MMAs and return, and this call then reports the timeout).
  */
 w4a16_status w4a16_moe_check_device_error(w4a16_moe_plan_t plan, void* workspace, void* stream);
 
@@ -322,6 +369,8 @@ w4a16_status w4a16_moe_set_stage_events(w4a16_moe_plan_t plan, void* const* even
  *   Every call shares the one array and leaves its contents behind (route
  *   preparation clears what must start at zero), so calls that overlap on the
  *   GPU -- on different streams without ordering -- race and must be avoided.
+ *   w4a16_moe_check_device_error(plan, NULL, stream) reads this array's
+ *   timeout flag.
  *   No cudaMalloc, cudaFree or allocating library routine is called.
  * Arguments as for w4a16_moe_forward (device pointers, same layouts).
  */

@@ -16,8 +16,9 @@ from ._lib import (Desc, RouteInfo, W4A16Error, w4a16_moe_check_device_error,  #
                    w4a16_moe_forward, w4a16_moe_forward_host, w4a16_moe_plan,
                    w4a16_moe_plan_destroy, w4a16_moe_prepare_routes, w4a16_moe_route_info,
                    w4a16_moe_route_topk, w4a16_moe_set_gemm_path, w4a16_moe_set_overrides,
-                   w4a16_moe_forward_masked)
+                   w4a16_moe_forward_masked, w4a16_moe_relayout_weights, w4a16_moe_set_weight_layout)
 from ._lib import PATH_AUTO, PATH_CUDA_CORES, PATH_TENSOR_CORES  # noqa: F401
+from ._lib import LAYOUT_CHECKPOINT, LAYOUT_INTERLEAVED  # noqa: F401
 
 ACT_SWIGLU, ACT_RELU2 = 0, 1
 SCALE_GROUP32_K, SCALE_PER_CHANNEL = 0, 1
@@ -98,6 +99,29 @@ class W4A16MoE:
         if need > self.workspace.numel():
             self.workspace = torch.empty(need, dtype=torch.uint8, device=self.device)
         self.workspace_bytes = need
+
+    def set_weight_layout(self, layout=LAYOUT_CHECKPOINT):
+        """Layout of the packed weights later forwards receive."""
+        w4a16_moe_set_weight_layout(self.plan, layout)
+
+    def relayout_weights(self, weights, stream=None, in_place=False):
+        """Plan-time relayout (``w4a16_moe_relayout_weights``) of both packed
+        weight tensors into the interleaved layout, and switch this plan to it.
+        Returns an object with the relaid-out ``w13``/``w2`` and the same
+        scales (group scales: in place when ``in_place``)."""
+        import copy
+        out = copy.copy(weights)
+        group = self.desc.scale_kind == SCALE_GROUP32_K
+        E, H, I = self.desc.num_experts, self.desc.hidden, self.desc.inter
+        N1 = 2 * I if self.desc.act == ACT_SWIGLU else I
+        for which, name, rows, k in ((0, "w13", N1, H), (1, "w2", H, I)):
+            src = getattr(weights, name)
+            dst = src if (in_place and group) else torch.empty(E, rows, k // 2, dtype=torch.uint8,
+                                                              device=src.device)
+            w4a16_moe_relayout_weights(self.plan, which, _ptr(src), _ptr(dst), _stream(stream))
+            setattr(out, name, dst)
+        self.set_weight_layout(LAYOUT_INTERLEAVED)
+        return out
 
     def route_info(self, num_tokens: int) -> RouteInfo:
         return w4a16_moe_route_info(self.plan, num_tokens)

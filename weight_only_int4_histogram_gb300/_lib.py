@@ -15,6 +15,7 @@ LIB_PATH = os.path.join(HERE, "libw4a16_moe.so")
 
 W4A16_OK = 0
 PATH_AUTO, PATH_TENSOR_CORES, PATH_CUDA_CORES = 0, 1, 2
+LAYOUT_CHECKPOINT, LAYOUT_INTERLEAVED = 0, 1
 STATUS_NAMES = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "WORKSPACE_TOO_SMALL",
                 4: "CUDA", 5: "DEVICE_TIMEOUT"}
 
@@ -34,6 +35,8 @@ EXPORTED = (
     "w4a16_moe_last_error",
     "w4a16_moe_route_topk",
     "w4a16_moe_forward_masked",
+    "w4a16_moe_relayout_weights",
+    "w4a16_moe_set_weight_layout",
 )
 
 
@@ -105,6 +108,10 @@ def load(path: str = LIB_PATH):
     L.w4a16_moe_forward_masked.argtypes = [P, i32, P, P, P, P, P, P, P, P, P]
     L.w4a16_moe_forward_masked.restype = ctypes.c_int
     L.w4a16_moe_route_topk.restype = ctypes.c_int
+    L.w4a16_moe_relayout_weights.argtypes = [P, i32, P, P, P]
+    L.w4a16_moe_relayout_weights.restype = st
+    L.w4a16_moe_set_weight_layout.argtypes = [P, i32]
+    L.w4a16_moe_set_weight_layout.restype = st
     L.w4a16_moe_last_error.argtypes = []
     L.w4a16_moe_last_error.restype = ctypes.c_char_p
     _lib = L
@@ -175,6 +182,14 @@ def w4a16_moe_forward_masked(plan, max_rows: int, counts_ptr: int, x_ptr: int, w
 def w4a16_moe_route_topk(logits_ptr: int, num_tokens: int, num_global: int, top_k: int, ids_ptr: int,
                          weights_ptr: int, stream: int):
     check(load().w4a16_moe_route_topk(logits_ptr, num_tokens, num_global, top_k, ids_ptr, weights_ptr, stream))
+
+
+def w4a16_moe_relayout_weights(plan, which: int, in_ptr: int, out_ptr: int, stream: int):
+    check(load().w4a16_moe_relayout_weights(plan, which, in_ptr, out_ptr, stream))
+
+
+def w4a16_moe_set_weight_layout(plan, layout: int):
+    check(load().w4a16_moe_set_weight_layout(plan, layout))
 
 
 def w4a16_moe_set_stage_events(plan, event_handles):

@@ -3,7 +3,7 @@
 // persistent grid sizes, workspace layout), TMA descriptor encoding and the
 // launch sequence
 //   route_prep -> gate/up GEMM -> down GEMM -> combine
-// chained with programmatic dependent launch.  Both GEMMs run either on the
+// chained with programmatic dependent launch; the plan-time weight relayout.  Both GEMMs run either on the
 // tensor cores (gemm.cuh) or, when experts see only a few routes each, on the
 // CUDA cores (gemv.cuh).  No allocation, host sync or
 // device->host copy happens in prepare_routes / forward.
@@ -29,7 +29,10 @@ struct w4a16_moe_plan_s {
   w4a16_moe_desc d;
   int num_sms;
   int ov_bn, ov_s1, ov_s2;
-  int path;  // W4A16_PATH_*
+  int ov_nt1, ov_nt2;  // tuning: weight tiles per tensor-core unit (0 = automatic)
+  int path;    // W4A16_PATH_*
+  int layout;  // W4A16_LAYOUT_* of the weights later forwards receive
+  uint64_t wait_ns;  // limit of the GEMM pipelines' bounded waits
   size_t ws_bytes;
   bool pdl;
   cudaEvent_t ev[4];
@@ -64,12 +67,15 @@ struct Layout {
   int n1;
   int nt1, kb1, s1, kbps1;
   int nt2, kb2, s2, kbps2;
+  int ntu1, ntu2;          // tensor-core path: weight tiles per unit (NT) of each GEMM
+  int acc1, acc2;          // tensor-core path: accumulator sets in TMEM
+  int stage_bytes2;        // tensor-core down GEMM stage
   int stages, stage_bytes, smem;   // gate/up GEMM (and the CUDA-core path's both GEMMs)
   int stages2, smem2;              // tensor-core down GEMM (output staging buffers)
   int grid1, grid2;
   size_t off_err, off_counts, off_offs, off_ntiles, off_tiles, off_perm, off_inv, off_ctr;
-  size_t off_part, off_inter, off_y, off_xs;
-  size_t off_sx, off_sids, off_sw, off_sout;
+  size_t off_part, off_inter, off_y;
+  size_t off_sx, off_sids, off_sw, off_sout;  // host-call staging (w4a16_moe_forward_host / masked)
   size_t total;
 };
 
@@ -106,6 +112,32 @@ int choose_bn_gemv(const w4a16_moe_plan_s& P, int T) {
 }
 
 constexpr int kAutoMaxBN = 64;
+
+// Tensor-core path: weight tiles per unit.  The NT tiles of a unit share each
+// stage's activation tile, so the activation rows cross from L2 into shared
+// memory once per NT tiles instead of once per tile (at 64-route tiles one
+// tile's activation stage is twice its weight stage).  The largest NT in
+// {max_nt, ..., 2, 1} that is still needed for the expert's tile count, leaves
+// room for 2 stages in the ring and 2 A slots in TMEM -- with two accumulator
+// sets when `double_acc` (units of few K blocks, where the epilogue must
+// overlap the next unit's MMAs), else with one if two do not fit.
+void choose_nt(int n_tiles, int bn, int smem_budget, int max_nt, bool double_acc, int& nt, int& acc_bufs) {
+  const int need_acc = double_acc ? 2 : 1;
+  nt = max_nt;
+  while (nt > 1 && (nt / 2 >= n_tiles || smem_budget / gemm_stage_bytes(nt, bn) < 2 ||
+                    gemm_a_slots(nt, bn, need_acc) < 2))
+    nt >>= 1;
+  acc_bufs = gemm_a_slots(nt, bn, 2) >= 2 ? 2 : 1;
+}
+
+// Units of at most this many K blocks keep two accumulator sets.
+constexpr int kDoubleAccMaxKb = 8;
+// Default weight tiles per tensor-core unit.  Measured on the 384-expert
+// H 7168 / I 256 shape at 1024 and 2048 tokens: 2 tiles per unit beat 1 (the
+// activation stage crosses from L2 half as often) and 4 (only two 106 KB
+// stages fit in shared memory, and units four times larger leave more of
+// the last wave idle).
+constexpr int kDefaultNT = 2;
 
 int choose_bn(const w4a16_moe_plan_s& P, int T) {
   if (P.ov_bn) return P.ov_bn;
@@ -163,8 +195,19 @@ Layout make_layout(const w4a16_moe_plan_s& P, int T) {
   const double touched = std::max(1.0, E * (1.0 - std::exp(-static_cast<double>(L.R) / E)));
   const double per = L.R / touched;
   const double tiles_est = touched * std::max(1.0, std::ceil(per / L.bn));
-  L.s1 = P.ov_s1 ? P.ov_s1 : choose_splits(tiles_est, L.nt1, L.kb1, P.num_sms, 1.5);
-  L.s2 = P.ov_s2 ? P.ov_s2 : choose_splits(tiles_est, L.nt2, L.kb2, P.num_sms, 1.0);
+  // unit groups per route tile on the tensor-core path (NT tiles per unit; the
+  // same choice choose_nt makes below for a full-size ring)
+  int g1 = L.nt1, g2 = L.nt2;
+  if (!L.gemv) {
+    int nt, ab;
+    choose_nt(L.nt1, L.bn, 232448 - 3072, P.ov_nt1 ? P.ov_nt1 : kDefaultNT, L.kb1 <= kDoubleAccMaxKb, nt, ab);
+    g1 = cdiv(L.nt1, nt);
+    choose_nt(L.nt2, L.bn, 232448 - 3072 - kEpiStageBytes, P.ov_nt2 ? P.ov_nt2 : kDefaultNT, L.kb2 <= kDoubleAccMaxKb,
+              nt, ab);
+    g2 = cdiv(L.nt2, nt);
+  }
+  L.s1 = P.ov_s1 ? P.ov_s1 : choose_splits(tiles_est, g1, L.kb1, P.num_sms, 1.5);
+  L.s2 = P.ov_s2 ? P.ov_s2 : choose_splits(tiles_est, g2, L.kb2, P.num_sms, 1.0);
   L.kbps1 = cdiv(L.kb1, L.s1);
   L.kbps2 = cdiv(L.kb2, L.s2);
   if (L.gemv) {
@@ -175,18 +218,26 @@ Layout make_layout(const w4a16_moe_plan_s& P, int T) {
     L.smem = gemv_smem_bytes(L.bn, ksplit);
     L.stages2 = L.stages;
     L.smem2 = L.smem;
+    L.ntu1 = L.ntu2 = 1;
+    L.acc1 = L.acc2 = 2;
   } else {
-    L.stage_bytes = kStageA + L.bn * kStageBRow + kStageS;
     // dynamic shared memory: 1 KB alignment slack + stages + 2 KB control block
-    // (mbarriers, TMEM address, flags, token list)
+    // (mbarriers, TMEM address, flags)
     const int smem_budget = 232448 - 3072;
+    choose_nt(L.nt1, L.bn, smem_budget, P.ov_nt1 ? P.ov_nt1 : kDefaultNT, L.kbps1 <= kDoubleAccMaxKb, L.ntu1, L.acc1);
+    choose_nt(L.nt2, L.bn, smem_budget - kEpiStageBytes, P.ov_nt2 ? P.ov_nt2 : kDefaultNT, L.kbps2 <= kDoubleAccMaxKb,
+              L.ntu2, L.acc2);
+    L.stage_bytes = gemm_stage_bytes(L.ntu1, L.bn);
     L.stages = std::min(kMaxStages, smem_budget / L.stage_bytes);
     L.smem = 3072 + L.stages * L.stage_bytes;
-    L.stages2 = std::min(kMaxStages, (smem_budget - kEpiStageBytes) / L.stage_bytes);
-    L.smem2 = 3072 + kEpiStageBytes + L.stages2 * L.stage_bytes;
+    L.stage_bytes2 = gemm_stage_bytes(L.ntu2, L.bn);
+    L.stages2 = std::min(kMaxStages, (smem_budget - kEpiStageBytes) / L.stage_bytes2);
+    L.smem2 = 3072 + kEpiStageBytes + L.stages2 * L.stage_bytes2;
   }
-  L.grid1 = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(P.num_sms, static_cast<int64_t>(L.tiles_cap) * L.nt1 * L.s1)));
-  L.grid2 = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(P.num_sms, static_cast<int64_t>(L.tiles_cap) * L.nt2 * L.s2)));
+  const int64_t units1 = static_cast<int64_t>(L.tiles_cap) * cdiv(L.nt1, L.ntu1) * L.s1;
+  const int64_t units2 = static_cast<int64_t>(L.tiles_cap) * cdiv(L.nt2, L.ntu2) * L.s2;
+  L.grid1 = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(P.num_sms, units1)));
+  L.grid2 = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(P.num_sms, units2)));
 
   const int act_bytes = 2;
   size_t o = 0;
@@ -207,7 +258,6 @@ Layout make_layout(const w4a16_moe_plan_s& P, int T) {
   L.off_inter = take(static_cast<size_t>(act_bytes) * L.slots_cap * d.inter);
   // expert outputs: the activation dtype without down split-K, FP32 partials with it
   L.off_y = take((L.s2 == 1 ? static_cast<size_t>(act_bytes) : sizeof(float) * L.s2) * L.slots_cap * d.hidden);
-  L.off_xs = take(L.gemv ? 0 : static_cast<size_t>(act_bytes) * L.slots_cap * d.hidden);
   L.off_sx = take(static_cast<size_t>(act_bytes) * T * d.hidden);
   L.off_sids = take(sizeof(int32_t) * std::max(L.R, 1));
   L.off_sw = take(sizeof(float) * std::max(L.R, 1));
@@ -365,9 +415,10 @@ w4a16_status launch_forward(const w4a16_moe_plan_s& P, const Layout& L, const vo
                             uint8_t* ws, cudaStream_t s) {
   const w4a16_moe_desc& d = P.d;
   const bool group = d.scale_kind == W4A16_SCALE_GROUP32_K;
+  const bool il = P.layout == W4A16_LAYOUT_INTERLEAVED;
   CUtensorMap tmA1, tmA2, tmB2;
   bool ok;
-  if (group) {
+  if (group || il) {
     // rows of packed bytes along K; boxes of 64 rows x one stage of K (128
     // bytes = 256 K values, 128-byte swizzle) on both paths
     static_assert(kGemvBlockK / 2 == 128 && kBlockK / 2 == 128, "weight boxes are 128 bytes wide");
@@ -379,10 +430,9 @@ w4a16_status launch_forward(const w4a16_moe_plan_s& P, const Layout& L, const vo
          encode_weights(&tmA2, w2, d.inter, d.hidden / 2, d.num_experts, 32);
   }
   ok = ok && encode_rows16(&tmB2, ws + L.off_inter, d.inter, L.slots_cap, L.bn, d.act_dtype);
-  // tensor-core path: activation rows copied into slot order, read as tiles
-  CUtensorMap tmX;
-  memset(&tmX, 0, sizeof(tmX));
-  if (!L.gemv) ok = ok && encode_rows16(&tmX, ws + L.off_xs, d.hidden, L.slots_cap, L.bn, d.act_dtype);
+  // the tensor-core gate/up GEMM gathers its activation rows itself (no map)
+  CUtensorMap tmNone;
+  memset(&tmNone, 0, sizeof(tmNone));
   // tensor-core path: expert outputs y [splits * slots_cap, H], TMA-stored
   const bool y16 = L.s2 == 1;
   CUtensorMap tmY;
@@ -413,8 +463,13 @@ w4a16_status launch_forward(const w4a16_moe_plan_s& P, const Layout& L, const vo
   g.slots_cap = L.slots_cap;
   g.err = reinterpret_cast<int32_t*>(ws + L.off_err);
   g.tiles_cap = L.tiles_cap;
+  g.wait_ns = P.wait_ns;
+  const int lay = il ? LAYOUT_IL : LAYOUT_CANON;
 
   GemmParams g1 = g;
+  g1.nt_unit = L.ntu1;
+  g1.n_groups = cdiv(L.nt1, L.ntu1);
+  g1.acc_bufs = L.acc1;
   g1.n_rows = L.n1;
   g1.K = d.hidden;
   g1.out_cols = d.inter;
@@ -429,27 +484,19 @@ w4a16_status launch_forward(const w4a16_moe_plan_s& P, const Layout& L, const vo
   g1.counters = reinterpret_cast<int32_t*>(ws + L.off_ctr);
   g1.scale_tma = stma1 ? 1 : 0;
   cudaError_t e;
-  if (!L.gemv) {
-    PermuteParams pp = {};
-    pp.x = x;
-    pp.inv = reinterpret_cast<const int32_t*>(ws + L.off_inv);
-    pp.xs = ws + L.off_xs;
-    pp.R = L.R;
-    pp.k = d.top_k;
-    pp.H = d.hidden;
-    const int warps_per_block = kPermuteThreads / 32;
-    const int grid = std::max(1, std::min((L.R + warps_per_block - 1) / warps_per_block, 8 * P.num_sms));
-    e = launch_permute(pp, grid, s, P.pdl);
-    if (e != cudaSuccess) return cuda_fail(e, "activation permute launch");
-  }
   if (P.has_ev && (e = cudaEventRecord(P.ev[0], s)) != cudaSuccess) return cuda_fail(e, "event record");
-  e = L.gemv ? launch_gemv(GEMM_UP, d.scale_kind, d.act_dtype, g1, tmA1, tmS1, L.grid1, L.smem, s, P.pdl)
-             : launch_gemm(GEMM_UP, d.scale_kind, d.act_dtype, g1, tmA1, tmX, tmY, tmS1, L.grid1, L.smem, s, P.pdl);
+  e = L.gemv ? launch_gemv(GEMM_UP, d.scale_kind, d.act_dtype, lay, g1, tmA1, tmS1, L.grid1, L.smem, s, P.pdl)
+             : launch_gemm(GEMM_UP, d.scale_kind, d.act_dtype, lay, g1, tmA1, tmNone, tmY, tmS1, L.grid1, L.smem, s,
+                           P.pdl);
   if (e != cudaSuccess) return cuda_fail(e, "gate/up GEMM launch");
   if (P.has_ev && (e = cudaEventRecord(P.ev[1], s)) != cudaSuccess) return cuda_fail(e, "event record");
 
   GemmParams g2 = g;
   g2.stages = L.stages2;
+  if (!L.gemv) g2.stage_bytes = L.stage_bytes2;
+  g2.nt_unit = L.ntu2;
+  g2.n_groups = cdiv(L.nt2, L.ntu2);
+  g2.acc_bufs = L.acc2;
   g2.n_rows = d.hidden;
   g2.K = d.inter;
   g2.out_cols = d.hidden;
@@ -464,8 +511,9 @@ w4a16_status launch_forward(const w4a16_moe_plan_s& P, const Layout& L, const vo
   g2.counters = nullptr;
   g2.scale_tma = stma2 ? 1 : 0;
   g2.out16 = y16 ? 1 : 0;
-  e = L.gemv ? launch_gemv(GEMM_DOWN, d.scale_kind, d.act_dtype, g2, tmA2, tmS2, L.grid2, L.smem2, s, P.pdl)
-             : launch_gemm(GEMM_DOWN, d.scale_kind, d.act_dtype, g2, tmA2, tmB2, tmY, tmS2, L.grid2, L.smem2, s, P.pdl);
+  e = L.gemv ? launch_gemv(GEMM_DOWN, d.scale_kind, d.act_dtype, lay, g2, tmA2, tmS2, L.grid2, L.smem2, s, P.pdl)
+             : launch_gemm(GEMM_DOWN, d.scale_kind, d.act_dtype, lay, g2, tmA2, tmB2, tmY, tmS2, L.grid2, L.smem2, s,
+                           P.pdl);
   if (e != cudaSuccess) return cuda_fail(e, "down GEMM launch");
   if (P.has_ev && (e = cudaEventRecord(P.ev[2], s)) != cudaSuccess) return cuda_fail(e, "event record");
 
@@ -490,37 +538,51 @@ w4a16_status launch_forward(const w4a16_moe_plan_s& P, const Layout& L, const vo
 }  // namespace
 
 namespace w4a16 {
-template <int DT>
+template <int DT, int LAYOUT>
 cudaError_t launch_gemm_dt(int which, int scale_kind, const GemmParams& p, const CUtensorMap& tmA,
                            const CUtensorMap& tmB, const CUtensorMap& tmC, const CUtensorMap& tmS,
                            int grid, int smem_bytes, cudaStream_t s, bool pdl);
-extern template cudaError_t launch_gemm_dt<DT_BF16>(int, int, const GemmParams&, const CUtensorMap&,
-                                                     const CUtensorMap&, const CUtensorMap&,
-                                                     const CUtensorMap&, int, int, cudaStream_t, bool);
-extern template cudaError_t launch_gemm_dt<DT_FP16>(int, int, const GemmParams&, const CUtensorMap&,
-                                                     const CUtensorMap&, const CUtensorMap&,
-                                                     const CUtensorMap&, int, int, cudaStream_t, bool);
+#define W4A16_GEMM_EXTERN(DT, LAYOUT)                                                                          \
+  extern template cudaError_t launch_gemm_dt<DT, LAYOUT>(int, int, const GemmParams&, const CUtensorMap&,     \
+                                                         const CUtensorMap&, const CUtensorMap&,              \
+                                                         const CUtensorMap&, int, int, cudaStream_t, bool);
+W4A16_GEMM_EXTERN(DT_BF16, LAYOUT_CANON)
+W4A16_GEMM_EXTERN(DT_FP16, LAYOUT_CANON)
+W4A16_GEMM_EXTERN(DT_BF16, LAYOUT_IL)
+W4A16_GEMM_EXTERN(DT_FP16, LAYOUT_IL)
+#undef W4A16_GEMM_EXTERN
 
-cudaError_t launch_gemm(int which, int scale_kind, int dtype, const GemmParams& p,
+cudaError_t launch_gemm(int which, int scale_kind, int dtype, int layout, const GemmParams& p,
                         const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
                         const CUtensorMap& tmS, int grid, int smem_bytes, cudaStream_t s, bool pdl) {
-  if (dtype == DT_BF16)
-    return launch_gemm_dt<DT_BF16>(which, scale_kind, p, tmA, tmB, tmC, tmS, grid, smem_bytes, s, pdl);
-  return launch_gemm_dt<DT_FP16>(which, scale_kind, p, tmA, tmB, tmC, tmS, grid, smem_bytes, s, pdl);
+  if (layout == LAYOUT_IL)
+    return dtype == DT_BF16
+               ? launch_gemm_dt<DT_BF16, LAYOUT_IL>(which, scale_kind, p, tmA, tmB, tmC, tmS, grid, smem_bytes, s, pdl)
+               : launch_gemm_dt<DT_FP16, LAYOUT_IL>(which, scale_kind, p, tmA, tmB, tmC, tmS, grid, smem_bytes, s, pdl);
+  return dtype == DT_BF16
+             ? launch_gemm_dt<DT_BF16, LAYOUT_CANON>(which, scale_kind, p, tmA, tmB, tmC, tmS, grid, smem_bytes, s, pdl)
+             : launch_gemm_dt<DT_FP16, LAYOUT_CANON>(which, scale_kind, p, tmA, tmB, tmC, tmS, grid, smem_bytes, s, pdl);
 }
 
-template <int DT>
+template <int DT, int LAYOUT>
 cudaError_t launch_gemv_dt(int which, int scale_kind, const GemmParams& p, const CUtensorMap& tmA,
                            const CUtensorMap& tmS, int grid, int smem_bytes, cudaStream_t s, bool pdl);
-extern template cudaError_t launch_gemv_dt<DT_BF16>(int, int, const GemmParams&, const CUtensorMap&,
-                                                     const CUtensorMap&, int, int, cudaStream_t, bool);
-extern template cudaError_t launch_gemv_dt<DT_FP16>(int, int, const GemmParams&, const CUtensorMap&,
-                                                     const CUtensorMap&, int, int, cudaStream_t, bool);
+#define W4A16_GEMV_EXTERN(DT, LAYOUT)                                                                          \
+  extern template cudaError_t launch_gemv_dt<DT, LAYOUT>(int, int, const GemmParams&, const CUtensorMap&,     \
+                                                         const CUtensorMap&, int, int, cudaStream_t, bool);
+W4A16_GEMV_EXTERN(DT_BF16, LAYOUT_CANON)
+W4A16_GEMV_EXTERN(DT_FP16, LAYOUT_CANON)
+W4A16_GEMV_EXTERN(DT_BF16, LAYOUT_IL)
+W4A16_GEMV_EXTERN(DT_FP16, LAYOUT_IL)
+#undef W4A16_GEMV_EXTERN
 
-cudaError_t launch_gemv(int which, int scale_kind, int dtype, const GemmParams& p, const CUtensorMap& tmA,
+cudaError_t launch_gemv(int which, int scale_kind, int dtype, int layout, const GemmParams& p, const CUtensorMap& tmA,
                         const CUtensorMap& tmS, int grid, int smem_bytes, cudaStream_t s, bool pdl) {
-  if (dtype == DT_BF16) return launch_gemv_dt<DT_BF16>(which, scale_kind, p, tmA, tmS, grid, smem_bytes, s, pdl);
-  return launch_gemv_dt<DT_FP16>(which, scale_kind, p, tmA, tmS, grid, smem_bytes, s, pdl);
+  if (layout == LAYOUT_IL)
+    return dtype == DT_BF16 ? launch_gemv_dt<DT_BF16, LAYOUT_IL>(which, scale_kind, p, tmA, tmS, grid, smem_bytes, s, pdl)
+                            : launch_gemv_dt<DT_FP16, LAYOUT_IL>(which, scale_kind, p, tmA, tmS, grid, smem_bytes, s, pdl);
+  return dtype == DT_BF16 ? launch_gemv_dt<DT_BF16, LAYOUT_CANON>(which, scale_kind, p, tmA, tmS, grid, smem_bytes, s, pdl)
+                          : launch_gemv_dt<DT_FP16, LAYOUT_CANON>(which, scale_kind, p, tmA, tmS, grid, smem_bytes, s, pdl);
 }
 }  // namespace w4a16
 
@@ -542,6 +604,17 @@ w4a16_status w4a16_moe_plan(const w4a16_moe_desc* desc, w4a16_moe_plan_t* out, s
     cudaGetLastError();  // no device here: plan with the GB300 SM count
   }
   P->pdl = env_flag("W4A16_MOE_PDL", true);
+  P->layout = W4A16_LAYOUT_CHECKPOINT;
+  // tuning knobs for measurements: weight tiles per tensor-core unit of each GEMM
+  if (const char* v = getenv("W4A16_MOE_NT_GATE_UP")) P->ov_nt1 = atoi(v);
+  if (const char* v = getenv("W4A16_MOE_NT_DOWN")) P->ov_nt2 = atoi(v);
+  if (P->ov_nt1 != 0 && P->ov_nt1 != 1 && P->ov_nt1 != 2 && P->ov_nt1 != 4) P->ov_nt1 = 0;
+  if (P->ov_nt2 != 0 && P->ov_nt2 != 1 && P->ov_nt2 != 2 && P->ov_nt2 != 4) P->ov_nt2 = 0;
+  P->wait_ns = kWaitTimeoutNs;
+  if (const char* v = getenv("W4A16_MOE_WAIT_TIMEOUT_NS")) {
+    const unsigned long long ns = strtoull(v, nullptr, 10);
+    if (ns > 0) P->wait_ns = ns;
+  }
   P->ws_bytes = max_workspace(*P);
   *out = P;
   *workspace_bytes = P->ws_bytes;
@@ -679,8 +752,17 @@ w4a16_status w4a16_moe_forward_host(w4a16_moe_plan_t plan, int32_t num_tokens, c
   return W4A16_OK;
 }
 
+namespace {
+w4a16_status static_workspace_ptr(void** out);
+}
+
 w4a16_status w4a16_moe_check_device_error(w4a16_moe_plan_t plan, void* workspace, void* stream) {
-  if (!plan || !workspace) return fail(W4A16_ERR_INVALID_ARG, "plan / workspace is NULL");
+  if (!plan) return fail(W4A16_ERR_INVALID_ARG, "plan is NULL");
+  if (!workspace) {
+    // the fixed workspace of w4a16_moe_forward_static_workspace
+    w4a16_status st = static_workspace_ptr(&workspace);
+    if (st != W4A16_OK) return st;
+  }
   const Layout L = make_layout(*plan, 1);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   int32_t flag = 0;
@@ -768,6 +850,37 @@ w4a16_status w4a16_moe_set_stage_events(w4a16_moe_plan_t plan, void* const* even
   return W4A16_OK;
 }
 
+w4a16_status w4a16_moe_set_weight_layout(w4a16_moe_plan_t plan, int32_t layout) {
+  if (!plan) return fail(W4A16_ERR_INVALID_ARG, "plan is NULL");
+  if (layout != W4A16_LAYOUT_CHECKPOINT && layout != W4A16_LAYOUT_INTERLEAVED)
+    return fail(W4A16_ERR_INVALID_ARG, "unknown weight layout %d", layout);
+  plan->layout = layout;
+  return W4A16_OK;
+}
+
+w4a16_status w4a16_moe_relayout_weights(w4a16_moe_plan_t plan, int32_t which, const uint8_t* in, uint8_t* out,
+                                        void* stream) {
+  if (!plan) return fail(W4A16_ERR_INVALID_ARG, "plan is NULL");
+  if (which != 0 && which != 1) return fail(W4A16_ERR_INVALID_ARG, "which must be 0 (W13) or 1 (W2), got %d", which);
+  w4a16_status st;
+  if ((st = check_ptr(in, 16, "in")) != W4A16_OK) return st;
+  if ((st = check_ptr(out, 16, "out")) != W4A16_OK) return st;
+  const w4a16_moe_desc& d = plan->d;
+  const int32_t N = which == 0 ? (d.act == W4A16_ACT_SWIGLU ? 2 * d.inter : d.inter) : d.hidden;
+  const int32_t K = which == 0 ? d.hidden : d.inter;
+  const bool row_pairs = d.scale_kind == W4A16_SCALE_PER_CHANNEL;
+  const size_t bytes = static_cast<size_t>(d.num_experts) * N * (K / 2);
+  const uintptr_t a = reinterpret_cast<uintptr_t>(in), b = reinterpret_cast<uintptr_t>(out);
+  if (row_pairs && a < b + bytes && b < a + bytes)
+    return fail(W4A16_ERR_INVALID_ARG, "per-channel relayout needs disjoint in / out buffers");
+  if (!row_pairs && a != b && a < b + bytes && b < a + bytes)
+    return fail(W4A16_ERR_INVALID_ARG, "in and out must be the same buffer or disjoint");
+  cudaError_t e = launch_relayout(row_pairs, in, out, d.num_experts, N, K, plan->num_sms,
+                                  static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "relayout launch");
+  return W4A16_OK;
+}
+
 const char* w4a16_moe_last_error(void) { return g_err.c_str(); }
 
 }  // extern "C"
@@ -814,7 +927,9 @@ w4a16_status w4a16_moe_forward_static_workspace(w4a16_moe_plan_t plan, int32_t n
   if (num_tokens < 0 || num_tokens > plan->d.max_tokens)
     return fail(W4A16_ERR_INVALID_ARG, "num_tokens %d outside [0, %d]", num_tokens, plan->d.max_tokens);
   if (num_tokens == 0) return W4A16_OK;
-  const size_t need = make_layout(*plan, num_tokens).total;
+  // device-side regions only: the host-call staging at the end of the layout
+  // (from off_sx on) serves w4a16_moe_forward_host and the masked layout
+  const size_t need = make_layout(*plan, num_tokens).off_sx;
   if (need > W4A16_STATIC_WORKSPACE_BYTES)
     return fail(W4A16_ERR_WORKSPACE_TOO_SMALL,
                 "batch of %d tokens needs %zu bytes of workspace; the static workspace holds %u",

@@ -17,16 +17,27 @@ namespace w4a16 {
 // ---------------------------------------------------------------------------
 constexpr int kTileRows = 128;       // weight rows per MMA tile (MMA M)
 constexpr int kBlockK = 256;         // K elements per pipeline stage (shared-memory ring)
-constexpr int kHalfK = kBlockK / 2;  // K elements per TMEM A buffer (one dequant warpgroup's half)
+constexpr int kHalfK = kBlockK / 2;
 constexpr int kGroup = 32;           // group size of the group-wise scales
 constexpr int kGroupsPerStage = kBlockK / kGroup;
 constexpr int kMaxStages = 12;
-constexpr int kGemmThreads = 512;    // 16 warps: see the role map in gemm.cuh
+constexpr int kGemmThreads = 768;    // 24 warps: see the role map in gemm.cuh
+constexpr int kGemmDqWarps = 16;     // dequantising warps: 4 warpgroups
+constexpr int kQuarterK = kBlockK / 4;  // K values each dequant warpgroup handles per stage
 constexpr int kTmemCols = 512;
-constexpr int kAbufCols = kHalfK / 2;   // one half-stage of BF16/FP16 A in TMEM columns
-constexpr int kNumAbuf = 4;             // A buffers: two per dequant warpgroup
-constexpr int kAccCol0 = kNumAbuf * kAbufCols;  // first accumulator column
+constexpr int kAslotCols = 128;           // one A slot: 16 MMAs (NT tiles x 256/NT K values)
+constexpr int kMaxAslots = 3;
+constexpr int kMaxNT = 4;                  // weight tiles per tensor-core unit
 constexpr int kMaxBN = 128;
+// TMEM split: A slots from column 0 (as many 128-column slots as fit, at most
+// 3), then acc_bufs accumulator sets of NT tiles x bn columns.
+__host__ __device__ constexpr int gemm_a_slots(int nt, int bn, int acc_bufs) {
+  return (kTmemCols - acc_bufs * nt * bn) / kAslotCols < kMaxAslots ? (kTmemCols - acc_bufs * nt * bn) / kAslotCols
+                                                                     : kMaxAslots;
+}
+// Tensor-core stage: NT weight tiles (16 KB packed + 2 KB scales each) and the
+// route tile's activation rows (bn x 512 B).
+__host__ __device__ constexpr int gemm_stage_bytes(int nt, int bn) { return nt * (kTileRows * kBlockK / 2 + kTileRows * 16) + bn * kBlockK * 2; }
 constexpr int kStageA = kTileRows * kBlockK / 2;   // 16 KB packed INT4 per stage
 constexpr int kStageS = kTileRows * kGroupsPerStage * 2;  // 2 KB BF16 group scales per stage
 constexpr int kStageBRow = kBlockK * 2;            // bytes of one activation row per stage
@@ -64,6 +75,13 @@ enum { ACT_SWIGLU = 0, ACT_RELU2 = 1 };
 enum { SCALE_GROUP = 0, SCALE_CHANNEL = 1 };
 enum { DT_BF16 = 0, DT_FP16 = 1 };
 enum { GEMM_UP = 0, GEMM_DOWN = 1 };
+// Packed weight layouts.  CANON: the caller's checkpoint layout (group scales:
+// two codes per byte along K, even K in the low nibble; per-channel: two rows
+// per byte along the output dim).  IL: the plan-time relayout -- always packed
+// along K, and inside every 32-bit word (8 consecutive K values 8w..8w+7) the
+// nibble at bit position 4p holds K index 8w + {0, 2, 4, 6, 1, 3, 5, 7}[p], so
+// that (word >> 4i) & 0x000F000F is the pair (8w + 2i, 8w + 2i + 1).
+enum { LAYOUT_CANON = 0, LAYOUT_IL = 1 };
 
 // ---------------------------------------------------------------------------
 // Launch parameters
@@ -82,14 +100,6 @@ struct RoutePrepParams {
   int32_t* err;            // device error flag, cleared here
 };
 
-// Slot-ordered copy of the activation rows for the tensor-core gate/up GEMM.
-struct PermuteParams {
-  const void* x;           // [T, H] activations (16-bit)
-  const int32_t* inv;      // [R] slot of flat route r = t * k + j, -1 if dropped
-  void* xs;                // [slots_cap, H]: row inv[r] receives x[r / k]
-  int32_t R, k, H;
-};
-
 struct GemmParams {
   int32_t act;             // ACT_* (gate/up GEMM epilogue)
   int32_t E;               // local experts
@@ -99,6 +109,9 @@ struct GemmParams {
   int32_t out_cols;        // row length of the output buffer (I or H)
   int32_t bn;              // route-tile height = MMA N
   int32_t n_tiles;         // 128-row weight tiles per expert
+  int32_t nt_unit;         // tensor-core path: weight tiles per unit (NT = 1, 2, 4)
+  int32_t n_groups;        // tensor-core path: ceil(n_tiles / NT) unit groups per route tile
+  int32_t acc_bufs;        // tensor-core path: accumulator sets in TMEM (1 or 2)
   int32_t kb_total;        // K blocks of kBlockK
   int32_t splits;          // split-K factor
   int32_t kb_per_split;
@@ -107,9 +120,9 @@ struct GemmParams {
   int32_t stage_bytes;
   const int4* tiles;       // route tiles (expert, first slot, valid rows, 0)
   const int32_t* num_tiles;
-  const int32_t* perm;     // slot -> flat route (CUDA-core path: activation rows by token)
-  const void* x;           // CUDA-core path only: activations [T, H] (gate/up)
-                           // or the intermediate [slots_cap, I] (down)
+  const int32_t* perm;     // slot -> flat route (gate/up: activation rows by token)
+  const void* x;           // gate/up: activations [T, H] (both paths); down, CUDA-core
+                           // path: the intermediate [slots_cap, I]
   const uint16_t* scales;  // BF16 scale bits of this GEMM's weights
   int64_t slots_cap;
   void* out;               // gate/up: intermediate [slots_cap, I] act dtype
@@ -121,6 +134,7 @@ struct GemmParams {
   int32_t scale_tma;       // group scales loaded by TMA (their rows are 16-byte multiples)
   int32_t out16;           // down GEMM: expert outputs in the activation dtype (no split-K),
                            // else FP32 split partials
+  uint64_t wait_ns;        // limit of every pipeline wait (drains use kWaitTimeoutNs)
 };
 
 struct CombineParams {
@@ -136,17 +150,17 @@ struct CombineParams {
 
 // Host-side launchers (one translation unit each).
 cudaError_t launch_route_prep(const RoutePrepParams& p, int smem_bytes, cudaStream_t s, bool pdl);
-cudaError_t launch_permute(const PermuteParams& p, int grid, cudaStream_t s, bool pdl);
-constexpr int kPermuteThreads = 256;
-cudaError_t launch_gemm(int which, int scale_kind, int dtype, const GemmParams& p,
+cudaError_t launch_gemm(int which, int scale_kind, int dtype, int layout, const GemmParams& p,
                         const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
                         const CUtensorMap& tmS, int grid, int smem_bytes, cudaStream_t s, bool pdl);
-cudaError_t launch_gemv(int which, int scale_kind, int dtype, const GemmParams& p,
+cudaError_t launch_gemv(int which, int scale_kind, int dtype, int layout, const GemmParams& p,
                         const CUtensorMap& tmA, const CUtensorMap& tmS, int grid, int smem_bytes,
                         cudaStream_t s, bool pdl);
 cudaError_t launch_combine(int dtype, const CombineParams& p, cudaStream_t s, bool pdl);
-int gemm_smem_bytes(int bn, int stages);
-int gemm_stage_bytes(int bn);
+// Checkpoint layout -> LAYOUT_IL for one packed weight tensor of E experts x N
+// rows x K values (row_pairs: per-channel [E, N/2, K] input, else [E, N, K/2]).
+cudaError_t launch_relayout(bool row_pairs, const uint8_t* in, uint8_t* out, int64_t E, int32_t N, int32_t K,
+                            int num_sms, cudaStream_t s);
 
 constexpr int kRoutePrepThreads = 1024;
 constexpr int kRoutePrepWarps = kRoutePrepThreads / 32;
@@ -155,7 +169,7 @@ constexpr int kRoutePrepWarps = kRoutePrepThreads / 32;
 
 // Error codes written to the device error flag.
 constexpr int kErrTimeout = 1;
-constexpr unsigned long long kWaitTimeoutNs = 2000000000ull;  // 2 s
+constexpr unsigned long long kWaitTimeoutNs = 2000000000ull;  // 2 s: default and drain limit
 
 // ---------------------------------------------------------------------------
 // Generic helpers
@@ -216,21 +230,40 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Non-blocking test of the phase (mbarrier.try_wait may instead suspend the
+// thread in hardware until the phase completes or a system-defined time
+// passes).
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Bounded wait: returns false when the CTA-wide abort flag is raised or the
-// wait has lasted kWaitTimeoutNs, after raising the abort flag and the global
-// error flag.  Every spin in the GEMM pipeline goes through here.
+// wait has lasted `limit_ns`, after raising the abort flag and the global
+// error flag.  Every spin in the GEMM pipelines goes through here: pipeline
+// waits pass the plan's limit (GemmParams::wait_ns), the waits that drain
+// copies and MMAs still in flight before a CTA exits pass kWaitTimeoutNs.
 static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                            int32_t* err) {
+                                                   int32_t* err, uint64_t limit_ns) {
+  // Checked after every attempt.  Limits shorter than the default poll with
+  // test_wait (a try_wait can outlast them while suspended), so a limit of one
+  // timer tick gives up after one tick.
+  const bool poll = limit_ns < kWaitTimeoutNs;
   const uint64_t t0 = global_timer_ns();
-  for (uint32_t n = 1;; ++n) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((n & 63) == 0) {
-      if (*abort_flag) return false;
-      if (global_timer_ns() - t0 > kWaitTimeoutNs) {
-        *abort_flag = 1;
-        atomicExch(err, kErrTimeout);
-        return false;
-      }
+  for (;;) {
+    if (poll ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (global_timer_ns() - t0 > limit_ns) {
+      *abort_flag = 1;
+      atomicExch(err, kErrTimeout);
+      return false;
     }
   }
 }
@@ -238,10 +271,21 @@ static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parit
 // Fast path inline (one try_wait), the bounded spin out of line: the wait is
 // used at many sites and inlining the spin loop everywhere bloats the code
 // that all warp roles share in the instruction cache.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                          int32_t* err) {
-  if (mbar_try_wait(bar, parity)) return true;
-  return mbar_wait_slow(bar, parity, abort_flag, err);
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int32_t* err,
+                                          uint64_t limit_ns = kWaitTimeoutNs) {
+  if (limit_ns < kWaitTimeoutNs ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity)) return true;
+  return mbar_wait_slow(bar, parity, abort_flag, err, limit_ns);
+}
+
+// One lane of a converged warp, chosen by the hardware (elect.sync).
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred = 0;
+  asm volatile(
+      "{\n\t.reg .pred P1;\n\t"
+      "elect.sync _|P1, 0xffffffff;\n\t"
+      "selp.b32 %0, 1, 0, P1;\n\t}"
+      : "=r"(pred));
+  return pred != 0;
 }
 
 // Next use of a ring of `stages` slots: slot index and the parity of its phase.
@@ -377,6 +421,19 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
       : "memory");
 }
 
+// Same MMA with the B descriptor given as two 32-bit halves (the address
+// fields live in the low half; offsets added there never reach the high half).
+__device__ __forceinline__ void mma_ts_lh(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, uint32_t b_hi, uint32_t idesc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b64 bd;\n\t"
+      "setp.ne.b32 p, %5, 0;\n\t"
+      "mov.b64 bd, {%2, %3};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], bd, %4, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Arrive on `bar` once every tcgen05.mma issued so far by this thread is done.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile(
@@ -445,6 +502,17 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
 
 __device__ __forceinline__ void tmem_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Waits for this thread's TMEM loads with their 16 destination registers as
+// in/out operands, so that no use of them can be scheduled before the wait.
+__device__ __forceinline__ void tmem_wait_ld(float (&v)[16]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+f"(v[0]), "+f"(v[1]), "+f"(v[2]), "+f"(v[3]), "+f"(v[4]), "+f"(v[5]), "+f"(v[6]), "+f"(v[7]),
+                 "+f"(v[8]), "+f"(v[9]), "+f"(v[10]), "+f"(v[11]), "+f"(v[12]), "+f"(v[13]), "+f"(v[14]),
+                 "+f"(v[15])
+               :
+               : "memory");
 }
 
 __device__ __forceinline__ uint32_t lop3_and_xor(uint32_t a, uint32_t b, uint32_t c) {

@@ -6,37 +6,47 @@
 // "down GEMM" of "feat(pytorch): add CuTeDSL W4A16 MoE backend" (LMDeploy),
 // sections Modification (register-side INT4 dequantisation, FP32
 // accumulation, TMA buffering, small-batch split-K, route-count-based tile
-// selection) and Benchmark; the dequantisation is done by two warp-specialised
+// selection) and Benchmark; the dequantisation is done by warp-specialised
 // warpgroups as in "perf: reduce split W4A16 routing and output overhead"
 // (FlashInfer), section Description.  Blackwell design (not the pages'):
 //
 //   weights (A, M = 128 rows)  TMA (128B swizzle) -> SMEM packed INT4, 256 K
-//                              values per stage -> dequant warps -> BF16/FP16
-//                              A operand in TMEM (four A buffers of 128 K
-//                              values: warpgroup g dequantises K-half g of
-//                              every stage into its two buffers, so
-//                              dequantisation overlaps the MMAs)
+//                              values per stage -> 4 dequant warpgroups, one
+//                              64-K quarter of every stage each -> BF16/FP16
+//                              A operand in TMEM (a ring of 2 or 3 whole-stage
+//                              slots, so dequantisation runs ahead of the MMAs)
 //   group scales               TMA boxes of 8 groups (16-byte rows), else cp.async
-//   activations (B, N = bn)    TMA tile of a slot-ordered matrix: the token
-//                              rows of x copied by route (gate/up) or the
-//                              intermediate (down) -> SMEM (128B-swizzled,
-//                              K-major)
-//   tcgen05.mma.kind::f16 (A from TMEM, B from SMEM), FP32 accumulators in TMEM,
-//   double-buffered, drained by four epilogue warps; the down GEMM's outputs
-//   (activation dtype, or FP32 split partials) leave through SMEM staging
-//   buffers as TMA tensor stores.
+//   activations (B, N = bn)    gate/up: token rows of x gathered by route with
+//                              cp.async (128B-swizzled, K-major; x stays in
+//                              L2); down: TMA tiles of the slot-ordered
+//                              intermediate
+//   tcgen05.mma.kind::f16 (A from TMEM, B from SMEM, N = the tile's valid rows
+//   rounded up to 16), FP32 accumulators in TMEM, double-buffered, drained by
+//   four epilogue warps; the down GEMM's outputs (activation dtype, or FP32
+//   split partials) leave through SMEM staging buffers as TMA tensor stores.
 //
-// Warp roles (512 threads):
-//   warp 0       TMA producer: packed weights, group scales and the activation
-//                tile
-//   warp 1       TMEM allocation + single-thread MMA issuer
-//   warps 2, 3   idle
-//   warps 4..11  two dequant warpgroups; warpgroup g dequantises K-half g of
-//                every stage into TMEM A buffer (2 * stage counter + g) & 3
-//   warps 12..15 epilogue (TMEM -> registers -> activation / scaling -> HBM)
+// Warp roles (768 threads):
+//   warp 0        TMA producer: packed weights, group scales (down GEMM: also
+//                 the activation tile)
+//   warp 1        TMEM allocation + MMA issuer: the whole warp walks the
+//                 pipeline, one elected lane issues (a converged issuer keeps
+//                 the tensor pipe fed; a lone lane issued at 2/3 the rate).
+//                 One wait and one commit per stage of 16 MMAs: this warp
+//                 shares its scheduler with four busy dequant warps, so every
+//                 instruction it saves is MMA throughput
+//   warps 2, 3    gate/up GEMM: activation-row gather (cp.async); down: idle
+//   warps 4..19   four dequant warpgroups; warpgroup h dequantises K-quarter h
+//                 of every stage into columns 32 h .. 32 h + 31 of the stage's
+//                 TMEM A slot
+//   warps 20..23  epilogue (TMEM -> registers -> activation / scaling -> HBM)
+// A warp can reach only the TMEM lanes 32 (warp % 4) .. + 31, so dequant and
+// epilogue warp w handles weight-tile rows of lane quadrant w % 4.
 //
-// Work is a persistent loop over units (route tile, weight tile, K split);
-// every role walks the same unit sequence.  All waits are bounded (see
+// Work is a persistent loop over units (route tile, group of NT weight tiles,
+// K split); every role walks the same unit sequence.  The NT tiles of a unit
+// share each stage's activation tile: with one tile per unit the activation
+// rows would cross from L2 twice for every byte of weights at 64-route tiles,
+// more than the L2-to-SM path carries at the weight-streaming rate.  All waits are bounded (see
 // mbar_wait): a stuck pipeline raises an error flag and the CTA winds down,
 // draining its copies and MMAs before freeing TMEM.
 #pragma once
@@ -92,17 +102,25 @@ __device__ __forceinline__ float bf16_bits_to_float(uint16_t b) {
   return __uint_as_float(static_cast<uint32_t>(b) << 16);
 }
 
-// Unit decoding shared by every role.
+// Weights packed along K (every layout except per-channel CANON, which packs
+// row pairs): 128-row SMEM tile of 2 boxes x 64 rows x 128 bytes.
+template <int SCALE, int LAYOUT>
+struct KPacked {
+  static constexpr bool value = SCALE == SCALE_GROUP || LAYOUT == LAYOUT_IL;
+};
+
+// Unit decoding shared by every role: unit u = (route tile, group of NT
+// weight tiles, K split), split fastest.
 struct Unit {
-  int tile, nt, split, kb0, kb1;
+  int tile, grp, split, kb0, kb1;
 };
 
 __device__ __forceinline__ Unit decode_unit(const GemmParams& p, int u) {
   Unit w;
   w.split = u % p.splits;
   const int r = u / p.splits;
-  w.nt = r % p.n_tiles;
-  w.tile = r / p.n_tiles;
+  w.grp = r % p.n_groups;
+  w.tile = r / p.n_groups;
   w.kb0 = w.split * p.kb_per_split;
   w.kb1 = min(w.kb0 + p.kb_per_split, p.kb_total);
   return w;
@@ -112,7 +130,7 @@ __device__ __forceinline__ Unit decode_unit(const GemmParams& p, int u) {
 // to a tile index below the tile-list capacity, so this may be issued before the
 // tile count is known (speculatively, to overlap its latency).
 __device__ __forceinline__ int4 load_tile(const GemmParams& p, int u) {
-  return p.tiles[u / (p.splits * p.n_tiles)];
+  return p.tiles[u / (p.splits * p.n_groups)];
 }
 
 // Row (within the expert) of the weight rows held in tile rows 0..63 / 64..127.
@@ -140,47 +158,69 @@ __device__ __forceinline__ int tile_row_of_lane(const GemmParams& p, int l) {
   return l;
 }
 
-// Dequantise K-half h (kHalfK = 128 K values) of one stage of this thread's
-// weight row into TMEM columns [a_col, a_col + 64) of its lane.
-//   group scales: 2 boxes (row block) of 64 rows x 128 B (256 K values) with
-//   the 128-byte swizzle (one 16 B chunk = one group of 32); scales as 128 rows
-//   x 16 B (8 groups); the A operand is q * s rounded once to the 16-bit type.
-//   per-channel: packed along rows, 4 boxes (row block, K half) of 32 row pairs
-//   x 128 B with the 128-byte swizzle; the A operand is the exact code q (the
-//   scale is applied to the FP32 accumulator in the epilogue).
-template <int SCALE, int DT>
-__device__ __forceinline__ void dequant_stage(const uint8_t* sA, const uint8_t* sS, int tr, int h,
-                                              uint32_t a_taddr) {
+// Eight INT4 codes of one 32-bit word -> four 16-bit pairs of consecutive K
+// values (k, k + 1), optionally times the scale pair s2.
+//   CANON (byte m = K 2m | K 2m+1 << 4): a byte permute moves byte m of the
+//   word and of word >> 4 into the two halves first;
+//   IL (nibble position p = K {0,2,4,6,1,3,5,7}[p]): shifts alone line the
+//   pairs up.
+// In both, (v & 0x000F000F) ^ magic is B + q exactly in each half (B = 136 for
+// BF16, 1032 for FP16; nibble = q & 15) and subtracting B leaves the exact q.
+template <int DT, int LAYOUT, bool SCALED>
+__device__ __forceinline__ void codes_of_word(uint32_t x, uint32_t s2, uint32_t* out) {
   using T = F16<DT>;
   const uint32_t kMask = 0x000F000Fu;
-  if (SCALE == SCALE_GROUP) {
-    const uint2 sc = *reinterpret_cast<const uint2*>(sS + tr * 16 + h * 8);
+  uint32_t p[4];
+  if (LAYOUT == LAYOUT_IL) {
+    p[0] = x;
+    p[1] = x >> 4;
+    p[2] = x >> 8;
+    p[3] = x >> 12;
+  } else {
+    const uint32_t sh = x >> 4;
+    p[0] = __byte_perm(x, sh, 0x0400);
+    p[1] = __byte_perm(x, sh, 0x0501);
+    p[2] = __byte_perm(x, sh, 0x0602);
+    p[3] = __byte_perm(x, sh, 0x0703);
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t q = T::sub(lop3_and_xor(p[i], kMask, T::kMagic), T::kMagic);
+    out[i] = SCALED ? T::mul(q, s2) : q;
+  }
+}
+
+// Dequantise K-quarter h (kQuarterK = 64 K values) of one stage of this
+// thread's weight row into TMEM columns [a_col, a_col + 32) of its lane.
+//   K-packed layouts: 2 boxes (row block) of 64 rows x 128 B (256 K values)
+//   with the 128-byte swizzle (one 16 B chunk = one group of 32); group
+//   scales as 128 rows x 16 B (8 groups); the A operand is q * s rounded once
+//   to the 16-bit type (group scales) or the exact code q (per-channel: the
+//   scale multiplies the FP32 accumulator in the epilogue).
+//   per-channel CANON: packed along rows, 4 boxes (row block, K half) of 32
+//   row pairs x 128 B with the 128-byte swizzle; the A operand is the exact q.
+template <int SCALE, int DT, int LAYOUT>
+__device__ __forceinline__ void dequant_quarter(const uint8_t* sA, const uint8_t* sS, int tr, int h,
+                                                uint32_t a_taddr) {
+  using T = F16<DT>;
+  if (KPacked<SCALE, LAYOUT>::value) {
     const uint8_t* row = sA + (tr >> 6) * 8192 + (tr & 63) * 128;
     const int sw = tr & 7;
-    // Compact loop (not unrolled): the body stays small in the instruction
-    // cache, which the other warp roles of the CTA share.
-#pragma unroll 1
-    for (int g = 0; g < kHalfK / kGroup; ++g) {
-      const uint4 w = *reinterpret_cast<const uint4*>(row + (((4 * h + g) ^ sw) << 4));
-      const uint32_t sword = (g < 2) ? sc.x : sc.y;
-      const uint16_t s16 = T::from_bf16(static_cast<uint16_t>(sword >> ((g & 1) * 16)));
-      const uint32_t s2 = static_cast<uint32_t>(s16) * 0x00010001u;
-      const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-      uint32_t out[16];
+    uint32_t sword = 0;
+    if (SCALE == SCALE_GROUP) sword = *reinterpret_cast<const uint32_t*>(sS + tr * 16 + h * 4);
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const uint32_t x = ws[i];
-        const uint32_t sh = x >> 4;
-        // (k, k+1) = low and high nibble of byte m, moved to the two halves
-        const uint32_t p0 = __byte_perm(x, sh, 0x0400);
-        const uint32_t p1 = __byte_perm(x, sh, 0x0501);
-        const uint32_t p2 = __byte_perm(x, sh, 0x0602);
-        const uint32_t p3 = __byte_perm(x, sh, 0x0703);
-        out[4 * i + 0] = T::mul(T::sub(lop3_and_xor(p0, kMask, T::kMagic), T::kMagic), s2);
-        out[4 * i + 1] = T::mul(T::sub(lop3_and_xor(p1, kMask, T::kMagic), T::kMagic), s2);
-        out[4 * i + 2] = T::mul(T::sub(lop3_and_xor(p2, kMask, T::kMagic), T::kMagic), s2);
-        out[4 * i + 3] = T::mul(T::sub(lop3_and_xor(p3, kMask, T::kMagic), T::kMagic), s2);
+    for (int g = 0; g < 2; ++g) {
+      const uint4 w = *reinterpret_cast<const uint4*>(row + (((2 * h + g) ^ sw) << 4));
+      uint32_t s2 = 0;
+      if (SCALE == SCALE_GROUP) {
+        const uint16_t s16 = T::from_bf16(static_cast<uint16_t>(sword >> (g * 16)));
+        s2 = static_cast<uint32_t>(s16) * 0x00010001u;
       }
+      uint32_t out[16];
+      codes_of_word<DT, LAYOUT, SCALE == SCALE_GROUP>(w.x, s2, out + 0);
+      codes_of_word<DT, LAYOUT, SCALE == SCALE_GROUP>(w.y, s2, out + 4);
+      codes_of_word<DT, LAYOUT, SCALE == SCALE_GROUP>(w.z, s2, out + 8);
+      codes_of_word<DT, LAYOUT, SCALE == SCALE_GROUP>(w.w, s2, out + 12);
       tmem_st16(a_taddr + 16 * g, out);
     }
   } else {
@@ -188,9 +228,11 @@ __device__ __forceinline__ void dequant_stage(const uint8_t* sA, const uint8_t* 
     const int lr = tr & 63;
     const int pr = lr >> 1;
     const int shift = (lr & 1) * 4;
-    const uint8_t* row = sA + (b * 2 + h) * 4096 + pr * 128;
-#pragma unroll 1
-    for (int c = 0; c < 8; ++c) {
+    const uint8_t* row = sA + (b * 2 + (h >> 1)) * 4096 + pr * 128;
+    const uint32_t kMask = 0x000F000Fu;
+#pragma unroll
+    for (int cc = 0; cc < 4; ++cc) {
+      const int c = 4 * (h & 1) + cc;  // 16-K chunk of the K half
       const uint4 w = *reinterpret_cast<const uint4*>(row + ((c ^ (pr & 7)) << 4));
       const uint32_t ws[4] = {w.x >> shift, w.y >> shift, w.z >> shift, w.w >> shift};
       uint32_t out[8];
@@ -201,33 +243,91 @@ __device__ __forceinline__ void dequant_stage(const uint8_t* sA, const uint8_t* 
         out[2 * i + 0] = T::sub(lop3_and_xor(p0, kMask, T::kMagic), T::kMagic);
         out[2 * i + 1] = T::sub(lop3_and_xor(p1, kMask, T::kMagic), T::kMagic);
       }
-      tmem_st8(a_taddr + c * 8, out);
+      tmem_st8(a_taddr + cc * 8, out);
     }
   }
 }
 
 __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + expf(-g)); }
 
-template <int WHICH, int SCALE, int DT>
+// MMA N for a route tile with `rows` valid routes: rows rounded up to 16
+// (kind::f16 with M = 128 takes N in steps of 16), at most bn.
+__device__ __forceinline__ int mma_n_of(int rows, int bn) { return min(bn, max(16, (rows + 15) & ~15)); }
+
+// Bounded wait by every lane of a warp, with a warp-uniform result: a lane
+// that gave up (timeout or abort) makes the whole warp give up, so no warp is
+// left diverged before a __syncwarp or elect.sync.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int32_t* err,
+                                          uint64_t limit_ns) {
+  const bool r = mbar_wait(bar, parity, abort_flag, err, limit_ns);
+  return __all_sync(0xFFFFFFFFu, r);
+}
+
+// The MMAs of one A slot (called by the elected lane): NT tiles x 16 / NT
+// K16 steps, fully unrolled so that every MMA costs the issuing warp only an
+// address add or two -- that warp shares its scheduler with busy dequant
+// warps, so its instruction count per MMA bounds the tensor-core rate.
+//   d_tmem   accumulator of tile 0 (tile t at + t * bn)
+//   a0       the slot's first TMEM column (tile t at + t * 128 / NT)
+//   b_j      B descriptor of the slot's first K16 step (64-value atoms of
+//            atom_step descriptor units; 32-byte K steps add 2 inside an atom)
+//   first    the unit's first slot: each tile's first MMA overwrites
+template <int NT>
+__device__ __forceinline__ void issue_slot(uint32_t d_tmem, int bn, uint32_t a0, uint64_t b_j, uint32_t atom_step,
+                                           uint32_t idesc, bool first, int nvalid) {
+  constexpr int kSteps = 16 / NT;  // K16 steps of one tile in a slot
+  const uint32_t b_hi = static_cast<uint32_t>(b_j >> 32);
+#pragma unroll
+  for (int t = 0; t < NT; ++t) {
+    if (t < nvalid) {
+      const uint32_t d = d_tmem + t * bn;
+      uint32_t b_lo = static_cast<uint32_t>(b_j);
+#pragma unroll
+      for (int kk = 0; kk < kSteps; ++kk) {
+        mma_ts_lh(d, a0 + t * (kAslotCols / NT) + kk * 8, b_lo + (kk & 3) * 2, b_hi, idesc,
+                  (kk > 0 || !first) ? 1u : 0u);
+        if ((kk & 3) == 3) b_lo += atom_step;
+      }
+    }
+  }
+}
+
+template <int WHICH, int SCALE, int DT, int LAYOUT>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     w4a16_gemm_kernel(const __grid_constant__ GemmParams p, const __grid_constant__ CUtensorMap tmA,
                       const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmC,
                       const __grid_constant__ CUtensorMap tmS) {
   using T = F16<DT>;
+  constexpr bool kPacked = KPacked<SCALE, LAYOUT>::value;
+  constexpr bool kGather = WHICH == GEMM_UP;  // activation rows gathered by cp.async
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte aligned base, derived by pointer arithmetic on the shared array so
   // the compiler keeps the shared address space (LDS/STS, not generic loads).
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const int stages = p.stages;
   const int bn = p.bn;
+  const int NT = p.nt_unit;
+  const int acc_bufs = p.acc_bufs;
+  const int a_slots = gemm_a_slots(NT, bn, acc_bufs);
+  const int acc_col0 = a_slots * kAslotCols;
+  // K values of one tile in one A slot (KA = 256 / NT) and 64-K quarters per
+  // tile in a slot (qpt = 4 / NT); NT is a power of two
+  const int lg_nt = NT == 4 ? 2 : (NT == 2 ? 1 : 0);
+  const int qpt = 4 >> lg_nt;
+  const int ka_cols = kAslotCols >> lg_nt;  // TMEM columns of one tile in a slot
+  // stage layout: NT weight tiles [kStageA each] | activations [bn x 512 B,
+  // 4 atoms] | NT scale tiles [kStageS each]
+  const int off_b = NT * kStageA;
+  const int off_s = off_b + bn * kStageBRow;
   // down GEMM: output staging [4 warps][2][16 x 32] after the stages
   float* epi_stage = reinterpret_cast<float*>(smem + stages * p.stage_bytes);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + stages * p.stage_bytes +
                                                (WHICH == GEMM_DOWN ? kEpiStageBytes : 0));
   uint64_t* empty = full + kMaxStages;
-  uint64_t* afull = empty + kMaxStages;
-  uint64_t* aempty = afull + kNumAbuf;
-  uint64_t* accfull = aempty + kNumAbuf;
+  uint64_t* bfull = empty + kMaxStages;
+  uint64_t* afull = bfull + kMaxStages;
+  uint64_t* aempty = afull + kMaxAslots;
+  uint64_t* accfull = aempty + kMaxAslots;
   uint64_t* accempty = accfull + 2;
   uint64_t* drain = accempty + 2;
   uint64_t* epibar = drain + 1;
@@ -237,15 +337,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const uint64_t wait_ns = p.wait_ns;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < stages; ++s) {
       mbar_init(&full[s], 1);                  // producer (TMA bytes + scale copies)
-      mbar_init(&empty[s], 9);                 // 8 dequant warps + MMA commit
+      mbar_init(&empty[s], kGemmDqWarps + 1);  // 16 dequant warps + MMA commit
+      mbar_init(&bfull[s], 64);                // the gather warps' 64 lanes
     }
-    for (int b = 0; b < kNumAbuf; ++b) {
-      mbar_init(&afull[b], 4);
-      mbar_init(&aempty[b], 1);
+    for (int b = 0; b < a_slots; ++b) {
+      mbar_init(&afull[b], kGemmDqWarps);  // every dequant warp (one 64-K quarter each)
+      mbar_init(&aempty[b], 1);            // MMA commit
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&accfull[b], 1);
@@ -259,8 +361,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   }
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmA);
-    tma_prefetch_desc(&tmB);
-    if (WHICH == GEMM_DOWN) tma_prefetch_desc(&tmC);
+    if (WHICH == GEMM_DOWN) {
+      tma_prefetch_desc(&tmB);
+      tma_prefetch_desc(&tmC);
+    }
     if (SCALE == SCALE_GROUP && p.scale_tma) tma_prefetch_desc(&tmS);
   }
   if (warp == 1) {
@@ -278,7 +382,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
   // The first unit's tile record is fetched together with the tile count.
   const int4 first_ti = load_tile(p, blockIdx.x);
-  const int n_units = (*p.num_tiles) * p.n_tiles * p.splits;
+  const int n_units = (*p.num_tiles) * p.n_groups * p.splits;
   const int N1 = p.n_rows;
 
   if (warp == 0) {
@@ -297,52 +401,39 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       if (u + (int)gridDim.x < n_units) ti_next = load_tile(p, u + gridDim.x);  // prefetch
       if (w.kb1 <= w.kb0) continue;
       const int e = ti.x, m0 = ti.y;
-      int r0, r1;
-      tile_row_bases<WHICH>(p, w.nt, r0, r1);
-      // cp.async scale rows of this unit for this lane's tile rows (lane + 32 i);
-      // null when the row lies beyond the expert's rows
+      const int nvalid = min(NT, p.n_tiles - w.grp * NT);  // weight tiles of this unit
       const bool scale_copy = SCALE == SCALE_GROUP && !p.scale_tma;
-      const uint8_t* srow[4];
-      bool srow_al16 = true;
-      if (scale_copy) {
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int tr = lane + 32 * i;
-          const int grow = tr < 64 ? r0 + tr : r1 + (tr - 64);
-          srow[i] = grow < N1 ? reinterpret_cast<const uint8_t*>(p.scales) +
-                                    (static_cast<int64_t>(e) * N1 + grow) * sbytes_row
-                              : nullptr;
-          srow_al16 = srow_al16 && ((reinterpret_cast<uintptr_t>(srow[i]) & 15) == 0);
-        }
-      }
-      const uint32_t stage_tx = kStageA + bn * kStageBRow + (SCALE == SCALE_GROUP && p.scale_tma ? kStageS : 0);
+      const uint32_t stage_tx = nvalid * (kStageA + (SCALE == SCALE_GROUP && p.scale_tma ? kStageS : 0)) +
+                                (kGather ? 0 : bn * kStageBRow);
       for (int kb = w.kb0; kb < w.kb1; ++kb, ++it, ring_next(st, ph, stages)) {
-        if (!mbar_wait(&empty[st], ph ^ 1, abort_flag, p.err)) {
+        if (!warp_wait(&empty[st], ph ^ 1, abort_flag, p.err, wait_ns)) {
           ok = false;
           break;
         }
         uint8_t* sA = smem + st * p.stage_bytes;
-        uint8_t* sB = sA + kStageA;
-        uint8_t* sS = sB + bn * kStageBRow;
         if (scale_copy) {
-          // kGroupsPerStage scales (16 B) per tile row; lane handles rows lane + 32 i.
+          // kGroupsPerStage scales (16 B) per tile row; lane handles rows lane + 32 i
+          // of every tile; rows beyond the expert's rows read as zero
           const int g0 = kb * kGroupsPerStage;
           const int ng = min(kGroupsPerStage, groups_row - g0);
-          if (srow_al16 && ng == kGroupsPerStage) {
-            // common case: one 16-byte copy per row
+          for (int t = 0; t < nvalid; ++t) {
+            int r0, r1;
+            tile_row_bases<WHICH>(p, w.grp * NT + t, r0, r1);
+            uint8_t* sS = sA + off_s + t * kStageS;
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-              uint8_t* dst = sS + (lane + 32 * i) * 16;
-              if (srow[i]) cp_async<16>(dst, srow[i] + g0 * 2);
-              else *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
-            }
-          } else {
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              uint8_t* dst = sS + (lane + 32 * i) * 16;
-              const int nbytes = srow[i] ? max(ng, 0) * 2 : 0;
-              for (int o = 0; o < nbytes; o += 4) cp_async<4>(dst + o, srow[i] + g0 * 2 + o);
-              for (int o = nbytes; o < 16; o += 4) *reinterpret_cast<uint32_t*>(dst + o) = 0u;
+              const int tr = lane + 32 * i;
+              const int grow = tr < 64 ? r0 + tr : r1 + (tr - 64);
+              uint8_t* dst = sS + tr * 16;
+              const uint8_t* src = reinterpret_cast<const uint8_t*>(p.scales) +
+                                   (static_cast<int64_t>(e) * N1 + grow) * sbytes_row + g0 * 2;
+              const int nbytes = grow < N1 ? max(ng, 0) * 2 : 0;
+              if (nbytes == 16 && (reinterpret_cast<uintptr_t>(src) & 15) == 0) {
+                cp_async<16>(dst, src);
+              } else {
+                for (int o = 0; o < nbytes; o += 4) cp_async<4>(dst + o, src + o);
+                for (int o = nbytes; o < 16; o += 4) *reinterpret_cast<uint32_t*>(dst + o) = 0u;
+              }
             }
           }
           cp_async_mbar_arrive(&full[st]);
@@ -350,27 +441,34 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         __syncwarp();
         if (lane == 0) {
           mbar_arrive_expect_tx(&full[st], stage_tx);
-          if (SCALE == SCALE_GROUP) {
-            // two 64-row boxes of 128 packed bytes (256 K values), 128-byte swizzle
-            tma_load_3d(sA, &tmA, &full[st], kb * (kBlockK / 2), r0, e, pol_w);
-            tma_load_3d(sA + 8192, &tmA, &full[st], kb * (kBlockK / 2), r1, e, pol_w);
-            if (p.scale_tma) {
-              // two 64-row boxes of 8 group scales (16 bytes)
-              tma_load_3d(sS, &tmS, &full[st], kb * kGroupsPerStage, r0, e, pol_w);
-              tma_load_3d(sS + 1024, &tmS, &full[st], kb * kGroupsPerStage, r1, e, pol_w);
-            }
-          } else {
-            // four boxes (row block, K half) of 32 row pairs x 128 K bytes, 128-byte swizzle
+          for (int t = 0; t < nvalid; ++t) {
+            int r0, r1;
+            tile_row_bases<WHICH>(p, w.grp * NT + t, r0, r1);
+            uint8_t* sAt = sA + t * kStageA;
+            if (kPacked) {
+              // two 64-row boxes of 128 packed bytes (256 K values), 128-byte swizzle
+              tma_load_3d(sAt, &tmA, &full[st], kb * (kBlockK / 2), r0, e, pol_w);
+              tma_load_3d(sAt + 8192, &tmA, &full[st], kb * (kBlockK / 2), r1, e, pol_w);
+              if (SCALE == SCALE_GROUP && p.scale_tma) {
+                // two 64-row boxes of 8 group scales (16 bytes)
+                uint8_t* sS = sA + off_s + t * kStageS;
+                tma_load_3d(sS, &tmS, &full[st], kb * kGroupsPerStage, r0, e, pol_w);
+                tma_load_3d(sS + 1024, &tmS, &full[st], kb * kGroupsPerStage, r1, e, pol_w);
+              }
+            } else {
+              // four boxes (row block, K half) of 32 row pairs x 128 K bytes, 128-byte swizzle
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              tma_load_3d(sA + h * 4096, &tmA, &full[st], kb * kBlockK + h * kHalfK, r0 / 2, e, pol_w);
-              tma_load_3d(sA + (2 + h) * 4096, &tmA, &full[st], kb * kBlockK + h * kHalfK, r1 / 2, e,
-                          pol_w);
+              for (int h = 0; h < 2; ++h) {
+                tma_load_3d(sAt + h * 4096, &tmA, &full[st], kb * kBlockK + h * kHalfK, r0 / 2, e, pol_w);
+                tma_load_3d(sAt + (2 + h) * 4096, &tmA, &full[st], kb * kBlockK + h * kHalfK, r1 / 2, e, pol_w);
+              }
             }
           }
+          if (!kGather) {
 #pragma unroll
-          for (int a = 0; a < kBlockK / 64; ++a)
-            tma_load_2d(sB + a * bn * 128, &tmB, &full[st], kb * kBlockK + a * 64, m0, pol_b);
+            for (int a = 0; a < kBlockK / 64; ++a)
+              tma_load_2d(sA + off_b + a * bn * 128, &tmB, &full[st], kb * kBlockK + a * 64, m0, pol_b);
+          }
         }
         __syncwarp();
       }
@@ -383,99 +481,179 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      const uint32_t idesc = make_idesc_f16(DT == DT_BF16, kTileRows, bn);
-      const uint64_t bdesc_base = smem_desc_sw128(smem_u32(smem + kStageA));
-      const uint64_t atom_step = static_cast<uint64_t>(bn) * 128 / 16;
-      uint32_t it = 0, jc = 0, ph = 0;
-      int st = 0;
-      uint64_t d_st = bdesc_base;  // B descriptor of stage st
-      const uint64_t d_stage = static_cast<uint64_t>(p.stage_bytes >> 4);
-      bool ok = true;
-      for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-        const Unit w = decode_unit(p, u);
-        if (w.kb1 <= w.kb0) continue;
-        const int b = jc & 1;
-        if (!mbar_wait(&accempty[b], ((jc >> 1) & 1) ^ 1, abort_flag, p.err)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t d_tmem = tmem + kAccCol0 + b * bn;
-        for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
-          // A: the dequant warps arrive on afull[ab] only after they observed
-          // full[st] complete, and full[st] also carries this stage's B bytes
-          // (one expect_tx covers weights, scales and activations), so afull
-          // alone orders both operands before the MMAs.
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const uint32_t a_seq = 2 * it + h;
-            const int ab = a_seq % kNumAbuf;
-            if (!mbar_wait(&afull[ab], (a_seq / kNumAbuf) & 1, abort_flag, p.err)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            // B descriptors of this stage: the start-address field (bits 0-13,
-            // address >> 4) advances by 2 per 32-byte K step inside a 128-byte
-            // swizzle atom and by bn * 8 per 64-value atom; adding to the 64-bit
-            // value never carries out of the field (shared addresses < 256 KB).
-            const uint64_t d0 = d_st + static_cast<uint64_t>(2 * h) * atom_step;
-            const uint32_t a0 = tmem + ab * kAbufCols;
-            const uint32_t acc0 = (kb > w.kb0 || h > 0) ? 1u : 0u;
-#pragma unroll
-            for (int kk = 0; kk < kHalfK / 16; ++kk) {
-              mma_ts(d_tmem, a0 + kk * 8, d0 + (kk >> 2) * atom_step + (kk & 3) * 2, idesc,
-                     kk > 0 ? 1u : acc0);
-            }
-            mma_commit(&aempty[ab]);
+    // The whole warp walks the pipeline (every lane waits on the barriers, so
+    // the warp stays converged); one elected lane issues.  Per A slot: one
+    // wait, 16 MMAs (NT tiles x 256 / NT K values), one commit.
+    const uint32_t idesc0 = make_idesc_f16(DT == DT_BF16, kTileRows, 16) & ~(0x3Fu << 17);
+    const uint32_t atom_step = static_cast<uint32_t>(bn) * 128 / 16;
+    const uint64_t d_stage = static_cast<uint64_t>(p.stage_bytes >> 4);
+    const uint64_t bdesc_base = smem_desc_sw128(smem_u32(smem + off_b));
+    uint32_t jc = 0, ph = 0, a_ph = 0;
+    int st = 0, a_st = 0;
+    uint64_t d_st = bdesc_base;  // B descriptor of stage st
+    bool ok = true;
+    int4 ti_next = first_ti;
+    for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+      const Unit w = decode_unit(p, u);
+      const int4 ti = ti_next;
+      if (u + (int)gridDim.x < n_units) ti_next = load_tile(p, u + gridDim.x);
+      if (w.kb1 <= w.kb0) continue;
+      const uint32_t idesc = idesc0 | (static_cast<uint32_t>(mma_n_of(ti.z, bn) >> 3) << 17);
+      const int nvalid = min(NT, p.n_tiles - w.grp * NT);
+      const int b = acc_bufs == 2 ? (jc & 1) : 0;
+      const uint32_t acc_par = acc_bufs == 2 ? ((jc >> 1) & 1) : (jc & 1);
+      if (!warp_wait(&accempty[b], acc_par ^ 1, abort_flag, p.err, wait_ns)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t d_tmem = tmem + acc_col0 + b * NT * bn;
+      for (int kb = w.kb0; kb < w.kb1 && ok; ++kb) {
+        // gathered activation rows: cp.async writes (generic proxy) become
+        // visible to the MMA's shared-memory reads (async proxy) after the
+        // barrier and a proxy fence.  The dequant warps arrive on an A slot
+        // only after they observed full[st] complete, which also carries the
+        // down GEMM's activation bytes, so afull orders both operands there.
+        if (kGather) {
+          if (!warp_wait(&bfull[st], ph, abort_flag, p.err, wait_ns)) {
+            ok = false;
+            break;
           }
-          if (!ok) break;
-          mma_commit(&empty[st]);
-          ring_next(st, ph, stages);
-          d_st = st == 0 ? bdesc_base : d_st + d_stage;
+          fence_proxy_async_smem();
+        }
+        for (int j = 0; j < NT; ++j) {  // the stage's NT A slots, K range j * 256 / NT ..
+          if (!warp_wait(&afull[a_st], a_ph, abort_flag, p.err, wait_ns)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          if (elect_one()) {
+            const uint32_t a0 = tmem + a_st * kAslotCols;
+            // slot j covers K16 steps j * 16 / NT .. of the stage: atom j * 4 / NT
+            const uint64_t b_j = d_st + static_cast<uint64_t>((j << (2 - lg_nt)) * atom_step);
+            const bool first = kb == w.kb0 && j == 0;
+            if (NT == 4) issue_slot<4>(d_tmem, bn, a0, b_j, atom_step, idesc, first, nvalid);
+            else if (NT == 2) issue_slot<2>(d_tmem, bn, a0, b_j, atom_step, idesc, first, nvalid);
+            else issue_slot<1>(d_tmem, bn, a0, b_j, atom_step, idesc, first, nvalid);
+            mma_commit(&aempty[a_st]);
+          }
+          __syncwarp();
+          ring_next(a_st, a_ph, a_slots);
         }
         if (!ok) break;
-        mma_commit(&accfull[b]);
-        ++jc;
+        if (elect_one()) mma_commit(&empty[st]);
+        __syncwarp();
+        ring_next(st, ph, stages);
+        d_st = st == 0 ? bdesc_base : d_st + d_stage;
       }
-      // Drain: every MMA issued by this thread has finished before TMEM is freed.
-      mma_commit(drain);
-      volatile int no_abort = 0;
-      mbar_wait(drain, 0, &no_abort, p.err);
+      if (!ok) break;
+      if (elect_one()) mma_commit(&accfull[b]);
+      __syncwarp();
+      ++jc;
     }
+    // Drain: every MMA issued by this warp has finished before TMEM is freed.
+    if (elect_one()) mma_commit(drain);
+    __syncwarp();
+    volatile int no_abort = 0;
+    mbar_wait(drain, 0, &no_abort, p.err);
   } else if (warp < 4) {
-    // warps 2 and 3 have no role
-  } else if (warp < 12) {
+    // ------------------------------------------------------------------ activation gather
+    if (kGather) {
+      // Lane l of gather warp g copies 16 bytes (8 K values) of every route row
+      // r = g, g + 2, ... of the tile: one row per warp instruction, 512 bytes
+      // = this stage's 256 K values, into the 128B-swizzled K-major B tile
+      // (atom l / 8, chunk l % 8 of row r at chunk position (l % 8) ^ (r & 7)).
+      // Token rows come from x (which stays in L2); K past the end is
+      // zero-filled by the copy.  Each lane's cp.async.mbarrier.arrive marks
+      // bfull once its copies have landed.
+      const int g = warp - 2;
+      const uint16_t* xsrc = reinterpret_cast<const uint16_t*>(p.x);
+      const int atom = lane >> 3, chunk = lane & 7;
+      uint32_t ph = 0;
+      int st = 0;
+      bool ok = true;
+      int4 ti_next = first_ti;
+      for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+        const Unit w = decode_unit(p, u);
+        const int4 ti = ti_next;
+        if (u + (int)gridDim.x < n_units) ti_next = load_tile(p, u + gridDim.x);
+        if (w.kb1 <= w.kb0) continue;
+        const int m0 = ti.y;
+        const int rows = min(ti.z, bn);
+        // source token of rows g + 2 (lane + 32 i), i < 2 (bn <= 128)
+        int src[2];
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          const int r = g + 2 * (lane + 32 * i);
+          int tok = 0;
+          if (r < rows) {
+            const int route = p.perm[m0 + r];
+            tok = route >= 0 ? route / p.top_k : 0;
+          }
+          src[i] = tok;
+        }
+        for (int kb = w.kb0; kb < w.kb1; ++kb, ring_next(st, ph, stages)) {
+          if (!warp_wait(&empty[st], ph ^ 1, abort_flag, p.err, wait_ns)) {
+            ok = false;
+            break;
+          }
+          uint8_t* sB = smem + st * p.stage_bytes + off_b + atom * bn * 128;
+          const int col = kb * kBlockK + lane * 8;
+          const bool valid = col < p.K;
+          const uint16_t* xcol = xsrc + (valid ? col : 0);
+          for (int r = g, i = 0; r < rows; r += 2, ++i) {
+            const int tok = __shfl_sync(0xFFFFFFFFu, i < 32 ? src[0] : src[1], i & 31);
+            cp_async_cg16(sB + r * 128 + ((chunk ^ (r & 7)) << 4), xcol + static_cast<int64_t>(tok) * p.K,
+                          valid ? 16u : 0u);
+          }
+          cp_async_mbar_arrive_noinc(&bfull[st]);
+        }
+      }
+      // Every copy lands before the CTA exits.
+      asm volatile("cp.async.wait_all;" ::: "memory");
+    }
+  } else if (warp < 4 + kGemmDqWarps) {
     // ------------------------------------------------------------------ dequant warpgroups
-    const int wg = (warp - 4) >> 2;
-    const int q = warp & 3;
+    // Warpgroup h fills 64-K quarter h of every A slot: tile h / qpt of the
+    // unit, stage quarter j * qpt + h % qpt for the stage's slot j.
+    const int h = (warp - 4) >> 2;
+    const int q = warp & 3;  // TMEM lane quadrant
     const int tr = tile_row_of_lane<WHICH>(p, q * 32 + lane);
-    const uint32_t t_lane = tmem + (static_cast<uint32_t>(q * 32) << 16);
-    uint32_t it = 0, ph = 0;
-    int st = 0;
+    const int t = h >> (2 - lg_nt);  // h / qpt
+    const int hq = h & (qpt - 1);
+    const uint32_t t_lane = tmem + (static_cast<uint32_t>(q * 32) << 16) + t * ka_cols + hq * (kQuarterK / 2);
+    uint32_t ph = 0, a_ph = 0;
+    int st = 0, a_st = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
       const Unit w = decode_unit(p, u);
       if (w.kb1 <= w.kb0) continue;
-      for (int kb = w.kb0; kb < w.kb1; ++kb, ++it, ring_next(st, ph, stages)) {
-        const uint32_t a_seq = 2 * it + wg;
-        const int ab = a_seq % kNumAbuf;
-        if (!mbar_wait(&full[st], ph, abort_flag, p.err) ||
-            !mbar_wait(&aempty[ab], ((a_seq / kNumAbuf) & 1) ^ 1, abort_flag, p.err)) {
+      const bool tile_ok = w.grp * NT + t < p.n_tiles;  // uniform over the warpgroup
+      for (int kb = w.kb0; kb < w.kb1 && ok; ++kb, ring_next(st, ph, stages)) {
+        if (!warp_wait(&full[st], ph, abort_flag, p.err, wait_ns)) {
           ok = false;
           break;
         }
-        tc_fence_after();
-        const uint8_t* sA = smem + st * p.stage_bytes;
-        const uint8_t* sS = sA + kStageA + bn * kStageBRow;
-        dequant_stage<SCALE, DT>(sA, sS, tr, wg, t_lane + ab * kAbufCols);
-        tmem_wait_st();
+        const uint8_t* sA = smem + st * p.stage_bytes + t * kStageA;
+        const uint8_t* sS = smem + st * p.stage_bytes + off_s + t * kStageS;
+        for (int j = 0; j < NT; ++j) {
+          if (!warp_wait(&aempty[a_st], a_ph ^ 1, abort_flag, p.err, wait_ns)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          if (tile_ok) {
+            dequant_quarter<SCALE, DT, LAYOUT>(sA, sS, tr, j * qpt + hq, t_lane + a_st * kAslotCols);
+            tmem_wait_st();
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&afull[a_st]);
+          ring_next(a_st, a_ph, a_slots);
+        }
+        if (!ok) break;
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[st]);
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&afull[ab]);
       }
     }
   } else {
@@ -483,7 +661,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int q = warp & 3;
     const int tr = tile_row_of_lane<WHICH>(p, q * 32 + lane);
     const uint32_t t_lane = tmem + (static_cast<uint32_t>(q * 32) << 16);
-    const int epi_tid = threadIdx.x - 12 * 32;
+    const int epi_tid = threadIdx.x - (4 + kGemmDqWarps) * 32;
     const bool swiglu = (WHICH == GEMM_UP && p.act == ACT_SWIGLU);
     uint32_t jc = 0, eph = 0;
     int sbuf = 0;  // down GEMM: staging buffer of this warp's next chunk
@@ -492,7 +670,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     auto epi_sync = [&]() -> bool {
       __syncwarp();
       if (lane == 0) mbar_arrive(epibar);
-      const bool r = mbar_wait(epibar, eph & 1, abort_flag, p.err);
+      const bool r = warp_wait(epibar, eph & 1, abort_flag, p.err, wait_ns);
       ++eph;
       return r;
     };
@@ -503,140 +681,157 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const int4 ti = ti_next;
       if (u + (int)gridDim.x < n_units) ti_next = load_tile(p, u + gridDim.x);  // prefetch
       const int e = ti.x, m0 = ti.y, rows = ti.z;
-      int r0, r1;
-      tile_row_bases<WHICH>(p, w.nt, r0, r1);
-      const int grow = tr < 64 ? r0 + tr : r1 + (tr - 64);   // weight row in the expert
-      const bool row_ok = swiglu ? (64 * w.nt + (tr & 63)) < p.inter : grow < N1;
-      float scale = 1.0f;
-      if (SCALE == SCALE_CHANNEL && row_ok)
-        scale = bf16_bits_to_float(p.scales[static_cast<int64_t>(e) * N1 + grow]);
-      const int b = jc & 1;
+      const int nvalid = min(NT, p.n_tiles - w.grp * NT);
+      const int b = acc_bufs == 2 ? (jc & 1) : 0;
+      const uint32_t acc_par = acc_bufs == 2 ? ((jc >> 1) & 1) : (jc & 1);
       if (has_k) {
-        if (!mbar_wait(&accfull[b], (jc >> 1) & 1, abort_flag, p.err)) {
+        if (!warp_wait(&accfull[b], acc_par, abort_flag, p.err, wait_ns)) {
           ok = false;
           break;
         }
         tc_fence_after();
       }
-      const uint32_t acc_col = kAccCol0 + b * bn;
-      // intermediate column of this lane (SwiGLU: gate/up pair index)
-      const int icol = swiglu ? 64 * w.nt + 16 * q + (lane & 15) : grow;
-      for (int c0 = 0; c0 < rows; c0 += 16) {
-        float v[16];
-        if (has_k) {
-          tmem_ld16(t_lane + acc_col + c0, v);
-          tmem_wait_ld();
-        } else {
+      for (int t = 0; t < nvalid && ok; ++t) {
+        const int nt = w.grp * NT + t;
+        int r0, r1;
+        tile_row_bases<WHICH>(p, nt, r0, r1);
+        const int grow = tr < 64 ? r0 + tr : r1 + (tr - 64);   // weight row in the expert
+        const bool row_ok = swiglu ? (64 * nt + (tr & 63)) < p.inter : grow < N1;
+        float scale = 1.0f;
+        if (SCALE == SCALE_CHANNEL && row_ok)
+          scale = bf16_bits_to_float(p.scales[static_cast<int64_t>(e) * N1 + grow]);
+        const uint32_t acc_col = acc_col0 + (b * NT + t) * bn;
+        // intermediate column of this lane (SwiGLU: gate/up pair index)
+        const int icol = swiglu ? 64 * nt + 16 * q + (lane & 15) : grow;
+        // down GEMM: TMEM loads run one 16-route chunk ahead of the conversion
+        // and stores (the gate/up epilogue is not on the critical path and
+        // keeps its registers for the activation)
+        float vn[16];
+        if (WHICH == GEMM_DOWN && has_k && rows > 0) tmem_ld16(t_lane + acc_col, vn);
+        for (int c0 = 0; c0 < rows; c0 += 16) {
+          float v[16];
+          if (has_k && WHICH == GEMM_DOWN) {
+            tmem_wait_ld(vn);
 #pragma unroll
-          for (int j = 0; j < 16; ++j) v[j] = 0.0f;
-        }
-#pragma unroll
-        for (int j = 0; j < 16; ++j) v[j] *= scale;
-        if (WHICH == GEMM_DOWN) {
-          // This warp's 32 output columns x 16 slots through a staging buffer
-          // (slot-major, conflict-free) and one TMA store, in the activation
-          // dtype (one rounding) or as FP32 split partials.  Slots past the
-          // tile's valid rows are padding slots of y, never read.
-          float* stg = epi_stage + (q * 2 + sbuf) * (16 * 32);
-          if (lane == 0) bulk_wait_read<1>();  // the store that last read this buffer
-          __syncwarp();
-          if (p.out16) {
-            uint16_t* stg16 = reinterpret_cast<uint16_t*>(stg);
-#pragma unroll
-            for (int j = 0; j < 16; ++j) stg16[j * 32 + lane] = T::from_float(v[j]);
+            for (int j = 0; j < 16; ++j) v[j] = vn[j];
+            if (c0 + 16 < rows) tmem_ld16(t_lane + acc_col + c0 + 16, vn);
+          } else if (has_k) {
+            tmem_ld16(t_lane + acc_col + c0, v);
+            tmem_wait_ld(v);
           } else {
 #pragma unroll
-            for (int j = 0; j < 16; ++j) stg[j * 32 + lane] = v[j];
+            for (int j = 0; j < 16; ++j) v[j] = 0.0f;
           }
-          fence_proxy_async_smem();
-          __syncwarp();
-          const int col0 = grow - lane;
-          if (lane == 0 && col0 < p.out_cols) {
-            tma_store_2d(&tmC, stg, col0, static_cast<int>(w.split * p.slots_cap) + m0 + c0);
-            bulk_commit();
-          }
-          sbuf ^= 1;
-        } else if (p.splits > 1) {
-          float* part = p.part + (static_cast<int64_t>(w.split) * p.slots_cap + m0) * N1 + grow;
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int r = c0 + j;
-            if (r < rows && row_ok) part[static_cast<int64_t>(r) * N1] = v[j];
-          }
-        } else {
-          uint16_t* inter = reinterpret_cast<uint16_t*>(p.out) + static_cast<int64_t>(m0) * p.inter;
+          for (int j = 0; j < 16; ++j) v[j] *= scale;
+          if (WHICH == GEMM_DOWN) {
+            // This warp's 32 output columns x 16 slots through a staging buffer
+            // (slot-major, conflict-free) and one TMA store, in the activation
+            // dtype (one rounding) or as FP32 split partials.  Slots past the
+            // tile's valid rows are padding slots of y, never read.
+            float* stg = epi_stage + (q * 2 + sbuf) * (16 * 32);
+            if (lane == 0) bulk_wait_read<1>();  // the store that last read this buffer
+            __syncwarp();
+            if (p.out16) {
+              uint16_t* stg16 = reinterpret_cast<uint16_t*>(stg);
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int r = c0 + j;
-            if (swiglu) {
-              const float other = __shfl_xor_sync(0xFFFFFFFFu, v[j], 16);
-              if ((j & 1) == (lane >> 4) && r < rows && row_ok) {
-                const float g = (lane < 16) ? v[j] : other;
-                const float up = (lane < 16) ? other : v[j];
-                inter[static_cast<int64_t>(r) * p.inter + icol] = T::from_float(silu_f(g) * up);
+              for (int j = 0; j < 16; ++j) stg16[j * 32 + lane] = T::from_float(v[j]);
+            } else {
+#pragma unroll
+              for (int j = 0; j < 16; ++j) stg[j * 32 + lane] = v[j];
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            const int col0 = grow - lane;
+            if (lane == 0 && col0 < p.out_cols) {
+              tma_store_2d(&tmC, stg, col0, static_cast<int>(w.split * p.slots_cap) + m0 + c0);
+              bulk_commit();
+            }
+            sbuf ^= 1;
+          } else if (p.splits > 1) {
+            float* part = p.part + (static_cast<int64_t>(w.split) * p.slots_cap + m0) * N1 + grow;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const int r = c0 + j;
+              if (r < rows && row_ok) part[static_cast<int64_t>(r) * N1] = v[j];
+            }
+          } else {
+            uint16_t* inter = reinterpret_cast<uint16_t*>(p.out) + static_cast<int64_t>(m0) * p.inter;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const int r = c0 + j;
+              if (swiglu) {
+                const float other = __shfl_xor_sync(0xFFFFFFFFu, v[j], 16);
+                if ((j & 1) == (lane >> 4) && r < rows && row_ok) {
+                  const float g = (lane < 16) ? v[j] : other;
+                  const float up = (lane < 16) ? other : v[j];
+                  inter[static_cast<int64_t>(r) * p.inter + icol] = T::from_float(silu_f(g) * up);
+                }
+              } else if (r < rows && row_ok) {
+                const float hh = v[j] > 0.0f ? v[j] : 0.0f;
+                inter[static_cast<int64_t>(r) * p.inter + icol] = T::from_float(hh * hh);
               }
-            } else if (r < rows && row_ok) {
-              const float h = v[j] > 0.0f ? v[j] : 0.0f;
-              inter[static_cast<int64_t>(r) * p.inter + icol] = T::from_float(h * h);
             }
           }
         }
+        if (WHICH == GEMM_UP && p.splits > 1) {
+          // Split-K fix-up: the last split to finish sums all partials in split
+          // order (deterministic) and applies the activation.
+          __threadfence();
+          if (!epi_sync()) {
+            ok = false;
+            break;
+          }
+          if (epi_tid == 0) {
+            const int prev = atomicAdd(&p.counters[w.tile * p.n_tiles + nt], 1);
+            *fixup_flag = (prev == p.splits - 1) ? 1 : 0;
+          }
+          if (!epi_sync()) {
+            ok = false;
+            break;
+          }
+          if (*fixup_flag) {
+            __threadfence();
+            uint16_t* inter = reinterpret_cast<uint16_t*>(p.out) + static_cast<int64_t>(m0) * p.inter;
+            for (int c0 = 0; c0 < rows; c0 += 16) {
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                const int r = c0 + j;
+                float hs = 0.0f;
+                if (r < rows && row_ok) {
+                  const float* src = p.part + static_cast<int64_t>(m0 + r) * N1 + grow;
+                  for (int s = 0; s < p.splits; ++s) hs += __ldcg(src + static_cast<int64_t>(s) * p.slots_cap * N1);
+                }
+                if (swiglu) {
+                  const float other = __shfl_xor_sync(0xFFFFFFFFu, hs, 16);
+                  if ((j & 1) == (lane >> 4) && r < rows && row_ok) {
+                    const float g = (lane < 16) ? hs : other;
+                    const float up = (lane < 16) ? other : hs;
+                    inter[static_cast<int64_t>(r) * p.inter + icol] = T::from_float(silu_f(g) * up);
+                  }
+                } else if (r < rows && row_ok) {
+                  const float a = hs > 0.0f ? hs : 0.0f;
+                  inter[static_cast<int64_t>(r) * p.inter + icol] = T::from_float(a * a);
+                }
+              }
+            }
+            // the flag is rewritten only after the next two barriers
+            if (epi_tid == 0) p.counters[w.tile * p.n_tiles + nt] = 0;
+          }
+        }
       }
+      if (!ok) break;
       if (has_k) {
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&accempty[b]);
         ++jc;
       }
-      if (WHICH == GEMM_UP && p.splits > 1) {
-        // Split-K fix-up: the last split to finish sums all partials in split
-        // order (deterministic) and applies the activation.
-        __threadfence();
-        if (!epi_sync()) {
-          ok = false;
-          break;
-        }
-        if (epi_tid == 0) {
-          const int prev = atomicAdd(&p.counters[w.tile * p.n_tiles + w.nt], 1);
-          *fixup_flag = (prev == p.splits - 1) ? 1 : 0;
-        }
-        if (!epi_sync()) {
-          ok = false;
-          break;
-        }
-        if (*fixup_flag) {
-          __threadfence();
-          uint16_t* inter = reinterpret_cast<uint16_t*>(p.out) + static_cast<int64_t>(m0) * p.inter;
-          for (int c0 = 0; c0 < rows; c0 += 16) {
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const int r = c0 + j;
-              float h = 0.0f;
-              if (r < rows && row_ok) {
-                const float* src = p.part + static_cast<int64_t>(m0 + r) * N1 + grow;
-                for (int s = 0; s < p.splits; ++s) h += __ldcg(src + static_cast<int64_t>(s) * p.slots_cap * N1);
-              }
-              if (swiglu) {
-                const float other = __shfl_xor_sync(0xFFFFFFFFu, h, 16);
-                if ((j & 1) == (lane >> 4) && r < rows && row_ok) {
-                  const float g = (lane < 16) ? h : other;
-                  const float up = (lane < 16) ? other : h;
-                  inter[static_cast<int64_t>(r) * p.inter + icol] = T::from_float(silu_f(g) * up);
-                }
-              } else if (r < rows && row_ok) {
-                const float a = h > 0.0f ? h : 0.0f;
-                inter[static_cast<int64_t>(r) * p.inter + icol] = T::from_float(a * a);
-              }
-            }
-          }
-          if (epi_tid == 0) p.counters[w.tile * p.n_tiles + w.nt] = 0;
-        }
-      }
     }
   }
 
   // ------------------------------------------------------------------ teardown
-  if (WHICH == GEMM_DOWN && warp >= 12 && lane == 0) bulk_wait_all();  // output stores done
+  if (WHICH == GEMM_DOWN && warp >= 4 + kGemmDqWarps && lane == 0) bulk_wait_all();  // output stores done
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
@@ -648,16 +843,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
 namespace w4a16 {
 
-template <int WHICH, int SCALE, int DT>
+template <int WHICH, int SCALE, int DT, int LAYOUT>
 cudaError_t launch_gemm_one(const GemmParams& p, const CUtensorMap& tmA, const CUtensorMap& tmB,
                             const CUtensorMap& tmC, const CUtensorMap& tmS, int grid, int smem_bytes,
                             cudaStream_t s, bool pdl) {
-  auto kern = w4a16_gemm_kernel<WHICH, SCALE, DT>;
+  auto kern = w4a16_gemm_kernel<WHICH, SCALE, DT, LAYOUT>;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   static int configured_for[64] = {0};
-  if (dev < 64 && configured_for[dev] < smem_bytes) {
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (configured_for[dev] < smem_bytes) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
     if (e != cudaSuccess) return e;
     configured_for[dev] = smem_bytes;
@@ -675,18 +871,18 @@ cudaError_t launch_gemm_one(const GemmParams& p, const CUtensorMap& tmA, const C
   return cudaLaunchKernelEx(&cfg, kern, p, tmA, tmB, tmC, tmS);
 }
 
-template <int DT>
+template <int DT, int LAYOUT>
 cudaError_t launch_gemm_dt(int which, int scale_kind, const GemmParams& p, const CUtensorMap& tmA,
                            const CUtensorMap& tmB, const CUtensorMap& tmC, const CUtensorMap& tmS,
                            int grid, int smem_bytes, cudaStream_t s, bool pdl) {
   if (which == GEMM_UP) {
     return scale_kind == SCALE_GROUP
-               ? launch_gemm_one<GEMM_UP, SCALE_GROUP, DT>(p, tmA, tmB, tmC, tmS, grid, smem_bytes, s, pdl)
-               : launch_gemm_one<GEMM_UP, SCALE_CHANNEL, DT>(p, tmA, tmB, tmC, tmS, grid, smem_bytes, s, pdl);
+               ? launch_gemm_one<GEMM_UP, SCALE_GROUP, DT, LAYOUT>(p, tmA, tmB, tmC, tmS, grid, smem_bytes, s, pdl)
+               : launch_gemm_one<GEMM_UP, SCALE_CHANNEL, DT, LAYOUT>(p, tmA, tmB, tmC, tmS, grid, smem_bytes, s, pdl);
   }
   return scale_kind == SCALE_GROUP
-             ? launch_gemm_one<GEMM_DOWN, SCALE_GROUP, DT>(p, tmA, tmB, tmC, tmS, grid, smem_bytes, s, pdl)
-             : launch_gemm_one<GEMM_DOWN, SCALE_CHANNEL, DT>(p, tmA, tmB, tmC, tmS, grid, smem_bytes, s, pdl);
+             ? launch_gemm_one<GEMM_DOWN, SCALE_GROUP, DT, LAYOUT>(p, tmA, tmB, tmC, tmS, grid, smem_bytes, s, pdl)
+             : launch_gemm_one<GEMM_DOWN, SCALE_CHANNEL, DT, LAYOUT>(p, tmA, tmB, tmC, tmS, grid, smem_bytes, s, pdl);
 }
 
 }  // namespace w4a16

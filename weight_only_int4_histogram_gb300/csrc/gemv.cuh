@@ -26,6 +26,10 @@
 //
 // A pipeline stage is 128 weight rows x kGemvBlockK (256) K values: 128 bytes
 // of every packed row per visit, read by TMA in 128-byte-swizzled boxes.
+// With the relaid-out weights (LAYOUT_IL, see common.cuh) every layout is
+// packed along K and each code pair holds consecutive K values, so the
+// activations feed the MMAs as stored (no byte permutes); per-channel weights
+// then take the group-scale data path without the group scales.
 //
 // Compute mapping: 16 warps = 8 row blocks (16 rows each) x 2 groups.
 //   * units of several stages: group h takes K half h of every stage; the
@@ -79,6 +83,11 @@ __device__ __forceinline__ int4 tile_of(const GemmParams& p, const int4* tab, in
   return i < kGemvTileTab ? tab[i] : load_tile(p, u);
 }
 
+// One unit of the CUDA-core path: (route tile, 128-row weight tile nt, K split).
+struct GvUnit {
+  int tile, nt, split, kb0, kb1;
+};
+
 // Iterates this CTA's units u = blockIdx.x + i * gridDim.x, keeping the
 // (split, weight tile, route tile) digits of u up to date with carries instead
 // of divisions.
@@ -112,8 +121,8 @@ struct UnitIter {
     }
     tile += dtile + c;
   }
-  __device__ __forceinline__ Unit unit(const GemmParams& p) const {
-    Unit w;
+  __device__ __forceinline__ GvUnit unit(const GemmParams& p) const {
+    GvUnit w;
     w.split = split;
     w.nt = nt;
     w.tile = tile;
@@ -179,16 +188,18 @@ __device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t& r0, uint32_
 //   per-channel (row-pair packed, one byte per K, even row in the low nibble):
 //     lane t takes 16-byte chunks t and t + 4 of each K half; word i of a chunk
 //     (4 K) gives (k0, k2) and (k1, k3) for one MMA.
-template <int SCALE, int DT, int NB, bool FULLK>
+template <int SCALE, int DT, int LAYOUT, int NB, bool FULLK>
 __device__ __forceinline__ void gemv_stage(const uint8_t* sA, int rowA, int rowB, int kh, int lane,
                                            uint32_t ld_row_off, int ld_row7, int ld_chunk, float (&tot)[4 * NB]) {
   const int g = lane >> 2, t = lane & 3;
   const uint8_t* sX = sA + kGvOffX + g * kGvRouteBytes;  // this lane's B column in block 0 (route g)
-  if (SCALE == SCALE_GROUP) {
+  if (SCALE == SCALE_GROUP || LAYOUT == LAYOUT_IL) {
+    constexpr bool kScaled = SCALE == SCALE_GROUP;
     // BF16 scales of the groups this warp handles, two per word: word pp holds
     // the groups of ldmatrix step pp
-    uint32_t saw[4], sbw[4];
-    if (FULLK) {
+    uint32_t saw[4] = {0u, 0u, 0u, 0u}, sbw[4] = {0u, 0u, 0u, 0u};
+    if (!kScaled) {
+    } else if (FULLK) {
       const uint4 sa = *reinterpret_cast<const uint4*>(sA + kGvOffS + rowA * kGvScaleRowBytes);
       const uint4 sb = *reinterpret_cast<const uint4*>(sA + kGvOffS + rowB * kGvScaleRowBytes);
       saw[0] = sa.x; saw[1] = sa.y; saw[2] = sa.z; saw[3] = sa.w;
@@ -220,18 +231,27 @@ __device__ __forceinline__ void gemv_stage(const uint8_t* sA, int rowA, int rowB
         const float fb = __uint_as_float(q ? (sbw[pp] & 0xFFFF0000u) : (sbw[pp] << 16));
 #pragma unroll
         for (int n = 0; n < NB; ++n) {
-          // activations K 32c + 8t .. + 7 of route 8n + g: (x0 x1) (x2 x3) (x4 x5)
-          // (x6 x7), paired as the codes: (x0 x4) (x1 x5) | (x2 x6) (x3 x7)
+          // activations K 32c + 8t .. + 7 of route 8n + g: (x0 x1) (x2 x3) (x4 x5) (x6 x7)
           const uint4 xv = *reinterpret_cast<const uint4*>(sX + n * 8 * kGvRouteBytes + (4 * c + t) * 16);
-          float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-          mma_16816<DT>(d[0], d[1], d[2], d[3], a0, a1, a2, a3, __byte_perm(xv.x, xv.z, 0x5410),
-                        __byte_perm(xv.x, xv.z, 0x7632));
-          mma_16816<DT>(d[0], d[1], d[2], d[3], a4, a5, a6, a7, __byte_perm(xv.y, xv.w, 0x5410),
-                        __byte_perm(xv.y, xv.w, 0x7632));
-          tot[4 * n + 0] = fmaf(fa, d[0], tot[4 * n + 0]);
-          tot[4 * n + 1] = fmaf(fa, d[1], tot[4 * n + 1]);
-          tot[4 * n + 2] = fmaf(fb, d[2], tot[4 * n + 2]);
-          tot[4 * n + 3] = fmaf(fb, d[3], tot[4 * n + 3]);
+          // B pairs in the codes' K order: CANON codes pair (k0 k4) (k1 k5) | (k2 k6) (k3 k7),
+          // IL codes pair (k0 k1) (k2 k3) | (k4 k5) (k6 k7), i.e. the words as stored
+          const uint32_t b0 = LAYOUT == LAYOUT_IL ? xv.x : __byte_perm(xv.x, xv.z, 0x5410);
+          const uint32_t b1 = LAYOUT == LAYOUT_IL ? xv.y : __byte_perm(xv.x, xv.z, 0x7632);
+          const uint32_t b2 = LAYOUT == LAYOUT_IL ? xv.z : __byte_perm(xv.y, xv.w, 0x5410);
+          const uint32_t b3 = LAYOUT == LAYOUT_IL ? xv.w : __byte_perm(xv.y, xv.w, 0x7632);
+          if (kScaled) {
+            float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+            mma_16816<DT>(d[0], d[1], d[2], d[3], a0, a1, a2, a3, b0, b1);
+            mma_16816<DT>(d[0], d[1], d[2], d[3], a4, a5, a6, a7, b2, b3);
+            tot[4 * n + 0] = fmaf(fa, d[0], tot[4 * n + 0]);
+            tot[4 * n + 1] = fmaf(fa, d[1], tot[4 * n + 1]);
+            tot[4 * n + 2] = fmaf(fb, d[2], tot[4 * n + 2]);
+            tot[4 * n + 3] = fmaf(fb, d[3], tot[4 * n + 3]);
+          } else {
+            // exact codes: the per-channel scale multiplies the total in the epilogue
+            mma_16816<DT>(tot[4 * n + 0], tot[4 * n + 1], tot[4 * n + 2], tot[4 * n + 3], a0, a1, a2, a3, b0, b1);
+            mma_16816<DT>(tot[4 * n + 0], tot[4 * n + 1], tot[4 * n + 2], tot[4 * n + 3], a4, a5, a6, a7, b2, b3);
+          }
         }
       }
     }
@@ -282,7 +302,7 @@ __device__ __forceinline__ void gemv_stage(const uint8_t* sA, int rowA, int rowB
 // and store, every warp takes part in the split-K barriers.
 template <int WHICH, int SCALE, int DT, int NB>
 __device__ __forceinline__ bool gemv_epilogue(const GemmParams& p, uint64_t* epibar, volatile int* abort_flag,
-                                              volatile int* fixup_flag, const Unit& w, int e, int m0, int rows,
+                                              volatile int* fixup_flag, const GvUnit& w, int e, int m0, int rows,
                                               int rowA, int rowB, int rb, int lane, bool fin, uint32_t& eph,
                                               const float (&tot)[4 * NB]) {
   using T = F16<DT>;
@@ -304,7 +324,7 @@ __device__ __forceinline__ bool gemv_epilogue(const GemmParams& p, uint64_t* epi
   auto grp_sync = [&]() -> bool {
     __syncwarp();
     if (lane == 0) mbar_arrive(epibar);
-    const bool ok = mbar_wait(epibar, eph & 1, abort_flag, p.err);
+    const bool ok = warp_wait(epibar, eph & 1, abort_flag, p.err, p.wait_ns);
     ++eph;
     return ok;
   };
@@ -432,10 +452,10 @@ __device__ __forceinline__ bool gemv_epilogue(const GemmParams& p, uint64_t* epi
 // are then its only consumers.  Parity waits therefore never see a slot more
 // than one phase away, and the producer refills a slot only after all of its
 // consumers left it.
-template <int WHICH, int SCALE, int DT, int NB>
+template <int WHICH, int SCALE, int DT, int LAYOUT, int NB>
 __device__ __forceinline__ bool gemv_unit(const GemmParams& p, uint8_t* smem, uint64_t* full, uint64_t* bfull,
                                           uint64_t* empty, uint64_t* epibar, volatile int* abort_flag,
-                                          volatile int* fixup_flag, float* red, const Unit& w, const int4& ti,
+                                          volatile int* fixup_flag, float* red, const GvUnit& w, const int4& ti,
                                           bool alt, int grp, int rowA, int rowB, int rb, int lane,
                                           uint32_t ld_row_off, int ld_row7, int ld_chunk, int ring0, int ring_len,
                                           int& st, uint32_t& ph, uint32_t& eph) {
@@ -444,11 +464,12 @@ __device__ __forceinline__ bool gemv_unit(const GemmParams& p, uint8_t* smem, ui
   for (int j = 0; j < 4 * NB; ++j) tot[j] = 0.0f;
   for (int kb = w.kb0; kb < w.kb1; ++kb) {
     const int slot = ring0 + st;
-    if (!mbar_wait(&full[slot], ph, abort_flag, p.err) || !mbar_wait(&bfull[slot], ph, abort_flag, p.err))
+    if (!warp_wait(&full[slot], ph, abort_flag, p.err, p.wait_ns) ||
+        !warp_wait(&bfull[slot], ph, abort_flag, p.err, p.wait_ns))
       return false;
     const uint8_t* sA = smem + slot * p.stage_bytes;
-    if (alt) gemv_stage<SCALE, DT, NB, true>(sA, rowA, rowB, grp, lane, ld_row_off, ld_row7, ld_chunk, tot);
-    else gemv_stage<SCALE, DT, NB, false>(sA, rowA, rowB, grp, lane, ld_row_off, ld_row7, ld_chunk, tot);
+    if (alt) gemv_stage<SCALE, DT, LAYOUT, NB, true>(sA, rowA, rowB, grp, lane, ld_row_off, ld_row7, ld_chunk, tot);
+    else gemv_stage<SCALE, DT, LAYOUT, NB, false>(sA, rowA, rowB, grp, lane, ld_row_off, ld_row7, ld_chunk, tot);
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[slot]);
     ring_next(st, ph, ring_len);
@@ -466,7 +487,7 @@ __device__ __forceinline__ bool gemv_unit(const GemmParams& p, uint8_t* smem, ui
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(epibar);
-    if (!mbar_wait(epibar, eph & 1, abort_flag, p.err)) return false;
+    if (!warp_wait(epibar, eph & 1, abort_flag, p.err, p.wait_ns)) return false;
     ++eph;
     fin = grp == 0;
     if (fin) {
@@ -484,7 +505,7 @@ __device__ __forceinline__ bool gemv_unit(const GemmParams& p, uint8_t* smem, ui
                                              min(ti.z, kGemvMaxR), rowA, rowB, rb, lane, fin, eph, tot);
 }
 
-template <int WHICH, int SCALE, int DT>
+template <int WHICH, int SCALE, int DT, int LAYOUT>
 __global__ void __launch_bounds__(kGemvThreads, 1)
     w4a16_gemv_kernel(const __grid_constant__ GemmParams p, const __grid_constant__ CUtensorMap tmA,
                       const __grid_constant__ CUtensorMap tmS) {
@@ -555,7 +576,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
     UnitIter it;
     it.init(p);
     for (int i = 0; it.u < n_units && ok; it.next(p), ++i) {
-      const Unit w = it.unit(p);
+      const GvUnit w = it.unit(p);
       const int4 ti = tile_of(p, tile_tab, i, it.u);
       if (w.kb1 <= w.kb0) continue;
       const int e = ti.x;
@@ -566,7 +587,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
       uint32_t ph = ring ? ph_r1 : ph_r0;
       for (int kb = w.kb0; kb < w.kb1; ++kb) {
         const int slot = ring * ring_len + st;
-        if (!mbar_wait(&empty[slot], ph ^ 1u, abort_flag, p.err)) {
+        if (!warp_wait(&empty[slot], ph ^ 1u, abort_flag, p.err, p.wait_ns)) {
           ok = false;
           break;
         }
@@ -597,7 +618,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
         __syncwarp();
         if (lane == 0) {
           mbar_arrive_expect_tx(&full[slot], kGvWeightBytes + (stma ? kTileRows * kGvScaleRowBytes : 0));
-          if (SCALE == SCALE_GROUP) {
+          if (SCALE == SCALE_GROUP || LAYOUT == LAYOUT_IL) {
             // two 64-row boxes of 128 packed bytes (256 K values)
             tma_load_3d(sA, &tmA, &full[slot], kb * (kGemvBlockK / 2), r0, e, pol_w);
             tma_load_3d(sA + 8192, &tmA, &full[slot], kb * (kGemvBlockK / 2), r1, e, pol_w);
@@ -668,7 +689,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
     it.init(p);
     for (int i = 0; it.u < n_units && ok; it.next(p), ++i) {
       const int u = it.u;
-      const Unit w = it.unit(p);
+      const GvUnit w = it.unit(p);
       const int4 ti = tile_of(p, tile_tab, i, u);
       const int src = src_next;
       const int rows = min(ti.z, kGemvMaxR);
@@ -677,7 +698,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
       uint32_t ph = ring ? ph_r1 : ph_r0;
       for (int kb = w.kb0; kb < w.kb1; ++kb) {
         const int slot = ring * ring_len + st;
-        if (!mbar_wait(&empty[slot], ph ^ 1u, abort_flag, p.err)) {
+        if (!warp_wait(&empty[slot], ph ^ 1u, abort_flag, p.err, p.wait_ns)) {
           ok = false;
           break;
         }
@@ -728,12 +749,12 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
     const int ring0 = alt ? grp * ring_len : 0;
     for (int i = 0; it.u < n_units; it.next(p), ++i) {
       if (alt && (i & 1) != grp) continue;  // the other group's unit, on the other ring
-      const Unit w = it.unit(p);
+      const GvUnit w = it.unit(p);
       const int4 ti = tile_of(p, tile_tab, i, it.u);
       const int nb = (min(ti.z, kGemvMaxR) + 7) >> 3;
       bool ok;
 #define W4A16_GEMV_UNIT(NBV)                                                                                    \
-  gemv_unit<WHICH, SCALE, DT, NBV>(p, smem, full, bfull, empty, epibar, abort_flag, fixup_flag, red, w, ti, alt, \
+  gemv_unit<WHICH, SCALE, DT, LAYOUT, NBV>(p, smem, full, bfull, empty, epibar, abort_flag, fixup_flag, red, w, ti, alt, \
                                    grp, rowA, rowB, rb, lane, ld_row_off, ld_row7, ld_chunk, ring0, ring_len, st, \
                                    ph, eph)
       if (nb <= 1) ok = W4A16_GEMV_UNIT(1);
@@ -746,15 +767,16 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
   __syncthreads();
 }
 
-template <int WHICH, int SCALE, int DT>
+template <int WHICH, int SCALE, int DT, int LAYOUT>
 cudaError_t launch_gemv_one(const GemmParams& p, const CUtensorMap& tmA, const CUtensorMap& tmS, int grid,
                             int smem_bytes, cudaStream_t s, bool pdl) {
-  auto kern = w4a16_gemv_kernel<WHICH, SCALE, DT>;
+  auto kern = w4a16_gemv_kernel<WHICH, SCALE, DT, LAYOUT>;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   static int configured_for[64] = {0};
-  if (dev < 64 && configured_for[dev] < smem_bytes) {
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (configured_for[dev] < smem_bytes) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
     if (e != cudaSuccess) return e;
     configured_for[dev] = smem_bytes;
@@ -772,17 +794,17 @@ cudaError_t launch_gemv_one(const GemmParams& p, const CUtensorMap& tmA, const C
   return cudaLaunchKernelEx(&cfg, kern, p, tmA, tmS);
 }
 
-template <int DT>
+template <int DT, int LAYOUT>
 cudaError_t launch_gemv_dt(int which, int scale_kind, const GemmParams& p, const CUtensorMap& tmA,
                            const CUtensorMap& tmS, int grid, int smem_bytes, cudaStream_t s, bool pdl) {
   if (which == GEMM_UP) {
     return scale_kind == SCALE_GROUP
-               ? launch_gemv_one<GEMM_UP, SCALE_GROUP, DT>(p, tmA, tmS, grid, smem_bytes, s, pdl)
-               : launch_gemv_one<GEMM_UP, SCALE_CHANNEL, DT>(p, tmA, tmS, grid, smem_bytes, s, pdl);
+               ? launch_gemv_one<GEMM_UP, SCALE_GROUP, DT, LAYOUT>(p, tmA, tmS, grid, smem_bytes, s, pdl)
+               : launch_gemv_one<GEMM_UP, SCALE_CHANNEL, DT, LAYOUT>(p, tmA, tmS, grid, smem_bytes, s, pdl);
   }
   return scale_kind == SCALE_GROUP
-             ? launch_gemv_one<GEMM_DOWN, SCALE_GROUP, DT>(p, tmA, tmS, grid, smem_bytes, s, pdl)
-             : launch_gemv_one<GEMM_DOWN, SCALE_CHANNEL, DT>(p, tmA, tmS, grid, smem_bytes, s, pdl);
+             ? launch_gemv_one<GEMM_DOWN, SCALE_GROUP, DT, LAYOUT>(p, tmA, tmS, grid, smem_bytes, s, pdl)
+             : launch_gemv_one<GEMM_DOWN, SCALE_CHANNEL, DT, LAYOUT>(p, tmA, tmS, grid, smem_bytes, s, pdl);
 }
 
 }  // namespace w4a16

@@ -1,7 +1,7 @@
-// FP16-activation instantiations of the grouped W4A16 GEMV (CUDA cores).
+// FP16-activation instantiations of the grouped W4A16 GEMV (CUDA cores), checkpoint-layout weights.
 #include "gemv.cuh"
 
 namespace w4a16 {
-template cudaError_t launch_gemv_dt<DT_FP16>(int, int, const GemmParams&, const CUtensorMap&,
-                                               const CUtensorMap&, int, int, cudaStream_t, bool);
+template cudaError_t launch_gemv_dt<DT_FP16, LAYOUT_CANON>(int, int, const GemmParams&, const CUtensorMap&,
+                                                     const CUtensorMap&, int, int, cudaStream_t, bool);
 }

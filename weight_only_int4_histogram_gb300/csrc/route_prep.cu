@@ -204,40 +204,6 @@ __global__ void __launch_bounds__(kRoutePrepThreads, 1) route_prep_kernel(const 
   }
 }
 
-// Activation rows in slot order for the tensor-core gate/up GEMM: every valid
-// flat route r copies token row x[r / k] to row inv[r] of xs, one warp per
-// route (16-byte vectors, H a multiple of 64), so that the GEMM reads its
-// activation operand as plain TMA tiles of consecutive slots.  Padding slots
-// are not written: their MMA columns are never read.
-__global__ void __launch_bounds__(kPermuteThreads) permute_rows_kernel(const PermuteParams p) {
-  pdl_wait();
-  pdl_launch_dependents();
-  const int lane = threadIdx.x & 31;
-  const int warps = gridDim.x * (kPermuteThreads / 32);
-  const int vecs = p.H / 8;  // 16-byte vectors per row
-  for (int r = blockIdx.x * (kPermuteThreads / 32) + (threadIdx.x >> 5); r < p.R; r += warps) {
-    const int slot = p.inv[r];
-    if (slot < 0) continue;
-    const uint4* src = reinterpret_cast<const uint4*>(p.x) + static_cast<int64_t>(r / p.k) * vecs;
-    uint4* dst = reinterpret_cast<uint4*>(p.xs) + static_cast<int64_t>(slot) * vecs;
-    for (int v = lane; v < vecs; v += 32) dst[v] = __ldg(src + v);
-  }
-}
-
-cudaError_t launch_permute(const PermuteParams& p, int grid, cudaStream_t s, bool pdl) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kPermuteThreads);
-  cfg.dynamicSmemBytes = 0;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, permute_rows_kernel, p);
-}
-
 // Masked-count layout ("feat(pytorch): add CuTeDSL W4A16 MoE backend"
 // (LMDeploy), section Modification: invalid routes and masked expert counts):
 // expert-major rows with a count per expert become single routes of weight 1
@@ -276,12 +242,18 @@ cudaError_t launch_masked_routes(const int32_t* counts, int32_t E, int32_t max_r
 }
 
 cudaError_t launch_route_prep(const RoutePrepParams& p, int smem_bytes, cudaStream_t s, bool pdl) {
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(route_prep_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+  // The shared-memory opt-in is a per-device function attribute: set it once
+  // for every device this process launches on (more than 48 KB is needed from
+  // about 350 experts on).
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  static bool configured_for[64] = {false};
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!configured_for[dev]) {
+    e = cudaFuncSetAttribute(route_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
     if (e != cudaSuccess) return e;
-    configured = true;
+    configured_for[dev] = true;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(1);
