@@ -202,7 +202,7 @@ Layout make_layout(const w4a16_moe_plan_s& P, int T) {
     int nt, ab;
     choose_nt(L.nt1, L.bn, 232448 - 3072, P.ov_nt1 ? P.ov_nt1 : kDefaultNT, L.kb1 <= kDoubleAccMaxKb, nt, ab);
     g1 = cdiv(L.nt1, nt);
-    choose_nt(L.nt2, L.bn, 232448 - 3072 - kEpiStageBytes, P.ov_nt2 ? P.ov_nt2 : kDefaultNT, L.kb2 <= kDoubleAccMaxKb,
+    choose_nt(L.nt2, L.bn, 232448 - 3072 - epi_stage_bytes(false), P.ov_nt2 ? P.ov_nt2 : kDefaultNT, L.kb2 <= kDoubleAccMaxKb,
               nt, ab);
     g2 = cdiv(L.nt2, nt);
   }
@@ -225,14 +225,15 @@ Layout make_layout(const w4a16_moe_plan_s& P, int T) {
     // (mbarriers, TMEM address, flags)
     const int smem_budget = 232448 - 3072;
     choose_nt(L.nt1, L.bn, smem_budget, P.ov_nt1 ? P.ov_nt1 : kDefaultNT, L.kbps1 <= kDoubleAccMaxKb, L.ntu1, L.acc1);
-    choose_nt(L.nt2, L.bn, smem_budget - kEpiStageBytes, P.ov_nt2 ? P.ov_nt2 : kDefaultNT, L.kbps2 <= kDoubleAccMaxKb,
+    const int epi_bytes = epi_stage_bytes(L.s2 == 1);  // 16-bit expert outputs unless split
+    choose_nt(L.nt2, L.bn, smem_budget - epi_bytes, P.ov_nt2 ? P.ov_nt2 : kDefaultNT, L.kbps2 <= kDoubleAccMaxKb,
               L.ntu2, L.acc2);
     L.stage_bytes = gemm_stage_bytes(L.ntu1, L.bn);
     L.stages = std::min(kMaxStages, smem_budget / L.stage_bytes);
     L.smem = 3072 + L.stages * L.stage_bytes;
     L.stage_bytes2 = gemm_stage_bytes(L.ntu2, L.bn);
-    L.stages2 = std::min(kMaxStages, (smem_budget - kEpiStageBytes) / L.stage_bytes2);
-    L.smem2 = 3072 + kEpiStageBytes + L.stages2 * L.stage_bytes2;
+    L.stages2 = std::min(kMaxStages, (smem_budget - epi_bytes) / L.stage_bytes2);
+    L.smem2 = 3072 + epi_bytes + L.stages2 * L.stage_bytes2;
   }
   const int64_t units1 = static_cast<int64_t>(L.tiles_cap) * cdiv(L.nt1, L.ntu1) * L.s1;
   const int64_t units2 = static_cast<int64_t>(L.tiles_cap) * cdiv(L.nt2, L.ntu2) * L.s2;

@@ -21,7 +21,8 @@ constexpr int kHalfK = kBlockK / 2;
 constexpr int kGroup = 32;           // group size of the group-wise scales
 constexpr int kGroupsPerStage = kBlockK / kGroup;
 constexpr int kMaxStages = 12;
-constexpr int kGemmThreads = 768;    // 24 warps: see the role map in gemm.cuh
+constexpr int kGemmThreads = 768;    // gate/up GEMM: 24 warps (see the role map in gemm.cuh)
+constexpr int kGemmThreadsDown = 896;  // down GEMM: 28 warps, two epilogue warp sets
 constexpr int kGemmDqWarps = 16;     // dequantising warps: 4 warpgroups
 constexpr int kQuarterK = kBlockK / 4;  // K values each dequant warpgroup handles per stage
 constexpr int kTmemCols = 512;
@@ -41,8 +42,9 @@ __host__ __device__ constexpr int gemm_stage_bytes(int nt, int bn) { return nt *
 constexpr int kStageA = kTileRows * kBlockK / 2;   // 16 KB packed INT4 per stage
 constexpr int kStageS = kTileRows * kGroupsPerStage * 2;  // 2 KB BF16 group scales per stage
 constexpr int kStageBRow = kBlockK * 2;            // bytes of one activation row per stage
-// Down-GEMM output staging: 4 epilogue warps x 2 buffers x (16 routes x 32 rows, up to FP32)
-constexpr int kEpiStageBytes = 4 * 2 * 16 * 32 * 4;
+// Down-GEMM output staging: 8 epilogue warps x 2 buffers x 16 routes x 32
+// rows of the output element (2 bytes, or 4 for FP32 split partials)
+__host__ __device__ constexpr int epi_stage_bytes(bool out16) { return 8 * 2 * 16 * 32 * (out16 ? 2 : 4); }
 
 // CUDA-core GEMV path (gemv.cuh): route tiles of at most kGemvMaxR routes,
 // pipeline stages of kGemvBlockK K values; the stage size (and so the number

@@ -38,7 +38,10 @@
 //   warps 4..19   four dequant warpgroups; warpgroup h dequantises K-quarter h
 //                 of every stage into columns 32 h .. 32 h + 31 of the stage's
 //                 TMEM A slot
-//   warps 20..23  epilogue (TMEM -> registers -> activation / scaling -> HBM)
+//   warps 20..23  epilogue (TMEM -> registers -> activation / scaling -> HBM);
+//   (24..27)      the down GEMM has a second epilogue set (its epilogue
+//                 stores every output element and would otherwise set the
+//                 pace); set s takes the unit's weight tiles t with t % 2 == s
 // A warp can reach only the TMEM lanes 32 (warp % 4) .. + 31, so dequant and
 // epilogue warp w handles weight-tile rows of lane quadrant w % 4.
 //
@@ -293,7 +296,7 @@ __device__ __forceinline__ void issue_slot(uint32_t d_tmem, int bn, uint32_t a0,
 }
 
 template <int WHICH, int SCALE, int DT, int LAYOUT>
-__global__ void __launch_bounds__(kGemmThreads, 1)
+__global__ void __launch_bounds__(WHICH == GEMM_DOWN ? kGemmThreadsDown : kGemmThreads, 1)
     w4a16_gemm_kernel(const __grid_constant__ GemmParams p, const __grid_constant__ CUtensorMap tmA,
                       const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmC,
                       const __grid_constant__ CUtensorMap tmS) {
@@ -319,10 +322,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   // 4 atoms] | NT scale tiles [kStageS each]
   const int off_b = NT * kStageA;
   const int off_s = off_b + bn * kStageBRow;
-  // down GEMM: output staging [4 warps][2][16 x 32] after the stages
+  // down GEMM: output staging [8 warps][2][16 x 32] after the stages
+  constexpr int kEpiWarps = WHICH == GEMM_DOWN ? 8 : 4;
   float* epi_stage = reinterpret_cast<float*>(smem + stages * p.stage_bytes);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + stages * p.stage_bytes +
-                                               (WHICH == GEMM_DOWN ? kEpiStageBytes : 0));
+                                               (WHICH == GEMM_DOWN ? epi_stage_bytes(p.out16 != 0) : 0));
   uint64_t* empty = full + kMaxStages;
   uint64_t* bfull = empty + kMaxStages;
   uint64_t* afull = bfull + kMaxStages;
@@ -351,7 +355,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&accfull[b], 1);
-      mbar_init(&accempty[b], 4);
+      mbar_init(&accempty[b], kEpiWarps);
     }
     mbar_init(drain, 1);
     mbar_init(epibar, 4);
@@ -659,6 +663,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   } else {
     // ------------------------------------------------------------------ epilogue
     const int q = warp & 3;
+    const int eset = (warp - (4 + kGemmDqWarps)) >> 2;  // epilogue set: tiles t % 2 == eset (down GEMM)
+    const int esets = kEpiWarps / 4;
     const int tr = tile_row_of_lane<WHICH>(p, q * 32 + lane);
     const uint32_t t_lane = tmem + (static_cast<uint32_t>(q * 32) << 16);
     const int epi_tid = threadIdx.x - (4 + kGemmDqWarps) * 32;
@@ -691,7 +697,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
         tc_fence_after();
       }
-      for (int t = 0; t < nvalid && ok; ++t) {
+      for (int t = eset; t < nvalid && ok; t += esets) {
         const int nt = w.grp * NT + t;
         int r0, r1;
         tile_row_bases<WHICH>(p, nt, r0, r1);
@@ -729,7 +735,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             // (slot-major, conflict-free) and one TMA store, in the activation
             // dtype (one rounding) or as FP32 split partials.  Slots past the
             // tile's valid rows are padding slots of y, never read.
-            float* stg = epi_stage + (q * 2 + sbuf) * (16 * 32);
+            // buffers of 16 x 32 output elements: 1 KB (16-bit) or 2 KB (FP32)
+            float* stg = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(epi_stage) +
+                                                  ((eset * 4 + q) * 2 + sbuf) * (16 * 32 * (p.out16 ? 2 : 4)));
             if (lane == 0) bulk_wait_read<1>();  // the store that last read this buffer
             __syncwarp();
             if (p.out16) {
@@ -860,7 +868,7 @@ cudaError_t launch_gemm_one(const GemmParams& p, const CUtensorMap& tmA, const C
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kGemmThreads);
+  cfg.blockDim = dim3(WHICH == GEMM_DOWN ? kGemmThreadsDown : kGemmThreads);
   cfg.dynamicSmemBytes = smem_bytes;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
