@@ -292,6 +292,30 @@ w4a16_status w4a16_moe_route_topk(const float* logits, int32_t num_tokens, int32
                                   int32_t* topk_ids, float* topk_weights, void* stream);
 
 /*
+ * w4a16_moe_route_and_prepare -- the router step and route preparation in one
+ * pass: for every token, softmax over its router logits and its top_k experts
+ * (exactly as w4a16_moe_route_topk), written to topk_ids / topk_weights, and
+ * the route layout of those ids (exactly as w4a16_moe_prepare_routes) left in
+ * the workspace for a following w4a16_moe_forward with the same ids and
+ * weights.  The router's per-CTA expert counts feed the layout directly, so
+ * the two steps take two kernels instead of three.  Passage: "feat(pytorch):
+ * add CuTeDSL W4A16 MoE backend" (LMDeploy), section Benchmark (routes from a
+ * router score / top-k step, then route preparation).
+ *   logits        [num_tokens, num_global] FP32 (device); num_global = experts
+ *                 of the whole model, 1..1024, >= the plan's top_k
+ *   topk_ids      [num_tokens, top_k] int32 out (device, global ids)
+ *   topk_weights  [num_tokens, top_k] FP32 out (device, softmax probabilities)
+ *   workspace     the plan's workspace
+ * Asynchronous on `stream`, no allocation, CUDA-graph capturable;
+ * num_tokens == 0 is a no-op.  Errors: W4A16_ERR_INVALID_ARG (NULL or
+ * misaligned pointers, num_tokens out of range), W4A16_ERR_UNSUPPORTED
+ * (num_global out of range), W4A16_ERR_CUDA (launch failure).
+ */
+w4a16_status w4a16_moe_route_and_prepare(w4a16_moe_plan_t plan, int32_t num_tokens, const float* logits,
+                                         int32_t num_global, int32_t* topk_ids, float* topk_weights, void* workspace,
+                                         void* stream);
+
+/*
  * w4a16_moe_relayout_weights -- plan-time relayout of one packed weight tensor
  * into W4A16_LAYOUT_INTERLEAVED, the order the GEMM kernels dequantise with
  * shifts and masks alone (no byte permutes).  Passages: "feat(pytorch): add

@@ -78,3 +78,39 @@ def test_router_then_forward_matches_generator_routes():
     out = moe(x, w, tw, ids)
     torch.cuda.synchronize()
     compare(out, oracle_rows(cfg, w, x, ids, tw), "router -> forward")
+
+
+@pytest.mark.parametrize("name,T", [("kimi_tp8_e384_h7168_i256_k8", 1), ("kimi_tp8_e384_h7168_i256_k8", 33),
+                                    ("kimi_tp8_e384_h7168_i256_k8", 2048),
+                                    ("deepseek_local_e32of256_h7168_i2048_k8", 512),
+                                    ("relu2_skew_e64_h2688_i1856_k6", 4096), ("tiny_e8_h256_i384_k2", 16)])
+def test_route_and_prepare_matches_router_then_prepare(name, T):
+    """The fused router + route preparation gives the router's ids and
+    weights bit for bit and the oracle's route layout bit for bit."""
+    cfg = gen.CONFIGS[name]
+    logits = gen.make_logits(cfg, T, "cuda")
+    moe = make_moe(cfg, T)
+    ids, w = moe.route_and_prepare(logits)
+    torch.cuda.synchronize()
+    rid, rw = W.route_topk(logits, cfg.top_k)
+    torch.cuda.synchronize()
+    assert torch.equal(ids, rid)
+    assert torch.equal(w.view(torch.int32), rw.view(torch.int32))
+    got = moe.read_route_layout(T)
+    want = oracle.prepare_routes(cfg, ids.cpu(), got["tile_rows"])
+    for key in ("counts", "offs", "perm", "inv", "tiles"):
+        np.testing.assert_array_equal(got[key].numpy(), want[key], err_msg=key)
+
+
+def test_route_and_prepare_then_forward():
+    cfg = small_cfg(E=16, H=512, I=256, k=4, expert_offset=16)
+    T = 70
+    w = gen.make_weights(cfg, "cuda")
+    x = gen.make_activations(cfg, T, "cuda")
+    logits = torch.randn(T, 64, device="cuda", generator=torch.Generator(device="cuda").manual_seed(7))
+    moe = make_moe(cfg, T)
+    ids, tw = moe.route_and_prepare(logits)
+    out = moe.forward(x, w, tw, ids)
+    torch.cuda.synchronize()
+    moe.check_device_error()
+    compare(out, oracle_rows(cfg, w, x, ids, tw), "route_and_prepare + forward")

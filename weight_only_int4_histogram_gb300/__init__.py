@@ -16,7 +16,8 @@ from ._lib import (Desc, RouteInfo, W4A16Error, w4a16_moe_check_device_error,  #
                    w4a16_moe_forward, w4a16_moe_forward_host, w4a16_moe_plan,
                    w4a16_moe_plan_destroy, w4a16_moe_prepare_routes, w4a16_moe_route_info,
                    w4a16_moe_route_topk, w4a16_moe_set_gemm_path, w4a16_moe_set_overrides,
-                   w4a16_moe_forward_masked, w4a16_moe_relayout_weights, w4a16_moe_set_weight_layout)
+                   w4a16_moe_forward_masked, w4a16_moe_relayout_weights, w4a16_moe_set_weight_layout,
+                   w4a16_moe_route_and_prepare)
 from ._lib import PATH_AUTO, PATH_CUDA_CORES, PATH_TENSOR_CORES  # noqa: F401
 from ._lib import LAYOUT_CHECKPOINT, LAYOUT_INTERLEAVED  # noqa: F401
 
@@ -125,6 +126,21 @@ class W4A16MoE:
 
     def route_info(self, num_tokens: int) -> RouteInfo:
         return w4a16_moe_route_info(self.plan, num_tokens)
+
+    def route_and_prepare(self, logits, stream=None):
+        """Router softmax + top-k and the route layout in one pass
+        (``w4a16_moe_route_and_prepare``).  logits [T, G] FP32 CUDA tensor;
+        returns (topk_ids int32 [T, k], topk_weights fp32 [T, k]) for the
+        following ``forward``."""
+        if logits.dtype != torch.float32 or not logits.is_cuda or logits.dim() != 2:
+            raise ValueError("logits must be a 2-D float32 CUDA tensor")
+        T, G = logits.shape
+        k = self.desc.top_k
+        ids = torch.empty(T, k, dtype=torch.int32, device=logits.device)
+        w = torch.empty(T, k, dtype=torch.float32, device=logits.device)
+        w4a16_moe_route_and_prepare(self.plan, T, _ptr(logits), G, _ptr(ids), _ptr(w), _ptr(self.workspace),
+                                    _stream(stream))
+        return ids, w
 
     def prepare_routes(self, topk_ids, stream=None):
         w4a16_moe_prepare_routes(self.plan, topk_ids.shape[0], _ptr(topk_ids),

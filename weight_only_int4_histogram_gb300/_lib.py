@@ -37,6 +37,7 @@ EXPORTED = (
     "w4a16_moe_forward_masked",
     "w4a16_moe_relayout_weights",
     "w4a16_moe_set_weight_layout",
+    "w4a16_moe_route_and_prepare",
 )
 
 
@@ -110,6 +111,8 @@ def load(path: str = LIB_PATH):
     L.w4a16_moe_route_topk.restype = ctypes.c_int
     L.w4a16_moe_relayout_weights.argtypes = [P, i32, P, P, P]
     L.w4a16_moe_relayout_weights.restype = st
+    L.w4a16_moe_route_and_prepare.argtypes = [P, i32, P, i32, P, P, P, P]
+    L.w4a16_moe_route_and_prepare.restype = st
     L.w4a16_moe_set_weight_layout.argtypes = [P, i32]
     L.w4a16_moe_set_weight_layout.restype = st
     L.w4a16_moe_last_error.argtypes = []
@@ -186,6 +189,12 @@ def w4a16_moe_route_topk(logits_ptr: int, num_tokens: int, num_global: int, top_
 
 def w4a16_moe_relayout_weights(plan, which: int, in_ptr: int, out_ptr: int, stream: int):
     check(load().w4a16_moe_relayout_weights(plan, which, in_ptr, out_ptr, stream))
+
+
+def w4a16_moe_route_and_prepare(plan, num_tokens: int, logits_ptr: int, num_global: int, ids_ptr: int,
+                                weights_ptr: int, workspace_ptr: int, stream: int):
+    check(load().w4a16_moe_route_and_prepare(plan, num_tokens, logits_ptr, num_global, ids_ptr, weights_ptr,
+                                             workspace_ptr, stream))
 
 
 def w4a16_moe_set_weight_layout(plan, layout: int):

@@ -73,7 +73,7 @@ struct Layout {
   int stages, stage_bytes, smem;   // gate/up GEMM (and the CUDA-core path's both GEMMs)
   int stages2, smem2;              // tensor-core down GEMM (output staging buffers)
   int grid1, grid2;
-  size_t off_err, off_counts, off_offs, off_ntiles, off_tiles, off_perm, off_inv, off_ctr;
+  size_t off_err, off_counts, off_offs, off_ntiles, off_tiles, off_perm, off_inv, off_ctr, off_chist;
   size_t off_part, off_inter, off_y;
   size_t off_sx, off_sids, off_sw, off_sout;  // host-call staging (w4a16_moe_forward_host / masked)
   size_t total;
@@ -255,6 +255,7 @@ Layout make_layout(const w4a16_moe_plan_s& P, int T) {
   L.off_perm = take(sizeof(int32_t) * L.slots_cap);
   L.off_inv = take(sizeof(int32_t) * std::max(L.R, 1));
   L.off_ctr = take(sizeof(int32_t) * L.tiles_cap * L.nt1);
+  L.off_chist = take(sizeof(int32_t) * kRouteMaxCtas * E);
   L.off_part = take(L.s1 > 1 ? sizeof(float) * L.s1 * L.slots_cap * L.n1 : 0);
   L.off_inter = take(static_cast<size_t>(act_bytes) * L.slots_cap * d.inter);
   // expert outputs: the activation dtype without down split-K, FP32 partials with it
@@ -273,7 +274,15 @@ size_t max_workspace(const w4a16_moe_plan_s& P) {
   return m;
 }
 
-int route_prep_smem(int E) { return (kRoutePrepWarps * E + E + 2 * (E + 1) + 64) * 4; }
+// Route preparation CTAs: about 256 routes each (the per-CTA histogram pass
+// is one route per thread), at most kRouteMaxCtas; with the router front end
+// one token per warp.
+void route_ctas(int T, int k, bool router, int& n_cta, int& tpc) {
+  const int64_t want = router ? (T + kRoutePrepWarps - 1) / kRoutePrepWarps
+                              : (static_cast<int64_t>(T) * k + 255) / 256;
+  n_cta = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(kRouteMaxCtas, want)));
+  tpc = std::max(1, (T + n_cta - 1) / n_cta);
+}
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
@@ -387,10 +396,14 @@ bool env_flag(const char* name, bool dflt) {
   return !(v[0] == '0' && v[1] == 0);
 }
 
-w4a16_status launch_prepare(const w4a16_moe_plan_s& P, const Layout& L, const int32_t* ids,
-                            uint8_t* ws, cudaStream_t s) {
+// Route preparation for the ids of `ids`, or (logits != NULL) for the top-k
+// of the router logits [T, G], whose ids / weights then go to ids_out /
+// weights_out.
+w4a16_status launch_prepare(const w4a16_moe_plan_s& P, const Layout& L, const int32_t* ids, uint8_t* ws,
+                            cudaStream_t s, const float* logits = nullptr, int32_t G = 0,
+                            int32_t* ids_out = nullptr, float* weights_out = nullptr) {
   RoutePrepParams rp = {};
-  rp.ids = ids;
+  rp.ids = logits ? ids_out : ids;
   rp.T = L.T;
   rp.k = P.d.top_k;
   rp.E = P.d.num_experts;
@@ -405,8 +418,14 @@ w4a16_status launch_prepare(const w4a16_moe_plan_s& P, const Layout& L, const in
   rp.counters = reinterpret_cast<int32_t*>(ws + L.off_ctr);
   rp.ctr_len = L.tiles_cap * L.nt1;
   rp.err = reinterpret_cast<int32_t*>(ws + L.off_err);
-  cudaError_t e = launch_route_prep(rp, route_prep_smem(P.d.num_experts), s, P.pdl);
-  if (e != cudaSuccess) return cuda_fail(e, "route_prep launch");
+  rp.cta_hist = reinterpret_cast<int32_t*>(ws + L.off_chist);
+  route_ctas(L.T, P.d.top_k, logits != nullptr, rp.n_cta, rp.tpc);
+  rp.logits = logits;
+  rp.G = G;
+  rp.ids_out = ids_out;
+  rp.weights_out = weights_out;
+  cudaError_t e = launch_route_prep(rp, s, P.pdl);
+  if (e != cudaSuccess) return cuda_fail(e, "route preparation launch");
   return W4A16_OK;
 }
 
@@ -834,6 +853,27 @@ w4a16_status w4a16_moe_route_topk(const float* logits, int32_t num_tokens, int32
   e = w4a16::launch_router(rp, sms, static_cast<cudaStream_t>(stream), env_flag("W4A16_MOE_PDL", true));
   if (e != cudaSuccess) return cuda_fail(e, "router launch");
   return W4A16_OK;
+}
+
+w4a16_status w4a16_moe_route_and_prepare(w4a16_moe_plan_t plan, int32_t num_tokens, const float* logits,
+                                         int32_t num_global, int32_t* topk_ids, float* topk_weights, void* workspace,
+                                         void* stream) {
+  if (!plan) return fail(W4A16_ERR_INVALID_ARG, "plan is NULL");
+  if (num_tokens < 0 || num_tokens > plan->d.max_tokens)
+    return fail(W4A16_ERR_INVALID_ARG, "num_tokens %d outside [0, %d]", num_tokens, plan->d.max_tokens);
+  if (num_global < 1 || num_global > 1024)
+    return fail(W4A16_ERR_UNSUPPORTED, "num_global must be in [1, 1024], got %d", num_global);
+  if (plan->d.top_k > num_global)
+    return fail(W4A16_ERR_UNSUPPORTED, "top_k %d exceeds num_global %d", plan->d.top_k, num_global);
+  if (num_tokens == 0) return W4A16_OK;
+  w4a16_status st;
+  if ((st = check_ptr(logits, 4, "logits")) != W4A16_OK) return st;
+  if ((st = check_ptr(topk_ids, 4, "topk_ids")) != W4A16_OK) return st;
+  if ((st = check_ptr(topk_weights, 4, "topk_weights")) != W4A16_OK) return st;
+  if ((st = check_ptr(workspace, 256, "workspace")) != W4A16_OK) return st;
+  const Layout L = make_layout(*plan, num_tokens);
+  return launch_prepare(*plan, L, nullptr, static_cast<uint8_t*>(workspace), static_cast<cudaStream_t>(stream),
+                        logits, num_global, topk_ids, topk_weights);
 }
 
 w4a16_status w4a16_moe_set_stage_events(w4a16_moe_plan_t plan, void* const* events, int32_t n) {

@@ -100,7 +100,18 @@ struct RoutePrepParams {
   int32_t* counters;       // [ctr_len] split-K arrival counters, zeroed here
   int32_t ctr_len;
   int32_t* err;            // device error flag, cleared here
+  int32_t* cta_hist;       // [n_cta][E] expert counts of each CTA's routes (n_cta > 1)
+  int32_t n_cta, tpc;      // CTAs and whole tokens per CTA (the last CTA may get fewer)
+  // router front end (logits != NULL): softmax + top-k over G experts writes
+  // ids_out / weights_out [T, k], which the placement then reads as `ids`
+  const float* logits;
+  int32_t G;
+  int32_t* ids_out;
+  float* weights_out;
 };
+// Route preparation: at most kRouteMaxCtas CTAs (the expert totals are summed
+// over them by every CTA of the placement kernel).
+constexpr int kRouteMaxCtas = 64;
 
 struct GemmParams {
   int32_t act;             // ACT_* (gate/up GEMM epilogue)
@@ -151,7 +162,7 @@ struct CombineParams {
 };
 
 // Host-side launchers (one translation unit each).
-cudaError_t launch_route_prep(const RoutePrepParams& p, int smem_bytes, cudaStream_t s, bool pdl);
+cudaError_t launch_route_prep(const RoutePrepParams& p, cudaStream_t s, bool pdl);
 cudaError_t launch_gemm(int which, int scale_kind, int dtype, int layout, const GemmParams& p,
                         const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
                         const CUtensorMap& tmS, int grid, int smem_bytes, cudaStream_t s, bool pdl);

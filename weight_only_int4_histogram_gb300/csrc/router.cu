@@ -7,11 +7,8 @@
 // p = softmax(logits[t, :]) over all experts of the model; the k largest p in
 // descending order, ties to the lower expert index; the weights are those p.
 //
-// One warp per token.  Lane l holds logits l, l + 32, ... in registers
-// (at most 1024 experts).  The maximum and the sum of exp(l - max) are warp
-// reductions in a fixed order (deterministic); each of the k rounds is a warp
-// argmax over the not yet selected logits.  softmax is strictly increasing in
-// the logit, so the selection compares the logits themselves, exactly.
+// One warp per token (warp_softmax_topk in router.cuh, shared with the fused
+// router + route preparation of route_prep.cu).
 #include <algorithm>
 
 #include "common.cuh"
@@ -29,54 +26,14 @@ __global__ void __launch_bounds__(kRouterThreads) router_topk_kernel(const Route
   pdl_launch_dependents();
   const int lane = threadIdx.x & 31;
   const int warps = gridDim.x * (kRouterThreads / 32);
-  const unsigned full = 0xFFFFFFFFu;
-  const int per_lane = (p.G + 31) / 32;
   for (int t = blockIdx.x * (kRouterThreads / 32) + (threadIdx.x >> 5); t < p.T; t += warps) {
-    const float* l = p.logits + static_cast<int64_t>(t) * p.G;
-    float v[kPerLane];
-    float m = -INFINITY;
-#pragma unroll
-    for (int i = 0; i < kPerLane; ++i) {
-      const int e = lane + 32 * i;
-      v[i] = (i < per_lane && e < p.G) ? l[e] : -INFINITY;
-      m = fmaxf(m, v[i]);
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(full, m, o));
-    float s = 0.0f;
-#pragma unroll
-    for (int i = 0; i < kPerLane; ++i)
-      if (i < per_lane && lane + 32 * i < p.G) s += expf(v[i] - m);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(full, s, o);
-    uint32_t taken = 0;  // bit i: element i of this lane already selected
-    for (int j = 0; j < p.k; ++j) {
-      // this lane's best remaining (largest logit, lowest index on ties)
-      float bv = -INFINITY;
-      int be = 0x7FFFFFFF;
-#pragma unroll
-      for (int i = 0; i < kPerLane; ++i) {
-        const int e = lane + 32 * i;
-        if (i < per_lane && e < p.G && !((taken >> i) & 1u) && (v[i] > bv || (v[i] == bv && e < be))) {
-          bv = v[i];
-          be = e;
-        }
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const float ov = __shfl_xor_sync(full, bv, o);
-        const int oe = __shfl_xor_sync(full, be, o);
-        if (ov > bv || (ov == bv && oe < be)) {
-          bv = ov;
-          be = oe;
-        }
-      }
-      if (be < p.G && (be & 31) == lane) taken |= 1u << (be >> 5);
-      if (lane == 0) {
-        p.ids[static_cast<int64_t>(t) * p.k + j] = be;
-        p.weights[static_cast<int64_t>(t) * p.k + j] = expf(bv - m) / s;
-      }
-    }
+    int32_t* ids = p.ids + static_cast<int64_t>(t) * p.k;
+    float* wts = p.weights + static_cast<int64_t>(t) * p.k;
+    warp_softmax_topk<kPerLane>(p.logits + static_cast<int64_t>(t) * p.G, p.G, p.k, lane,
+                                [&](int j, int id, float prob) {
+                                  ids[j] = id;
+                                  wts[j] = prob;
+                                });
   }
 }
 
