@@ -382,6 +382,31 @@ def max_over_ranks(values, dist, device):
     return [float(v) for v in t.tolist()]
 
 
+def run_ncu_target(args):
+    """A short, profiler-friendly run: the workload's weights and one batch,
+    `--warmup` eager forwards, then one more, synchronised.  Prints one line.
+    (Kernel launches per forward: route preparation (one or two), the gate/up
+    GEMM, the down GEMM, the combine.)"""
+    from weight_only_int4_histogram_gb300 import W4A16MoE, build
+    build.build()
+    torch.cuda.set_device(0)
+    cfg = gen.CONFIGS[args.config]
+    w_ckpt = gen.make_weights(cfg, "cuda")
+    moe = W4A16MoE.from_config(cfg, max_tokens=args.tokens)
+    moe.set_gemm_path(GEMM_PATHS[args.gemm_path])
+    w = moe.relayout_weights(w_ckpt) if args.weights == "interleaved" else w_ckpt
+    x = gen.make_activations(cfg, args.tokens, "cuda")
+    ids, tw = gen.make_routes(cfg, args.tokens, "cuda")
+    for _ in range(args.warmup + 1):
+        moe(x, w, tw, ids)
+    torch.cuda.synchronize()
+    moe.check_device_error()
+    info = moe.route_info(args.tokens)
+    print(json.dumps({"ncu_target": cfg.name, "tokens": args.tokens, "forwards": args.warmup + 1,
+                      "gemm_path": PATH_NAMES[info.gemm_path], "tile_rows": info.tile_rows,
+                      "splits": [info.gemm1_splits, info.gemm2_splits]}))
+
+
 def run_gpu(args):
     from weight_only_int4_histogram_gb300 import W4A16MoE, build
     build.build()
@@ -608,10 +633,15 @@ def main():
     ap.add_argument("--weights", default="interleaved", choices=["interleaved", "checkpoint"],
                     help="packed weight layout the forward reads (interleaved: relaid out once at setup)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ncu", action="store_true",
+                    help="profiler target: --warmup eager forwards + 1 of one batch, no timing")
     ap.add_argument("--cpu-sample-tokens", type=int, default=512)
     ap.add_argument("--ref-sample-tokens", type=int, default=16)
     args = ap.parse_args()
     args.sweep_tokens = tuple(int(t) for t in args.sweep.split(",") if t.strip())
+    if args.ncu:
+        run_ncu_target(args)
+        return
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
