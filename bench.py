@@ -6,10 +6,12 @@ synthetic inputs, renormalize=False.  One step = route preparation + gate/up
 GEMM + SwiGLU + down GEMM + FP32 top-k combine over one batch of T tokens
 (default T = 2048), replayed from a CUDA graph.  The L2 is flushed (a 512 MB
 write) before every timed step, outside the timed events.  The token sweep
-1, 8, 32, 256, 1024 is measured the same way and reported under "sweep".
+1, 8, 32, 256, 1024 is measured the same way and reported under "sweep"; the
+other workloads (the 32-of-256-expert local shape, the per-channel BF16 and
+FP16 shapes, the skewed ReLU^2 shape) under "workloads".
 
-Prints ONE JSON line.  ``--impl reference`` times the CPU oracle instead (a
-bounded sample of the same workload on the host cores).
+Prints ONE JSON line.  ``--impl reference`` times the CPU oracle instead (the
+same workload on the host cores; whole batches, fewer steps).
 """
 from __future__ import annotations
 
@@ -407,6 +409,63 @@ def run_ncu_target(args):
                       "splits": [info.gemm1_splits, info.gemm2_splits]}))
 
 
+# Other workloads reported beside the headline: (workload, tokens).
+OTHER_WORKLOADS = (("deepseek_local_e32of256_h7168_i2048_k8", 2048),
+                   ("deepseek_local_e32of256_h7168_i2048_k8", 64),
+                   ("per_channel_e60_h2048_i1408_k4", 1024),
+                   ("per_channel_fp16_e60_h2048_i1408_k4", 1024),
+                   ("relu2_skew_e64_h2688_i1856_k6", 4096),
+                   ("relu2_skew_e64_h2688_i1856_k6", 32))
+
+
+def metric_name(cfg):
+    return f"W4A16 MoE forward latency (us), {cfg.name}"
+
+
+def roofline_of(cfg, ids, us, hbm, bf16):
+    nbytes = gen.algorithmic_bytes(cfg, ids)
+    flops = gen.algorithmic_flops(cfg, ids)
+    t_hbm = nbytes / (hbm * 1e9) * 1e6
+    t_tc = flops / (bf16 * 1e12) * 1e6
+    t_roof = max(t_hbm, t_tc)
+    return dict(gbs=round(nbytes / us / 1e3, 1), alg_bytes=nbytes, alg_flops=flops,
+                roofline_us=round(t_roof, 3), roofline_frac=round(t_roof / us, 4),
+                hbm_frac=round(t_hbm / us, 4), tensor_frac=round(t_tc / us, 4),
+                bound="hbm" if t_hbm >= t_tc else "tensor")
+
+
+def measure_other_workloads(dev, flush, stream, hbm, bf16, steps, weights_layout):
+    """Each other workload at its listed token count: its own weights and
+    plan, relaid out like the headline's, CUDA-graph replay with the L2
+    flushed, median of `steps`."""
+    from weight_only_int4_histogram_gb300 import W4A16MoE
+    out = {}
+    cache = {}
+    for name, T in OTHER_WORKLOADS:
+        cfg = gen.CONFIGS[name]
+        if name not in cache:
+            cache.clear()
+            w_ckpt = gen.make_weights(cfg, dev)
+            moe = W4A16MoE.from_config(cfg, max_tokens=max(cfg.tokens), device=dev)
+            w = moe.relayout_weights(w_ckpt) if weights_layout == "interleaved" else w_ckpt
+            cache[name] = (moe, w)
+        moe, w = cache[name]
+        x = gen.make_activations(cfg, T, dev)
+        ids, tw = gen.make_routes(cfg, T, dev)
+        o = torch.empty(T, cfg.hidden, dtype=cfg.torch_act_dtype(), device=dev)
+        g = capture(moe, w, x, ids, tw, o, stream)
+        times = time_graph(g, flush, stream, steps, 3)
+        moe.check_device_error()
+        med = statistics.median(times)
+        r = dict(tokens=T, us=round(med, 3), gemm_path=PATH_NAMES[moe.route_info(T).gemm_path])
+        r.update(roofline_of(cfg, ids, med, hbm, bf16))
+        out[f"{name}@{T}"] = r
+        del g
+    cache.clear()
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_gpu(args):
     from weight_only_int4_histogram_gb300 import W4A16MoE, build
     build.build()
@@ -450,14 +509,9 @@ def run_gpu(args):
         clocks = clk.stop() if sample_clocks else None
         moe.check_device_error()
         med = statistics.median(times)
-        nbytes = gen.algorithmic_bytes(cfg, ids)
-        flops = gen.algorithmic_flops(cfg, ids)
-        t_roof = max(nbytes / (hbm * 1e9), flops / (bf16 * 1e12)) * 1e6
         res = dict(tokens=T, us=round(med, 3), us_min=round(min(times), 3),
-                   gbs=round(nbytes / med / 1e3, 1), alg_bytes=nbytes, alg_flops=flops,
-                   roofline_us=round(t_roof, 3), roofline_frac=round(t_roof / med, 4),
-                   bound="hbm" if nbytes / (hbm * 1e9) >= flops / (bf16 * 1e12) else "tensor",
                    gemm_path=PATH_NAMES[moe.route_info(T).gemm_path])
+        res.update(roofline_of(cfg, ids, med, hbm, bf16))
         return res, (x, ids, tw, out, g), times, clocks
 
     head, (x, ids, tw, out, g), times, clocks = measure(args.tokens, args.steps, args.warmup, True)
@@ -511,8 +565,11 @@ def run_gpu(args):
     d2h = oh.numel() * 2
 
     med, e2e_med, warm = max_over_ranks([head["us"], e2e_med, warm], dist, dev)
+    workloads = {}
+    if not args.no_workloads:
+        workloads = measure_other_workloads(dev, flush, stream, hbm, bf16, max(10, args.steps // 2), args.weights)
     line = {
-        "metric": "W4A16 MoE forward latency (us), Kimi TP8 shard shape",
+        "metric": metric_name(cfg),
         "value": round(med, 3),
         "unit": "us",
         "n_gpus": world,
@@ -541,11 +598,11 @@ def run_gpu(args):
                         "protocol": "the pages' timing: warm CUDA-graph replays, mean of 10, median of 3 samples"},
         "router": router,
         "masked_layout": masked,
+        "workloads": workloads,
         "clocks": clocks,
     }
     if not args.no_cpu_baseline and rank == 0 and world == 1:
-        line["cpu_baseline"] = cpu_baseline(cfg, args.tokens, args.cpu_sample_tokens,
-                                            (w_ckpt.to("cpu"), x.cpu(), ids.cpu(), tw.cpu()))
+        line["cpu_baseline"] = cpu_baseline(cfg, args.tokens, (w_ckpt.to("cpu"), x.cpu(), ids.cpu(), tw.cpu()))
     if rank == 0:
         print(json.dumps(line), flush=True)
     if dist is not None:
@@ -556,21 +613,24 @@ def run_gpu(args):
 # CPU oracle (reported baseline / reference arm)
 # ---------------------------------------------------------------------------
 
-def cpu_baseline(cfg, tokens, sample_tokens, inputs=None):
+def cpu_baseline(cfg, tokens, inputs=None):
+    """The CPU oracle (plain loops, OpenMP) on the host cores: the whole batch
+    once, measured, plus one token on a single thread."""
     import oracle
     oracle.build()
     if inputs is None:
         inputs = make_inputs_for_cpu(cfg, tokens)
     w, x, ids, tw = inputs
-    rows = list(range(min(sample_tokens, tokens)))
+    cores = oracle.num_threads()
     t0 = time.perf_counter()
-    oracle.moe_forward(cfg, x, w, tw, ids, rows=rows)
+    oracle.moe_forward(cfg, x, w, tw, ids, nthreads=cores)
     dt = time.perf_counter() - t0
-    per_step_us = dt * 1e6 * tokens / len(rows)
-    return {"value": round(per_step_us, 1), "unit": "us", "cores": oracle.num_threads(),
-            "kind": "oracle",
-            "sample": f"first {len(rows)} of {tokens} tokens of the same workload, "
-                      f"{dt:.2f} s of CPU work, scaled by {tokens}/{len(rows)}"}
+    t1 = time.perf_counter()
+    oracle.moe_forward(cfg, x[:1], w, tw[:1], ids[:1], nthreads=1)
+    dt1 = time.perf_counter() - t1
+    return {"value": round(dt * 1e6, 1), "unit": "us", "cores": cores, "kind": "oracle",
+            "sample": f"the whole {tokens}-token batch once ({dt:.2f} s on {cores} threads)",
+            "single_thread": {"tokens": 1, "us": round(dt1 * 1e6, 1), "cores": 1}}
 
 
 def make_inputs_for_cpu(cfg, tokens):
@@ -584,6 +644,9 @@ def make_inputs_for_cpu(cfg, tokens):
 
 
 def run_reference(args):
+    """The CPU oracle as the reference arm: every step is the whole batch of
+    the same workload (no extrapolation); steps are capped so that the run
+    stays within minutes."""
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
@@ -591,27 +654,28 @@ def run_reference(args):
     import oracle
     oracle.build()
     w, x, ids, tw = make_inputs_for_cpu(cfg, args.tokens)
-    rows = list(range(min(args.ref_sample_tokens, args.tokens)))
-    for _ in range(args.warmup):
-        oracle.moe_forward(cfg, x, w, tw, ids, rows=rows[:1])
+    steps = max(1, min(args.steps, args.ref_max_steps))
+    cores = oracle.num_threads()
+    for _ in range(min(args.warmup, 1)):
+        oracle.moe_forward(cfg, x[:1], w, tw[:1], ids[:1], nthreads=cores)
     times = []
-    for _ in range(args.steps):
+    for _ in range(steps):
         t0 = time.perf_counter()
-        oracle.moe_forward(cfg, x, w, tw, ids, rows=rows)
-        times.append((time.perf_counter() - t0) * 1e6 * args.tokens / len(rows))
+        oracle.moe_forward(cfg, x, w, tw, ids, nthreads=cores)
+        times.append((time.perf_counter() - t0) * 1e6)
     v = statistics.median(times)
     line = {
         "impl": "reference",
-        "metric": "W4A16 MoE forward latency (us), Kimi TP8 shard shape",
+        "metric": metric_name(cfg),
         "value": round(v, 1), "unit": "us", "n_gpus": int(os.environ.get("WORLD_SIZE", "1")),
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(v / 1000.0, 3),
+        "steps": steps, "warmup": min(args.warmup, 1), "ms_per_step": round(v / 1000.0, 3),
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded)",
         "config": {"workload": cfg.name, "tokens": args.tokens},
-        "cpu_baseline": {"value": round(v, 1), "unit": "us", "cores": oracle.num_threads(),
+        "cpu_baseline": {"value": round(v, 1), "unit": "us", "cores": cores,
                          "kind": "oracle",
-                         "sample": f"each step: first {len(rows)} of {args.tokens} tokens, "
-                                   f"scaled by {args.tokens}/{len(rows)}"},
+                         "sample": f"every step the whole {args.tokens}-token batch; {steps} steps "
+                                   f"(requested {args.steps}, capped at {args.ref_max_steps})"},
         "e2e": {"value": round(v, 1), "unit": "us", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -635,8 +699,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ncu", action="store_true",
                     help="profiler target: --warmup eager forwards + 1 of one batch, no timing")
-    ap.add_argument("--cpu-sample-tokens", type=int, default=512)
-    ap.add_argument("--ref-sample-tokens", type=int, default=16)
+    ap.add_argument("--ref-max-steps", type=int, default=3,
+                    help="reference arm: at most this many whole-batch oracle steps")
+    ap.add_argument("--no-workloads", action="store_true", help="skip the other workloads")
     args = ap.parse_args()
     args.sweep_tokens = tuple(int(t) for t in args.sweep.split(",") if t.strip())
     if args.ncu:

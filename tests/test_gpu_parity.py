@@ -172,6 +172,33 @@ def test_activation_magnitudes(shape, mag, path):
         compare(out[t:t + 1], ref[t:t + 1], f"{mag} token {t} {path}")
 
 
+@pytest.mark.parametrize("path", list(PATHS))
+@pytest.mark.parametrize("scale", [gen.SCALE_GROUP32, gen.SCALE_PER_CHANNEL])
+def test_fp16_outputs_in_the_subnormal_range(scale, path):
+    """FP16 activations scaled by 2^-7: the expert outputs (quadratic in x
+    through the gated MLP) land in FP16's subnormal range, where the final
+    cast itself moves values by up to half of 2^-24.  The reference is then
+    the oracle's own FP16 output (its FP32 accumulator cast once): both sides
+    round the same FP32 sum to the same grid, so they are compared element by
+    element, within the parity bars plus one subnormal step."""
+    cfg = small_cfg(E=4, H=512, I=256, k=2, scale=scale, dt=gen.DT_FP16)
+    T = 24
+    w, x, ids, tw = case_on_gpu(cfg, T)
+    x = (x.float() * 2.0 ** -7).to(x.dtype)
+    moe = make_moe(cfg, T)
+    moe.set_gemm_path(PATHS[path])
+    out = moe(x, w, tw, ids)
+    torch.cuda.synchronize()
+    _, bits = oracle.moe_forward(cfg, x.cpu(), w.to("cpu"), tw.cpu(), ids.cpu())
+    ref = oracle.fp16_decode(bits)
+    g = out.float().cpu().numpy().astype(np.float64)
+    assert (np.abs(ref[ref != 0]) < 2.0 ** -14).mean() > 0.5, "case must exercise subnormal outputs"
+    step = 2.0 ** -24
+    err = np.abs(g - ref)
+    assert err.max() <= 2e-2 * np.abs(ref).max() + step, (err.max(), np.abs(ref).max())
+    assert np.linalg.norm(g - ref) <= 5e-3 * np.linalg.norm(ref) + step * np.sqrt(ref.size)
+
+
 @pytest.mark.parametrize("tile_rows", [16, 32, 48, 128])
 def test_route_tile_heights(tile_rows):
     """Route-tile boundary cases: full tiles plus partial tails at several
@@ -294,33 +321,86 @@ def test_forward_host_matches_device_path():
 
 
 # ---------------------------------------------------------------------------
-# full-size workloads, sampled tokens, benchmark launch configuration
+# full-size workloads: every token count of every workload, in the launch
+# configuration the benchmark times (planner's path, relaid-out weights)
 # ---------------------------------------------------------------------------
 
-FULL = [("kimi_tp8_e384_h7168_i256_k8", (1, 32, 2048)),
-        ("deepseek_local_e32of256_h7168_i2048_k8", (4, 2048)),
-        ("per_channel_e60_h2048_i1408_k4", (8, 1024)),
-        ("per_channel_fp16_e60_h2048_i1408_k4", (1024,)),
-        ("relu2_skew_e64_h2688_i1856_k6", (32, 4096))]
+FULL = [(name, T) for name, cfg in gen.CONFIGS.items() if name != gen.TINY.name for T in cfg.tokens]
 
 
-@pytest.mark.parametrize("name,tokens", FULL, ids=[f[0] for f in FULL])
-def test_full_size_sampled_rows(name, tokens):
+def boundary_tokens(moe, ids, T, k, want=64, seed=0):
+    """Tokens whose routes sit in the last route tile of their expert (one per
+    expert: the token of the tile's last valid slot -- the partial tiles the
+    padding logic touches), topped up with random tokens to at least `want`."""
+    lay = moe.read_route_layout(T)
+    perm = lay["perm"].numpy()
+    tiles = lay["tiles"].numpy()
+    last = {}
+    for e, m0, rows, _ in tiles:
+        last[int(e)] = (int(m0), int(rows))
+    toks = set()
+    for e, (m0, rows) in last.items():
+        r = int(perm[m0 + rows - 1])
+        assert r >= 0
+        toks.add(r // k)
+    rng = np.random.default_rng(seed)
+    extra = rng.permutation(T)
+    i = 0
+    while len(toks) < min(want, T):
+        toks.add(int(extra[i]))
+        i += 1
+    toks.update([0, T - 1])
+    return sorted(toks)
+
+
+@pytest.mark.parametrize("name,T", FULL, ids=[f"{n}-T{t}" for n, t in FULL])
+def test_full_size_every_token_count(name, T):
     cfg = gen.CONFIGS[name]
-    w = gen.make_weights(cfg, "cuda")
-    w_cpu = w.to("cpu")
+    w = _full_weights(cfg)
     moe = make_moe(cfg, max(cfg.tokens))
-    for T in tokens:
-        _, x, ids, tw = case_on_gpu(cfg, T, weights_gpu=w)
-        out = moe(x, w, tw, ids)
-        torch.cuda.synchronize()
-        moe.check_device_error()
-        # repeat runs are bit-identical (also catches stale operand reads)
-        for _ in range(2):
-            again = moe(x, w, tw, ids)
-            torch.cuda.synchronize()
-            assert torch.equal(again.view(torch.int16), out.view(torch.int16)), f"{name} T={T} not deterministic"
-        rng = np.random.default_rng(T)
-        rows = sorted(set([0, T - 1] + rng.integers(0, T, size=min(T, 6)).tolist()))
-        ref = oracle_rows(cfg, w, x, ids, tw, rows=rows, w_cpu=w_cpu)
-        compare(out[rows], ref, f"{name} T={T}")
+    wi = moe.relayout_weights(w)
+    _, x, ids, tw = case_on_gpu(cfg, T, weights_gpu=w)
+    out = moe(x, wi, tw, ids)
+    torch.cuda.synchronize()
+    moe.check_device_error()
+    # repeat runs are bit-identical (also catches stale operand reads)
+    again = moe(x, wi, tw, ids)
+    torch.cuda.synchronize()
+    assert torch.equal(again.view(torch.int16), out.view(torch.int16)), f"{name} T={T} not deterministic"
+    rows = boundary_tokens(moe, ids, T, cfg.top_k, seed=T)
+    assert len(rows) >= min(64, T)
+    ref = oracle_rows(cfg, w, x, ids, tw, rows=rows, w_cpu=_full_weights_cpu(cfg))
+    compare(out[rows], ref, f"{name} T={T} ({moe.route_info(T).gemm_path})")
+
+
+@pytest.mark.parametrize("T", [8, 256, 1024])
+def test_full_size_checkpoint_layout_kimi(T):
+    """The checkpoint weight layout at full size, on the planner's path."""
+    cfg = gen.KIMI
+    w = _full_weights(cfg)
+    moe = make_moe(cfg, T)
+    _, x, ids, tw = case_on_gpu(cfg, T, weights_gpu=w)
+    out = moe(x, w, tw, ids)
+    torch.cuda.synchronize()
+    moe.check_device_error()
+    rows = boundary_tokens(moe, ids, T, cfg.top_k, seed=T + 1)
+    compare(out[rows], oracle_rows(cfg, w, x, ids, tw, rows=rows, w_cpu=_full_weights_cpu(cfg)), f"kimi T={T} ckpt")
+
+
+_W = {}
+
+
+def _full_weights(cfg):
+    # one workload's weights on the device at a time (bounded device memory)
+    if cfg.name not in _W:
+        _W.clear()
+        _W[cfg.name] = (gen.make_weights(cfg, "cuda"), None)
+    return _W[cfg.name][0]
+
+
+def _full_weights_cpu(cfg):
+    w, wc = _W[cfg.name]
+    if wc is None:
+        wc = w.to("cpu")
+        _W[cfg.name] = (w, wc)
+    return wc

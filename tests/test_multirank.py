@@ -57,10 +57,12 @@ def test_reference_arm_under_two_rank_launch_prints_once():
     cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
            "--master-addr", "127.0.0.1", "--master-port", str(port), "bench.py", "--impl", "reference",
            "--gpus", "2", "--steps", "1", "--warmup", "3", "--tokens", "16",
-           "--config", "tiny_e8_h256_i384_k2", "--ref-sample-tokens", "2"]
+           "--config", "tiny_e8_h256_i384_k2", "--ref-max-steps", "2"]
     r = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=600)
     assert r.returncode == 0, r.stderr[-2000:]
     lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
     assert len(lines) == 1
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
+    # whole batches are timed, never extrapolated: the steps taken are reported
+    assert d["steps"] == 1 and d["ms_per_step"] * 1000.0 == pytest.approx(d["value"], rel=1e-3)

@@ -122,12 +122,17 @@ constexpr int kAutoMaxBN = 64;
 // sets when `double_acc` (units of few K blocks, where the epilogue must
 // overlap the next unit's MMAs), else with one if two do not fit.
 void choose_nt(int n_tiles, int bn, int smem_budget, int max_nt, bool double_acc, int& nt, int& acc_bufs) {
-  const int need_acc = double_acc ? 2 : 1;
-  nt = max_nt;
-  while (nt > 1 && (nt / 2 >= n_tiles || smem_budget / gemm_stage_bytes(nt, bn) < 2 ||
-                    gemm_a_slots(nt, bn, need_acc) < 2))
-    nt >>= 1;
-  acc_bufs = gemm_a_slots(nt, bn, 2) >= 2 ? 2 : 1;
+  (void)double_acc;
+  // two accumulator sets whenever they fit (measured: the epilogue overlap
+  // they give outweighs a third A slot even for 28-stage units)
+  for (int acc = 2; acc >= 1; --acc) {
+    nt = max_nt;
+    while (nt > 1 && (nt / 2 >= n_tiles || smem_budget / gemm_stage_bytes(nt, bn) < 2 ||
+                      gemm_a_slots(nt, bn, acc) < 2))
+      nt >>= 1;
+    acc_bufs = acc;
+    if (smem_budget / gemm_stage_bytes(nt, bn) >= 2 && gemm_a_slots(nt, bn, acc) >= 2) return;
+  }
 }
 
 // Units of at most this many K blocks keep two accumulator sets.
@@ -142,10 +147,15 @@ constexpr int kDefaultNT = 2;
 int choose_bn(const w4a16_moe_plan_s& P, int T) {
   if (P.ov_bn) return P.ov_bn;
   // Route-count-based tile height: expected routes per expert plus three
-  // standard deviations, so that one route tile usually covers an expert, at
-  // most kAutoMaxBN routes: a stage holds the tile's activation rows (512 bytes
-  // each), and taller tiles leave too few stages in shared memory to cover
-  // the weight-load latency (4 stages at 64 routes, 2 at 128).
+  // standard deviations, so that one route tile usually covers an expert
+  // (every extra tile of an expert streams its weights once more), at most
+  // kAutoMaxBN = 64 routes.  A stage holds the tile's activation rows (512
+  // bytes each): above 64 routes only one weight tile per unit fits, the
+  // activation rows then cross from L2 once per weight tile, and on GB300
+  // that cost more than the second weight pass it saves (measured at 2048
+  // tokens on the 32-local-expert H 7168 / I 2048 shape and at 4096 on the
+  // skewed ReLU^2 shape; only the 60-expert per-channel shape at 1024 tokens
+  // gained).
   const double lam = static_cast<double>(T) * P.d.top_k / P.d.num_experts;
   const double want = lam + 3.0 * std::sqrt(lam) + 1.0;
   int bn = static_cast<int>(std::ceil(want / 16.0)) * 16;
