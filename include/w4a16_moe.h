@@ -85,8 +85,8 @@ typedef enum {
  *   num_experts   E, experts held by this GPU (1..1024)
  *   expert_offset global id of local expert 0 (>= 0); stands in for expert
  *                 parallelism: ids outside [offset, offset + E) are masked
- *   hidden        H, multiple of 64
- *   inter         I, multiple of 64
+ *   hidden        H, multiple of 32
+ *   inter         I, multiple of 32
  *   top_k         k, 1..16
  *   max_tokens    largest T any later call may pass (1..65536)
  *   act           w4a16_act: SWIGLU (W13 has N1 = 2I rows) or RELU2 (N1 = I)

@@ -56,7 +56,7 @@ def test_plan_ok_and_workspace_positive(lib):
 
 @pytest.mark.parametrize("kw,status", [
     (dict(num_experts=0), 2), (dict(num_experts=2000), 2), (dict(expert_offset=-1), 1),
-    (dict(hidden=100), 2), (dict(inter=96), 2), (dict(top_k=0), 2), (dict(top_k=17), 2),
+    (dict(hidden=100), 2), (dict(inter=80), 2), (dict(hidden=48), 2), (dict(top_k=0), 2), (dict(top_k=17), 2),
     (dict(max_tokens=0), 2), (dict(act=5), 1), (dict(scale_kind=3), 1), (dict(act_dtype=2), 1),
 ])
 def test_plan_rejects_bad_descriptors(lib, kw, status):

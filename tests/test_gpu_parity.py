@@ -121,6 +121,57 @@ def test_small_shapes_parity(shape, T, path):
     run_and_compare(cfg, T, path=path)
 
 
+@pytest.mark.parametrize("path", list(PATHS))
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: f"a{s['act']}s{s['scale']}d{s['dt']}")
+@pytest.mark.parametrize("relaid", [False, True], ids=["ckpt", "il"])
+def test_sizes_that_are_odd_multiples_of_32(shape, path, relaid):
+    """H = 1056 (33 groups of 32: group-scale rows of 66 bytes, only 2-byte
+    aligned; a partial last 64-column activation box and 256-K stage) and
+    I = 352 (a half-used last SwiGLU tile pair, a partial last stage of the
+    down GEMM)."""
+    cfg = small_cfg(E=5, H=1056, I=352, k=3, **shape)
+    T = 29
+    w, x, ids, tw = case_on_gpu(cfg, T)
+    moe = make_moe(cfg, T)
+    moe.set_gemm_path(PATHS[path])
+    wts = moe.relayout_weights(w) if relaid else w
+    out = moe(x, wts, tw, ids)
+    torch.cuda.synchronize()
+    moe.check_device_error()
+    compare(out, oracle_rows(cfg, w, x, ids, tw), f"{cfg.name} {path} relaid={relaid}")
+
+
+@pytest.mark.parametrize("path", list(PATHS))
+def test_cuda_graph_replay_at_k_1056(path):
+    """"feat(pytorch): add CuTeDSL W4A16 MoE backend" (LMDeploy), Validation:
+    full MoE CUDA-graph replay at K = 1056 -- here hidden 1056 (the gate/up
+    GEMM's K) and inter 1056 (the down GEMM's K), new inputs copied into the
+    captured buffers before each replay."""
+    cfg = small_cfg(E=6, H=1056, I=1056, k=2, seed=13)
+    T = 37
+    w, x, ids, tw = case_on_gpu(cfg, T)
+    moe = make_moe(cfg, T)
+    moe.set_gemm_path(PATHS[path])
+    out = torch.empty(T, cfg.hidden, dtype=torch.bfloat16, device="cuda")
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        moe(x, w, tw, ids, out=out, stream=s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        moe(x, w, tw, ids, out=out, stream=s)
+    for trial in range(2):
+        x2 = gen.make_activations(cfg, T, "cuda", seed=300 + trial)
+        ids2, tw2 = gen.make_routes(cfg, T, "cuda", seed=400 + trial)
+        x.copy_(x2)
+        ids.copy_(ids2)
+        tw.copy_(tw2)
+        g.replay()
+        torch.cuda.synchronize()
+        moe.check_device_error()
+        compare(out, oracle_rows(cfg, w, x2, ids2, tw2), f"K=1056 graph replay {trial} {path}")
+
+
 def bucket_ids(E, counts, k, seed=0):
     """ids [T, k] giving expert e exactly counts[e] routes (remaining slots
     -1), tokens shuffled."""

@@ -196,7 +196,9 @@ Layout make_layout(const w4a16_moe_plan_s& P, int T) {
   L.slots_cap = static_cast<int64_t>(L.R) + static_cast<int64_t>(touched_max) * (L.bn - 1) + L.bn;
   const bool gated = d.act == W4A16_ACT_SWIGLU;
   L.n1 = gated ? 2 * d.inter : d.inter;
-  L.nt1 = gated ? d.inter / 64 : cdiv(d.inter, kTileRows);
+  // SwiGLU tiles pair 64 gate rows with their 64 up rows (the last tile of an
+  // inter that is an odd multiple of 32 is half used)
+  L.nt1 = gated ? cdiv(d.inter, 64) : cdiv(d.inter, kTileRows);
   const int block_k = L.gemv ? kGemvBlockK : kBlockK;  // K values per pipeline stage
   L.kb1 = cdiv(d.hidden, block_k);
   L.nt2 = cdiv(d.hidden, kTileRows);
@@ -375,10 +377,10 @@ w4a16_status validate_desc(const w4a16_moe_desc* d) {
   if (d->num_experts < 1 || d->num_experts > 1024)
     return fail(W4A16_ERR_UNSUPPORTED, "num_experts must be in [1, 1024], got %d", d->num_experts);
   if (d->expert_offset < 0) return fail(W4A16_ERR_INVALID_ARG, "expert_offset must be >= 0");
-  if (d->hidden <= 0 || d->hidden % 64 != 0)
-    return fail(W4A16_ERR_UNSUPPORTED, "hidden must be a positive multiple of 64, got %d", d->hidden);
-  if (d->inter <= 0 || d->inter % 64 != 0)
-    return fail(W4A16_ERR_UNSUPPORTED, "inter must be a positive multiple of 64, got %d", d->inter);
+  if (d->hidden <= 0 || d->hidden % 32 != 0)
+    return fail(W4A16_ERR_UNSUPPORTED, "hidden must be a positive multiple of 32, got %d", d->hidden);
+  if (d->inter <= 0 || d->inter % 32 != 0)
+    return fail(W4A16_ERR_UNSUPPORTED, "inter must be a positive multiple of 32, got %d", d->inter);
   if (d->top_k < 1 || d->top_k > 16)
     return fail(W4A16_ERR_UNSUPPORTED, "top_k must be in [1, 16], got %d", d->top_k);
   if (d->max_tokens < 1 || d->max_tokens > 65536)

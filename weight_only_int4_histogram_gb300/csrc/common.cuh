@@ -373,6 +373,29 @@ __device__ __forceinline__ void cp_async(void* dst, const void* src) {
                : "memory");
 }
 
+// The BF16 group scales of one row for one stage: nbytes (even, <= 16) from
+// global src into the 16-byte shared slot dst, the rest zeroed.  One 16-byte
+// cp.async when the piece is whole and 16-byte aligned, 4-byte cp.async
+// pieces when it is 4-byte aligned, else 16-bit loads and stores (rows of an
+// odd number of groups -- K an odd multiple of 32 -- are only 2-byte
+// aligned).  The caller then arrives on the stage barrier with
+// cp.async.mbarrier.arrive (which waits for the copies) and, after a
+// __syncwarp, publishes the plain stores through one lane's release arrive.
+__device__ __forceinline__ void copy_scale_piece(uint8_t* dst, const uint8_t* src, int nbytes) {
+  const uintptr_t a = reinterpret_cast<uintptr_t>(src);
+  if (nbytes == 16 && (a & 15) == 0) {
+    cp_async<16>(dst, src);
+    return;
+  }
+  if ((a & 3) == 0 && (nbytes & 3) == 0) {
+    for (int o = 0; o < nbytes; o += 4) cp_async<4>(dst + o, src + o);
+  } else {
+    for (int o = 0; o < nbytes; o += 2)
+      *reinterpret_cast<uint16_t*>(dst + o) = *reinterpret_cast<const uint16_t*>(src + o);
+  }
+  for (int o = nbytes; o < 16; o += 2) *reinterpret_cast<uint16_t*>(dst + o) = 0;
+}
+
 // 16-byte copy that bypasses L1; copies src_bytes (0 or 16) and zero-fills the rest.
 __device__ __forceinline__ void cp_async_cg16(void* dst, const void* src, uint32_t src_bytes) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src),

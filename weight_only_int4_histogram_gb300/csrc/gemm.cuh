@@ -431,13 +431,7 @@ __global__ void __launch_bounds__(WHICH == GEMM_DOWN ? kGemmThreadsDown : kGemmT
               uint8_t* dst = sS + tr * 16;
               const uint8_t* src = reinterpret_cast<const uint8_t*>(p.scales) +
                                    (static_cast<int64_t>(e) * N1 + grow) * sbytes_row + g0 * 2;
-              const int nbytes = grow < N1 ? max(ng, 0) * 2 : 0;
-              if (nbytes == 16 && (reinterpret_cast<uintptr_t>(src) & 15) == 0) {
-                cp_async<16>(dst, src);
-              } else {
-                for (int o = 0; o < nbytes; o += 4) cp_async<4>(dst + o, src + o);
-                for (int o = nbytes; o < 16; o += 4) *reinterpret_cast<uint32_t*>(dst + o) = 0u;
-              }
+              copy_scale_piece(dst, src, grow < N1 ? max(ng, 0) * 2 : 0);
             }
           }
           cp_async_mbar_arrive(&full[st]);

@@ -605,13 +605,8 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
             uint8_t* dst = sS + tr * kGvScaleRowBytes;
             const uint8_t* src = reinterpret_cast<const uint8_t*>(p.scales) +
                                  (static_cast<int64_t>(e) * N1 + grow) * sbytes_row + g0 * 2;
-            const int nbytes = grow < N1 ? max(ng, 0) * 2 : 0;
-            if (nbytes == kGvScaleRowBytes && (reinterpret_cast<uintptr_t>(src) & 15) == 0) {
-              cp_async_cg16(dst, src, 16u);
-            } else {
-              for (int o = 0; o < nbytes; o += 4) cp_async<4>(dst + o, src + o);
-              for (int o = nbytes; o < kGvScaleRowBytes; o += 4) *reinterpret_cast<uint32_t*>(dst + o) = 0u;
-            }
+            static_assert(kGvScaleRowBytes == 16, "one 16-byte scale piece per row and stage");
+            copy_scale_piece(dst, src, grow < N1 ? max(ng, 0) * 2 : 0);
           }
           cp_async_mbar_arrive(&full[slot]);
         }
