@@ -471,8 +471,10 @@ __global__ void __launch_bounds__(WHICH == GEMM_DOWN ? kGemmThreadsDown : kGemmT
         __syncwarp();
       }
     }
-    // Wind-down after an abort: wait (bounded) for the copies still in flight.
-    if (!ok && lane == 0) {
+    // Wind-down: wait (bounded) until the copies of the last stages have
+    // landed -- at once after a normal run (the dequantisation warps consumed
+    // them), while copies may still be in flight after an abort.
+    if (lane == 0) {
       volatile int no_abort = 0;
       for (uint32_t j = (it > (uint32_t)stages ? it - stages : 0); j < it; ++j)
         mbar_wait(&full[j % stages], (j / stages) & 1, &no_abort, p.err);

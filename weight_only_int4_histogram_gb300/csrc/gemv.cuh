@@ -45,6 +45,12 @@
 //   warp 1      activation rows: cp.async of the tile's rows (gate/up: token
 //               rows of x by slot; down: intermediate rows), completion
 //               signalled on the stage's mbarrier without blocking the warp
+//   One mbarrier per stage completes on the producer's TMA bytes and arrival
+//   plus one cp.async-tracked arrival per lane of warp 1, so the compute warps
+//   wait once per stage (two waits per stage cost ~7 % at 8 to 256 tokens:
+//   every poll takes issue slots from the dequantisation).  After an abort
+//   warp 1 completes, without copying, the arrivals it owes to stages the
+//   producer issued, so that the producer can drain its copies.
 //   warps 2-17  compute: warp 2 + c is in group c / 8 and takes row block
 //               c % 8 (16 rows: MMA rows g and g + 8).  For SwiGLU a row block
 //               holds 8 gate rows and their 8 up rows, so the activation is
@@ -65,6 +71,9 @@ static_assert(kGvRouteBytes == 576, "stage size formula");
 constexpr int kGemvMaxNB = kGemvMaxR / 8;
 constexpr int kGemvComputeWarps = 16;
 static_assert(kGemvThreads == 32 * (2 + kGemvComputeWarps), "warp roles");
+// Arrivals that complete a stage: the producer's expect-tx arrival and one
+// cp.async-tracked arrival per lane of the activation warp.
+constexpr int kGvFullArrivals = 1 + 32;
 // Control block: mbarriers and flags, then the tile records of the CTA's first
 // kGemvTileTab units from kGvCtrlTabOff, then (units of several stages) the
 // K-half exchange from kGvCtrlRedOff: two buffers of 8 warps x NB blocks x 32
@@ -72,7 +81,9 @@ static_assert(kGemvThreads == 32 * (2 + kGemvComputeWarps), "warp roles");
 constexpr int kGvCtrlTabOff = 512;
 constexpr int kGvCtrlRedOff = kGemvCtrlBytes;
 constexpr int kGemvTileTab = 256;
-static_assert(3 * kGemvMaxStages * 8 + 8 + 8 <= kGvCtrlTabOff, "control block");
+// mbarriers full / empty, the group barrier, abort and fix-up flags, the
+// producer's stage counts per ring and its stop flag
+static_assert(2 * kGemvMaxStages * 8 + 8 + 8 + 12 <= kGvCtrlTabOff, "control block");
 static_assert(kGvCtrlTabOff + kGemvTileTab * 16 <= kGemvCtrlBytes, "tile table");
 static_assert(kGemvTileTab <= kGemvThreads, "one record per thread");
 static_assert(gemv_smem_bytes(kGemvMaxR, true) <= kGemvSmemLimit && gemv_stages(kGemvMaxR, true) >= 4, "smem");
@@ -453,8 +464,7 @@ __device__ __forceinline__ bool gemv_epilogue(const GemmParams& p, uint64_t* epi
 // than one phase away, and the producer refills a slot only after all of its
 // consumers left it.
 template <int WHICH, int SCALE, int DT, int LAYOUT, int NB>
-__device__ __forceinline__ bool gemv_unit(const GemmParams& p, uint8_t* smem, uint64_t* full, uint64_t* bfull,
-                                          uint64_t* empty, uint64_t* epibar, volatile int* abort_flag,
+__device__ __forceinline__ bool gemv_unit(const GemmParams& p, uint8_t* smem, uint64_t* full, uint64_t* empty, uint64_t* epibar, volatile int* abort_flag,
                                           volatile int* fixup_flag, float* red, const GvUnit& w, const int4& ti,
                                           bool alt, int grp, int rowA, int rowB, int rb, int lane,
                                           uint32_t ld_row_off, int ld_row7, int ld_chunk, int ring0, int ring_len,
@@ -464,9 +474,7 @@ __device__ __forceinline__ bool gemv_unit(const GemmParams& p, uint8_t* smem, ui
   for (int j = 0; j < 4 * NB; ++j) tot[j] = 0.0f;
   for (int kb = w.kb0; kb < w.kb1; ++kb) {
     const int slot = ring0 + st;
-    if (!warp_wait(&full[slot], ph, abort_flag, p.err, p.wait_ns) ||
-        !warp_wait(&bfull[slot], ph, abort_flag, p.err, p.wait_ns))
-      return false;
+    if (!warp_wait(&full[slot], ph, abort_flag, p.err, p.wait_ns)) return false;
     const uint8_t* sA = smem + slot * p.stage_bytes;
     if (alt) gemv_stage<SCALE, DT, LAYOUT, NB, true>(sA, rowA, rowB, grp, lane, ld_row_off, ld_row7, ld_chunk, tot);
     else gemv_stage<SCALE, DT, LAYOUT, NB, false>(sA, rowA, rowB, grp, lane, ld_row_off, ld_row7, ld_chunk, tot);
@@ -514,11 +522,12 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
   const int stages = p.stages;
   uint8_t* ctrl = smem + stages * p.stage_bytes;
   uint64_t* full = reinterpret_cast<uint64_t*>(ctrl);
-  uint64_t* bfull = full + kGemvMaxStages;
-  uint64_t* empty = bfull + kGemvMaxStages;
+  uint64_t* empty = full + kGemvMaxStages;
   uint64_t* epibar = empty + kGemvMaxStages;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(epibar + 1);
   volatile int* fixup_flag = abort_flag + 1;
+  volatile int* prod_issued = fixup_flag + 1;  // [2]: stages the producer issued per ring
+  volatile int* prod_stopped = prod_issued + 2;
   int4* tile_tab = reinterpret_cast<int4*>(ctrl + kGvCtrlTabOff);
   float* red = reinterpret_cast<float*>(ctrl + kGvCtrlRedOff);
   // single-stage units without split: the compute groups take alternate units,
@@ -532,13 +541,13 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < stages; ++s) {
-      mbar_init(&full[s], 1);                    // producer (TMA bytes + scale copies)
-      mbar_init(&bfull[s], 32);                  // the 32 lanes' activation copies
+      mbar_init(&full[s], kGvFullArrivals);      // producer (TMA bytes) + activation copies
       mbar_init(&empty[s], alt ? kGemvComputeWarps / 2 : kGemvComputeWarps);  // the ring's consumers
     }
     mbar_init(epibar, kGemvComputeWarps);
     *abort_flag = 0;
     *fixup_flag = 0;
+    *prod_stopped = 0;
     fence_barrier_init();
   }
   if (warp == 0 && lane == 0) {
@@ -645,8 +654,16 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
         ph_r0 = ph;
       }
     }
-    // Wind-down after an abort: wait (bounded) for the copies still in flight.
-    if (!ok && lane == 0) {
+    // Wind-down: publish the stage counts for warp 1 (which owes the stages
+    // it did not reach after an abort their arrivals), then wait (bounded)
+    // until the copies of the last stages of each ring have landed -- after
+    // a normal run the compute warps consumed them all and the waits return
+    // at once; after an abort copies may still be in flight.
+    if (lane == 0) {
+      prod_issued[0] = static_cast<int>(issued_r0);
+      prod_issued[1] = static_cast<int>(issued_r1);
+      __threadfence_block();
+      *prod_stopped = 1;
       volatile int no_abort = 0;
       auto drain = [&](int r, uint32_t n) {
         const uint32_t from = n > static_cast<uint32_t>(ring_len) ? n - ring_len : 0;
@@ -660,11 +677,12 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
     // ------------------------------------------------------------------ activation rows
     // One route row per pass, 8 K values (16 B) per lane, straight from x (by
     // token) or the intermediate (by slot) with cp.async; out-of-range K is
-    // zero-filled by the copy.  Each lane's cp.async.mbarrier.arrive marks the
-    // stage's bfull once its copies have landed; the warp never blocks on them.
+    // zero-filled by the copy.  Each lane's cp.async.mbarrier.arrive counts as one
+    // of the stage's arrivals once its copies have landed; the warp never
+    // blocks on them.
     const uint16_t* xsrc = reinterpret_cast<const uint16_t*>(p.x);
     int st_r0 = 0, st_r1 = 0;
-    uint32_t ph_r0 = 0, ph_r1 = 0;
+    uint32_t ph_r0 = 0, ph_r1 = 0, done_r0 = 0, done_r1 = 0;
     bool ok = true;
     // source row of route `lane` of a tile (lanes below its route count)
     auto src_of = [&](const int4& t) -> int {
@@ -705,7 +723,9 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
           cp_async_cg16(xs + r * kGvRouteBytes + lane * 16,
                         xsrc + static_cast<int64_t>(srow) * p.K + (valid ? col : 0), valid ? 16u : 0u);
         }
-        cp_async_mbar_arrive_noinc(&bfull[slot]);
+        cp_async_mbar_arrive_noinc(&full[slot]);
+        if (ring) ++done_r1;
+        else ++done_r0;
         ring_next(st, ph, ring_len);
       }
       if (ring) {
@@ -719,8 +739,23 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
       const int u_next = u + G;
       if (u_next < n_units) src_next = src_of(tile_of(p, tile_tab, i + 1, u_next));
     }
-    // Every copy lands before the CTA exits (bounded by the compute warps'
-    // waits on bfull; the final barrier below follows them).
+    // After an abort: the arrivals owed to stages the producer issued beyond
+    // this warp's last one (the producer is at most a ring ahead: a stage is
+    // released only after its activation copies).
+    if (!ok && lane == 0) {
+      const uint64_t t0 = global_timer_ns();
+      while (!*prod_stopped && global_timer_ns() - t0 < kWaitTimeoutNs) {
+      }
+      if (*prod_stopped) {
+        __threadfence_block();
+        auto owe = [&](int r, uint32_t from, uint32_t to) {
+          for (uint32_t j = from; j < to; ++j) mbar_arrive_cnt(&full[r * ring_len + j % ring_len], 32);
+        };
+        owe(0, done_r0, static_cast<uint32_t>(prod_issued[0]));
+        if (alt) owe(1, done_r1, static_cast<uint32_t>(prod_issued[1]));
+      }
+    }
+    // Every copy lands before the CTA exits.
     asm volatile("cp.async.wait_all;" ::: "memory");
   } else {
     // ------------------------------------------------------------------ compute + epilogue
@@ -749,7 +784,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
       const int nb = (min(ti.z, kGemvMaxR) + 7) >> 3;
       bool ok;
 #define W4A16_GEMV_UNIT(NBV)                                                                                    \
-  gemv_unit<WHICH, SCALE, DT, LAYOUT, NBV>(p, smem, full, bfull, empty, epibar, abort_flag, fixup_flag, red, w, ti, alt, \
+  gemv_unit<WHICH, SCALE, DT, LAYOUT, NBV>(p, smem, full, empty, epibar, abort_flag, fixup_flag, red, w, ti, alt, \
                                    grp, rowA, rowB, rb, lane, ld_row_off, ld_row7, ld_chunk, ring0, ring_len, st, \
                                    ph, eph)
       if (nb <= 1) ok = W4A16_GEMV_UNIT(1);
