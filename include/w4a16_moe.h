@@ -208,6 +208,8 @@ typedef struct {
   size_t off_inter;        /* intermediate activations [max_slots, I] (act dtype) */
   size_t off_expert_out;   /* expert outputs [max_slots, H] in the activation dtype, or FP32
                               split partials [gemm2_splits, max_slots, H] when gemm2_splits > 1 */
+  int32_t fused_gemms;     /* 1: CUDA-core path with both GEMMs in one launch (then
+                              gemm1_ctas = gemm2_ctas = that launch's grid) */
 } w4a16_route_info;
 
 w4a16_status w4a16_moe_route_info(w4a16_moe_plan_t plan, int32_t num_tokens,

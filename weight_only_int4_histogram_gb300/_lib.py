@@ -64,6 +64,7 @@ class RouteInfo(ctypes.Structure):
         ("off_perm", ctypes.c_size_t), ("off_inv", ctypes.c_size_t),
         ("off_tiles", ctypes.c_size_t), ("off_num_tiles", ctypes.c_size_t),
         ("off_inter", ctypes.c_size_t), ("off_expert_out", ctypes.c_size_t),
+        ("fused_gemms", ctypes.c_int32),
     ]
 
 

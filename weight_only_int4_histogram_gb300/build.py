@@ -19,7 +19,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libw4a16_moe.so")
 SOURCES = ["api.cu", "route_prep.cu", "gemm_bf16.cu", "gemm_fp16.cu", "gemm_bf16_il.cu", "gemm_fp16_il.cu",
-           "gemv_bf16.cu", "gemv_fp16.cu", "gemv_bf16_il.cu", "gemv_fp16_il.cu", "combine.cu", "router.cu",
+           "gemv_bf16.cu", "gemv_fp16.cu", "gemv_bf16_il.cu", "gemv_fp16_il.cu", "gemv_fused_bf16.cu",
+           "gemv_fused_fp16.cu", "gemv_fused_bf16_il.cu", "gemv_fused_fp16_il.cu", "combine.cu", "router.cu",
            "relayout.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

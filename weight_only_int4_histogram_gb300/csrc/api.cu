@@ -35,6 +35,8 @@ struct w4a16_moe_plan_s {
   uint64_t wait_ns;  // limit of the GEMM pipelines' bounded waits
   size_t ws_bytes;
   bool pdl;
+  bool fused;        // CUDA-core path: both GEMMs in one launch
+  int ov_chunk;      // tuning: down weight tiles per fused queue entry (0 = automatic)
   cudaEvent_t ev[4];
   bool has_ev;
 };
@@ -62,6 +64,9 @@ int cdiv(int a, int b) { return (a + b - 1) / b; }
 
 struct Layout {
   bool gemv;  // CUDA-core path for both GEMMs
+  bool fused;       // CUDA-core path: both GEMMs in one launch (gemv_fused.cuh)
+  int down_chunk;   // fused: down weight tiles per queue entry
+  int ctr_len;      // counters zeroed by route preparation
   int T, R, bn, tiles_cap;
   int64_t slots_cap;
   int n1;
@@ -162,6 +167,20 @@ int choose_bn(const w4a16_moe_plan_s& P, int T) {
   return std::min(kAutoMaxBN, std::max(16, bn));
 }
 
+// Gate/up split-K factor of the fused CUDA-core launch: the smallest that
+// gives every SM a gate/up queue entry (the down entries wait for the gate/up
+// rows of their route tile, so SMs without gate/up work would idle until the
+// first route tiles are done), at most kMaxFusedSplits.
+int choose_fused_splits(double tiles_est, int nt1, int kb, int num_sms) {
+  int best = 1;
+  for (int s = 1; s <= std::min(kb, kMaxFusedSplits); ++s) {
+    if (cdiv(kb, cdiv(kb, s)) != s) continue;
+    best = s;
+    if (tiles_est * nt1 * s >= num_sms) break;
+  }
+  return best;
+}
+
 // Split-K factor for the expected number of route tiles: the cost model is
 // (waves of units) x (K blocks per unit + per-unit overhead); among factors
 // within 5% of the cheapest, the smallest wins (splits add partial traffic).
@@ -218,16 +237,30 @@ Layout make_layout(const w4a16_moe_plan_s& P, int T) {
               nt, ab);
     g2 = cdiv(L.nt2, nt);
   }
-  L.s1 = P.ov_s1 ? P.ov_s1 : choose_splits(tiles_est, g1, L.kb1, P.num_sms, 1.5);
-  L.s2 = P.ov_s2 ? P.ov_s2 : choose_splits(tiles_est, g2, L.kb2, P.num_sms, 1.0);
+  L.fused = L.gemv && P.fused;
+  if (L.fused) {
+    L.s1 = P.ov_s1 ? std::min(P.ov_s1, kMaxFusedSplits) : choose_fused_splits(tiles_est, L.nt1, L.kb1, P.num_sms);
+    // every split must own K blocks: each one's arrival completes its row blocks
+    L.s1 = cdiv(L.kb1, cdiv(L.kb1, L.s1));
+    L.s2 = 1;  // the down GEMM is balanced by the queue instead
+    L.down_chunk = P.ov_chunk > 0 ? P.ov_chunk : (L.kb2 == 1 ? 4 : 1);
+  } else {
+    L.s1 = P.ov_s1 ? P.ov_s1 : choose_splits(tiles_est, g1, L.kb1, P.num_sms, 1.5);
+    L.s2 = P.ov_s2 ? P.ov_s2 : choose_splits(tiles_est, g2, L.kb2, P.num_sms, 1.0);
+  }
   L.kbps1 = cdiv(L.kb1, L.s1);
   L.kbps2 = cdiv(L.kb2, L.s2);
   if (L.gemv) {
     // K-half exchange buffers unless both GEMMs have single-stage units only
-    const bool ksplit = !(L.kb1 == 1 && L.s1 == 1 && L.kb2 == 1 && L.s2 == 1);
+    const bool ksplit = L.fused || !(L.kb1 == 1 && L.s1 == 1 && L.kb2 == 1 && L.s2 == 1);
     L.stage_bytes = gemv_stage_bytes(L.bn);
     L.stages = gemv_stages(L.bn, ksplit);
     L.smem = gemv_smem_bytes(L.bn, ksplit);
+    if (L.fused) {
+      // the two compute groups take the stages of their parity: an even ring
+      L.stages &= ~1;
+      L.smem = 1024 + L.stages * L.stage_bytes + gemv_ctrl_bytes(L.bn, true);
+    }
     L.stages2 = L.stages;
     L.smem2 = L.smem;
     L.ntu1 = L.ntu2 = 1;
@@ -251,6 +284,10 @@ Layout make_layout(const w4a16_moe_plan_s& P, int T) {
   const int64_t units2 = static_cast<int64_t>(L.tiles_cap) * cdiv(L.nt2, L.ntu2) * L.s2;
   L.grid1 = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(P.num_sms, units1)));
   L.grid2 = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(P.num_sms, units2)));
+  if (L.fused) L.grid1 = L.grid2 = P.num_sms;  // one queue for both GEMMs
+  // split-K arrival counters; the fused launch adds its queue head (padded to
+  // 32 entries), the ready counts of the route tiles and per-row-block counters
+  L.ctr_len = L.fused ? 32 + L.tiles_cap + L.tiles_cap * L.nt1 * 8 : L.tiles_cap * L.nt1;
 
   const int act_bytes = 2;
   size_t o = 0;
@@ -266,7 +303,7 @@ Layout make_layout(const w4a16_moe_plan_s& P, int T) {
   L.off_tiles = take(sizeof(int32_t) * 4 * L.tiles_cap);
   L.off_perm = take(sizeof(int32_t) * L.slots_cap);
   L.off_inv = take(sizeof(int32_t) * std::max(L.R, 1));
-  L.off_ctr = take(sizeof(int32_t) * L.tiles_cap * L.nt1);
+  L.off_ctr = take(sizeof(int32_t) * L.ctr_len);
   L.off_chist = take(sizeof(int32_t) * kRouteMaxCtas * E);
   L.off_part = take(L.s1 > 1 ? sizeof(float) * L.s1 * L.slots_cap * L.n1 : 0);
   L.off_inter = take(static_cast<size_t>(act_bytes) * L.slots_cap * d.inter);
@@ -428,7 +465,7 @@ w4a16_status launch_prepare(const w4a16_moe_plan_s& P, const Layout& L, const in
   rp.tiles = reinterpret_cast<int4*>(ws + L.off_tiles);
   rp.num_tiles = reinterpret_cast<int32_t*>(ws + L.off_ntiles);
   rp.counters = reinterpret_cast<int32_t*>(ws + L.off_ctr);
-  rp.ctr_len = L.tiles_cap * L.nt1;
+  rp.ctr_len = L.ctr_len;
   rp.err = reinterpret_cast<int32_t*>(ws + L.off_err);
   rp.cta_hist = reinterpret_cast<int32_t*>(ws + L.off_chist);
   route_ctas(L.T, P.d.top_k, logits != nullptr, rp.n_cta, rp.tpc);
@@ -439,6 +476,68 @@ w4a16_status launch_prepare(const w4a16_moe_plan_s& P, const Layout& L, const in
   cudaError_t e = launch_route_prep(rp, s, P.pdl);
   if (e != cudaSuccess) return cuda_fail(e, "route preparation launch");
   return W4A16_OK;
+}
+
+// Expert outputs -> output rows: the deterministic weighted combine.
+w4a16_status launch_combine_of(const w4a16_moe_plan_s& P, const Layout& L, bool y16, const float* tw, int32_t renorm,
+                               void* out, uint8_t* ws, cudaStream_t s) {
+  CombineParams c = {};
+  c.y = ws + L.off_y;
+  c.y16 = y16 ? 1 : 0;
+  c.slots_cap = L.slots_cap;
+  c.splits = L.s2;
+  c.inv = reinterpret_cast<const int32_t*>(ws + L.off_inv);
+  c.topk_weights = tw;
+  c.T = L.T;
+  c.H = P.d.hidden;
+  c.k = P.d.top_k;
+  c.renormalize = renorm ? 1 : 0;
+  c.out = out;
+  if (L.fused) {
+    c.zero = reinterpret_cast<int32_t*>(ws + L.off_ctr);
+    c.zero_len = L.ctr_len;
+  }
+  cudaError_t e = launch_combine(P.d.act_dtype, c, s, P.pdl);
+  if (e != cudaSuccess) return cuda_fail(e, "combine launch");
+  if (P.has_ev && (e = cudaEventRecord(P.ev[3], s)) != cudaSuccess) return cuda_fail(e, "event record");
+  return W4A16_OK;
+}
+
+// CUDA-core path, both GEMMs in one launch (gemv_fused.cuh), then the combine.
+w4a16_status launch_forward_fused(const w4a16_moe_plan_s& P, const Layout& L, const GemmParams& g,
+                                  const GemmParams& g1, const CUtensorMap& tmA1, const CUtensorMap& tmS1,
+                                  const CUtensorMap& tmA2, const CUtensorMap& tmS2, bool stma2, const uint16_t* s2,
+                                  const float* tw, int32_t renorm, void* out, uint8_t* ws, cudaStream_t s) {
+  const w4a16_moe_desc& d = P.d;
+  FusedParams fp = {};
+  fp.up = g1;
+  fp.down = g;
+  fp.down.n_rows = d.hidden;
+  fp.down.K = d.inter;
+  fp.down.out_cols = d.hidden;
+  fp.down.n_tiles = L.nt2;
+  fp.down.n_groups = L.nt2;
+  fp.down.kb_total = L.kb2;
+  fp.down.splits = 1;
+  fp.down.kb_per_split = L.kb2;
+  fp.down.x = ws + L.off_inter;
+  fp.down.scales = s2;
+  fp.down.out = ws + L.off_y;
+  fp.down.scale_tma = stma2 ? 1 : 0;
+  fp.down.out16 = 1;
+  int32_t* ctr = reinterpret_cast<int32_t*>(ws + L.off_ctr);
+  fp.queue = ctr;
+  fp.ready = ctr + 32;
+  fp.fix = ctr + 32 + L.tiles_cap;
+  fp.down_chunk = L.down_chunk;
+  const int lay = P.layout == W4A16_LAYOUT_INTERLEAVED ? LAYOUT_IL : LAYOUT_CANON;
+  cudaError_t e =
+      launch_gemv_fused(d.scale_kind, d.act_dtype, lay, fp, tmA1, tmS1, tmA2, tmS2, L.grid1, L.smem, s, P.pdl);
+  if (e != cudaSuccess) return cuda_fail(e, "fused expert GEMM launch");
+  // both GEMMs end with the one launch: the gate/up and down stage marks coincide
+  if (P.has_ev && ((e = cudaEventRecord(P.ev[1], s)) != cudaSuccess || (e = cudaEventRecord(P.ev[2], s)) != cudaSuccess))
+    return cuda_fail(e, "event record");
+  return launch_combine_of(P, L, true, tw, renorm, out, ws, s);
 }
 
 w4a16_status launch_forward(const w4a16_moe_plan_s& P, const Layout& L, const void* x,
@@ -517,6 +616,7 @@ w4a16_status launch_forward(const w4a16_moe_plan_s& P, const Layout& L, const vo
   g1.scale_tma = stma1 ? 1 : 0;
   cudaError_t e;
   if (P.has_ev && (e = cudaEventRecord(P.ev[0], s)) != cudaSuccess) return cuda_fail(e, "event record");
+  if (L.fused) return launch_forward_fused(P, L, g, g1, tmA1, tmS1, tmA2, tmS2, stma2, s2, tw, renorm, out, ws, s);
   e = L.gemv ? launch_gemv(GEMM_UP, d.scale_kind, d.act_dtype, lay, g1, tmA1, tmS1, L.grid1, L.smem, s, P.pdl)
              : launch_gemm(GEMM_UP, d.scale_kind, d.act_dtype, lay, g1, tmA1, tmNone, tmY, tmS1, L.grid1, L.smem, s,
                            P.pdl);
@@ -549,22 +649,7 @@ w4a16_status launch_forward(const w4a16_moe_plan_s& P, const Layout& L, const vo
   if (e != cudaSuccess) return cuda_fail(e, "down GEMM launch");
   if (P.has_ev && (e = cudaEventRecord(P.ev[2], s)) != cudaSuccess) return cuda_fail(e, "event record");
 
-  CombineParams c = {};
-  c.y = ws + L.off_y;
-  c.y16 = y16 ? 1 : 0;
-  c.slots_cap = L.slots_cap;
-  c.splits = L.s2;
-  c.inv = reinterpret_cast<const int32_t*>(ws + L.off_inv);
-  c.topk_weights = tw;
-  c.T = L.T;
-  c.H = d.hidden;
-  c.k = d.top_k;
-  c.renormalize = renorm ? 1 : 0;
-  c.out = out;
-  e = launch_combine(d.act_dtype, c, s, P.pdl);
-  if (e != cudaSuccess) return cuda_fail(e, "combine launch");
-  if (P.has_ev && (e = cudaEventRecord(P.ev[3], s)) != cudaSuccess) return cuda_fail(e, "event record");
-  return W4A16_OK;
+  return launch_combine_of(P, L, y16, tw, renorm, out, ws, s);
 }
 
 }  // namespace
@@ -616,6 +701,32 @@ cudaError_t launch_gemv(int which, int scale_kind, int dtype, int layout, const 
   return dtype == DT_BF16 ? launch_gemv_dt<DT_BF16, LAYOUT_CANON>(which, scale_kind, p, tmA, tmS, grid, smem_bytes, s, pdl)
                           : launch_gemv_dt<DT_FP16, LAYOUT_CANON>(which, scale_kind, p, tmA, tmS, grid, smem_bytes, s, pdl);
 }
+
+template <int DT, int LAYOUT>
+cudaError_t launch_gemv_fused_dt(int scale_kind, const FusedParams& fp, const CUtensorMap& tmA1,
+                                 const CUtensorMap& tmS1, const CUtensorMap& tmA2, const CUtensorMap& tmS2, int grid,
+                                 int smem_bytes, cudaStream_t s, bool pdl);
+#define W4A16_FUSED_EXTERN(DT, LAYOUT)                                                                          \
+  extern template cudaError_t launch_gemv_fused_dt<DT, LAYOUT>(int, const FusedParams&, const CUtensorMap&,    \
+                                                               const CUtensorMap&, const CUtensorMap&,         \
+                                                               const CUtensorMap&, int, int, cudaStream_t, bool);
+W4A16_FUSED_EXTERN(DT_BF16, LAYOUT_CANON)
+W4A16_FUSED_EXTERN(DT_FP16, LAYOUT_CANON)
+W4A16_FUSED_EXTERN(DT_BF16, LAYOUT_IL)
+W4A16_FUSED_EXTERN(DT_FP16, LAYOUT_IL)
+#undef W4A16_FUSED_EXTERN
+
+cudaError_t launch_gemv_fused(int scale_kind, int dtype, int layout, const FusedParams& p, const CUtensorMap& tmA1,
+                              const CUtensorMap& tmS1, const CUtensorMap& tmA2, const CUtensorMap& tmS2, int grid,
+                              int smem_bytes, cudaStream_t s, bool pdl) {
+  if (layout == LAYOUT_IL)
+    return dtype == DT_BF16
+               ? launch_gemv_fused_dt<DT_BF16, LAYOUT_IL>(scale_kind, p, tmA1, tmS1, tmA2, tmS2, grid, smem_bytes, s, pdl)
+               : launch_gemv_fused_dt<DT_FP16, LAYOUT_IL>(scale_kind, p, tmA1, tmS1, tmA2, tmS2, grid, smem_bytes, s, pdl);
+  return dtype == DT_BF16
+             ? launch_gemv_fused_dt<DT_BF16, LAYOUT_CANON>(scale_kind, p, tmA1, tmS1, tmA2, tmS2, grid, smem_bytes, s, pdl)
+             : launch_gemv_fused_dt<DT_FP16, LAYOUT_CANON>(scale_kind, p, tmA1, tmS1, tmA2, tmS2, grid, smem_bytes, s, pdl);
+}
 }  // namespace w4a16
 
 extern "C" {
@@ -636,6 +747,8 @@ w4a16_status w4a16_moe_plan(const w4a16_moe_desc* desc, w4a16_moe_plan_t* out, s
     cudaGetLastError();  // no device here: plan with the GB300 SM count
   }
   P->pdl = env_flag("W4A16_MOE_PDL", true);
+  P->fused = env_flag("W4A16_MOE_FUSED", true);
+  if (const char* v = getenv("W4A16_MOE_DOWN_CHUNK")) P->ov_chunk = std::max(0, atoi(v));
   P->layout = W4A16_LAYOUT_CHECKPOINT;
   // tuning knobs for measurements: weight tiles per tensor-core unit of each GEMM
   if (const char* v = getenv("W4A16_MOE_NT_GATE_UP")) P->ov_nt1 = atoi(v);
@@ -697,6 +810,7 @@ w4a16_status w4a16_moe_route_info(w4a16_moe_plan_t plan, int32_t num_tokens, w4a
   info->gemm2_ctas = L.grid2;
   info->pipeline_stages = L.stages;
   info->gemm_path = L.gemv ? W4A16_PATH_CUDA_CORES : W4A16_PATH_TENSOR_CORES;
+  info->fused_gemms = L.fused ? 1 : 0;
   info->off_counts = L.off_counts;
   info->off_offs = L.off_offs;
   info->off_perm = L.off_perm;

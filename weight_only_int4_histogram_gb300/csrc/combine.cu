@@ -61,6 +61,10 @@ template <int DT, bool Y16>
 __global__ void __launch_bounds__(256) combine_kernel(const CombineParams p) {
   pdl_wait();
   pdl_launch_dependents();
+  // the fused expert launch's queue state, reset for a forward that reuses
+  // this route layout (that launch has completed: pdl_wait)
+  if (blockIdx.x == 0 && blockIdx.y == 0)
+    for (int i = threadIdx.x; i < p.zero_len; i += blockDim.x) p.zero[i] = 0;
   const int t = blockIdx.x;
   const int c = (blockIdx.y * blockDim.x + threadIdx.x) * 4;
   if (c >= p.H) return;

@@ -150,6 +150,17 @@ struct GemmParams {
   uint64_t wait_ns;        // limit of every pipeline wait (drains use kWaitTimeoutNs)
 };
 
+// Both CUDA-core GEMMs in one launch (gemv_fused.cuh).
+constexpr int kMaxFusedSplits = 8;  // gate/up split-K factor of the fused launch
+struct FusedParams {
+  GemmParams up;           // gate/up GEMM: x -> intermediate (split-K partials in up.part)
+  GemmParams down;         // down GEMM: intermediate -> expert outputs y (activation dtype)
+  int32_t* queue;          // [1] work-queue head, zeroed by route preparation
+  int32_t* ready;          // [tiles_cap] published gate/up row blocks per route tile
+  int32_t* fix;            // [tiles_cap * nt1 * 8] split arrivals per (route tile, weight tile, row block)
+  int32_t down_chunk;      // down weight tiles per queue entry
+};
+
 struct CombineParams {
   const void* y;           // [splits, slots_cap, H]: activation dtype when y16, else FP32
   int32_t y16;
@@ -159,6 +170,8 @@ struct CombineParams {
   const float* topk_weights;
   int32_t T, H, k, renormalize;
   void* out;               // [T, H] act dtype
+  int32_t* zero;           // counters to reset once the expert GEMMs are done (or NULL)
+  int32_t zero_len;
 };
 
 // Host-side launchers (one translation unit each).
@@ -169,6 +182,9 @@ cudaError_t launch_gemm(int which, int scale_kind, int dtype, int layout, const 
 cudaError_t launch_gemv(int which, int scale_kind, int dtype, int layout, const GemmParams& p,
                         const CUtensorMap& tmA, const CUtensorMap& tmS, int grid, int smem_bytes,
                         cudaStream_t s, bool pdl);
+cudaError_t launch_gemv_fused(int scale_kind, int dtype, int layout, const FusedParams& p, const CUtensorMap& tmA1,
+                              const CUtensorMap& tmS1, const CUtensorMap& tmA2, const CUtensorMap& tmS2, int grid,
+                              int smem_bytes, cudaStream_t s, bool pdl);
 cudaError_t launch_combine(int dtype, const CombineParams& p, cudaStream_t s, bool pdl);
 // Checkpoint layout -> LAYOUT_IL for one packed weight tensor of E experts x N
 // rows x K values (row_pairs: per-channel [E, N/2, K] input, else [E, N, K/2]).

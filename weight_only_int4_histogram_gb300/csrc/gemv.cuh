@@ -487,7 +487,9 @@ __device__ __forceinline__ bool gemv_unit(const GemmParams& p, uint8_t* smem, ui
     // K halves meet: group 1 leaves its sums in one of two buffers (alternating
     // per unit: a buffer is rewritten only after every warp passed the next
     // barrier, i.e. after group 0 read it); group 0 adds them and finishes.
-    float4* rbuf = reinterpret_cast<float4*>(red) + ((eph & 1) * 8 + rb) * NB * 32 + lane;
+    // (buffers of the plan's largest NB, bn / 8: units of different NB never
+    // overlap in them)
+    float4* rbuf = reinterpret_cast<float4*>(red) + ((eph & 1) * 8 + rb) * (p.bn >> 3) * 32 + lane;
     if (grp == 1) {
 #pragma unroll
       for (int n = 0; n < NB; ++n)

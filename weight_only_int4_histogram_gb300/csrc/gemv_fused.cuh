@@ -1,0 +1,675 @@
+// Both expert GEMMs of a decode-sized batch in one launch on the CUDA-core
+// path (sm_103a): gate/up GEMM + activation, then the down GEMM, fed from one
+// device-side work queue.
+//
+// Same operation as the two launches of gemv.cuh (the "gate/up GEMM" and
+// "down GEMM" of "feat(pytorch): add CuTeDSL W4A16 MoE backend" (LMDeploy),
+// sections Modification and Benchmark; the same stage arithmetic,
+// gemv_stage), for the batches where an expert sees only a few routes and
+// every expert's weights are streamed once.  There two separate launches lose
+// time twice: the second launch starts only after the last gate/up unit of
+// the first has finished (a whole second wave of long gate/up units runs on
+// part of the SMs while the others idle), and every launch pays its own ramp
+// (tile records, first weight bytes).  Here every CTA takes queue entries in
+// order -- all gate/up units first, then the down units -- so SMs that run
+// out of gate/up work stream down weights at once; a down unit needs only the
+// intermediate rows of its route tile, which its activation warp waits for
+// (the weight bytes are fetched meanwhile).
+//
+// Queue (one atomic head per forward, zeroed by route preparation):
+//   entries [0, Q1):   gate/up units (route tile m, weight tile nt, K split s),
+//                      m-major, Q1 = tiles x nt1 x S1
+//   entries [Q1, Qt):  down entries (route tile m, down_chunk consecutive
+//                      weight tiles), m-major
+// Every unit is computed whole by one CTA (split-K partials are summed in
+// split order by the last split), so the result does not depend on which CTA
+// took which entry: forwards are bit-identical.
+//
+// No CTA waits for an entry that no running CTA holds: a down entry is taken
+// only after every gate/up entry has been taken, a CTA issues its entries in
+// the order it took them, and gate/up work never waits on other CTAs.  So the
+// grid needs no co-residency, and every wait is bounded all the same.
+//
+// Pipeline: one ring of stages (weights by TMA, scales, activation rows) with
+// an even length; the compute warps form two groups of 8 and group g consumes
+// the stages of parity g (each warp: 16 weight rows over the stage's 256 K
+// values).  A unit of several stages is split between the groups; at its end
+// the group holding the unit's last stage (the finisher) adds the other
+// group's sums from a double-buffered exchange and runs the epilogue.  Each
+// stage carries a header (unit, K block, tile record) written by the producer.
+//
+// Warp roles (576 threads):
+//   warp 0      producer: takes queue entries, writes stage headers, TMA of
+//               weights and scales (cp.async for unaligned scale rows)
+//   warp 1      activation rows: reads each stage's header; gate/up: token rows
+//               of x by route; down: the route tile's intermediate rows, after
+//               waiting until all of its gate/up row blocks are published
+//   warps 2-17  compute groups 0 and 1 (row block = warp index mod 8)
+//
+// Epilogue signals: each finishing warp publishes its 16 intermediate rows of
+// route tile m with a release increment of ready[m] (8 row blocks x nt1 weight
+// tiles per route tile); with split-K, per-(m, nt, row block) counters elect
+// the last split's warp, which sums the FP32 partials in split order.
+#pragma once
+#include "gemv.cuh"
+
+namespace w4a16 {
+
+constexpr int kItemUp = 0;
+constexpr int kItemDown = 1;
+constexpr int kItemEnd = 2;
+
+// Stage header (written by the producer, read by the activation warp and the
+// compute group of the stage).
+struct StageHdr {
+  int32_t type, m, nt, kb;         // unit kind, route tile, weight tile, K block
+  int32_t e, m0, rows, split;      // tile record (expert, first slot, routes), K split
+  uint32_t first_seq, last_seq;    // stage sequence numbers of the unit's first and last stage
+  int32_t pad[6];
+};
+static_assert(sizeof(StageHdr) == 64, "header size");
+
+// Control block of the fused kernel: mbarriers full / empty / hdr per slot,
+// the exchange barriers, flags, then the stage headers; the exchange buffers
+// follow at kGemvCtrlBytes as in gemv.cuh.
+constexpr int kFzOffFull = 0;
+constexpr int kFzOffEmpty = kFzOffFull + 8 * kGemvMaxStages;
+constexpr int kFzOffHdrBar = kFzOffEmpty + 8 * kGemvMaxStages;
+constexpr int kFzOffXBar = kFzOffHdrBar + 8 * kGemvMaxStages;  // xfull[2], xempty[2]
+constexpr int kFzOffFlags = kFzOffXBar + 32;                    // abort, issued, stopped
+constexpr int kFzOffHdr = 512;
+static_assert(kFzOffFlags + 16 <= kFzOffHdr, "control block");
+static_assert(kFzOffHdr + kGemvMaxStages * 64 <= kGemvCtrlBytes, "stage headers");
+
+__device__ __forceinline__ int ld_acquire_gpu(const int32_t* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Publish the calling warp's earlier global stores (ordered by __syncwarp)
+// with a release increment of *ctr.
+__device__ __forceinline__ void warp_publish(int32_t* ctr, int lane) {
+  __syncwarp();
+  if (lane == 0) {
+    __threadfence();
+    atomicAdd(ctr, 1);
+  }
+  __syncwarp();
+}
+
+// Epilogue of a gate/up unit on one finishing warp (row block rb): the
+// activation of the summed rows into the intermediate, or the FP32 partial of
+// this split and, on the last split, the sum of all partials in split order.
+template <int SCALE, int DT, int NB>
+__device__ __forceinline__ void fused_up_epilogue(const FusedParams& fp, const StageHdr& h, int rowA, int rowB,
+                                                  int rb, int lane, const float (&tot)[4 * NB]) {
+  using T = F16<DT>;
+  const GemmParams& p = fp.up;
+  const int t = lane & 3;
+  const bool gated = p.act == ACT_SWIGLU;
+  const int N1 = p.n_rows;
+  const int rows = min(h.rows, kGemvMaxR);
+  int r0, r1;
+  tile_row_bases<GEMM_UP>(p, h.nt, r0, r1);
+  const int growA = rowA < 64 ? r0 + rowA : r1 + (rowA - 64);
+  const int growB = rowB < 64 ? r0 + rowB : r1 + (rowB - 64);
+  const bool okA = gated ? (64 * h.nt + (rowA & 63)) < p.inter : growA < N1;
+  const bool okB = gated ? okA : growB < N1;
+  float scA = 1.0f, scB = 1.0f;
+  if (SCALE == SCALE_CHANNEL) {
+    if (okA) scA = bf16_bits_to_float(p.scales[static_cast<int64_t>(h.e) * N1 + growA]);
+    if (okB) scB = bf16_bits_to_float(p.scales[static_cast<int64_t>(h.e) * N1 + growB]);
+  }
+  uint16_t* inter = reinterpret_cast<uint16_t*>(p.out) + static_cast<int64_t>(h.m0) * p.inter;
+  auto relu2 = [](float v) {
+    const float a = v > 0.0f ? v : 0.0f;
+    return a * a;
+  };
+  if (p.splits == 1) {
+#pragma unroll
+    for (int n = 0; n < NB; ++n) {
+      const int rt0 = 8 * n + 2 * t, rt1 = rt0 + 1;
+      const float vA0 = tot[4 * n + 0] * scA, vA1 = tot[4 * n + 1] * scA;
+      const float vB0 = tot[4 * n + 2] * scB, vB1 = tot[4 * n + 3] * scB;
+      if (gated) {
+        const int i = 64 * h.nt + (rowA & 63);
+        if (okA) {
+          if (rt0 < rows) inter[static_cast<int64_t>(rt0) * p.inter + i] = T::from_float(silu_f(vA0) * vB0);
+          if (rt1 < rows) inter[static_cast<int64_t>(rt1) * p.inter + i] = T::from_float(silu_f(vA1) * vB1);
+        }
+      } else {
+        if (rt0 < rows && okA) inter[static_cast<int64_t>(rt0) * p.inter + growA] = T::from_float(relu2(vA0));
+        if (rt1 < rows && okA) inter[static_cast<int64_t>(rt1) * p.inter + growA] = T::from_float(relu2(vA1));
+        if (rt0 < rows && okB) inter[static_cast<int64_t>(rt0) * p.inter + growB] = T::from_float(relu2(vB0));
+        if (rt1 < rows && okB) inter[static_cast<int64_t>(rt1) * p.inter + growB] = T::from_float(relu2(vB1));
+      }
+    }
+    warp_publish(fp.ready + h.m, lane);
+    return;
+  }
+  // split-K: this split's scaled sums, then the arrival of this row block
+  float* part = p.part + (static_cast<int64_t>(h.split) * p.slots_cap + h.m0) * N1;
+#pragma unroll
+  for (int n = 0; n < NB; ++n) {
+    const int rt0 = 8 * n + 2 * t, rt1 = rt0 + 1;
+    if (rt0 < rows && okA) part[static_cast<int64_t>(rt0) * N1 + growA] = tot[4 * n + 0] * scA;
+    if (rt1 < rows && okA) part[static_cast<int64_t>(rt1) * N1 + growA] = tot[4 * n + 1] * scA;
+    if (rt0 < rows && okB) part[static_cast<int64_t>(rt0) * N1 + growB] = tot[4 * n + 2] * scB;
+    if (rt1 < rows && okB) part[static_cast<int64_t>(rt1) * N1 + growB] = tot[4 * n + 3] * scB;
+  }
+  __syncwarp();
+  int last = 0;
+  if (lane == 0) {
+    __threadfence();
+    const int prev = atomicAdd(fp.fix + (static_cast<int64_t>(h.m) * p.n_tiles + h.nt) * 8 + rb, 1);
+    last = prev == p.splits - 1;
+    if (last) __threadfence();
+  }
+  last = __shfl_sync(0xFFFFFFFFu, last, 0);
+  if (!last) return;
+  __syncwarp();  // lane 0's acquire orders the other lanes' loads
+  // the last split of this row block: partials of every split, summed in split
+  // order (all loads of a route issued before the sums)
+  const int64_t sstride = p.slots_cap * static_cast<int64_t>(N1);
+  const float* src0 = p.part + static_cast<int64_t>(h.m0) * N1;
+#pragma unroll
+  for (int n = 0; n < NB; ++n) {
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      const int rt = 8 * n + 2 * t + c;
+      if (rt >= rows) continue;
+      const float* src = src0 + static_cast<int64_t>(rt) * N1;
+      float a[kMaxFusedSplits], b[kMaxFusedSplits];
+#pragma unroll
+      for (int s = 0; s < kMaxFusedSplits; ++s) {
+        a[s] = (s < p.splits && okA) ? __ldcg(src + s * sstride + growA) : 0.0f;
+        b[s] = (s < p.splits && okB) ? __ldcg(src + s * sstride + growB) : 0.0f;
+      }
+      float sa = 0.0f, sb = 0.0f;
+#pragma unroll
+      for (int s = 0; s < kMaxFusedSplits; ++s) {
+        if (s < p.splits) {
+          sa += a[s];
+          sb += b[s];
+        }
+      }
+      if (gated) {
+        if (okA) inter[static_cast<int64_t>(rt) * p.inter + 64 * h.nt + (rowA & 63)] = T::from_float(silu_f(sa) * sb);
+      } else {
+        if (okA) inter[static_cast<int64_t>(rt) * p.inter + growA] = T::from_float(relu2(sa));
+        if (okB) inter[static_cast<int64_t>(rt) * p.inter + growB] = T::from_float(relu2(sb));
+      }
+    }
+  }
+  if (lane == 0) fp.fix[(static_cast<int64_t>(h.m) * p.n_tiles + h.nt) * 8 + rb] = 0;
+  warp_publish(fp.ready + h.m, lane);
+}
+
+// Epilogue of a down unit on one finishing warp: expert outputs in the
+// activation dtype (one rounding), per-channel scales applied here.
+template <int SCALE, int DT, int NB>
+__device__ __forceinline__ void fused_down_epilogue(const FusedParams& fp, const StageHdr& h, int rowA, int rowB,
+                                                    int lane, const float (&tot)[4 * NB]) {
+  const GemmParams& p = fp.down;
+  const int t = lane & 3;
+  const int N = p.n_rows;
+  const int rows = min(h.rows, kGemvMaxR);
+  const int growA = 128 * h.nt + rowA;  // tile rows in order: expert rows 128 nt + 0..127
+  const int growB = 128 * h.nt + rowB;
+  const bool okA = growA < N, okB = growB < N;
+  float scA = 1.0f, scB = 1.0f;
+  if (SCALE == SCALE_CHANNEL) {
+    if (okA) scA = bf16_bits_to_float(p.scales[static_cast<int64_t>(h.e) * N + growA]);
+    if (okB) scB = bf16_bits_to_float(p.scales[static_cast<int64_t>(h.e) * N + growB]);
+  }
+  const int64_t oc = p.out_cols;
+  uint16_t* y = reinterpret_cast<uint16_t*>(p.out) + static_cast<int64_t>(h.m0) * oc;
+#pragma unroll
+  for (int n = 0; n < NB; ++n) {
+    const int rt0 = 8 * n + 2 * t, rt1 = rt0 + 1;
+    if (rt0 < rows && okA) y[rt0 * oc + growA] = F16<DT>::from_float(tot[4 * n + 0] * scA);
+    if (rt1 < rows && okA) y[rt1 * oc + growA] = F16<DT>::from_float(tot[4 * n + 1] * scA);
+    if (rt0 < rows && okB) y[rt0 * oc + growB] = F16<DT>::from_float(tot[4 * n + 2] * scB);
+    if (rt1 < rows && okB) y[rt1 * oc + growB] = F16<DT>::from_float(tot[4 * n + 3] * scB);
+  }
+}
+
+// Ring walk of one compute group: slots of parity grp, ring_len even.
+struct GroupRing {
+  int slot;
+  uint32_t ph, seq;
+  __device__ __forceinline__ void next(int ring_len) {
+    slot += 2;
+    seq += 2;
+    if (slot >= ring_len) {
+      slot -= ring_len;
+      ph ^= 1u;
+    }
+  }
+};
+
+// This group's stages of one unit (the first already waited for), its share
+// of the exchange and, on the finishing group, the epilogue.
+template <int SCALE, int DT, int LAYOUT, int NB>
+__device__ __forceinline__ bool fused_unit(const FusedParams& fp, uint8_t* smem, int stage_bytes, uint64_t* full,
+                                           uint64_t* empty, uint64_t* xfull, uint64_t* xempty,
+                                           const StageHdr* hdrs, volatile int* abort_flag, float* red,
+                                           int ring_len, int grp, int rowA, int rowB, int rb, int lane,
+                                           uint32_t ld_row_off, int ld_row7, int ld_chunk, GroupRing& r,
+                                           uint32_t& xj) {
+  const StageHdr h = hdrs[r.slot];
+  float tot[4 * NB];
+#pragma unroll
+  for (int j = 0; j < 4 * NB; ++j) tot[j] = 0.0f;
+  for (;;) {
+    const uint8_t* sA = smem + r.slot * stage_bytes;
+    gemv_stage<SCALE, DT, LAYOUT, NB, true>(sA, rowA, rowB, 0, lane, ld_row_off, ld_row7, ld_chunk, tot);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[r.slot]);
+    r.next(ring_len);
+    if (r.seq > h.last_seq) break;
+    if (!warp_wait(&full[r.slot], r.ph, abort_flag, fp.up.err, fp.up.wait_ns)) return false;
+  }
+  const bool finisher = static_cast<int>(h.last_seq & 1u) == grp;
+  if (h.last_seq > h.first_seq) {
+    // both groups took stages of this unit: meet in exchange buffer xj % 2
+    const int b = xj & 1;
+    const uint32_t use = xj >> 1;
+    ++xj;
+    // buffers of the plan's largest NB (bn / 8), so that units of different
+    // NB never overlap in them
+    float4* rbuf = reinterpret_cast<float4*>(red) + (b * 8 + rb) * (fp.up.bn >> 3) * 32 + lane;
+    if (!finisher) {
+      if (!warp_wait(&xempty[b], (use & 1u) ^ 1u, abort_flag, fp.up.err, fp.up.wait_ns)) return false;
+#pragma unroll
+      for (int n = 0; n < NB; ++n)
+        rbuf[n * 32] = make_float4(tot[4 * n + 0], tot[4 * n + 1], tot[4 * n + 2], tot[4 * n + 3]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&xfull[b]);
+      return true;
+    }
+    if (!warp_wait(&xfull[b], use & 1u, abort_flag, fp.up.err, fp.up.wait_ns)) return false;
+#pragma unroll
+    for (int n = 0; n < NB; ++n) {
+      const float4 o = rbuf[n * 32];
+      tot[4 * n + 0] += o.x;
+      tot[4 * n + 1] += o.y;
+      tot[4 * n + 2] += o.z;
+      tot[4 * n + 3] += o.w;
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&xempty[b]);
+  } else if (!finisher) {
+    return true;
+  }
+  if (h.type == kItemUp) fused_up_epilogue<SCALE, DT, NB>(fp, h, rowA, rowB, rb, lane, tot);
+  else fused_down_epilogue<SCALE, DT, NB>(fp, h, rowA, rowB, lane, tot);
+  return true;
+}
+
+template <int SCALE, int DT, int LAYOUT>
+__global__ void __launch_bounds__(kGemvThreads, 1)
+    w4a16_gemv_fused_kernel(const __grid_constant__ FusedParams fp, const __grid_constant__ CUtensorMap tmA1,
+                            const __grid_constant__ CUtensorMap tmS1, const __grid_constant__ CUtensorMap tmA2,
+                            const __grid_constant__ CUtensorMap tmS2) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  const GemmParams& pu = fp.up;
+  const int ring_len = pu.stages;  // even (host)
+  const int stage_bytes = pu.stage_bytes;
+  uint8_t* ctrl = smem + ring_len * stage_bytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(ctrl + kFzOffFull);
+  uint64_t* empty = reinterpret_cast<uint64_t*>(ctrl + kFzOffEmpty);
+  uint64_t* hdrb = reinterpret_cast<uint64_t*>(ctrl + kFzOffHdrBar);
+  uint64_t* xfull = reinterpret_cast<uint64_t*>(ctrl + kFzOffXBar);
+  uint64_t* xempty = xfull + 2;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(ctrl + kFzOffFlags);
+  volatile int* prod_issued = abort_flag + 1;
+  volatile int* prod_stopped = abort_flag + 2;
+  StageHdr* hdrs = reinterpret_cast<StageHdr*>(ctrl + kFzOffHdr);
+  float* red = reinterpret_cast<float*>(ctrl + kGemvCtrlBytes);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < ring_len; ++s) {
+      mbar_init(&full[s], 1 + 32);                 // producer (+ TMA bytes), activation lanes
+      mbar_init(&empty[s], kGemvComputeWarps / 2);  // the stage's compute group
+      mbar_init(&hdrb[s], 1);                       // producer: header written
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&xfull[b], kGemvComputeWarps / 2);
+      mbar_init(&xempty[b], kGemvComputeWarps / 2);
+    }
+    *abort_flag = 0;
+    *prod_stopped = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA1);
+    tma_prefetch_desc(&tmA2);
+  }
+  __syncthreads();
+
+  // Everything below reads what route preparation wrote.
+  pdl_wait();
+  pdl_launch_dependents();
+
+  if (warp == 0) {
+    // ------------------------------------------------------------------ producer
+    const uint64_t pol_w = l2_policy_evict_first();
+    const uint64_t pol_s = l2_policy_evict_last();
+    const int n_t = *pu.num_tiles;
+    const int nt1 = pu.n_tiles, s1 = pu.splits;
+    const GemmParams& pd = fp.down;
+    const int nt2 = pd.n_tiles, nch = (nt2 + fp.down_chunk - 1) / fp.down_chunk;
+    const int q1 = n_t * nt1 * s1;
+    const int qt = q1 + n_t * nch;
+    int slot = 0;
+    uint32_t ph = 0, seq = 0;
+    bool ok = true;
+    int q_lane0 = 0;
+    if (lane == 0) q_lane0 = atomicAdd(fp.queue, 1);
+    // issue one stage: header, scales, weights
+    auto issue = [&](const GemmParams& g, const CUtensorMap& tmA, const CUtensorMap& tmS, int type, int m,
+                     const int4& ti, int nt, int kb, int split, uint32_t first, uint32_t last) -> bool {
+      if (!warp_wait(&empty[slot], ph ^ 1u, abort_flag, pu.err, pu.wait_ns)) return false;
+      uint8_t* sA = smem + slot * stage_bytes;
+      uint8_t* sS = sA + kGvOffS;
+      const int e = ti.x;
+      const int N = g.n_rows;
+      int r0, r1;
+      if (type == kItemUp) tile_row_bases<GEMM_UP>(g, nt, r0, r1);
+      else tile_row_bases<GEMM_DOWN>(g, nt, r0, r1);
+      const bool stma = SCALE == SCALE_GROUP && g.scale_tma;
+      if (SCALE == SCALE_GROUP && !stma) {
+        const int groups_row = g.K / kGroup;
+        const int g0 = kb * (kGemvBlockK / kGroup);
+        const int ng = min(kGemvBlockK / kGroup, groups_row - g0);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int tr = lane + 32 * j;
+          const int grow = tr < 64 ? r0 + tr : r1 + (tr - 64);
+          const uint8_t* src = reinterpret_cast<const uint8_t*>(g.scales) +
+                               (static_cast<int64_t>(e) * N + grow) * (groups_row * 2) + g0 * 2;
+          copy_scale_piece(sS + tr * kGvScaleRowBytes, src, grow < N ? max(ng, 0) * 2 : 0);
+        }
+        cp_async_mbar_arrive(&full[slot]);
+      }
+      if (lane == 0) {
+        StageHdr& h = hdrs[slot];
+        h.type = type;
+        h.m = m;
+        h.nt = nt;
+        h.kb = kb;
+        h.e = e;
+        h.m0 = ti.y;
+        h.rows = ti.z;
+        h.split = split;
+        h.first_seq = first;
+        h.last_seq = last;
+      }
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&hdrb[slot]);
+        mbar_arrive_expect_tx(&full[slot], kGvWeightBytes + (stma ? kTileRows * kGvScaleRowBytes : 0));
+        if (SCALE == SCALE_GROUP || LAYOUT == LAYOUT_IL) {
+          tma_load_3d(sA, &tmA, &full[slot], kb * (kGemvBlockK / 2), r0, e, pol_w);
+          tma_load_3d(sA + 8192, &tmA, &full[slot], kb * (kGemvBlockK / 2), r1, e, pol_w);
+          if (stma) {
+            tma_load_3d(sS, &tmS, &full[slot], kb * (kGemvBlockK / kGroup), r0, e, pol_s);
+            tma_load_3d(sS + 64 * kGvScaleRowBytes, &tmS, &full[slot], kb * (kGemvBlockK / kGroup), r1, e, pol_s);
+          }
+        } else {
+#pragma unroll
+          for (int b = 0; b < 2; ++b)
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh)
+              tma_load_3d(sA + (b * 2 + hh) * 4096, &tmA, &full[slot], kb * kGemvBlockK + hh * 128,
+                          (b ? r1 : r0) / 2, e, pol_w);
+        }
+      }
+      __syncwarp();
+      ++seq;
+      if (++slot == ring_len) {
+        slot = 0;
+        ph ^= 1u;
+      }
+      return true;
+    };
+    while (ok) {
+      const int q = __shfl_sync(0xFFFFFFFFu, q_lane0, 0);
+      if (q >= qt) break;
+      if (lane == 0) q_lane0 = atomicAdd(fp.queue, 1);  // the next entry, taken while this one streams
+      if (q < q1) {
+        const int m = q / (nt1 * s1);
+        const int rem = q - m * (nt1 * s1);
+        const int nt = rem / s1, split = rem - nt * s1;
+        const int4 ti = pu.tiles[m];
+        const int kb0 = split * pu.kb_per_split;
+        const int kb1 = min(kb0 + pu.kb_per_split, pu.kb_total);
+        const uint32_t first = seq, last = seq + static_cast<uint32_t>(kb1 - kb0) - 1u;
+        for (int kb = kb0; kb < kb1 && ok; ++kb) ok = issue(pu, tmA1, tmS1, kItemUp, m, ti, nt, kb, split, first, last);
+      } else {
+        const int qq = q - q1;
+        const int m = qq / nch;
+        const int c = qq - m * nch;
+        const int4 ti = pd.tiles[m];
+        const int ntb = c * fp.down_chunk, nte = min(ntb + fp.down_chunk, nt2);
+        for (int nt = ntb; nt < nte && ok; ++nt) {
+          const uint32_t first = seq, last = seq + static_cast<uint32_t>(pd.kb_total) - 1u;
+          for (int kb = 0; kb < pd.kb_total && ok; ++kb)
+            ok = issue(pd, tmA2, tmS2, kItemDown, m, ti, nt, kb, 0, first, last);
+        }
+      }
+    }
+    // two end markers, one for each compute group
+    for (int j = 0; j < 2 && ok; ++j) {
+      if (!warp_wait(&empty[slot], ph ^ 1u, abort_flag, pu.err, pu.wait_ns)) {
+        ok = false;
+        break;
+      }
+      if (lane == 0) {
+        hdrs[slot].type = kItemEnd;
+        mbar_arrive(&hdrb[slot]);
+        mbar_arrive(&full[slot]);
+      }
+      __syncwarp();
+      ++seq;
+      if (++slot == ring_len) {
+        slot = 0;
+        ph ^= 1u;
+      }
+    }
+    // Wind-down (as in gemv.cuh): publish the stage count for the activation
+    // warp, then wait (bounded) for the copies of the last ring of stages.
+    if (lane == 0) {
+      *prod_issued = static_cast<int>(seq);
+      __threadfence_block();
+      *prod_stopped = 1;
+      volatile int no_abort = 0;
+      const uint32_t from = seq > static_cast<uint32_t>(ring_len) ? seq - ring_len : 0;
+      for (uint32_t j = from; j < seq; ++j)
+        mbar_wait(&full[j % ring_len], (j / ring_len) & 1, &no_abort, pu.err);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ activation rows
+    const int need = 8 * pu.n_tiles;  // published row blocks of a finished route tile
+    int slot = 0, ends = 0;
+    uint32_t ph = 0, done = 0;
+    bool ok = true;
+    int src_type = -1, src_m = -1, src = 0, ready_m = -1;
+    while (ends < 2) {
+      if (!warp_wait(&hdrb[slot], ph, abort_flag, pu.err, pu.wait_ns)) {
+        ok = false;
+        break;
+      }
+      const StageHdr h = hdrs[slot];
+      if (h.type == kItemEnd) {
+        if (lane == 0) mbar_arrive_cnt(&full[slot], 32);
+        ++ends;
+      } else {
+        const bool up = h.type == kItemUp;
+        const GemmParams& g = up ? fp.up : fp.down;
+        const int rows = min(h.rows, kGemvMaxR);
+        if (!up && h.m != ready_m) {
+          // the intermediate rows of route tile m: wait until every row block
+          // of every gate/up weight tile is published
+          int rdy = 1;
+          if (lane == 0) {
+            const uint64_t t0 = global_timer_ns();
+            while (ld_acquire_gpu(fp.ready + h.m) < need) {
+              if (*abort_flag) {
+                rdy = 0;
+                break;
+              }
+              if (global_timer_ns() - t0 > pu.wait_ns) {
+                *abort_flag = 1;
+                atomicExch(pu.err, kErrTimeout);
+                rdy = 0;
+                break;
+              }
+            }
+          }
+          rdy = __shfl_sync(0xFFFFFFFFu, rdy, 0);
+          __syncwarp();  // lane 0's acquire orders the other lanes' copies
+          if (!rdy) {
+            ok = false;
+            break;
+          }
+          ready_m = h.m;
+        }
+        if (h.type != src_type || h.m != src_m) {
+          src = 0;
+          if (lane < rows) {
+            if (up) {
+              const int route = g.perm[h.m0 + lane];
+              src = route >= 0 ? route / g.top_k : 0;
+            } else {
+              src = h.m0 + lane;
+            }
+          }
+          src_type = h.type;
+          src_m = h.m;
+        }
+        const uint16_t* xsrc = reinterpret_cast<const uint16_t*>(g.x);
+        uint8_t* xs = smem + slot * stage_bytes + kGvOffX;
+        const int col = h.kb * kGemvBlockK + lane * 8;
+        const bool valid = col < g.K;
+        for (int r = 0; r < rows; ++r) {
+          const int srow = __shfl_sync(0xFFFFFFFFu, src, r);
+          cp_async_cg16(xs + r * kGvRouteBytes + lane * 16,
+                        xsrc + static_cast<int64_t>(srow) * g.K + (valid ? col : 0), valid ? 16u : 0u);
+        }
+        cp_async_mbar_arrive_noinc(&full[slot]);
+      }
+      ++done;
+      if (++slot == ring_len) {
+        slot = 0;
+        ph ^= 1u;
+      }
+    }
+    // After an abort: the arrivals owed to stages the producer issued beyond
+    // this warp's last one (see gemv.cuh).
+    if (!ok && lane == 0) {
+      const uint64_t t0 = global_timer_ns();
+      while (!*prod_stopped && global_timer_ns() - t0 < kWaitTimeoutNs) {
+      }
+      if (*prod_stopped) {
+        __threadfence_block();
+        const uint32_t to = static_cast<uint32_t>(*prod_issued);
+        for (uint32_t j = done; j < to; ++j) mbar_arrive_cnt(&full[j % ring_len], 32);
+      }
+    }
+    asm volatile("cp.async.wait_all;" ::: "memory");
+  } else {
+    // ------------------------------------------------------------------ compute groups
+    const int cw = warp - 2, grp = cw >> 3, rb = cw & 7, g = lane >> 2;
+    // rows of this warp: SwiGLU gate/up tiles pair gate row 8 rb + g with its
+    // up row; otherwise (ReLU^2 gate/up, down) 16 consecutive rows.  The
+    // gate/up row map depends on the activation only, the down tiles always
+    // take the plain map: both use tile rows (rowA, rowB) as the stage layout
+    // and the epilogues interpret them per GEMM.
+    const bool gated = pu.act == ACT_SWIGLU;
+    const int rowA_up = gated ? 8 * rb + g : 16 * rb + g;
+    const int rowB_up = gated ? 64 + 8 * rb + g : 16 * rb + 8 + g;
+    const int rowA_dn = 16 * rb + g, rowB_dn = 16 * rb + 8 + g;
+    auto ld_off = [&](int rowA, int rowB, uint32_t& off, int& r7, int& ch) {
+      const int ld_i = lane & 7, ld_j = lane >> 3;
+      const int ld_row = (ld_j & 1) ? rowB - g + ld_i : rowA - g + ld_i;
+      off = (ld_row >> 6) * 8192 + (ld_row & 63) * 128;
+      r7 = ld_row & 7;
+      ch = ld_j >> 1;
+    };
+    uint32_t off_up, off_dn;
+    int r7_up, r7_dn, ch_up, ch_dn;
+    ld_off(rowA_up, rowB_up, off_up, r7_up, ch_up);
+    ld_off(rowA_dn, rowB_dn, off_dn, r7_dn, ch_dn);
+    GroupRing r;
+    r.slot = grp;
+    r.ph = 0;
+    r.seq = static_cast<uint32_t>(grp);
+    uint32_t xj = 0;
+    for (;;) {
+      if (!warp_wait(&full[r.slot], r.ph, abort_flag, pu.err, pu.wait_ns)) break;
+      const int type = hdrs[r.slot].type;
+      if (type == kItemEnd) break;
+      const int nb = (min(hdrs[r.slot].rows, kGemvMaxR) + 7) >> 3;
+      const bool up = type == kItemUp;
+      const int rowA = up ? rowA_up : rowA_dn, rowB = up ? rowB_up : rowB_dn;
+      const uint32_t off = up ? off_up : off_dn;
+      const int r7 = up ? r7_up : r7_dn, ch = up ? ch_up : ch_dn;
+      bool ok;
+#define W4A16_FUSED_UNIT(NBV)                                                                                   \
+  fused_unit<SCALE, DT, LAYOUT, NBV>(fp, smem, stage_bytes, full, empty, xfull, xempty, hdrs, abort_flag, red, \
+                                     ring_len, grp, rowA, rowB, rb, lane, off, r7, ch, r, xj)
+      if (nb <= 1) ok = W4A16_FUSED_UNIT(1);
+      else if (nb == 2) ok = W4A16_FUSED_UNIT(2);
+      else ok = W4A16_FUSED_UNIT(4);
+#undef W4A16_FUSED_UNIT
+      if (!ok) break;
+    }
+  }
+  __syncthreads();
+}
+
+template <int SCALE, int DT, int LAYOUT>
+cudaError_t launch_gemv_fused_one(const FusedParams& fp, const CUtensorMap& tmA1, const CUtensorMap& tmS1,
+                                  const CUtensorMap& tmA2, const CUtensorMap& tmS2, int grid, int smem_bytes,
+                                  cudaStream_t s, bool pdl) {
+  auto kern = w4a16_gemv_fused_kernel<SCALE, DT, LAYOUT>;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  static int configured_for[64] = {0};
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (configured_for[dev] < smem_bytes) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+    if (e != cudaSuccess) return e;
+    configured_for[dev] = smem_bytes;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kGemvThreads);
+  cfg.dynamicSmemBytes = smem_bytes;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, fp, tmA1, tmS1, tmA2, tmS2);
+}
+
+template <int DT, int LAYOUT>
+cudaError_t launch_gemv_fused_dt(int scale_kind, const FusedParams& fp, const CUtensorMap& tmA1,
+                                 const CUtensorMap& tmS1, const CUtensorMap& tmA2, const CUtensorMap& tmS2, int grid,
+                                 int smem_bytes, cudaStream_t s, bool pdl) {
+  return scale_kind == SCALE_GROUP
+             ? launch_gemv_fused_one<SCALE_GROUP, DT, LAYOUT>(fp, tmA1, tmS1, tmA2, tmS2, grid, smem_bytes, s, pdl)
+             : launch_gemv_fused_one<SCALE_CHANNEL, DT, LAYOUT>(fp, tmA1, tmS1, tmA2, tmS2, grid, smem_bytes, s, pdl);
+}
+
+}  // namespace w4a16
