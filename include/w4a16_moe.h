@@ -210,6 +210,7 @@ typedef struct {
                               split partials [gemm2_splits, max_slots, H] when gemm2_splits > 1 */
   int32_t fused_gemms;     /* 1: CUDA-core path with both GEMMs in one launch (then
                               gemm1_ctas = gemm2_ctas = that launch's grid) */
+  int32_t fused_finalize;  /* 1: that launch also combines the routes (no combine launch) */
 } w4a16_route_info;
 
 w4a16_status w4a16_moe_route_info(w4a16_moe_plan_t plan, int32_t num_tokens,
@@ -351,6 +352,21 @@ w4a16_status w4a16_moe_relayout_weights(w4a16_moe_plan_t plan, int32_t which, co
  * W4A16_ERR_INVALID_ARG.
  */
 w4a16_status w4a16_moe_set_weight_layout(w4a16_moe_plan_t plan, int32_t layout);
+
+/*
+ * Deterministic fused finalize ("perf: reduce split W4A16 routing and output
+ * overhead" (FlashInfer), sections Description and Benchmarks: the combine
+ * done inside the down GEMM's epilogue instead of a separate pass).  With
+ * enable != 0, forwards that take the CUDA-core path with both GEMMs in one
+ * launch (w4a16_route_info.fused_gemms) combine the routes there: no data
+ * atomics -- per (token, 16-column block) arrival counters elect the warp of
+ * the token's last valid route, which sums the token's expert outputs in
+ * top-k order with the combine's arithmetic.  The output is bit-identical to
+ * the separate combine.  Other forwards are unaffected.  Default: off (also
+ * set by the environment variable W4A16_MOE_FUSED_FINALIZE=1 at plan
+ * creation).  Host only; plan NULL: W4A16_ERR_INVALID_ARG.
+ */
+w4a16_status w4a16_moe_set_fused_finalize(w4a16_moe_plan_t plan, int32_t enable);
 
 /*
  * Reads (synchronously, on `stream`) and clears the device error flag in the

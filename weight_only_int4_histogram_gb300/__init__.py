@@ -17,6 +17,7 @@ from ._lib import (Desc, RouteInfo, W4A16Error, w4a16_moe_check_device_error,  #
                    w4a16_moe_plan_destroy, w4a16_moe_prepare_routes, w4a16_moe_route_info,
                    w4a16_moe_route_topk, w4a16_moe_set_gemm_path, w4a16_moe_set_overrides,
                    w4a16_moe_forward_masked, w4a16_moe_relayout_weights, w4a16_moe_set_weight_layout,
+                   w4a16_moe_set_fused_finalize,
                    w4a16_moe_route_and_prepare)
 from ._lib import PATH_AUTO, PATH_CUDA_CORES, PATH_TENSOR_CORES  # noqa: F401
 from ._lib import LAYOUT_CHECKPOINT, LAYOUT_INTERLEAVED  # noqa: F401
@@ -100,6 +101,11 @@ class W4A16MoE:
         if need > self.workspace.numel():
             self.workspace = torch.empty(need, dtype=torch.uint8, device=self.device)
         self.workspace_bytes = need
+
+    def set_fused_finalize(self, enable=True):
+        """Combine the routes inside the fused CUDA-core launch (bit-identical
+        to the separate combine; only forwards with fused_gemms use it)."""
+        w4a16_moe_set_fused_finalize(self.plan, enable)
 
     def set_weight_layout(self, layout=LAYOUT_CHECKPOINT):
         """Layout of the packed weights later forwards receive."""

@@ -37,6 +37,7 @@ EXPORTED = (
     "w4a16_moe_forward_masked",
     "w4a16_moe_relayout_weights",
     "w4a16_moe_set_weight_layout",
+    "w4a16_moe_set_fused_finalize",
     "w4a16_moe_route_and_prepare",
 )
 
@@ -64,7 +65,7 @@ class RouteInfo(ctypes.Structure):
         ("off_perm", ctypes.c_size_t), ("off_inv", ctypes.c_size_t),
         ("off_tiles", ctypes.c_size_t), ("off_num_tiles", ctypes.c_size_t),
         ("off_inter", ctypes.c_size_t), ("off_expert_out", ctypes.c_size_t),
-        ("fused_gemms", ctypes.c_int32),
+        ("fused_gemms", ctypes.c_int32), ("fused_finalize", ctypes.c_int32),
     ]
 
 
@@ -116,6 +117,8 @@ def load(path: str = LIB_PATH):
     L.w4a16_moe_route_and_prepare.restype = st
     L.w4a16_moe_set_weight_layout.argtypes = [P, i32]
     L.w4a16_moe_set_weight_layout.restype = st
+    L.w4a16_moe_set_fused_finalize.argtypes = [P, i32]
+    L.w4a16_moe_set_fused_finalize.restype = st
     L.w4a16_moe_last_error.argtypes = []
     L.w4a16_moe_last_error.restype = ctypes.c_char_p
     _lib = L
@@ -200,6 +203,10 @@ def w4a16_moe_route_and_prepare(plan, num_tokens: int, logits_ptr: int, num_glob
 
 def w4a16_moe_set_weight_layout(plan, layout: int):
     check(load().w4a16_moe_set_weight_layout(plan, layout))
+
+
+def w4a16_moe_set_fused_finalize(plan, enable: bool):
+    check(load().w4a16_moe_set_fused_finalize(plan, 1 if enable else 0))
 
 
 def w4a16_moe_set_stage_events(plan, event_handles):

@@ -36,6 +36,7 @@ struct w4a16_moe_plan_s {
   size_t ws_bytes;
   bool pdl;
   bool fused;        // CUDA-core path: both GEMMs in one launch
+  bool finalize;     // fused launch: combine inside the down epilogue (no combine launch)
   int ov_chunk;      // tuning: down weight tiles per fused queue entry (0 = automatic)
   cudaEvent_t ev[4];
   bool has_ev;
@@ -67,6 +68,8 @@ struct Layout {
   bool fused;       // CUDA-core path: both GEMMs in one launch (gemv_fused.cuh)
   int down_chunk;   // fused: down weight tiles per queue entry
   int ctr_len;      // counters zeroed by route preparation
+  bool fin;         // fused finalize in this forward
+  int fix_len;      // fused: queue head + ready counts + split counters (reset after a forward)
   int T, R, bn, tiles_cap;
   int64_t slots_cap;
   int n1;
@@ -287,7 +290,11 @@ Layout make_layout(const w4a16_moe_plan_s& P, int T) {
   if (L.fused) L.grid1 = L.grid2 = P.num_sms;  // one queue for both GEMMs
   // split-K arrival counters; the fused launch adds its queue head (padded to
   // 32 entries), the ready counts of the route tiles and per-row-block counters
-  L.ctr_len = L.fused ? 32 + L.tiles_cap + L.tiles_cap * L.nt1 * 8 : L.tiles_cap * L.nt1;
+  // (and, always reserved so that the finalize switch never outgrows a
+  // workspace, the finalize counters of T tokens x H / 16 column blocks)
+  L.fix_len = 32 + L.tiles_cap + L.tiles_cap * L.nt1 * 8;
+  L.ctr_len = L.fused ? L.fix_len + T * (d.hidden / 16) : L.tiles_cap * L.nt1;
+  L.fin = L.fused && P.finalize;
 
   const int act_bytes = 2;
   size_t o = 0;
@@ -495,7 +502,7 @@ w4a16_status launch_combine_of(const w4a16_moe_plan_s& P, const Layout& L, bool 
   c.out = out;
   if (L.fused) {
     c.zero = reinterpret_cast<int32_t*>(ws + L.off_ctr);
-    c.zero_len = L.ctr_len;
+    c.zero_len = L.fix_len;
   }
   cudaError_t e = launch_combine(P.d.act_dtype, c, s, P.pdl);
   if (e != cudaSuccess) return cuda_fail(e, "combine launch");
@@ -530,6 +537,19 @@ w4a16_status launch_forward_fused(const w4a16_moe_plan_s& P, const Layout& L, co
   fp.ready = ctr + 32;
   fp.fix = ctr + 32 + L.tiles_cap;
   fp.down_chunk = L.down_chunk;
+  if (L.fin) {
+    fp.finalize = 1;
+    fp.fin_ctr = ctr + L.fix_len;
+    fp.inv = reinterpret_cast<const int32_t*>(ws + L.off_inv);
+    fp.topk_weights = tw;
+    fp.T = L.T;
+    fp.k = d.top_k;
+    fp.renormalize = renorm ? 1 : 0;
+    fp.out = out;
+    fp.exit_ctr = ctr + 1;  // inside the queue head's padding, so reset with it
+    fp.reset = ctr;
+    fp.reset_len = L.fix_len;
+  }
   const int lay = P.layout == W4A16_LAYOUT_INTERLEAVED ? LAYOUT_IL : LAYOUT_CANON;
   cudaError_t e =
       launch_gemv_fused(d.scale_kind, d.act_dtype, lay, fp, tmA1, tmS1, tmA2, tmS2, L.grid1, L.smem, s, P.pdl);
@@ -537,6 +557,10 @@ w4a16_status launch_forward_fused(const w4a16_moe_plan_s& P, const Layout& L, co
   // both GEMMs end with the one launch: the gate/up and down stage marks coincide
   if (P.has_ev && ((e = cudaEventRecord(P.ev[1], s)) != cudaSuccess || (e = cudaEventRecord(P.ev[2], s)) != cudaSuccess))
     return cuda_fail(e, "event record");
+  if (L.fin) {
+    if (P.has_ev && (e = cudaEventRecord(P.ev[3], s)) != cudaSuccess) return cuda_fail(e, "event record");
+    return W4A16_OK;
+  }
   return launch_combine_of(P, L, true, tw, renorm, out, ws, s);
 }
 
@@ -748,6 +772,7 @@ w4a16_status w4a16_moe_plan(const w4a16_moe_desc* desc, w4a16_moe_plan_t* out, s
   }
   P->pdl = env_flag("W4A16_MOE_PDL", true);
   P->fused = env_flag("W4A16_MOE_FUSED", true);
+  P->finalize = env_flag("W4A16_MOE_FUSED_FINALIZE", false);
   if (const char* v = getenv("W4A16_MOE_DOWN_CHUNK")) P->ov_chunk = std::max(0, atoi(v));
   P->layout = W4A16_LAYOUT_CHECKPOINT;
   // tuning knobs for measurements: weight tiles per tensor-core unit of each GEMM
@@ -811,6 +836,7 @@ w4a16_status w4a16_moe_route_info(w4a16_moe_plan_t plan, int32_t num_tokens, w4a
   info->pipeline_stages = L.stages;
   info->gemm_path = L.gemv ? W4A16_PATH_CUDA_CORES : W4A16_PATH_TENSOR_CORES;
   info->fused_gemms = L.fused ? 1 : 0;
+  info->fused_finalize = L.fin ? 1 : 0;
   info->off_counts = L.off_counts;
   info->off_offs = L.off_offs;
   info->off_perm = L.off_perm;
@@ -1014,6 +1040,12 @@ w4a16_status w4a16_moe_set_stage_events(w4a16_moe_plan_t plan, void* const* even
     plan->ev[i] = static_cast<cudaEvent_t>(events[i]);
   }
   plan->has_ev = true;
+  return W4A16_OK;
+}
+
+w4a16_status w4a16_moe_set_fused_finalize(w4a16_moe_plan_t plan, int32_t enable) {
+  if (!plan) return fail(W4A16_ERR_INVALID_ARG, "plan is NULL");
+  plan->finalize = enable != 0;
   return W4A16_OK;
 }
 

@@ -159,6 +159,20 @@ struct FusedParams {
   int32_t* ready;          // [tiles_cap] published gate/up row blocks per route tile
   int32_t* fix;            // [tiles_cap * nt1 * 8] split arrivals per (route tile, weight tile, row block)
   int32_t down_chunk;      // down weight tiles per queue entry
+  // Fused finalize (finalize != 0): the down epilogue combines the expert
+  // outputs itself (no combine launch).  Per (token, 16-column block) arrival
+  // counters elect the last route's warp, which sums the token's routes in
+  // top-k order with the combine's arithmetic; the last CTA to exit resets the
+  // queue state.
+  int32_t finalize;
+  int32_t* fin_ctr;        // [T * H / 16]
+  const int32_t* inv;      // [T * k] slot of each route, -1 when invalid
+  const float* topk_weights;
+  int32_t T, k, renormalize;
+  void* out;               // [T, H] act dtype
+  int32_t* exit_ctr;       // CTAs done (inside the reset range)
+  int32_t* reset;          // [reset_len] queue state zeroed by the last CTA
+  int32_t reset_len;
 };
 
 struct CombineParams {

@@ -78,6 +78,7 @@ template <> struct F16<DT_BF16> {
     __nv_bfloat16 h = __float2bfloat16_rn(f);
     return *reinterpret_cast<uint16_t*>(&h);
   }
+  __device__ static __forceinline__ float to_float(uint16_t b) { return __uint_as_float(static_cast<uint32_t>(b) << 16); }
 };
 template <> struct F16<DT_FP16> {
   // FP16: 1024 + (nibble ^ 8) and 1032.0
@@ -98,6 +99,11 @@ template <> struct F16<DT_FP16> {
   __device__ static __forceinline__ uint16_t from_float(float f) {
     __half h = __float2half_rn(f);
     return *reinterpret_cast<uint16_t*>(&h);
+  }
+  __device__ static __forceinline__ float to_float(uint16_t b) {
+    __half h;
+    *reinterpret_cast<uint16_t*>(&h) = b;
+    return __half2float(h);
   }
 };
 

@@ -206,11 +206,51 @@ __device__ __forceinline__ void fused_up_epilogue(const FusedParams& fp, const S
   warp_publish(fp.ready + h.m, lane);
 }
 
+// Output columns [c0, c0 + 16) of token t: its routes' expert outputs in
+// top-k order, acc = acc + w * y with two roundings (the combine's arithmetic,
+// so the result is bit-identical to the separate combine launch).
+template <int DT>
+__device__ __forceinline__ void finalize_block(const FusedParams& fp, int t, int c0) {
+  const int k = fp.k, H = fp.down.out_cols;
+  const float* tw = fp.topk_weights + static_cast<int64_t>(t) * k;
+  const int32_t* inv = fp.inv + static_cast<int64_t>(t) * k;
+  float wsum = 0.0f;
+  if (fp.renormalize)
+    for (int j = 0; j < k; ++j) wsum = __fadd_rn(wsum, tw[j]);
+  float acc[16];
+#pragma unroll
+  for (int c = 0; c < 16; ++c) acc[c] = 0.0f;
+  const uint16_t* y = reinterpret_cast<const uint16_t*>(fp.down.out);
+  for (int j = 0; j < k; ++j) {
+    const int slot = inv[j];
+    if (slot < 0) continue;
+    float w = tw[j];
+    if (fp.renormalize) w = (wsum != 0.0f) ? __fdiv_rn(w, wsum) : 0.0f;
+    const uint4* yr = reinterpret_cast<const uint4*>(y + static_cast<int64_t>(slot) * H + c0);
+    const uint4 u0 = __ldcg(yr), u1 = __ldcg(yr + 1);
+    const uint32_t v[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      acc[2 * c] = __fadd_rn(acc[2 * c], __fmul_rn(w, F16<DT>::to_float(static_cast<uint16_t>(v[c] & 0xFFFFu))));
+      acc[2 * c + 1] = __fadd_rn(acc[2 * c + 1], __fmul_rn(w, F16<DT>::to_float(static_cast<uint16_t>(v[c] >> 16))));
+    }
+  }
+  uint32_t o[8];
+#pragma unroll
+  for (int c = 0; c < 8; ++c)
+    o[c] = static_cast<uint32_t>(F16<DT>::from_float(acc[2 * c])) |
+           (static_cast<uint32_t>(F16<DT>::from_float(acc[2 * c + 1])) << 16);
+  uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(fp.out) + static_cast<int64_t>(t) * H + c0);
+  dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+  dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+}
+
 // Epilogue of a down unit on one finishing warp: expert outputs in the
 // activation dtype (one rounding), per-channel scales applied here.
 template <int SCALE, int DT, int NB>
 __device__ __forceinline__ void fused_down_epilogue(const FusedParams& fp, const StageHdr& h, int rowA, int rowB,
                                                     int lane, const float (&tot)[4 * NB]) {
+  // (fused finalize: rowA = 16 rb + g, so rowA >> 4 is the row block)
   const GemmParams& p = fp.down;
   const int t = lane & 3;
   const int N = p.n_rows;
@@ -233,6 +273,30 @@ __device__ __forceinline__ void fused_down_epilogue(const FusedParams& fp, const
     if (rt0 < rows && okB) y[rt0 * oc + growB] = F16<DT>::from_float(tot[4 * n + 2] * scB);
     if (rt1 < rows && okB) y[rt1 * oc + growB] = F16<DT>::from_float(tot[4 * n + 3] * scB);
   }
+  if (!fp.finalize) return;
+  // Fused finalize: this warp's 16 output columns are done for its routes; the
+  // last arrival of a token's valid routes sums that token's block.
+  const int c0 = 128 * h.nt + 16 * (rowA >> 4);
+  if (c0 >= N) return;
+  __syncwarp();
+  if (lane == 0) __threadfence();  // publish the stores above
+  __syncwarp();
+  const int nblk = N / 16;
+  int fin_t = -1;
+  if (lane < rows) {
+    const int route = p.perm[h.m0 + lane];
+    const int t = route / fp.k;
+    int valid = 0;
+    for (int j = 0; j < fp.k; ++j) valid += fp.inv[static_cast<int64_t>(t) * fp.k + j] >= 0;
+    int32_t* ctr = fp.fin_ctr + static_cast<int64_t>(t) * nblk + c0 / 16;
+    const int old = atomicAdd(ctr, 1);
+    if (old == valid - 1) {
+      __threadfence();  // acquire the other routes' stores
+      *ctr = 0;         // for a forward that reuses this route layout
+      fin_t = t;
+    }
+  }
+  if (fin_t >= 0) finalize_block<DT>(fp, fin_t, c0);
 }
 
 // Ring walk of one compute group: slots of parity grp, ring_len even.
@@ -359,6 +423,16 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------------ producer
+    if (fp.finalize) {
+      // fused finalize: output rows of tokens without a valid route are zero
+      // (nothing arrives for them); token t is this CTA's when t % grid == cta
+      for (int t = blockIdx.x; t < fp.T; t += gridDim.x) {
+        const bool any = __any_sync(0xFFFFFFFFu, lane < fp.k && fp.inv[static_cast<int64_t>(t) * fp.k + lane] >= 0);
+        if (any) continue;
+        uint4* row = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(fp.out) + static_cast<int64_t>(t) * fp.down.out_cols);
+        for (int c = lane; c < fp.down.out_cols / 8; c += 32) row[c] = make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
     const uint64_t pol_w = l2_policy_evict_first();
     const uint64_t pol_s = l2_policy_evict_last();
     const int n_t = *pu.num_tiles;
@@ -633,6 +707,20 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
     }
   }
   __syncthreads();
+  if (fp.finalize) {
+    // The last CTA to finish resets the queue state (no combine launch follows
+    // to do it), so that a forward can reuse this route layout.
+    __shared__ int last_cta;
+    if (threadIdx.x == 0) {
+      __threadfence();
+      last_cta = atomicAdd(fp.exit_ctr, 1) == static_cast<int>(gridDim.x) - 1;
+    }
+    __syncthreads();
+    if (last_cta) {
+      __threadfence();
+      for (int i = threadIdx.x; i < fp.reset_len; i += blockDim.x) fp.reset[i] = 0;
+    }
+  }
 }
 
 template <int SCALE, int DT, int LAYOUT>
