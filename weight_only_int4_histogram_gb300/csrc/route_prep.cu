@@ -113,14 +113,18 @@ __global__ void __launch_bounds__(kRoutePrepThreads, 1) route_place_kernel(const
   pdl_wait();
   pdl_launch_dependents();
 
-  for (int i = tid; i < kRoutePrepWarps * E; i += kRoutePrepThreads) whist[i] = 0;
+  const int R0 = cta * p.tpc * p.k;
+  const int R1 = min(p.T, (cta + 1) * p.tpc) * p.k;
+  const int chunk = ((max(R1 - R0, 0) + kRoutePrepWarps - 1) / kRoutePrepWarps + 31) / 32 * 32;
+  // warps that hold routes: only their histogram rows are used (small batches
+  // touch two or three warps' rows, not 32)
+  const int nw = max(1, min(kRoutePrepWarps, (max(R1 - R0, 0) + chunk - 1) / max(chunk, 1)));
+
+  for (int i = tid; i < nw * E; i += kRoutePrepThreads) whist[i] = 0;
   for (int i = cta * kRoutePrepThreads + tid; i < p.ctr_len; i += p.n_cta * kRoutePrepThreads) p.counters[i] = 0;
   if (cta == 0 && tid == 0) *p.err = 0;  // the flag reports timeouts since this call
   __syncthreads();
 
-  const int R0 = cta * p.tpc * p.k;
-  const int R1 = min(p.T, (cta + 1) * p.tpc) * p.k;
-  const int chunk = ((max(R1 - R0, 0) + kRoutePrepWarps - 1) / kRoutePrepWarps + 31) / 32 * 32;
   const int r_begin = R0 + warp * chunk;
   const int r_end = min(R1, r_begin + chunk);
   const unsigned full = 0xFFFFFFFFu;
@@ -133,10 +137,12 @@ __global__ void __launch_bounds__(kRoutePrepThreads, 1) route_place_kernel(const
   auto local_of = [&](int r) -> int { return r < r_end ? local_expert(p.ids[r], p.expert_offset, E) : -1; };
 
   // pass 1: per-warp counts of this CTA's routes (ids fetched kBatch rounds at
-  // a time so the global loads overlap instead of forming a latency chain)
+  // a time so the global loads overlap instead of forming a latency chain; a
+  // warp with a single batch keeps its experts for pass 3)
   constexpr int kBatch = 8;
+  const bool one_batch = chunk <= 32 * kBatch;  // uniform over the CTA
+  int eb[kBatch];
   for (int base = r_begin; base < r_end; base += 32 * kBatch) {
-    int eb[kBatch];
 #pragma unroll
     for (int i = 0; i < kBatch; ++i) eb[i] = local_of(base + 32 * i + lane);
 #pragma unroll
@@ -150,7 +156,7 @@ __global__ void __launch_bounds__(kRoutePrepThreads, 1) route_place_kernel(const
   if (tid < E) {
     const int e = tid;
     int run = 0;
-    for (int w = 0; w < kRoutePrepWarps; ++w) {
+    for (int w = 0; w < nw; ++w) {
       const int t = whist[w * E + e];
       whist[w * E + e] = run;
       run += t;
@@ -223,9 +229,10 @@ __global__ void __launch_bounds__(kRoutePrepThreads, 1) route_place_kernel(const
 
   // pass 3: stable placement of this CTA's routes
   for (int base = r_begin; base < r_end; base += 32 * kBatch) {
-    int eb[kBatch];
+    if (!one_batch) {
 #pragma unroll
-    for (int i = 0; i < kBatch; ++i) eb[i] = local_of(base + 32 * i + lane);
+      for (int i = 0; i < kBatch; ++i) eb[i] = local_of(base + 32 * i + lane);
+    }
 #pragma unroll
     for (int i = 0; i < kBatch; ++i) {
       const int r = base + 32 * i + lane;
