@@ -49,6 +49,7 @@ def kernel_source_hash():
     h = hashlib.sha256()
     for f in ("weight_only_int4_histogram_gb300/csrc/gemm.cuh",
               "weight_only_int4_histogram_gb300/csrc/gemv.cuh",
+              "weight_only_int4_histogram_gb300/csrc/gemv_fused.cuh",
               "weight_only_int4_histogram_gb300/csrc/common.cuh"):
         with open(os.path.join(ROOT, f), "rb") as fh:
             h.update(fh.read())
@@ -518,9 +519,13 @@ def run_gpu(args):
     warm = time_warm(g, stream)
     # the dominant kernel's live timing and roofline
     st = time_stages(moe, w, x, ids, tw, out, flush, stream, max(args.steps, 5))
-    b = stage_bytes(cfg, ids)
-    k = max(range(3), key=lambda i: st[i])
+    b = list(stage_bytes(cfg, ids))
     names = ["gate_up_gemm", "down_gemm", "combine"]
+    if moe.route_info(args.tokens).fused_gemms:
+        # CUDA-core path with both GEMMs in one launch: its events coincide
+        names = ["expert_gemms_fused", "down_gemm_in_fused", "combine"]
+        b = [b[0] + b[1], 0, b[2]]
+    k = max(range(3), key=lambda i: st[i])
     achieved = b[k] / (st[k] * 1e-6) / 1e9
     roof = {"kernel": names[k], "bound": "hbm", "achieved": round(achieved, 1), "peak": hbm,
             "peak_kind": f"{peak_kind} hbm_gbs", "unit": "GB/s",
