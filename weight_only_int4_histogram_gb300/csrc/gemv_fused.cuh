@@ -79,7 +79,31 @@ constexpr int kFzOffXBar = kFzOffHdrBar + 8 * kGemvMaxStages;  // xfull[2], xemp
 constexpr int kFzOffFlags = kFzOffXBar + 32;                    // abort, issued, stopped
 constexpr int kFzOffHdr = 512;
 static_assert(kFzOffFlags + 16 <= kFzOffHdr, "control block");
-static_assert(kFzOffHdr + kGemvMaxStages * 64 <= kGemvCtrlBytes, "stage headers");
+// Fused finalize: a queue of finished (slot range, 16-column block) records
+// from the compute warps to the finalize warp.
+constexpr int kFinQ = 128;
+constexpr int kFzOffFinRec = kFzOffHdr + kGemvMaxStages * 64;  // int4 [kFinQ]
+constexpr int kFzOffFinFlag = kFzOffFinRec + kFinQ * 16;       // int [kFinQ]
+constexpr int kFzOffFinCtl = kFzOffFinFlag + kFinQ * 4;        // tail, head, done
+static_assert(kFzOffFinCtl + 16 <= kGemvCtrlBytes, "finalize queue");
+// Warps: producer, activation rows, 16 compute, finalize.
+constexpr int kFusedThreads = 32 * (2 + kGemvComputeWarps + 1);
+constexpr int kFinWarp = 2 + kGemvComputeWarps;
+
+struct FinQueue {
+  int4* rec;              // (first slot, routes, first output column, 0)
+  volatile int* flag;     // record i is ready when flag[i % kFinQ] == i + 1
+  int* tail;              // records allocated (shared-memory atomic)
+  volatile int* head;     // records consumed by the finalize warp
+  int* done;              // compute warps finished
+};
+
+// A compute warp's last down unit, published one unit later (its fence then
+// finds those stores long completed).
+struct FinPending {
+  int m0, rows, c0;
+  bool valid;
+};
 
 __device__ __forceinline__ int ld_acquire_gpu(const int32_t* p) {
   int v;
@@ -221,18 +245,39 @@ __device__ __forceinline__ void finalize_block(const FusedParams& fp, int t, int
 #pragma unroll
   for (int c = 0; c < 16; ++c) acc[c] = 0.0f;
   const uint16_t* y = reinterpret_cast<const uint16_t*>(fp.down.out);
-  for (int j = 0; j < k; ++j) {
-    const int slot = inv[j];
-    if (slot < 0) continue;
-    float w = tw[j];
-    if (fp.renormalize) w = (wsum != 0.0f) ? __fdiv_rn(w, wsum) : 0.0f;
-    const uint4* yr = reinterpret_cast<const uint4*>(y + static_cast<int64_t>(slot) * H + c0);
-    const uint4 u0 = __ldcg(yr), u1 = __ldcg(yr + 1);
-    const uint32_t v[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+  // routes in chunks of 4: every load of a chunk is issued before its sums
+  // (which stay in top-k order)
+  for (int j0 = 0; j0 < k; j0 += 4) {
+    int slot[4];
+    float w[4];
 #pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      acc[2 * c] = __fadd_rn(acc[2 * c], __fmul_rn(w, F16<DT>::to_float(static_cast<uint16_t>(v[c] & 0xFFFFu))));
-      acc[2 * c + 1] = __fadd_rn(acc[2 * c + 1], __fmul_rn(w, F16<DT>::to_float(static_cast<uint16_t>(v[c] >> 16))));
+    for (int i = 0; i < 4; ++i) {
+      slot[i] = j0 + i < k ? inv[j0 + i] : -1;
+      w[i] = j0 + i < k ? tw[j0 + i] : 0.0f;
+    }
+    uint4 u[4][2];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      if (slot[i] >= 0) {
+        const uint4* yr = reinterpret_cast<const uint4*>(y + static_cast<int64_t>(slot[i]) * H + c0);
+        u[i][0] = __ldcg(yr);
+        u[i][1] = __ldcg(yr + 1);
+      } else {
+        u[i][0] = u[i][1] = make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      if (slot[i] < 0) continue;
+      float wi = w[i];
+      if (fp.renormalize) wi = (wsum != 0.0f) ? __fdiv_rn(wi, wsum) : 0.0f;
+      const uint32_t v[8] = {u[i][0].x, u[i][0].y, u[i][0].z, u[i][0].w, u[i][1].x, u[i][1].y, u[i][1].z, u[i][1].w};
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        acc[2 * c] = __fadd_rn(acc[2 * c], __fmul_rn(wi, F16<DT>::to_float(static_cast<uint16_t>(v[c] & 0xFFFFu))));
+        acc[2 * c + 1] =
+            __fadd_rn(acc[2 * c + 1], __fmul_rn(wi, F16<DT>::to_float(static_cast<uint16_t>(v[c] >> 16))));
+      }
     }
   }
   uint32_t o[8];
@@ -245,13 +290,122 @@ __device__ __forceinline__ void finalize_block(const FusedParams& fp, int t, int
   dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
 }
 
+// Publish a compute warp's pending record: every lane's fence makes its output
+// stores visible to the device, then lane 0 queues the record for the finalize
+// warp (waiting, bounded, for a free entry).
+__device__ __forceinline__ bool fin_publish(const FusedParams& fp, const FinQueue& fq, FinPending& pend, int lane,
+                                            volatile int* abort_flag) {
+  __threadfence();
+  __syncwarp();
+  int ok = 1;
+  if (lane == 0) {
+    const int i = atomicAdd(fq.tail, 1);
+    const uint64_t t0 = global_timer_ns();
+    while (i - *fq.head >= kFinQ) {
+      if (*abort_flag) {
+        ok = 0;
+        break;
+      }
+      if (global_timer_ns() - t0 > fp.up.wait_ns) {
+        *abort_flag = 1;
+        atomicExch(fp.up.err, kErrTimeout);
+        ok = 0;
+        break;
+      }
+      __nanosleep(64);
+    }
+    if (ok) {
+      fq.rec[i % kFinQ] = make_int4(pend.m0, pend.rows, pend.c0, 0);
+      __threadfence_block();
+      fq.flag[i % kFinQ] = i + 1;
+    }
+  }
+  pend.valid = false;
+  return __shfl_sync(0xFFFFFFFFu, ok, 0) != 0;
+}
+
+// The finalize warp: takes ready records in order, up to 32 routes at a time
+// (one lane per route); per route one arrival on its (token, 16-column block)
+// counter; the arrival that completes a token's valid routes sums the block.
+template <int DT>
+__device__ __forceinline__ void fin_warp(const FusedParams& fp, const FinQueue& fq, int lane,
+                                         volatile int* abort_flag) {
+  const GemmParams& p = fp.down;
+  const int nblk = p.n_rows / 16;
+  int head = 0;
+  const uint64_t t0 = global_timer_ns();
+  uint64_t last_progress = t0;
+  for (;;) {
+    const int idx = head + lane;
+    const bool rdy = fq.flag[idx % kFinQ] == idx + 1;
+    const unsigned m = __ballot_sync(0xFFFFFFFFu, rdy);
+    const int n = (m == 0xFFFFFFFFu) ? 32 : __ffs(~m) - 1;  // ready records in order
+    if (n == 0) {
+      if (*fq.done == kGemvComputeWarps && *reinterpret_cast<volatile int*>(fq.tail) == head) break;
+      if (*abort_flag) break;
+      if (global_timer_ns() - last_progress > fp.up.wait_ns) {
+        if (lane == 0) {
+          *abort_flag = 1;
+          atomicExch(fp.up.err, kErrTimeout);
+        }
+        break;
+      }
+      __nanosleep(64);
+      continue;
+    }
+    __threadfence_block();
+    const int4 rec = lane < n ? fq.rec[idx % kFinQ] : make_int4(0, 0, 0, 0);
+    // records whose routes fit in this pass (every record holds <= 32 routes)
+    int incl = rec.y;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    const int ex = incl - rec.y;
+    const int taken = __popc(__ballot_sync(0xFFFFFFFFu, lane < n && incl <= 32));
+    const int total = __shfl_sync(0xFFFFFFFFu, incl, taken - 1);
+    // lane -> (record j, route r)
+    int j = 0;
+    for (int i = 1; i < taken; ++i)
+      if (__shfl_sync(0xFFFFFFFFu, ex, i) <= lane) j = i;
+    const int m0 = __shfl_sync(0xFFFFFFFFu, rec.x, j);
+    const int c0 = __shfl_sync(0xFFFFFFFFu, rec.z, j);
+    const int r = lane - __shfl_sync(0xFFFFFFFFu, ex, j);
+    int fin_t = -1;
+    if (lane < total) {
+      const int route = p.perm[m0 + r];
+      const int t = route / fp.k;
+      int valid = 0;
+#pragma unroll 4
+      for (int q = 0; q < fp.k; ++q) valid += fp.inv[static_cast<int64_t>(t) * fp.k + q] >= 0;
+      int32_t* ctr = fp.fin_ctr + static_cast<int64_t>(t) * nblk + c0 / 16;
+      const int old = atomicAdd(ctr, 1);
+      if (old == valid - 1) {
+        __threadfence();  // acquire the other routes' outputs
+        *ctr = 0;         // for a forward that reuses this route layout
+        fin_t = t;
+      }
+    }
+    if (fin_t >= 0) finalize_block<DT>(fp, fin_t, c0);
+    head += taken;
+    __syncwarp();
+    if (lane == 0) *fq.head = head;
+    last_progress = global_timer_ns();
+  }
+}
+
 // Epilogue of a down unit on one finishing warp: expert outputs in the
 // activation dtype (one rounding), per-channel scales applied here.
 template <int SCALE, int DT, int NB>
-__device__ __forceinline__ void fused_down_epilogue(const FusedParams& fp, const StageHdr& h, int rowA, int rowB,
-                                                    int lane, const float (&tot)[4 * NB]) {
+__device__ __forceinline__ bool fused_down_epilogue(const FusedParams& fp, const StageHdr& h, int rowA, int rowB,
+                                                    int lane, const float (&tot)[4 * NB], const FinQueue& fq,
+                                                    FinPending& pend, volatile int* abort_flag) {
   // (fused finalize: rowA = 16 rb + g, so rowA >> 4 is the row block)
   const GemmParams& p = fp.down;
+  if (fp.finalize && pend.valid) {
+    if (!fin_publish(fp, fq, pend, lane, abort_flag)) return false;
+  }
   const int t = lane & 3;
   const int N = p.n_rows;
   const int rows = min(h.rows, kGemvMaxR);
@@ -273,30 +427,13 @@ __device__ __forceinline__ void fused_down_epilogue(const FusedParams& fp, const
     if (rt0 < rows && okB) y[rt0 * oc + growB] = F16<DT>::from_float(tot[4 * n + 2] * scB);
     if (rt1 < rows && okB) y[rt1 * oc + growB] = F16<DT>::from_float(tot[4 * n + 3] * scB);
   }
-  if (!fp.finalize) return;
-  // Fused finalize: this warp's 16 output columns are done for its routes; the
-  // last arrival of a token's valid routes sums that token's block.
-  const int c0 = 128 * h.nt + 16 * (rowA >> 4);
-  if (c0 >= N) return;
-  __syncwarp();
-  if (lane == 0) __threadfence();  // publish the stores above
-  __syncwarp();
-  const int nblk = N / 16;
-  int fin_t = -1;
-  if (lane < rows) {
-    const int route = p.perm[h.m0 + lane];
-    const int t = route / fp.k;
-    int valid = 0;
-    for (int j = 0; j < fp.k; ++j) valid += fp.inv[static_cast<int64_t>(t) * fp.k + j] >= 0;
-    int32_t* ctr = fp.fin_ctr + static_cast<int64_t>(t) * nblk + c0 / 16;
-    const int old = atomicAdd(ctr, 1);
-    if (old == valid - 1) {
-      __threadfence();  // acquire the other routes' stores
-      *ctr = 0;         // for a forward that reuses this route layout
-      fin_t = t;
-    }
+  if (fp.finalize) {
+    // this warp's 16 output columns of the tile's routes: published with the
+    // next down unit of this warp (or when it finishes)
+    const int c0 = 128 * h.nt + 16 * (rowA >> 4);
+    if (c0 < N) pend = FinPending{h.m0, rows, c0, true};
   }
-  if (fin_t >= 0) finalize_block<DT>(fp, fin_t, c0);
+  return true;
 }
 
 // Ring walk of one compute group: slots of parity grp, ring_len even.
@@ -321,7 +458,7 @@ __device__ __forceinline__ bool fused_unit(const FusedParams& fp, uint8_t* smem,
                                            const StageHdr* hdrs, volatile int* abort_flag, float* red,
                                            int ring_len, int grp, int rowA, int rowB, int rb, int lane,
                                            uint32_t ld_row_off, int ld_row7, int ld_chunk, GroupRing& r,
-                                           uint32_t& xj) {
+                                           uint32_t& xj, const FinQueue& fq, FinPending& pend) {
   const StageHdr h = hdrs[r.slot];
   float tot[4 * NB];
 #pragma unroll
@@ -367,13 +504,15 @@ __device__ __forceinline__ bool fused_unit(const FusedParams& fp, uint8_t* smem,
   } else if (!finisher) {
     return true;
   }
-  if (h.type == kItemUp) fused_up_epilogue<SCALE, DT, NB>(fp, h, rowA, rowB, rb, lane, tot);
-  else fused_down_epilogue<SCALE, DT, NB>(fp, h, rowA, rowB, lane, tot);
-  return true;
+  if (h.type == kItemUp) {
+    fused_up_epilogue<SCALE, DT, NB>(fp, h, rowA, rowB, rb, lane, tot);
+    return true;
+  }
+  return fused_down_epilogue<SCALE, DT, NB>(fp, h, rowA, rowB, lane, tot, fq, pend, abort_flag);
 }
 
 template <int SCALE, int DT, int LAYOUT>
-__global__ void __launch_bounds__(kGemvThreads, 1)
+__global__ void __launch_bounds__(kFusedThreads, 1)
     w4a16_gemv_fused_kernel(const __grid_constant__ FusedParams fp, const __grid_constant__ CUtensorMap tmA1,
                             const __grid_constant__ CUtensorMap tmS1, const __grid_constant__ CUtensorMap tmA2,
                             const __grid_constant__ CUtensorMap tmS2) {
@@ -392,6 +531,12 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
   volatile int* prod_issued = abort_flag + 1;
   volatile int* prod_stopped = abort_flag + 2;
   StageHdr* hdrs = reinterpret_cast<StageHdr*>(ctrl + kFzOffHdr);
+  FinQueue fq;
+  fq.rec = reinterpret_cast<int4*>(ctrl + kFzOffFinRec);
+  fq.flag = reinterpret_cast<volatile int*>(ctrl + kFzOffFinFlag);
+  fq.tail = reinterpret_cast<int*>(ctrl + kFzOffFinCtl);
+  fq.head = reinterpret_cast<volatile int*>(ctrl + kFzOffFinCtl + 4);
+  fq.done = reinterpret_cast<int*>(ctrl + kFzOffFinCtl + 8);
   float* red = reinterpret_cast<float*>(ctrl + kGemvCtrlBytes);
 
   const int warp = threadIdx.x >> 5;
@@ -409,6 +554,10 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
     }
     *abort_flag = 0;
     *prod_stopped = 0;
+    *fq.tail = 0;
+    *fq.head = 0;
+    *fq.done = 0;
+    for (int i = 0; i < kFinQ; ++i) fq.flag[i] = 0;
     fence_barrier_init();
   }
   if (warp == 0 && lane == 0) {
@@ -658,7 +807,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
       }
     }
     asm volatile("cp.async.wait_all;" ::: "memory");
-  } else {
+  } else if (warp < kFinWarp) {
     // ------------------------------------------------------------------ compute groups
     const int cw = warp - 2, grp = cw >> 3, rb = cw & 7, g = lane >> 2;
     // rows of this warp: SwiGLU gate/up tiles pair gate row 8 rb + g with its
@@ -686,6 +835,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
     r.ph = 0;
     r.seq = static_cast<uint32_t>(grp);
     uint32_t xj = 0;
+    FinPending pend{0, 0, 0, false};
     for (;;) {
       if (!warp_wait(&full[r.slot], r.ph, abort_flag, pu.err, pu.wait_ns)) break;
       const int type = hdrs[r.slot].type;
@@ -698,13 +848,25 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
       bool ok;
 #define W4A16_FUSED_UNIT(NBV)                                                                                   \
   fused_unit<SCALE, DT, LAYOUT, NBV>(fp, smem, stage_bytes, full, empty, xfull, xempty, hdrs, abort_flag, red, \
-                                     ring_len, grp, rowA, rowB, rb, lane, off, r7, ch, r, xj)
+                                     ring_len, grp, rowA, rowB, rb, lane, off, r7, ch, r, xj, fq, pend)
       if (nb <= 1) ok = W4A16_FUSED_UNIT(1);
       else if (nb == 2) ok = W4A16_FUSED_UNIT(2);
       else ok = W4A16_FUSED_UNIT(4);
 #undef W4A16_FUSED_UNIT
       if (!ok) break;
     }
+    if (fp.finalize) {
+      // the last down unit's record, then this warp's end
+      if (pend.valid && !*abort_flag) fin_publish(fp, fq, pend, lane, abort_flag);
+      __syncwarp();
+      if (lane == 0) {
+        __threadfence_block();
+        atomicAdd(fq.done, 1);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------------ finalize
+    if (fp.finalize) fin_warp<DT>(fp, fq, lane, abort_flag);
   }
   __syncthreads();
   if (fp.finalize) {
@@ -740,7 +902,7 @@ cudaError_t launch_gemv_fused_one(const FusedParams& fp, const CUtensorMap& tmA1
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kGemvThreads);
+  cfg.blockDim = dim3(kFusedThreads);
   cfg.dynamicSmemBytes = smem_bytes;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
