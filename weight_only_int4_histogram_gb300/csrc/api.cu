@@ -167,6 +167,12 @@ int choose_bn(const w4a16_moe_plan_s& P, int T) {
   const double lam = static_cast<double>(T) * P.d.top_k / P.d.num_experts;
   const double want = lam + 3.0 * std::sqrt(lam) + 1.0;
   int bn = static_cast<int>(std::ceil(want / 16.0)) * 16;
+  // Exception: short gate/up reductions (at most 8 stages of 256) whose
+  // experts a 96-route tile covers where 64 would take two tiles: one tile
+  // per expert dequantises every weight once instead of twice, which outweighs
+  // the shallower ring on such short units (the 60-expert H 2048 per-channel
+  // shape at 1024 tokens: 239 -> 186 us; the long-K shapes got slower).
+  if (bn > kAutoMaxBN && bn <= 96 && cdiv(P.d.hidden, kBlockK) <= 8) return 96;
   return std::min(kAutoMaxBN, std::max(16, bn));
 }
 
