@@ -52,3 +52,29 @@ def test_short_wait_limit_reports_timeout_and_context_survives(monkeypatch, path
     torch.cuda.synchronize()
     normal.check_device_error()
     compare(out, oracle_rows(cfg, w, x, ids, tw), "after a timed-out forward")
+
+
+def test_short_wait_limit_with_fused_finalize(monkeypatch):
+    # the fused CUDA-core launch with its finalize warp: every one of its waits
+    # (stage, queue-space, record and ready waits) gives up cleanly too
+    cfg = small_cfg(E=4, H=7168, I=256, k=2)
+    T = 48
+    w, x, ids, tw = case_on_gpu(cfg, T)
+    monkeypatch.setenv("W4A16_MOE_WAIT_TIMEOUT_NS", "1")
+    short = make_moe(cfg, T)
+    monkeypatch.delenv("W4A16_MOE_WAIT_TIMEOUT_NS")
+    short.set_gemm_path(2)
+    short.set_fused_finalize(True)
+    assert short.route_info(T).fused_finalize == 1
+    short(x, w, tw, ids)
+    torch.cuda.synchronize()
+    with pytest.raises(_lib.W4A16Error) as ei:
+        short.check_device_error()
+    assert ei.value.status == 5  # W4A16_ERR_DEVICE_TIMEOUT
+    normal = make_moe(cfg, T)
+    normal.set_gemm_path(2)
+    normal.set_fused_finalize(True)
+    out = normal(x, w, tw, ids)
+    torch.cuda.synchronize()
+    normal.check_device_error()
+    compare(out, oracle_rows(cfg, w, x, ids, tw), "fused finalize after a timed-out forward")
