@@ -376,6 +376,36 @@ bool encode_weights(CUtensorMap* m, const void* base, uint64_t inner, uint64_t r
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// One whole 128-row weight tile per copy (the fused CUDA-core launch).
+// Gated W13 with inter a multiple of 64: a 5D view [E][gate | up][I / 64][64
+// rows][inner bytes], so that one box takes a tile's 64 gate rows and their 64
+// up rows (inter rows apart) -- the view covers the tensor exactly.  Otherwise
+// rows are contiguous: boxes of 128 rows of a 3D [E][rows][inner] view (rows
+// past the end read as zero).  elem: 1 (packed bytes, 128-byte swizzle) or 2
+// (BF16 scales, unswizzled); box_inner in elements.
+bool encode_tile128(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint64_t E, uint64_t gated_half,
+                    int elem, uint32_t box_inner) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const CUtensorMapDataType t = elem == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const CUtensorMapSwizzle sw = elem == 1 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE;
+  const uint64_t row_bytes = inner * elem;
+  if (gated_half != 0) {
+    cuuint64_t dims[5] = {inner, 64, gated_half / 64, 2, E};
+    cuuint64_t strides[4] = {row_bytes, 64 * row_bytes, gated_half * row_bytes, 2 * gated_half * row_bytes};
+    cuuint32_t box[5] = {box_inner, 64, 1, 2, 1};
+    cuuint32_t es[5] = {1, 1, 1, 1, 1};
+    return fn(m, t, 5, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  }
+  cuuint64_t dims[3] = {inner, rows, E};
+  cuuint64_t strides[2] = {row_bytes, row_bytes * rows};
+  cuuint32_t box[3] = {box_inner, 128, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, t, 3, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Expert outputs y [rows][cols] (FP32, or the 16-bit activation dtype), unswizzled
 // boxes of 32 columns x 16 rows (the down GEMM's output stores).
 bool encode_out(CUtensorMap* m, void* base, uint64_t cols, uint64_t rows, bool fp32, int dtype) {
@@ -517,10 +547,17 @@ w4a16_status launch_combine_of(const w4a16_moe_plan_s& P, const Layout& L, bool 
 }
 
 // CUDA-core path, both GEMMs in one launch (gemv_fused.cuh), then the combine.
+// Gate rows per half of a gated W13 when the whole-tile 5D view applies
+// (inter a multiple of 64), else 0.  The fused kernel takes the same decision.
+uint64_t fused_gate_half(const w4a16_moe_desc& d) {
+  return (d.act == W4A16_ACT_SWIGLU && d.inter % 64 == 0) ? static_cast<uint64_t>(d.inter) : 0;
+}
+
 w4a16_status launch_forward_fused(const w4a16_moe_plan_s& P, const Layout& L, const GemmParams& g,
                                   const GemmParams& g1, const CUtensorMap& tmA1, const CUtensorMap& tmS1,
-                                  const CUtensorMap& tmA2, const CUtensorMap& tmS2, bool stma2, const uint16_t* s2,
-                                  const float* tw, int32_t renorm, void* out, uint8_t* ws, cudaStream_t s) {
+                                  const CUtensorMap& tmA2, const CUtensorMap& tmS2, bool stma2, const uint8_t* w13,
+                                  const uint16_t* s13, const uint8_t* w2, const uint16_t* s2, const float* tw,
+                                  int32_t renorm, void* out, uint8_t* ws, cudaStream_t s) {
   const w4a16_moe_desc& d = P.d;
   FusedParams fp = {};
   fp.up = g1;
@@ -557,8 +594,24 @@ w4a16_status launch_forward_fused(const w4a16_moe_plan_s& P, const Layout& L, co
     fp.reset_len = L.fix_len;
   }
   const int lay = P.layout == W4A16_LAYOUT_INTERLEAVED ? LAYOUT_IL : LAYOUT_CANON;
+  // whole-tile copies (one box per weight tile and stage) for the K-packed
+  // layouts; the per-channel row-pair layout keeps its four boxes
+  CUtensorMap wA1 = tmA1, wS1 = tmS1, wA2 = tmA2, wS2 = tmS2;
+  const bool group = d.scale_kind == W4A16_SCALE_GROUP32_K;
+  if (group || lay == LAYOUT_IL) {
+    const uint64_t half = fused_gate_half(d);
+    // gated W13 whose inter is an odd multiple of 32 keeps its 64-row boxes
+    // (a tile's halves are neither consecutive nor a whole 5D view)
+    const bool up_whole = d.act != W4A16_ACT_SWIGLU || half != 0;
+    bool ok = !up_whole || encode_tile128(&wA1, w13, d.hidden / 2, L.n1, d.num_experts, half, 1, 128);
+    ok = ok && encode_tile128(&wA2, w2, d.inter / 2, d.hidden, d.num_experts, 0, 1, 128);
+    if (ok && up_whole && fp.up.scale_tma)
+      ok = encode_tile128(&wS1, s13, d.hidden / kGroup, L.n1, d.num_experts, half, 2, 8);
+    if (ok && fp.down.scale_tma) ok = encode_tile128(&wS2, s2, d.inter / kGroup, d.hidden, d.num_experts, 0, 2, 8);
+    if (!ok) return fail(W4A16_ERR_CUDA, "cuTensorMapEncodeTiled failed (whole-tile weight boxes)");
+  }
   cudaError_t e =
-      launch_gemv_fused(d.scale_kind, d.act_dtype, lay, fp, tmA1, tmS1, tmA2, tmS2, L.grid1, L.smem, s, P.pdl);
+      launch_gemv_fused(d.scale_kind, d.act_dtype, lay, fp, wA1, wS1, wA2, wS2, L.grid1, L.smem, s, P.pdl);
   if (e != cudaSuccess) return cuda_fail(e, "fused expert GEMM launch");
   // both GEMMs end with the one launch: the gate/up and down stage marks coincide
   if (P.has_ev && ((e = cudaEventRecord(P.ev[1], s)) != cudaSuccess || (e = cudaEventRecord(P.ev[2], s)) != cudaSuccess))
@@ -646,7 +699,8 @@ w4a16_status launch_forward(const w4a16_moe_plan_s& P, const Layout& L, const vo
   g1.scale_tma = stma1 ? 1 : 0;
   cudaError_t e;
   if (P.has_ev && (e = cudaEventRecord(P.ev[0], s)) != cudaSuccess) return cuda_fail(e, "event record");
-  if (L.fused) return launch_forward_fused(P, L, g, g1, tmA1, tmS1, tmA2, tmS2, stma2, s2, tw, renorm, out, ws, s);
+  if (L.fused)
+    return launch_forward_fused(P, L, g, g1, tmA1, tmS1, tmA2, tmS2, stma2, w13, s13, w2, s2, tw, renorm, out, ws, s);
   e = L.gemv ? launch_gemv(GEMM_UP, d.scale_kind, d.act_dtype, lay, g1, tmA1, tmS1, L.grid1, L.smem, s, P.pdl)
              : launch_gemm(GEMM_UP, d.scale_kind, d.act_dtype, lay, g1, tmA1, tmNone, tmY, tmS1, L.grid1, L.smem, s,
                            P.pdl);

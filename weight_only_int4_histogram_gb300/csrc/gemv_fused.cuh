@@ -584,6 +584,10 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     }
     const uint64_t pol_w = l2_policy_evict_first();
     const uint64_t pol_s = l2_policy_evict_last();
+    // gated gate/up tiles through the 5D whole-tile view (inter a multiple of
+    // 64; the host encodes the maps by the same rule)
+    const bool gated_up = pu.act == ACT_SWIGLU;
+    const bool gate5d = gated_up && (pu.inter % 64) == 0;
     const int n_t = *pu.num_tiles;
     const int nt1 = pu.n_tiles, s1 = pu.splits;
     const GemmParams& pd = fp.down;
@@ -639,11 +643,26 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
         mbar_arrive(&hdrb[slot]);
         mbar_arrive_expect_tx(&full[slot], kGvWeightBytes + (stma ? kTileRows * kGvScaleRowBytes : 0));
         if (SCALE == SCALE_GROUP || LAYOUT == LAYOUT_IL) {
-          tma_load_3d(sA, &tmA, &full[slot], kb * (kGemvBlockK / 2), r0, e, pol_w);
-          tma_load_3d(sA + 8192, &tmA, &full[slot], kb * (kGemvBlockK / 2), r1, e, pol_w);
-          if (stma) {
-            tma_load_3d(sS, &tmS, &full[slot], kb * (kGemvBlockK / kGroup), r0, e, pol_s);
-            tma_load_3d(sS + 64 * kGvScaleRowBytes, &tmS, &full[slot], kb * (kGemvBlockK / kGroup), r1, e, pol_s);
+          // one box per tile: the weight rows (and their group scales) of the
+          // whole 128-row tile -- a 5D view pairs a gated tile's gate and up
+          // halves, otherwise the tile's rows are consecutive
+          if (type == kItemUp && gated_up) {
+            if (gate5d) {
+              tma_load_5d(sA, &tmA, &full[slot], kb * (kGemvBlockK / 2), 0, nt, 0, e, pol_w);
+              if (stma) tma_load_5d(sS, &tmS, &full[slot], kb * (kGemvBlockK / kGroup), 0, nt, 0, e, pol_s);
+            } else {
+              // inter an odd multiple of 32: 64-row boxes of the gate and up halves
+              tma_load_3d(sA, &tmA, &full[slot], kb * (kGemvBlockK / 2), r0, e, pol_w);
+              tma_load_3d(sA + 8192, &tmA, &full[slot], kb * (kGemvBlockK / 2), r1, e, pol_w);
+              if (stma) {
+                tma_load_3d(sS, &tmS, &full[slot], kb * (kGemvBlockK / kGroup), r0, e, pol_s);
+                tma_load_3d(sS + 64 * kGvScaleRowBytes, &tmS, &full[slot], kb * (kGemvBlockK / kGroup), r1, e,
+                            pol_s);
+              }
+            }
+          } else {
+            tma_load_3d(sA, &tmA, &full[slot], kb * (kGemvBlockK / 2), r0, e, pol_w);
+            if (stma) tma_load_3d(sS, &tmS, &full[slot], kb * (kGemvBlockK / kGroup), r0, e, pol_s);
           }
         } else {
 #pragma unroll
