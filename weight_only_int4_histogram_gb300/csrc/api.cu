@@ -662,6 +662,17 @@ w4a16_status launch_forward(const w4a16_moe_plan_s& P, const Layout& L, const vo
   if (stma1) ok = ok && encode_scales(&tmS1, s13, d.hidden / kGroup, L.n1, d.num_experts);
   if (stma2) ok = ok && encode_scales(&tmS2, s2, d.inter / kGroup, d.hidden, d.num_experts);
   if (!ok) return fail(W4A16_ERR_CUDA, "cuTensorMapEncodeTiled failed (driver entry point or arguments)");
+  // tensor-core path: whole-tile boxes for the K-packed layouts (one copy per
+  // 128-row weight tile and stage; see encode_tile128)
+  if (!L.gemv && (group || il)) {
+    const uint64_t half = fused_gate_half(d);
+    const bool up_whole = d.act != W4A16_ACT_SWIGLU || half != 0;
+    ok = (!up_whole || encode_tile128(&tmA1, w13, d.hidden / 2, L.n1, d.num_experts, half, 1, 128)) &&
+         encode_tile128(&tmA2, w2, d.inter / 2, d.hidden, d.num_experts, 0, 1, 128);
+    if (ok && up_whole && stma1) ok = encode_tile128(&tmS1, s13, d.hidden / kGroup, L.n1, d.num_experts, half, 2, 8);
+    if (ok && stma2) ok = encode_tile128(&tmS2, s2, d.inter / kGroup, d.hidden, d.num_experts, 0, 2, 8);
+    if (!ok) return fail(W4A16_ERR_CUDA, "cuTensorMapEncodeTiled failed (whole-tile weight boxes)");
+  }
 
   GemmParams g = {};
   g.act = d.act;

@@ -399,6 +399,8 @@ __global__ void __launch_bounds__(WHICH == GEMM_DOWN ? kGemmThreadsDown : kGemmT
     // ------------------------------------------------------------------ producer
     const uint64_t pol_w = l2_policy_evict_first();
     const uint64_t pol_b = l2_policy_evict_last();
+    const bool gated = WHICH == GEMM_UP && p.act == ACT_SWIGLU;
+    const bool gate5d = gated && (p.inter % 64) == 0;
     const int groups_row = p.K / kGroup;
     const int sbytes_row = groups_row * 2;
     uint32_t it = 0, ph = 0;
@@ -450,14 +452,27 @@ __global__ void __launch_bounds__(WHICH == GEMM_DOWN ? kGemmThreadsDown : kGemmT
             tile_row_bases<WHICH>(p, w.grp * NT + t, r0, r1);
             uint8_t* sAt = sA + t * kStageA;
             if (kPacked) {
-              // two 64-row boxes of 128 packed bytes (256 K values), 128-byte swizzle
-              tma_load_3d(sAt, &tmA, &full[st], kb * (kBlockK / 2), r0, e, pol_w);
-              tma_load_3d(sAt + 8192, &tmA, &full[st], kb * (kBlockK / 2), r1, e, pol_w);
-              if (SCALE == SCALE_GROUP && p.scale_tma) {
-                // two 64-row boxes of 8 group scales (16 bytes)
-                uint8_t* sS = sA + off_s + t * kStageS;
-                tma_load_3d(sS, &tmS, &full[st], kb * kGroupsPerStage, r0, e, pol_w);
-                tma_load_3d(sS + 1024, &tmS, &full[st], kb * kGroupsPerStage, r1, e, pol_w);
+              // the whole 128-row tile of 128 packed bytes (256 K values) per
+              // box, 128-byte swizzle, and its 8 group scales per row: a 5D
+              // view pairs a gated tile's 64 gate and 64 up rows, other tiles
+              // are 128 consecutive rows (the host encodes the maps by the same
+              // rule; gated tiles of an inter that is an odd multiple of 32
+              // keep two 64-row boxes)
+              uint8_t* sS = sA + off_s + t * kStageS;
+              const bool stma = SCALE == SCALE_GROUP && p.scale_tma;
+              if (gated && gate5d) {
+                tma_load_5d(sAt, &tmA, &full[st], kb * (kBlockK / 2), 0, w.grp * NT + t, 0, e, pol_w);
+                if (stma) tma_load_5d(sS, &tmS, &full[st], kb * kGroupsPerStage, 0, w.grp * NT + t, 0, e, pol_w);
+              } else if (gated) {
+                tma_load_3d(sAt, &tmA, &full[st], kb * (kBlockK / 2), r0, e, pol_w);
+                tma_load_3d(sAt + 8192, &tmA, &full[st], kb * (kBlockK / 2), r1, e, pol_w);
+                if (stma) {
+                  tma_load_3d(sS, &tmS, &full[st], kb * kGroupsPerStage, r0, e, pol_w);
+                  tma_load_3d(sS + 1024, &tmS, &full[st], kb * kGroupsPerStage, r1, e, pol_w);
+                }
+              } else {
+                tma_load_3d(sAt, &tmA, &full[st], kb * (kBlockK / 2), r0, e, pol_w);
+                if (stma) tma_load_3d(sS, &tmS, &full[st], kb * kGroupsPerStage, r0, e, pol_w);
               }
             } else {
               // four boxes (row block, K half) of 32 row pairs x 128 K bytes, 128-byte swizzle
