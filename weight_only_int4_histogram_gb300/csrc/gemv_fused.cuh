@@ -51,6 +51,8 @@
 // tiles per route tile); with split-K, per-(m, nt, row block) counters elect
 // the last split's warp, which sums the FP32 partials in split order.
 #pragma once
+#include <type_traits>
+
 #include "gemv.cuh"
 
 namespace w4a16 {
@@ -594,6 +596,20 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     const int nt2 = pd.n_tiles, nch = (nt2 + fp.down_chunk - 1) / fp.down_chunk;
     const int q1 = n_t * nt1 * s1;
     const int qt = q1 + n_t * nch;
+    // The producer runs on lane 0 alone (no warp-wide waits or syncs on its
+    // issue path, which paces the whole ring) unless group scales of a GEMM
+    // have rows that are not 16-byte multiples, whose cp.async pieces take
+    // the whole warp.
+    const bool solo = SCALE != SCALE_GROUP || (fp.up.scale_tma && fp.down.scale_tma);
+    auto produce = [&](auto solo_c) {
+    constexpr bool kSolo = decltype(solo_c)::value;
+    auto wwait = [&](uint64_t* bar, uint32_t parity) -> bool {
+      if (kSolo) return mbar_wait(bar, parity, abort_flag, pu.err, pu.wait_ns);
+      return warp_wait(bar, parity, abort_flag, pu.err, pu.wait_ns);
+    };
+    auto wsync = [&]() {
+      if (!kSolo) __syncwarp();
+    };
     int slot = 0;
     uint32_t ph = 0, seq = 0;
     bool ok = true;
@@ -602,7 +618,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     // issue one stage: header, scales, weights
     auto issue = [&](const GemmParams& g, const CUtensorMap& tmA, const CUtensorMap& tmS, int type, int m,
                      const int4& ti, int nt, int kb, int split, uint32_t first, uint32_t last) -> bool {
-      if (!warp_wait(&empty[slot], ph ^ 1u, abort_flag, pu.err, pu.wait_ns)) return false;
+      if (!wwait(&empty[slot], ph ^ 1u)) return false;
       uint8_t* sA = smem + slot * stage_bytes;
       uint8_t* sS = sA + kGvOffS;
       const int e = ti.x;
@@ -611,7 +627,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
       if (type == kItemUp) tile_row_bases<GEMM_UP>(g, nt, r0, r1);
       else tile_row_bases<GEMM_DOWN>(g, nt, r0, r1);
       const bool stma = SCALE == SCALE_GROUP && g.scale_tma;
-      if (SCALE == SCALE_GROUP && !stma) {
+      if (!kSolo && SCALE == SCALE_GROUP && !stma) {
         const int groups_row = g.K / kGroup;
         const int g0 = kb * (kGemvBlockK / kGroup);
         const int ng = min(kGemvBlockK / kGroup, groups_row - g0);
@@ -638,7 +654,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
         h.first_seq = first;
         h.last_seq = last;
       }
-      __syncwarp();
+      wsync();
       if (lane == 0) {
         mbar_arrive(&hdrb[slot]);
         mbar_arrive_expect_tx(&full[slot], kGvWeightBytes + (stma ? kTileRows * kGvScaleRowBytes : 0));
@@ -673,7 +689,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
                           (b ? r1 : r0) / 2, e, pol_w);
         }
       }
-      __syncwarp();
+      wsync();
       ++seq;
       if (++slot == ring_len) {
         slot = 0;
@@ -682,7 +698,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
       return true;
     };
     while (ok) {
-      const int q = __shfl_sync(0xFFFFFFFFu, q_lane0, 0);
+      const int q = kSolo ? q_lane0 : __shfl_sync(0xFFFFFFFFu, q_lane0, 0);
       if (q >= qt) break;
       if (lane == 0) q_lane0 = atomicAdd(fp.queue, 1);  // the next entry, taken while this one streams
       if (q < q1) {
@@ -709,7 +725,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     }
     // two end markers, one for each compute group
     for (int j = 0; j < 2 && ok; ++j) {
-      if (!warp_wait(&empty[slot], ph ^ 1u, abort_flag, pu.err, pu.wait_ns)) {
+      if (!wwait(&empty[slot], ph ^ 1u)) {
         ok = false;
         break;
       }
@@ -718,7 +734,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
         mbar_arrive(&hdrb[slot]);
         mbar_arrive(&full[slot]);
       }
-      __syncwarp();
+      wsync();
       ++seq;
       if (++slot == ring_len) {
         slot = 0;
@@ -735,6 +751,12 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
       const uint32_t from = seq > static_cast<uint32_t>(ring_len) ? seq - ring_len : 0;
       for (uint32_t j = from; j < seq; ++j)
         mbar_wait(&full[j % ring_len], (j / ring_len) & 1, &no_abort, pu.err);
+    }
+    };
+    if (solo) {
+      if (lane == 0) produce(std::integral_constant<bool, true>());
+    } else {
+      produce(std::integral_constant<bool, false>());
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------------ activation rows
