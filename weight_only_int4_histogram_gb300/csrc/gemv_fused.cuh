@@ -513,7 +513,7 @@ __device__ __forceinline__ bool fused_unit(const FusedParams& fp, uint8_t* smem,
   return fused_down_epilogue<SCALE, DT, NB>(fp, h, rowA, rowB, lane, tot, fq, pend, abort_flag);
 }
 
-template <int SCALE, int DT, int LAYOUT>
+template <int SCALE, int DT, int LAYOUT, int NBMAX>
 __global__ void __launch_bounds__(kFusedThreads, 1)
     w4a16_gemv_fused_kernel(const __grid_constant__ FusedParams fp, const __grid_constant__ CUtensorMap tmA1,
                             const __grid_constant__ CUtensorMap tmS1, const __grid_constant__ CUtensorMap tmA2,
@@ -890,8 +890,8 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
 #define W4A16_FUSED_UNIT(NBV)                                                                                   \
   fused_unit<SCALE, DT, LAYOUT, NBV>(fp, smem, stage_bytes, full, empty, xfull, xempty, hdrs, abort_flag, red, \
                                      ring_len, grp, rowA, rowB, rb, lane, off, r7, ch, r, xj, fq, pend)
-      if (nb <= 1) ok = W4A16_FUSED_UNIT(1);
-      else if (nb == 2) ok = W4A16_FUSED_UNIT(2);
+      if (NBMAX == 1 || nb <= 1) ok = W4A16_FUSED_UNIT(1);
+      else if (NBMAX == 2 || nb == 2) ok = W4A16_FUSED_UNIT(2);
       else ok = W4A16_FUSED_UNIT(4);
 #undef W4A16_FUSED_UNIT
       if (!ok) break;
@@ -926,11 +926,11 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
   }
 }
 
-template <int SCALE, int DT, int LAYOUT>
+template <int SCALE, int DT, int LAYOUT, int NBMAX>
 cudaError_t launch_gemv_fused_one(const FusedParams& fp, const CUtensorMap& tmA1, const CUtensorMap& tmS1,
                                   const CUtensorMap& tmA2, const CUtensorMap& tmS2, int grid, int smem_bytes,
                                   cudaStream_t s, bool pdl) {
-  auto kern = w4a16_gemv_fused_kernel<SCALE, DT, LAYOUT>;
+  auto kern = w4a16_gemv_fused_kernel<SCALE, DT, LAYOUT, NBMAX>;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -958,9 +958,18 @@ template <int DT, int LAYOUT>
 cudaError_t launch_gemv_fused_dt(int scale_kind, const FusedParams& fp, const CUtensorMap& tmA1,
                                  const CUtensorMap& tmS1, const CUtensorMap& tmA2, const CUtensorMap& tmS2, int grid,
                                  int smem_bytes, cudaStream_t s, bool pdl) {
-  return scale_kind == SCALE_GROUP
-             ? launch_gemv_fused_one<SCALE_GROUP, DT, LAYOUT>(fp, tmA1, tmS1, tmA2, tmS2, grid, smem_bytes, s, pdl)
-             : launch_gemv_fused_one<SCALE_CHANNEL, DT, LAYOUT>(fp, tmA1, tmS1, tmA2, tmS2, grid, smem_bytes, s, pdl);
+  // one kernel per largest route block count of the plan's tiles (bn / 8): the
+  // 32-route code path costs registers that the 8-route one then lacks
+  // (measured: 3-5 % at 1 to 32 tokens on the Kimi shard with 8-route tiles)
+#define W4A16_FUSED_ONE(SC, NBM) \
+  launch_gemv_fused_one<SC, DT, LAYOUT, NBM>(fp, tmA1, tmS1, tmA2, tmS2, grid, smem_bytes, s, pdl)
+  const int bn = fp.up.bn;
+  if (scale_kind == SCALE_GROUP)
+    return bn <= 8 ? W4A16_FUSED_ONE(SCALE_GROUP, 1)
+                   : (bn <= 16 ? W4A16_FUSED_ONE(SCALE_GROUP, 2) : W4A16_FUSED_ONE(SCALE_GROUP, 4));
+  return bn <= 8 ? W4A16_FUSED_ONE(SCALE_CHANNEL, 1)
+                 : (bn <= 16 ? W4A16_FUSED_ONE(SCALE_CHANNEL, 2) : W4A16_FUSED_ONE(SCALE_CHANNEL, 4));
+#undef W4A16_FUSED_ONE
 }
 
 }  // namespace w4a16
