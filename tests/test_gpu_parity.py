@@ -269,6 +269,31 @@ def test_split_k_with_nan_poisoned_workspace(s1, s2, path):
         split_case(cfg, s1, s2, path)
 
 
+@pytest.mark.parametrize("act,inter", [(gen.ACT_SWIGLU, 512), (gen.ACT_RELU2, 1024)])
+def test_tensor_core_tail_pieces(monkeypatch, act, inter):
+    """More gate/up units than SMs (48 route tiles x 4 unit groups = 192 on
+    152 SMs): the 40 units of the last, partial wave are cut into 2 or 3 K
+    pieces (6 K blocks) whose partials the last piece to finish sums in piece
+    order.  On a NaN-poisoned workspace each setting matches the oracle and
+    repeats bit for bit."""
+    cfg = small_cfg(E=48, H=1536, I=inter, k=4, act=act, seed=23)
+    T = 96
+    w, x, ids, tw = case_on_gpu(cfg, T)
+    ref = oracle_rows(cfg, w, x, ids, tw)
+    for pieces in ("0", "2", "4"):
+        monkeypatch.setenv("W4A16_MOE_TAIL_PIECES", pieces)
+        moe = make_moe(cfg, T)
+        moe.set_gemm_path(PATHS["tc"])
+        moe.workspace.fill_(0xFF)
+        a = moe(x, w, tw, ids).clone()
+        b = moe(x, w, tw, ids)
+        torch.cuda.synchronize()
+        moe.check_device_error()
+        assert moe.read_route_layout(T)["num_tiles"] >= 40
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+        compare(a, ref, f"tail pieces {pieces} act {act}")
+
+
 def split_case(cfg, s1, s2, path):
     w, x, ids, tw = case_on_gpu(cfg, 9)
     moe = make_moe(cfg, 9)

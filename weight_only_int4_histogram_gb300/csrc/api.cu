@@ -38,6 +38,8 @@ struct w4a16_moe_plan_s {
   bool fused;        // CUDA-core path: both GEMMs in one launch
   bool finalize;     // fused launch: combine inside the down epilogue (no combine launch)
   int ov_chunk;      // tuning: down weight tiles per fused queue entry (0 = automatic)
+  int tail_max;      // tensor-core gate/up: K pieces per unit of the last partial wave (<= 1: none)
+  int ov_stages;     // tuning: tensor-core ring stages at most (0 = as many as fit)
   cudaEvent_t ev[4];
   bool has_ev;
 };
@@ -69,6 +71,7 @@ struct Layout {
   int down_chunk;   // fused: down weight tiles per queue entry
   int ctr_len;      // counters zeroed by route preparation
   bool fin;         // fused finalize in this forward
+  int tail;         // tensor-core gate/up: tail pieces per unit at most (0: none)
   int fix_len;      // fused: queue head + ready counts + split counters (reset after a forward)
   int T, R, bn, tiles_cap;
   int64_t slots_cap;
@@ -151,6 +154,15 @@ constexpr int kDoubleAccMaxKb = 8;
 // stages fit in shared memory, and units four times larger leave more of
 // the last wave idle).
 constexpr int kDefaultNT = 2;
+
+// Tensor-core gate/up GEMM: units of the last, partial wave are cut into at
+// most this many K pieces (summed by the last piece in piece order), so that
+// the wave's few units do not keep most SMs idle for a whole unit.  Measured
+// on the Kimi shard (768 units on 152 SMs): 1024 / 2048 tokens 427.7 / 504.5 us
+// uncut, 422.6 / 498.3 with 2 pieces, 422.5 / 501.3 with 4, 432.8 / 513.6 with
+// 8 -- the few units of a last wave run faster than a full wave's (they have
+// the memory system to themselves), so the gain is small.
+constexpr int kDefaultTailPieces = 2;
 
 int choose_bn(const w4a16_moe_plan_s& P, int T) {
   if (P.ov_bn) return P.ov_bn;
@@ -284,9 +296,11 @@ Layout make_layout(const w4a16_moe_plan_s& P, int T) {
               L.ntu2, L.acc2);
     L.stage_bytes = gemm_stage_bytes(L.ntu1, L.bn);
     L.stages = std::min(kMaxStages, smem_budget / L.stage_bytes);
+    if (P.ov_stages >= 2) L.stages = std::min(L.stages, P.ov_stages);
     L.smem = 3072 + L.stages * L.stage_bytes;
     L.stage_bytes2 = gemm_stage_bytes(L.ntu2, L.bn);
     L.stages2 = std::min(kMaxStages, (smem_budget - epi_bytes) / L.stage_bytes2);
+    if (P.ov_stages >= 2) L.stages2 = std::min(L.stages2, P.ov_stages);
     L.smem2 = 3072 + epi_bytes + L.stages2 * L.stage_bytes2;
   }
   const int64_t units1 = static_cast<int64_t>(L.tiles_cap) * cdiv(L.nt1, L.ntu1) * L.s1;
@@ -318,7 +332,10 @@ Layout make_layout(const w4a16_moe_plan_s& P, int T) {
   L.off_inv = take(sizeof(int32_t) * std::max(L.R, 1));
   L.off_ctr = take(sizeof(int32_t) * L.ctr_len);
   L.off_chist = take(sizeof(int32_t) * kRouteMaxCtas * E);
-  L.off_part = take(L.s1 > 1 ? sizeof(float) * L.s1 * L.slots_cap * L.n1 : 0);
+  // gate/up split-K partials, or the tail pieces' (at most one per CTA)
+  L.tail = (!L.gemv && L.s1 == 1 && P.tail_max > 1) ? P.tail_max : 0;
+  L.off_part = take(L.s1 > 1 ? sizeof(float) * L.s1 * L.slots_cap * L.n1
+                             : (L.tail ? sizeof(float) * L.grid1 * L.ntu1 * L.bn * 128 : 0));
   L.off_inter = take(static_cast<size_t>(act_bytes) * L.slots_cap * d.inter);
   // expert outputs: the activation dtype without down split-K, FP32 partials with it
   L.off_y = take((L.s2 == 1 ? static_cast<size_t>(act_bytes) : sizeof(float) * L.s2) * L.slots_cap * d.hidden);
@@ -707,6 +724,7 @@ w4a16_status launch_forward(const w4a16_moe_plan_s& P, const Layout& L, const vo
   g1.out = ws + L.off_inter;
   g1.part = reinterpret_cast<float*>(ws + L.off_part);
   g1.counters = reinterpret_cast<int32_t*>(ws + L.off_ctr);
+  g1.tail_max = L.tail;
   g1.scale_tma = stma1 ? 1 : 0;
   cudaError_t e;
   if (P.has_ev && (e = cudaEventRecord(P.ev[0], s)) != cudaSuccess) return cuda_fail(e, "event record");
@@ -845,10 +863,13 @@ w4a16_status w4a16_moe_plan(const w4a16_moe_desc* desc, w4a16_moe_plan_t* out, s
   P->fused = env_flag("W4A16_MOE_FUSED", true);
   P->finalize = env_flag("W4A16_MOE_FUSED_FINALIZE", false);
   if (const char* v = getenv("W4A16_MOE_DOWN_CHUNK")) P->ov_chunk = std::max(0, atoi(v));
+  P->tail_max = kDefaultTailPieces;
+  if (const char* v = getenv("W4A16_MOE_TAIL_PIECES")) P->tail_max = std::min(std::max(0, atoi(v)), 64);
   P->layout = W4A16_LAYOUT_CHECKPOINT;
   // tuning knobs for measurements: weight tiles per tensor-core unit of each GEMM
   if (const char* v = getenv("W4A16_MOE_NT_GATE_UP")) P->ov_nt1 = atoi(v);
   if (const char* v = getenv("W4A16_MOE_NT_DOWN")) P->ov_nt2 = atoi(v);
+  if (const char* v = getenv("W4A16_MOE_TC_STAGES")) P->ov_stages = atoi(v);
   if (P->ov_nt1 != 0 && P->ov_nt1 != 1 && P->ov_nt1 != 2 && P->ov_nt1 != 4) P->ov_nt1 = 0;
   if (P->ov_nt2 != 0 && P->ov_nt2 != 1 && P->ov_nt2 != 2 && P->ov_nt2 != 4) P->ov_nt2 = 0;
   P->wait_ns = kWaitTimeoutNs;

@@ -128,6 +128,8 @@ struct GemmParams {
   int32_t kb_total;        // K blocks of kBlockK
   int32_t splits;          // split-K factor
   int32_t kb_per_split;
+  int32_t tail_max;        // tensor-core gate/up without split-K: at most this many K pieces
+                           // for each unit of the last, partial wave (0 or 1: none)
   int32_t stages;
   int32_t top_k;
   int32_t stage_bytes;
@@ -140,7 +142,9 @@ struct GemmParams {
   int64_t slots_cap;
   void* out;               // gate/up: intermediate [slots_cap, I] act dtype
                            // down: FP32 partial outputs [splits, slots_cap, H]
-  float* part;             // gate/up split-K partials [splits, slots_cap, N1]
+  float* part;             // gate/up split-K partials [splits, slots_cap, N1]; with tail
+                           // pieces instead [pieces, NT, bn, 128] (piece-major, then tile,
+                           // route, TMEM lane)
   int32_t* counters;       // gate/up split-K arrival counters [tiles_cap * n_tiles]
   int32_t* err;
   int32_t tiles_cap;       // capacity of `tiles`

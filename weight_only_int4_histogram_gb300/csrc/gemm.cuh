@@ -122,6 +122,8 @@ struct KPacked {
 // weight tiles, K split), split fastest.
 struct Unit {
   int tile, grp, split, kb0, kb1;
+  int nsplit;  // K pieces of this unit (1: whole)
+  int tj;      // tail pieces: index of the unit among the tail units, else -1
 };
 
 __device__ __forceinline__ Unit decode_unit(const GemmParams& p, int u) {
@@ -132,6 +134,8 @@ __device__ __forceinline__ Unit decode_unit(const GemmParams& p, int u) {
   w.tile = r / p.n_groups;
   w.kb0 = w.split * p.kb_per_split;
   w.kb1 = min(w.kb0 + p.kb_per_split, p.kb_total);
+  w.nsplit = p.splits;
+  w.tj = -1;
   return w;
 }
 
@@ -140,6 +144,58 @@ __device__ __forceinline__ Unit decode_unit(const GemmParams& p, int u) {
 // tile count is known (speculatively, to overlap its latency).
 __device__ __forceinline__ int4 load_tile(const GemmParams& p, int u) {
   return p.tiles[u / (p.splits * p.n_groups)];
+}
+
+// The CTAs take units round robin, so with U units on G CTAs the last wave
+// holds U mod G of them and leaves the other SMs idle for a whole unit.  Tail
+// pieces (gate/up without split-K only): the first G * floor(U / G) units stay
+// whole; each unit of the partial last wave is cut into S K pieces (at most
+// tail_max, at most G / (U mod G), every piece owning K blocks), whose partial
+// sums the last piece to finish adds up in piece order.
+struct UnitMap {
+  int main;   // whole units [0, main)
+  int S;      // pieces per later unit (1: no tail pieces)
+  int kbps;   // K blocks per piece
+  int total;  // unit indices
+};
+
+template <int WHICH>
+__device__ __forceinline__ UnitMap make_unit_map(const GemmParams& p, int n_tiles_rt) {
+  const int base = n_tiles_rt * p.n_groups * p.splits;
+  UnitMap m{base, 1, p.kb_per_split, base};
+  const int G = static_cast<int>(gridDim.x);
+  if (WHICH == GEMM_UP && p.splits == 1 && p.tail_max > 1) {
+    const int W = base / G, r = base - W * G;
+    if (W >= 1 && r > 0) {
+      int S = min(min(p.tail_max, p.kb_total), G / r);
+      if (S >= 2) {
+        const int kbps = (p.kb_total + S - 1) / S;
+        S = (p.kb_total + kbps - 1) / kbps;
+        m = UnitMap{W * G, S, kbps, W * G + r * S};
+      }
+    }
+  }
+  return m;
+}
+
+__device__ __forceinline__ Unit decode_unit(const GemmParams& p, const UnitMap& m, int u) {
+  if (u < m.main || m.S == 1) return decode_unit(p, u);
+  const int v = u - m.main;
+  const int b = m.main + v / m.S;  // the whole-unit index (p.splits == 1)
+  Unit w;
+  w.split = v % m.S;
+  w.grp = b % p.n_groups;
+  w.tile = b / p.n_groups;
+  w.kb0 = w.split * m.kbps;
+  w.kb1 = min(w.kb0 + m.kbps, p.kb_total);
+  w.nsplit = m.S;
+  w.tj = b - m.main;
+  return w;
+}
+
+__device__ __forceinline__ int4 load_tile(const GemmParams& p, const UnitMap& m, int u) {
+  if (u < m.main || m.S == 1) return load_tile(p, u);
+  return p.tiles[(m.main + (u - m.main) / m.S) / p.n_groups];
 }
 
 // Row (within the expert) of the weight rows held in tile rows 0..63 / 64..127.
@@ -391,8 +447,10 @@ __global__ void __launch_bounds__(WHICH == GEMM_DOWN ? kGemmThreadsDown : kGemmT
   pdl_launch_dependents();
 
   // The first unit's tile record is fetched together with the tile count.
+  // (blockIdx.x < gridDim.x <= the whole units whenever there are tail pieces)
   const int4 first_ti = load_tile(p, blockIdx.x);
-  const int n_units = (*p.num_tiles) * p.n_groups * p.splits;
+  const UnitMap um = make_unit_map<WHICH>(p, *p.num_tiles);
+  const int n_units = um.total;
   const int N1 = p.n_rows;
 
   if (warp == 0) {
@@ -408,9 +466,9 @@ __global__ void __launch_bounds__(WHICH == GEMM_DOWN ? kGemmThreadsDown : kGemmT
     bool ok = true;
     int4 ti_next = first_ti;
     for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-      const Unit w = decode_unit(p, u);
+      const Unit w = decode_unit(p, um, u);
       const int4 ti = ti_next;
-      if (u + (int)gridDim.x < n_units) ti_next = load_tile(p, u + gridDim.x);  // prefetch
+      if (u + (int)gridDim.x < n_units) ti_next = load_tile(p, um, u + gridDim.x);  // prefetch
       if (w.kb1 <= w.kb0) continue;
       const int e = ti.x, m0 = ti.y;
       const int nvalid = min(NT, p.n_tiles - w.grp * NT);  // weight tiles of this unit
@@ -515,9 +573,9 @@ __global__ void __launch_bounds__(WHICH == GEMM_DOWN ? kGemmThreadsDown : kGemmT
     bool ok = true;
     int4 ti_next = first_ti;
     for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-      const Unit w = decode_unit(p, u);
+      const Unit w = decode_unit(p, um, u);
       const int4 ti = ti_next;
-      if (u + (int)gridDim.x < n_units) ti_next = load_tile(p, u + gridDim.x);
+      if (u + (int)gridDim.x < n_units) ti_next = load_tile(p, um, u + gridDim.x);
       if (w.kb1 <= w.kb0) continue;
       const uint32_t idesc = idesc0 | (static_cast<uint32_t>(mma_n_of(ti.z, bn) >> 3) << 17);
       const int nvalid = min(NT, p.n_tiles - w.grp * NT);
@@ -595,9 +653,9 @@ __global__ void __launch_bounds__(WHICH == GEMM_DOWN ? kGemmThreadsDown : kGemmT
       bool ok = true;
       int4 ti_next = first_ti;
       for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-        const Unit w = decode_unit(p, u);
+        const Unit w = decode_unit(p, um, u);
         const int4 ti = ti_next;
-        if (u + (int)gridDim.x < n_units) ti_next = load_tile(p, u + gridDim.x);
+        if (u + (int)gridDim.x < n_units) ti_next = load_tile(p, um, u + gridDim.x);
         if (w.kb1 <= w.kb0) continue;
         const int m0 = ti.y;
         const int rows = min(ti.z, bn);
@@ -647,7 +705,7 @@ __global__ void __launch_bounds__(WHICH == GEMM_DOWN ? kGemmThreadsDown : kGemmT
     int st = 0, a_st = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-      const Unit w = decode_unit(p, u);
+      const Unit w = decode_unit(p, um, u);
       if (w.kb1 <= w.kb0) continue;
       const bool tile_ok = w.grp * NT + t < p.n_tiles;  // uniform over the warpgroup
       for (int kb = w.kb0; kb < w.kb1 && ok; ++kb, ring_next(st, ph, stages)) {
@@ -699,10 +757,10 @@ __global__ void __launch_bounds__(WHICH == GEMM_DOWN ? kGemmThreadsDown : kGemmT
     };
     int4 ti_next = first_ti;
     for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-      const Unit w = decode_unit(p, u);
+      const Unit w = decode_unit(p, um, u);
       const bool has_k = w.kb1 > w.kb0;
       const int4 ti = ti_next;
-      if (u + (int)gridDim.x < n_units) ti_next = load_tile(p, u + gridDim.x);  // prefetch
+      if (u + (int)gridDim.x < n_units) ti_next = load_tile(p, um, u + gridDim.x);  // prefetch
       const int e = ti.x, m0 = ti.y, rows = ti.z;
       const int nvalid = min(NT, p.n_tiles - w.grp * NT);
       const int b = acc_bufs == 2 ? (jc & 1) : 0;
@@ -773,6 +831,15 @@ __global__ void __launch_bounds__(WHICH == GEMM_DOWN ? kGemmThreadsDown : kGemmT
               bulk_commit();
             }
             sbuf ^= 1;
+          } else if (w.tj >= 0) {
+            // tail piece: [piece][tile][route][TMEM lane], whole rows of 128 lanes
+            float* part = p.part + ((static_cast<int64_t>(w.tj) * w.nsplit + w.split) * NT + t) * (p.bn * 128) +
+                          q * 32 + lane;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const int r = c0 + j;
+              if (r < rows) part[r * 128] = v[j];
+            }
           } else if (p.splits > 1) {
             float* part = p.part + (static_cast<int64_t>(w.split) * p.slots_cap + m0) * N1 + grow;
 #pragma unroll
@@ -799,7 +866,7 @@ __global__ void __launch_bounds__(WHICH == GEMM_DOWN ? kGemmThreadsDown : kGemmT
             }
           }
         }
-        if (WHICH == GEMM_UP && p.splits > 1) {
+        if (WHICH == GEMM_UP && w.nsplit > 1) {
           // Split-K fix-up: the last split to finish sums all partials in split
           // order (deterministic) and applies the activation.
           __threadfence();
@@ -809,7 +876,7 @@ __global__ void __launch_bounds__(WHICH == GEMM_DOWN ? kGemmThreadsDown : kGemmT
           }
           if (epi_tid == 0) {
             const int prev = atomicAdd(&p.counters[w.tile * p.n_tiles + nt], 1);
-            *fixup_flag = (prev == p.splits - 1) ? 1 : 0;
+            *fixup_flag = (prev == w.nsplit - 1) ? 1 : 0;
           }
           if (!epi_sync()) {
             ok = false;
@@ -818,15 +885,36 @@ __global__ void __launch_bounds__(WHICH == GEMM_DOWN ? kGemmThreadsDown : kGemmT
           if (*fixup_flag) {
             __threadfence();
             uint16_t* inter = reinterpret_cast<uint16_t*>(p.out) + static_cast<int64_t>(m0) * p.inter;
-            for (int c0 = 0; c0 < rows; c0 += 16) {
+            // partials of route r, split s: src + s * sstride + r * rstride
+            const float* src;
+            int64_t sstride, rstride;
+            if (w.tj >= 0) {
+              src = p.part + (static_cast<int64_t>(w.tj) * w.nsplit * NT + t) * (p.bn * 128) + q * 32 + lane;
+              sstride = static_cast<int64_t>(NT) * p.bn * 128;
+              rstride = 128;
+            } else {
+              src = p.part + static_cast<int64_t>(m0) * N1 + grow;
+              sstride = static_cast<int64_t>(p.slots_cap) * N1;
+              rstride = N1;
+            }
+            const bool lane_ok = w.tj >= 0 || row_ok;
+            for (int c0 = 0; c0 < rows; c0 += 8) {
+              // 8 routes' loads in flight per split, splits summed in order
+              float acc[8];
 #pragma unroll
-              for (int j = 0; j < 16; ++j) {
+              for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
+              for (int s = 0; s < w.nsplit; ++s) {
+                float ld[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                  ld[j] = (c0 + j < rows && lane_ok) ? __ldcg(src + s * sstride + (c0 + j) * rstride) : 0.0f;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) acc[j] += ld[j];
+              }
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
                 const int r = c0 + j;
-                float hs = 0.0f;
-                if (r < rows && row_ok) {
-                  const float* src = p.part + static_cast<int64_t>(m0 + r) * N1 + grow;
-                  for (int s = 0; s < p.splits; ++s) hs += __ldcg(src + static_cast<int64_t>(s) * p.slots_cap * N1);
-                }
+                const float hs = acc[j];
                 if (swiglu) {
                   const float other = __shfl_xor_sync(0xFFFFFFFFu, hs, 16);
                   if ((j & 1) == (lane >> 4) && r < rows && row_ok) {
