@@ -758,14 +758,21 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     } else {
       produce(std::integral_constant<bool, false>());
     }
-  } else if (warp == 1) {
+  } else if (warp == 1 || (NBMAX > 1 && warp == kFinWarp && !fp.finalize)) {
     // ------------------------------------------------------------------ activation rows
+    // With route tiles of more than 8 routes two copy warps take the stages
+    // of even and odd sequence number (one warp's per-stage copies, slowed by
+    // the compute warps beside it on its scheduler, would pace the ring:
+    // Kimi shard, 256 tokens, 16-route tiles 312 -> 297 us; with 8-route
+    // tiles one warp is as fast).  The fused finalize keeps its warp busy.
+    const int cstride = NBMAX > 1 && !fp.finalize ? 2 : 1;
+    const int cfirst = warp == 1 ? 0 : 1;
     const int need = 8 * pu.n_tiles;  // published row blocks of a finished route tile
-    int slot = 0, ends = 0;
-    uint32_t ph = 0, done = 0;
+    int slot = cfirst, ends = 0;
+    uint32_t ph = 0, done = static_cast<uint32_t>(cfirst);
     bool ok = true;
     int src_type = -1, src_m = -1, src = 0, ready_m = -1;
-    while (ends < 2) {
+    while (ends < 2 / cstride) {
       if (!warp_wait(&hdrb[slot], ph, abort_flag, pu.err, pu.wait_ns)) {
         ok = false;
         break;
@@ -829,14 +836,15 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
         }
         cp_async_mbar_arrive_noinc(&full[slot]);
       }
-      ++done;
-      if (++slot == ring_len) {
-        slot = 0;
+      done += cstride;
+      slot += cstride;
+      if (slot >= ring_len) {
+        slot -= ring_len;
         ph ^= 1u;
       }
     }
-    // After an abort: the arrivals owed to stages the producer issued beyond
-    // this warp's last one (see gemv.cuh).
+    // After an abort: the arrivals owed to this warp's stages that the
+    // producer issued beyond its last one (see gemv.cuh).
     if (!ok && lane == 0) {
       const uint64_t t0 = global_timer_ns();
       while (!*prod_stopped && global_timer_ns() - t0 < kWaitTimeoutNs) {
@@ -844,7 +852,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
       if (*prod_stopped) {
         __threadfence_block();
         const uint32_t to = static_cast<uint32_t>(*prod_issued);
-        for (uint32_t j = done; j < to; ++j) mbar_arrive_cnt(&full[j % ring_len], 32);
+        for (uint32_t j = done; j < to; j += cstride) mbar_arrive_cnt(&full[j % ring_len], 32);
       }
     }
     asm volatile("cp.async.wait_all;" ::: "memory");
