@@ -92,12 +92,20 @@ static_assert(kFzOffFinCtl + 16 <= kGemvCtrlBytes, "finalize queue");
 constexpr int kFusedThreads = 32 * (2 + kGemvComputeWarps + 1);
 constexpr int kFinWarp = 2 + kGemvComputeWarps;
 
+// The queue's parts at fixed offsets of the control block (one base pointer:
+// every compute warp carries it, and registers are scarce there).
 struct FinQueue {
-  int4* rec;              // (first slot, routes, first output column, 0)
-  volatile int* flag;     // record i is ready when flag[i % kFinQ] == i + 1
-  int* tail;              // records allocated (shared-memory atomic)
-  volatile int* head;     // records consumed by the finalize warp
-  int* done;              // compute warps finished
+  uint8_t* c;  // the control block
+  // records (first slot, routes, first output column, 0)
+  __device__ __forceinline__ int4* rec() const { return reinterpret_cast<int4*>(c + kFzOffFinRec); }
+  // record i is ready when flag[i % kFinQ] == i + 1
+  __device__ __forceinline__ volatile int* flag() const { return reinterpret_cast<volatile int*>(c + kFzOffFinFlag); }
+  // records allocated (shared-memory atomic)
+  __device__ __forceinline__ int* tail() const { return reinterpret_cast<int*>(c + kFzOffFinCtl); }
+  // records consumed by the finalize warp
+  __device__ __forceinline__ volatile int* head() const { return reinterpret_cast<volatile int*>(c + kFzOffFinCtl + 4); }
+  // compute warps finished
+  __device__ __forceinline__ int* done() const { return reinterpret_cast<int*>(c + kFzOffFinCtl + 8); }
 };
 
 // A compute warp's last down unit, published one unit later (its fence then
@@ -301,9 +309,9 @@ __device__ __forceinline__ bool fin_publish(const FusedParams& fp, const FinQueu
   __syncwarp();
   int ok = 1;
   if (lane == 0) {
-    const int i = atomicAdd(fq.tail, 1);
+    const int i = atomicAdd(fq.tail(), 1);
     const uint64_t t0 = global_timer_ns();
-    while (i - *fq.head >= kFinQ) {
+    while (i - *fq.head() >= kFinQ) {
       if (*abort_flag) {
         ok = 0;
         break;
@@ -317,9 +325,9 @@ __device__ __forceinline__ bool fin_publish(const FusedParams& fp, const FinQueu
       __nanosleep(64);
     }
     if (ok) {
-      fq.rec[i % kFinQ] = make_int4(pend.m0, pend.rows, pend.c0, 0);
+      fq.rec()[i % kFinQ] = make_int4(pend.m0, pend.rows, pend.c0, 0);
       __threadfence_block();
-      fq.flag[i % kFinQ] = i + 1;
+      fq.flag()[i % kFinQ] = i + 1;
     }
   }
   pend.valid = false;
@@ -339,11 +347,11 @@ __device__ __forceinline__ void fin_warp(const FusedParams& fp, const FinQueue& 
   uint64_t last_progress = t0;
   for (;;) {
     const int idx = head + lane;
-    const bool rdy = fq.flag[idx % kFinQ] == idx + 1;
+    const bool rdy = fq.flag()[idx % kFinQ] == idx + 1;
     const unsigned m = __ballot_sync(0xFFFFFFFFu, rdy);
     const int n = (m == 0xFFFFFFFFu) ? 32 : __ffs(~m) - 1;  // ready records in order
     if (n == 0) {
-      if (*fq.done == kGemvComputeWarps && *reinterpret_cast<volatile int*>(fq.tail) == head) break;
+      if (*fq.done() == kGemvComputeWarps && *reinterpret_cast<volatile int*>(fq.tail()) == head) break;
       if (*abort_flag) break;
       if (global_timer_ns() - last_progress > fp.up.wait_ns) {
         if (lane == 0) {
@@ -356,7 +364,7 @@ __device__ __forceinline__ void fin_warp(const FusedParams& fp, const FinQueue& 
       continue;
     }
     __threadfence_block();
-    const int4 rec = lane < n ? fq.rec[idx % kFinQ] : make_int4(0, 0, 0, 0);
+    const int4 rec = lane < n ? fq.rec()[idx % kFinQ] : make_int4(0, 0, 0, 0);
     // records whose routes fit in this pass (every record holds <= 32 routes)
     int incl = rec.y;
 #pragma unroll
@@ -392,7 +400,7 @@ __device__ __forceinline__ void fin_warp(const FusedParams& fp, const FinQueue& 
     if (fin_t >= 0) finalize_block<DT>(fp, fin_t, c0);
     head += taken;
     __syncwarp();
-    if (lane == 0) *fq.head = head;
+    if (lane == 0) *fq.head() = head;
     last_progress = global_timer_ns();
   }
 }
@@ -533,12 +541,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
   volatile int* prod_issued = abort_flag + 1;
   volatile int* prod_stopped = abort_flag + 2;
   StageHdr* hdrs = reinterpret_cast<StageHdr*>(ctrl + kFzOffHdr);
-  FinQueue fq;
-  fq.rec = reinterpret_cast<int4*>(ctrl + kFzOffFinRec);
-  fq.flag = reinterpret_cast<volatile int*>(ctrl + kFzOffFinFlag);
-  fq.tail = reinterpret_cast<int*>(ctrl + kFzOffFinCtl);
-  fq.head = reinterpret_cast<volatile int*>(ctrl + kFzOffFinCtl + 4);
-  fq.done = reinterpret_cast<int*>(ctrl + kFzOffFinCtl + 8);
+  const FinQueue fq{ctrl};
   float* red = reinterpret_cast<float*>(ctrl + kGemvCtrlBytes);
 
   const int warp = threadIdx.x >> 5;
@@ -556,10 +559,10 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     }
     *abort_flag = 0;
     *prod_stopped = 0;
-    *fq.tail = 0;
-    *fq.head = 0;
-    *fq.done = 0;
-    for (int i = 0; i < kFinQ; ++i) fq.flag[i] = 0;
+    *fq.tail() = 0;
+    *fq.head() = 0;
+    *fq.done() = 0;
+    for (int i = 0; i < kFinQ; ++i) fq.flag()[i] = 0;
     fence_barrier_init();
   }
   if (warp == 0 && lane == 0) {
@@ -875,10 +878,6 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
       r7 = ld_row & 7;
       ch = ld_j >> 1;
     };
-    uint32_t off_up, off_dn;
-    int r7_up, r7_dn, ch_up, ch_dn;
-    ld_off(rowA_up, rowB_up, off_up, r7_up, ch_up);
-    ld_off(rowA_dn, rowB_dn, off_dn, r7_dn, ch_dn);
     GroupRing r;
     r.slot = grp;
     r.ph = 0;
@@ -892,8 +891,10 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
       const int nb = (min(hdrs[r.slot].rows, kGemvMaxR) + 7) >> 3;
       const bool up = type == kItemUp;
       const int rowA = up ? rowA_up : rowA_dn, rowB = up ? rowB_up : rowB_dn;
-      const uint32_t off = up ? off_up : off_dn;
-      const int r7 = up ? r7_up : r7_dn, ch = up ? ch_up : ch_dn;
+      // this lane's ldmatrix row (recomputed per unit: registers are scarce)
+      uint32_t off;
+      int r7, ch;
+      ld_off(rowA, rowB, off, r7, ch);
       bool ok;
 #define W4A16_FUSED_UNIT(NBV)                                                                                   \
   fused_unit<SCALE, DT, LAYOUT, NBV>(fp, smem, stage_bytes, full, empty, xfull, xempty, hdrs, abort_flag, red, \
@@ -910,7 +911,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
       __syncwarp();
       if (lane == 0) {
         __threadfence_block();
-        atomicAdd(fq.done, 1);
+        atomicAdd(fq.done(), 1);
       }
     }
   } else {
