@@ -257,6 +257,12 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
       : "memory");
 }
 
+// Transaction bytes counted as arrived without a copy (abort paths: bytes
+// of copies that will never be issued).
+__device__ __forceinline__ void mbar_complete_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.complete_tx.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+
 // `count` arrivals at once.
 __device__ __forceinline__ void mbar_arrive_cnt(uint64_t* bar, uint32_t count) {
   asm volatile(

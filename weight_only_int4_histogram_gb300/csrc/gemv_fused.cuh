@@ -546,6 +546,11 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  // Two activation warps (even / odd stages) unless the finalize warp is
+  // busy; they also issue the group-scale TMA of their stages when both GEMMs
+  // load scales by TMA (the producer then issues one TMA per stage).
+  const bool two_copy = !fp.finalize;
+  const bool scale_by_copier = two_copy && SCALE == SCALE_GROUP && fp.up.scale_tma && fp.down.scale_tma;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < ring_len; ++s) {
@@ -618,35 +623,46 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     bool ok = true;
     int q_lane0 = 0;
     if (lane == 0) q_lane0 = atomicAdd(fp.queue, 1);
-    // issue one stage: header, scales, weights
-    auto issue = [&](const GemmParams& g, const CUtensorMap& tmA, const CUtensorMap& tmS, int type, int m,
-                     const int4& ti, int nt, int kb, int split, uint32_t first, uint32_t last) -> bool {
+    // Per-GEMM constants as scalars (a reference chosen at run time between
+    // the two parameter blocks would be read through memory at every stage).
+    const int n_up = pu.n_rows, n_dn = pd.n_rows, inter = pu.inter;
+    const int k_up = pu.K, k_dn = pd.K;
+    const bool stma_up = SCALE == SCALE_GROUP && pu.scale_tma, stma_dn = SCALE == SCALE_GROUP && pd.scale_tma;
+    const uint16_t* const sc_up = pu.scales;
+    const uint16_t* const sc_dn = pd.scales;
+    // Issue one stage: header, scales, weights.  One call site, so that the
+    // ring state stays in registers.
+    auto issue = [&](bool upq, int m, const int4& ti, int nt, int kb, int split, uint32_t first,
+                     uint32_t last) -> bool {
       if (!wwait(&empty[slot], ph ^ 1u)) return false;
       uint8_t* sA = smem + slot * stage_bytes;
       uint8_t* sS = sA + kGvOffS;
       const int e = ti.x;
-      const int N = g.n_rows;
-      int r0, r1;
-      if (type == kItemUp) tile_row_bases<GEMM_UP>(g, nt, r0, r1);
-      else tile_row_bases<GEMM_DOWN>(g, nt, r0, r1);
-      const bool stma = SCALE == SCALE_GROUP && g.scale_tma;
+      const int N = upq ? n_up : n_dn;
+      // tile rows 0..63 / 64..127: SwiGLU gate rows and their up rows, else consecutive rows
+      const int r0 = (upq && gated_up) ? 64 * nt : 128 * nt;
+      const int r1 = (upq && gated_up) ? inter + 64 * nt : r0 + 64;
+      const CUtensorMap* tmA = upq ? &tmA1 : &tmA2;
+      const CUtensorMap* tmS = upq ? &tmS1 : &tmS2;
+      const bool stma = upq ? stma_up : stma_dn;
+      const bool stma_here = stma && !scale_by_copier;  // else the stage's activation warp issues it
       if (!kSolo && SCALE == SCALE_GROUP && !stma) {
-        const int groups_row = g.K / kGroup;
+        const int groups_row = (upq ? k_up : k_dn) / kGroup;
         const int g0 = kb * (kGemvBlockK / kGroup);
         const int ng = min(kGemvBlockK / kGroup, groups_row - g0);
+        const uint8_t* sbase = reinterpret_cast<const uint8_t*>(upq ? sc_up : sc_dn);
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           const int tr = lane + 32 * j;
           const int grow = tr < 64 ? r0 + tr : r1 + (tr - 64);
-          const uint8_t* src = reinterpret_cast<const uint8_t*>(g.scales) +
-                               (static_cast<int64_t>(e) * N + grow) * (groups_row * 2) + g0 * 2;
+          const uint8_t* src = sbase + (static_cast<int64_t>(e) * N + grow) * (groups_row * 2) + g0 * 2;
           copy_scale_piece(sS + tr * kGvScaleRowBytes, src, grow < N ? max(ng, 0) * 2 : 0);
         }
         cp_async_mbar_arrive(&full[slot]);
       }
       if (lane == 0) {
         StageHdr& h = hdrs[slot];
-        h.type = type;
+        h.type = upq ? kItemUp : kItemDown;
         h.m = m;
         h.nt = nt;
         h.kb = kb;
@@ -665,30 +681,30 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
           // one box per tile: the weight rows (and their group scales) of the
           // whole 128-row tile -- a 5D view pairs a gated tile's gate and up
           // halves, otherwise the tile's rows are consecutive
-          if (type == kItemUp && gated_up) {
+          if (upq && gated_up) {
             if (gate5d) {
-              tma_load_5d(sA, &tmA, &full[slot], kb * (kGemvBlockK / 2), 0, nt, 0, e, pol_w);
-              if (stma) tma_load_5d(sS, &tmS, &full[slot], kb * (kGemvBlockK / kGroup), 0, nt, 0, e, pol_s);
+              tma_load_5d(sA, tmA, &full[slot], kb * (kGemvBlockK / 2), 0, nt, 0, e, pol_w);
+              if (stma_here) tma_load_5d(sS, tmS, &full[slot], kb * (kGemvBlockK / kGroup), 0, nt, 0, e, pol_s);
             } else {
               // inter an odd multiple of 32: 64-row boxes of the gate and up halves
-              tma_load_3d(sA, &tmA, &full[slot], kb * (kGemvBlockK / 2), r0, e, pol_w);
-              tma_load_3d(sA + 8192, &tmA, &full[slot], kb * (kGemvBlockK / 2), r1, e, pol_w);
-              if (stma) {
-                tma_load_3d(sS, &tmS, &full[slot], kb * (kGemvBlockK / kGroup), r0, e, pol_s);
-                tma_load_3d(sS + 64 * kGvScaleRowBytes, &tmS, &full[slot], kb * (kGemvBlockK / kGroup), r1, e,
+              tma_load_3d(sA, tmA, &full[slot], kb * (kGemvBlockK / 2), r0, e, pol_w);
+              tma_load_3d(sA + 8192, tmA, &full[slot], kb * (kGemvBlockK / 2), r1, e, pol_w);
+              if (stma_here) {
+                tma_load_3d(sS, tmS, &full[slot], kb * (kGemvBlockK / kGroup), r0, e, pol_s);
+                tma_load_3d(sS + 64 * kGvScaleRowBytes, tmS, &full[slot], kb * (kGemvBlockK / kGroup), r1, e,
                             pol_s);
               }
             }
           } else {
-            tma_load_3d(sA, &tmA, &full[slot], kb * (kGemvBlockK / 2), r0, e, pol_w);
-            if (stma) tma_load_3d(sS, &tmS, &full[slot], kb * (kGemvBlockK / kGroup), r0, e, pol_s);
+            tma_load_3d(sA, tmA, &full[slot], kb * (kGemvBlockK / 2), r0, e, pol_w);
+            if (stma_here) tma_load_3d(sS, tmS, &full[slot], kb * (kGemvBlockK / kGroup), r0, e, pol_s);
           }
         } else {
 #pragma unroll
           for (int b = 0; b < 2; ++b)
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh)
-              tma_load_3d(sA + (b * 2 + hh) * 4096, &tmA, &full[slot], kb * kGemvBlockK + hh * 128,
+              tma_load_3d(sA + (b * 2 + hh) * 4096, tmA, &full[slot], kb * kGemvBlockK + hh * 128,
                           (b ? r1 : r0) / 2, e, pol_w);
         }
       }
@@ -704,26 +720,31 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
       const int q = kSolo ? q_lane0 : __shfl_sync(0xFFFFFFFFu, q_lane0, 0);
       if (q >= qt) break;
       if (lane == 0) q_lane0 = atomicAdd(fp.queue, 1);  // the next entry, taken while this one streams
-      if (q < q1) {
-        const int m = q / (nt1 * s1);
+      // entry -> route tile m, weight tiles [ntb, nte), K blocks [kb0, kb1) of each
+      const bool upq = q < q1;
+      int m, ntb, nte, kb0, kb1, split;
+      if (upq) {
+        m = q / (nt1 * s1);
         const int rem = q - m * (nt1 * s1);
-        const int nt = rem / s1, split = rem - nt * s1;
-        const int4 ti = pu.tiles[m];
-        const int kb0 = split * pu.kb_per_split;
-        const int kb1 = min(kb0 + pu.kb_per_split, pu.kb_total);
-        const uint32_t first = seq, last = seq + static_cast<uint32_t>(kb1 - kb0) - 1u;
-        for (int kb = kb0; kb < kb1 && ok; ++kb) ok = issue(pu, tmA1, tmS1, kItemUp, m, ti, nt, kb, split, first, last);
+        ntb = rem / s1;
+        nte = ntb + 1;
+        split = rem - ntb * s1;
+        kb0 = split * pu.kb_per_split;
+        kb1 = min(kb0 + pu.kb_per_split, pu.kb_total);
       } else {
         const int qq = q - q1;
-        const int m = qq / nch;
+        m = qq / nch;
         const int c = qq - m * nch;
-        const int4 ti = pd.tiles[m];
-        const int ntb = c * fp.down_chunk, nte = min(ntb + fp.down_chunk, nt2);
-        for (int nt = ntb; nt < nte && ok; ++nt) {
-          const uint32_t first = seq, last = seq + static_cast<uint32_t>(pd.kb_total) - 1u;
-          for (int kb = 0; kb < pd.kb_total && ok; ++kb)
-            ok = issue(pd, tmA2, tmS2, kItemDown, m, ti, nt, kb, 0, first, last);
-        }
+        ntb = c * fp.down_chunk;
+        nte = min(ntb + fp.down_chunk, nt2);
+        split = 0;
+        kb0 = 0;
+        kb1 = pd.kb_total;
+      }
+      const int4 ti = upq ? pu.tiles[m] : pd.tiles[m];
+      for (int nt = ntb; nt < nte && ok; ++nt) {
+        const uint32_t first = seq, last = seq + static_cast<uint32_t>(kb1 - kb0) - 1u;
+        for (int kb = kb0; kb < kb1 && ok; ++kb) ok = issue(upq, m, ti, nt, kb, split, first, last);
       }
     }
     // two end markers, one for each compute group
@@ -761,15 +782,18 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     } else {
       produce(std::integral_constant<bool, false>());
     }
-  } else if (warp == 1 || (NBMAX > 1 && warp == kFinWarp && !fp.finalize)) {
+  } else if (warp == 1 || (warp == kFinWarp && two_copy)) {
     // ------------------------------------------------------------------ activation rows
-    // With route tiles of more than 8 routes two copy warps take the stages
-    // of even and odd sequence number (one warp's per-stage copies, slowed by
-    // the compute warps beside it on its scheduler, would pace the ring:
-    // Kimi shard, 256 tokens, 16-route tiles 312 -> 297 us; with 8-route
-    // tiles one warp is as fast).  The fused finalize keeps its warp busy.
-    const int cstride = NBMAX > 1 && !fp.finalize ? 2 : 1;
+    // Two copy warps take the stages of even and odd sequence number: one
+    // warp's per-stage work, slowed by the compute warps beside it on its
+    // scheduler, would pace the ring together with the producer's.  The
+    // fused finalize keeps its warp busy.
+    const int cstride = two_copy ? 2 : 1;
+    const uint64_t pol_s = l2_policy_evict_last();
+    const bool gated_up = pu.act == ACT_SWIGLU;
+    const bool gate5d = gated_up && (pu.inter % 64) == 0;
     const int cfirst = warp == 1 ? 0 : 1;
+    uint32_t scale_done = static_cast<uint32_t>(cfirst);  // stages below this had their scale TMA issued
     const int need = 8 * pu.n_tiles;  // published row blocks of a finished route tile
     int slot = cfirst, ends = 0;
     uint32_t ph = 0, done = static_cast<uint32_t>(cfirst);
@@ -786,6 +810,27 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
         ++ends;
       } else {
         const bool up = h.type == kItemUp;
+        if (scale_by_copier) {
+          // the stage's group scales (the producer's expect-tx counts them)
+          if (lane == 0) {
+            uint8_t* sS = smem + slot * stage_bytes + kGvOffS;
+            const int c0 = h.kb * (kGemvBlockK / kGroup);
+            if (up && gate5d) {
+              tma_load_5d(sS, &tmS1, &full[slot], c0, 0, h.nt, 0, h.e, pol_s);
+            } else if (up && gated_up) {
+              int r0, r1;
+              tile_row_bases<GEMM_UP>(pu, h.nt, r0, r1);
+              tma_load_3d(sS, &tmS1, &full[slot], c0, r0, h.e, pol_s);
+              tma_load_3d(sS + 64 * kGvScaleRowBytes, &tmS1, &full[slot], c0, r1, h.e, pol_s);
+            } else {
+              int r0, r1;
+              if (up) tile_row_bases<GEMM_UP>(pu, h.nt, r0, r1);
+              else tile_row_bases<GEMM_DOWN>(fp.down, h.nt, r0, r1);
+              tma_load_3d(sS, up ? &tmS1 : &tmS2, &full[slot], c0, r0, h.e, pol_s);
+            }
+          }
+          scale_done = done + cstride;
+        }
         const GemmParams& g = up ? fp.up : fp.down;
         const int rows = min(h.rows, kGemvMaxR);
         if (!up && h.m != ready_m) {
@@ -855,7 +900,13 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
       if (*prod_stopped) {
         __threadfence_block();
         const uint32_t to = static_cast<uint32_t>(*prod_issued);
-        for (uint32_t j = done; j < to; j += cstride) mbar_arrive_cnt(&full[j % ring_len], 32);
+        for (uint32_t j = done; j < to; j += cstride) {
+          mbar_arrive_cnt(&full[j % ring_len], 32);
+          // scale bytes the producer counted but this warp never loaded (the
+          // slot still holds stage j's header: its reuse needs this arrival)
+          if (scale_by_copier && j >= scale_done && hdrs[j % ring_len].type != kItemEnd)
+            mbar_complete_tx(&full[j % ring_len], kTileRows * kGvScaleRowBytes);
+        }
       }
     }
     asm volatile("cp.async.wait_all;" ::: "memory");
