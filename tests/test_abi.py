@@ -161,10 +161,10 @@ def test_gemm_path_choice_and_validation(lib):
     tensor cores; forced paths hold at every batch size."""
     plan, _ = _lib.w4a16_moe_plan(good_desc(num_experts=384, hidden=7168, inter=256, top_k=8,
                                             max_tokens=2048))
-    # 384 experts, top-8, group scales: 13 routes per expert at 624 tokens
-    paths = {t: _lib.w4a16_moe_route_info(plan, t).gemm_path for t in (1, 32, 624, 625, 2048)}
-    assert paths == {1: _lib.PATH_CUDA_CORES, 32: _lib.PATH_CUDA_CORES, 624: _lib.PATH_CUDA_CORES,
-                     625: _lib.PATH_TENSOR_CORES, 2048: _lib.PATH_TENSOR_CORES}
+    # 384 experts, top-8, group scales: 11 routes per expert at 528 tokens
+    paths = {t: _lib.w4a16_moe_route_info(plan, t).gemm_path for t in (1, 32, 528, 529, 2048)}
+    assert paths == {1: _lib.PATH_CUDA_CORES, 32: _lib.PATH_CUDA_CORES, 528: _lib.PATH_CUDA_CORES,
+                     529: _lib.PATH_TENSOR_CORES, 2048: _lib.PATH_TENSOR_CORES}
     assert _lib.w4a16_moe_route_info(plan, 32).tile_rows == 8
     with pytest.raises(_lib.W4A16Error) as ei:
         _lib.w4a16_moe_set_gemm_path(plan, 3)

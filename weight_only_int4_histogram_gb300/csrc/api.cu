@@ -92,14 +92,18 @@ struct Layout {
 
 // Expected routes per local expert up to which the warp-MMA GEMV runs both
 // GEMMs; above it the tcgen05 path wins (its MMA time per weight is the same
-// for any tile fill up to 64 routes).  Measured crossovers on GB300: about 13
-// routes per expert for the group-scale Kimi and ReLU^2 shapes, about 10 for
-// the per-channel shape.  When both GEMMs reduce over at least 2048 values
-// (every GEMV unit streams eight or more 256-value stages) the GEMV stays
-// ahead much longer: on the 32-expert H = 7168, I = 2048 shape it was faster
-// through 64 routes per expert and slower at 96.
-constexpr double kGemvMaxRoutesGroup = 13.0;
-constexpr double kGemvMaxRoutesChannel = 10.0;
+// for any tile fill up to 64 routes).  Measured crossovers on GB300 (whole
+// forward, both paths forced, graph replay): the group-scale Kimi shape
+// (E 384, H 7168, I 256) is even at 10.7 routes per expert (378 vs 382 us) and
+// slower on CUDA cores at 13.3 (423 vs 386); the per-channel shapes are
+// faster on CUDA cores through 21 routes per expert (E 60, H 2048, I 1408:
+// 132 vs 140 us at 1280 routes; ReLU^2 E 64, H 2688, I 1856: 158 vs 173 at 18)
+// and slower at 24 (ReLU^2: 175 vs 163).  When both GEMMs reduce over at least
+// 2048 values (every GEMV unit streams eight or more 256-value stages) the
+// GEMV stays ahead much longer: on the 32-expert H = 7168, I = 2048 shape it
+// was faster through 64 routes per expert and slower at 96.
+constexpr double kGemvMaxRoutesGroup = 11.0;
+constexpr double kGemvMaxRoutesChannel = 20.0;
 constexpr double kGemvMaxRoutesLongK = 80.0;
 
 bool use_gemv(const w4a16_moe_plan_s& P, int T) {
