@@ -92,6 +92,11 @@ typedef enum {
  *   act           w4a16_act: SWIGLU (W13 has N1 = 2I rows) or RELU2 (N1 = I)
  *   scale_kind    w4a16_scale
  *   act_dtype     w4a16_dtype of x and out (and of the intermediate)
+ *   global_experts experts the router spreads routes over (ids in [0, global_experts));
+ *                 0 = num_experts.  Only the planner reads it: the expected routes per
+ *                 local expert T * top_k / global_experts set the route-tile height and
+ *                 the GEMM path.  Results do not depend on it.  0 or >= num_experts
+ *                 (at most 1 << 20).
  *
  * Weight layouts (uint8 packed codes, uint16 BF16 scale bits):
  *   GROUP32_K:    W13 [E, N1, H/2]  S13 [E, N1, H/32]
@@ -111,6 +116,7 @@ typedef struct {
   int32_t act;
   int32_t scale_kind;
   int32_t act_dtype;
+  int32_t global_experts;
 } w4a16_moe_desc;
 
 typedef struct w4a16_moe_plan_s* w4a16_moe_plan_t;

@@ -156,6 +156,29 @@ def test_planner_tile_height_follows_route_counts(lib):
     _lib.w4a16_moe_plan_destroy(plan)
 
 
+def test_global_experts_set_the_routing_density(lib):
+    """A declared global expert count makes the planner expect T * k / global
+    routes per local expert (an expert-parallel shard's share), not T * k / E:
+    32 local of 256 global experts, H 7168, I 2048, top-8 -> 2 routes per local
+    expert at 64 tokens: CUDA cores with 8-route tiles; undeclared, the same
+    shard is planned for 16 routes per expert.  Results never depend on it;
+    fewer global than local experts is refused."""
+    shard = dict(num_experts=32, expert_offset=64, hidden=7168, inter=2048, top_k=8, max_tokens=4096)
+    plan, _ = _lib.w4a16_moe_plan(good_desc(global_experts=256, **shard))
+    info = _lib.w4a16_moe_route_info(plan, 64)
+    assert info.gemm_path == _lib.PATH_CUDA_CORES and info.tile_rows == 8
+    # 11 routes per local expert at 352 tokens; tensor cores above
+    assert _lib.w4a16_moe_route_info(plan, 352).gemm_path == _lib.PATH_CUDA_CORES
+    assert _lib.w4a16_moe_route_info(plan, 353).gemm_path == _lib.PATH_TENSOR_CORES
+    _lib.w4a16_moe_plan_destroy(plan)
+    plan, _ = _lib.w4a16_moe_plan(good_desc(**shard))
+    assert _lib.w4a16_moe_route_info(plan, 64).tile_rows == 32
+    _lib.w4a16_moe_plan_destroy(plan)
+    with pytest.raises(_lib.W4A16Error) as ei:
+        _lib.w4a16_moe_plan(good_desc(global_experts=16, **shard))
+    assert ei.value.status == 1
+
+
 def test_gemm_path_choice_and_validation(lib):
     """Few routes per expert -> CUDA-core GEMV with 8- to 32-route tiles; many ->
     tensor cores; forced paths hold at every batch size."""

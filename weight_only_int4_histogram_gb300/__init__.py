@@ -63,10 +63,11 @@ class W4A16MoE:
     """
 
     def __init__(self, num_experts, hidden, inter, top_k, max_tokens, act=ACT_SWIGLU,
-                 scale_kind=SCALE_GROUP32_K, act_dtype=DT_BF16, expert_offset=0, device="cuda"):
+                 scale_kind=SCALE_GROUP32_K, act_dtype=DT_BF16, expert_offset=0, device="cuda",
+                 global_experts=0):
         _lib.load()
         self.desc = Desc(num_experts, expert_offset, hidden, inter, top_k, max_tokens, act,
-                         scale_kind, act_dtype)
+                         scale_kind, act_dtype, global_experts)
         self.plan, self.workspace_bytes = w4a16_moe_plan(self.desc)
         self.device = torch.device(device)
         self.workspace = torch.empty(self.workspace_bytes, dtype=torch.uint8, device=self.device)
@@ -76,7 +77,8 @@ class W4A16MoE:
     def from_config(cls, cfg, max_tokens=None, device="cuda"):
         return cls(cfg.num_experts, cfg.hidden, cfg.inter, cfg.top_k,
                    max_tokens or max(cfg.tokens), act=cfg.act, scale_kind=cfg.scale_kind,
-                   act_dtype=cfg.act_dtype, expert_offset=cfg.expert_offset, device=device)
+                   act_dtype=cfg.act_dtype, expert_offset=cfg.expert_offset, device=device,
+                   global_experts=cfg.global_experts)
 
     def close(self):
         if self.plan is not None:

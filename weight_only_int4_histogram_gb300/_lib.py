@@ -51,7 +51,7 @@ class W4A16Error(RuntimeError):
 class Desc(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "num_experts", "expert_offset", "hidden", "inter", "top_k", "max_tokens",
-        "act", "scale_kind", "act_dtype")]
+        "act", "scale_kind", "act_dtype", "global_experts")]
 
 
 class RouteInfo(ctypes.Structure):

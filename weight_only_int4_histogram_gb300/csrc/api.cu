@@ -40,6 +40,7 @@ struct w4a16_moe_plan_s {
   int ov_chunk;      // tuning: down weight tiles per fused queue entry (0 = automatic)
   int tail_max;      // tensor-core gate/up: K pieces per unit of the last partial wave (<= 1: none)
   int ov_stages;     // tuning: tensor-core ring stages at most (0 = as many as fit)
+  int ov_bn_cc;      // tuning: CUDA-core route-tile height (8, 16, 32; 0 = automatic)
   cudaEvent_t ev[4];
   bool has_ev;
 };
@@ -106,11 +107,21 @@ constexpr double kGemvMaxRoutesGroup = 11.0;
 constexpr double kGemvMaxRoutesChannel = 20.0;
 constexpr double kGemvMaxRoutesLongK = 80.0;
 
+// Expected routes per local expert of a T-token batch under uniform routing
+// over the declared global experts (the local count when none is declared).
+double routes_per_expert(const w4a16_moe_plan_s& P, int T) {
+  const int eg = P.d.global_experts > 0 ? P.d.global_experts : P.d.num_experts;
+  return static_cast<double>(T) * P.d.top_k / eg;
+}
+
 bool use_gemv(const w4a16_moe_plan_s& P, int T) {
   if (P.path == W4A16_PATH_TENSOR_CORES) return false;
   if (P.path == W4A16_PATH_CUDA_CORES) return true;
-  const double lam = static_cast<double>(T) * P.d.top_k / P.d.num_experts;
-  const bool long_k = P.d.hidden >= 2048 && P.d.inter >= 2048;
+  const double lam = routes_per_expert(P, T);
+  // Without a declared global expert count an expert-parallel shard's
+  // routing density is overestimated by global / local; the long-K limit
+  // below was measured that way (8 x on the 32-of-256-expert shape).
+  const bool long_k = P.d.global_experts == 0 && P.d.hidden >= 2048 && P.d.inter >= 2048;
   const double limit = long_k ? kGemvMaxRoutesLongK
                               : (P.d.scale_kind == W4A16_SCALE_GROUP32_K ? kGemvMaxRoutesGroup
                                                                         : kGemvMaxRoutesChannel);
@@ -122,7 +133,8 @@ bool use_gemv(const w4a16_moe_plan_s& P, int T) {
 // larger stages (a shallower ring); measured on GB300 they pay off from about
 // 4 (16 routes) and 10 (32 routes) expected routes per expert.
 int choose_bn_gemv(const w4a16_moe_plan_s& P, int T) {
-  const double lam = static_cast<double>(T) * P.d.top_k / P.d.num_experts;
+  if (P.ov_bn_cc == 8 || P.ov_bn_cc == 16 || P.ov_bn_cc == kGemvMaxR) return P.ov_bn_cc;
+  const double lam = routes_per_expert(P, T);
   return lam <= 4.0 ? 8 : (lam <= 10.0 ? 16 : kGemvMaxR);
 }
 
@@ -180,7 +192,7 @@ int choose_bn(const w4a16_moe_plan_s& P, int T) {
   // tokens on the 32-local-expert H 7168 / I 2048 shape and at 4096 on the
   // skewed ReLU^2 shape; only the 60-expert per-channel shape at 1024 tokens
   // gained).
-  const double lam = static_cast<double>(T) * P.d.top_k / P.d.num_experts;
+  const double lam = routes_per_expert(P, T);
   const double want = lam + 3.0 * std::sqrt(lam) + 1.0;
   int bn = static_cast<int>(std::ceil(want / 16.0)) * 16;
   // Exception: short gate/up reductions (at most 8 stages of 256) whose
@@ -206,10 +218,16 @@ int choose_fused_splits(double tiles_est, int nt1, int kb, int num_sms) {
   return best;
 }
 
-// Split-K factor for the expected number of route tiles: the cost model is
-// (waves of units) x (K blocks per unit + per-unit overhead); among factors
-// within 5% of the cheapest, the smallest wins (splits add partial traffic).
+// Split-K factor for the expected number of route tiles.  With at least one
+// full wave of units, none: every split writes FP32 partials that the last
+// one reads back, which costs far more than the wave quantisation it removes
+// (the Kimi shard at 2048 tokens, 768 units on 152 SMs: 2 splits 1233 us, none
+// 501; the gate/up GEMM's partial last wave is cut into K pieces instead).
+// Below one wave the cost model is (waves of units) x (K blocks per unit +
+// per-unit overhead); among factors within 5% of the cheapest, the smallest
+// wins.
 int choose_splits(double tiles_est, int n_tiles, int kb, int num_sms, double overhead) {
+  if (tiles_est * n_tiles >= num_sms) return 1;
   double cost[65] = {0};
   double best_cost = 1e300;
   const int smax = std::min(kb, 64);
@@ -247,9 +265,11 @@ Layout make_layout(const w4a16_moe_plan_s& P, int T) {
   L.kb1 = cdiv(d.hidden, block_k);
   L.nt2 = cdiv(d.hidden, kTileRows);
   L.kb2 = cdiv(d.inter, block_k);
-  // expected route tiles (uniform routing): touched experts x tiles per expert
-  const double touched = std::max(1.0, E * (1.0 - std::exp(-static_cast<double>(L.R) / E)));
-  const double per = L.R / touched;
+  // expected route tiles (uniform routing over the declared global experts):
+  // touched local experts x tiles per expert
+  const double r_loc = routes_per_expert(P, T) * E;  // expected local routes
+  const double touched = std::max(1.0, E * (1.0 - std::exp(-r_loc / E)));
+  const double per = r_loc / touched;
   const double tiles_est = touched * std::max(1.0, std::ceil(per / L.bn));
   // unit groups per route tile on the tensor-core path (NT tiles per unit; the
   // same choice choose_nt makes below for a full-size ring)
@@ -492,6 +512,9 @@ w4a16_status validate_desc(const w4a16_moe_desc* d) {
     return fail(W4A16_ERR_INVALID_ARG, "unknown scale kind %d", d->scale_kind);
   if (d->act_dtype != W4A16_DT_BF16 && d->act_dtype != W4A16_DT_FP16)
     return fail(W4A16_ERR_INVALID_ARG, "unknown activation dtype %d", d->act_dtype);
+  if (d->global_experts != 0 && (d->global_experts < d->num_experts || d->global_experts > (1 << 20)))
+    return fail(W4A16_ERR_INVALID_ARG, "global_experts must be 0 or in [num_experts, 2^20], got %d",
+                d->global_experts);
   if (static_cast<int64_t>(d->max_tokens) * d->top_k > (1 << 24))
     return fail(W4A16_ERR_UNSUPPORTED, "max_tokens * top_k too large");
   return W4A16_OK;
@@ -874,6 +897,7 @@ w4a16_status w4a16_moe_plan(const w4a16_moe_desc* desc, w4a16_moe_plan_t* out, s
   if (const char* v = getenv("W4A16_MOE_NT_GATE_UP")) P->ov_nt1 = atoi(v);
   if (const char* v = getenv("W4A16_MOE_NT_DOWN")) P->ov_nt2 = atoi(v);
   if (const char* v = getenv("W4A16_MOE_TC_STAGES")) P->ov_stages = atoi(v);
+  if (const char* v = getenv("W4A16_MOE_CC_TILE_ROWS")) P->ov_bn_cc = atoi(v);
   if (P->ov_nt1 != 0 && P->ov_nt1 != 1 && P->ov_nt1 != 2 && P->ov_nt1 != 4) P->ov_nt1 = 0;
   if (P->ov_nt2 != 0 && P->ov_nt2 != 1 && P->ov_nt2 != 2 && P->ov_nt2 != 4) P->ov_nt2 = 0;
   P->wait_ns = kWaitTimeoutNs;
