@@ -464,6 +464,21 @@ bool encode_out(CUtensorMap* m, void* base, uint64_t cols, uint64_t rows, bool f
             CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The masked-count layout's output [E][max_rows][H] as a 3D tensor with the
+// same 32-column x 16-row boxes: a tile's rows past max_rows are dropped.
+bool encode_out_masked(CUtensorMap* m, void* base, uint64_t cols, uint64_t max_rows, uint64_t E, int dtype) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {cols, max_rows, E};
+  cuuint64_t strides[2] = {cols * 2, cols * max_rows * 2};
+  cuuint32_t box[3] = {32, 16, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  const CUtensorMapDataType t =
+      dtype == W4A16_DT_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  return fn(m, t, 3, base, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // BF16 group scales as a 3D tensor [E][rows][groups], unswizzled boxes of 8
 // groups (16 bytes) x 64 rows; needs 16-byte aligned rows (groups % 8 == 0).
 bool encode_scales(CUtensorMap* m, const void* base, uint64_t groups, uint64_t rows, uint64_t E) {
@@ -667,10 +682,14 @@ w4a16_status launch_forward_fused(const w4a16_moe_plan_s& P, const Layout& L, co
   return launch_combine_of(P, L, true, tw, renorm, out, ws, s);
 }
 
+// masked_rows > 0: the masked-count layout's [E][masked_rows][H] output, which
+// the tensor-core down GEMM (without split-K) writes directly -- its single
+// unit-weight route per row needs no combine; rows past the counts are then
+// zeroed.  Other paths combine as usual.
 w4a16_status launch_forward(const w4a16_moe_plan_s& P, const Layout& L, const void* x,
                             const uint8_t* w13, const uint16_t* s13, const uint8_t* w2,
                             const uint16_t* s2, const float* tw, int32_t renorm, void* out,
-                            uint8_t* ws, cudaStream_t s) {
+                            uint8_t* ws, cudaStream_t s, int32_t masked_rows = 0) {
   const w4a16_moe_desc& d = P.d;
   const bool group = d.scale_kind == W4A16_SCALE_GROUP32_K;
   const bool il = P.layout == W4A16_LAYOUT_INTERLEAVED;
@@ -693,9 +712,12 @@ w4a16_status launch_forward(const w4a16_moe_plan_s& P, const Layout& L, const vo
   memset(&tmNone, 0, sizeof(tmNone));
   // tensor-core path: expert outputs y [splits * slots_cap, H], TMA-stored
   const bool y16 = L.s2 == 1;
+  const bool masked_direct = masked_rows > 0 && !L.gemv && y16;
   CUtensorMap tmY;
   memset(&tmY, 0, sizeof(tmY));
-  if (!L.gemv)
+  if (masked_direct)
+    ok = ok && encode_out_masked(&tmY, out, d.hidden, masked_rows, d.num_experts, d.act_dtype);
+  else if (!L.gemv)
     ok = ok && encode_out(&tmY, ws + L.off_y, d.hidden, static_cast<uint64_t>(L.s2) * L.slots_cap, !y16, d.act_dtype);
   // group scales by TMA (boxes of 8 groups) where their rows are 16-byte multiples
   CUtensorMap tmS1, tmS2;
@@ -783,12 +805,21 @@ w4a16_status launch_forward(const w4a16_moe_plan_s& P, const Layout& L, const vo
   g2.counters = nullptr;
   g2.scale_tma = stma2 ? 1 : 0;
   g2.out16 = y16 ? 1 : 0;
+  g2.masked_rows = masked_direct ? masked_rows : 0;
+  g2.seg_offs = masked_direct ? reinterpret_cast<const int32_t*>(ws + L.off_offs) : nullptr;
   e = L.gemv ? launch_gemv(GEMM_DOWN, d.scale_kind, d.act_dtype, lay, g2, tmA2, tmS2, L.grid2, L.smem2, s, P.pdl)
              : launch_gemm(GEMM_DOWN, d.scale_kind, d.act_dtype, lay, g2, tmA2, tmB2, tmY, tmS2, L.grid2, L.smem2, s,
                            P.pdl);
   if (e != cudaSuccess) return cuda_fail(e, "down GEMM launch");
   if (P.has_ev && (e = cudaEventRecord(P.ev[2], s)) != cudaSuccess) return cuda_fail(e, "event record");
 
+  if (masked_direct) {
+    e = launch_masked_zero_rows(reinterpret_cast<const int32_t*>(ws + L.off_counts), d.num_experts, masked_rows,
+                                d.hidden, out, s, P.pdl);
+    if (e != cudaSuccess) return cuda_fail(e, "masked zero-rows launch");
+    if (P.has_ev && (e = cudaEventRecord(P.ev[3], s)) != cudaSuccess) return cuda_fail(e, "event record");
+    return W4A16_OK;
+  }
   return launch_combine_of(P, L, y16, tw, renorm, out, ws, s);
 }
 
@@ -1096,7 +1127,15 @@ w4a16_status w4a16_moe_forward_masked(w4a16_moe_plan_t plan, int32_t max_rows, c
   if (e != cudaSuccess) return cuda_fail(e, "masked-route launch");
   st = w4a16_moe_prepare_routes(plan, T, ids, workspace, stream);
   if (st != W4A16_OK) return st;
-  return w4a16_moe_forward(plan, T, x, w13, s13, w2, s2, wts, ids, 0, y, workspace, stream);
+  if ((st = check_ptr(x, 16, "x")) != W4A16_OK) return st;
+  if ((st = check_ptr(w13, 16, "w13")) != W4A16_OK) return st;
+  if ((st = check_ptr(s13, 4, "s13")) != W4A16_OK) return st;
+  if ((st = check_ptr(w2, 16, "w2")) != W4A16_OK) return st;
+  if ((st = check_ptr(s2, 4, "s2")) != W4A16_OK) return st;
+  if ((st = check_ptr(y, 16, "y")) != W4A16_OK) return st;
+  // the rows' single unit-weight routes: the tensor-core down GEMM writes y
+  // directly (no combine), other paths combine into it
+  return launch_forward(*plan, L, x, w13, s13, w2, s2, wts, 0, y, ws, static_cast<cudaStream_t>(stream), max_rows);
 }
 
 w4a16_status w4a16_moe_route_topk(const float* logits, int32_t num_tokens, int32_t num_global, int32_t top_k,

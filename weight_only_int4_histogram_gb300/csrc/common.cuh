@@ -151,6 +151,9 @@ struct GemmParams {
   int32_t scale_tma;       // group scales loaded by TMA (their rows are 16-byte multiples)
   int32_t out16;           // down GEMM: expert outputs in the activation dtype (no split-K),
                            // else FP32 split partials
+  int32_t masked_rows;     // down GEMM, masked-count layout: the output is [E][masked_rows][H]
+                           // (expert e's slot offs[e] + i to row i; rows past max are dropped)
+  const int32_t* seg_offs; // ... with the experts' first slots (route preparation's offsets)
   uint64_t wait_ns;        // limit of every pipeline wait (drains use kWaitTimeoutNs)
 };
 
@@ -411,6 +414,12 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void*
   asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
                    reinterpret_cast<uint64_t>(map)),
                "r"(smem_u32(src)), "r"(c0), "r"(c1)
+               : "memory");
+}
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void* src, int c0, int c1, int c2) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2)
                : "memory");
 }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }

@@ -357,7 +357,10 @@ __device__ __forceinline__ void issue_slot(uint32_t d_tmem, int bn, uint32_t a0,
   }
 }
 
-template <int WHICH, int SCALE, int DT, int LAYOUT>
+// MASKED (down GEMM only): the masked-count layout's output [E][max_rows][H]
+// takes the expert outputs directly (a separate instance, so that the usual
+// one's epilogue code is unchanged).
+template <int WHICH, int SCALE, int DT, int LAYOUT, bool MASKED = false>
 __global__ void __launch_bounds__(WHICH == GEMM_DOWN ? kGemmThreadsDown : kGemmThreads, 1)
     w4a16_gemm_kernel(const __grid_constant__ GemmParams p, const __grid_constant__ CUtensorMap tmA,
                       const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmC,
@@ -827,7 +830,10 @@ __global__ void __launch_bounds__(WHICH == GEMM_DOWN ? kGemmThreadsDown : kGemmT
             __syncwarp();
             const int col0 = grow - lane;
             if (lane == 0 && col0 < p.out_cols) {
-              tma_store_2d(&tmC, stg, col0, static_cast<int>(w.split * p.slots_cap) + m0 + c0);
+              if (MASKED)  // straight into the caller's [E][max_rows][H] output
+                tma_store_3d(&tmC, stg, col0, m0 - __ldg(p.seg_offs + e) + c0, e);
+              else
+                tma_store_2d(&tmC, stg, col0, static_cast<int>(w.split * p.slots_cap) + m0 + c0);
               bulk_commit();
             }
             sbuf ^= 1;
@@ -956,11 +962,11 @@ __global__ void __launch_bounds__(WHICH == GEMM_DOWN ? kGemmThreadsDown : kGemmT
 
 namespace w4a16 {
 
-template <int WHICH, int SCALE, int DT, int LAYOUT>
+template <int WHICH, int SCALE, int DT, int LAYOUT, bool MASKED = false>
 cudaError_t launch_gemm_one(const GemmParams& p, const CUtensorMap& tmA, const CUtensorMap& tmB,
                             const CUtensorMap& tmC, const CUtensorMap& tmS, int grid, int smem_bytes,
                             cudaStream_t s, bool pdl) {
-  auto kern = w4a16_gemm_kernel<WHICH, SCALE, DT, LAYOUT>;
+  auto kern = w4a16_gemm_kernel<WHICH, SCALE, DT, LAYOUT, MASKED>;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -993,6 +999,12 @@ cudaError_t launch_gemm_dt(int which, int scale_kind, const GemmParams& p, const
                ? launch_gemm_one<GEMM_UP, SCALE_GROUP, DT, LAYOUT>(p, tmA, tmB, tmC, tmS, grid, smem_bytes, s, pdl)
                : launch_gemm_one<GEMM_UP, SCALE_CHANNEL, DT, LAYOUT>(p, tmA, tmB, tmC, tmS, grid, smem_bytes, s, pdl);
   }
+  if (p.masked_rows > 0)
+    return scale_kind == SCALE_GROUP
+               ? launch_gemm_one<GEMM_DOWN, SCALE_GROUP, DT, LAYOUT, true>(p, tmA, tmB, tmC, tmS, grid, smem_bytes, s,
+                                                                             pdl)
+               : launch_gemm_one<GEMM_DOWN, SCALE_CHANNEL, DT, LAYOUT, true>(p, tmA, tmB, tmC, tmS, grid, smem_bytes,
+                                                                               s, pdl);
   return scale_kind == SCALE_GROUP
              ? launch_gemm_one<GEMM_DOWN, SCALE_GROUP, DT, LAYOUT>(p, tmA, tmB, tmC, tmS, grid, smem_bytes, s, pdl)
              : launch_gemm_one<GEMM_DOWN, SCALE_CHANNEL, DT, LAYOUT>(p, tmA, tmB, tmC, tmS, grid, smem_bytes, s, pdl);

@@ -316,6 +316,40 @@ cudaError_t launch_masked_routes(const int32_t* counts, int32_t E, int32_t max_r
   return cudaLaunchKernelEx(&cfg, masked_routes_kernel, counts, E, max_rows, expert_offset, ids, weights);
 }
 
+// Masked-count layout written directly by the down GEMM: rows i >= counts[e]
+// of every expert are +0 (the GEMM's padding slots may have landed there).
+// counts: route preparation's per-expert route counts; 16-bit elements.
+__global__ void __launch_bounds__(256) masked_zero_rows_kernel(const int32_t* counts, int32_t max_rows, int32_t H,
+                                                               uint4* out) {
+  pdl_wait();
+  pdl_launch_dependents();
+  const int e = blockIdx.y;
+  const int c = min(counts[e], max_rows);
+  const int vec_row = H / 8;  // 16-byte vectors of a row
+  const int64_t n = static_cast<int64_t>(max_rows - c) * vec_row;
+  uint4* base = out + (static_cast<int64_t>(e) * max_rows + c) * vec_row;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+    base[i] = make_uint4(0u, 0u, 0u, 0u);
+}
+
+cudaError_t launch_masked_zero_rows(const int32_t* counts, int32_t E, int32_t max_rows, int32_t H, void* out,
+                                    cudaStream_t s, bool pdl) {
+  const int64_t per_expert = static_cast<int64_t>(max_rows) * (H / 8);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(std::max<int64_t>(1, std::min<int64_t>((per_expert + 255) / 256, 64))),
+                     static_cast<unsigned>(E));
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, masked_zero_rows_kernel, counts, max_rows, H, static_cast<uint4*>(out));
+}
+
 namespace {
 template <typename K>
 cudaError_t launch_rp(K kern, const RoutePrepParams& p, int grid, int smem_bytes, cudaStream_t s, bool pdl) {
