@@ -20,7 +20,8 @@ PATHS = {"tc": 1, "cc": 2}
 
 @pytest.mark.parametrize("path", list(PATHS))
 @pytest.mark.parametrize("shape", [dict(E=6, H=512, I=256), dict(E=5, H=704, I=320, scale=gen.SCALE_PER_CHANNEL),
-                                   dict(E=4, H=640, I=192, act=gen.ACT_RELU2)])
+                                   dict(E=4, H=640, I=192, act=gen.ACT_RELU2),
+                                   dict(E=6, H=512, I=256, dt=gen.DT_FP16)])
 def test_masked_layout_matches_oracle(shape, path):
     cfg = small_cfg(k=1, seed=41, **shape)
     E, M = cfg.num_experts, 24
@@ -29,7 +30,9 @@ def test_masked_layout_matches_oracle(shape, path):
     x = gen.make_activations(cfg, E * M, "cuda").view(E, M, cfg.hidden)
     moe = make_moe(cfg, E * M)
     moe.set_gemm_path(PATHS[path])
-    y = moe.forward_masked(x, w, counts.cuda())
+    # rows past the counts must come out +0 whatever the buffer held
+    y = torch.full((E, M, cfg.hidden), float("nan"), dtype=x.dtype, device="cuda")
+    moe.forward_masked(x, w, counts.cuda(), out=y)
     torch.cuda.synchronize()
     moe.check_device_error()
     acc, _ = oracle.masked_forward(cfg, x.view(E * M, cfg.hidden).cpu(), w.to("cpu"), counts, M)
