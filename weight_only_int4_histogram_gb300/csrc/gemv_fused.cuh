@@ -38,13 +38,20 @@
 // group's sums from a double-buffered exchange and runs the epilogue.  Each
 // stage carries a header (unit, K block, tile record) written by the producer.
 //
-// Warp roles (576 threads):
-//   warp 0      producer: takes queue entries, writes stage headers, TMA of
-//               weights and scales (cp.async for unaligned scale rows)
-//   warp 1      activation rows: reads each stage's header; gate/up: token rows
+// Warp roles (608 threads):
+//   warp 0      producer (one lane when every scale row comes by TMA): takes
+//               queue entries, writes stage headers, TMA of the weight tile
+//               (and of the scales unless the activation warps issue them;
+//               cp.async by the whole warp for unaligned scale rows)
+//   warp 1      activation rows of the even stages (of every stage with the
+//               fused finalize): reads the stage's header; gate/up: token rows
 //               of x by route; down: the route tile's intermediate rows, after
-//               waiting until all of its gate/up row blocks are published
+//               waiting until all of its gate/up row blocks are published;
+//               issues the stage's group-scale TMA when both GEMMs load
+//               scales by TMA
 //   warps 2-17  compute groups 0 and 1 (row block = warp index mod 8)
+//   warp 18     activation rows of the odd stages, or with the fused finalize
+//               the finalize warp
 //
 // Epilogue signals: each finishing warp publishes its 16 intermediate rows of
 // route tile m with a release increment of ready[m] (8 row blocks x nt1 weight
