@@ -215,7 +215,8 @@ typedef struct {
   size_t off_expert_out;   /* expert outputs [max_slots, H] in the activation dtype, or FP32
                               split partials [gemm2_splits, max_slots, H] when gemm2_splits > 1 */
   int32_t fused_gemms;     /* 1: CUDA-core path with both GEMMs in one launch (then
-                              gemm1_ctas = gemm2_ctas = that launch's grid) */
+                              gemm1_ctas = gemm2_ctas = that launch's grid: one CTA
+                              per SM, or two with one compute group each) */
   int32_t fused_finalize;  /* 1: that launch also combines the routes (no combine launch) */
 } w4a16_route_info;
 

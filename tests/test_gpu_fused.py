@@ -11,7 +11,11 @@ device work queue) and of the deterministic fused finalize.
 * forwards are bit-identical when repeated, and a forward that reuses a route
   layout (no prepare_routes in between) is still correct: the queue state is
   reset by the combine, or by the last CTA when the finalize is fused;
-* the fused and the two-launch CUDA-core forwards agree within tolerance.
+* the fused and the two-launch CUDA-core forwards agree within tolerance;
+* the one-group form of the fused launch (one compute group per CTA, two CTAs
+  per SM, 8-route tiles) matches the oracle on every combination, repeats bit
+  for bit and agrees with the two-group form; the planner takes it on the
+  Kimi shard at 32 tokens.
 """
 import numpy as np
 import pytest
@@ -138,10 +142,13 @@ def test_fused_and_two_launch_paths_agree(monkeypatch):
 
 
 @pytest.mark.parametrize("T", [1, 8, 32])
-def test_full_size_kimi_fused_finalize_sampled_rows(T):
+def test_full_size_kimi_fused_finalize_sampled_rows(monkeypatch, T):
     cfg = gen.CONFIGS["kimi_tp8_e384_h7168_i256_k8"]
     w = gen.make_weights(cfg, "cuda")
     _, x, ids, tw = case_on_gpu(cfg, T, weights_gpu=w)
+    # the finalize runs with two compute groups per CTA: the combine-launch
+    # forward it must equal bit for bit sums each unit the same way
+    monkeypatch.setenv("W4A16_MOE_FUSED_GROUPS", "2")
     base, wl = fused_moe(cfg, T, finalize=False, interleaved=True, w=w)
     want = base(x, wl, tw, ids).clone()
     fin, wl2 = fused_moe(cfg, T, finalize=True, interleaved=True, w=w)
@@ -151,3 +158,52 @@ def test_full_size_kimi_fused_finalize_sampled_rows(T):
     assert torch.equal(got.view(torch.int16), want.view(torch.int16))
     rows = sorted(set([0, T - 1] + np.random.default_rng(T).integers(0, T, size=min(T, 12)).tolist()))
     compare(got[rows], oracle_rows(cfg, w, x, ids, tw, rows=rows), f"kimi T={T} fused finalize")
+
+
+def _sms():
+    return torch.cuda.get_device_properties(0).multi_processor_count
+
+
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: f"a{s['act']}s{s['scale']}d{s['dt']}")
+@pytest.mark.parametrize("interleaved", [False, True], ids=["ckpt", "il"])
+def test_one_compute_group_per_cta(monkeypatch, shape, interleaved):
+    # 64 experts, k = 2 over 40 tokens: 1.25 routes per expert (8-route tiles);
+    # H = 1056: 5 gate/up K blocks (ragged last) that one group walks alone
+    cfg = small_cfg(E=64, H=1056, I=320, k=2, seed=53, **shape)
+    T = 40
+    w, x, ids, tw = case_on_gpu(cfg, T)
+    outs = {}
+    for groups in ("1", "2"):
+        monkeypatch.setenv("W4A16_MOE_FUSED_GROUPS", groups)
+        moe, wl = fused_moe(cfg, T, interleaved=interleaved, w=w)
+        info = moe.route_info(T)
+        assert info.tile_rows == 8
+        assert info.gemm1_ctas == (2 if groups == "1" else 1) * _sms()
+        out = moe(x, wl, tw, ids).clone()
+        again = moe(x, wl, tw, ids)
+        torch.cuda.synchronize()
+        moe.check_device_error()
+        assert torch.equal(again.view(torch.int16), out.view(torch.int16))
+        outs[groups] = out
+    ref = oracle_rows(cfg, w, x, ids, tw)
+    compare(outs["1"], ref, f"one group {cfg.name}")
+    compare(outs["2"], ref, f"two groups {cfg.name}")
+    compare(outs["1"], outs["2"].float().cpu().numpy(), f"one vs two groups {cfg.name}")
+
+
+def test_full_size_kimi_one_group_sampled_rows():
+    """The planner's choice at 32 tokens on the Kimi shard: one compute group
+    per CTA, two CTAs per SM."""
+    cfg = gen.CONFIGS["kimi_tp8_e384_h7168_i256_k8"]
+    T = 32
+    w = gen.make_weights(cfg, "cuda")
+    _, x, ids, tw = case_on_gpu(cfg, T, weights_gpu=w)
+    moe, wl = fused_moe(cfg, T, interleaved=True, w=w)
+    assert moe.route_info(T).gemm1_ctas == 2 * _sms()
+    out = moe(x, wl, tw, ids).clone()
+    again = moe(x, wl, tw, ids)
+    torch.cuda.synchronize()
+    moe.check_device_error()
+    assert torch.equal(again.view(torch.int16), out.view(torch.int16))
+    rows = sorted(set([0, T - 1] + np.random.default_rng(7).integers(0, T, size=10).tolist()))
+    compare(out[rows], oracle_rows(cfg, w, x, ids, tw, rows=rows), "kimi T=32 one group")

@@ -41,6 +41,7 @@ struct w4a16_moe_plan_s {
   int tail_max;      // tensor-core gate/up: K pieces per unit of the last partial wave (<= 1: none)
   int ov_stages;     // tuning: tensor-core ring stages at most (0 = as many as fit)
   int ov_bn_cc;      // tuning: CUDA-core route-tile height (8, 16, 32; 0 = automatic)
+  int ov_fgroups;    // tuning: fused launch compute groups per CTA (1, 2; 0 = automatic)
   cudaEvent_t ev[4];
   bool has_ev;
 };
@@ -69,6 +70,7 @@ int cdiv(int a, int b) { return (a + b - 1) / b; }
 struct Layout {
   bool gemv;  // CUDA-core path for both GEMMs
   bool fused;       // CUDA-core path: both GEMMs in one launch (gemv_fused.cuh)
+  int fgroups;      // fused: compute groups per CTA (2: one CTA per SM; 1: two CTAs per SM)
   int down_chunk;   // fused: down weight tiles per queue entry
   int ctr_len;      // counters zeroed by route preparation
   bool fin;         // fused finalize in this forward
@@ -161,6 +163,19 @@ void choose_nt(int n_tiles, int bn, int smem_budget, int max_nt, bool double_acc
     if (smem_budget / gemm_stage_bytes(nt, bn) >= 2 && gemm_a_slots(nt, bn, acc) >= 2) return;
   }
 }
+
+// Fused CUDA-core launch at 8-route tiles: one compute group per CTA and two
+// CTAs per SM (each group owns whole units and its own ring, so one group's
+// epilogue never holds up the other's stages) once the expected gate/up units
+// fill this many waves of those CTAs; with fewer units, two groups splitting
+// each unit's stages finish the gate/up phase sooner.  Measured (whole
+// forward, one group vs two): Kimi shard 24 / 32 / 64 tokens (1.99 / 2.46 /
+// 3.7 waves) 120.5 / 138.9 / 200.4 vs 126.6 / 147.1 / 212.6 us, but 8 / 16
+// tokens (0.78 / 1.43) 70.3 / 104.1 vs 63.1 / 99.0; DeepSeek-like 32-of-256
+// shard 32 / 64 tokens (2.13 / 2.9) 131.7 / 163.5 vs 134.8 / 173.7; ReLU^2
+// E64 32 tokens (2.96) 85.6 vs 91.8 but 8 tokens (1.67) 50.8 vs 44.7;
+// per-channel E60 16 / 32 tokens (2.85 / 3.8) 55.9 / 69.3 vs 59.0 / 73.4.
+constexpr double kOneGroupWaves = 1.9;
 
 // Units of at most this many K blocks keep two accumulator sets.
 constexpr int kDoubleAccMaxKb = 8;
@@ -283,8 +298,13 @@ Layout make_layout(const w4a16_moe_plan_s& P, int T) {
     g2 = cdiv(L.nt2, nt);
   }
   L.fused = L.gemv && P.fused;
+  L.fgroups = 2;
+  if (L.fused && L.bn == 8 && !P.finalize &&
+      (P.ov_fgroups == 1 || (P.ov_fgroups == 0 && tiles_est * L.nt1 >= kOneGroupWaves * 2 * P.num_sms)))
+    L.fgroups = 1;
   if (L.fused) {
-    L.s1 = P.ov_s1 ? std::min(P.ov_s1, kMaxFusedSplits) : choose_fused_splits(tiles_est, L.nt1, L.kb1, P.num_sms);
+    const int ctas = P.num_sms * (L.fgroups == 1 ? 2 : 1);
+    L.s1 = P.ov_s1 ? std::min(P.ov_s1, kMaxFusedSplits) : choose_fused_splits(tiles_est, L.nt1, L.kb1, ctas);
     // every split must own K blocks: each one's arrival completes its row blocks
     L.s1 = cdiv(L.kb1, cdiv(L.kb1, L.s1));
     L.s2 = 1;  // the down GEMM is balanced by the queue instead
@@ -301,7 +321,12 @@ Layout make_layout(const w4a16_moe_plan_s& P, int T) {
     L.stage_bytes = gemv_stage_bytes(L.bn);
     L.stages = gemv_stages(L.bn, ksplit);
     L.smem = gemv_smem_bytes(L.bn, ksplit);
-    if (L.fused) {
+    if (L.fgroups == 1) {
+      // one compute group per CTA (no exchange buffers), two CTAs per SM:
+      // each CTA gets half of the SM's shared memory less its 1 KB reserve
+      L.stages = std::min(kGemvMaxStages, (kSmemPerSM / 2 - 1024 - 1024 - kGemvCtrlBytes) / L.stage_bytes);
+      L.smem = 1024 + L.stages * L.stage_bytes + kGemvCtrlBytes;
+    } else if (L.fused) {
       // the two compute groups take the stages of their parity: an even ring
       L.stages &= ~1;
       L.smem = 1024 + L.stages * L.stage_bytes + gemv_ctrl_bytes(L.bn, true);
@@ -331,7 +356,7 @@ Layout make_layout(const w4a16_moe_plan_s& P, int T) {
   const int64_t units2 = static_cast<int64_t>(L.tiles_cap) * cdiv(L.nt2, L.ntu2) * L.s2;
   L.grid1 = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(P.num_sms, units1)));
   L.grid2 = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(P.num_sms, units2)));
-  if (L.fused) L.grid1 = L.grid2 = P.num_sms;  // one queue for both GEMMs
+  if (L.fused) L.grid1 = L.grid2 = P.num_sms * (L.fgroups == 1 ? 2 : 1);  // one queue for both GEMMs
   // split-K arrival counters; the fused launch adds its queue head (padded to
   // 32 entries), the ready counts of the route tiles and per-row-block counters
   // (and, always reserved so that the finalize switch never outgrows a
@@ -639,6 +664,7 @@ w4a16_status launch_forward_fused(const w4a16_moe_plan_s& P, const Layout& L, co
   fp.ready = ctr + 32;
   fp.fix = ctr + 32 + L.tiles_cap;
   fp.down_chunk = L.down_chunk;
+  fp.groups = L.fgroups;
   if (L.fin) {
     fp.finalize = 1;
     fp.fin_ctr = ctr + L.fix_len;
@@ -929,6 +955,7 @@ w4a16_status w4a16_moe_plan(const w4a16_moe_desc* desc, w4a16_moe_plan_t* out, s
   if (const char* v = getenv("W4A16_MOE_NT_DOWN")) P->ov_nt2 = atoi(v);
   if (const char* v = getenv("W4A16_MOE_TC_STAGES")) P->ov_stages = atoi(v);
   if (const char* v = getenv("W4A16_MOE_CC_TILE_ROWS")) P->ov_bn_cc = atoi(v);
+  if (const char* v = getenv("W4A16_MOE_FUSED_GROUPS")) P->ov_fgroups = atoi(v);
   if (P->ov_nt1 != 0 && P->ov_nt1 != 1 && P->ov_nt1 != 2 && P->ov_nt1 != 4) P->ov_nt1 = 0;
   if (P->ov_nt2 != 0 && P->ov_nt2 != 1 && P->ov_nt2 != 2 && P->ov_nt2 != 4) P->ov_nt2 = 0;
   P->wait_ns = kWaitTimeoutNs;

@@ -56,6 +56,7 @@ constexpr int kGemvBlockK = 256;
 constexpr int kGemvMaxStages = 12;
 constexpr int kGemvCtrlBytes = 4608;   // mbarriers, flags, tile table
 constexpr int kGemvSmemLimit = 232448;
+constexpr int kSmemPerSM = 233472;     // shared memory of one SM (228 KB)
 // weights (16 KB) + BF16 scales (2 KB) + rows of bn routes (512 B + 64 B pad each)
 __host__ __device__ constexpr int gemv_stage_bytes(int bn) {
   return (kTileRows * kGemvBlockK / 2 + kTileRows * 16 + bn * 576 + 1023) / 1024 * 1024;
@@ -180,6 +181,8 @@ struct FusedParams {
   int32_t* exit_ctr;       // CTAs done (inside the reset range)
   int32_t* reset;          // [reset_len] queue state zeroed by the last CTA
   int32_t reset_len;
+  int32_t groups;          // compute groups per CTA: 2 (one CTA per SM) or 1 (two CTAs per SM,
+                           // 8-route tiles, no fused finalize)
 };
 
 struct CombineParams {

@@ -38,6 +38,12 @@
 // group's sums from a double-buffered exchange and runs the epilogue.  Each
 // stage carries a header (unit, K block, tile record) written by the producer.
 //
+// One-group form (8-route tiles with enough gate/up units, no fused
+// finalize; the host decides): 320 threads -- the producer, one activation
+// warp taking every stage, one compute group of 8 warps that runs every stage
+// of its units (no exchange) -- and two CTAs per SM, each with its own ring of
+// half the shared memory.  A group's epilogue then holds up only its own ring.
+//
 // Warp roles (608 threads):
 //   warp 0      producer (one lane when every scale row comes by TMA): takes
 //               queue entries, writes stage headers, TMA of the weight tile
@@ -98,6 +104,10 @@ static_assert(kFzOffFinCtl + 16 <= kGemvCtrlBytes, "finalize queue");
 // Warps: producer, activation rows, 16 compute, finalize.
 constexpr int kFusedThreads = 32 * (2 + kGemvComputeWarps + 1);
 constexpr int kFinWarp = 2 + kGemvComputeWarps;
+// One-group form (8-route tiles without the fused finalize): producer,
+// activation warp and one compute group of 8 warps, two CTAs per SM.
+constexpr int kFusedThreads1 = 32 * (2 + kGemvComputeWarps / 2);
+__host__ __device__ constexpr int fused_threads(int groups) { return groups == 1 ? kFusedThreads1 : kFusedThreads; }
 
 // The queue's parts at fixed offsets of the control block (one base pointer:
 // every compute warp carries it, and registers are scarce there).
@@ -453,13 +463,15 @@ __device__ __forceinline__ bool fused_down_epilogue(const FusedParams& fp, const
   return true;
 }
 
-// Ring walk of one compute group: slots of parity grp, ring_len even.
+// Ring walk of one compute group: with two groups the slots of parity grp
+// (ring_len even), with one group every slot.
+template <int GROUPS>
 struct GroupRing {
   int slot;
   uint32_t ph, seq;
   __device__ __forceinline__ void next(int ring_len) {
-    slot += 2;
-    seq += 2;
+    slot += GROUPS;
+    seq += GROUPS;
     if (slot >= ring_len) {
       slot -= ring_len;
       ph ^= 1u;
@@ -468,13 +480,14 @@ struct GroupRing {
 };
 
 // This group's stages of one unit (the first already waited for), its share
-// of the exchange and, on the finishing group, the epilogue.
-template <int SCALE, int DT, int LAYOUT, int NB>
+// of the exchange and, on the finishing group, the epilogue.  One group takes
+// every stage of its units: no exchange.
+template <int SCALE, int DT, int LAYOUT, int NB, int GROUPS>
 __device__ __forceinline__ bool fused_unit(const FusedParams& fp, uint8_t* smem, int stage_bytes, uint64_t* full,
                                            uint64_t* empty, uint64_t* xfull, uint64_t* xempty,
                                            const StageHdr* hdrs, volatile int* abort_flag, float* red,
                                            int ring_len, int grp, int rowA, int rowB, int rb, int lane,
-                                           uint32_t ld_row_off, int ld_row7, int ld_chunk, GroupRing& r,
+                                           uint32_t ld_row_off, int ld_row7, int ld_chunk, GroupRing<GROUPS>& r,
                                            uint32_t& xj, const FinQueue& fq, FinPending& pend) {
   const StageHdr h = hdrs[r.slot];
   float tot[4 * NB];
@@ -489,8 +502,8 @@ __device__ __forceinline__ bool fused_unit(const FusedParams& fp, uint8_t* smem,
     if (r.seq > h.last_seq) break;
     if (!warp_wait(&full[r.slot], r.ph, abort_flag, fp.up.err, fp.up.wait_ns)) return false;
   }
-  const bool finisher = static_cast<int>(h.last_seq & 1u) == grp;
-  if (h.last_seq > h.first_seq) {
+  const bool finisher = GROUPS == 1 || static_cast<int>(h.last_seq & 1u) == grp;
+  if (GROUPS == 2 && h.last_seq > h.first_seq) {
     // both groups took stages of this unit: meet in exchange buffer xj % 2
     const int b = xj & 1;
     const uint32_t use = xj >> 1;
@@ -528,15 +541,15 @@ __device__ __forceinline__ bool fused_unit(const FusedParams& fp, uint8_t* smem,
   return fused_down_epilogue<SCALE, DT, NB>(fp, h, rowA, rowB, lane, tot, fq, pend, abort_flag);
 }
 
-template <int SCALE, int DT, int LAYOUT, int NBMAX>
-__global__ void __launch_bounds__(kFusedThreads, 1)
+template <int SCALE, int DT, int LAYOUT, int NBMAX, int GROUPS>
+__global__ void __launch_bounds__(fused_threads(GROUPS), GROUPS == 1 ? 2 : 1)
     w4a16_gemv_fused_kernel(const __grid_constant__ FusedParams fp, const __grid_constant__ CUtensorMap tmA1,
                             const __grid_constant__ CUtensorMap tmS1, const __grid_constant__ CUtensorMap tmA2,
                             const __grid_constant__ CUtensorMap tmS2) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const GemmParams& pu = fp.up;
-  const int ring_len = pu.stages;  // even (host)
+  const int ring_len = pu.stages;  // even with two groups (host)
   const int stage_bytes = pu.stage_bytes;
   uint8_t* ctrl = smem + ring_len * stage_bytes;
   uint64_t* full = reinterpret_cast<uint64_t*>(ctrl + kFzOffFull);
@@ -556,7 +569,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
   // Two activation warps (even / odd stages) unless the finalize warp is
   // busy; they also issue the group-scale TMA of their stages when both GEMMs
   // load scales by TMA (the producer then issues one TMA per stage).
-  const bool two_copy = !fp.finalize;
+  const bool two_copy = GROUPS == 2 && !fp.finalize;
   const bool scale_by_copier = two_copy && SCALE == SCALE_GROUP && fp.up.scale_tma && fp.down.scale_tma;
 
   if (threadIdx.x == 0) {
@@ -789,7 +802,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     } else {
       produce(std::integral_constant<bool, false>());
     }
-  } else if (warp == 1 || (warp == kFinWarp && two_copy)) {
+  } else if (warp == 1 || (GROUPS == 2 && warp == kFinWarp && two_copy)) {
     // ------------------------------------------------------------------ activation rows
     // Two copy warps take the stages of even and odd sequence number: one
     // warp's per-stage work, slowed by the compute warps beside it on its
@@ -917,7 +930,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
       }
     }
     asm volatile("cp.async.wait_all;" ::: "memory");
-  } else if (warp < kFinWarp) {
+  } else if (warp < 2 + 8 * GROUPS) {
     // ------------------------------------------------------------------ compute groups
     const int cw = warp - 2, grp = cw >> 3, rb = cw & 7, g = lane >> 2;
     // rows of this warp: SwiGLU gate/up tiles pair gate row 8 rb + g with its
@@ -936,7 +949,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
       r7 = ld_row & 7;
       ch = ld_j >> 1;
     };
-    GroupRing r;
+    GroupRing<GROUPS> r;
     r.slot = grp;
     r.ph = 0;
     r.seq = static_cast<uint32_t>(grp);
@@ -955,7 +968,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
       ld_off(rowA, rowB, off, r7, ch);
       bool ok;
 #define W4A16_FUSED_UNIT(NBV)                                                                                   \
-  fused_unit<SCALE, DT, LAYOUT, NBV>(fp, smem, stage_bytes, full, empty, xfull, xempty, hdrs, abort_flag, red, \
+  fused_unit<SCALE, DT, LAYOUT, NBV, GROUPS>(fp, smem, stage_bytes, full, empty, xfull, xempty, hdrs, abort_flag, red, \
                                      ring_len, grp, rowA, rowB, rb, lane, off, r7, ch, r, xj, fq, pend)
       if (NBMAX == 1 || nb <= 1) ok = W4A16_FUSED_UNIT(1);
       else if (NBMAX == 2 || nb == 2) ok = W4A16_FUSED_UNIT(2);
@@ -972,7 +985,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
         atomicAdd(fq.done(), 1);
       }
     }
-  } else {
+  } else if (GROUPS == 2) {
     // ------------------------------------------------------------------ finalize
     if (fp.finalize) fin_warp<DT>(fp, fq, lane, abort_flag);
   }
@@ -993,11 +1006,11 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
   }
 }
 
-template <int SCALE, int DT, int LAYOUT, int NBMAX>
+template <int SCALE, int DT, int LAYOUT, int NBMAX, int GROUPS>
 cudaError_t launch_gemv_fused_one(const FusedParams& fp, const CUtensorMap& tmA1, const CUtensorMap& tmS1,
                                   const CUtensorMap& tmA2, const CUtensorMap& tmS2, int grid, int smem_bytes,
                                   cudaStream_t s, bool pdl) {
-  auto kern = w4a16_gemv_fused_kernel<SCALE, DT, LAYOUT, NBMAX>;
+  auto kern = w4a16_gemv_fused_kernel<SCALE, DT, LAYOUT, NBMAX, GROUPS>;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -1005,12 +1018,15 @@ cudaError_t launch_gemv_fused_one(const FusedParams& fp, const CUtensorMap& tmA1
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (configured_for[dev] < smem_bytes) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+    // two CTAs per SM need the largest shared-memory carveout
+    if (e == cudaSuccess && GROUPS == 1)
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
     if (e != cudaSuccess) return e;
     configured_for[dev] = smem_bytes;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kFusedThreads);
+  cfg.blockDim = dim3(fused_threads(GROUPS));
   cfg.dynamicSmemBytes = smem_bytes;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
@@ -1029,8 +1045,16 @@ cudaError_t launch_gemv_fused_dt(int scale_kind, const FusedParams& fp, const CU
   // 32-route code path costs registers that the 8-route one then lacks
   // (measured: 3-5 % at 1 to 32 tokens on the Kimi shard with 8-route tiles)
 #define W4A16_FUSED_ONE(SC, NBM) \
-  launch_gemv_fused_one<SC, DT, LAYOUT, NBM>(fp, tmA1, tmS1, tmA2, tmS2, grid, smem_bytes, s, pdl)
+  launch_gemv_fused_one<SC, DT, LAYOUT, NBM, 2>(fp, tmA1, tmS1, tmA2, tmS2, grid, smem_bytes, s, pdl)
   const int bn = fp.up.bn;
+  if (fp.groups == 1) {
+    // one compute group per CTA, two CTAs per SM (8-route tiles only)
+    if (bn > 8 || fp.finalize) return cudaErrorInvalidValue;
+    return scale_kind == SCALE_GROUP
+               ? launch_gemv_fused_one<SCALE_GROUP, DT, LAYOUT, 1, 1>(fp, tmA1, tmS1, tmA2, tmS2, grid, smem_bytes, s, pdl)
+               : launch_gemv_fused_one<SCALE_CHANNEL, DT, LAYOUT, 1, 1>(fp, tmA1, tmS1, tmA2, tmS2, grid, smem_bytes, s,
+                                                                        pdl);
+  }
   if (scale_kind == SCALE_GROUP)
     return bn <= 8 ? W4A16_FUSED_ONE(SCALE_GROUP, 1)
                    : (bn <= 16 ? W4A16_FUSED_ONE(SCALE_GROUP, 2) : W4A16_FUSED_ONE(SCALE_GROUP, 4));
