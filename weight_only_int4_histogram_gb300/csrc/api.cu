@@ -164,8 +164,9 @@ void choose_nt(int n_tiles, int bn, int smem_budget, int max_nt, bool double_acc
   }
 }
 
-// Fused CUDA-core launch at 8-route tiles: one compute group per CTA and two
-// CTAs per SM (each group owns whole units and its own ring, so one group's
+// Fused CUDA-core launch: one compute group per CTA and two CTAs per SM
+// (rings of 4 / 3 / 2 stages at 8 / 16 / 32-route tiles; each group owns
+// whole units and its own ring, so one group's
 // epilogue never holds up the other's stages) once the expected gate/up units
 // fill this many waves of those CTAs; with fewer units, two groups splitting
 // each unit's stages finish the gate/up phase sooner.  Measured (whole
@@ -175,7 +176,14 @@ void choose_nt(int n_tiles, int bn, int smem_budget, int max_nt, bool double_acc
 // shard 32 / 64 tokens (2.13 / 2.9) 131.7 / 163.5 vs 134.8 / 173.7; ReLU^2
 // E64 32 tokens (2.96) 85.6 vs 91.8 but 8 tokens (1.67) 50.8 vs 44.7;
 // per-channel E60 16 / 32 tokens (2.85 / 3.8) 55.9 / 69.3 vs 59.0 / 73.4.
+// Taller tiles: Kimi shard 256 / 384 tokens 284.3 / 306.7 vs 296.6 / 319.1,
+// ReLU^2 E64 64 / 128 tokens 106.6 / 128.7 vs 114.3 / 138.9.
 constexpr double kOneGroupWaves = 1.9;
+// Ring stages of one CTA of the one-group form: half the SM's shared memory
+// less the CTA's 1 KB reserve, the alignment slack and the control block.
+int gemv_stages1(int bn) {
+  return std::min(kGemvMaxStages, (kSmemPerSM / 2 - 1024 - 1024 - kGemvCtrlBytes) / gemv_stage_bytes(bn));
+}
 
 // Units of at most this many K blocks keep two accumulator sets.
 constexpr int kDoubleAccMaxKb = 8;
@@ -299,7 +307,7 @@ Layout make_layout(const w4a16_moe_plan_s& P, int T) {
   }
   L.fused = L.gemv && P.fused;
   L.fgroups = 2;
-  if (L.fused && L.bn == 8 && !P.finalize &&
+  if (L.fused && !P.finalize && gemv_stages1(L.bn) >= 2 &&
       (P.ov_fgroups == 1 || (P.ov_fgroups == 0 && tiles_est * L.nt1 >= kOneGroupWaves * 2 * P.num_sms)))
     L.fgroups = 1;
   if (L.fused) {
@@ -324,7 +332,7 @@ Layout make_layout(const w4a16_moe_plan_s& P, int T) {
     if (L.fgroups == 1) {
       // one compute group per CTA (no exchange buffers), two CTAs per SM:
       // each CTA gets half of the SM's shared memory less its 1 KB reserve
-      L.stages = std::min(kGemvMaxStages, (kSmemPerSM / 2 - 1024 - 1024 - kGemvCtrlBytes) / L.stage_bytes);
+      L.stages = gemv_stages1(L.bn);
       L.smem = 1024 + L.stages * L.stage_bytes + kGemvCtrlBytes;
     } else if (L.fused) {
       // the two compute groups take the stages of their parity: an even ring

@@ -182,7 +182,7 @@ struct FusedParams {
   int32_t* reset;          // [reset_len] queue state zeroed by the last CTA
   int32_t reset_len;
   int32_t groups;          // compute groups per CTA: 2 (one CTA per SM) or 1 (two CTAs per SM,
-                           // 8-route tiles, no fused finalize)
+                           // no fused finalize)
 };
 
 struct CombineParams {

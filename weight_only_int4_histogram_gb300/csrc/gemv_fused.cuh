@@ -38,8 +38,8 @@
 // group's sums from a double-buffered exchange and runs the epilogue.  Each
 // stage carries a header (unit, K block, tile record) written by the producer.
 //
-// One-group form (8-route tiles with enough gate/up units, no fused
-// finalize; the host decides): 320 threads -- the producer, one activation
+// One-group form (enough gate/up units, no fused finalize; the host
+// decides): 320 threads -- the producer, one activation
 // warp taking every stage, one compute group of 8 warps that runs every stage
 // of its units (no exchange) -- and two CTAs per SM, each with its own ring of
 // half the shared memory.  A group's epilogue then holds up only its own ring.
@@ -1048,12 +1048,16 @@ cudaError_t launch_gemv_fused_dt(int scale_kind, const FusedParams& fp, const CU
   launch_gemv_fused_one<SC, DT, LAYOUT, NBM, 2>(fp, tmA1, tmS1, tmA2, tmS2, grid, smem_bytes, s, pdl)
   const int bn = fp.up.bn;
   if (fp.groups == 1) {
-    // one compute group per CTA, two CTAs per SM (8-route tiles only)
-    if (bn > 8 || fp.finalize) return cudaErrorInvalidValue;
-    return scale_kind == SCALE_GROUP
-               ? launch_gemv_fused_one<SCALE_GROUP, DT, LAYOUT, 1, 1>(fp, tmA1, tmS1, tmA2, tmS2, grid, smem_bytes, s, pdl)
-               : launch_gemv_fused_one<SCALE_CHANNEL, DT, LAYOUT, 1, 1>(fp, tmA1, tmS1, tmA2, tmS2, grid, smem_bytes, s,
-                                                                        pdl);
+    // one compute group per CTA, two CTAs per SM
+    if (fp.finalize) return cudaErrorInvalidValue;
+#define W4A16_FUSED_ONE1(SC, NBM) \
+  launch_gemv_fused_one<SC, DT, LAYOUT, NBM, 1>(fp, tmA1, tmS1, tmA2, tmS2, grid, smem_bytes, s, pdl)
+    if (scale_kind == SCALE_GROUP)
+      return bn <= 8 ? W4A16_FUSED_ONE1(SCALE_GROUP, 1)
+                     : (bn <= 16 ? W4A16_FUSED_ONE1(SCALE_GROUP, 2) : W4A16_FUSED_ONE1(SCALE_GROUP, 4));
+    return bn <= 8 ? W4A16_FUSED_ONE1(SCALE_CHANNEL, 1)
+                   : (bn <= 16 ? W4A16_FUSED_ONE1(SCALE_CHANNEL, 2) : W4A16_FUSED_ONE1(SCALE_CHANNEL, 4));
+#undef W4A16_FUSED_ONE1
   }
   if (scale_kind == SCALE_GROUP)
     return bn <= 8 ? W4A16_FUSED_ONE(SCALE_GROUP, 1)
