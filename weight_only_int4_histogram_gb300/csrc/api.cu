@@ -96,17 +96,19 @@ struct Layout {
 // Expected routes per local expert up to which the warp-MMA GEMV runs both
 // GEMMs; above it the tcgen05 path wins (its MMA time per weight is the same
 // for any tile fill up to 64 routes).  Measured crossovers on GB300 (whole
-// forward, both paths forced, graph replay): the group-scale Kimi shape
-// (E 384, H 7168, I 256) is even at 10.7 routes per expert (378 vs 382 us) and
-// slower on CUDA cores at 13.3 (423 vs 386); the per-channel shapes are
-// faster on CUDA cores through 21 routes per expert (E 60, H 2048, I 1408:
-// 132 vs 140 us at 1280 routes; ReLU^2 E 64, H 2688, I 1856: 158 vs 173 at 18)
-// and slower at 24 (ReLU^2: 175 vs 163).  When both GEMMs reduce over at least
+// forward, both paths forced, graph replay): group scales -- the Kimi shape
+// (E 384, H 7168, I 256) is faster on CUDA cores at 10.7 routes per expert
+// (357 vs 380 us), even at 12 (384 vs 388) and slower at 13.3 (409 vs 388);
+// the 32-of-256-expert shard (H 7168, I 2048) faster at 10 (212 vs 239) and
+// slower at 12 (247 vs 236).  Per-channel scales -- E 60, H 2048, I 1408 is
+// faster on CUDA cores through 30 routes per expert (125 vs 138 us at 21,
+// 147 vs 153 at 30); the skewed ReLU^2 E 64, H 2688, I 1856 at 18 (148 vs
+// 172) but not at 24 (166 vs 163).  When both GEMMs reduce over at least
 // 2048 values (every GEMV unit streams eight or more 256-value stages) the
 // GEMV stays ahead much longer: on the 32-expert H = 7168, I = 2048 shape it
 // was faster through 64 routes per expert and slower at 96.
 constexpr double kGemvMaxRoutesGroup = 11.0;
-constexpr double kGemvMaxRoutesChannel = 20.0;
+constexpr double kGemvMaxRoutesChannel = 24.0;
 constexpr double kGemvMaxRoutesLongK = 80.0;
 
 // Expected routes per local expert of a T-token batch under uniform routing
