@@ -369,7 +369,11 @@ w4a16_status w4a16_moe_set_weight_layout(w4a16_moe_plan_t plan, int32_t layout);
  * atomics -- per (token, 16-column block) arrival counters elect the warp of
  * the token's last valid route, which sums the token's expert outputs in
  * top-k order with the combine's arithmetic.  The output is bit-identical to
- * the separate combine.  Other forwards are unaffected.  Default: off (also
+ * the separate combine after the same expert GEMMs: the fused finalize runs
+ * the launch with two compute groups per CTA, so it equals a combine-launch
+ * forward of that form (W4A16_MOE_FUSED_GROUPS=2); where the planner gives
+ * the combine-launch forward one group per CTA, the two differ only in the
+ * FP32 summation order of the units' K stages.  Other forwards are unaffected.  Default: off (also
  * set by the environment variable W4A16_MOE_FUSED_FINALIZE=1 at plan
  * creation).  Host only; plan NULL: W4A16_ERR_INVALID_ARG.
  */
