@@ -78,3 +78,30 @@ def test_short_wait_limit_with_fused_finalize(monkeypatch):
     torch.cuda.synchronize()
     normal.check_device_error()
     compare(out, oracle_rows(cfg, w, x, ids, tw), "fused finalize after a timed-out forward")
+
+
+def test_short_wait_limit_one_group_fused_launch(monkeypatch):
+    # the fused CUDA-core launch in its one-group form (two CTAs per SM, one
+    # activation warp taking every stage): its waits give up cleanly as well
+    cfg = small_cfg(E=4, H=7168, I=256, k=2)
+    T = 48
+    w, x, ids, tw = case_on_gpu(cfg, T)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    monkeypatch.setenv("W4A16_MOE_FUSED_GROUPS", "1")
+    monkeypatch.setenv("W4A16_MOE_WAIT_TIMEOUT_NS", "1")
+    short = make_moe(cfg, T)
+    monkeypatch.delenv("W4A16_MOE_WAIT_TIMEOUT_NS")
+    short.set_gemm_path(2)
+    assert short.route_info(T).gemm1_ctas == 2 * sms
+    short(x, w, tw, ids)
+    torch.cuda.synchronize()
+    with pytest.raises(_lib.W4A16Error) as ei:
+        short.check_device_error()
+    assert ei.value.status == 5  # W4A16_ERR_DEVICE_TIMEOUT
+    normal = make_moe(cfg, T)
+    normal.set_gemm_path(2)
+    assert normal.route_info(T).gemm1_ctas == 2 * sms
+    out = normal(x, w, tw, ids)
+    torch.cuda.synchronize()
+    normal.check_device_error()
+    compare(out, oracle_rows(cfg, w, x, ids, tw), "one-group fused launch after a timed-out forward")
