@@ -318,7 +318,10 @@ Layout make_layout(const w4a16_moe_plan_s& P, int T) {
     // every split must own K blocks: each one's arrival completes its row blocks
     L.s1 = cdiv(L.kb1, cdiv(L.kb1, L.s1));
     L.s2 = 1;  // the down GEMM is balanced by the queue instead
-    L.down_chunk = P.ov_chunk > 0 ? P.ov_chunk : (L.kb2 == 1 ? 4 : 1);
+    // down weight tiles per queue entry (single-stage down units): 4 with two
+    // compute groups per CTA, 2 with one (Kimi shard 32 / 256 tokens 137.9 /
+    // 282.3 us against 139.9 / 284.3 with 4 and 143.0 / 288.4 with 8)
+    L.down_chunk = P.ov_chunk > 0 ? P.ov_chunk : (L.kb2 == 1 ? (L.fgroups == 1 ? 2 : 4) : 1);
   } else {
     L.s1 = P.ov_s1 ? P.ov_s1 : choose_splits(tiles_est, g1, L.kb1, P.num_sms, 1.5);
     L.s2 = P.ov_s2 ? P.ov_s2 : choose_splits(tiles_est, g2, L.kb2, P.num_sms, 1.0);
