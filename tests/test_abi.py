@@ -209,7 +209,8 @@ def test_fused_launch_compute_groups(lib, monkeypatch):
 
 def test_gemm_path_choice_and_validation(lib):
     """Few routes per expert -> CUDA-core GEMV with 8- to 32-route tiles; many ->
-    tensor cores; forced paths hold at every batch size."""
+    tensor cores (above 11 routes per expert with group scales, 24 with
+    per-channel scales); forced paths hold at every batch size."""
     plan, _ = _lib.w4a16_moe_plan(good_desc(num_experts=384, hidden=7168, inter=256, top_k=8,
                                             max_tokens=2048))
     # 384 experts, top-8, group scales: 11 routes per expert at 528 tokens
@@ -232,4 +233,11 @@ def test_gemm_path_choice_and_validation(lib):
     _lib.w4a16_moe_set_overrides(plan, 0, 0, 0)
     ws_auto = _lib.w4a16_moe_set_gemm_path(plan, _lib.PATH_AUTO)
     assert ws_cc > 0 and ws_auto > 0
+    _lib.w4a16_moe_plan_destroy(plan)
+    # per-channel scales (scale_kind 1): 24 routes per expert, E 60 top-4 -> 360 tokens
+    plan, _ = _lib.w4a16_moe_plan(good_desc(num_experts=60, hidden=2048, inter=1408, top_k=4,
+                                            scale_kind=1, max_tokens=1024))
+    paths = {t: _lib.w4a16_moe_route_info(plan, t).gemm_path for t in (8, 360, 361, 1024)}
+    assert paths == {8: _lib.PATH_CUDA_CORES, 360: _lib.PATH_CUDA_CORES, 361: _lib.PATH_TENSOR_CORES,
+                     1024: _lib.PATH_TENSOR_CORES}
     _lib.w4a16_moe_plan_destroy(plan)
